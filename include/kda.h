@@ -1,0 +1,219 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention library.
+ *
+ * What it computes.  Per chain (one sequence and one head) with a 128 x 128
+ * fp32 state S (row = key channel, column = value channel):
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(exp g_t) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = scale * S_t^T q_t
+ *
+ * "Kimi Delta Attention (KDA) prefill" as named on the TensorRT-LLM page
+ * "Kimi K3 KDA prefill: K1 warps finish reading sPartialLast before the next
+ * chunk" (Description: in-chunk gate prefix scan and chunk total, fused beta
+ * sigmoid, padded equal-length and varlen modes), with the dtypes of the
+ * cuDNN-frontend sm90 KDA prefill page (Conversation: BF16 Q/K/V, FP32 gate,
+ * beta and state, non-zero initial_state) and the short-chunk MTP verify of the
+ * TensorRT-LLM page "Kimi K3 work for Rubin (SM107)" (Description: tcgen05 KDA
+ * MTP verify kernel, WY-form chunk, fp32 state pools).
+ *
+ * Conventions shared by every call.
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *    allocates no device or pinned memory and caches none; scratch memory is
+ *    the caller's `workspace`.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL
+ *    = the legacy default stream).  Argument errors found on the host come
+ *    back synchronously and launch nothing.
+ *  - Element strides are in elements, not bytes.  The channel (last) dim must
+ *    have stride 1; every other stride must be a multiple of 8 elements for
+ *    bf16 tensors and 4 for fp32 tensors (16-byte rows for 128-bit / TMA
+ *    loads), and every base pointer 16-byte aligned.  Layouts that break this
+ *    are refused with KDA_ERR_UNSUPPORTED, never read wrongly (the stride
+ *    finding on the cuDNN-frontend sm90 KDA page, Conversation).
+ *  - head_dim_k = head_dim_v = 128 and chunk = 64 only; anything else is
+ *    KDA_ERR_UNSUPPORTED.
+ *  - Errors that only the device can see (cu_seqlens not non-decreasing or not
+ *    ending at the token count, accepted or slot out of range, a bounded wait
+ *    that ran out) are written as a kda_status value to *device_status when it
+ *    is non-NULL (a caller-owned device int32 that the caller zeroes); the
+ *    kernels then skip the offending work instead of faulting.
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KDA_ABI_VERSION 1
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1,  /* bad pointer / size / cu_seqlens / accepted / slot */
+    KDA_ERR_UNSUPPORTED = 2,  /* valid but not supported: dims, chunk, strides, alignment */
+    KDA_ERR_CUDA = 3,         /* a CUDA runtime or driver call failed */
+    KDA_ERR_TIMEOUT = 4       /* (device_status only) a bounded on-chip wait ran out */
+} kda_status;
+
+/*
+ * Prefill arguments.
+ *
+ * Padded mode (cu_seqlens == NULL): B = batch sequences of T = seqlen tokens.
+ *   q, k: bf16, g: fp32, element (b, t, h, c) at b*s[0] + t*s[1] + h*s[2] + c
+ *   v, out: bf16 (b, t, h, j) likewise with their own strides
+ *   beta: fp32 (b, t, h) at b*s[0] + t*s[1] + h*s[2]
+ *   num_seqs must equal batch.
+ * Varlen mode (cu_seqlens != NULL): num_seqs = N packed sequences over
+ *   seqlen = T_total tokens; cu_seqlens is a DEVICE int32 [N+1] with
+ *   cu[0] = 0, cu[n] <= cu[n+1], cu[N] = T_total; sequence n owns tokens
+ *   cu[n] .. cu[n+1]-1; batch must be 1 and stride [0] is ignored.
+ *   Zero-length sequences are allowed: they produce no outputs and their final
+ *   state equals their initial state.
+ * initial_state: fp32 [N, H, 128, 128] contiguous (row = key) or NULL = zeros.
+ * final_state:   fp32 [N, H, 128, 128] contiguous or NULL = not stored.  It may
+ *   alias initial_state (in-place update).
+ * beta_is_logit: 1 = beta holds logits b and the kernel uses sigmoid(b) (the
+ *   fused beta sigmoid); 0 = beta already holds beta in [0, 1].
+ * g: log decay per key channel, g <= 0.  Gates below -10 per token are handled
+ *   with a bounded error of at most exp(-10) relative to |k_i . k_j| in the
+ *   within-16-token interaction terms (the chunk factorisation's guard against
+ *   exp overflow); the production gate bound is -5, which is exact.
+ * scale: multiplies q (o_t = scale * S_t^T q_t); 1.0 for the plain recurrence.
+ * workspace: device scratch of at least kda_prefill_workspace_size(args) bytes,
+ *   256-byte aligned, owned by the caller, used only during the call's kernels
+ *   (so it may be reused by the next call on the same stream).
+ */
+typedef struct kda_prefill_args {
+    const void* q;              /* bf16 */
+    const void* k;              /* bf16 */
+    const void* v;              /* bf16 */
+    const float* g;             /* fp32 */
+    const float* beta;          /* fp32 */
+    void* out;                  /* bf16 */
+    int64_t q_stride[3];        /* (batch, token, head) element strides */
+    int64_t k_stride[3];
+    int64_t v_stride[3];
+    int64_t g_stride[3];
+    int64_t beta_stride[3];
+    int64_t out_stride[3];
+    const float* initial_state; /* fp32 [N,H,128,128] or NULL */
+    float* final_state;         /* fp32 [N,H,128,128] or NULL */
+    const int32_t* cu_seqlens;  /* device int32 [N+1] or NULL (padded) */
+    int64_t batch;              /* padded: B; varlen: 1 */
+    int64_t seqlen;             /* padded: T; varlen: T_total */
+    int64_t num_seqs;           /* N (padded: = batch) */
+    int64_t num_heads;          /* H >= 1 */
+    int64_t head_dim_k;         /* must be 128 */
+    int64_t head_dim_v;         /* must be 128 */
+    int32_t chunk;              /* must be 64 */
+    int32_t beta_is_logit;
+    float scale;
+    void* workspace;
+    size_t workspace_bytes;
+    int32_t* device_status;     /* optional device int32 */
+} kda_prefill_args;
+
+/*
+ * Bytes of workspace kda_prefill needs for these arguments (depends only on
+ * batch, seqlen, num_seqs and num_heads).  Returns 0 if args is NULL.
+ */
+size_t kda_prefill_workspace_size(const kda_prefill_args* args);
+
+/*
+ * KDA prefill: out for every token and (if final_state) the final state of
+ * every chain.  Runs the chunked form with 64-token chunks:
+ *   A1 chunk table from cu_seqlens (gap-safe for zero-length sequences:
+ *      cuDNN-frontend sm90 KDA page, Conversation, "virtual chunk mapping");
+ *   A2-A5 per-chunk prep: in-chunk gate cumsum and chunk total, beta sigmoid,
+ *      tail masking, gate-scaled operands, the UT transform
+ *      (I + Diag(beta) tril(K K^T . decay))^{-1}, W, U and the intra-chunk
+ *      attention folded into Q' = Q e^Gam - Aqk W and O_loc = Aqk U;
+ *   A6-A7 the serial inter-chunk state pass on tcgen05 tensor cores, per
+ *      (sequence, head, value slab), with the output epilogue.
+ * Returns KDA_OK once the kernels are enqueued.
+ */
+kda_status kda_prefill(const kda_prefill_args* args, void* stream);
+
+/*
+ * Runs only steps A1-A5 of kda_prefill and leaves the per-chunk operands in
+ * the workspace, laid out as kda_prefill_workspace_layout describes.  Meant for
+ * testing the stages one at a time.
+ */
+kda_status kda_prefill_prep(const kda_prefill_args* args, void* stream);
+
+/*
+ * Workspace layout (byte offsets from `workspace`) of the per-chunk records
+ * that kda_prefill_prep writes.  Records are indexed by r = chunk * H + head,
+ * where chunk is the global chunk index (sequence n's chunks are
+ * chunk_offset[n] .. chunk_offset[n+1]-1 in token order).  Per record:
+ *   W    bf16 [64][128]   T Diag(beta) (K e^Gam)
+ *   Qp   bf16 [64][128]   scale*Q e^Gam - Aqk W
+ *   Kt   bf16 [128][64]   (K e^{gam - Gam})^T
+ *   U    fp32 [64][128]   T Diag(beta) V
+ *   Ol   fp32 [64][128]   Aqk U
+ *   eg   fp32 [128]       exp(gam), gam = chunk total of g per key channel
+ * chunk_offset: int32 [N+1] (device).  Rows past a tail chunk's length are 0.
+ */
+typedef struct kda_workspace_layout {
+    size_t w, qp, kt, u, ol, eg, chunk_offset, status, total;
+    int64_t max_chunks;         /* records per head */
+} kda_workspace_layout;
+kda_status kda_prefill_workspace_layout(const kda_prefill_args* args,
+                                        kda_workspace_layout* layout);
+
+/*
+ * MTP verify: R requests, each with D <= 16 draft tokens, run against a fp32
+ * state pool.  For request r and head h the state is read from
+ * state_pool[slot[r], h] (slot == NULL: slot r), all D drafts go through the
+ * recurrence in order and produce outputs, and the state after the first
+ * accepted[r] drafts is written back to the same pool slot (accepted 0 leaves
+ * it unchanged).  Each state is read before it is written; slots must be
+ * distinct across requests.
+ *   q, k: bf16, g: fp32, element (r, t, h, c) at r*s[0] + t*s[1] + h*s[2] + c
+ *   v, out: bf16 likewise; beta: fp32 (r, t, h)
+ *   state_pool: fp32 [pool_size, H, 128, 128] contiguous
+ *   slot, accepted: device int32 [R]; accepted[r] in 0..D, slot[r] in
+ *   0..pool_size-1 (out-of-range entries are skipped and reported through
+ *   device_status)
+ */
+typedef struct kda_verify_args {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* g;
+    const float* beta;
+    void* out;
+    int64_t q_stride[3];        /* (request, draft, head) element strides */
+    int64_t k_stride[3];
+    int64_t v_stride[3];
+    int64_t g_stride[3];
+    int64_t beta_stride[3];
+    int64_t out_stride[3];
+    float* state_pool;
+    int64_t pool_size;
+    const int32_t* slot;        /* device int32 [R] or NULL */
+    const int32_t* accepted;    /* device int32 [R] */
+    int64_t num_requests;       /* R */
+    int64_t num_drafts;         /* D, 1..16 */
+    int64_t num_heads;
+    int64_t head_dim_k;         /* must be 128 */
+    int64_t head_dim_v;         /* must be 128 */
+    int32_t beta_is_logit;
+    float scale;
+    int32_t* device_status;     /* optional device int32 */
+} kda_verify_args;
+
+kda_status kda_verify(const kda_verify_args* args, void* stream);
+
+/* Static string naming a status code. */
+const char* kda_status_string(kda_status status);
+
+/* KDA_ABI_VERSION of the loaded library. */
+int kda_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KDA_H */
