@@ -1,0 +1,243 @@
+// kda_api.cu -- the C ABI of include/kda.h: host-side argument checks, the
+// workspace plan, TMA descriptors and the kernel launches.  Nothing here
+// allocates or caches device memory.
+#include <string.h>
+
+#include "../../include/kda.h"
+#include "kda_internal.h"
+#include "tmap.h"
+
+using namespace kda;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Upper bound on chunk records per head.
+int64_t max_chunks_of(const kda_prefill_args* a) {
+    if (a->cu_seqlens == nullptr) return a->batch * ((a->seqlen + kChunk - 1) / kChunk);
+    return a->seqlen / kChunk + a->num_seqs;
+}
+
+bool layout_of(const kda_prefill_args* a, kda_workspace_layout* L) {
+    const int64_t mc = max_chunks_of(a);
+    if (mc < 0 || a->num_heads < 1) return false;
+    const size_t nrec = (size_t)mc * (size_t)a->num_heads;
+    size_t o = 0;
+    L->max_chunks = mc;
+    L->w = o;  o = align_up(o + nrec * kRecW);
+    L->qp = o; o = align_up(o + nrec * kRecQp);
+    L->kt = o; o = align_up(o + nrec * kRecKt);
+    L->u = o;  o = align_up(o + nrec * kRecU);
+    L->ol = o; o = align_up(o + nrec * kRecOl);
+    L->eg = o; o = align_up(o + nrec * kRecEg);
+    L->chunk_offset = o; o = align_up(o + sizeof(int32_t) * (size_t)(a->num_seqs + 1));
+    L->status = o; o = align_up(o + sizeof(int32_t));
+    L->total = o;
+    return true;
+}
+
+bool strides_ok(const int64_t* s, int64_t mult) {
+    for (int i = 0; i < 3; ++i)
+        if (s[i] < 0 || (s[i] % mult) != 0) return false;
+    return true;
+}
+
+kda_status check_prefill(const kda_prefill_args* a) {
+    if (!a) return KDA_ERR_INVALID_ARG;
+    if (a->head_dim_k != kHeadDim || a->head_dim_v != kHeadDim || a->chunk != kChunk)
+        return KDA_ERR_UNSUPPORTED;
+    if (a->num_heads < 1 || a->seqlen < 0 || a->num_seqs < 0 || a->batch < 0)
+        return KDA_ERR_INVALID_ARG;
+    if (a->cu_seqlens == nullptr) {
+        if (a->num_seqs != a->batch) return KDA_ERR_INVALID_ARG;
+    } else {
+        if (a->batch != 1 || a->num_seqs < 1) return KDA_ERR_INVALID_ARG;
+    }
+    const bool tokens = a->seqlen > 0 && a->num_seqs > 0;
+    if (tokens && (!a->q || !a->k || !a->v || !a->g || !a->beta || !a->out))
+        return KDA_ERR_INVALID_ARG;
+    if (tokens) {
+        if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->g) ||
+            !aligned16(a->out))
+            return KDA_ERR_UNSUPPORTED;
+        if (!strides_ok(a->q_stride, 8) || !strides_ok(a->k_stride, 8) ||
+            !strides_ok(a->v_stride, 8) || !strides_ok(a->out_stride, 8) ||
+            !strides_ok(a->g_stride, 4) || !strides_ok(a->beta_stride, 1))
+            return KDA_ERR_UNSUPPORTED;
+    }
+    if ((a->initial_state && !aligned16(a->initial_state)) ||
+        (a->final_state && !aligned16(a->final_state)))
+        return KDA_ERR_UNSUPPORTED;
+    if (a->num_seqs > (1 << 30) || a->num_heads > 65535 || a->seqlen > (int64_t)1 << 31)
+        return KDA_ERR_UNSUPPORTED;
+    kda_workspace_layout L;
+    if (!layout_of(a, &L)) return KDA_ERR_INVALID_ARG;
+    // TMA coordinates are int32: rows of the Kt array must stay below 2^31.
+    if ((double)L.max_chunks * (double)a->num_heads * 128.0 >= 2147483647.0)
+        return KDA_ERR_UNSUPPORTED;
+    if (!a->workspace || a->workspace_bytes < L.total) return KDA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(a->workspace) & (kAlign - 1)) != 0) return KDA_ERR_UNSUPPORTED;
+    return KDA_OK;
+}
+
+void fill_params(const kda_prefill_args* a, const kda_workspace_layout& L, PrefillParams* p) {
+    memset(p, 0, sizeof(*p));
+    uint8_t* ws = static_cast<uint8_t*>(a->workspace);
+    p->q = static_cast<const __nv_bfloat16*>(a->q);
+    p->k = static_cast<const __nv_bfloat16*>(a->k);
+    p->v = static_cast<const __nv_bfloat16*>(a->v);
+    p->g = a->g;
+    p->beta = a->beta;
+    p->out = static_cast<__nv_bfloat16*>(a->out);
+    for (int i = 0; i < 3; ++i) {
+        p->qs[i] = a->q_stride[i]; p->ks[i] = a->k_stride[i]; p->vs[i] = a->v_stride[i];
+        p->gs[i] = a->g_stride[i]; p->bs[i] = a->beta_stride[i]; p->os[i] = a->out_stride[i];
+    }
+    p->h0 = a->initial_state;
+    p->hT = a->final_state;
+    p->cu = a->cu_seqlens;
+    p->chunk_off = reinterpret_cast<int32_t*>(ws + L.chunk_offset);
+    p->status = a->device_status ? a->device_status : reinterpret_cast<int32_t*>(ws + L.status);
+    p->B = (int)a->batch;
+    p->T = (int)a->seqlen;
+    p->N = (int)a->num_seqs;
+    p->H = (int)a->num_heads;
+    p->max_chunks = (int)L.max_chunks;
+    p->beta_is_logit = a->beta_is_logit ? 1 : 0;
+    p->scale = a->scale;
+    p->ws_w = reinterpret_cast<__nv_bfloat16*>(ws + L.w);
+    p->ws_qp = reinterpret_cast<__nv_bfloat16*>(ws + L.qp);
+    p->ws_kt = reinterpret_cast<__nv_bfloat16*>(ws + L.kt);
+    p->ws_u = reinterpret_cast<float*>(ws + L.u);
+    p->ws_ol = reinterpret_cast<float*>(ws + L.ol);
+    p->ws_eg = reinterpret_cast<float*>(ws + L.eg);
+}
+
+bool make_state_maps(const PrefillParams& p, StateMaps* m) {
+    const uint64_t nrec = (uint64_t)p.max_chunks * (uint64_t)p.H;
+    if (nrec == 0) return true;
+    const uint64_t d_w[2] = {128, nrec * 64}, s_w[1] = {256};
+    const uint32_t b_w[2] = {64, 64};
+    const uint64_t d_kt[2] = {64, nrec * 128}, s_kt[1] = {128};
+    const uint32_t b_kt[2] = {64, 128};
+    const uint64_t d_u[2] = {128, nrec * 64}, s_u[1] = {512};
+    const uint32_t b_u[2] = {kSlab, 64};
+    const uint64_t d_eg[2] = {128, nrec}, s_eg[1] = {512};
+    const uint32_t b_eg[2] = {128, 1};
+    return make_tensor_map(&m->w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.ws_w, d_w, s_w, b_w,
+                           CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_tensor_map(&m->qp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.ws_qp, d_w, s_w, b_w,
+                           CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_tensor_map(&m->kt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.ws_kt, d_kt, s_kt, b_kt,
+                           CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_tensor_map(&m->u, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.ws_u, d_u, s_u, b_u,
+                           CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_tensor_map(&m->ol, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.ws_ol, d_u, s_u, b_u,
+                           CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_tensor_map(&m->eg, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.ws_eg, d_eg, s_eg, b_eg,
+                           CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+kda_status run_prefill(const kda_prefill_args* a, void* stream, bool state_pass) {
+    kda_status st = check_prefill(a);
+    if (st != KDA_OK) return st;
+    kda_workspace_layout L;
+    layout_of(a, &L);
+    PrefillParams p;
+    fill_params(a, L, &p);
+    StateMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    if (state_pass && !make_state_maps(p, &maps)) return KDA_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!a->device_status && cudaMemsetAsync(p.status, 0, sizeof(int32_t), s) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    if (launch_chunk_table(p, s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (launch_prep(p, s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (state_pass && launch_state(p, maps, s) != cudaSuccess) return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kda_prefill_workspace_size(const kda_prefill_args* args) {
+    if (!args) return 0;
+    kda_workspace_layout L;
+    if (!layout_of(args, &L)) return 0;
+    return L.total;
+}
+
+kda_status kda_prefill_workspace_layout(const kda_prefill_args* args, kda_workspace_layout* layout) {
+    if (!args || !layout) return KDA_ERR_INVALID_ARG;
+    return layout_of(args, layout) ? KDA_OK : KDA_ERR_INVALID_ARG;
+}
+
+kda_status kda_prefill(const kda_prefill_args* args, void* stream) {
+    return run_prefill(args, stream, true);
+}
+
+kda_status kda_prefill_prep(const kda_prefill_args* args, void* stream) {
+    return run_prefill(args, stream, false);
+}
+
+kda_status kda_verify(const kda_verify_args* a, void* stream) {
+    if (!a) return KDA_ERR_INVALID_ARG;
+    if (a->head_dim_k != kHeadDim || a->head_dim_v != kHeadDim) return KDA_ERR_UNSUPPORTED;
+    if (a->num_requests < 0 || a->num_heads < 1 || a->num_drafts < 1 || a->pool_size < 0)
+        return KDA_ERR_INVALID_ARG;
+    if (a->num_drafts > 16) return KDA_ERR_UNSUPPORTED;
+    if (a->num_requests == 0) return KDA_OK;
+    if (!a->q || !a->k || !a->v || !a->g || !a->beta || !a->out || !a->state_pool || !a->accepted ||
+        a->pool_size < 1)
+        return KDA_ERR_INVALID_ARG;
+    if (a->num_requests > 65535 || a->num_heads > 65535 || a->pool_size > (1 << 30))
+        return KDA_ERR_UNSUPPORTED;
+    const int64_t* ss[6] = {a->q_stride, a->k_stride, a->v_stride, a->g_stride, a->beta_stride,
+                            a->out_stride};
+    for (int t = 0; t < 6; ++t)
+        for (int i = 0; i < 3; ++i)
+            if (ss[t][i] < 0) return KDA_ERR_UNSUPPORTED;
+    VerifyParams p;
+    memset(&p, 0, sizeof(p));
+    p.q = static_cast<const __nv_bfloat16*>(a->q);
+    p.k = static_cast<const __nv_bfloat16*>(a->k);
+    p.v = static_cast<const __nv_bfloat16*>(a->v);
+    p.g = a->g;
+    p.beta = a->beta;
+    p.out = static_cast<__nv_bfloat16*>(a->out);
+    for (int i = 0; i < 3; ++i) {
+        p.qs[i] = a->q_stride[i]; p.ks[i] = a->k_stride[i]; p.vs[i] = a->v_stride[i];
+        p.gs[i] = a->g_stride[i]; p.bs[i] = a->beta_stride[i]; p.os[i] = a->out_stride[i];
+    }
+    p.pool = a->state_pool;
+    p.slot = a->slot;
+    p.accepted = a->accepted;
+    p.status = a->device_status;
+    p.R = (int)a->num_requests;
+    p.D = (int)a->num_drafts;
+    p.H = (int)a->num_heads;
+    p.P = (int)a->pool_size;
+    p.beta_is_logit = a->beta_is_logit ? 1 : 0;
+    p.scale = a->scale;
+    return launch_verify(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KDA_OK
+                                                                               : KDA_ERR_CUDA;
+}
+
+const char* kda_status_string(kda_status s) {
+    switch (s) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG: invalid argument";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED: unsupported shape, stride or alignment";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA: a CUDA call failed";
+        case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT: a bounded on-chip wait ran out";
+    }
+    return "unknown kda_status";
+}
+
+int kda_abi_version(void) { return KDA_ABI_VERSION; }
+
+}  // extern "C"

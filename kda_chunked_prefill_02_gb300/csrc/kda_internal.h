@@ -1,0 +1,113 @@
+// kda_internal.h -- parameters passed from the host API (kda_api.cu) to the
+// prefill / verify kernels, and the launchers each kernel file provides.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kda {
+
+constexpr int kHeadDim = 128;   // K = V = 128
+constexpr int kChunk = 64;      // tokens per chunk
+constexpr int kSlab = 32;       // value columns per state-pass CTA
+constexpr float kGateClamp = -10.0f;  // per-token gate floor inside 16-token blocks
+
+// Workspace record sizes (bytes) per (chunk, head).
+constexpr size_t kRecW = kChunk * kHeadDim * 2;    // bf16 [64][128]
+constexpr size_t kRecQp = kChunk * kHeadDim * 2;   // bf16 [64][128]
+constexpr size_t kRecKt = kHeadDim * kChunk * 2;   // bf16 [128][64]
+constexpr size_t kRecU = kChunk * kHeadDim * 4;    // fp32 [64][128]
+constexpr size_t kRecOl = kChunk * kHeadDim * 4;   // fp32 [64][128]
+constexpr size_t kRecEg = kHeadDim * 4;            // fp32 [128]
+
+struct PrefillParams {
+    const __nv_bfloat16* q;
+    const __nv_bfloat16* k;
+    const __nv_bfloat16* v;
+    const float* g;
+    const float* beta;
+    __nv_bfloat16* out;
+    int64_t qs[3], ks[3], vs[3], gs[3], bs[3], os[3];
+    const float* h0;
+    float* hT;
+    const int32_t* cu;       // device cu_seqlens (varlen) or nullptr (padded)
+    int32_t* chunk_off;      // [N+1] in the workspace (varlen)
+    int32_t* status;         // device status word (never null)
+    int B, T, N, H;          // T: per-sequence length (padded) or total tokens (varlen)
+    int max_chunks;          // chunk records per head (upper bound)
+    int beta_is_logit;
+    float scale;
+    __nv_bfloat16* ws_w;
+    __nv_bfloat16* ws_qp;
+    __nv_bfloat16* ws_kt;
+    float* ws_u;
+    float* ws_ol;
+    float* ws_eg;
+};
+
+// Chunk c (global index) -> sequence, token start and length.
+struct ChunkInfo {
+    int n;        // sequence
+    int b;        // batch coordinate used for addressing (padded: n, varlen: 0)
+    int t0;       // first token (padded: within the sequence; varlen: packed index)
+    int len;      // valid tokens, 1..64 (0 = no such chunk)
+    int local;    // chunk index within the sequence
+};
+
+__device__ __forceinline__ ChunkInfo chunk_info(const PrefillParams& p, int c) {
+    ChunkInfo ci{0, 0, 0, 0, 0};
+    if (p.cu == nullptr) {
+        const int cps = (p.T + kChunk - 1) / kChunk;
+        if (cps == 0 || c >= p.B * cps) return ci;
+        ci.n = c / cps;
+        ci.b = ci.n;
+        ci.local = c - ci.n * cps;
+        ci.t0 = ci.local * kChunk;
+        ci.len = min(kChunk, p.T - ci.t0);
+    } else {
+        if (c >= p.chunk_off[p.N]) return ci;
+        int lo = 0, hi = p.N;  // find n with chunk_off[n] <= c < chunk_off[n+1]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (p.chunk_off[mid] <= c) lo = mid; else hi = mid;
+        }
+        ci.n = lo;
+        ci.b = 0;
+        ci.local = c - p.chunk_off[lo];
+        ci.t0 = p.cu[lo] + ci.local * kChunk;
+        ci.len = min(kChunk, p.cu[lo + 1] - ci.t0);
+    }
+    return ci;
+}
+
+// TMA descriptors of the workspace arrays, built on the host per call.
+struct StateMaps {
+    CUtensorMap w, qp, kt, u, ol, eg;
+};
+
+cudaError_t launch_chunk_table(const PrefillParams& p, cudaStream_t s);
+cudaError_t launch_prep(const PrefillParams& p, cudaStream_t s);
+cudaError_t launch_state(const PrefillParams& p, const StateMaps& maps, cudaStream_t s);
+
+struct VerifyParams {
+    const __nv_bfloat16* q;
+    const __nv_bfloat16* k;
+    const __nv_bfloat16* v;
+    const float* g;
+    const float* beta;
+    __nv_bfloat16* out;
+    int64_t qs[3], ks[3], vs[3], gs[3], bs[3], os[3];
+    float* pool;
+    const int32_t* slot;
+    const int32_t* accepted;
+    int32_t* status;         // may be null
+    int R, D, H, P;
+    int beta_is_logit;
+    float scale;
+};
+
+cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s);
+
+}  // namespace kda

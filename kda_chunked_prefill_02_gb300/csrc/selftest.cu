@@ -1,0 +1,109 @@
+// selftest.cu -- test-only checks of the sm_103a building blocks in sm103.cuh:
+// a single-tile tcgen05 GEMM D = A * B^T (A 128 x 128, B N x 128, bf16, fp32
+// accumulation in TMEM) with the operands staged either by threads writing the
+// 128-byte-swizzled K-major layout themselves or by TMA with the 128-byte
+// swizzle.  Built into its own library (libkda_selftest.so); the product
+// library does not contain it.
+#include <cuda_runtime.h>
+
+#include "sm103.cuh"
+#include "tmap.h"
+
+using namespace kda;
+
+namespace {
+
+__global__ void __launch_bounds__(128)
+    umma_selftest_kernel(const __nv_bfloat16* __restrict__ A, const __nv_bfloat16* __restrict__ B,
+                         float* __restrict__ D, int N, int use_tma,
+                         const __grid_constant__ CUtensorMap map_a,
+                         const __grid_constant__ CUtensorMap map_b, int* status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    uint8_t* sA = smem;          // 2 column blocks x 128 rows x 128 B
+    uint8_t* sB = smem + 32768;  // 2 column blocks x N rows x 128 B
+    __shared__ uint64_t bar_mma, bar_tma;
+    __shared__ uint32_t tmem_base;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        mbar_init(&bar_mma, 1);
+        mbar_init(&bar_tma, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_base, 256);
+        tmem_relinquish();
+    }
+    if (!use_tma) {
+        for (int i = tid; i < 128 * 128; i += 128) {
+            const int r = i >> 7, c = i & 127;
+            *reinterpret_cast<__nv_bfloat16*>(sA + (c >> 6) * 16384 + sw128_off(r, c & 63)) = A[i];
+        }
+        for (int i = tid; i < N * 128; i += 128) {
+            const int r = i >> 7, c = i & 127;
+            *reinterpret_cast<__nv_bfloat16*>(sB + (c >> 6) * (N * 128) + sw128_off(r, c & 63)) =
+                B[i];
+        }
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    bool ok = true;
+    if (use_tma) {
+        if (tid == 0) {
+            mbar_arrive_expect_tx(&bar_tma, (128 + N) * 256);
+            for (int kb = 0; kb < 2; ++kb) {
+                tma_load_2d(sA + kb * 16384, &map_a, kb * 64, 0, &bar_tma);
+                tma_load_2d(sB + kb * N * 128, &map_b, kb * 64, 0, &bar_tma);
+            }
+        }
+        ok = mbar_wait(&bar_tma, 0, nullptr);
+    }
+    if (tid == 0 && ok) {
+        umma_tile(tmem_base, smem_u32(sA), 16384, smem_u32(sB), N * 128, 128,
+                  idesc_bf16_f32(128, N), false);
+        umma_commit(&bar_mma);
+    }
+    if (ok) ok = mbar_wait(&bar_mma, 0, nullptr);
+    if (!ok) atomicExch(status, 4);
+    tc_fence_after();
+    if (ok) {
+        for (int c0 = 0; c0 < N; c0 += 16) {
+            float v[16];
+            tmem_ld16(tmem_addr(tmem_base, warp * 32, c0), v);
+            const int row = warp * 32 + lane;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) D[row * N + c0 + i] = v[i];
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem_base, 256);
+}
+
+}  // namespace
+
+extern "C" int kda_selftest_umma(const void* A, const void* B, float* D, int N, int use_tma,
+                                 int* status, void* stream) {
+    if (N < 16 || N > 256 || (N % 16) != 0) return 1;
+    CUtensorMap ma{}, mb{};
+    if (use_tma) {
+        const uint64_t dims_a[2] = {128, 128}, dims_b[2] = {128, (uint64_t)N};
+        const uint64_t strides[1] = {256};
+        const uint32_t box_a[2] = {64, 128}, box_b[2] = {64, (uint32_t)N};
+        if (!make_tensor_map(&ma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, dims_a, strides, box_a,
+                             CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !make_tensor_map(&mb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, dims_b, strides, box_b,
+                             CU_TENSOR_MAP_SWIZZLE_128B))
+            return 3;
+    }
+    const size_t smem = 1024 + 32768 + 2 * (size_t)N * 128;
+    if (cudaFuncSetAttribute(umma_selftest_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+        return 3;
+    umma_selftest_kernel<<<1, 128, smem, (cudaStream_t)stream>>>(
+        (const __nv_bfloat16*)A, (const __nv_bfloat16*)B, D, N, use_tma, ma, mb, status);
+    return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}

@@ -1,0 +1,264 @@
+"""ctypes binding of libkda.so (include/kda.h): argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels; this module
+only turns torch tensors into pointers, strides and sizes, allocates outputs
+and the workspace through torch (the library itself allocates nothing), and
+raises on any status other than KDA_OK.  There is no fallback: if the library
+is missing or a tensor is not on a CUDA device, the call fails.
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkda.so")
+
+KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT = range(5)
+HEAD_DIM = 128
+CHUNK = 64
+
+_p = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_i64x3 = ctypes.c_int64 * 3
+
+
+class PrefillArgs(ctypes.Structure):
+    _fields_ = [("q", _p), ("k", _p), ("v", _p), ("g", _p), ("beta", _p), ("out", _p),
+                ("q_stride", _i64x3), ("k_stride", _i64x3), ("v_stride", _i64x3),
+                ("g_stride", _i64x3), ("beta_stride", _i64x3), ("out_stride", _i64x3),
+                ("initial_state", _p), ("final_state", _p), ("cu_seqlens", _p),
+                ("batch", _i64), ("seqlen", _i64), ("num_seqs", _i64), ("num_heads", _i64),
+                ("head_dim_k", _i64), ("head_dim_v", _i64),
+                ("chunk", ctypes.c_int32), ("beta_is_logit", ctypes.c_int32),
+                ("scale", ctypes.c_float),
+                ("workspace", _p), ("workspace_bytes", ctypes.c_size_t),
+                ("device_status", _p)]
+
+
+class VerifyArgs(ctypes.Structure):
+    _fields_ = [("q", _p), ("k", _p), ("v", _p), ("g", _p), ("beta", _p), ("out", _p),
+                ("q_stride", _i64x3), ("k_stride", _i64x3), ("v_stride", _i64x3),
+                ("g_stride", _i64x3), ("beta_stride", _i64x3), ("out_stride", _i64x3),
+                ("state_pool", _p), ("pool_size", _i64), ("slot", _p), ("accepted", _p),
+                ("num_requests", _i64), ("num_drafts", _i64), ("num_heads", _i64),
+                ("head_dim_k", _i64), ("head_dim_v", _i64),
+                ("beta_is_logit", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("device_status", _p)]
+
+
+class WorkspaceLayout(ctypes.Structure):
+    _fields_ = [("w", ctypes.c_size_t), ("qp", ctypes.c_size_t), ("kt", ctypes.c_size_t),
+                ("u", ctypes.c_size_t), ("ol", ctypes.c_size_t), ("eg", ctypes.c_size_t),
+                ("chunk_offset", ctypes.c_size_t), ("status", ctypes.c_size_t),
+                ("total", ctypes.c_size_t), ("max_chunks", _i64)]
+
+
+_lib = None
+
+
+def lib():
+    """Load libkda.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libkda.so is not built; run `python -m "
+                               "kda_chunked_prefill_02_gb300.build` (needs nvcc)")
+        L = ctypes.CDLL(LIB_PATH)
+        L.kda_prefill_workspace_size.restype = ctypes.c_size_t
+        L.kda_prefill_workspace_size.argtypes = [ctypes.POINTER(PrefillArgs)]
+        L.kda_prefill_workspace_layout.restype = ctypes.c_int
+        L.kda_prefill_workspace_layout.argtypes = [ctypes.POINTER(PrefillArgs),
+                                                   ctypes.POINTER(WorkspaceLayout)]
+        for name in ("kda_prefill", "kda_prefill_prep"):
+            f = getattr(L, name)
+            f.restype = ctypes.c_int
+            f.argtypes = [ctypes.POINTER(PrefillArgs), _p]
+        L.kda_verify.restype = ctypes.c_int
+        L.kda_verify.argtypes = [ctypes.POINTER(VerifyArgs), _p]
+        L.kda_status_string.restype = ctypes.c_char_p
+        L.kda_status_string.argtypes = [ctypes.c_int]
+        L.kda_abi_version.restype = ctypes.c_int
+        L.kda_abi_version.argtypes = []
+        _lib = L
+    return _lib
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status):
+        self.status = status
+        super().__init__(lib().kda_status_string(status).decode())
+
+
+def status_string(status: int) -> str:
+    return lib().kda_status_string(int(status)).decode()
+
+
+def _check(status):
+    if status != KDA_OK:
+        raise KdaError(status)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need_cuda(name, t, dtype):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+
+
+def _strides3(t, varlen, last_is_channel=True):
+    """(batch, token, head) element strides; the channel dim must be contiguous."""
+    s = t.stride()
+    if last_is_channel:
+        if s[-1] != 1:
+            raise ValueError("the channel (last) dim must have stride 1")
+        s = s[:-1]
+    return (0, s[0], s[1]) if varlen else (s[0], s[1], s[2])
+
+
+def _prefill_args(q, k, v, g, beta, initial_state, cu_seqlens, out, final_state, beta_is_logit,
+                  scale, workspace, device_status, chunk):
+    varlen = cu_seqlens is not None
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16),
+                        ("v", v, torch.bfloat16), ("g", g, torch.float32),
+                        ("beta", beta, torch.float32), ("out", out, torch.bfloat16),
+                        ("initial_state", initial_state, torch.float32),
+                        ("final_state", final_state, torch.float32),
+                        ("cu_seqlens", cu_seqlens, torch.int32),
+                        ("device_status", device_status, torch.int32)):
+        _need_cuda(name, t, dt)
+    for name, t in (("initial_state", initial_state), ("final_state", final_state)):
+        if t is not None and not t.is_contiguous():
+            raise ValueError("%s must be contiguous [N, H, 128, 128]" % name)
+    a = PrefillArgs()
+    a.q, a.k, a.v, a.g, a.beta, a.out = (_ptr(t) for t in (q, k, v, g, beta, out))
+    a.q_stride = _i64x3(*_strides3(q, varlen))
+    a.k_stride = _i64x3(*_strides3(k, varlen))
+    a.v_stride = _i64x3(*_strides3(v, varlen))
+    a.g_stride = _i64x3(*_strides3(g, varlen))
+    a.out_stride = _i64x3(*_strides3(out, varlen))
+    a.beta_stride = _i64x3(*_strides3(beta, varlen, last_is_channel=False))
+    a.initial_state = _ptr(initial_state)
+    a.final_state = _ptr(final_state)
+    a.cu_seqlens = _ptr(cu_seqlens)
+    if varlen:
+        a.batch, a.seqlen, a.num_seqs = 1, q.shape[0], cu_seqlens.shape[0] - 1
+        a.num_heads = q.shape[1]
+    else:
+        a.batch, a.seqlen, a.num_seqs = q.shape[0], q.shape[1], q.shape[0]
+        a.num_heads = q.shape[2]
+    a.head_dim_k, a.head_dim_v = q.shape[-1], v.shape[-1]
+    a.chunk = int(chunk)
+    a.beta_is_logit = 1 if beta_is_logit else 0
+    a.scale = float(scale)
+    a.workspace = _ptr(workspace)
+    a.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    a.device_status = _ptr(device_status)
+    return a
+
+
+def workspace_size(q, v, *, cu_seqlens=None):
+    """Workspace bytes that kda_prefill needs for these shapes."""
+    a = PrefillArgs()
+    if cu_seqlens is not None:
+        a.batch, a.seqlen, a.num_seqs = 1, q.shape[0], cu_seqlens.shape[0] - 1
+        a.num_heads = q.shape[1]
+        a.cu_seqlens = ctypes.c_void_p(1)
+    else:
+        a.batch, a.seqlen, a.num_seqs = q.shape[0], q.shape[1], q.shape[0]
+        a.num_heads = q.shape[2]
+    return int(lib().kda_prefill_workspace_size(ctypes.byref(a)))
+
+
+def workspace_layout(q, *, cu_seqlens=None):
+    a = PrefillArgs()
+    if cu_seqlens is not None:
+        a.batch, a.seqlen, a.num_seqs, a.num_heads = 1, q.shape[0], cu_seqlens.shape[0] - 1, q.shape[1]
+        a.cu_seqlens = ctypes.c_void_p(1)
+    else:
+        a.batch, a.seqlen, a.num_seqs, a.num_heads = q.shape[0], q.shape[1], q.shape[0], q.shape[2]
+    L = WorkspaceLayout()
+    _check(lib().kda_prefill_workspace_layout(ctypes.byref(a), ctypes.byref(L)))
+    return L
+
+
+def kda_prefill(q, k, v, g, beta, *, initial_state=None, cu_seqlens=None, chunk=CHUNK,
+                beta_is_logit=True, scale=1.0, out=None, final_state=None,
+                output_final_state=True, workspace=None, device_status=None, stream=None,
+                prep_only=False):
+    """KDA prefill through the C ABI.
+
+    Padded: q, k, g [B, T, H, 128]; v [B, T, H, 128]; beta [B, T, H].
+    Varlen: q, k, g [T_total, H, 128]; beta [T_total, H]; cu_seqlens int32 [N+1]
+    on the device.  initial_state fp32 [N, H, 128, 128] or None.
+    Returns (out, final_state); with prep_only=True runs steps A1-A5 only and
+    returns (workspace, layout).
+    """
+    N = (cu_seqlens.shape[0] - 1) if cu_seqlens is not None else q.shape[0]
+    H = q.shape[-2]
+    if out is None:
+        out = torch.empty(v.shape, dtype=torch.bfloat16, device=v.device)
+    if final_state is None and output_final_state and not prep_only:
+        final_state = torch.empty((N, H, q.shape[-1], v.shape[-1]), dtype=torch.float32,
+                                  device=q.device)
+    if workspace is None:
+        nbytes = workspace_size(q, v, cu_seqlens=cu_seqlens)
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    a = _prefill_args(q, k, v, g, beta, initial_state, cu_seqlens, out, final_state,
+                      beta_is_logit, scale, workspace, device_status, chunk)
+    fn = lib().kda_prefill_prep if prep_only else lib().kda_prefill
+    _check(fn(ctypes.byref(a), _stream_handle(stream)))
+    if prep_only:
+        return workspace, workspace_layout(q, cu_seqlens=cu_seqlens)
+    return out, final_state
+
+
+def kda_verify(q, k, v, g, beta, state_pool, accepted, *, slot=None, beta_is_logit=True,
+               scale=1.0, out=None, device_status=None, stream=None):
+    """MTP verify through the C ABI; state_pool is updated in place.
+
+    q, k, g [R, D, H, 128]; v [R, D, H, 128]; beta [R, D, H]; state_pool fp32
+    [P, H, 128, 128]; accepted (and slot) int32 [R] on the device.  Returns out.
+    """
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16),
+                        ("v", v, torch.bfloat16), ("g", g, torch.float32),
+                        ("beta", beta, torch.float32), ("state_pool", state_pool, torch.float32),
+                        ("accepted", accepted, torch.int32), ("slot", slot, torch.int32),
+                        ("device_status", device_status, torch.int32)):
+        _need_cuda(name, t, dt)
+    if not state_pool.is_contiguous():
+        raise ValueError("state_pool must be contiguous [P, H, 128, 128]")
+    if out is None:
+        out = torch.empty(v.shape, dtype=torch.bfloat16, device=v.device)
+    _need_cuda("out", out, torch.bfloat16)
+    a = VerifyArgs()
+    a.q, a.k, a.v, a.g, a.beta, a.out = (_ptr(t) for t in (q, k, v, g, beta, out))
+    a.q_stride = _i64x3(*_strides3(q, False))
+    a.k_stride = _i64x3(*_strides3(k, False))
+    a.v_stride = _i64x3(*_strides3(v, False))
+    a.g_stride = _i64x3(*_strides3(g, False))
+    a.out_stride = _i64x3(*_strides3(out, False))
+    a.beta_stride = _i64x3(*_strides3(beta, False, last_is_channel=False))
+    a.state_pool = _ptr(state_pool)
+    a.pool_size = state_pool.shape[0]
+    a.slot = _ptr(slot)
+    a.accepted = _ptr(accepted)
+    a.num_requests, a.num_drafts, a.num_heads = q.shape[0], q.shape[1], q.shape[2]
+    a.head_dim_k, a.head_dim_v = q.shape[-1], v.shape[-1]
+    a.beta_is_logit = 1 if beta_is_logit else 0
+    a.scale = float(scale)
+    a.device_status = _ptr(device_status)
+    _check(lib().kda_verify(ctypes.byref(a), _stream_handle(stream)))
+    return out

@@ -1,0 +1,105 @@
+"""CPU-only checks of the C ABI: the library loads, exports every function that
+include/*.h declares, and refuses bad arguments on the host (before any CUDA
+call, so these run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def K():
+    from kda_chunked_prefill_02_gb300 import build, kda
+    build.build()
+    return kda
+
+
+def _declared(header):
+    src = open(os.path.join(ROOT, "include", header)).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return set(re.findall(r"\b(kda_[a-z_0-9]+)\s*\(", src))
+
+
+def test_exports_every_declared_symbol(K):
+    lib = K.lib()
+    names = set()
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            names |= _declared(h)
+    assert {"kda_prefill", "kda_verify", "kda_prefill_workspace_size",
+            "kda_status_string"} <= names
+    for n in sorted(names):
+        assert hasattr(lib, n), n
+    assert lib.kda_abi_version() == 1
+
+
+def _args(K, **kw):
+    a = K.PrefillArgs()
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: validation fails first
+    a.q = a.k = a.v = a.g = a.beta = a.out = fake
+    for f in ("q_stride", "k_stride", "v_stride", "g_stride", "out_stride"):
+        setattr(a, f, K._i64x3(4 * 256 * 128, 2 * 128, 128))
+    a.beta_stride = K._i64x3(512, 2, 1)
+    a.batch, a.seqlen, a.num_seqs, a.num_heads = 1, 256, 1, 2
+    a.head_dim_k = a.head_dim_v = 128
+    a.chunk = 64
+    a.beta_is_logit = 1
+    a.scale = 1.0
+    a.workspace = ctypes.c_void_p(1 << 30)
+    a.workspace_bytes = K.lib().kda_prefill_workspace_size(ctypes.byref(a))
+    for k_, v_ in kw.items():
+        setattr(a, k_, v_)
+    return a
+
+
+def test_host_validation(K):
+    lib = K.lib()
+    run = lambda a: lib.kda_prefill(ctypes.byref(a), None)
+    assert run(_args(K, head_dim_k=64)) == K.KDA_ERR_UNSUPPORTED
+    assert run(_args(K, head_dim_v=256)) == K.KDA_ERR_UNSUPPORTED
+    assert run(_args(K, chunk=32)) == K.KDA_ERR_UNSUPPORTED
+    assert run(_args(K, q_stride=K._i64x3(4 * 256 * 128, 2 * 128 + 3, 128))) == K.KDA_ERR_UNSUPPORTED
+    assert run(_args(K, g_stride=K._i64x3(0, 2 * 128 + 2, 128))) == K.KDA_ERR_UNSUPPORTED
+    assert run(_args(K, q=ctypes.c_void_p((1 << 20) + 2))) == K.KDA_ERR_UNSUPPORTED
+    assert run(_args(K, num_seqs=2)) == K.KDA_ERR_INVALID_ARG
+    assert run(_args(K, num_heads=0)) == K.KDA_ERR_INVALID_ARG
+    assert run(_args(K, workspace_bytes=100)) == K.KDA_ERR_INVALID_ARG
+    assert run(_args(K, workspace=ctypes.c_void_p((1 << 30) + 64))) == K.KDA_ERR_UNSUPPORTED
+    assert run(_args(K, q=None)) == K.KDA_ERR_INVALID_ARG
+    assert lib.kda_prefill(None, None) == K.KDA_ERR_INVALID_ARG
+    assert lib.kda_prefill_workspace_size(None) == 0
+
+
+def test_workspace_plan(K):
+    lib = K.lib()
+    a = _args(K)
+    L = K.WorkspaceLayout()
+    assert lib.kda_prefill_workspace_layout(ctypes.byref(a), ctypes.byref(L)) == 0
+    assert L.max_chunks == 4                        # padded: ceil(256 / 64)
+    assert L.total == lib.kda_prefill_workspace_size(ctypes.byref(a))
+    offs = [L.w, L.qp, L.kt, L.u, L.ol, L.eg, L.chunk_offset, L.status]
+    assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
+    # varlen upper bound on chunks: floor(T / 64) + N
+    a2 = _args(K, cu_seqlens=ctypes.c_void_p(1 << 12), num_seqs=3, seqlen=130)
+    assert lib.kda_prefill_workspace_layout(ctypes.byref(a2), ctypes.byref(L)) == 0
+    assert L.max_chunks == 130 // 64 + 3
+
+
+def test_verify_validation(K):
+    lib = K.lib()
+    a = K.VerifyArgs()
+    a.head_dim_k = a.head_dim_v = 128
+    a.num_requests, a.num_drafts, a.num_heads, a.pool_size = 4, 17, 2, 4
+    assert lib.kda_verify(ctypes.byref(a), None) == K.KDA_ERR_UNSUPPORTED
+    a.num_drafts = 4
+    assert lib.kda_verify(ctypes.byref(a), None) == K.KDA_ERR_INVALID_ARG  # null pointers
+    a.num_requests = 0
+    assert lib.kda_verify(ctypes.byref(a), None) == 0                      # nothing to do
+
+
+def test_status_strings(K):
+    for s in range(5):
+        assert K.status_string(s).startswith("KDA_")

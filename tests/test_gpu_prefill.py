@@ -1,0 +1,179 @@
+"""GPU parity of kda_prefill against the fp64 oracle (through the C ABI).
+
+Element-by-element on small seeded inputs that span several chunks and a
+ragged tail; on sampled heads at the full workload sizes; plus the edge cases
+(empty and length-1 sequences, strided views, in-place state, extreme gates,
+determinism, bad cu_seqlens)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import chunked
+from kda_chunked_prefill_02_gb300 import inputs
+from kda_test_util import (assert_parity, gpu_prefill, head_subset, oracle_prefill, rel_fro,
+                           to_np)
+
+pytestmark = pytest.mark.gpu
+
+
+def _bf16(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).view(torch.bfloat16).float().numpy()
+
+
+def test_prep_stage_intermediates():
+    """Steps A1-A5 alone: every per-chunk record matches the chunked fp64 form."""
+    import kda_chunked_prefill_02_gb300 as K
+    inp = inputs.prefill_inputs(5, B=2, T=200, H=2)
+    d = inp.to("cuda")
+    ws, L = K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, scale=0.8, prep_only=True)
+    torch.cuda.synchronize()
+    raw = ws.cpu().numpy()
+    nrec = L.max_chunks * 2
+
+    def arr(off, dt, shape):
+        n = int(np.prod(shape))
+        return raw[off:off + n * np.dtype(dt).itemsize].view(dt).reshape(shape)
+
+    W = _bf16(arr(L.w, np.uint16, (nrec, 64, 128)))
+    Qp = _bf16(arr(L.qp, np.uint16, (nrec, 64, 128)))
+    Kt = _bf16(arr(L.kt, np.uint16, (nrec, 128, 64)))
+    U = arr(L.u, np.float32, (nrec, 64, 128))
+    Ol = arr(L.ol, np.float32, (nrec, 64, 128))
+    eg = arr(L.eg, np.float32, (nrec, 128))
+    q, k, v, g, b = (to_np(t) for t in (inp.q, inp.k, inp.v, inp.g, inp.beta))
+    beta = 1.0 / (1.0 + np.exp(-b))
+    cps = 4
+    for bb in range(2):
+        for c in range(cps):
+            t0, t1 = 64 * c, min(64 * c + 64, 200)
+            n = t1 - t0
+            for h in range(2):
+                r = (bb * cps + c) * 2 + h
+                ref = chunked.chunk_step(np.zeros((128, 128)), 0.8 * q[bb, t0:t1, h], k[bb, t0:t1, h],
+                                         v[bb, t0:t1, h], g[bb, t0:t1, h], beta[bb, t0:t1, h])
+                for name, got, want in (("W", W[r, :n], ref["W"]), ("U", U[r, :n], ref["U"]),
+                                        ("Qp", Qp[r, :n], ref["Qp"]), ("Ol", Ol[r, :n], ref["Oloc"]),
+                                        ("Kt", Kt[r, :, :n], ref["Kh"].T)):
+                    assert rel_fro(got, want) < 1e-2, (name, bb, c, h, rel_fro(got, want))
+                np.testing.assert_allclose(eg[r], np.exp(ref["gam"]), rtol=1e-5, atol=1e-30)
+                for name, tail in (("W", W[r, n:]), ("U", U[r, n:]), ("Qp", Qp[r, n:]),
+                                   ("Ol", Ol[r, n:]), ("Kt", Kt[r, :, n:])):
+                    assert not np.any(tail), name
+
+
+def test_tiny_config():
+    inp = inputs.config_inputs("tiny")
+    out, fin = gpu_prefill(inp)
+    ro, rf = oracle_prefill(inp)
+    assert_parity(out, fin, ro, rf, "tiny")
+
+
+@pytest.mark.parametrize("lengths,H", [([17, 0, 16], 2), ([1024], 4), ([1025, 0, 31], 2),
+                                       ([1, 64, 65, 127, 128, 129], 3)])
+def test_varlen_small_shapes(lengths, H):
+    inp = inputs.prefill_inputs(7 + len(lengths), lengths=lengths, H=H)
+    out, fin = gpu_prefill(inp)
+    ro, rf = oracle_prefill(inp)
+    assert_parity(out, fin, ro, rf, str(lengths))
+    for n, L in enumerate(lengths):  # zero-length sequences keep their state exactly
+        if L == 0:
+            assert torch.equal(fin[n].cpu(), inp.initial_state[n])
+
+
+def test_padded_ragged_tail_no_initial_state():
+    inp = inputs.prefill_inputs(31, B=3, T=333, H=2, init_std=None)
+    out, fin = gpu_prefill(inp)
+    ro, rf = oracle_prefill(inp)
+    assert_parity(out, fin, ro, rf, "padded T=333")
+
+
+def test_beta_probabilities_scale_and_extreme_gates():
+    inp = inputs.prefill_inputs(41, B=2, T=192, H=2)
+    inp.beta = torch.sigmoid(inp.beta)
+    inp.g[0, 10:12] = -1e4        # forget everything
+    inp.g[0, 70:90, 0] = -20.0    # beyond the in-block gate floor
+    inp.g[1, :, 1] = 0.0          # no decay on one head
+    out, fin = gpu_prefill(inp, beta_is_logit=False, scale=0.7)
+    ro, rf = oracle_prefill(inp, beta_is_logit=False, scale=0.7)
+    assert_parity(out, fin, ro, rf, "beta prob / scale / gates")
+
+
+def test_strided_views_match_contiguous():
+    """Row-padded q/k/v/g/out views (token and head strides not dense) give the
+    same bits as contiguous tensors: declared strides are honoured."""
+    import kda_chunked_prefill_02_gb300 as K
+    inp = inputs.prefill_inputs(51, B=2, T=130, H=3)
+    d = inp.to("cuda")
+    ref_out, ref_fin = K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, initial_state=d.initial_state)
+
+    def pad(t, extra):
+        big = torch.zeros(t.shape[:-1] + (t.shape[-1] + extra,), dtype=t.dtype, device=t.device)
+        big[..., :t.shape[-1]] = t
+        return big[..., :t.shape[-1]]
+
+    q, k, v, g = pad(d.q, 64), pad(d.k, 8), pad(d.v, 128), pad(d.g, 4)
+    beta = torch.zeros(2, 130, 3, 5, device="cuda")[..., 1]
+    beta.copy_(d.beta)
+    out = pad(torch.empty_like(d.v), 16)
+    K.kda_prefill(q, k, v, g, beta, initial_state=d.initial_state, out=out)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref_out)
+
+
+def test_in_place_state_and_continuation():
+    """final_state may alias initial_state; prefill of x[:m] then x[m:] from the
+    first call's final state equals one call."""
+    import kda_chunked_prefill_02_gb300 as K
+    inp = inputs.prefill_inputs(61, B=1, T=300, H=2)
+    d = inp.to("cuda")
+    out, fin = K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, initial_state=d.initial_state)
+    st = d.initial_state.clone()
+    m = 100
+    o1, _ = K.kda_prefill(d.q[:, :m], d.k[:, :m], d.v[:, :m], d.g[:, :m], d.beta[:, :m],
+                          initial_state=st, final_state=st)
+    o2, _ = K.kda_prefill(d.q[:, m:], d.k[:, m:], d.v[:, m:], d.g[:, m:], d.beta[:, m:],
+                          initial_state=st, final_state=st)
+    torch.cuda.synchronize()
+    ro, rf = oracle_prefill(inp)
+    assert_parity(torch.cat([o1, o2], 1), st, ro, rf, "continuation")
+    assert_parity(out, fin, ro, rf, "single call")
+
+
+def test_bit_identical_across_runs():
+    import kda_chunked_prefill_02_gb300 as K
+    inp = inputs.prefill_inputs(71, lengths=[300, 1, 0, 700], H=4)
+    d = inp.to("cuda")
+    a = K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, initial_state=d.initial_state,
+                      cu_seqlens=d.cu_seqlens)
+    b = K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, initial_state=d.initial_state,
+                      cu_seqlens=d.cu_seqlens)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_bad_cu_seqlens_reported_not_faulted():
+    import kda_chunked_prefill_02_gb300 as K
+    inp = inputs.prefill_inputs(81, lengths=[40, 30], H=2)
+    d = inp.to("cuda")
+    cu = torch.tensor([0, 50, 45], dtype=torch.int32, device="cuda")  # decreasing, wrong end
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, fin = K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, initial_state=d.initial_state,
+                             cu_seqlens=cu, device_status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 1
+    assert torch.equal(fin, d.initial_state)  # no chunk was processed
+
+
+@pytest.mark.parametrize("name,heads", [("padded", None), ("varlen", [0, 13, 31]),
+                                        ("long", [5, 30])])
+def test_full_size_configs(name, heads):
+    """The full workloads in the launch configuration the bench times; the
+    oracle runs on all heads (padded) or on sampled heads."""
+    inp = inputs.config_inputs(name)
+    out, fin = gpu_prefill(inp)
+    sub = inp if heads is None else head_subset(inp, heads)
+    ro, rf = oracle_prefill(sub)
+    og = out if heads is None else out[..., heads, :]
+    fg = fin if heads is None else fin[:, heads]
+    assert_parity(og, fg, ro, rf, name)

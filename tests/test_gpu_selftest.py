@@ -1,0 +1,36 @@
+"""GPU check of the tcgen05 / TMA building blocks: one 128 x N x 128 tile
+D = A B^T on the tensor cores, operands staged by threads (hand-written
+128-byte swizzle) or by TMA (hardware swizzle), against a torch fp32 matmul."""
+import ctypes
+import os
+
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def selftest():
+    from kda_chunked_prefill_02_gb300 import build
+    build.build()
+    lib = ctypes.CDLL(build.SELFTEST_LIB)
+    lib.kda_selftest_umma.restype = ctypes.c_int
+    lib.kda_selftest_umma.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 2 + [ctypes.c_void_p] * 2
+    return lib
+
+
+@pytest.mark.parametrize("use_tma", [0, 1])
+@pytest.mark.parametrize("N", [32, 64, 96, 256])
+def test_umma_tile(selftest, N, use_tma):
+    g = torch.Generator(device="cpu").manual_seed(N + use_tma)
+    A = torch.randn(128, 128, generator=g).to(torch.bfloat16).cuda()
+    B = torch.randn(N, 128, generator=g).to(torch.bfloat16).cuda()
+    D = torch.full((128, N), float("nan"), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = selftest.kda_selftest_umma(A.data_ptr(), B.data_ptr(), D.data_ptr(), N, use_tma,
+                                    status.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert rc == 0 and status.item() == 0
+    ref = A.float() @ B.float().T
+    torch.testing.assert_close(D, ref, atol=2e-3, rtol=1e-4)
