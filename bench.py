@@ -1,0 +1,371 @@
+#!/usr/bin/env python
+"""KDA prefill throughput on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config long|varlen|padded|tiny]
+
+One step = one kda_prefill call (chunk prep + serial state pass, the whole hot
+path) over the workload, inputs resident in HBM.  The default workload is the
+long-context configuration B=1, T=131072, H=32, K=V=128, chunk 64 (inputs of
+~5.4 GB, larger than L2, so no flush is needed between steps).  Prints one JSON
+line (rank 0).  Under torchrun every rank runs its own copy of the workload on
+its own GPU (chains are independent: no collective on the data path), so the
+scaling is weak and value = tokens processed by all ranks / max-over-ranks time.
+
+--impl reference times the fp64 CPU oracle (sequential recurrence, OpenMP over
+chains) on the host cores, on a bounded sample of the same workload per step;
+it is a deliberately slow reference, not a target.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA prefill tokens/s (H=32, dk=dv=128) and % of tensor-pipe peak, 1×GB300"
+# Algorithmic cost per token per head (chunk 64, K = V = 128):
+#   bytes: q,k,v bf16 3*256 + g fp32 512 + beta 4 + out bf16 256 = 1540
+#   tensor FLOP of the chunked form: 11,534,336 per 64-token chunk = 180,224
+BYTES_PREP = 3 * 256 + 512 + 4      # what the prep kernel must read
+BYTES_STATE = 256                   # what the state pass must write (plus state I/O)
+FLOP_TOKEN_HEAD = 180224
+STATE_BYTES = 128 * 128 * 4
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", choices=["long", "varlen", "padded", "tiny"], default="long")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), float(m["bf16_tflops"]), float(m.get("bf16_tflops_sustained", m["bf16_tflops"])), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def dist_init(n):
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, ws, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while a region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.3)
+        self.proc.terminate()
+        self.proc.wait(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def workload(name):
+    from kda_chunked_prefill_02_gb300 import inputs
+    return inputs.config_inputs(name)
+
+
+def config_dict(name, inp):
+    from kda_chunked_prefill_02_gb300 import inputs
+    return {"workload": name, "description": inputs.CONFIG_DESCRIPTIONS[name],
+            "num_seqs": inp.num_seqs, "total_tokens": inp.total_tokens,
+            "heads": inp.num_heads, "head_dim": 128, "chunk": 64,
+            "l2": "inputs larger than L2 (no flush)" if inp.total_tokens * inp.num_heads * 1284 > 129e6
+            else "L2 flushed between steps"}
+
+
+def cpu_oracle_sample(inp, max_tokens):
+    """Run the fp64 oracle on the first `max_tokens` tokens of every sequence
+    (all heads).  Returns (tokens, seconds, threads)."""
+    import oracle
+    from kda_chunked_prefill_02_gb300 import inputs
+    sub = inputs.prefix_sample(inp, max_tokens)
+    t0 = time.perf_counter()
+    _, _, used = oracle.prefill(sub.q, sub.k, sub.v, sub.g, sub.beta, cu_seqlens=sub.cu_seqlens,
+                                initial_state=sub.initial_state, return_threads=True)
+    return sub.total_tokens, time.perf_counter() - t0, used
+
+
+def run_ours(args, rank, ws, local):
+    import torch
+
+    import kda_chunked_prefill_02_gb300 as K
+
+    hbm, tf_burst, tf_sust, peak_src = peaks()
+    inp = workload(args.config)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    d = inp.to(dev)
+    N, H, T = inp.num_seqs, inp.num_heads, inp.total_tokens
+    out = torch.empty(d.v.shape, dtype=torch.bfloat16, device=dev)
+    fin = torch.empty((N, H, 128, 128), dtype=torch.float32, device=dev)
+    wsb = torch.empty(K.workspace_size(d.q, d.v, cu_seqlens=d.cu_seqlens), dtype=torch.uint8,
+                      device=dev)
+    stream = torch.cuda.current_stream()
+    flush = None
+    if T * H * BYTES_PREP < 256e6:
+        flush = torch.empty(int(256e6) // 4, dtype=torch.float32, device=dev)
+
+    def step(stage=None):
+        if flush is not None:
+            flush.zero_()
+        K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, initial_state=d.initial_state,
+                      cu_seqlens=d.cu_seqlens, out=out, final_state=fin, workspace=wsb,
+                      stream=stream, stage=stage)
+
+    def timed(fn, k):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(ws)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(k):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        return e0.elapsed_time(e1) / k
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    ms = timed(step, args.steps)
+    clk = clocks.stop()
+    ms = max_over_ranks(ms, ws)
+
+    # per-kernel durations (each stage alone, same stream, same workspace)
+    for _ in range(2):
+        step("prep")
+        step("state")
+    ms_prep = timed(lambda: step("prep"), args.steps)
+    ms_state = timed(lambda: step("state"), args.steps)
+    if flush is not None:  # remove the flush's own time from the stage timings
+        ms_flush = timed(lambda: flush.zero_(), args.steps)
+        ms_prep -= ms_flush
+        ms_state -= ms_flush
+        ms -= ms_flush
+
+    tokens_step = T * ws
+    value = tokens_step / (ms / 1e3)
+    th = T * H
+    init_bytes = STATE_BYTES * N * H if inp.initial_state is not None else 0
+    bytes_prep = th * BYTES_PREP
+    bytes_state = th * BYTES_STATE + init_bytes + STATE_BYTES * N * H
+    kern = {"prep": (ms_prep, bytes_prep), "state": (ms_state, bytes_state)}
+    dom = max(kern, key=lambda k_: kern[k_][0])
+    dms, dbytes = kern[dom]
+    achieved = dbytes / (dms / 1e3) / 1e9
+    flops = th * FLOP_TOKEN_HEAD
+    tensor_frac = flops / (ms / 1e3) / 1e12 / tf_burst
+    path_bytes = bytes_prep + bytes_state
+    return dict(ms=ms, value=value, clk=clk, ms_prep=ms_prep, ms_state=ms_state, dom=dom,
+                achieved=achieved, hbm=hbm, peak_src=peak_src, tensor_frac=tensor_frac,
+                tf_burst=tf_burst, path_gbs=path_bytes / (ms / 1e3) / 1e9, inp=inp, d=d,
+                out=out, fin=fin, wsb=wsb, stream=stream, flops=flops, dbytes=dbytes)
+
+
+def run_e2e(r, args, ws):
+    """Same metric through the public call with host buffers: every step copies
+    the inputs from pinned host memory, runs kda_prefill and reads out and the
+    final state back to pinned host memory."""
+    import torch
+
+    import kda_chunked_prefill_02_gb300 as K
+    inp, d, stream = r["inp"], r["d"], r["stream"]
+    host = inp.pin_memory()
+    out_h = torch.empty(d.v.shape, dtype=torch.bfloat16, pin_memory=True)
+    fin_h = torch.empty(r["fin"].shape, dtype=torch.float32, pin_memory=True)
+    pairs = [(d.q, host.q), (d.k, host.k), (d.v, host.v), (d.g, host.g), (d.beta, host.beta)]
+    if inp.initial_state is not None:
+        pairs.append((d.initial_state, host.initial_state))
+    if inp.cu_seqlens is not None:
+        pairs.append((d.cu_seqlens, host.cu_seqlens))
+    h2d = sum(h.numel() * h.element_size() for _, h in pairs)
+    d2h = out_h.numel() * out_h.element_size() + fin_h.numel() * fin_h.element_size()
+
+    def step():
+        for dv, hv in pairs:
+            dv.copy_(hv, non_blocking=True)
+        K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, initial_state=d.initial_state,
+                      cu_seqlens=d.cu_seqlens, out=r["out"], final_state=r["fin"],
+                      workspace=r["wsb"], stream=stream)
+        out_h.copy_(r["out"], non_blocking=True)
+        fin_h.copy_(r["fin"], non_blocking=True)
+
+    for _ in range(2):
+        step()
+    k = max(3, args.steps // 4)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(k):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    ms = max_over_ranks(e0.elapsed_time(e1) / k, ws)
+    return {"value": inp.total_tokens * ws / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def cpu_baseline(inp, target_s=15.0):
+    """The oracle, as it stands, on a bounded prefix sample of the workload."""
+    tok, sec, used = cpu_oracle_sample(inp, 256)
+    m = int(256 * max(1.0, min(64.0, target_s / max(sec, 1e-3))))
+    m = min(m, max(inp.lengths))
+    tok, sec, used = cpu_oracle_sample(inp, m)
+    return {"value": tok / sec, "unit": "tokens/s", "cores": used, "kind": "oracle",
+            "sample": "first %d tokens of every sequence, all %d heads (%d tokens), fp64, %.1f s"
+                      % (m, inp.num_heads, tok, sec),
+            "host_cores_available": len(os.sched_getaffinity(0))}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return main_reference(args)
+    import torch
+    rank, ws, local = dist_init(args.gpus)
+    r = run_ours(args, rank, ws, local)
+    e2e = run_e2e(r, args, ws)
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(r["inp"])
+    if rank == 0:
+        inp = r["inp"]
+        line = {
+            "metric": METRIC, "value": r["value"], "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16 q/k/v/out, fp32 gate/beta/state, bf16 tcgen05 MMA with fp32 accumulation",
+            "data": "synthetic, seeded (q,k L2-normalised, g=-5*sigmoid(N(0,1)), beta=sigmoid(N(0,1)))",
+            "config": dict(config_dict(args.config, inp), parallelism="replica per GPU" if ws > 1 else "1 GPU"),
+            "tensor_pipe": {"algorithmic_tflops": r["flops"] / (r["ms"] / 1e3) / 1e12,
+                            "peak": r["tf_burst"], "frac": r["tensor_frac"],
+                            "note": "whole-call algorithmic tensor FLOP (180,224 per token-head) / call time, of measured peak"},
+            "roofline": {"bound": "hbm", "kernel": r["dom"], "achieved": r["achieved"],
+                         "peak": r["hbm"], "unit": "GB/s", "frac": r["achieved"] / r["hbm"],
+                         "traffic": None, "peak_source": r["peak_src"]},
+            "kernels_ms": {"prep": r["ms_prep"], "state": r["ms_state"]},
+            "path_gbs": r["path_gbs"],
+            "e2e": e2e, "cpu_baseline": cpu,
+            "gpu_launches": 2 * args.steps + (args.steps if inp.cu_seqlens is not None else 0),
+            "clocks": r["clk"],
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    inp = workload(args.config)
+    sample = 256
+    for _ in range(args.warmup):
+        cpu_oracle_sample(inp, 16)
+    times, tok, used = [], 0, 1
+    for _ in range(args.steps):
+        tok, sec, used = cpu_oracle_sample(inp, sample)
+        times.append(sec)
+    sec = statistics.median(times)
+    value = tok / sec
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic, seeded",
+            "config": config_dict(args.config, inp),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": used, "kind": "oracle",
+                             "sample": "first %d tokens of every sequence, all heads, per step" % sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

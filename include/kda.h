@@ -144,6 +144,14 @@ kda_status kda_prefill(const kda_prefill_args* args, void* stream);
 kda_status kda_prefill_prep(const kda_prefill_args* args, void* stream);
 
 /*
+ * Runs only steps A6-A7 of kda_prefill: the serial state pass and the output
+ * epilogue, reading the per-chunk records that a previous kda_prefill_prep
+ * with the same arguments and workspace left there.  Together the two calls
+ * do exactly what kda_prefill does; split, each stage can be timed alone.
+ */
+kda_status kda_prefill_state(const kda_prefill_args* args, void* stream);
+
+/*
  * Workspace layout (byte offsets from `workspace`) of the per-chunk records
  * that kda_prefill_prep writes.  Records are indexed by r = chunk * H + head,
  * where chunk is the global chunk index (sequence n's chunks are

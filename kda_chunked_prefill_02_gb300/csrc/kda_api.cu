@@ -141,7 +141,9 @@ bool make_state_maps(const PrefillParams& p, StateMaps* m) {
                            CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-kda_status run_prefill(const kda_prefill_args* a, void* stream, bool state_pass) {
+// stages: bit 0 = A1-A5 (chunk table and prep), bit 1 = A6-A7 (state pass)
+kda_status run_prefill(const kda_prefill_args* a, void* stream, int stages) {
+    const bool state_pass = (stages & 2) != 0, prep = (stages & 1) != 0;
     kda_status st = check_prefill(a);
     if (st != KDA_OK) return st;
     kda_workspace_layout L;
@@ -152,10 +154,12 @@ kda_status run_prefill(const kda_prefill_args* a, void* stream, bool state_pass)
     memset(&maps, 0, sizeof(maps));
     if (state_pass && !make_state_maps(p, &maps)) return KDA_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (!a->device_status && cudaMemsetAsync(p.status, 0, sizeof(int32_t), s) != cudaSuccess)
-        return KDA_ERR_CUDA;
-    if (launch_chunk_table(p, s) != cudaSuccess) return KDA_ERR_CUDA;
-    if (launch_prep(p, s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (prep) {
+        if (!a->device_status && cudaMemsetAsync(p.status, 0, sizeof(int32_t), s) != cudaSuccess)
+            return KDA_ERR_CUDA;
+        if (launch_chunk_table(p, s) != cudaSuccess) return KDA_ERR_CUDA;
+        if (launch_prep(p, s) != cudaSuccess) return KDA_ERR_CUDA;
+    }
     if (state_pass && launch_state(p, maps, s) != cudaSuccess) return KDA_ERR_CUDA;
     return KDA_OK;
 }
@@ -177,11 +181,15 @@ kda_status kda_prefill_workspace_layout(const kda_prefill_args* args, kda_worksp
 }
 
 kda_status kda_prefill(const kda_prefill_args* args, void* stream) {
-    return run_prefill(args, stream, true);
+    return run_prefill(args, stream, 3);
 }
 
 kda_status kda_prefill_prep(const kda_prefill_args* args, void* stream) {
-    return run_prefill(args, stream, false);
+    return run_prefill(args, stream, 1);
+}
+
+kda_status kda_prefill_state(const kda_prefill_args* args, void* stream) {
+    return run_prefill(args, stream, 2);
 }
 
 kda_status kda_verify(const kda_verify_args* a, void* stream) {

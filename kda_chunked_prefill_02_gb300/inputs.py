@@ -220,3 +220,24 @@ def config_inputs(name: str):
     if name == "verify":
         return verify_inputs(4, R=256, D=4, H=32)
     raise KeyError(name)
+
+
+def prefix_sample(inp: PrefillInputs, max_tokens: int) -> PrefillInputs:
+    """The first `max_tokens` tokens of every sequence (all heads), repacked the
+    same way; used to time bounded samples of a workload."""
+    if inp.cu_seqlens is None:
+        m = min(max_tokens, inp.q.shape[1])
+        f = lambda t: t[:, :m].contiguous()
+        return PrefillInputs(f(inp.q), f(inp.k), f(inp.v), f(inp.g), f(inp.beta),
+                             inp.initial_state, None, [m] * inp.q.shape[0])
+    cu = inp.cu_seqlens.tolist()
+    idx, lens = [], []
+    for n in range(len(cu) - 1):
+        m = min(max_tokens, cu[n + 1] - cu[n])
+        idx.extend(range(cu[n], cu[n] + m))
+        lens.append(m)
+    ix = torch.tensor(idx, dtype=torch.long)
+    f = lambda t: t.index_select(0, ix).contiguous()
+    new_cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32))
+    return PrefillInputs(f(inp.q), f(inp.k), f(inp.v), f(inp.g), f(inp.beta),
+                         inp.initial_state, new_cu, lens)

@@ -70,7 +70,7 @@ def lib():
         L.kda_prefill_workspace_layout.restype = ctypes.c_int
         L.kda_prefill_workspace_layout.argtypes = [ctypes.POINTER(PrefillArgs),
                                                    ctypes.POINTER(WorkspaceLayout)]
-        for name in ("kda_prefill", "kda_prefill_prep"):
+        for name in ("kda_prefill", "kda_prefill_prep", "kda_prefill_state"):
             f = getattr(L, name)
             f.restype = ctypes.c_int
             f.argtypes = [ctypes.POINTER(PrefillArgs), _p]
@@ -197,14 +197,16 @@ def workspace_layout(q, *, cu_seqlens=None):
 def kda_prefill(q, k, v, g, beta, *, initial_state=None, cu_seqlens=None, chunk=CHUNK,
                 beta_is_logit=True, scale=1.0, out=None, final_state=None,
                 output_final_state=True, workspace=None, device_status=None, stream=None,
-                prep_only=False):
+                prep_only=False, stage=None):
     """KDA prefill through the C ABI.
 
     Padded: q, k, g [B, T, H, 128]; v [B, T, H, 128]; beta [B, T, H].
     Varlen: q, k, g [T_total, H, 128]; beta [T_total, H]; cu_seqlens int32 [N+1]
     on the device.  initial_state fp32 [N, H, 128, 128] or None.
     Returns (out, final_state); with prep_only=True runs steps A1-A5 only and
-    returns (workspace, layout).
+    returns (workspace, layout).  stage="prep" / "state" run one stage alone
+    (the state stage reads the records a previous "prep" call left in
+    `workspace`) and return (out, final_state).
     """
     N = (cu_seqlens.shape[0] - 1) if cu_seqlens is not None else q.shape[0]
     H = q.shape[-2]
@@ -218,7 +220,10 @@ def kda_prefill(q, k, v, g, beta, *, initial_state=None, cu_seqlens=None, chunk=
         workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
     a = _prefill_args(q, k, v, g, beta, initial_state, cu_seqlens, out, final_state,
                       beta_is_logit, scale, workspace, device_status, chunk)
-    fn = lib().kda_prefill_prep if prep_only else lib().kda_prefill
+    fn = {None: lib().kda_prefill, "prep": lib().kda_prefill_prep,
+          "state": lib().kda_prefill_state}[stage]
+    if prep_only:
+        fn = lib().kda_prefill_prep
     _check(fn(ctypes.byref(a), _stream_handle(stream)))
     if prep_only:
         return workspace, workspace_layout(q, cu_seqlens=cu_seqlens)

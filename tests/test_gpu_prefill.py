@@ -177,3 +177,20 @@ def test_full_size_configs(name, heads):
     og = out if heads is None else out[..., heads, :]
     fg = fin if heads is None else fin[:, heads]
     assert_parity(og, fg, ro, rf, name)
+
+
+def test_split_stages_equal_one_call():
+    """kda_prefill_prep followed by kda_prefill_state gives the bits of kda_prefill."""
+    import kda_chunked_prefill_02_gb300 as K
+    inp = inputs.prefill_inputs(91, lengths=[129, 0, 64, 1], H=2)
+    d = inp.to("cuda")
+    a = K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, initial_state=d.initial_state,
+                      cu_seqlens=d.cu_seqlens)
+    ws = torch.empty(K.workspace_size(d.q, d.v, cu_seqlens=d.cu_seqlens), dtype=torch.uint8,
+                     device="cuda")
+    K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, initial_state=d.initial_state,
+                  cu_seqlens=d.cu_seqlens, workspace=ws, stage="prep")
+    b = K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, initial_state=d.initial_state,
+                      cu_seqlens=d.cu_seqlens, workspace=ws, stage="state")
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
