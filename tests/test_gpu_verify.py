@@ -22,7 +22,7 @@ def _run(vi, **kw):
 def _check(vi, out, pool, rows=None, **kw):
     R = vi.q.shape[0]
     rows = list(range(R)) if rows is None else list(rows)
-    sl = None if vi.slot is None else vi.slot[rows]
+    sl = torch.tensor(rows, dtype=torch.int32) if vi.slot is None else vi.slot[rows]
     o_ref, st_ref = oracle.verify(vi.q[rows], vi.k[rows], vi.v[rows], vi.g[rows], vi.beta[rows],
                                   vi.state_pool, vi.accepted[rows], slot=sl, **kw)
     err = np.abs(to_np(out[rows]) - o_ref).max()
