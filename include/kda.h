@@ -215,6 +215,34 @@ typedef struct kda_verify_args {
 
 kda_status kda_verify(const kda_verify_args* args, void* stream);
 
+/*
+ * kda_prefill for callers that cannot allocate device memory.  (The pages have
+ * no counterpart to this call; it exists for users of this library.)
+ *
+ * Who needs it: code that runs inside another runtime's fixed device-memory
+ * budget, or in a latency-critical loop where cudaMalloc is not allowed (it can
+ * synchronise the device and fragment a memory pool), and therefore cannot hand
+ * kda_prefill a workspace.  Same arguments and results as kda_prefill, except
+ * that `workspace` / `workspace_bytes` are ignored: the call uses a scratch
+ * array of KDA_NOALLOC_MAX_WORKSPACE_BYTES compiled into the library, which
+ * every GPU that loads the library keeps in device memory until the process
+ * exits.  The caller still passes (and owns) all inputs and outputs.
+ *
+ * Limits and behaviour:
+ *  - Returns KDA_ERR_UNSUPPORTED, launching nothing, when
+ *    kda_prefill_workspace_size(args) exceeds KDA_NOALLOC_MAX_WORKSPACE_BYTES
+ *    (about 290 chunk-head records: e.g. 2048 tokens x 8 heads).
+ *  - The first call on each device looks up the array's device address for
+ *    that device (with the device current); make that first call before any
+ *    stream capture.  It allocates nothing, here or later.
+ *  - Every call on a device shares the one array.  Calls whose kernels overlap
+ *    on the GPU (different streams, or different host threads) race on it and
+ *    give wrong results: serialise them.  Nothing in the array needs to start
+ *    at zero; each call writes what it later reads.
+ */
+#define KDA_NOALLOC_MAX_WORKSPACE_BYTES ((size_t)32 << 20)
+kda_status kda_prefill_noalloc(const kda_prefill_args* args, void* stream);
+
 /* Static string naming a status code. */
 const char* kda_status_string(kda_status status);
 

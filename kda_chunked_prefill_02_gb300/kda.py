@@ -267,3 +267,29 @@ def kda_verify(q, k, v, g, beta, state_pool, accepted, *, slot=None, beta_is_log
     a.device_status = _ptr(device_status)
     _check(lib().kda_verify(ctypes.byref(a), _stream_handle(stream)))
     return out
+
+
+NOALLOC_MAX_WORKSPACE_BYTES = 32 << 20
+
+
+def kda_prefill_noalloc(q, k, v, g, beta, *, initial_state=None, cu_seqlens=None, chunk=CHUNK,
+                        beta_is_logit=True, scale=1.0, out=None, final_state=None,
+                        device_status=None, stream=None):
+    """kda_prefill through the allocation-free entry point: the library uses its
+    built-in scratch array instead of a workspace (see kda_prefill_noalloc in
+    include/kda.h for the size limit and the rule that calls must not overlap
+    on the GPU).  Outputs are still allocated here when not given."""
+    L = lib()
+    f = L.kda_prefill_noalloc
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.POINTER(PrefillArgs), _p]
+    N = (cu_seqlens.shape[0] - 1) if cu_seqlens is not None else q.shape[0]
+    if out is None:
+        out = torch.empty(v.shape, dtype=torch.bfloat16, device=v.device)
+    if final_state is None:
+        final_state = torch.empty((N, q.shape[-2], q.shape[-1], v.shape[-1]),
+                                  dtype=torch.float32, device=q.device)
+    a = _prefill_args(q, k, v, g, beta, initial_state, cu_seqlens, out, final_state,
+                      beta_is_logit, scale, None, device_status, chunk)
+    _check(f(ctypes.byref(a), _stream_handle(stream)))
+    return out, final_state
