@@ -76,10 +76,12 @@ typedef enum {
  *   alias initial_state (in-place update).
  * beta_is_logit: 1 = beta holds logits b and the kernel uses sigmoid(b) (the
  *   fused beta sigmoid); 0 = beta already holds beta in [0, 1].
- * g: log decay per key channel, g <= 0.  Gates below -10 per token are handled
- *   with a bounded error of at most exp(-10) relative to |k_i . k_j| in the
- *   within-16-token interaction terms (the chunk factorisation's guard against
- *   exp overflow); the production gate bound is -5, which is exact.
+ * g: log decay per key channel, g <= 0.  Inside the 16-token blocks of a chunk
+ *   the interaction terms use the per-token gate floored at -5.4 (the chunk
+ *   factorisation's guard against exp overflow): exact for gates >= -5.4 (the
+ *   production gate bound is -5), otherwise a term whose true decay is below
+ *   e^-5.4 is replaced by one that is also below e^-5.4.  The inter-chunk state
+ *   recurrence always uses the exact gates.
  * scale: multiplies q (o_t = scale * S_t^T q_t); 1.0 for the plain recurrence.
  * workspace: device scratch of at least kda_prefill_workspace_size(args) bytes,
  *   256-byte aligned, owned by the caller, used only during the call's kernels

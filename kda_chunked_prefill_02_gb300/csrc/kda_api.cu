@@ -142,6 +142,27 @@ bool make_state_maps(const PrefillParams& p, StateMaps* m) {
 }
 
 // stages: bit 0 = A1-A5 (chunk table and prep), bit 1 = A6-A7 (state pass)
+// 4-D input tensor map [channel 128, head, token, batch] with one chunk of
+// one head per box.  Returns false if the driver refuses the layout.
+bool make_input_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint32_t esize,
+                    const int64_t* st, int64_t H, int64_t T, int64_t B) {
+    const uint64_t tstride = (uint64_t)st[1] * esize;
+    const uint64_t bstride = st[0] != 0 ? (uint64_t)st[0] * esize : tstride * (uint64_t)(T > 0 ? T : 1);
+    const uint64_t dims[4] = {128, (uint64_t)H, (uint64_t)T, (uint64_t)B};
+    const uint64_t strides[3] = {(uint64_t)st[2] * esize, tstride, bstride};
+    const uint32_t box[4] = {128, 1, (uint32_t)kChunk, 1};
+    return make_tensor_map(m, dt, 4, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+bool make_prep_maps(const kda_prefill_args* a, PrepMaps* m) {
+    const int64_t T = a->seqlen, B = a->cu_seqlens ? 1 : a->batch, H = a->num_heads;
+    if (T == 0 || B == 0) return true;
+    return make_input_map(&m->q, a->q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a->q_stride, H, T, B) &&
+           make_input_map(&m->k, a->k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a->k_stride, H, T, B) &&
+           make_input_map(&m->v, a->v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a->v_stride, H, T, B) &&
+           make_input_map(&m->g, a->g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a->g_stride, H, T, B);
+}
+
 kda_status run_prefill(const kda_prefill_args* a, void* stream, int stages) {
     const bool state_pass = (stages & 2) != 0, prep = (stages & 1) != 0;
     kda_status st = check_prefill(a);
@@ -153,12 +174,22 @@ kda_status run_prefill(const kda_prefill_args* a, void* stream, int stages) {
     StateMaps maps;
     memset(&maps, 0, sizeof(maps));
     if (state_pass && !make_state_maps(p, &maps)) return KDA_ERR_CUDA;
+    PrepMaps pmaps;
+    memset(&pmaps, 0, sizeof(pmaps));
+    int num_sms = 1;
+    if (prep) {
+        if (!make_prep_maps(a, &pmaps)) return KDA_ERR_UNSUPPORTED;
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return KDA_ERR_CUDA;
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (prep) {
         if (!a->device_status && cudaMemsetAsync(p.status, 0, sizeof(int32_t), s) != cudaSuccess)
             return KDA_ERR_CUDA;
         if (launch_chunk_table(p, s) != cudaSuccess) return KDA_ERR_CUDA;
-        if (launch_prep(p, s) != cudaSuccess) return KDA_ERR_CUDA;
+        if (launch_prep(p, pmaps, num_sms, s) != cudaSuccess) return KDA_ERR_CUDA;
     }
     if (state_pass && launch_state(p, maps, s) != cudaSuccess) return KDA_ERR_CUDA;
     return KDA_OK;

@@ -12,7 +12,7 @@ namespace kda {
 constexpr int kHeadDim = 128;   // K = V = 128
 constexpr int kChunk = 64;      // tokens per chunk
 constexpr int kSlab = 32;       // value columns per state-pass CTA
-constexpr float kGateClamp = -10.0f;  // per-token gate floor inside 16-token blocks
+constexpr float kGateFloor = -5.4f;   // per-token gate floor inside 16-token blocks (16 * 5.4 < 87)
 
 // Workspace record sizes (bytes) per (chunk, head).
 constexpr size_t kRecW = kChunk * kHeadDim * 2;    // bf16 [64][128]
@@ -87,8 +87,15 @@ struct StateMaps {
     CUtensorMap w, qp, kt, u, ol, eg;
 };
 
+// TMA descriptors of the inputs q, k, v (bf16) and g (fp32), each viewed as a
+// 4-D tensor [channel 128, head H, token T, batch B] with the caller's strides;
+// one box is one chunk of one head: [128, 1, 64, 1].
+struct PrepMaps {
+    CUtensorMap q, k, v, g;
+};
+
 cudaError_t launch_chunk_table(const PrefillParams& p, cudaStream_t s);
-cudaError_t launch_prep(const PrefillParams& p, cudaStream_t s);
+cudaError_t launch_prep(const PrefillParams& p, const PrepMaps& maps, int num_sms, cudaStream_t s);
 cudaError_t launch_state(const PrefillParams& p, const StateMaps& maps, cudaStream_t s);
 
 struct VerifyParams {
