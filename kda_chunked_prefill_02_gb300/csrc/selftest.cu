@@ -83,7 +83,80 @@ __global__ void __launch_bounds__(128)
     if (warp == 0) tmem_dealloc(tmem_base, 256);
 }
 
+// D = A B^T with B stored MN-major (B^T as [K rows][N contiguous]); mode 0 uses
+// lbo = 1024 (atoms along N adjacent) and sbo = N/64 * 1024, mode 1 swaps them.
+__global__ void __launch_bounds__(128)
+    umma_mn_selftest_kernel(const __nv_bfloat16* __restrict__ A, const __nv_bfloat16* __restrict__ B,
+                            float* __restrict__ D, int N, int mode, int* status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + 32768;
+    __shared__ uint64_t bar_mma;
+    __shared__ uint32_t tmem_base;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t sbo = (uint32_t)(N / 64) * 1024u;
+    if (tid == 0) {
+        mbar_init(&bar_mma, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_base, 256);
+        tmem_relinquish();
+    }
+    for (int i = tid; i < 128 * 128; i += 128) {
+        const int r = i >> 7, c = i & 127;
+        *reinterpret_cast<__nv_bfloat16*>(sA + (c >> 6) * 16384 + sw128_off(r, c & 63)) = A[i];
+    }
+    for (int i = tid; i < N * 128; i += 128) {  // B[n][k] -> MN-major (k, n)
+        const int n = i >> 7, k = i & 127;
+        *reinterpret_cast<__nv_bfloat16*>(sB + mn_sw128_off(k, n, sbo)) = B[i];
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {
+        const uint32_t lbo = mode == 0 ? 1024u : sbo, sb = mode == 0 ? sbo : 1024u;
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t kb = k >> 2, kin = (k & 3u) * 32u;
+            umma_bf16(tmem_base, sdesc_kmajor_sw128(smem_u32(sA) + kb * 16384 + kin),
+                      sdesc_mnmajor_sw128(smem_u32(sB) + (uint32_t)k * 2u * sbo, lbo, sb),
+                      idesc_bf16_f32_bmn(128, N), k > 0 ? 1u : 0u);
+        }
+        umma_commit(&bar_mma);
+    }
+    const bool ok = mbar_wait(&bar_mma, 0, nullptr);
+    if (!ok) atomicExch(status, 4);
+    tc_fence_after();
+    if (ok) {
+        for (int c0 = 0; c0 < N; c0 += 16) {
+            float v[16];
+            tmem_ld16(tmem_addr(tmem_base, warp * 32, c0), v);
+            const int row = warp * 32 + lane;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) D[row * N + c0 + i] = v[i];
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem_base, 256);
+}
+
 }  // namespace
+
+extern "C" int kda_selftest_umma_mn(const void* A, const void* B, float* D, int N, int mode,
+                                    int* status, void* stream) {
+    if (N < 64 || N > 256 || (N % 64) != 0) return 1;
+    const size_t smem = 1024 + 32768 + 2 * (size_t)N * 128;
+    if (cudaFuncSetAttribute(umma_mn_selftest_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+        return 3;
+    umma_mn_selftest_kernel<<<1, 128, smem, (cudaStream_t)stream>>>(
+        (const __nv_bfloat16*)A, (const __nv_bfloat16*)B, D, N, mode, status);
+    return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
 
 extern "C" int kda_selftest_umma(const void* A, const void* B, float* D, int N, int use_tma,
                                  int* status, void* stream) {

@@ -191,6 +191,28 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
            | ((uint64_t)2 << 61);                   // swizzle: 128 B
 }
 
+// Shared-memory matrix descriptor for an MN-major operand stored with the
+// 128-byte swizzle: for each K index a 128-byte row of 64 consecutive M/N
+// elements; 8 such rows (8 consecutive K) form a 1024-byte atom.  `lbo` is the
+// byte distance between atoms along M/N, `sbo` between 8-row groups along K.
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t lbo,
+                                                        uint32_t sbo) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor as idesc_bf16_f32 but with B MN-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_bmn(uint32_t M, uint32_t N) {
+    return idesc_bf16_f32(M, N) | (1u << 16);
+}
+
+// Byte offset of bf16 element (k, n) of an MN-major SW128 operand laid out as
+// [K/8][N/64] atoms (atom (kg, m) at kg * sbo + m * 1024).
+__host__ __device__ __forceinline__ uint32_t mn_sw128_off(uint32_t k, uint32_t n, uint32_t sbo) {
+    return (k >> 3) * sbo + (n >> 6) * 1024u + (k & 7u) * 128u +
+           (((((n & 63u) >> 3) ^ (k & 7u)) << 4) | ((n & 7u) << 1));
+}
+
 // D[tmem] (+)= A * B^T, issued by a single thread.  A is M x 16 (K-major),
 // B is N x 16 (K-major), one K step of 16 bf16 elements.
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,

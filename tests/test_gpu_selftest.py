@@ -34,3 +34,22 @@ def test_umma_tile(selftest, N, use_tma):
     assert rc == 0 and status.item() == 0
     ref = A.float() @ B.float().T
     torch.testing.assert_close(D, ref, atol=2e-3, rtol=1e-4)
+
+
+@pytest.mark.parametrize("N", [64, 128, 256])
+def test_umma_tile_b_mn_major(selftest, N):
+    """B stored MN-major (128-byte swizzle, atoms along N 1024 B apart, 8-row K
+    groups N/64 KB apart): the layout the prep kernel uses for [K e^Gam | V]."""
+    f = selftest.kda_selftest_umma_mn
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 2 + [ctypes.c_void_p] * 2
+    g = torch.Generator(device="cpu").manual_seed(100 + N)
+    A = torch.randn(128, 128, generator=g).to(torch.bfloat16).cuda()
+    B = torch.randn(N, 128, generator=g).to(torch.bfloat16).cuda()
+    D = torch.full((128, N), float("nan"), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert f(A.data_ptr(), B.data_ptr(), D.data_ptr(), N, 0, status.data_ptr(),
+             torch.cuda.current_stream().cuda_stream) == 0
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    torch.testing.assert_close(D, A.float() @ B.float().T, atol=2e-3, rtol=1e-4)
