@@ -155,19 +155,24 @@ kda_status kda_prefill_state(const kda_prefill_args* args, void* stream);
 
 /*
  * Workspace layout (byte offsets from `workspace`) of the per-chunk records
- * that kda_prefill_prep writes.  Records are indexed by r = chunk * H + head,
- * where chunk is the global chunk index (sequence n's chunks are
- * chunk_offset[n] .. chunk_offset[n+1]-1 in token order).  Per record:
- *   W    bf16 [64][128]   T Diag(beta) (K e^Gam)
- *   Qp   bf16 [64][128]   scale*Q e^Gam - Aqk W
- *   Kt   bf16 [128][64]   (K e^{gam - Gam})^T
- *   U    fp32 [64][128]   T Diag(beta) V
- *   Ol   fp32 [64][128]   Aqk U
- *   eg   fp32 [128]       exp(gam), gam = chunk total of g per key channel
- * chunk_offset: int32 [N+1] (device).  Rows past a tail chunk's length are 0.
+ * that kda_prefill_prep writes.  Record r = chunk * H + head (chunk is the
+ * global chunk index; sequence n owns chunks chunk_offset[n] ..
+ * chunk_offset[n+1]-1 in token order) starts at records + r * record_bytes and
+ * holds shared-memory images of the state pass's operands.  bf16 images use
+ * the 128-byte swizzle (16-byte chunk c of 128-byte row x stored at
+ * x*128 + ((c ^ (x mod 8)) * 16)):
+ *   [0, 32768)        [W ; Q'] bf16: key channels 0-63 then 64-127, each
+ *                     128 rows x 128 B; rows 0-63 W = T Diag(beta)(K e^Gam),
+ *                     rows 64-127 Q' = scale*Q e^Gam - Aqk W
+ *   [32768, 49152)    Kt bf16: 128 key rows x 64 tokens, (K e^{gam - Gam})^T
+ *   [49152, 81920)    U = T Diag(beta) V fp32: value slabs 0-3 (32 columns
+ *                     each), each 64 rows x 128 B, same swizzle on fp32 rows
+ *   [81920, 114688)   O_loc = Aqk U fp32, same layout
+ *   [114688, 115200)  exp(gam) fp32 [128], gam = chunk total of g
+ * Rows past a tail chunk's length are zero.  chunk_offset: int32 [N+1].
  */
 typedef struct kda_workspace_layout {
-    size_t w, qp, kt, u, ol, eg, chunk_offset, status, total;
+    size_t records, record_bytes, chunk_offset, status, total;
     int64_t max_chunks;         /* records per head */
 } kda_workspace_layout;
 kda_status kda_prefill_workspace_layout(const kda_prefill_args* args,

@@ -27,12 +27,8 @@ bool layout_of(const kda_prefill_args* a, kda_workspace_layout* L) {
     const size_t nrec = (size_t)mc * (size_t)a->num_heads;
     size_t o = 0;
     L->max_chunks = mc;
-    L->w = o;  o = align_up(o + nrec * kRecW);
-    L->qp = o; o = align_up(o + nrec * kRecQp);
-    L->kt = o; o = align_up(o + nrec * kRecKt);
-    L->u = o;  o = align_up(o + nrec * kRecU);
-    L->ol = o; o = align_up(o + nrec * kRecOl);
-    L->eg = o; o = align_up(o + nrec * kRecEg);
+    L->record_bytes = kRecBytes;
+    L->records = o; o = align_up(o + nrec * kRecBytes);
     L->chunk_offset = o; o = align_up(o + sizeof(int32_t) * (size_t)(a->num_seqs + 1));
     L->status = o; o = align_up(o + sizeof(int32_t));
     L->total = o;
@@ -75,9 +71,6 @@ kda_status check_prefill(const kda_prefill_args* a) {
         return KDA_ERR_UNSUPPORTED;
     kda_workspace_layout L;
     if (!layout_of(a, &L)) return KDA_ERR_INVALID_ARG;
-    // TMA coordinates are int32: rows of the Kt array must stay below 2^31.
-    if ((double)L.max_chunks * (double)a->num_heads * 128.0 >= 2147483647.0)
-        return KDA_ERR_UNSUPPORTED;
     if (!a->workspace || a->workspace_bytes < L.total) return KDA_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(a->workspace) & (kAlign - 1)) != 0) return KDA_ERR_UNSUPPORTED;
     return KDA_OK;
@@ -108,40 +101,9 @@ void fill_params(const kda_prefill_args* a, const kda_workspace_layout& L, Prefi
     p->max_chunks = (int)L.max_chunks;
     p->beta_is_logit = a->beta_is_logit ? 1 : 0;
     p->scale = a->scale;
-    p->ws_w = reinterpret_cast<__nv_bfloat16*>(ws + L.w);
-    p->ws_qp = reinterpret_cast<__nv_bfloat16*>(ws + L.qp);
-    p->ws_kt = reinterpret_cast<__nv_bfloat16*>(ws + L.kt);
-    p->ws_u = reinterpret_cast<float*>(ws + L.u);
-    p->ws_ol = reinterpret_cast<float*>(ws + L.ol);
-    p->ws_eg = reinterpret_cast<float*>(ws + L.eg);
+    p->ws_rec = ws + L.records;
 }
 
-bool make_state_maps(const PrefillParams& p, StateMaps* m) {
-    const uint64_t nrec = (uint64_t)p.max_chunks * (uint64_t)p.H;
-    if (nrec == 0) return true;
-    const uint64_t d_w[2] = {128, nrec * 64}, s_w[1] = {256};
-    const uint32_t b_w[2] = {64, 64};
-    const uint64_t d_kt[2] = {64, nrec * 128}, s_kt[1] = {128};
-    const uint32_t b_kt[2] = {64, 128};
-    const uint64_t d_u[2] = {128, nrec * 64}, s_u[1] = {512};
-    const uint32_t b_u[2] = {kSlab, 64};
-    const uint64_t d_eg[2] = {128, nrec}, s_eg[1] = {512};
-    const uint32_t b_eg[2] = {128, 1};
-    return make_tensor_map(&m->w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.ws_w, d_w, s_w, b_w,
-                           CU_TENSOR_MAP_SWIZZLE_128B) &&
-           make_tensor_map(&m->qp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.ws_qp, d_w, s_w, b_w,
-                           CU_TENSOR_MAP_SWIZZLE_128B) &&
-           make_tensor_map(&m->kt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.ws_kt, d_kt, s_kt, b_kt,
-                           CU_TENSOR_MAP_SWIZZLE_128B) &&
-           make_tensor_map(&m->u, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.ws_u, d_u, s_u, b_u,
-                           CU_TENSOR_MAP_SWIZZLE_128B) &&
-           make_tensor_map(&m->ol, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.ws_ol, d_u, s_u, b_u,
-                           CU_TENSOR_MAP_SWIZZLE_128B) &&
-           make_tensor_map(&m->eg, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.ws_eg, d_eg, s_eg, b_eg,
-                           CU_TENSOR_MAP_SWIZZLE_NONE);
-}
-
-// stages: bit 0 = A1-A5 (chunk table and prep), bit 1 = A6-A7 (state pass)
 // 4-D input tensor map [channel 128, head, token, batch] with one chunk of
 // one head per box.  Returns false if the driver refuses the layout.
 bool make_input_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint32_t esize,
@@ -171,9 +133,6 @@ kda_status run_prefill(const kda_prefill_args* a, void* stream, int stages) {
     layout_of(a, &L);
     PrefillParams p;
     fill_params(a, L, &p);
-    StateMaps maps;
-    memset(&maps, 0, sizeof(maps));
-    if (state_pass && !make_state_maps(p, &maps)) return KDA_ERR_CUDA;
     PrepMaps pmaps;
     memset(&pmaps, 0, sizeof(pmaps));
     int num_sms = 1;
@@ -191,7 +150,7 @@ kda_status run_prefill(const kda_prefill_args* a, void* stream, int stages) {
         if (launch_chunk_table(p, s) != cudaSuccess) return KDA_ERR_CUDA;
         if (launch_prep(p, pmaps, num_sms, s) != cudaSuccess) return KDA_ERR_CUDA;
     }
-    if (state_pass && launch_state(p, maps, s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (state_pass && launch_state(p, s) != cudaSuccess) return KDA_ERR_CUDA;
     return KDA_OK;
 }
 

@@ -14,13 +14,17 @@ constexpr int kChunk = 64;      // tokens per chunk
 constexpr int kSlab = 32;       // value columns per state-pass CTA
 constexpr float kGateFloor = -5.4f;   // per-token gate floor inside 16-token blocks (16 * 5.4 < 87)
 
-// Workspace record sizes (bytes) per (chunk, head).
-constexpr size_t kRecW = kChunk * kHeadDim * 2;    // bf16 [64][128]
-constexpr size_t kRecQp = kChunk * kHeadDim * 2;   // bf16 [64][128]
-constexpr size_t kRecKt = kHeadDim * kChunk * 2;   // bf16 [128][64]
-constexpr size_t kRecU = kChunk * kHeadDim * 4;    // fp32 [64][128]
-constexpr size_t kRecOl = kChunk * kHeadDim * 4;   // fp32 [64][128]
-constexpr size_t kRecEg = kHeadDim * 4;            // fp32 [128]
+// Workspace record per (chunk, head): shared-memory images, written by the prep
+// kernel with bulk copies and read back by the state pass with bulk copies.
+// bf16 images use the 128-byte swizzle of K-major tcgen05 operands (16-byte
+// chunk c of 128-byte row r at r*128 + ((c ^ (r & 7)) << 4)); fp32 slabs use
+// the same swizzle on 128-byte rows of 32 floats.
+constexpr uint32_t kRecA1 = 0;          // [W ; Q'] bf16: 2 column blocks x 128 rows x 128 B
+constexpr uint32_t kRecKt = 32768;      // Kt bf16: 128 key rows x 64 tokens
+constexpr uint32_t kRecU = 49152;       // U fp32: 4 value slabs x 64 rows x 32 floats
+constexpr uint32_t kRecOl = 81920;      // O_loc fp32: 4 value slabs x 64 rows x 32 floats
+constexpr uint32_t kRecEg = 114688;     // e^gam fp32 [128]
+constexpr uint32_t kRecBytes = 115200;
 
 struct PrefillParams {
     const __nv_bfloat16* q;
@@ -39,12 +43,7 @@ struct PrefillParams {
     int max_chunks;          // chunk records per head (upper bound)
     int beta_is_logit;
     float scale;
-    __nv_bfloat16* ws_w;
-    __nv_bfloat16* ws_qp;
-    __nv_bfloat16* ws_kt;
-    float* ws_u;
-    float* ws_ol;
-    float* ws_eg;
+    uint8_t* ws_rec;         // kRecBytes per (chunk, head) record, record r = chunk * H + head
 };
 
 // Chunk c (global index) -> sequence, token start and length.
@@ -82,11 +81,6 @@ __device__ __forceinline__ ChunkInfo chunk_info(const PrefillParams& p, int c) {
     return ci;
 }
 
-// TMA descriptors of the workspace arrays, built on the host per call.
-struct StateMaps {
-    CUtensorMap w, qp, kt, u, ol, eg;
-};
-
 // TMA descriptors of the inputs q, k, v (bf16) and g (fp32), each viewed as a
 // 4-D tensor [channel 128, head H, token T, batch B] with the caller's strides;
 // one box is one chunk of one head: [128, 1, 64, 1].
@@ -96,7 +90,7 @@ struct PrepMaps {
 
 cudaError_t launch_chunk_table(const PrefillParams& p, cudaStream_t s);
 cudaError_t launch_prep(const PrefillParams& p, const PrepMaps& maps, int num_sms, cudaStream_t s);
-cudaError_t launch_state(const PrefillParams& p, const StateMaps& maps, cudaStream_t s);
+cudaError_t launch_state(const PrefillParams& p, cudaStream_t s);
 
 struct VerifyParams {
     const __nv_bfloat16* q;

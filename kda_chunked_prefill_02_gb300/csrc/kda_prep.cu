@@ -50,7 +50,8 @@ constexpr uint32_t kInBytes = 81920;
 constexpr uint32_t O_R = 81920;       // A operand R = [K ac ; Q ac]: 2 x (128 rows x 128 B)
 constexpr uint32_t O_Y = 114688;      // B operand [Yoff (96 rows) ; Yd (64 rows)]: 2 x (160 x 128 B)
 constexpr uint32_t kYBlock = 160 * 128;
-constexpr uint32_t O_KV = 155648;     // B operand [K e^Gam | V]^T: 256 rows x 64 tokens
+constexpr uint32_t O_KV = 155648;     // B operand [K e^Gam | V], MN-major: 8 token groups x 4 KB
+constexpr uint32_t kKvSbo = 4096;     // byte distance between 8-token groups of the KV operand
 constexpr uint32_t O_QT = 188416;     // bf16 [64][136] Q e^Gam (row pitch 272 B)
 constexpr uint32_t kQtPitch = 272;
 constexpr uint32_t O_TOT = 205824;    // fp32 [4][128] block gate totals
@@ -64,6 +65,10 @@ constexpr uint32_t O_X = 115200;      // fp32 [32][33] products
 constexpr uint32_t O_AQK = 119808;    // A operand Aqk: 64 rows x 128 B (rows 64..127 are don't-care)
 constexpr uint32_t O_TT = 128000;     // A operand [T' ; Aqk T']: 128 rows x 128 B
 constexpr uint32_t O_TTR = 144384;    // B operand T'^T: 64 rows x 128 B
+// Staging of the record images written by the last epilogue (over R, Y, KV).
+constexpr uint32_t O_SA1 = 81920;     // [W ; Q'] image, 32 KB
+constexpr uint32_t O_SU = 114688;     // U image, 32 KB
+constexpr uint32_t O_SOL = 147456;    // O_loc image, 32 KB
 
 // TMEM columns.
 constexpr uint32_t TM_A = 0, TM_DIAG = 96, TM_B = 192, TM_C = 0, TM_COLS = 256;
@@ -167,6 +172,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             tot[G * 128 + c0] = d0;
             tot[G * 128 + c0 + 1] = d1;
         }
+        if (tid == 0) bulk_wait_read();  // the previous record's images have left the staging area
         __syncthreads();
 
         // ---- E2: the MMA operands and the records that need no MMA.
@@ -195,14 +201,15 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             // 1 / (floored-gate block product): <= e^86.4
             const float ib0 = 1.0f / (fmaxf(p0[0], kPFloor) * zc0[0]);
             const float ib1 = 1.0f / (fmaxf(p1[0], kPFloor) * zc1[0]);
+            uint8_t* rp = p.ws_rec + (size_t)rec * kRecBytes;
             if (G == 0)
-                *reinterpret_cast<float2*>(p.ws_eg + (size_t)rec * kHeadDim + c0) =
+                *reinterpret_cast<float2*>(rp + kRecEg + c0 * 4) =
                     make_float2(__expf(d0[0] + d0[1] + d0[2] + d0[3]),
                                 __expf(d1[0] + d1[1] + d1[2] + d1[3]));
             const float qscale = p.scale;
             const uint32_t bo = blk * 16384u, yb = blk * kYBlock;
             float a0 = 1.f, a1 = 1.f, ac0 = 1.f, ac1 = 1.f;
-            float ek0 = 0.f, ek1 = 0.f, ev0 = 0.f, ev1 = 0.f, eh0 = 0.f, eh1 = 0.f;
+            float eh0 = 0.f, eh1 = 0.f;
             uint32_t kh0[8], kh1[8];
 #pragma unroll
             for (int l = 0; l < 16; ++l) {
@@ -230,28 +237,24 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                 // Q e^Gam for Q'
                 const float ea0 = a0 * B0, ea1 = a1 * B1;
                 st_u32(sm + O_QT + i * kQtPitch + c0 * 2, pack_bf16x2(qq.x * ea0, qq.y * ea1));
-                // [K e^Gam | V]^T and Kt = (K e^{gam - Gam})^T, by token pairs
-                const float ke0 = kk.x * ea0, ke1 = kk.y * ea1;
+                // [K e^Gam | V] (MN-major: token row i, channels contiguous)
+                st_u32(sm + O_KV + mn_sw128_off(i, c0, kKvSbo), pack_bf16x2(kk.x * ea0, kk.y * ea1));
+                st_u32(sm + O_KV + mn_sw128_off(i, 128 + c0, kKvSbo), pack_bf16x2(vv.x, vv.y));
+                // Kt = (K e^{gam - Gam})^T, packed by token pairs
                 const float hh0 = kk.x * z0[l] * E0, hh1 = kk.y * z1[l] * E1;
                 if ((l & 1) == 0) {
-                    ek0 = ke0; ek1 = ke1; ev0 = vv.x; ev1 = vv.y; eh0 = hh0; eh1 = hh1;
+                    eh0 = hh0; eh1 = hh1;
                 } else {
-                    const int ie = i - 1;
-                    st_u32(sm + O_KV + sw128_off(c0, ie), pack_bf16x2(ek0, ke0));
-                    st_u32(sm + O_KV + sw128_off(c0 + 1, ie), pack_bf16x2(ek1, ke1));
-                    st_u32(sm + O_KV + sw128_off(128 + c0, ie), pack_bf16x2(ev0, vv.x));
-                    st_u32(sm + O_KV + sw128_off(128 + c0 + 1, ie), pack_bf16x2(ev1, vv.y));
                     kh0[l >> 1] = pack_bf16x2(eh0, hh0);
                     kh1[l >> 1] = pack_bf16x2(eh1, hh1);
                 }
             }
-            const int t0c = 16 * G;
-            uint4* kt0 = reinterpret_cast<uint4*>(p.ws_kt + (size_t)rec * (kHeadDim * kChunk) + c0 * kChunk + t0c);
-            uint4* kt1 = reinterpret_cast<uint4*>(p.ws_kt + (size_t)rec * (kHeadDim * kChunk) + (c0 + 1) * kChunk + t0c);
-            kt0[0] = make_uint4(kh0[0], kh0[1], kh0[2], kh0[3]);
-            kt0[1] = make_uint4(kh0[4], kh0[5], kh0[6], kh0[7]);
-            kt1[0] = make_uint4(kh1[0], kh1[1], kh1[2], kh1[3]);
-            kt1[1] = make_uint4(kh1[4], kh1[5], kh1[6], kh1[7]);
+            // Kt image rows c0, c0 + 1: tokens 16G..16G+15 are 16-byte chunks 2G, 2G+1
+            uint8_t* kt = rp + kRecKt;
+            *reinterpret_cast<uint4*>(kt + sw128_off(c0, 16 * G)) = make_uint4(kh0[0], kh0[1], kh0[2], kh0[3]);
+            *reinterpret_cast<uint4*>(kt + sw128_off(c0, 16 * G + 8)) = make_uint4(kh0[4], kh0[5], kh0[6], kh0[7]);
+            *reinterpret_cast<uint4*>(kt + sw128_off(c0 + 1, 16 * G)) = make_uint4(kh1[0], kh1[1], kh1[2], kh1[3]);
+            *reinterpret_cast<uint4*>(kt + sw128_off(c0 + 1, 16 * G + 8)) = make_uint4(kh1[4], kh1[5], kh1[6], kh1[7]);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -322,67 +325,103 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         // ---- UT transform: T = (I + A)^-1 for the unit lower-triangular 64 x 64
         // system, fp32, blocked: four 16 x 16 diagonal inverses by forward
         // substitution, then [[Ta,0],[Aba,Tb]]^-1 = [[Ta^-1,0],[-Tb^-1 Aba Ta^-1, Tb^-1]]
-        // at 16 -> 32 and 32 -> 64.
-        for (int e = tid; e < 64 * kPA; e += kPrepThreads) sT[e] = 0.f;
-        __syncthreads();
+        // at 16 -> 32 and 32 -> 64.  Blocks above the diagonal are never read
+        // except the two 16 x 16 ones inside the 32 x 32 diagonal blocks, which
+        // are written as zeros.
         if (tid < 64) {
-            const int I = tid >> 4, l = tid & 15, s = 16 * I;
+            const int I = tid >> 4, l = tid & 15, s0 = 16 * I;
             float x[16];
 #pragma unroll
             for (int r = 0; r < 16; ++r) x[r] = (r == l) ? 1.f : 0.f;
 #pragma unroll
             for (int r = 1; r < 16; ++r) {
-                float acc = x[r];
+                float acc0 = x[r], acc1 = 0.f;
 #pragma unroll
-                for (int m = 0; m < r; ++m) acc = fmaf(-sA[(s + r) * kPA + s + m], x[m], acc);
-                x[r] = acc;
+                for (int m = 0; m < r; m += 2) {
+                    acc0 = fmaf(-sA[(s0 + r) * kPA + s0 + m], x[m], acc0);
+                    if (m + 1 < r) acc1 = fmaf(-sA[(s0 + r) * kPA + s0 + m + 1], x[m + 1], acc1);
+                }
+                x[r] = acc0 + acc1;
             }
 #pragma unroll
-            for (int r = 0; r < 16; ++r) sT[(s + r) * kPA + s + l] = x[r];
+            for (int r = 0; r < 16; ++r) sT[(s0 + r) * kPA + s0 + l] = x[r];
         }
         __syncthreads();
-        for (int e = tid; e < 512; e += kPrepThreads) {  // X = A_10 T_00 (both 32-blocks)
-            const int pb = 32 * (e >> 8), r = (e >> 4) & 15, c = e & 15;
-            float acc = 0.f;
+        {
+            float acc[2];
 #pragma unroll
-            for (int m = 0; m < 16; ++m)
-                acc = fmaf(sA[(pb + 16 + r) * kPA + pb + m], sT[(pb + m) * kPA + pb + c], acc);
-            sX[e] = acc;
+            for (int u = 0; u < 2; ++u) {  // X = A_10 T_00 (both 32-blocks)
+                const int e = tid + 256 * u, pb = 32 * (e >> 8), r = (e >> 4) & 15, c = e & 15;
+                acc[u] = 0.f;
+#pragma unroll
+                for (int m = 0; m < 16; ++m)
+                    acc[u] = fmaf(sA[(pb + 16 + r) * kPA + pb + m], sT[(pb + m) * kPA + pb + c], acc[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) sX[tid + 256 * u] = acc[u];
         }
         __syncthreads();
-        for (int e = tid; e < 512; e += kPrepThreads) {  // T_10 = -T_11 X
-            const int pb = 32 * (e >> 8), r = (e >> 4) & 15, c = e & 15;
-            float acc = 0.f;
+        {
+            float acc[2];
 #pragma unroll
-            for (int m = 0; m < 16; ++m)
-                acc = fmaf(sT[(pb + 16 + r) * kPA + pb + 16 + m], sX[(e & 256) + m * 16 + c], acc);
-            sT[(pb + 16 + r) * kPA + pb + c] = -acc;
+            for (int u = 0; u < 2; ++u) {  // T_10 = -T_11 X
+                const int e = tid + 256 * u, pb = 32 * (e >> 8), r = (e >> 4) & 15, c = e & 15;
+                acc[u] = 0.f;
+#pragma unroll
+                for (int m = 0; m < 16; ++m)
+                    acc[u] = fmaf(sT[(pb + 16 + r) * kPA + pb + 16 + m], sX[(e & 256) + m * 16 + c], acc[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int e = tid + 256 * u, pb = 32 * (e >> 8), r = (e >> 4) & 15, c = e & 15;
+                sT[(pb + 16 + r) * kPA + pb + c] = -acc[u];
+                sT[(pb + r) * kPA + pb + 16 + c] = 0.f;  // block above the diagonal
+            }
         }
         __syncthreads();
-        for (int e = tid; e < 1024; e += kPrepThreads) {  // X = A[32:,:32] T[:32,:32]
-            const int r = e >> 5, c = e & 31;
-            float acc = 0.f;
+        {
+            float acc[4];
 #pragma unroll
-            for (int m = 0; m < 32; ++m) acc = fmaf(sA[(32 + r) * kPA + m], sT[m * kPA + c], acc);
-            sX[r * 33 + c] = acc;
+            for (int u = 0; u < 4; ++u) {  // X = A[32:,:32] T[:32,:32]
+                const int e = tid + 256 * u, r = e >> 5, c = e & 31;
+                acc[u] = 0.f;
+#pragma unroll
+                for (int m = 0; m < 32; ++m) acc[u] = fmaf(sA[(32 + r) * kPA + m], sT[m * kPA + c], acc[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int e = tid + 256 * u;
+                sX[(e >> 5) * 33 + (e & 31)] = acc[u];
+            }
         }
         __syncthreads();
-        for (int e = tid; e < 1024; e += kPrepThreads) {  // T[32:,:32] = -T[32:,32:] X
-            const int r = e >> 5, c = e & 31;
-            float acc = 0.f;
+        {
+            float acc[4];
 #pragma unroll
-            for (int m = 0; m < 32; ++m) acc = fmaf(sT[(32 + r) * kPA + 32 + m], sX[m * 33 + c], acc);
-            sT[(32 + r) * kPA + c] = -acc;
+            for (int u = 0; u < 4; ++u) {  // T[32:,:32] = -T[32:,32:] X
+                const int e = tid + 256 * u, r = e >> 5, c = e & 31;
+                acc[u] = 0.f;
+#pragma unroll
+                for (int m = 0; m < 32; ++m) acc[u] = fmaf(sT[(32 + r) * kPA + 32 + m], sX[m * 33 + c], acc[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int e = tid + 256 * u;
+                sT[(32 + (e >> 5)) * kPA + (e & 31)] = -acc[u];
+            }
         }
         __syncthreads();
         // T' = T Diag(beta): rows 0..63 of the TT operand (K-major over j) and
-        // T'^T, the B operand of MMA B (row n, K index j).
+        // T'^T, the B operand of MMA B (row n, K index j); entries above the
+        // diagonal are zero.
         for (int e = tid; e < 64 * 32; e += kPrepThreads) {
             const int r = e >> 5, jp = 2 * (e & 31);
-            st_u32(sm + O_TT + sw128_off(r, jp),
-                   pack_bf16x2(sT[r * kPA + jp] * sBeta[jp], sT[r * kPA + jp + 1] * sBeta[jp + 1]));
-            st_u32(sm + O_TTR + sw128_off(r, jp),
-                   pack_bf16x2(sT[jp * kPA + r] * sBeta[r], sT[(jp + 1) * kPA + r] * sBeta[r]));
+            const float t0 = jp <= r ? sT[r * kPA + jp] * sBeta[jp] : 0.f;
+            const float t1 = jp + 1 <= r ? sT[r * kPA + jp + 1] * sBeta[jp + 1] : 0.f;
+            st_u32(sm + O_TT + sw128_off(r, jp), pack_bf16x2(t0, t1));
+            const float u0 = r <= jp ? sT[jp * kPA + r] * sBeta[r] : 0.f;
+            const float u1 = r <= jp + 1 ? sT[(jp + 1) * kPA + r] * sBeta[r] : 0.f;
+            st_u32(sm + O_TTR + sw128_off(r, jp), pack_bf16x2(u0, u1));
         }
         fence_proxy_async_smem();
         __syncthreads();
@@ -416,19 +455,22 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         // ---- MMA C: [T' ; Aqk T'] [K e^Gam | V] = [W | U ; Aqk W | Aqk U]  (N = 256)
         if (tid == 0) {
             tc_fence_after();
-            umma_tile(tb + TM_C, smem_u32(sm + O_TT), 0, smem_u32(sm + O_KV), 0, 64,
-                      idesc_bf16_f32(128, 256), false);
+            const uint32_t tt = smem_u32(sm + O_TT), kv = smem_u32(sm + O_KV);
+            for (uint32_t k = 0; k < 4; ++k)
+                umma_bf16(tb + TM_C, sdesc_kmajor_sw128(tt + k * 32u),
+                          sdesc_mnmajor_sw128(kv + k * 2u * kKvSbo, 1024u, kKvSbo),
+                          idesc_bf16_f32_bmn(128, 256), k > 0 ? 1u : 0u);
             umma_commit(&bar_mma[2]);
         }
         ok = __syncthreads_and(mbar_wait(&bar_mma[2], it & 1, nullptr));
         tc_fence_after();
         if (!ok) break;
         {
-            // ---- Epilogue C: W, U (rows 0..63) and Q' = Q e^Gam - Aqk W,
-            // O_loc = Aqk U (rows 64..127) to the workspace records.
-            const int i = 32 * (qd & 1) + lane;
+            // ---- Epilogue C: [W ; Q'] rows (Q' = Q e^Gam - Aqk W) from the first 128
+            // columns and U / O_loc from the last 128, written as the record's
+            // shared-memory images and stored with bulk copies.
+            const int r = 32 * qd + lane, i = r & 63;
             const bool top = qd < 2;
-            const size_t rb = (size_t)rec * (kChunk * kHeadDim) + (size_t)i * kHeadDim;
 #pragma unroll 1
             for (int cg = 0; cg < 8; ++cg) {
                 const int col = 16 * cg;
@@ -447,16 +489,28 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                             w[x] = pack_bf16x2(q2.x - v[2 * x], q2.y - v[2 * x + 1]);
                         }
                     }
-                    uint4* dst = reinterpret_cast<uint4*>((top ? p.ws_w : p.ws_qp) + rb + col);
-                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    uint8_t* img = sm + O_SA1 + (col >> 6) * 16384;
+                    *reinterpret_cast<uint4*>(img + sw128_off(r, col & 63)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<uint4*>(img + sw128_off(r, (col & 63) + 8)) = make_uint4(w[4], w[5], w[6], w[7]);
                 } else {
-                    float4* dst = reinterpret_cast<float4*>((top ? p.ws_u : p.ws_ol) + rb + col);
+                    uint8_t* img = sm + (top ? O_SU : O_SOL) + (col >> 5) * 8192;
+                    const int cs = col & 31;
 #pragma unroll
                     for (int x = 0; x < 4; ++x)
-                        dst[x] = make_float4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
+                        *reinterpret_cast<float4*>(img + i * 128 + ((((cs >> 2) + x) ^ (i & 7)) << 4)) =
+                            make_float4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
                 }
             }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            uint8_t* rp = p.ws_rec + (size_t)rec * kRecBytes;
+            bulk_store(rp + kRecA1, sm + O_SA1, 32768);
+            bulk_store(rp + kRecU, sm + O_SU, 32768);
+            bulk_store(rp + kRecOl, sm + O_SOL, 32768);
+            bulk_commit();
         }
         tc_fence_before();
         __syncthreads();
@@ -464,6 +518,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         ci = cn;
     }
     if (!ok && tid == 0) atomicExch(p.status, 4);
+    if (tid == 0) bulk_wait_all();  // no bulk store may outlive the CTA's shared memory
     // Never leave with a copy in flight (only possible after a failed wait).
     if (pend_parity >= 0 && tid == 0) mbar_wait(&bar_in, (uint32_t)pend_parity, nullptr);
     tc_fence_before();

@@ -3,8 +3,8 @@
 // One CTA owns one chain slab: (sequence n, head h, 32 value columns of the
 // 128 x 128 state).  Value columns of the state never interact, so the four
 // slabs of a chain run in parallel (the "independent value-row slabs" of the
-// cuDNN-frontend sm90 KDA page, Conversation).  Per chunk, with the operands
-// that the prep kernel left in the workspace:
+// cuDNN-frontend sm90 KDA page, Conversation).  Per chunk, with the record the
+// prep kernel left in the workspace:
 //   P1 (tensor core)  D1 = [W ; Q'] S          M = 128 (64 W rows + 64 Q' rows), K = 128
 //   epilogue          V_new = U - D1[0:64],  O = O_loc + D1[64:128] -> out (bf16)
 //   P2 (tensor core)  D2 = Kt V_new             M = 128 keys, K = 64 tokens
@@ -12,54 +12,53 @@
 // The fp32 state lives in the epilogue threads' registers (thread = key row);
 // its bf16 image in shared memory is the B operand of the next chunk's P1.
 //
-// Warp roles: warp 0 issues the TMA loads of the next chunk's operands (two
-// stages), warp 1 owns TMEM and issues the MMAs, warps 2-5 are the epilogue
-// (one TMEM lane quarter each).  Every hand-off is an mbarrier, so the reads of
-// one chunk's buffers are ordered before the next chunk's writes (the
-// sPartialLast race of the TensorRT-LLM K1 page), and every thread that read
-// TMEM has waited for its loads and crossed a tcgen05 fence plus a CTA barrier
-// before TMEM is freed (the dealloc ordering of the TensorRT-LLM MQA-logits
-// page).  All waits are bounded; a wait that runs out sets KDA_ERR_TIMEOUT and
-// the CTA winds down.
+// Warp roles: warp 0 fetches the next chunks' records with 1-D bulk copies
+// (two stages); warps 1-4 are the epilogue (one TMEM lane quarter each), and
+// one of their threads issues the MMAs right after the named barrier that
+// publishes the operand they need, so the serial chain has no hand-off to a
+// separate MMA warp.  Every buffer hand-off is an mbarrier or a named barrier,
+// so the reads of one chunk's buffers are ordered before the next chunk's
+// writes (the sPartialLast race of the TensorRT-LLM K1 page), and every thread
+// that read TMEM has waited for its loads and crossed a tcgen05 fence plus a CTA
+// barrier before TMEM is freed (the dealloc ordering of the TensorRT-LLM
+// MQA-logits page).  All mbarrier waits are bounded; a wait that runs out sets
+// KDA_ERR_TIMEOUT, and every epilogue warp still reaches the named barriers of
+// that chunk before all of them stop together.
 #include "kda_internal.h"
 #include "sm103.cuh"
 
 namespace kda {
 namespace {
 
-constexpr int kStateThreads = 192;
+constexpr int kStateThreads = 160;
 constexpr uint32_t ST_A1 = 0;          // [W ; Q'] 2 x (128 rows x 128 B)
 constexpr uint32_t ST_KT = 32768;      // Kt 128 rows x 128 B
 constexpr uint32_t ST_U = 49152;       // U slab: 64 rows x 32 fp32 (SW128)
 constexpr uint32_t ST_OL = 57344;      // O_loc slab
 constexpr uint32_t ST_EG = 65536;      // e^gam [128] fp32
 constexpr uint32_t kStage = 66560;
-constexpr uint32_t kStageTx = 16384 * 2 + 16384 + 8192 * 2 + 512;
+constexpr uint32_t kStageTx = 32768 + 16384 + 8192 * 2 + 512;
 constexpr uint32_t O_S = 2 * kStage;           // S^T bf16: 2 x (32 rows x 128 B)
 constexpr uint32_t O_VN = O_S + 8192;          // V_new^T bf16: 32 rows x 128 B
 constexpr uint32_t kStateSmem = O_VN + 4096 + 1024;
 constexpr uint32_t TM_D1 = 0, TM_D2 = 32, TM_COLS = 64;
+constexpr uint32_t kBarVn = 1, kBarChunk = 2;  // named barriers (0 is __syncthreads)
 
 // fp32 element (row, col) of a SW128 tile with 128-byte rows (32 floats).
 __device__ __forceinline__ uint32_t sw128_f32(uint32_t row, uint32_t col) {
     return row * 128u + ((((col >> 2) ^ (row & 7u)) << 4) | ((col & 3u) << 2));
 }
 
-struct Maps {
-    CUtensorMap w, qp, kt, u, ol, eg;
-};
-
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
     const bool ok = mbar_wait(bar, parity, abort);
     return __all_sync(0xffffffffu, ok);
 }
 
-__global__ void __launch_bounds__(kStateThreads, 1)
-    state_kernel(const PrefillParams p, const __grid_constant__ Maps maps) {
+__global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-    __shared__ uint64_t full[2], empty[2], p1_done, vn_ready, p2_done, s_ready;
+    __shared__ uint64_t full[2], empty[2], p1_done, p2_done;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
 
@@ -81,9 +80,8 @@ __global__ void __launch_bounds__(kStateThreads, 1)
 
     if (tid == 0) {
         mbar_init(&full[0], 1); mbar_init(&full[1], 1);
-        mbar_init(&empty[0], 5); mbar_init(&empty[1], 5);
+        mbar_init(&empty[0], 2); mbar_init(&empty[1], 2);
         mbar_init(&p1_done, 1); mbar_init(&p2_done, 1);
-        mbar_init(&vn_ready, 64); mbar_init(&s_ready, 128);
         abort_flag = 0;
         fence_mbar_init();
     }
@@ -101,23 +99,20 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     };
 
     if (warp == 0) {
-        // ---------------- TMA producer
+        // ---------------- record fetcher (1-D bulk copies, two stages)
         if (lane == 0) {
             int issued = 0;
             for (int c = 0; c < count; ++c) {
                 const int st = c & 1;
                 if (c >= 2 && !mbar_wait(&empty[st], ((c >> 1) - 1) & 1, abort)) { fail(); break; }
                 uint8_t* sb = sm + st * kStage;
-                const int rec = (first + c) * p.H + h;
+                const uint8_t* rp = p.ws_rec + (size_t)((first + c) * p.H + h) * kRecBytes;
                 mbar_arrive_expect_tx(&full[st], kStageTx);
-                for (int kb = 0; kb < 2; ++kb) {
-                    tma_load_2d(sb + ST_A1 + kb * 16384, &maps.w, kb * 64, rec * 64, &full[st]);
-                    tma_load_2d(sb + ST_A1 + kb * 16384 + 8192, &maps.qp, kb * 64, rec * 64, &full[st]);
-                }
-                tma_load_2d(sb + ST_KT, &maps.kt, 0, rec * 128, &full[st]);
-                tma_load_2d(sb + ST_U, &maps.u, slab * kSlab, rec * 64, &full[st]);
-                tma_load_2d(sb + ST_OL, &maps.ol, slab * kSlab, rec * 64, &full[st]);
-                tma_load_2d(sb + ST_EG, &maps.eg, 0, rec, &full[st]);
+                bulk_load(sb + ST_A1, rp + kRecA1, 32768, &full[st]);
+                bulk_load(sb + ST_KT, rp + kRecKt, 16384, &full[st]);
+                bulk_load(sb + ST_U, rp + kRecU + slab * 8192, 8192, &full[st]);
+                bulk_load(sb + ST_OL, rp + kRecOl + slab * 8192, 8192, &full[st]);
+                bulk_load(sb + ST_EG, rp + kRecEg, 512, &full[st]);
                 issued = c + 1;
             }
             // Never leave the CTA with copies in flight: wait (bounded) for the
@@ -125,33 +120,14 @@ __global__ void __launch_bounds__(kStateThreads, 1)
             for (int c = issued - 2; c < issued; ++c)
                 if (c >= 0) mbar_wait(&full[c & 1], (c >> 1) & 1, nullptr);
         }
-    } else if (warp == 1) {
-        // ---------------- MMA issuer
-        if (lane == 0) {
-            const uint32_t id = idesc_bf16_f32(128, kSlab);
-            const uint32_t sS = smem_u32(sm + O_S), sVn = smem_u32(sm + O_VN);
-            bool ok = mbar_wait(&s_ready, 0, abort);
-            for (int c = 0; ok && c < count; ++c) {
-                const int st = c & 1;
-                const uint32_t sb = smem_u32(sm + st * kStage);
-                if (!(ok = mbar_wait(&full[st], (c >> 1) & 1, abort))) break;
-                tc_fence_after();
-                umma_tile(tb + TM_D1, sb + ST_A1, 16384, sS, kSlab * 128, 128, id, false);
-                umma_commit(&p1_done);
-                if (!(ok = mbar_wait(&vn_ready, c & 1, abort))) break;
-                tc_fence_after();
-                umma_tile(tb + TM_D2, sb + ST_KT, 0, sVn, 0, 64, id, false);
-                umma_commit(&p2_done);
-                umma_commit(&empty[st]);
-                if (!(ok = mbar_wait(&s_ready, (c + 1) & 1, abort))) break;
-            }
-            if (!ok) fail();
-        }
     } else {
-        // ---------------- epilogue: TMEM lane quarter qd, thread row = key / token
+        // ---------------- epilogue (+ MMA issue): TMEM lane quarter qd, thread row = key / token
         const int qd = warp & 3;
         const int row = 32 * qd + lane;
+        const bool issuer = (qd == 0 && lane == 0);
         const uint32_t lane_base = (uint32_t)(32 * qd) << 16;
+        const uint32_t id = idesc_bf16_f32(128, kSlab);
+        const uint32_t sS_addr = smem_u32(sm + O_S), sVn_addr = smem_u32(sm + O_VN);
         float S[kSlab];
         const size_t st_off = (((size_t)n * p.H + h) * kHeadDim + row) * kHeadDim + slab * kSlab;
         if (p.h0) {
@@ -174,31 +150,45 @@ __global__ void __launch_bounds__(kStateThreads, 1)
             tc_fence_before();
         };
         write_state_image();
-        mbar_arrive(&s_ready);
+        named_bar_sync(kBarChunk, 128);
 
-        bool ok = true;
         for (int c = 0; c < count; ++c) {
             const int st = c & 1;
             const uint8_t* sb = sm + st * kStage;
-            if (!(ok = warp_wait(&full[st], (c >> 1) & 1, abort))) break;
-            if (!(ok = warp_wait(&p1_done, c & 1, abort))) break;
+            const uint32_t sb_addr = smem_u32(sb);
+            bool ok = warp_wait(&full[st], (c >> 1) & 1, abort);
+            if (issuer && ok) {
+                tc_fence_after();
+                umma_tile(tb + TM_D1, sb_addr + ST_A1, 16384, sS_addr, kSlab * 128, 128, id, false);
+                umma_commit(&p1_done);
+            }
+            ok = ok && warp_wait(&p1_done, c & 1, abort);
             tc_fence_after();
             float d[kSlab];
-            tmem_ld16(tb + lane_base + TM_D1, *reinterpret_cast<float(*)[16]>(&d[0]));
-            tmem_ld16(tb + lane_base + TM_D1 + 16, *reinterpret_cast<float(*)[16]>(&d[16]));
+            if (ok) {
+                tmem_ld16(tb + lane_base + TM_D1, *reinterpret_cast<float(*)[16]>(&d[0]));
+                tmem_ld16(tb + lane_base + TM_D1 + 16, *reinterpret_cast<float(*)[16]>(&d[16]));
+            }
             if (qd < 2) {
                 // V_new = U - W S for token row `row`; stored transposed (K-major over tokens)
-                const int i = row;
+                if (ok) {
 #pragma unroll
-                for (int j = 0; j < kSlab; ++j) {
-                    const float u = *reinterpret_cast<const float*>(sb + ST_U + sw128_f32(i, j));
-                    *reinterpret_cast<__nv_bfloat16*>(sm + O_VN + sw128_off(j, i)) =
-                        __float2bfloat16_rn(u - d[j]);
+                    for (int j = 0; j < kSlab; ++j) {
+                        const float u = *reinterpret_cast<const float*>(sb + ST_U + sw128_f32(row, j));
+                        *reinterpret_cast<__nv_bfloat16*>(sm + O_VN + sw128_off(j, row)) =
+                            __float2bfloat16_rn(u - d[j]);
+                    }
+                    fence_proxy_async_smem();
                 }
-                fence_proxy_async_smem();
                 tc_fence_before();
-                mbar_arrive(&vn_ready);
-            } else {
+                named_bar_sync(kBarVn, 64);
+                if (issuer && ok && !*abort) {
+                    tc_fence_after();
+                    umma_tile(tb + TM_D2, sb_addr + ST_KT, 0, sVn_addr, 0, 64, id, false);
+                    umma_commit(&p2_done);
+                    umma_commit(&empty[st]);
+                }
+            } else if (ok) {
                 // O = O_loc + Q' S for token row `row - 64`
                 const int i = row - 64;
                 const int t0 = 64 * c;
@@ -218,20 +208,23 @@ __global__ void __launch_bounds__(kStateThreads, 1)
                 }
                 tc_fence_before();
             }
-            if (!(ok = warp_wait(&p2_done, c & 1, abort))) break;
+            ok = ok && warp_wait(&p2_done, c & 1, abort);
             tc_fence_after();
-            tmem_ld16(tb + lane_base + TM_D2, *reinterpret_cast<float(*)[16]>(&d[0]));
-            tmem_ld16(tb + lane_base + TM_D2 + 16, *reinterpret_cast<float(*)[16]>(&d[16]));
-            const float eg = reinterpret_cast<const float*>(sb + ST_EG)[row];
+            if (ok) {
+                tmem_ld16(tb + lane_base + TM_D2, *reinterpret_cast<float(*)[16]>(&d[0]));
+                tmem_ld16(tb + lane_base + TM_D2 + 16, *reinterpret_cast<float(*)[16]>(&d[16]));
+                const float eg = reinterpret_cast<const float*>(sb + ST_EG)[row];
 #pragma unroll
-            for (int j = 0; j < kSlab; ++j) S[j] = fmaf(eg, S[j], d[j]);
-            write_state_image();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[st]);
-            mbar_arrive(&s_ready);
+                for (int j = 0; j < kSlab; ++j) S[j] = fmaf(eg, S[j], d[j]);
+                write_state_image();
+            } else {
+                fail();
+            }
+            named_bar_sync(kBarChunk, 128);
+            if (*abort) break;
+            if (issuer) mbar_arrive(&empty[st]);
         }
-        if (!ok) fail();
-        if (ok && p.hT) {
+        if (!*abort && p.hT) {
             float4* dst = reinterpret_cast<float4*>(p.hT + st_off);
 #pragma unroll
             for (int x = 0; x < kSlab / 4; ++x)
@@ -245,15 +238,13 @@ __global__ void __launch_bounds__(kStateThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_state(const PrefillParams& p, const StateMaps& m, cudaStream_t s) {
+cudaError_t launch_state(const PrefillParams& p, cudaStream_t s) {
     if (p.N == 0 || p.H == 0) return cudaSuccess;
-    Maps maps;
-    maps.w = m.w; maps.qp = m.qp; maps.kt = m.kt; maps.u = m.u; maps.ol = m.ol; maps.eg = m.eg;
     cudaError_t e = cudaFuncSetAttribute(state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kStateSmem);
     if (e != cudaSuccess) return e;
     dim3 grid(kHeadDim / kSlab, p.H, p.N);
-    state_kernel<<<grid, kStateThreads, kStateSmem, s>>>(p, maps);
+    state_kernel<<<grid, kStateThreads, kStateSmem, s>>>(p);
     return cudaGetLastError();
 }
 

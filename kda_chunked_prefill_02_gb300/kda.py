@@ -48,8 +48,7 @@ class VerifyArgs(ctypes.Structure):
 
 
 class WorkspaceLayout(ctypes.Structure):
-    _fields_ = [("w", ctypes.c_size_t), ("qp", ctypes.c_size_t), ("kt", ctypes.c_size_t),
-                ("u", ctypes.c_size_t), ("ol", ctypes.c_size_t), ("eg", ctypes.c_size_t),
+    _fields_ = [("records", ctypes.c_size_t), ("record_bytes", ctypes.c_size_t),
                 ("chunk_offset", ctypes.c_size_t), ("status", ctypes.c_size_t),
                 ("total", ctypes.c_size_t), ("max_chunks", _i64)]
 

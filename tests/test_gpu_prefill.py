@@ -21,6 +21,33 @@ def _bf16(x):
     return torch.from_numpy(np.ascontiguousarray(x)).view(torch.bfloat16).float().numpy()
 
 
+def _unswizzle_bf16(img, rows):
+    """[rows x 64] bf16 block stored with the 128-byte swizzle -> float array."""
+    r = np.arange(rows)[:, None]
+    c = np.arange(64)[None, :]
+    off = r * 128 + (((c // 8) ^ (r % 8)) * 16) + (c % 8) * 2
+    u16 = np.frombuffer(img.tobytes(), dtype=np.uint16)
+    return _bf16(u16[off // 2])
+
+
+def _unswizzle_f32(img, rows):
+    """[rows x 32] fp32 block stored with the 128-byte swizzle."""
+    r = np.arange(rows)[:, None]
+    c = np.arange(32)[None, :]
+    off = r * 128 + (((c // 4) ^ (r % 8)) * 16) + (c % 4) * 4
+    return np.frombuffer(img.tobytes(), dtype=np.float32)[off // 4]
+
+
+def decode_record(raw):
+    """Workspace record (include/kda.h layout) -> dict of W, Qp, Kt, U, Ol, eg."""
+    a1 = np.concatenate([_unswizzle_bf16(raw[0:16384], 128), _unswizzle_bf16(raw[16384:32768], 128)], 1)
+    kt = _unswizzle_bf16(raw[32768:49152], 128)
+    u = np.concatenate([_unswizzle_f32(raw[49152 + 8192 * s:49152 + 8192 * (s + 1)], 64) for s in range(4)], 1)
+    ol = np.concatenate([_unswizzle_f32(raw[81920 + 8192 * s:81920 + 8192 * (s + 1)], 64) for s in range(4)], 1)
+    eg = np.frombuffer(raw[114688:115200].tobytes(), dtype=np.float32)
+    return dict(W=a1[:64], Qp=a1[64:], Kt=kt, U=u, Ol=ol, eg=eg)
+
+
 def test_prep_stage_intermediates():
     """Steps A1-A5 alone: every per-chunk record matches the chunked fp64 form."""
     import kda_chunked_prefill_02_gb300 as K
@@ -29,18 +56,6 @@ def test_prep_stage_intermediates():
     ws, L = K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, scale=0.8, prep_only=True)
     torch.cuda.synchronize()
     raw = ws.cpu().numpy()
-    nrec = L.max_chunks * 2
-
-    def arr(off, dt, shape):
-        n = int(np.prod(shape))
-        return raw[off:off + n * np.dtype(dt).itemsize].view(dt).reshape(shape)
-
-    W = _bf16(arr(L.w, np.uint16, (nrec, 64, 128)))
-    Qp = _bf16(arr(L.qp, np.uint16, (nrec, 64, 128)))
-    Kt = _bf16(arr(L.kt, np.uint16, (nrec, 128, 64)))
-    U = arr(L.u, np.float32, (nrec, 64, 128))
-    Ol = arr(L.ol, np.float32, (nrec, 64, 128))
-    eg = arr(L.eg, np.float32, (nrec, 128))
     q, k, v, g, b = (to_np(t) for t in (inp.q, inp.k, inp.v, inp.g, inp.beta))
     beta = 1.0 / (1.0 + np.exp(-b))
     cps = 4
@@ -50,15 +65,16 @@ def test_prep_stage_intermediates():
             n = t1 - t0
             for h in range(2):
                 r = (bb * cps + c) * 2 + h
+                rec = decode_record(raw[L.records + r * L.record_bytes:L.records + (r + 1) * L.record_bytes])
                 ref = chunked.chunk_step(np.zeros((128, 128)), 0.8 * q[bb, t0:t1, h], k[bb, t0:t1, h],
                                          v[bb, t0:t1, h], g[bb, t0:t1, h], beta[bb, t0:t1, h])
-                for name, got, want in (("W", W[r, :n], ref["W"]), ("U", U[r, :n], ref["U"]),
-                                        ("Qp", Qp[r, :n], ref["Qp"]), ("Ol", Ol[r, :n], ref["Oloc"]),
-                                        ("Kt", Kt[r, :, :n], ref["Kh"].T)):
+                for name, got, want in (("W", rec["W"][:n], ref["W"]), ("U", rec["U"][:n], ref["U"]),
+                                        ("Qp", rec["Qp"][:n], ref["Qp"]), ("Ol", rec["Ol"][:n], ref["Oloc"]),
+                                        ("Kt", rec["Kt"][:, :n], ref["Kh"].T)):
                     assert rel_fro(got, want) < 1e-2, (name, bb, c, h, rel_fro(got, want))
-                np.testing.assert_allclose(eg[r], np.exp(ref["gam"]), rtol=1e-5, atol=1e-30)
-                for name, tail in (("W", W[r, n:]), ("U", U[r, n:]), ("Qp", Qp[r, n:]),
-                                   ("Ol", Ol[r, n:]), ("Kt", Kt[r, :, n:])):
+                np.testing.assert_allclose(rec["eg"], np.exp(ref["gam"]), rtol=1e-5, atol=1e-30)
+                for name, tail in (("W", rec["W"][n:]), ("U", rec["U"][n:]), ("Qp", rec["Qp"][n:]),
+                                   ("Ol", rec["Ol"][n:]), ("Kt", rec["Kt"][:, n:])):
                     assert not np.any(tail), name
 
 
