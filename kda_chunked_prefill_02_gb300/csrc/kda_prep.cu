@@ -85,6 +85,32 @@ __device__ __forceinline__ uint32_t yoff_row(int I, int J, int l) {
     return 8 * I * (I - 1) + 16 * J + l;
 }
 
+// Warp-level m16n8k8 tf32 MMA with fp32 accumulation (used for the small block
+// products of the UT solve; fragment layouts of the PTX m16n8k8 tf32 shape).
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+// d (16 x 8 tile) = P (16 x kdim, row pitch pp) * Q (kdim x 8, row pitch pq),
+// fp32 matrices in shared memory.  Thread (g = lane/4, t = lane%4) gets
+// d0 (g, 2t), d1 (g, 2t+1), d2 (g+8, 2t), d3 (g+8, 2t+1).
+__device__ __forceinline__ void warp_mma_16x8(const float* P, int pp, const float* Q, int pq,
+                                              int kdim, float (&d)[4], int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    d[0] = d[1] = d[2] = d[3] = 0.f;
+    for (int k0 = 0; k0 < kdim; k0 += 8) {
+        const uint32_t a0 = to_tf32(P[g * pp + k0 + t]), a1 = to_tf32(P[(g + 8) * pp + k0 + t]);
+        const uint32_t a2 = to_tf32(P[g * pp + k0 + t + 4]), a3 = to_tf32(P[(g + 8) * pp + k0 + t + 4]);
+        const uint32_t b0 = to_tf32(Q[(k0 + t) * pq + g]), b1 = to_tf32(Q[(k0 + t + 4) * pq + g]);
+        asm volatile(
+            "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+            "{%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
+}
+
 // Issues the TMA loads of one record's q, k, v, g tiles.
 __device__ __forceinline__ void load_inputs(uint8_t* sm, const PrepMaps& m, const ChunkInfo& ci,
                                             int h, uint64_t* bar) {
@@ -131,6 +157,13 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     int rec = blockIdx.x;
     ChunkInfo ci = chunk_info(p, rec / p.H);
     if (tid == 0 && ci.len > 0) load_inputs(sm, maps, ci, rec % p.H, &bar_in);
+    // beta of the current record, loaded one record ahead (raw value; the
+    // sigmoid is applied when it is stored)
+    auto load_beta = [&](const ChunkInfo& c, int hh) -> float {
+        return (tid < c.len) ? __ldg(p.beta + c.b * p.bs[0] + ((int64_t)c.t0 + tid) * p.bs[1] + hh * p.bs[2])
+                             : 0.f;
+    };
+    float bcur = load_beta(ci, rec % p.H);
     bool ok = true;
     int pend_parity = ci.len > 0 ? 0 : -1;  // parity of an input load still in flight
     for (uint32_t it = 0; ci.len > 0; ++it) {
@@ -138,15 +171,14 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         const int len = ci.len;
         const int rec_next = rec + gridDim.x;
         const ChunkInfo cn = rec_next < nrec ? chunk_info(p, rec_next / p.H) : ChunkInfo{0, 0, 0, 0, 0};
-        float bval = 0.f;
-        if (tid < len) {
-            bval = __ldg(p.beta + ci.b * p.bs[0] + ((int64_t)ci.t0 + tid) * p.bs[1] + h * p.bs[2]);
-            if (p.beta_is_logit) bval = 1.0f / (1.0f + __expf(-bval));
-        }
         ok = __syncthreads_and(mbar_wait(&bar_in, it & 1, nullptr));
         if (!ok) break;
         pend_parity = -1;
-        if (tid < 64) reinterpret_cast<float*>(sm + O_BETA)[tid] = bval;
+        if (tid < 64) {
+            float bval = bcur;
+            if (tid < len && p.beta_is_logit) bval = 1.0f / (1.0f + __expf(-bval));
+            reinterpret_cast<float*>(sm + O_BETA)[tid] = tid < len ? bval : 0.f;
+        }
 
         // ---- E1: p = exp(g) (masked past the chunk length), block gate totals,
         // and the suffix products z (exact) and zc (floored gate) by a backward pass.
@@ -265,6 +297,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         if (tid == 0 && cn.len > 0) {
             load_inputs(sm, maps, cn, rec_next % p.H, &bar_in);
         }
+        if (cn.len > 0) bcur = load_beta(cn, rec_next % p.H);
         if (cn.len > 0) pend_parity = (int)((it + 1) & 1);
 
         // ---- MMA A: D = R [Yoff ; Yd]^T, N = 160 (off-diagonal and diagonal blocks)
@@ -347,68 +380,46 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             for (int r = 0; r < 16; ++r) sT[(s0 + r) * kPA + s0 + l] = x[r];
         }
         __syncthreads();
-        {
-            float acc[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {  // X = A_10 T_00 (both 32-blocks)
-                const int e = tid + 256 * u, pb = 32 * (e >> 8), r = (e >> 4) & 15, c = e & 15;
-                acc[u] = 0.f;
-#pragma unroll
-                for (int m = 0; m < 16; ++m)
-                    acc[u] = fmaf(sA[(pb + 16 + r) * kPA + pb + m], sT[(pb + m) * kPA + pb + c], acc[u]);
-            }
-#pragma unroll
-            for (int u = 0; u < 2; ++u) sX[tid + 256 * u] = acc[u];
+        // Off-diagonal blocks with warp-level tf32 tensor-core products
+        // (fp32 accumulation; the result is rounded to bf16 for MMA C anyway).
+        const int g4 = lane >> 2, t4 = lane & 3;
+        if (warp < 4) {  // X_p = A_10 T_00 of 32-block p (two 16 x 8 tiles each)
+            const int pb = 32 * (warp >> 1), c0 = 8 * (warp & 1);
+            float d[4];
+            warp_mma_16x8(sA + (pb + 16) * kPA + pb, kPA, sT + pb * kPA + pb + c0, kPA, 16, d, lane);
+            float* x = sX + (warp >> 1) * 256;
+            x[g4 * 16 + c0 + 2 * t4] = d[0]; x[g4 * 16 + c0 + 2 * t4 + 1] = d[1];
+            x[(g4 + 8) * 16 + c0 + 2 * t4] = d[2]; x[(g4 + 8) * 16 + c0 + 2 * t4 + 1] = d[3];
         }
         __syncthreads();
-        {
-            float acc[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {  // T_10 = -T_11 X
-                const int e = tid + 256 * u, pb = 32 * (e >> 8), r = (e >> 4) & 15, c = e & 15;
-                acc[u] = 0.f;
-#pragma unroll
-                for (int m = 0; m < 16; ++m)
-                    acc[u] = fmaf(sT[(pb + 16 + r) * kPA + pb + 16 + m], sX[(e & 256) + m * 16 + c], acc[u]);
-            }
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int e = tid + 256 * u, pb = 32 * (e >> 8), r = (e >> 4) & 15, c = e & 15;
-                sT[(pb + 16 + r) * kPA + pb + c] = -acc[u];
-                sT[(pb + r) * kPA + pb + 16 + c] = 0.f;  // block above the diagonal
-            }
+        if (warp < 4) {  // T_10 = -T_11 X_p; the block above the diagonal is zero
+            const int pb = 32 * (warp >> 1), c0 = 8 * (warp & 1);
+            float d[4];
+            warp_mma_16x8(sT + (pb + 16) * kPA + pb + 16, kPA, sX + (warp >> 1) * 256 + c0, 16, 16, d, lane);
+            float* t10 = sT + (pb + 16) * kPA + pb + c0;
+            t10[g4 * kPA + 2 * t4] = -d[0]; t10[g4 * kPA + 2 * t4 + 1] = -d[1];
+            t10[(g4 + 8) * kPA + 2 * t4] = -d[2]; t10[(g4 + 8) * kPA + 2 * t4 + 1] = -d[3];
+            float* t01 = sT + pb * kPA + pb + 16 + c0;
+            t01[g4 * kPA + 2 * t4] = 0.f; t01[g4 * kPA + 2 * t4 + 1] = 0.f;
+            t01[(g4 + 8) * kPA + 2 * t4] = 0.f; t01[(g4 + 8) * kPA + 2 * t4 + 1] = 0.f;
         }
         __syncthreads();
-        {
-            float acc[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {  // X = A[32:,:32] T[:32,:32]
-                const int e = tid + 256 * u, r = e >> 5, c = e & 31;
-                acc[u] = 0.f;
-#pragma unroll
-                for (int m = 0; m < 32; ++m) acc[u] = fmaf(sA[(32 + r) * kPA + m], sT[m * kPA + c], acc[u]);
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int e = tid + 256 * u;
-                sX[(e >> 5) * 33 + (e & 31)] = acc[u];
-            }
+        {  // X = A[32:,:32] T[:32,:32]: eight 16 x 8 tiles, one per warp
+            const int r0 = 16 * (warp >> 2), c0 = 8 * (warp & 3);
+            float d[4];
+            warp_mma_16x8(sA + (32 + r0) * kPA, kPA, sT + c0, kPA, 32, d, lane);
+            float* x = sX + r0 * 33 + c0;
+            x[g4 * 33 + 2 * t4] = d[0]; x[g4 * 33 + 2 * t4 + 1] = d[1];
+            x[(g4 + 8) * 33 + 2 * t4] = d[2]; x[(g4 + 8) * 33 + 2 * t4 + 1] = d[3];
         }
         __syncthreads();
-        {
-            float acc[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {  // T[32:,:32] = -T[32:,32:] X
-                const int e = tid + 256 * u, r = e >> 5, c = e & 31;
-                acc[u] = 0.f;
-#pragma unroll
-                for (int m = 0; m < 32; ++m) acc[u] = fmaf(sT[(32 + r) * kPA + 32 + m], sX[m * 33 + c], acc[u]);
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int e = tid + 256 * u;
-                sT[(32 + (e >> 5)) * kPA + (e & 31)] = -acc[u];
-            }
+        {  // T[32:,:32] = -T[32:,32:] X
+            const int r0 = 16 * (warp >> 2), c0 = 8 * (warp & 3);
+            float d[4];
+            warp_mma_16x8(sT + (32 + r0) * kPA + 32, kPA, sX + c0, 33, 32, d, lane);
+            float* t = sT + (32 + r0) * kPA + c0;
+            t[g4 * kPA + 2 * t4] = -d[0]; t[g4 * kPA + 2 * t4 + 1] = -d[1];
+            t[(g4 + 8) * kPA + 2 * t4] = -d[2]; t[(g4 + 8) * kPA + 2 * t4 + 1] = -d[3];
         }
         __syncthreads();
         // T' = T Diag(beta): rows 0..63 of the TT operand (K-major over j) and

@@ -38,16 +38,16 @@ constexpr uint32_t ST_OL = 57344;      // O_loc slab
 constexpr uint32_t ST_EG = 65536;      // e^gam [128] fp32
 constexpr uint32_t kStage = 66560;
 constexpr uint32_t kStageTx = 32768 + 16384 + 8192 * 2 + 512;
-constexpr uint32_t O_S = 2 * kStage;           // S^T bf16: 2 x (32 rows x 128 B)
-constexpr uint32_t O_VN = O_S + 8192;          // V_new^T bf16: 32 rows x 128 B
-constexpr uint32_t kStateSmem = O_VN + 4096 + 1024;
+constexpr int kStages = 3;
+// B operands of P1 and P2, MN-major with the 128-byte swizzle: one 128-byte
+// row per K index (key for S, token for V_new) holding the slab's 32 columns,
+// 8-row groups 1024 B apart, so each thread stores its own row.
+constexpr uint32_t O_S = kStages * kStage;     // S bf16: 128 key rows (16 KB)
+constexpr uint32_t O_VN = O_S + 16384;         // V_new bf16: 64 token rows (8 KB)
+constexpr uint32_t kStateSmem = O_VN + 8192 + 1024;
+constexpr uint32_t kRowGroup = 1024;
 constexpr uint32_t TM_D1 = 0, TM_D2 = 32, TM_COLS = 64;
 constexpr uint32_t kBarVn = 1, kBarChunk = 2;  // named barriers (0 is __syncthreads)
-
-// fp32 element (row, col) of a SW128 tile with 128-byte rows (32 floats).
-__device__ __forceinline__ uint32_t sw128_f32(uint32_t row, uint32_t col) {
-    return row * 128u + ((((col >> 2) ^ (row & 7u)) << 4) | ((col & 3u) << 2));
-}
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
     const bool ok = mbar_wait(bar, parity, abort);
@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-    __shared__ uint64_t full[2], empty[2], p1_done, p2_done;
+    __shared__ uint64_t full[kStages], empty[kStages], p1_done, p2_done;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
 
@@ -79,8 +79,10 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
     }
 
     if (tid == 0) {
-        mbar_init(&full[0], 1); mbar_init(&full[1], 1);
-        mbar_init(&empty[0], 2); mbar_init(&empty[1], 2);
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 2);
+        }
         mbar_init(&p1_done, 1); mbar_init(&p2_done, 1);
         abort_flag = 0;
         fence_mbar_init();
@@ -99,12 +101,12 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
     };
 
     if (warp == 0) {
-        // ---------------- record fetcher (1-D bulk copies, two stages)
+        // ---------------- record fetcher (1-D bulk copies, kStages stages)
         if (lane == 0) {
             int issued = 0;
             for (int c = 0; c < count; ++c) {
-                const int st = c & 1;
-                if (c >= 2 && !mbar_wait(&empty[st], ((c >> 1) - 1) & 1, abort)) { fail(); break; }
+                const int st = c % kStages;
+                if (c >= kStages && !mbar_wait(&empty[st], ((c / kStages) - 1) & 1, abort)) { fail(); break; }
                 uint8_t* sb = sm + st * kStage;
                 const uint8_t* rp = p.ws_rec + (size_t)((first + c) * p.H + h) * kRecBytes;
                 mbar_arrive_expect_tx(&full[st], kStageTx);
@@ -117,8 +119,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
             }
             // Never leave the CTA with copies in flight: wait (bounded) for the
             // last stages issued.  In a normal run these phases completed long ago.
-            for (int c = issued - 2; c < issued; ++c)
-                if (c >= 0) mbar_wait(&full[c & 1], (c >> 1) & 1, nullptr);
+            for (int c = issued - kStages; c < issued; ++c)
+                if (c >= 0) mbar_wait(&full[c % kStages], (c / kStages) & 1, nullptr);
         }
     } else {
         // ---------------- epilogue (+ MMA issue): TMEM lane quarter qd, thread row = key / token
@@ -126,7 +128,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
         const int row = 32 * qd + lane;
         const bool issuer = (qd == 0 && lane == 0);
         const uint32_t lane_base = (uint32_t)(32 * qd) << 16;
-        const uint32_t id = idesc_bf16_f32(128, kSlab);
+        const uint32_t id = idesc_bf16_f32_bmn(128, kSlab);
         const uint32_t sS_addr = smem_u32(sm + O_S), sVn_addr = smem_u32(sm + O_VN);
         float S[kSlab];
         const size_t st_off = (((size_t)n * p.H + h) * kHeadDim + row) * kHeadDim + slab * kSlab;
@@ -141,11 +143,17 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
 #pragma unroll
             for (int j = 0; j < kSlab; ++j) S[j] = 0.f;
         }
-        uint8_t* sS = sm + O_S + (row >> 6) * (kSlab * 128);
-        auto write_state_image = [&]() {
+        // Row `row` of an MN-major operand: 32 bf16 in four swizzled 16-byte chunks.
+        auto store_row = [&](uint8_t* base, int r, const float* x) {
+            uint8_t* rp = base + (r >> 3) * kRowGroup + (r & 7) * 128;
 #pragma unroll
-            for (int j = 0; j < kSlab; ++j)
-                *reinterpret_cast<__nv_bfloat16*>(sS + sw128_off(j, row & 63)) = __float2bfloat16_rn(S[j]);
+            for (int ch = 0; ch < 4; ++ch)
+                *reinterpret_cast<uint4*>(rp + ((ch ^ (r & 7)) << 4)) =
+                    make_uint4(pack_bf16x2(x[8 * ch], x[8 * ch + 1]), pack_bf16x2(x[8 * ch + 2], x[8 * ch + 3]),
+                               pack_bf16x2(x[8 * ch + 4], x[8 * ch + 5]), pack_bf16x2(x[8 * ch + 6], x[8 * ch + 7]));
+        };
+        auto write_state_image = [&]() {
+            store_row(sm + O_S, row, S);
             fence_proxy_async_smem();
             tc_fence_before();
         };
@@ -153,13 +161,16 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
         named_bar_sync(kBarChunk, 128);
 
         for (int c = 0; c < count; ++c) {
-            const int st = c & 1;
+            const int st = c % kStages;
             const uint8_t* sb = sm + st * kStage;
             const uint32_t sb_addr = smem_u32(sb);
-            bool ok = warp_wait(&full[st], (c >> 1) & 1, abort);
+            bool ok = warp_wait(&full[st], (c / kStages) & 1, abort);
             if (issuer && ok) {
                 tc_fence_after();
-                umma_tile(tb + TM_D1, sb_addr + ST_A1, 16384, sS_addr, kSlab * 128, 128, id, false);
+                for (uint32_t k = 0; k < 8; ++k)  // K = 128 keys: A K-major, B (S) MN-major
+                    umma_bf16(tb + TM_D1, sdesc_kmajor_sw128(sb_addr + ST_A1 + (k >> 2) * 16384 + (k & 3) * 32),
+                              sdesc_mnmajor_sw128(sS_addr + k * 2 * kRowGroup, kRowGroup, kRowGroup), id,
+                              k > 0 ? 1u : 0u);
                 umma_commit(&p1_done);
             }
             ok = ok && warp_wait(&p1_done, c & 1, abort);
@@ -172,19 +183,26 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
             if (qd < 2) {
                 // V_new = U - W S for token row `row`; stored transposed (K-major over tokens)
                 if (ok) {
+                    float vn[kSlab];
 #pragma unroll
-                    for (int j = 0; j < kSlab; ++j) {
-                        const float u = *reinterpret_cast<const float*>(sb + ST_U + sw128_f32(row, j));
-                        *reinterpret_cast<__nv_bfloat16*>(sm + O_VN + sw128_off(j, row)) =
-                            __float2bfloat16_rn(u - d[j]);
+                    for (int ch = 0; ch < kSlab / 4; ++ch) {
+                        const float4 u = *reinterpret_cast<const float4*>(sb + ST_U + row * 128 + ((ch ^ (row & 7)) << 4));
+                        vn[4 * ch] = u.x - d[4 * ch];
+                        vn[4 * ch + 1] = u.y - d[4 * ch + 1];
+                        vn[4 * ch + 2] = u.z - d[4 * ch + 2];
+                        vn[4 * ch + 3] = u.w - d[4 * ch + 3];
                     }
+                    store_row(sm + O_VN, row, vn);
                     fence_proxy_async_smem();
                 }
                 tc_fence_before();
                 named_bar_sync(kBarVn, 64);
                 if (issuer && ok && !*abort) {
                     tc_fence_after();
-                    umma_tile(tb + TM_D2, sb_addr + ST_KT, 0, sVn_addr, 0, 64, id, false);
+                    for (uint32_t k = 0; k < 4; ++k)  // K = 64 tokens: A K-major, B (V_new) MN-major
+                        umma_bf16(tb + TM_D2, sdesc_kmajor_sw128(sb_addr + ST_KT + k * 32),
+                                  sdesc_mnmajor_sw128(sVn_addr + k * 2 * kRowGroup, kRowGroup, kRowGroup), id,
+                                  k > 0 ? 1u : 0u);
                     umma_commit(&p2_done);
                     umma_commit(&empty[st]);
                 }
@@ -195,10 +213,10 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
                 if (t0 + i < seq_len) {
                     uint32_t o[kSlab / 2];
 #pragma unroll
-                    for (int j = 0; j < kSlab; j += 2) {
-                        const float a = *reinterpret_cast<const float*>(sb + ST_OL + sw128_f32(i, j)) + d[j];
-                        const float e = *reinterpret_cast<const float*>(sb + ST_OL + sw128_f32(i, j + 1)) + d[j + 1];
-                        o[j >> 1] = pack_bf16x2(a, e);
+                    for (int ch = 0; ch < kSlab / 4; ++ch) {
+                        const float4 ol = *reinterpret_cast<const float4*>(sb + ST_OL + i * 128 + ((ch ^ (i & 7)) << 4));
+                        o[2 * ch] = pack_bf16x2(ol.x + d[4 * ch], ol.y + d[4 * ch + 1]);
+                        o[2 * ch + 1] = pack_bf16x2(ol.z + d[4 * ch + 2], ol.w + d[4 * ch + 3]);
                     }
                     const int64_t t = (int64_t)tbase + t0 + i;
                     uint4* dst = reinterpret_cast<uint4*>(p.out + b * p.os[0] + t * p.os[1] + h * p.os[2] + slab * kSlab);

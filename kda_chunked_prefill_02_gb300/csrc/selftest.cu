@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(128)
     __shared__ uint64_t bar_mma;
     __shared__ uint32_t tmem_base;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t sbo = (uint32_t)(N / 64) * 1024u;
+    const uint32_t sbo = (uint32_t)(N >= 64 ? N / 64 : 1) * 1024u;
     if (tid == 0) {
         mbar_init(&bar_mma, 1);
         fence_mbar_init();
@@ -148,8 +148,8 @@ __global__ void __launch_bounds__(128)
 
 extern "C" int kda_selftest_umma_mn(const void* A, const void* B, float* D, int N, int mode,
                                     int* status, void* stream) {
-    if (N < 64 || N > 256 || (N % 64) != 0) return 1;
-    const size_t smem = 1024 + 32768 + 2 * (size_t)N * 128;
+    if (!(N == 32 || (N >= 64 && N <= 256 && N % 64 == 0))) return 1;
+    const size_t smem = 1024 + 32768 + (N >= 64 ? 2 * (size_t)N * 128 : 16384);
     if (cudaFuncSetAttribute(umma_mn_selftest_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
         return 3;

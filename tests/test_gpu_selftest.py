@@ -36,10 +36,11 @@ def test_umma_tile(selftest, N, use_tma):
     torch.testing.assert_close(D, ref, atol=2e-3, rtol=1e-4)
 
 
-@pytest.mark.parametrize("N", [64, 128, 256])
+@pytest.mark.parametrize("N", [32, 64, 128, 256])
 def test_umma_tile_b_mn_major(selftest, N):
     """B stored MN-major (128-byte swizzle, atoms along N 1024 B apart, 8-row K
-    groups N/64 KB apart): the layout the prep kernel uses for [K e^Gam | V]."""
+    groups max(N/64, 1) KB apart): the layout of the prep kernel's [K e^Gam | V]
+    (N = 256) and of the state pass's S and V_new operands (N = 32)."""
     f = selftest.kda_selftest_umma_mn
     f.restype = ctypes.c_int
     f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 2 + [ctypes.c_void_p] * 2
