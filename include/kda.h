@@ -165,10 +165,11 @@ kda_status kda_prefill_state(const kda_prefill_args* args, void* stream);
  *                     128 rows x 128 B; rows 0-63 W = T Diag(beta)(K e^Gam),
  *                     rows 64-127 Q' = scale*Q e^Gam - Aqk W
  *   [32768, 49152)    Kt bf16: 128 key rows x 64 tokens, (K e^{gam - Gam})^T
- *   [49152, 81920)    U = T Diag(beta) V fp32: value slabs 0-3 (32 columns
- *                     each), each 64 rows x 128 B, same swizzle on fp32 rows
- *   [81920, 114688)   O_loc = Aqk U fp32, same layout
- *   [114688, 115200)  exp(gam) fp32 [128], gam = chunk total of g
+ *   [49152, 65536)    U = T Diag(beta) V bf16: value slabs 0-3 (32 columns
+ *                     each, 4 KB), 64-byte rows, 16-byte chunk c of row x at
+ *                     x*64 + ((c ^ ((x / 2) mod 4)) * 16)
+ *   [65536, 81920)    O_loc = Aqk U bf16, same layout
+ *   [81920, 82432)    exp(gam) fp32 [128], gam = chunk total of g
  * Rows past a tail chunk's length are zero.  chunk_offset: int32 [N+1].
  */
 typedef struct kda_workspace_layout {

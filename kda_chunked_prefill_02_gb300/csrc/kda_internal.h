@@ -16,15 +16,22 @@ constexpr float kGateFloor = -5.4f;   // per-token gate floor inside 16-token bl
 
 // Workspace record per (chunk, head): shared-memory images, written by the prep
 // kernel with bulk copies and read back by the state pass with bulk copies.
-// bf16 images use the 128-byte swizzle of K-major tcgen05 operands (16-byte
-// chunk c of 128-byte row r at r*128 + ((c ^ (r & 7)) << 4)); fp32 slabs use
-// the same swizzle on 128-byte rows of 32 floats.
+// [W ; Q'] and Kt use the 128-byte swizzle of K-major tcgen05 operands (16-byte
+// chunk c of 128-byte row r at r*128 + ((c ^ (r & 7)) << 4)).  U and O_loc are
+// bf16 value slabs of 32 columns, 64-byte rows, chunk c of row r at
+// r*64 + ((c ^ ((r >> 1) & 3)) << 4) (conflict-free row reads).
 constexpr uint32_t kRecA1 = 0;          // [W ; Q'] bf16: 2 column blocks x 128 rows x 128 B
 constexpr uint32_t kRecKt = 32768;      // Kt bf16: 128 key rows x 64 tokens
-constexpr uint32_t kRecU = 49152;       // U fp32: 4 value slabs x 64 rows x 32 floats
-constexpr uint32_t kRecOl = 81920;      // O_loc fp32: 4 value slabs x 64 rows x 32 floats
-constexpr uint32_t kRecEg = 114688;     // e^gam fp32 [128]
-constexpr uint32_t kRecBytes = 115200;
+constexpr uint32_t kRecU = 49152;       // U bf16: 4 value slabs x 64 rows x 32
+constexpr uint32_t kRecOl = 65536;      // O_loc bf16: 4 value slabs x 64 rows x 32
+constexpr uint32_t kRecEg = 81920;      // e^gam fp32 [128]
+constexpr uint32_t kRecBytes = 82432;
+constexpr uint32_t kSlabImg = 4096;     // bytes of one U / O_loc slab image
+
+// Byte offset of 16-byte chunk c of row r in a U / O_loc slab image.
+__host__ __device__ __forceinline__ uint32_t slab_chunk_off(uint32_t r, uint32_t c) {
+    return r * 64u + ((c ^ ((r >> 1) & 3u)) << 4);
+}
 
 struct PrefillParams {
     const __nv_bfloat16* q;

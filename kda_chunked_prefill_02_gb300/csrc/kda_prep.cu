@@ -67,8 +67,8 @@ constexpr uint32_t O_TT = 128000;     // A operand [T' ; Aqk T']: 128 rows x 128
 constexpr uint32_t O_TTR = 144384;    // B operand T'^T: 64 rows x 128 B
 // Staging of the record images written by the last epilogue (over R, Y, KV).
 constexpr uint32_t O_SA1 = 81920;     // [W ; Q'] image, 32 KB
-constexpr uint32_t O_SU = 114688;     // U image, 32 KB
-constexpr uint32_t O_SOL = 147456;    // O_loc image, 32 KB
+constexpr uint32_t O_SU = 114688;     // U image, 16 KB
+constexpr uint32_t O_SOL = 131072;    // O_loc image, 16 KB
 
 // TMEM columns.
 constexpr uint32_t TM_A = 0, TM_DIAG = 96, TM_B = 192, TM_C = 0, TM_COLS = 256;
@@ -504,12 +504,13 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                     *reinterpret_cast<uint4*>(img + sw128_off(r, col & 63)) = make_uint4(w[0], w[1], w[2], w[3]);
                     *reinterpret_cast<uint4*>(img + sw128_off(r, (col & 63) + 8)) = make_uint4(w[4], w[5], w[6], w[7]);
                 } else {
-                    uint8_t* img = sm + (top ? O_SU : O_SOL) + (col >> 5) * 8192;
-                    const int cs = col & 31;
+                    uint8_t* img = sm + (top ? O_SU : O_SOL) + (col >> 5) * kSlabImg;
+                    const int c8 = (col & 31) >> 3;
+                    uint32_t w[8];
 #pragma unroll
-                    for (int x = 0; x < 4; ++x)
-                        *reinterpret_cast<float4*>(img + i * 128 + ((((cs >> 2) + x) ^ (i & 7)) << 4)) =
-                            make_float4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
+                    for (int x = 0; x < 8; ++x) w[x] = pack_bf16x2(v[2 * x], v[2 * x + 1]);
+                    *reinterpret_cast<uint4*>(img + slab_chunk_off(i, c8)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<uint4*>(img + slab_chunk_off(i, c8 + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
                 }
             }
         }
@@ -519,8 +520,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         if (tid == 0) {
             uint8_t* rp = p.ws_rec + (size_t)rec * kRecBytes;
             bulk_store(rp + kRecA1, sm + O_SA1, 32768);
-            bulk_store(rp + kRecU, sm + O_SU, 32768);
-            bulk_store(rp + kRecOl, sm + O_SOL, 32768);
+            bulk_store(rp + kRecU, sm + O_SU, 4 * kSlabImg);
+            bulk_store(rp + kRecOl, sm + O_SOL, 4 * kSlabImg);
             bulk_commit();
         }
         tc_fence_before();

@@ -33,11 +33,11 @@ namespace {
 constexpr int kStateThreads = 160;
 constexpr uint32_t ST_A1 = 0;          // [W ; Q'] 2 x (128 rows x 128 B)
 constexpr uint32_t ST_KT = 32768;      // Kt 128 rows x 128 B
-constexpr uint32_t ST_U = 49152;       // U slab: 64 rows x 32 fp32 (SW128)
-constexpr uint32_t ST_OL = 57344;      // O_loc slab
-constexpr uint32_t ST_EG = 65536;      // e^gam [128] fp32
-constexpr uint32_t kStage = 66560;
-constexpr uint32_t kStageTx = 32768 + 16384 + 8192 * 2 + 512;
+constexpr uint32_t ST_U = 49152;       // U slab: 64 rows x 32 bf16
+constexpr uint32_t ST_OL = 53248;      // O_loc slab
+constexpr uint32_t ST_EG = 57344;      // e^gam [128] fp32
+constexpr uint32_t kStage = 58368;
+constexpr uint32_t kStageTx = 32768 + 16384 + kSlabImg * 2 + 512;
 constexpr int kStages = 3;
 // B operands of P1 and P2, MN-major with the 128-byte swizzle: one 128-byte
 // row per K index (key for S, token for V_new) holding the slab's 32 columns,
@@ -112,8 +112,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
                 mbar_arrive_expect_tx(&full[st], kStageTx);
                 bulk_load(sb + ST_A1, rp + kRecA1, 32768, &full[st]);
                 bulk_load(sb + ST_KT, rp + kRecKt, 16384, &full[st]);
-                bulk_load(sb + ST_U, rp + kRecU + slab * 8192, 8192, &full[st]);
-                bulk_load(sb + ST_OL, rp + kRecOl + slab * 8192, 8192, &full[st]);
+                bulk_load(sb + ST_U, rp + kRecU + slab * kSlabImg, kSlabImg, &full[st]);
+                bulk_load(sb + ST_OL, rp + kRecOl + slab * kSlabImg, kSlabImg, &full[st]);
                 bulk_load(sb + ST_EG, rp + kRecEg, 512, &full[st]);
                 issued = c + 1;
             }
@@ -185,12 +185,15 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
                 if (ok) {
                     float vn[kSlab];
 #pragma unroll
-                    for (int ch = 0; ch < kSlab / 4; ++ch) {
-                        const float4 u = *reinterpret_cast<const float4*>(sb + ST_U + row * 128 + ((ch ^ (row & 7)) << 4));
-                        vn[4 * ch] = u.x - d[4 * ch];
-                        vn[4 * ch + 1] = u.y - d[4 * ch + 1];
-                        vn[4 * ch + 2] = u.z - d[4 * ch + 2];
-                        vn[4 * ch + 3] = u.w - d[4 * ch + 3];
+                    for (int ch = 0; ch < 4; ++ch) {
+                        const uint4 u = *reinterpret_cast<const uint4*>(sb + ST_U + slab_chunk_off(row, ch));
+                        const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                        for (int x = 0; x < 4; ++x) {
+                            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&uw[x]));
+                            vn[8 * ch + 2 * x] = f.x - d[8 * ch + 2 * x];
+                            vn[8 * ch + 2 * x + 1] = f.y - d[8 * ch + 2 * x + 1];
+                        }
                     }
                     store_row(sm + O_VN, row, vn);
                     fence_proxy_async_smem();
@@ -213,10 +216,14 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
                 if (t0 + i < seq_len) {
                     uint32_t o[kSlab / 2];
 #pragma unroll
-                    for (int ch = 0; ch < kSlab / 4; ++ch) {
-                        const float4 ol = *reinterpret_cast<const float4*>(sb + ST_OL + i * 128 + ((ch ^ (i & 7)) << 4));
-                        o[2 * ch] = pack_bf16x2(ol.x + d[4 * ch], ol.y + d[4 * ch + 1]);
-                        o[2 * ch + 1] = pack_bf16x2(ol.z + d[4 * ch + 2], ol.w + d[4 * ch + 3]);
+                    for (int ch = 0; ch < 4; ++ch) {
+                        const uint4 ol = *reinterpret_cast<const uint4*>(sb + ST_OL + slab_chunk_off(i, ch));
+                        const uint32_t ow[4] = {ol.x, ol.y, ol.z, ol.w};
+#pragma unroll
+                        for (int x = 0; x < 4; ++x) {
+                            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[x]));
+                            o[4 * ch + x] = pack_bf16x2(f.x + d[8 * ch + 2 * x], f.y + d[8 * ch + 2 * x + 1]);
+                        }
                     }
                     const int64_t t = (int64_t)tbase + t0 + i;
                     uint4* dst = reinterpret_cast<uint4*>(p.out + b * p.os[0] + t * p.os[1] + h * p.os[2] + slab * kSlab);

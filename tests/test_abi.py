@@ -82,7 +82,7 @@ def test_workspace_plan(K):
     assert L.total == lib.kda_prefill_workspace_size(ctypes.byref(a))
     offs = [L.records, L.chunk_offset, L.status]
     assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
-    assert L.record_bytes == 115200 and L.chunk_offset >= L.records + 8 * L.record_bytes
+    assert L.record_bytes == 82432 and L.chunk_offset >= L.records + 8 * L.record_bytes
     # varlen upper bound on chunks: floor(T / 64) + N
     a2 = _args(K, cu_seqlens=ctypes.c_void_p(1 << 12), num_seqs=3, seqlen=130)
     assert lib.kda_prefill_workspace_layout(ctypes.byref(a2), ctypes.byref(L)) == 0

@@ -30,21 +30,23 @@ def _unswizzle_bf16(img, rows):
     return _bf16(u16[off // 2])
 
 
-def _unswizzle_f32(img, rows):
-    """[rows x 32] fp32 block stored with the 128-byte swizzle."""
-    r = np.arange(rows)[:, None]
+def _unswizzle_slab(img):
+    """bf16 value slab: 64 rows x 32, 64-byte rows, chunk c of row r at
+    r*64 + ((c ^ ((r // 2) % 4)) * 16)."""
+    r = np.arange(64)[:, None]
     c = np.arange(32)[None, :]
-    off = r * 128 + (((c // 4) ^ (r % 8)) * 16) + (c % 4) * 4
-    return np.frombuffer(img.tobytes(), dtype=np.float32)[off // 4]
+    off = r * 64 + (((c // 8) ^ ((r // 2) % 4)) * 16) + (c % 8) * 2
+    u16 = np.frombuffer(img.tobytes(), dtype=np.uint16)
+    return _bf16(u16[off // 2])
 
 
 def decode_record(raw):
     """Workspace record (include/kda.h layout) -> dict of W, Qp, Kt, U, Ol, eg."""
     a1 = np.concatenate([_unswizzle_bf16(raw[0:16384], 128), _unswizzle_bf16(raw[16384:32768], 128)], 1)
     kt = _unswizzle_bf16(raw[32768:49152], 128)
-    u = np.concatenate([_unswizzle_f32(raw[49152 + 8192 * s:49152 + 8192 * (s + 1)], 64) for s in range(4)], 1)
-    ol = np.concatenate([_unswizzle_f32(raw[81920 + 8192 * s:81920 + 8192 * (s + 1)], 64) for s in range(4)], 1)
-    eg = np.frombuffer(raw[114688:115200].tobytes(), dtype=np.float32)
+    u = np.concatenate([_unswizzle_slab(raw[49152 + 4096 * s:49152 + 4096 * (s + 1)]) for s in range(4)], 1)
+    ol = np.concatenate([_unswizzle_slab(raw[65536 + 4096 * s:65536 + 4096 * (s + 1)]) for s in range(4)], 1)
+    eg = np.frombuffer(raw[81920:82432].tobytes(), dtype=np.float32)
     return dict(W=a1[:64], Qp=a1[64:], Kt=kt, U=u, Ol=ol, eg=eg)
 
 
