@@ -144,7 +144,79 @@ __global__ void __launch_bounds__(128)
     if (warp == 0) tmem_dealloc(tmem_base, 256);
 }
 
+// D = A B^T, N = 32, with B stored MN-major in the 64-byte swizzle
+// (element (k, n) at k*64 + (((n/8) ^ ((k/2) % 4)) * 16) + (n%8)*2; 8-row
+// groups 512 B apart).
+__global__ void __launch_bounds__(128)
+    umma_mn64_selftest_kernel(const __nv_bfloat16* __restrict__ A, const __nv_bfloat16* __restrict__ B,
+                              float* __restrict__ D, int* status) {
+    constexpr int N = 32;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + 32768;  // 128 K rows x 64 B = 8 KB
+    __shared__ uint64_t bar_mma;
+    __shared__ uint32_t tmem_base;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        mbar_init(&bar_mma, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_base, 32);
+        tmem_relinquish();
+    }
+    for (int i = tid; i < 128 * 128; i += 128) {
+        const int r = i >> 7, c = i & 127;
+        *reinterpret_cast<__nv_bfloat16*>(sA + (c >> 6) * 16384 + sw128_off(r, c & 63)) = A[i];
+    }
+    for (int i = tid; i < N * 128; i += 128) {  // B[n][k] -> (k, n)
+        const int n = i >> 7, k = i & 127;
+        *reinterpret_cast<__nv_bfloat16*>(sB + k * 64 + ((((n >> 3) ^ ((k >> 1) & 3))) << 4) + (n & 7) * 2) = B[i];
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t kb = k >> 2, kin = (k & 3u) * 32u;
+            umma_bf16(tmem_base, sdesc_kmajor_sw128(smem_u32(sA) + kb * 16384 + kin),
+                      sdesc_mnmajor_sw64(smem_u32(sB) + (uint32_t)k * 1024u, 512u, 512u),
+                      idesc_bf16_f32_bmn(128, N), k > 0 ? 1u : 0u);
+        }
+        umma_commit(&bar_mma);
+    }
+    const bool ok = mbar_wait(&bar_mma, 0, nullptr);
+    if (!ok) atomicExch(status, 4);
+    tc_fence_after();
+    if (ok) {
+        for (int c0 = 0; c0 < N; c0 += 16) {
+            float v[16];
+            tmem_ld16(tmem_addr(tmem_base, warp * 32, c0), v);
+            const int row = warp * 32 + lane;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) D[row * N + c0 + i] = v[i];
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem_base, 32);
+}
+
 }  // namespace
+
+extern "C" int kda_selftest_umma_mn64(const void* A, const void* B, float* D, int* status,
+                                      void* stream) {
+    const size_t smem = 1024 + 32768 + 8192;
+    if (cudaFuncSetAttribute(umma_mn64_selftest_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+        return 3;
+    umma_mn64_selftest_kernel<<<1, 128, smem, (cudaStream_t)stream>>>(
+        (const __nv_bfloat16*)A, (const __nv_bfloat16*)B, D, status);
+    return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
 
 extern "C" int kda_selftest_umma_mn(const void* A, const void* B, float* D, int N, int mode,
                                     int* status, void* stream) {

@@ -229,6 +229,14 @@ __device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
+// Same for the 64-byte swizzle: for each K index a 64-byte row of 32
+// consecutive M/N elements; 8 rows form a 512-byte atom (16-byte chunk c of
+// row k at k*64 + ((c ^ ((k >> 1) & 3)) << 4)).
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw64(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)4 << 61);
+}
+
 // Instruction descriptor as idesc_bf16_f32 but with B MN-major.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32_bmn(uint32_t M, uint32_t N) {
     return idesc_bf16_f32(M, N) | (1u << 16);

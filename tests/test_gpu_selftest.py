@@ -54,3 +54,21 @@ def test_umma_tile_b_mn_major(selftest, N):
     torch.cuda.synchronize()
     assert status.item() == 0
     torch.testing.assert_close(D, A.float() @ B.float().T, atol=2e-3, rtol=1e-4)
+
+
+def test_umma_tile_b_mn_major_sw64(selftest):
+    """N = 32 B operand stored MN-major with the 64-byte swizzle (64-byte rows,
+    8-row groups 512 B apart): the state pass's S and V operands."""
+    f = selftest.kda_selftest_umma_mn64
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] * 5
+    g = torch.Generator(device="cpu").manual_seed(77)
+    A = torch.randn(128, 128, generator=g).to(torch.bfloat16).cuda()
+    B = torch.randn(32, 128, generator=g).to(torch.bfloat16).cuda()
+    D = torch.full((128, 32), float("nan"), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert f(A.data_ptr(), B.data_ptr(), D.data_ptr(), status.data_ptr(),
+             torch.cuda.current_stream().cuda_stream) == 0
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    torch.testing.assert_close(D, A.float() @ B.float().T, atol=2e-3, rtol=1e-4)
