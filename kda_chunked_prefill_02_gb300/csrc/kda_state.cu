@@ -42,12 +42,14 @@ constexpr uint32_t ST_OL = 53248;      // O_loc slab
 constexpr uint32_t ST_EG = 57344;      // e^gam [128] fp32
 constexpr uint32_t kStage = 58368;
 constexpr uint32_t kStageTx = 32768 + 16384 + kSlabImg * 2 + 512;
-// B operands with N = 32 value columns, MN-major, 128-byte swizzle: one
-// 128-byte row per K index, 8-row groups 1024 B apart; each thread stores its row.
-constexpr uint32_t kRowGroup = 1024;
-constexpr uint32_t O_SH = kStages * kStage;     // Diag(e^gam) S (or S for the first chunk): 128 key rows, 16 KB
-constexpr uint32_t O_VN = O_SH + 16384;         // V: 64 token rows, 8 KB
-constexpr uint32_t O_G = O_VN + 8192;           // G bf16, K-major A operand: 128 rows x 64 tokens, 16 KB
+// B operands with N = 32 value columns, MN-major, 64-byte swizzle: one
+// 64-byte row per K index (16-byte chunk c of row r at r*64 + ((c ^ ((r>>1)&3)) << 4)),
+// 8-row groups 512 B apart; each thread stores its own row.
+constexpr uint32_t kRowGroup = 512;
+constexpr uint32_t kShBytes = 8192;              // 128 key rows
+constexpr uint32_t O_SH = kStages * kStage;     // two buffers: Diag(e^gam_c) S_c (S_0 in buffer 1 first)
+constexpr uint32_t O_VN = O_SH + 2 * kShBytes;  // V: 64 token rows, 4 KB
+constexpr uint32_t O_G = O_VN + 4096;           // G bf16, K-major A operand: 128 rows x 64 tokens, 16 KB
 constexpr uint32_t kStateSmem = O_G + 16384 + 1024;
 // TMEM columns (fp32): two D1 accumulators, D2, G.
 constexpr uint32_t TM_D1 = 0, TM_D2 = 64, TM_G = 128, TM_COLS = 256;
@@ -60,10 +62,10 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 
 // Row r of an MN-major N = 32 operand: 32 bf16 in four swizzled 16-byte chunks.
 __device__ __forceinline__ void store_row32(uint8_t* base, int r, const float* x) {
-    uint8_t* rp = base + (r >> 3) * kRowGroup + (r & 7) * 128;
+    uint8_t* rp = base + r * 64;
 #pragma unroll
     for (int ch = 0; ch < 4; ++ch)
-        *reinterpret_cast<uint4*>(rp + ((ch ^ (r & 7)) << 4)) =
+        *reinterpret_cast<uint4*>(rp + ((ch ^ ((r >> 1) & 3)) << 4)) =
             make_uint4(pack_bf16x2(x[8 * ch], x[8 * ch + 1]), pack_bf16x2(x[8 * ch + 2], x[8 * ch + 3]),
                        pack_bf16x2(x[8 * ch + 4], x[8 * ch + 5]), pack_bf16x2(x[8 * ch + 6], x[8 * ch + 7]));
 }
@@ -171,34 +173,44 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
             const uint32_t sh = smem_u32(sm + O_SH), vnb = smem_u32(sm + O_VN), gb = smem_u32(sm + O_G);
             auto stage_addr = [&](int c) { return smem_u32(sm + (c % kStages) * kStage); };
             // D = A1 * B with A1 K-major (K = 128 keys) and B an MN-major operand.
-            auto mma_a1 = [&](uint32_t d, uint32_t a1, uint32_t bb, uint32_t idesc, bool acc) {
+            // (sw64: B is a N = 32 operand in the 64-byte swizzle; otherwise the
+            // N = 64 Kt image in the 128-byte swizzle.)
+            auto mma_a1 = [&](uint32_t d, uint32_t a1, uint32_t bb, uint32_t idesc, bool acc, bool sw64) {
                 for (uint32_t k = 0; k < 8; ++k)
                     umma_bf16(d, sdesc_kmajor_sw128(a1 + (k >> 2) * 16384 + (k & 3) * 32),
-                              sdesc_mnmajor_sw128(bb + k * 2 * kRowGroup, kRowGroup, kRowGroup), idesc,
-                              (acc || k > 0) ? 1u : 0u);
+                              sw64 ? sdesc_mnmajor_sw64(bb + k * 2 * kRowGroup, kRowGroup, kRowGroup)
+                                   : sdesc_mnmajor_sw128(bb + k * 2048, 1024, 1024),
+                              idesc, (acc || k > 0) ? 1u : 0u);
             };
             // D (+)= A * V with A K-major (K = 64 tokens) and V the MN-major V operand.
             auto mma_v = [&](uint32_t d, uint32_t a, bool acc) {
                 for (uint32_t k = 0; k < 4; ++k)
                     umma_bf16(d, sdesc_kmajor_sw128(a + k * 32),
-                              sdesc_mnmajor_sw128(vnb + k * 2 * kRowGroup, kRowGroup, kRowGroup), id32,
+                              sdesc_mnmajor_sw64(vnb + k * 2 * kRowGroup, kRowGroup, kRowGroup), id32,
                               (acc || k > 0) ? 1u : 0u);
             };
             bool ok = mbar_wait(&full[0], 0, abort);
-            if (ok) {  // D1_0 = A1_0 S_0 (the Y warps stored S_0 in the SH buffer)
+            if (ok) {  // D1_0 = A1_0 S_0 (the Y warps stored S_0 in SH buffer 1)
                 tc_fence_after();
-                mma_a1(tb + TM_D1, stage_addr(0) + ST_A1, sh, id32, false);
+                mma_a1(tb + TM_D1, stage_addr(0) + ST_A1, sh + kShBytes, id32, false, true);
                 umma_commit(&d1_ready[0]);
             }
             for (int c = 0; ok && c < count; ++c) {
                 const bool more = c + 1 < count;
                 const uint32_t s0 = stage_addr(c), s1 = stage_addr(c + 1);
-                if (more) {  // G_c+1 = A1_c+1 Kt_c (off the chain)
+                const uint32_t d1 = tb + TM_D1 + 32 * ((c + 1) & 1);
+                if (more) {
+                    // G_c+1 = A1_c+1 Kt_c (does not depend on the state)
                     if (!(ok = mbar_wait(&full[(c + 1) % kStages], ((c + 1) / kStages) & 1, abort))) break;
                     if (c >= 1 && !(ok = mbar_wait(&g_img_ready, (c - 1) & 1, abort))) break;
                     tc_fence_after();
-                    mma_a1(tb + TM_G, s1 + ST_A1, s0 + ST_KT, id64, false);
+                    mma_a1(tb + TM_G, s1 + ST_A1, s0 + ST_KT, id64, false, false);
                     umma_commit(&g_ready);
+                    // D1_c+1 = A1_c+1 Diag(e^gam_c) S_c  (+ G_c+1 V_c below)
+                    if (!(ok = mbar_wait(&s_img_ready, c & 1, abort))) break;
+                    if (c >= 1 && !(ok = mbar_wait(&d1_free[(c + 1) & 1], ((c - 1) >> 1) & 1, abort))) break;
+                    tc_fence_after();
+                    mma_a1(d1, s1 + ST_A1, sh + (c & 1) * kShBytes, id32, false, true);
                 }
                 // D2 = Kt_c V_c (once the Y warps have read the previous D2)
                 if (!(ok = mbar_wait(&vn_ready, c & 1, abort))) break;
@@ -207,12 +219,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
                 mma_v(tb + TM_D2, s0 + ST_KT, false);
                 umma_commit(&d2_ready);
                 umma_commit(&empty[c % kStages]);
-                if (more) {  // D1_c+1 = A1_c+1 Diag(e^gam_c) S_c + G_c+1 V_c
-                    const uint32_t d1 = tb + TM_D1 + 32 * ((c + 1) & 1);
-                    if (!(ok = mbar_wait(&s_img_ready, c & 1, abort))) break;
-                    if (c >= 1 && !(ok = mbar_wait(&d1_free[(c + 1) & 1], ((c - 1) >> 1) & 1, abort))) break;
-                    tc_fence_after();
-                    mma_a1(d1, s1 + ST_A1, sh, id32, false);
+                if (more) {
                     if (!(ok = mbar_wait(&g_img_ready, c & 1, abort))) break;
                     tc_fence_after();
                     mma_v(d1, gb, true);
@@ -294,26 +301,31 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
         }
         bool ok = true;
         if (count > 0) {
-            store_row32(sm + O_SH, row, S);  // S_0 for D1_0
+            store_row32(sm + O_SH + kShBytes, row, S);  // S_0 for D1_0
             fence_proxy_async_smem();
             tc_fence_before();
             named_bar_sync(kBarProlog, 160);
-        }
-        for (int c = 0; ok && c < count; ++c) {
-            const uint8_t* sb = sm + (c % kStages) * kStage;
-            // (a) Diag(e^gam_c) S_c once D1_c no longer reads the SH buffer
-            if (!(ok = warp_wait(&d1_ready[c & 1], (c >> 1) & 1, abort))) break;
-            if (!(ok = warp_wait(&full[c % kStages], (c / kStages) & 1, abort))) break;
-            const float eg = reinterpret_cast<const float*>(sb + ST_EG)[row];
-            if (c + 1 < count) {
+            // Diag(e^gam_0) S_0 for D1_1
+            if ((ok = warp_wait(&full[0], 0, abort)) && count > 1) {
+                const float eg0 = reinterpret_cast<const float*>(sm + ST_EG)[row];
                 float sh[kSlab];
 #pragma unroll
-                for (int j = 0; j < kSlab; ++j) sh[j] = eg * S[j];
+                for (int j = 0; j < kSlab; ++j) sh[j] = eg0 * S[j];
                 store_row32(sm + O_SH, row, sh);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&s_img_ready);
-                // (b) G_c+1 (fp32 in TMEM) -> bf16 K-major operand, row `row`
+            }
+        }
+        for (int c = 0; ok && c < count; ++c) {
+            const uint8_t* sb = sm + (c % kStages) * kStage;
+            const bool more = c + 1 < count;
+            // D1_c complete: the G operand and SH buffer (c+1)&1 are free again
+            if (!(ok = warp_wait(&d1_ready[c & 1], (c >> 1) & 1, abort))) break;
+            if (!(ok = warp_wait(&full[c % kStages], (c / kStages) & 1, abort))) break;
+            const float eg = reinterpret_cast<const float*>(sb + ST_EG)[row];
+            if (more) {
+                // G_c+1 (fp32 in TMEM) -> bf16 K-major operand, row `row`
                 if (!(ok = warp_wait(&g_ready, c & 1, abort))) break;
                 tc_fence_after();
                 uint8_t* gr = sm + O_G + row * 128;
@@ -334,7 +346,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&g_img_ready);
             }
-            // (c) S_c+1 = Diag(e^gam_c) S_c + Kt_c V_c
+            // S_c+1 = Diag(e^gam_c) S_c + Kt_c V_c
             if (!(ok = warp_wait(&d2_ready, c & 1, abort))) break;
             tc_fence_after();
             float d[kSlab];
@@ -344,6 +356,18 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
             if (lane == 0) mbar_arrive(&d2_free);
 #pragma unroll
             for (int j = 0; j < kSlab; ++j) S[j] = fmaf(eg, S[j], d[j]);
+            if (c + 2 < count) {
+                // Diag(e^gam_c+1) S_c+1 for D1_c+2, into SH buffer (c+1)&1
+                if (!(ok = warp_wait(&full[(c + 1) % kStages], ((c + 1) / kStages) & 1, abort))) break;
+                const float eg1 = reinterpret_cast<const float*>(sm + ((c + 1) % kStages) * kStage + ST_EG)[row];
+                float sh[kSlab];
+#pragma unroll
+                for (int j = 0; j < kSlab; ++j) sh[j] = eg1 * S[j];
+                store_row32(sm + O_SH + ((c + 1) & 1) * kShBytes, row, sh);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s_img_ready);
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[c % kStages]);
         }
