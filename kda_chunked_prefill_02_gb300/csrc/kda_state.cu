@@ -172,22 +172,29 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
             const uint32_t id32 = idesc_bf16_f32_bmn(128, kSlab), id64 = idesc_bf16_f32_bmn(128, 64);
             const uint32_t sh = smem_u32(sm + O_SH), vnb = smem_u32(sm + O_VN), gb = smem_u32(sm + O_G);
             auto stage_addr = [&](int c) { return smem_u32(sm + (c % kStages) * kStage); };
-            // D = A1 * B with A1 K-major (K = 128 keys) and B an MN-major operand.
-            // (sw64: B is a N = 32 operand in the 64-byte swizzle; otherwise the
-            // N = 64 Kt image in the 128-byte swizzle.)
+            // D = A1 * B with A1 K-major (K = 128 keys) and B an MN-major operand
+            // (sw64: a N = 32 operand in the 64-byte swizzle; otherwise the
+            // N = 64 Kt image in the 128-byte swizzle).  Descriptors are built
+            // once per operand base; inside the unrolled K loop only the start
+            // address (16-byte units, low bits) changes, so each tcgen05.mma
+            // costs an add or two to issue.
             auto mma_a1 = [&](uint32_t d, uint32_t a1, uint32_t bb, uint32_t idesc, bool acc, bool sw64) {
+                const uint64_t ad = sdesc_kmajor_sw128(a1);
+                const uint64_t bd = sw64 ? sdesc_mnmajor_sw64(bb, kRowGroup, kRowGroup)
+                                         : sdesc_mnmajor_sw128(bb, 1024, 1024);
+                const uint32_t bstep = sw64 ? (2 * kRowGroup) >> 4 : (2048 >> 4);
+#pragma unroll
                 for (uint32_t k = 0; k < 8; ++k)
-                    umma_bf16(d, sdesc_kmajor_sw128(a1 + (k >> 2) * 16384 + (k & 3) * 32),
-                              sw64 ? sdesc_mnmajor_sw64(bb + k * 2 * kRowGroup, kRowGroup, kRowGroup)
-                                   : sdesc_mnmajor_sw128(bb + k * 2048, 1024, 1024),
-                              idesc, (acc || k > 0) ? 1u : 0u);
+                    umma_bf16(d, ad + ((k >> 2) * (16384 >> 4) + (k & 3) * 2), bd + k * bstep, idesc,
+                              (acc || k > 0) ? 1u : 0u);
             };
             // D (+)= A * V with A K-major (K = 64 tokens) and V the MN-major V operand.
+            const uint64_t vdesc = sdesc_mnmajor_sw64(vnb, kRowGroup, kRowGroup);
             auto mma_v = [&](uint32_t d, uint32_t a, bool acc) {
+                const uint64_t ad = sdesc_kmajor_sw128(a);
+#pragma unroll
                 for (uint32_t k = 0; k < 4; ++k)
-                    umma_bf16(d, sdesc_kmajor_sw128(a + k * 32),
-                              sdesc_mnmajor_sw64(vnb + k * 2 * kRowGroup, kRowGroup, kRowGroup), id32,
-                              (acc || k > 0) ? 1u : 0u);
+                    umma_bf16(d, ad + k * 2, vdesc + k * ((2 * kRowGroup) >> 4), id32, (acc || k > 0) ? 1u : 0u);
             };
             bool ok = mbar_wait(&full[0], 0, abort);
             if (ok) {  // D1_0 = A1_0 S_0 (the Y warps stored S_0 in SH buffer 1)

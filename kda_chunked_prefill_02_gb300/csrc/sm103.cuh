@@ -276,11 +276,14 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 __device__ __forceinline__ void umma_tile(uint32_t d_tmem, uint32_t a_base, uint32_t a_block_bytes,
                                           uint32_t b_base, uint32_t b_block_bytes, uint32_t K,
                                           uint32_t idesc, bool accumulate) {
+    // Descriptors are built once; per K step only the start address (16-byte
+    // units in the low bits) moves.  Shared addresses stay below 2^18, so the
+    // 14-bit field cannot carry.
+    const uint64_t ad = sdesc_kmajor_sw128(a_base), bd = sdesc_kmajor_sw128(b_base);
     for (uint32_t k = 0; k < K / 16; ++k) {
-        const uint32_t kb = k >> 2, kin = (k & 3u) * 32u;
-        umma_bf16(d_tmem, sdesc_kmajor_sw128(a_base + kb * a_block_bytes + kin),
-                  sdesc_kmajor_sw128(b_base + kb * b_block_bytes + kin), idesc,
-                  (accumulate || k > 0) ? 1u : 0u);
+        const uint32_t kb = k >> 2, kin = (k & 3u) * 2u;
+        umma_bf16(d_tmem, ad + kb * (a_block_bytes >> 4) + kin, bd + kb * (b_block_bytes >> 4) + kin,
+                  idesc, (accumulate || k > 0) ? 1u : 0u);
     }
 }
 
