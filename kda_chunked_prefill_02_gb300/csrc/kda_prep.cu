@@ -368,33 +368,30 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             for (int r = 0; r < 16; ++r) x[r] = (r == l) ? 1.f : 0.f;
 #pragma unroll
             for (int r = 1; r < 16; ++r) {
-                float acc0 = x[r], acc1 = 0.f;
+                const float* ar = sA + (s0 + r) * kPA + s0;
+                float acc[4] = {x[r], 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int m = 0; m < r; m += 2) {
-                    acc0 = fmaf(-sA[(s0 + r) * kPA + s0 + m], x[m], acc0);
-                    if (m + 1 < r) acc1 = fmaf(-sA[(s0 + r) * kPA + s0 + m + 1], x[m + 1], acc1);
-                }
-                x[r] = acc0 + acc1;
+                for (int m = 0; m < r; ++m) acc[m & 3] = fmaf(-ar[m], x[m], acc[m & 3]);
+                x[r] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
             }
 #pragma unroll
             for (int r = 0; r < 16; ++r) sT[(s0 + r) * kPA + s0 + l] = x[r];
         }
         __syncthreads();
-        // Off-diagonal blocks with warp-level tf32 tensor-core products
-        // (fp32 accumulation; the result is rounded to bf16 for MMA C anyway).
+        // Off-diagonal blocks with warp-level tf32 tensor-core products (fp32
+        // accumulation; the result is rounded to bf16 for MMA C anyway).  Each
+        // warp owns a column block of its products, so the two dependent
+        // products of a level need only a warp barrier between them.
         const int g4 = lane >> 2, t4 = lane & 3;
-        if (warp < 4) {  // X_p = A_10 T_00 of 32-block p (two 16 x 8 tiles each)
+        if (warp < 4) {
+            // 16 -> 32: in 32-block p, X = A_10 T_00, then T_10 = -T_11 X and T_01 = 0
             const int pb = 32 * (warp >> 1), c0 = 8 * (warp & 1);
             float d[4];
             warp_mma_16x8(sA + (pb + 16) * kPA + pb, kPA, sT + pb * kPA + pb + c0, kPA, 16, d, lane);
             float* x = sX + (warp >> 1) * 256;
             x[g4 * 16 + c0 + 2 * t4] = d[0]; x[g4 * 16 + c0 + 2 * t4 + 1] = d[1];
             x[(g4 + 8) * 16 + c0 + 2 * t4] = d[2]; x[(g4 + 8) * 16 + c0 + 2 * t4 + 1] = d[3];
-        }
-        __syncthreads();
-        if (warp < 4) {  // T_10 = -T_11 X_p; the block above the diagonal is zero
-            const int pb = 32 * (warp >> 1), c0 = 8 * (warp & 1);
-            float d[4];
+            __syncwarp();
             warp_mma_16x8(sT + (pb + 16) * kPA + pb + 16, kPA, sX + (warp >> 1) * 256 + c0, 16, 16, d, lane);
             float* t10 = sT + (pb + 16) * kPA + pb + c0;
             t10[g4 * kPA + 2 * t4] = -d[0]; t10[g4 * kPA + 2 * t4 + 1] = -d[1];
@@ -404,22 +401,26 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             t01[(g4 + 8) * kPA + 2 * t4] = 0.f; t01[(g4 + 8) * kPA + 2 * t4 + 1] = 0.f;
         }
         __syncthreads();
-        {  // X = A[32:,:32] T[:32,:32]: eight 16 x 8 tiles, one per warp
-            const int r0 = 16 * (warp >> 2), c0 = 8 * (warp & 3);
-            float d[4];
-            warp_mma_16x8(sA + (32 + r0) * kPA, kPA, sT + c0, kPA, 32, d, lane);
-            float* x = sX + r0 * 33 + c0;
-            x[g4 * 33 + 2 * t4] = d[0]; x[g4 * 33 + 2 * t4 + 1] = d[1];
-            x[(g4 + 8) * 33 + 2 * t4] = d[2]; x[(g4 + 8) * 33 + 2 * t4 + 1] = d[3];
-        }
-        __syncthreads();
-        {  // T[32:,:32] = -T[32:,32:] X
-            const int r0 = 16 * (warp >> 2), c0 = 8 * (warp & 3);
-            float d[4];
-            warp_mma_16x8(sT + (32 + r0) * kPA + 32, kPA, sX + c0, 33, 32, d, lane);
-            float* t = sT + (32 + r0) * kPA + c0;
-            t[g4 * kPA + 2 * t4] = -d[0]; t[g4 * kPA + 2 * t4 + 1] = -d[1];
-            t[(g4 + 8) * kPA + 2 * t4] = -d[2]; t[(g4 + 8) * kPA + 2 * t4 + 1] = -d[3];
+        if (warp < 4) {
+            // 32 -> 64: warp w owns columns c0..c0+7 of X = A[32:,:32] T[:32,:32]
+            // (both 16-row tiles) and then of T[32:,:32] = -T[32:,32:] X
+            const int c0 = 8 * warp;
+            float d0[4], d1[4];
+            warp_mma_16x8(sA + 32 * kPA, kPA, sT + c0, kPA, 32, d0, lane);
+            warp_mma_16x8(sA + 48 * kPA, kPA, sT + c0, kPA, 32, d1, lane);
+            float* x = sX + c0;
+            x[g4 * 33 + 2 * t4] = d0[0]; x[g4 * 33 + 2 * t4 + 1] = d0[1];
+            x[(g4 + 8) * 33 + 2 * t4] = d0[2]; x[(g4 + 8) * 33 + 2 * t4 + 1] = d0[3];
+            x[(g4 + 16) * 33 + 2 * t4] = d1[0]; x[(g4 + 16) * 33 + 2 * t4 + 1] = d1[1];
+            x[(g4 + 24) * 33 + 2 * t4] = d1[2]; x[(g4 + 24) * 33 + 2 * t4 + 1] = d1[3];
+            __syncwarp();
+            warp_mma_16x8(sT + 32 * kPA + 32, kPA, sX + c0, 33, 32, d0, lane);
+            warp_mma_16x8(sT + 48 * kPA + 32, kPA, sX + c0, 33, 32, d1, lane);
+            float* t = sT + 32 * kPA + c0;
+            t[g4 * kPA + 2 * t4] = -d0[0]; t[g4 * kPA + 2 * t4 + 1] = -d0[1];
+            t[(g4 + 8) * kPA + 2 * t4] = -d0[2]; t[(g4 + 8) * kPA + 2 * t4 + 1] = -d0[3];
+            t[(g4 + 16) * kPA + 2 * t4] = -d1[0]; t[(g4 + 16) * kPA + 2 * t4 + 1] = -d1[1];
+            t[(g4 + 24) * kPA + 2 * t4] = -d1[2]; t[(g4 + 24) * kPA + 2 * t4 + 1] = -d1[3];
         }
         __syncthreads();
         // T' = T Diag(beta): rows 0..63 of the TT operand (K-major over j) and
