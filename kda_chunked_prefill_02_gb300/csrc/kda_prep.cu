@@ -79,6 +79,18 @@ __device__ __forceinline__ float2 ld_bf16x2(const uint8_t* p) {
 __device__ __forceinline__ void st_u32(uint8_t* p, uint32_t v) {
     *reinterpret_cast<uint32_t*>(p) = v;
 }
+__device__ __forceinline__ void st_bf16(uint8_t* p, float v) {
+    *reinterpret_cast<__nv_bfloat16*>(p) = __float2bfloat16_rn(v);
+}
+// Stores T' = T Diag(beta) entries (i, j) and (i, j + 1) of a computed T block
+// into the TT operand (row i, K index j) and the T'^T operand (row j, K index i).
+__device__ __forceinline__ void store_tprime_pair(uint8_t* sm, int i, int j, float t0, float t1,
+                                                  const float* sBeta) {
+    const float a = t0 * sBeta[j], b = t1 * sBeta[j + 1];
+    st_u32(sm + O_TT + sw128_off(i, j), pack_bf16x2(a, b));
+    st_bf16(sm + O_TTR + sw128_off(j, i), a);
+    st_bf16(sm + O_TTR + sw128_off(j + 1, i), b);
+}
 // Row of the Yoff operand holding column block J as seen from row block I > J:
 // block I's group holds its 16*I earlier columns.
 __device__ __forceinline__ uint32_t yoff_row(int I, int J, int l) {
@@ -376,6 +388,28 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             }
 #pragma unroll
             for (int r = 0; r < 16; ++r) sT[(s0 + r) * kPA + s0 + l] = x[r];
+            // T' of the diagonal block: column s0+l of TT, row s0+l of T'^T
+            const float bl = sBeta[s0 + l];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) st_bf16(sm + O_TT + sw128_off(s0 + r, s0 + l), x[r] * bl);
+            uint32_t w[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) w[r] = pack_bf16x2(x[2 * r] * bl, x[2 * r + 1] * bl);
+            *reinterpret_cast<uint4*>(sm + O_TTR + sw128_off(s0 + l, s0)) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(sm + O_TTR + sw128_off(s0 + l, s0 + 8)) = make_uint4(w[4], w[5], w[6], w[7]);
+        } else {
+            // Zero the 16 x 16 blocks of T' above the diagonal (TT: column block
+            // J > row block I) and below it in T'^T: 12 blocks x 16 rows x 2 chunks.
+            for (int e = tid - 64; e < 12 * 32; e += kPrepThreads - 64) {
+                const int blkid = e >> 5, rr = (e >> 1) & 15, half = e & 1;
+                const int bi = blkid % 6;
+                const int I = bi < 3 ? 0 : (bi < 5 ? 1 : 2);
+                const int J = bi < 3 ? bi + 1 : (bi < 5 ? bi - 1 : 3);
+                const int row = blkid < 6 ? 16 * I + rr : 16 * J + rr;
+                const int col = blkid < 6 ? 16 * J + 8 * half : 16 * I + 8 * half;
+                *reinterpret_cast<uint4*>(sm + (blkid < 6 ? O_TT : O_TTR) + sw128_off(row, col)) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
         }
         __syncthreads();
         // Off-diagonal blocks with warp-level tf32 tensor-core products (fp32
@@ -396,6 +430,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             float* t10 = sT + (pb + 16) * kPA + pb + c0;
             t10[g4 * kPA + 2 * t4] = -d[0]; t10[g4 * kPA + 2 * t4 + 1] = -d[1];
             t10[(g4 + 8) * kPA + 2 * t4] = -d[2]; t10[(g4 + 8) * kPA + 2 * t4 + 1] = -d[3];
+            store_tprime_pair(sm, pb + 16 + g4, pb + c0 + 2 * t4, -d[0], -d[1], sBeta);
+            store_tprime_pair(sm, pb + 24 + g4, pb + c0 + 2 * t4, -d[2], -d[3], sBeta);
             float* t01 = sT + pb * kPA + pb + 16 + c0;
             t01[g4 * kPA + 2 * t4] = 0.f; t01[g4 * kPA + 2 * t4 + 1] = 0.f;
             t01[(g4 + 8) * kPA + 2 * t4] = 0.f; t01[(g4 + 8) * kPA + 2 * t4 + 1] = 0.f;
@@ -421,23 +457,13 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             t[(g4 + 8) * kPA + 2 * t4] = -d0[2]; t[(g4 + 8) * kPA + 2 * t4 + 1] = -d0[3];
             t[(g4 + 16) * kPA + 2 * t4] = -d1[0]; t[(g4 + 16) * kPA + 2 * t4 + 1] = -d1[1];
             t[(g4 + 24) * kPA + 2 * t4] = -d1[2]; t[(g4 + 24) * kPA + 2 * t4 + 1] = -d1[3];
-        }
-        __syncthreads();
-        // T' = T Diag(beta): rows 0..63 of the TT operand (K-major over j) and
-        // T'^T, the B operand of MMA B (row n, K index j); entries above the
-        // diagonal are zero.
-        for (int e = tid; e < 64 * 32; e += kPrepThreads) {
-            const int r = e >> 5, jp = 2 * (e & 31);
-            const float t0 = jp <= r ? sT[r * kPA + jp] * sBeta[jp] : 0.f;
-            const float t1 = jp + 1 <= r ? sT[r * kPA + jp + 1] * sBeta[jp + 1] : 0.f;
-            st_u32(sm + O_TT + sw128_off(r, jp), pack_bf16x2(t0, t1));
-            const float u0 = r <= jp ? sT[jp * kPA + r] * sBeta[r] : 0.f;
-            const float u1 = r <= jp + 1 ? sT[(jp + 1) * kPA + r] * sBeta[r] : 0.f;
-            st_u32(sm + O_TTR + sw128_off(r, jp), pack_bf16x2(u0, u1));
+            store_tprime_pair(sm, 32 + g4, c0 + 2 * t4, -d0[0], -d0[1], sBeta);
+            store_tprime_pair(sm, 40 + g4, c0 + 2 * t4, -d0[2], -d0[3], sBeta);
+            store_tprime_pair(sm, 48 + g4, c0 + 2 * t4, -d1[0], -d1[1], sBeta);
+            store_tprime_pair(sm, 56 + g4, c0 + 2 * t4, -d1[2], -d1[3], sBeta);
         }
         fence_proxy_async_smem();
         __syncthreads();
-
         // ---- MMA B: D_b = Aqk T'  -> rows 64..127 of the TT operand
         if (tid == 0) {
             tc_fence_after();
