@@ -17,6 +17,7 @@ chains) on the host cores, on a bounded sample of the same workload per step;
 it is a deliberately slow reference, not a target.
 """
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -141,6 +142,27 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+def captured_traffic(kernel, token_heads):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary
+    (profiles/<kernel>_kernel_traffic.txt), scaled to `token_heads`; None when
+    there is no capture or the kernel source changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "%s_kernel_traffic.txt" % kernel)
+    src = os.path.join(ROOT, "kda_chunked_prefill_02_gb300", "csrc", "kda_%s.cu" % kernel)
+    if not (os.path.exists(path) and os.path.exists(src)):
+        return None
+    rec = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line:
+                k, v = line.split(":", 1)
+                rec[k.strip()] = v.strip()
+    with open(src, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    if rec.get("source_sha256_prefix") != sha or "dram_bytes_per_token_head" not in rec:
+        return None
+    return float(rec["dram_bytes_per_token_head"]) * token_heads
+
+
 def workload(name):
     from kda_chunked_prefill_02_gb300 import inputs
     return inputs.config_inputs(name)
@@ -239,7 +261,8 @@ def run_ours(args, rank, ws, local):
     flops = th * FLOP_TOKEN_HEAD
     tensor_frac = flops / (ms / 1e3) / 1e12 / tf_burst
     path_bytes = bytes_prep + bytes_state
-    return dict(ms=ms, value=value, clk=clk, ms_prep=ms_prep, ms_state=ms_state, dom=dom,
+    traffic = captured_traffic(dom, th)
+    return dict(traffic=traffic, ms=ms, value=value, clk=clk, ms_prep=ms_prep, ms_state=ms_state, dom=dom,
                 achieved=achieved, hbm=hbm, peak_src=peak_src, tensor_frac=tensor_frac,
                 tf_burst=tf_burst, path_gbs=path_bytes / (ms / 1e3) / 1e9, inp=inp, d=d,
                 out=out, fin=fin, wsb=wsb, stream=stream, flops=flops, dbytes=dbytes)
@@ -327,7 +350,9 @@ def main():
                             "note": "whole-call algorithmic tensor FLOP (180,224 per token-head) / call time, of measured peak"},
             "roofline": {"bound": "hbm", "kernel": r["dom"], "achieved": r["achieved"],
                          "peak": r["hbm"], "unit": "GB/s", "frac": r["achieved"] / r["hbm"],
-                         "traffic": None, "peak_source": r["peak_src"]},
+                         "traffic": r["traffic"], "peak_source": r["peak_src"],
+                         "algorithmic_bytes": r["dbytes"],
+                         "traffic_note": "ncu DRAM bytes of the capture in profiles/, scaled by token-heads"},
             "kernels_ms": {"prep": r["ms_prep"], "state": r["ms_state"]},
             "path_gbs": r["path_gbs"],
             "e2e": e2e, "cpu_baseline": cpu,
