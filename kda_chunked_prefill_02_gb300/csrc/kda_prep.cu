@@ -29,7 +29,7 @@
 // when its true decay is already below e^-5.4, and never for gates >= -5.4
 // (the production gate bound is -5).
 //
-// Organisation: a persistent CTA (8 warps) per SM loops over (chunk, head)
+// Organisation: a persistent CTA (16 warps) per SM loops over (chunk, head)
 // records.  The q, k, v and g tiles of a record arrive by TMA; the next
 // record's tiles are requested as soon as the current record's gate phase has
 // consumed its inputs, so the loads overlap the tensor-core and solve phases.
@@ -39,7 +39,7 @@
 namespace kda {
 namespace {
 
-constexpr int kPrepThreads = 256;
+constexpr int kPrepThreads = 512;
 
 // Dynamic shared memory map (bytes from a 1024-aligned base).
 constexpr uint32_t O_IQ = 0;          // bf16 [64][128] q tile (TMA, plain rows)
@@ -54,17 +54,21 @@ constexpr uint32_t O_KV = 155648;     // B operand [K e^Gam | V], MN-major: 8 to
 constexpr uint32_t kKvSbo = 4096;     // byte distance between 8-token groups of the KV operand
 constexpr uint32_t O_QT = 188416;     // bf16 [64][136] Q e^Gam (row pitch 272 B)
 constexpr uint32_t kQtPitch = 272;
-constexpr uint32_t O_TOT = 205824;    // fp32 [4][128] block gate totals
-constexpr uint32_t O_BETA = 207872;   // fp32 [64] beta
-constexpr uint32_t kPrepSmem = 208128 + 1024;
+constexpr uint32_t O_TOT = 205824;    // fp32 [2][8][128] gate sums (exact, floored) of 8-token groups
+constexpr uint32_t O_BETA = 214016;   // fp32 [64] beta
+constexpr uint32_t kPrepSmem = 214272 + 1024;
 // Scratch of the solve and MMA B / C, over R and Y once MMA A has completed.
-constexpr int kPA = 65;               // fp32 row pitch (conflict-free columns)
-constexpr uint32_t O_A = 81920;       // fp32 [64][65] beta-scaled A
-constexpr uint32_t O_T = 98560;       // fp32 [64][65] T
-constexpr uint32_t O_X = 115200;      // fp32 [32][33] products
-constexpr uint32_t O_AQK = 119808;    // A operand Aqk: 64 rows x 128 B (rows 64..127 are don't-care)
-constexpr uint32_t O_TT = 128000;     // A operand [T' ; Aqk T']: 128 rows x 128 B
-constexpr uint32_t O_TTR = 144384;    // B operand T'^T: 64 rows x 128 B
+// The fp32 matrices hold tf32-rounded values (operands of the warp MMAs); the
+// row pitch 68 (4 mod 32) makes the MMA row-fragment loads and the epilogue's
+// float4 row stores conflict-free.
+constexpr int kPA = 68;               // fp32 row pitch of A and T
+constexpr int kPX = 40;               // fp32 row pitch of the products X (8 mod 32)
+constexpr uint32_t O_A = 81920;       // fp32 [64][68] beta-scaled A
+constexpr uint32_t O_T = 99328;       // fp32 [64][68] T
+constexpr uint32_t O_X = 116736;      // fp32 [32][40] products
+constexpr uint32_t O_AQK = 122880;    // A operand Aqk: 64 rows x 128 B (rows 64..127 are don't-care)
+constexpr uint32_t O_TT = 131072;     // A operand [T' ; Aqk T']: 128 rows x 128 B
+constexpr uint32_t O_TTR = 147456;    // B operand T'^T: 64 rows x 128 B
 // Staging of the record images written by the last epilogue (over R, Y, KV).
 constexpr uint32_t O_SA1 = 81920;     // [W ; Q'] image, 32 KB
 constexpr uint32_t O_SU = 114688;     // U image, 16 KB
@@ -99,28 +103,38 @@ __device__ __forceinline__ uint32_t yoff_row(int I, int J, int l) {
 
 // Warp-level m16n8k8 tf32 MMA with fp32 accumulation (used for the small block
 // products of the UT solve; fragment layouts of the PTX m16n8k8 tf32 shape).
-__device__ __forceinline__ uint32_t to_tf32(float x) {
+__device__ __forceinline__ float tf32_round(float x) {
     uint32_t r;
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
+    return __uint_as_float(r);
 }
-// d (16 x 8 tile) = P (16 x kdim, row pitch pp) * Q (kdim x 8, row pitch pq),
-// fp32 matrices in shared memory.  Thread (g = lane/4, t = lane%4) gets
-// d0 (g, 2t), d1 (g, 2t+1), d2 (g+8, 2t), d3 (g+8, 2t+1).
+// d (16 x 8 tile) = P (16 x 8*ke, row pitch pp) * Q (8*ke x 8, row pitch pq) over
+// the k-steps kb .. ke-1 (8 each), fp32 matrices of tf32-rounded values in shared
+// memory.  Thread (g = lane/4, t = lane%4) gets d0 (g, 2t), d1 (g, 2t+1),
+// d2 (g+8, 2t), d3 (g+8, 2t+1).
 __device__ __forceinline__ void warp_mma_16x8(const float* P, int pp, const float* Q, int pq,
-                                              int kdim, float (&d)[4], int lane) {
+                                              int kb, int ke, float (&d)[4], int lane) {
     const int g = lane >> 2, t = lane & 3;
     d[0] = d[1] = d[2] = d[3] = 0.f;
-    for (int k0 = 0; k0 < kdim; k0 += 8) {
-        const uint32_t a0 = to_tf32(P[g * pp + k0 + t]), a1 = to_tf32(P[(g + 8) * pp + k0 + t]);
-        const uint32_t a2 = to_tf32(P[g * pp + k0 + t + 4]), a3 = to_tf32(P[(g + 8) * pp + k0 + t + 4]);
-        const uint32_t b0 = to_tf32(Q[(k0 + t) * pq + g]), b1 = to_tf32(Q[(k0 + t + 4) * pq + g]);
+    for (int ks = kb; ks < ke; ++ks) {
+        const int k0 = 8 * ks;
+        const uint32_t a0 = __float_as_uint(P[g * pp + k0 + t]), a1 = __float_as_uint(P[(g + 8) * pp + k0 + t]);
+        const uint32_t a2 = __float_as_uint(P[g * pp + k0 + t + 4]);
+        const uint32_t a3 = __float_as_uint(P[(g + 8) * pp + k0 + t + 4]);
+        const uint32_t b0 = __float_as_uint(Q[(k0 + t) * pq + g]), b1 = __float_as_uint(Q[(k0 + t + 4) * pq + g]);
         asm volatile(
             "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
             "{%8,%9}, {%0,%1,%2,%3};"
             : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
             : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
     }
+}
+// Stores a 16 x 8 accumulator tile (fragment layout above) at X (row pitch pq),
+// rounded to tf32.
+__device__ __forceinline__ void store_tile_tf32(float* X, int pq, const float (&d)[4], int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    *reinterpret_cast<float2*>(X + g * pq + 2 * t) = make_float2(tf32_round(d[0]), tf32_round(d[1]));
+    *reinterpret_cast<float2*>(X + (g + 8) * pq + 2 * t) = make_float2(tf32_round(d[2]), tf32_round(d[3]));
 }
 
 // Issues the TMA loads of one record's q, k, v, g tiles.
@@ -160,10 +174,13 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     tc_fence_after();
     const uint32_t tb = tmem_base_sh;
 
-    // Thread roles in the gate phases: block G (16 tokens), channels c0, c0 + 1.
-    const int G = tid >> 6, c0 = 2 * (tid & 63), blk = c0 >> 6, cc = c0 & 63;
-    // Roles in the TMEM epilogues: lane quarter qd, column half.
-    const int qd = warp & 3, half = warp >> 2;
+    // Thread roles in the gate phases: key channels c0, c0 + 1 and the 8-token
+    // group h8 (half hf of the 16-token block G).  A warp covers 64 channels
+    // (one 128-byte operand row) of one token row per store.
+    const int c0 = 2 * (tid & 63), h8 = tid >> 6, G = h8 >> 1, hf = h8 & 1;
+    const int blk = c0 >> 6, cc = c0 & 63;
+    // Roles in the TMEM epilogues: lane quarter qd, column quarter cq.
+    const int qd = warp & 3, cq = warp >> 2;
     const float kPFloor = __expf(kGateFloor);
 
     int rec = blockIdx.x;
@@ -192,29 +209,31 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             reinterpret_cast<float*>(sm + O_BETA)[tid] = tid < len ? bval : 0.f;
         }
 
-        // ---- E1: p = exp(g) (masked past the chunk length), block gate totals,
-        // and the suffix products z (exact) and zc (floored gate) by a backward pass.
-        float p0[16], p1[16], z0[16], z1[16], zc0[16], zc1[16];
+        // ---- E1: p = exp(g) (masked past the chunk length), the suffix products
+        // z (exact) and zc (floored gate) inside the 8-token group, and the
+        // group's gate sums, exact and floored.
+        float p0[8], p1[8], z0[8], z1[8], zc0[8], zc1[8];
         {
-            float d0 = 0.f, d1 = 0.f;
+            float d0 = 0.f, d1 = 0.f, e0 = 0.f, e1 = 0.f;
 #pragma unroll
-            for (int l = 0; l < 16; ++l) {
-                const int i = 16 * G + l;
+            for (int l = 0; l < 8; ++l) {
+                const int i = 8 * h8 + l;
                 float2 gv = *reinterpret_cast<const float2*>(sm + O_IG + i * 512 + c0 * 4);
                 if (i >= len) gv = make_float2(0.f, 0.f);
                 d0 += gv.x; d1 += gv.y;
+                e0 += fmaxf(gv.x, kGateFloor); e1 += fmaxf(gv.y, kGateFloor);
                 p0[l] = __expf(gv.x); p1[l] = __expf(gv.y);
             }
             float s0 = 1.f, s1 = 1.f, t0 = 1.f, t1 = 1.f;
 #pragma unroll
-            for (int l = 15; l >= 0; --l) {
+            for (int l = 7; l >= 0; --l) {
                 z0[l] = s0; z1[l] = s1; zc0[l] = t0; zc1[l] = t1;
                 s0 *= p0[l]; s1 *= p1[l];
                 t0 *= fmaxf(p0[l], kPFloor); t1 *= fmaxf(p1[l], kPFloor);
             }
             float* tot = reinterpret_cast<float*>(sm + O_TOT);
-            tot[G * 128 + c0] = d0;
-            tot[G * 128 + c0 + 1] = d1;
+            *reinterpret_cast<float2*>(tot + h8 * 128 + c0) = make_float2(d0, d1);
+            *reinterpret_cast<float2*>(tot + 1024 + h8 * 128 + c0) = make_float2(e0, e1);
         }
         if (tid == 0) bulk_wait_read();  // the previous record's images have left the staging area
         __syncthreads();
@@ -222,42 +241,57 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         // ---- E2: the MMA operands and the records that need no MMA.
         {
             const float* tot = reinterpret_cast<const float*>(sm + O_TOT);
-            float d0[4], d1[4];
+            float h0[8], h1[8];  // exact gate sums of the eight 8-token groups
 #pragma unroll
-            for (int J = 0; J < 4; ++J) { d0[J] = tot[J * 128 + c0]; d1[J] = tot[J * 128 + c0 + 1]; }
+            for (int q = 0; q < 8; ++q) {
+                const float2 t = *reinterpret_cast<const float2*>(tot + q * 128 + c0);
+                h0[q] = t.x; h1[q] = t.y;
+            }
+            // exact (hA, hB) and floored (fA, fB) sums of block G's two halves
+            const float2 hA = *reinterpret_cast<const float2*>(tot + (2 * G) * 128 + c0);
+            const float2 hB = *reinterpret_cast<const float2*>(tot + (2 * G + 1) * 128 + c0);
+            const float2 fA = *reinterpret_cast<const float2*>(tot + 1024 + (2 * G) * 128 + c0);
+            const float2 fB = *reinterpret_cast<const float2*>(tot + 1024 + (2 * G + 1) * 128 + c0);
             float pre0 = 0.f, pre1 = 0.f, post0 = 0.f, post1 = 0.f;
 #pragma unroll
             for (int J = 0; J < 4; ++J) {
-                if (J < G) { pre0 += d0[J]; pre1 += d1[J]; }
-                if (J > G) { post0 += d0[J]; post1 += d1[J]; }
+                if (J < G) { pre0 += h0[2 * J] + h0[2 * J + 1]; pre1 += h1[2 * J] + h1[2 * J + 1]; }
+                if (J > G) { post0 += h0[2 * J] + h0[2 * J + 1]; post1 += h1[2 * J] + h1[2 * J + 1]; }
             }
-            const float B0 = __expf(pre0), B1 = __expf(pre1);    // chunk start -> block start
-            const float E0 = __expf(post0), E1 = __expf(post1);  // block end -> chunk end
-            float Dm0[4], Dm1[4];  // decay over the blocks strictly between G and I
+            // Factors that carry the running products across the two halves of block G:
+            // the second half starts from the first half's product, the first half's
+            // suffix products continue through the second half.
+            const float am0 = hf ? __expf(hA.x) : 1.f, am1 = hf ? __expf(hA.y) : 1.f;
+            const float acm0 = hf ? __expf(fA.x) : 1.f, acm1 = hf ? __expf(fA.y) : 1.f;
+            const float zm0 = hf ? 1.f : __expf(hB.x), zm1 = hf ? 1.f : __expf(hB.y);
+            const float zcm0 = hf ? 1.f : __expf(fB.x), zcm1 = hf ? 1.f : __expf(fB.y);
+            // 1 / (floored-gate block product) <= e^86.4, folded into the suffix factor
+            const float zci0 = zcm0 * __expf(-(fA.x + fB.x)), zci1 = zcm1 * __expf(-(fA.y + fB.y));
+            const float Bg0 = __expf(pre0), Bg1 = __expf(pre1);    // chunk start -> block start
+            const float zE0 = zm0 * __expf(post0), zE1 = zm1 * __expf(post1);  // -> chunk end
+            float zD0[4], zD1[4];  // decay over the blocks strictly between G and I
             {
                 float s0 = 0.f, s1 = 0.f;
 #pragma unroll
                 for (int I = 0; I < 4; ++I) {
-                    Dm0[I] = __expf(s0); Dm1[I] = __expf(s1);
-                    if (I > G) { s0 += d0[I]; s1 += d1[I]; }
+                    zD0[I] = zm0 * __expf(s0); zD1[I] = zm1 * __expf(s1);
+                    if (I > G) { s0 += h0[2 * I] + h0[2 * I + 1]; s1 += h1[2 * I] + h1[2 * I + 1]; }
                 }
             }
-            // 1 / (floored-gate block product): <= e^86.4
-            const float ib0 = 1.0f / (fmaxf(p0[0], kPFloor) * zc0[0]);
-            const float ib1 = 1.0f / (fmaxf(p1[0], kPFloor) * zc1[0]);
             uint8_t* rp = p.ws_rec + (size_t)rec * kRecBytes;
-            if (G == 0)
-                *reinterpret_cast<float2*>(rp + kRecEg + c0 * 4) =
-                    make_float2(__expf(d0[0] + d0[1] + d0[2] + d0[3]),
-                                __expf(d1[0] + d1[1] + d1[2] + d1[3]));
+            if (h8 == 0) {
+                float t0 = 0.f, t1 = 0.f;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) { t0 += h0[q]; t1 += h1[q]; }
+                *reinterpret_cast<float2*>(rp + kRecEg + c0 * 4) = make_float2(__expf(t0), __expf(t1));
+            }
             const float qscale = p.scale;
             const uint32_t bo = blk * 16384u, yb = blk * kYBlock;
-            float a0 = 1.f, a1 = 1.f, ac0 = 1.f, ac1 = 1.f;
-            float eh0 = 0.f, eh1 = 0.f;
-            uint32_t kh0[8], kh1[8];
+            float a0 = am0, a1 = am1, ac0 = acm0, ac1 = acm1, eh0 = 0.f, eh1 = 0.f;
+            uint32_t kh0[4], kh1[4];
 #pragma unroll
-            for (int l = 0; l < 16; ++l) {
-                const int i = 16 * G + l;
+            for (int l = 0; l < 8; ++l) {
+                const int i = 8 * h8 + l;
                 const bool valid = i < len;
                 a0 *= p0[l]; a1 *= p1[l];
                 ac0 *= fmaxf(p0[l], kPFloor); ac1 *= fmaxf(p1[l], kPFloor);
@@ -270,22 +304,22 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                 st_u32(sm + O_R + bo + sw128_off(i, cc), pack_bf16x2(kk.x * ac0, kk.y * ac1));
                 st_u32(sm + O_R + bo + sw128_off(64 + i, cc), pack_bf16x2(qq.x * ac0, qq.y * ac1));
                 // Yd (diagonal blocks): K / ac = K zc / ac_block
+                const float kz0 = kk.x * z0[l], kz1 = kk.y * z1[l];
                 st_u32(sm + O_Y + yb + sw128_off(96 + i, cc),
-                       pack_bf16x2(kk.x * zc0[l] * ib0, kk.y * zc1[l] * ib1));
+                       pack_bf16x2(kk.x * zc0[l] * zci0, kk.y * zc1[l] * zci1));
                 // Yoff: column block G seen from each later row block I
 #pragma unroll
                 for (int I = 1; I < 4; ++I)
                     if (I > G)
-                        st_u32(sm + O_Y + yb + sw128_off(yoff_row(I, G, l), cc),
-                               pack_bf16x2(kk.x * z0[l] * Dm0[I], kk.y * z1[l] * Dm1[I]));
-                // Q e^Gam for Q'
-                const float ea0 = a0 * B0, ea1 = a1 * B1;
+                        st_u32(sm + O_Y + yb + sw128_off(yoff_row(I, G, 8 * hf + l), cc),
+                               pack_bf16x2(kz0 * zD0[I], kz1 * zD1[I]));
+                // Q e^Gam for Q', [K e^Gam | V] (MN-major: token row i, channels contiguous)
+                const float ea0 = a0 * Bg0, ea1 = a1 * Bg1;
                 st_u32(sm + O_QT + i * kQtPitch + c0 * 2, pack_bf16x2(qq.x * ea0, qq.y * ea1));
-                // [K e^Gam | V] (MN-major: token row i, channels contiguous)
                 st_u32(sm + O_KV + mn_sw128_off(i, c0, kKvSbo), pack_bf16x2(kk.x * ea0, kk.y * ea1));
                 st_u32(sm + O_KV + mn_sw128_off(i, 128 + c0, kKvSbo), pack_bf16x2(vv.x, vv.y));
                 // Kt = (K e^{gam - Gam})^T, packed by token pairs
-                const float hh0 = kk.x * z0[l] * E0, hh1 = kk.y * z1[l] * E1;
+                const float hh0 = kz0 * zE0, hh1 = kz1 * zE1;
                 if ((l & 1) == 0) {
                     eh0 = hh0; eh1 = hh1;
                 } else {
@@ -293,12 +327,10 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                     kh1[l >> 1] = pack_bf16x2(eh1, hh1);
                 }
             }
-            // Kt image rows c0, c0 + 1: tokens 16G..16G+15 are 16-byte chunks 2G, 2G+1
+            // Kt image rows c0, c0 + 1: tokens 8 h8 .. 8 h8 + 7 are 16-byte chunk h8
             uint8_t* kt = rp + kRecKt;
-            *reinterpret_cast<uint4*>(kt + sw128_off(c0, 16 * G)) = make_uint4(kh0[0], kh0[1], kh0[2], kh0[3]);
-            *reinterpret_cast<uint4*>(kt + sw128_off(c0, 16 * G + 8)) = make_uint4(kh0[4], kh0[5], kh0[6], kh0[7]);
-            *reinterpret_cast<uint4*>(kt + sw128_off(c0 + 1, 16 * G)) = make_uint4(kh1[0], kh1[1], kh1[2], kh1[3]);
-            *reinterpret_cast<uint4*>(kt + sw128_off(c0 + 1, 16 * G + 8)) = make_uint4(kh1[4], kh1[5], kh1[6], kh1[7]);
+            *reinterpret_cast<uint4*>(kt + sw128_off(c0, 8 * h8)) = make_uint4(kh0[0], kh0[1], kh0[2], kh0[3]);
+            *reinterpret_cast<uint4*>(kt + sw128_off(c0 + 1, 8 * h8)) = make_uint4(kh1[0], kh1[1], kh1[2], kh1[3]);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -333,34 +365,32 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             const int i = 32 * (qd & 1) + lane, I = i >> 4, I0 = 2 * (qd & 1), I1 = I0 + 1;
             const bool lo = lane < 16;
             const float bi = sBeta[i];
+            const int J = cq;
+            float t0[16], t1[16], tm[16];
 #pragma unroll
-            for (int jg = 0; jg < 2; ++jg) {
-                const int J = 2 * half + jg;
-                float t0[16], t1[16], tm[16];
+            for (int x = 0; x < 16; ++x) { t0[x] = 0.f; t1[x] = 0.f; tm[x] = 0.f; }
+            if (J < I0) tmem_ld16(tmem_addr(tb, 32 * qd, TM_A + yoff_row(I0, J, 0)), t0);
+            if (J < I1) tmem_ld16(tmem_addr(tb, 32 * qd, TM_A + yoff_row(I1, J, 0)), t1);
+            if (J <= I1) tmem_ld16(tmem_addr(tb, 32 * qd, TM_DIAG + 16 * J), tm);
+            float v[16];
 #pragma unroll
-                for (int x = 0; x < 16; ++x) { t0[x] = 0.f; t1[x] = 0.f; tm[x] = 0.f; }
-                if (J < I0) tmem_ld16(tmem_addr(tb, 32 * qd, TM_A + yoff_row(I0, J, 0)), t0);
-                if (J < I1) tmem_ld16(tmem_addr(tb, 32 * qd, TM_A + yoff_row(I1, J, 0)), t1);
-                if (J <= I1) tmem_ld16(tmem_addr(tb, 32 * qd, TM_DIAG + 16 * J), tm);
+            for (int x = 0; x < 16; ++x) {
+                const int j = 16 * J + x;
+                float val = 0.f;
+                if (J < I) val = lo ? t0[x] : t1[x];
+                else if (J == I) val = tm[x];
+                v[x] = isq ? ((j <= i) ? val : 0.f) : ((j < i) ? tf32_round(bi * val) : 0.f);
+            }
+            if (!isq) {
+                float4* dst = reinterpret_cast<float4*>(sA + i * kPA + 16 * J);
 #pragma unroll
-                for (int jj = 0; jj < 16; jj += 2) {
-                    float v2[2];
+                for (int u = 0; u < 4; ++u) dst[u] = make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+            } else {
+                uint32_t w[8];
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int j = 16 * J + jj + e;
-                        float val = 0.f;
-                        if (J < I) val = lo ? t0[jj + e] : t1[jj + e];
-                        else if (J == I) val = tm[jj + e];
-                        v2[e] = isq ? ((j <= i) ? val : 0.f) : ((j < i) ? bi * val : 0.f);
-                    }
-                    const int j = 16 * J + jj;
-                    if (!isq) {
-                        sA[i * kPA + j] = v2[0];
-                        sA[i * kPA + j + 1] = v2[1];
-                    } else {
-                        st_u32(sm + O_AQK + sw128_off(i, j), pack_bf16x2(v2[0], v2[1]));
-                    }
-                }
+                for (int x = 0; x < 8; ++x) w[x] = pack_bf16x2(v[2 * x], v[2 * x + 1]);
+                *reinterpret_cast<uint4*>(sm + O_AQK + sw128_off(i, 16 * J)) = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4*>(sm + O_AQK + sw128_off(i, 16 * J + 8)) = make_uint4(w[4], w[5], w[6], w[7]);
             }
         }
         fence_proxy_async_smem();
@@ -368,99 +398,82 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         __syncthreads();
 
         // ---- UT transform: T = (I + A)^-1 for the unit lower-triangular 64 x 64
-        // system, fp32, blocked: four 16 x 16 diagonal inverses by forward
-        // substitution, then [[Ta,0],[Aba,Tb]]^-1 = [[Ta^-1,0],[-Tb^-1 Aba Ta^-1, Tb^-1]]
-        // at 16 -> 32 and 32 -> 64.  Blocks above the diagonal are never read
-        // except the two 16 x 16 ones inside the 32 x 32 diagonal blocks, which
-        // are written as zeros.
-        if (tid < 64) {
-            const int I = tid >> 4, l = tid & 15, s0 = 16 * I;
-            float x[16];
+        // system, blocked: four 16 x 16 diagonal inverses by forward substitution,
+        // then [[Ta,0],[Aba,Tb]]^-1 = [[Ta^-1,0],[-Tb^-1 Aba Ta^-1, Tb^-1]] at
+        // 16 -> 32 and 32 -> 64.  T' = T Diag(beta) goes to the TT / T'^T operands
+        // as each block is produced; the products skip the k-steps that are zero
+        // because T is lower triangular, so T's upper blocks are never read.
+        {
+            // Diagonal blocks: warp (block I, columns l, l + 1 for lanes >= 16 two
+            // further), lane row m.  The substitution runs down the rows: once row r
+            // is final it is broadcast and every later row subtracts A[m][r] x_r.
+            const int I = warp >> 2, m = lane & 15, s0 = 16 * I;
+            const int l = 4 * (warp & 3) + 2 * (lane >> 4);
+            float ar[16];
+            const float4* arow = reinterpret_cast<const float4*>(sA + (s0 + m) * kPA + s0);
 #pragma unroll
-            for (int r = 0; r < 16; ++r) x[r] = (r == l) ? 1.f : 0.f;
-#pragma unroll
-            for (int r = 1; r < 16; ++r) {
-                const float* ar = sA + (s0 + r) * kPA + s0;
-                float acc[4] = {x[r], 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int m = 0; m < r; ++m) acc[m & 3] = fmaf(-ar[m], x[m], acc[m & 3]);
-                x[r] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+            for (int u = 0; u < 4; ++u) {
+                const float4 t = arow[u];
+                ar[4 * u] = t.x; ar[4 * u + 1] = t.y; ar[4 * u + 2] = t.z; ar[4 * u + 3] = t.w;
             }
+            float xa = (m == l) ? 1.f : 0.f, xb = (m == l + 1) ? 1.f : 0.f;
+            const int src = lane & 16;
 #pragma unroll
-            for (int r = 0; r < 16; ++r) sT[(s0 + r) * kPA + s0 + l] = x[r];
-            // T' of the diagonal block: column s0+l of TT, row s0+l of T'^T
-            const float bl = sBeta[s0 + l];
-#pragma unroll
-            for (int r = 0; r < 16; ++r) st_bf16(sm + O_TT + sw128_off(s0 + r, s0 + l), x[r] * bl);
-            uint32_t w[8];
-#pragma unroll
-            for (int r = 0; r < 8; ++r) w[r] = pack_bf16x2(x[2 * r] * bl, x[2 * r + 1] * bl);
-            *reinterpret_cast<uint4*>(sm + O_TTR + sw128_off(s0 + l, s0)) = make_uint4(w[0], w[1], w[2], w[3]);
-            *reinterpret_cast<uint4*>(sm + O_TTR + sw128_off(s0 + l, s0 + 8)) = make_uint4(w[4], w[5], w[6], w[7]);
-        } else {
+            for (int r = 0; r < 15; ++r) {  // A[m][r] = 0 for r >= m: rows <= r are unchanged
+                const float ya = __shfl_sync(0xffffffffu, xa, src + r);
+                const float yb = __shfl_sync(0xffffffffu, xb, src + r);
+                xa = fmaf(-ar[r], ya, xa);
+                xb = fmaf(-ar[r], yb, xb);
+            }
+            const int i = s0 + m, j = s0 + l;
+            *reinterpret_cast<float2*>(sT + i * kPA + j) = make_float2(tf32_round(xa), tf32_round(xb));
+            store_tprime_pair(sm, i, j, xa, xb, sBeta);
             // Zero the 16 x 16 blocks of T' above the diagonal (TT: column block
             // J > row block I) and below it in T'^T: 12 blocks x 16 rows x 2 chunks.
-            for (int e = tid - 64; e < 12 * 32; e += kPrepThreads - 64) {
-                const int blkid = e >> 5, rr = (e >> 1) & 15, half = e & 1;
+            if (tid < 12 * 32) {
+                const int blkid = tid >> 5, rr = (tid >> 1) & 15, hc = tid & 1;
                 const int bi = blkid % 6;
-                const int I = bi < 3 ? 0 : (bi < 5 ? 1 : 2);
-                const int J = bi < 3 ? bi + 1 : (bi < 5 ? bi - 1 : 3);
-                const int row = blkid < 6 ? 16 * I + rr : 16 * J + rr;
-                const int col = blkid < 6 ? 16 * J + 8 * half : 16 * I + 8 * half;
+                const int Ib = bi < 3 ? 0 : (bi < 5 ? 1 : 2);
+                const int Jb = bi < 3 ? bi + 1 : (bi < 5 ? bi - 1 : 3);
+                const int row = blkid < 6 ? 16 * Ib + rr : 16 * Jb + rr;
+                const int col = blkid < 6 ? 16 * Jb + 8 * hc : 16 * Ib + 8 * hc;
                 *reinterpret_cast<uint4*>(sm + (blkid < 6 ? O_TT : O_TTR) + sw128_off(row, col)) =
                     make_uint4(0u, 0u, 0u, 0u);
             }
         }
         __syncthreads();
         // Off-diagonal blocks with warp-level tf32 tensor-core products (fp32
-        // accumulation; the result is rounded to bf16 for MMA C anyway).  Each
-        // warp owns a column block of its products, so the two dependent
-        // products of a level need only a warp barrier between them.
+        // accumulation; T' is rounded to bf16 for MMA C anyway).
         const int g4 = lane >> 2, t4 = lane & 3;
         if (warp < 4) {
-            // 16 -> 32: in 32-block p, X = A_10 T_00, then T_10 = -T_11 X and T_01 = 0
-            const int pb = 32 * (warp >> 1), c0 = 8 * (warp & 1);
+            // 16 -> 32 in 32-block p, columns c0..c0+7: X = A_10 T_00 (T_00 lower
+            // triangular: k >= c0), then T_10 = -T_11 X.
+            const int pb = 32 * (warp >> 1), ct = warp & 1, c0 = 8 * ct;
+            float* x = sX + (warp >> 1) * 16 * kPX + c0;
             float d[4];
-            warp_mma_16x8(sA + (pb + 16) * kPA + pb, kPA, sT + pb * kPA + pb + c0, kPA, 16, d, lane);
-            float* x = sX + (warp >> 1) * 256;
-            x[g4 * 16 + c0 + 2 * t4] = d[0]; x[g4 * 16 + c0 + 2 * t4 + 1] = d[1];
-            x[(g4 + 8) * 16 + c0 + 2 * t4] = d[2]; x[(g4 + 8) * 16 + c0 + 2 * t4 + 1] = d[3];
+            warp_mma_16x8(sA + (pb + 16) * kPA + pb, kPA, sT + pb * kPA + pb + c0, kPA, ct, 2, d, lane);
+            store_tile_tf32(x, kPX, d, lane);
             __syncwarp();
-            warp_mma_16x8(sT + (pb + 16) * kPA + pb + 16, kPA, sX + (warp >> 1) * 256 + c0, 16, 16, d, lane);
-            float* t10 = sT + (pb + 16) * kPA + pb + c0;
-            t10[g4 * kPA + 2 * t4] = -d[0]; t10[g4 * kPA + 2 * t4 + 1] = -d[1];
-            t10[(g4 + 8) * kPA + 2 * t4] = -d[2]; t10[(g4 + 8) * kPA + 2 * t4 + 1] = -d[3];
-            store_tprime_pair(sm, pb + 16 + g4, pb + c0 + 2 * t4, -d[0], -d[1], sBeta);
-            store_tprime_pair(sm, pb + 24 + g4, pb + c0 + 2 * t4, -d[2], -d[3], sBeta);
-            float* t01 = sT + pb * kPA + pb + 16 + c0;
-            t01[g4 * kPA + 2 * t4] = 0.f; t01[g4 * kPA + 2 * t4 + 1] = 0.f;
-            t01[(g4 + 8) * kPA + 2 * t4] = 0.f; t01[(g4 + 8) * kPA + 2 * t4 + 1] = 0.f;
+            warp_mma_16x8(sT + (pb + 16) * kPA + pb + 16, kPA, x, kPX, 0, 2, d, lane);
+            d[0] = -d[0]; d[1] = -d[1]; d[2] = -d[2]; d[3] = -d[3];
+            store_tile_tf32(sT + (pb + 16) * kPA + pb + c0, kPA, d, lane);
+            store_tprime_pair(sm, pb + 16 + g4, pb + c0 + 2 * t4, d[0], d[1], sBeta);
+            store_tprime_pair(sm, pb + 24 + g4, pb + c0 + 2 * t4, d[2], d[3], sBeta);
         }
         __syncthreads();
-        if (warp < 4) {
-            // 32 -> 64: warp w owns columns c0..c0+7 of X = A[32:,:32] T[:32,:32]
-            // (both 16-row tiles) and then of T[32:,:32] = -T[32:,32:] X
-            const int c0 = 8 * warp;
-            float d0[4], d1[4];
-            warp_mma_16x8(sA + 32 * kPA, kPA, sT + c0, kPA, 32, d0, lane);
-            warp_mma_16x8(sA + 48 * kPA, kPA, sT + c0, kPA, 32, d1, lane);
-            float* x = sX + c0;
-            x[g4 * 33 + 2 * t4] = d0[0]; x[g4 * 33 + 2 * t4 + 1] = d0[1];
-            x[(g4 + 8) * 33 + 2 * t4] = d0[2]; x[(g4 + 8) * 33 + 2 * t4 + 1] = d0[3];
-            x[(g4 + 16) * 33 + 2 * t4] = d1[0]; x[(g4 + 16) * 33 + 2 * t4 + 1] = d1[1];
-            x[(g4 + 24) * 33 + 2 * t4] = d1[2]; x[(g4 + 24) * 33 + 2 * t4 + 1] = d1[3];
-            __syncwarp();
-            warp_mma_16x8(sT + 32 * kPA + 32, kPA, sX + c0, 33, 32, d0, lane);
-            warp_mma_16x8(sT + 48 * kPA + 32, kPA, sX + c0, 33, 32, d1, lane);
-            float* t = sT + 32 * kPA + c0;
-            t[g4 * kPA + 2 * t4] = -d0[0]; t[g4 * kPA + 2 * t4 + 1] = -d0[1];
-            t[(g4 + 8) * kPA + 2 * t4] = -d0[2]; t[(g4 + 8) * kPA + 2 * t4 + 1] = -d0[3];
-            t[(g4 + 16) * kPA + 2 * t4] = -d1[0]; t[(g4 + 16) * kPA + 2 * t4 + 1] = -d1[1];
-            t[(g4 + 24) * kPA + 2 * t4] = -d1[2]; t[(g4 + 24) * kPA + 2 * t4 + 1] = -d1[3];
-            store_tprime_pair(sm, 32 + g4, c0 + 2 * t4, -d0[0], -d0[1], sBeta);
-            store_tprime_pair(sm, 40 + g4, c0 + 2 * t4, -d0[2], -d0[3], sBeta);
-            store_tprime_pair(sm, 48 + g4, c0 + 2 * t4, -d1[0], -d1[1], sBeta);
-            store_tprime_pair(sm, 56 + g4, c0 + 2 * t4, -d1[2], -d1[3], sBeta);
+        if (warp < 8) {
+            // 32 -> 64, row tile rt (16 rows), columns c0..c0+7:
+            // X = A[32:, :32] T[:32, :32] (k >= c0), then T[32:, :32] = -T[32:, 32:] X
+            // (row tile rt of T[32:, 32:] is zero beyond k = 16 (rt + 1)).
+            const int rt = warp >> 2, ct = warp & 3, c0 = 8 * ct;
+            float d[4];
+            warp_mma_16x8(sA + (32 + 16 * rt) * kPA, kPA, sT + c0, kPA, ct, 4, d, lane);
+            store_tile_tf32(sX + 16 * rt * kPX + c0, kPX, d, lane);
+            named_bar_sync(1, 256);
+            warp_mma_16x8(sT + (32 + 16 * rt) * kPA + 32, kPA, sX + c0, kPX, 0, 2 * (rt + 1), d, lane);
+            const int r0 = 32 + 16 * rt + g4;
+            store_tprime_pair(sm, r0, c0 + 2 * t4, -d[0], -d[1], sBeta);
+            store_tprime_pair(sm, r0 + 8, c0 + 2 * t4, -d[2], -d[3], sBeta);
         }
         fence_proxy_async_smem();
         __syncthreads();
@@ -476,9 +489,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         if (!ok) break;
         if (qd < 2) {
             const int i = 32 * qd + lane;
-#pragma unroll
-            for (int cg = 0; cg < 2; ++cg) {
-                const int col = 32 * half + 16 * cg;
+            {
+                const int col = 16 * cq;
                 float v[16];
                 tmem_ld16(tmem_addr(tb, 32 * qd, TM_B + col), v);
 #pragma unroll
@@ -509,9 +521,10 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             // shared-memory images and stored with bulk copies.
             const int r = 32 * qd + lane, i = r & 63;
             const bool top = qd < 2;
+            const int half = cq >> 1;
 #pragma unroll 1
-            for (int cg = 0; cg < 8; ++cg) {
-                const int col = 16 * cg;
+            for (int cg = 0; cg < 4; ++cg) {
+                const int col = 64 * (cq & 1) + 16 * cg;
                 float v[16];
                 tmem_ld16(tmem_addr(tb, 32 * qd, TM_C + 128 * half + col), v);
                 if (half == 0) {
