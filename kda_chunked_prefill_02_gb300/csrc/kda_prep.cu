@@ -47,6 +47,10 @@ constexpr uint32_t O_IK = 16384;      // bf16 [64][128] k tile
 constexpr uint32_t O_IV = 32768;      // bf16 [64][128] v tile
 constexpr uint32_t O_IG = 49152;      // fp32 [64][128] g tile
 constexpr uint32_t kInBytes = 81920;
+// Once the gate phase has read the g tile, its space stages the record's Kt
+// image (16 KB, same bytes as in the record) and e^gam (512 B).
+constexpr uint32_t O_SKT = O_IG;
+constexpr uint32_t O_SEG = O_IG + 16384;
 constexpr uint32_t O_R = 81920;       // A operand R = [K ac ; Q ac]: 2 x (128 rows x 128 B)
 constexpr uint32_t O_Y = 114688;      // B operand [Yoff (96 rows) ; Yd (64 rows)]: 2 x (160 x 128 B)
 constexpr uint32_t kYBlock = 160 * 128;
@@ -79,6 +83,9 @@ constexpr uint32_t TM_A = 0, TM_DIAG = 96, TM_B = 192, TM_C = 0, TM_COLS = 256;
 
 __device__ __forceinline__ float2 ld_bf16x2(const uint8_t* p) {
     return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 __device__ __forceinline__ void st_u32(uint8_t* p, uint32_t v) {
     *reinterpret_cast<uint32_t*>(p) = v;
@@ -200,7 +207,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         const int len = ci.len;
         const int rec_next = rec + gridDim.x;
         const ChunkInfo cn = rec_next < nrec ? chunk_info(p, rec_next / p.H) : ChunkInfo{0, 0, 0, 0, 0};
-        ok = __syncthreads_and(mbar_wait(&bar_in, it & 1, nullptr));
+        // One thread waits on each mbarrier; the others wait at the CTA barrier.
+        ok = __syncthreads_and(tid == 0 ? mbar_wait(&bar_in, it & 1, nullptr) : true);
         if (!ok) break;
         pend_parity = -1;
         if (tid < 64) {
@@ -209,27 +217,28 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             reinterpret_cast<float*>(sm + O_BETA)[tid] = tid < len ? bval : 0.f;
         }
 
-        // ---- E1: p = exp(g) (masked past the chunk length), the suffix products
-        // z (exact) and zc (floored gate) inside the 8-token group, and the
-        // group's gate sums, exact and floored.
-        float p0[8], p1[8], z0[8], z1[8], zc0[8], zc1[8];
+        // Tokens past the chunk length (the tail of a sequence) read as zeros:
+        // k = q = v = 0 and g = 0 (no decay).
+        if (len < kChunk) {
+            for (int e = tid; e < (kChunk - len) * 80; e += kPrepThreads) {
+                const int row = len + e / 80, u = e % 80;
+                uint8_t* dst = u < 48 ? sm + (u >> 4) * 16384 + row * 256 + (u & 15) * 16
+                                      : sm + O_IG + row * 512 + (u - 48) * 16;
+                *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            __syncthreads();
+        }
+
+        // ---- E1: p = exp(g) and the 8-token group's gate sums, exact and floored.
+        float p0[8], p1[8];
         {
             float d0 = 0.f, d1 = 0.f, e0 = 0.f, e1 = 0.f;
 #pragma unroll
             for (int l = 0; l < 8; ++l) {
-                const int i = 8 * h8 + l;
-                float2 gv = *reinterpret_cast<const float2*>(sm + O_IG + i * 512 + c0 * 4);
-                if (i >= len) gv = make_float2(0.f, 0.f);
+                const float2 gv = *reinterpret_cast<const float2*>(sm + O_IG + (8 * h8 + l) * 512 + c0 * 4);
                 d0 += gv.x; d1 += gv.y;
                 e0 += fmaxf(gv.x, kGateFloor); e1 += fmaxf(gv.y, kGateFloor);
                 p0[l] = __expf(gv.x); p1[l] = __expf(gv.y);
-            }
-            float s0 = 1.f, s1 = 1.f, t0 = 1.f, t1 = 1.f;
-#pragma unroll
-            for (int l = 7; l >= 0; --l) {
-                z0[l] = s0; z1[l] = s1; zc0[l] = t0; zc1[l] = t1;
-                s0 *= p0[l]; s1 *= p1[l];
-                t0 *= fmaxf(p0[l], kPFloor); t1 *= fmaxf(p1[l], kPFloor);
             }
             float* tot = reinterpret_cast<float*>(sm + O_TOT);
             *reinterpret_cast<float2*>(tot + h8 * 128 + c0) = make_float2(d0, d1);
@@ -258,101 +267,125 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                 if (J < G) { pre0 += h0[2 * J] + h0[2 * J + 1]; pre1 += h1[2 * J] + h1[2 * J + 1]; }
                 if (J > G) { post0 += h0[2 * J] + h0[2 * J + 1]; post1 += h1[2 * J] + h1[2 * J + 1]; }
             }
-            // Factors that carry the running products across the two halves of block G:
-            // the second half starts from the first half's product, the first half's
-            // suffix products continue through the second half.
-            const float am0 = hf ? __expf(hA.x) : 1.f, am1 = hf ? __expf(hA.y) : 1.f;
-            const float acm0 = hf ? __expf(fA.x) : 1.f, acm1 = hf ? __expf(fA.y) : 1.f;
-            const float zm0 = hf ? 1.f : __expf(hB.x), zm1 = hf ? 1.f : __expf(hB.y);
-            const float zcm0 = hf ? 1.f : __expf(fB.x), zcm1 = hf ? 1.f : __expf(fB.y);
-            // 1 / (floored-gate block product) <= e^86.4, folded into the suffix factor
-            const float zci0 = zcm0 * __expf(-(fA.x + fB.x)), zci1 = zcm1 * __expf(-(fA.y + fB.y));
-            const float Bg0 = __expf(pre0), Bg1 = __expf(pre1);    // chunk start -> block start
-            const float zE0 = zm0 * __expf(post0), zE1 = zm1 * __expf(post1);  // -> chunk end
-            float zD0[4], zD1[4];  // decay over the blocks strictly between G and I
+            float Dm0[4], Dm1[4];  // decay over the blocks strictly between G and I
             {
                 float s0 = 0.f, s1 = 0.f;
 #pragma unroll
                 for (int I = 0; I < 4; ++I) {
-                    zD0[I] = zm0 * __expf(s0); zD1[I] = zm1 * __expf(s1);
+                    Dm0[I] = __expf(s0); Dm1[I] = __expf(s1);
                     if (I > G) { s0 += h0[2 * I] + h0[2 * I + 1]; s1 += h1[2 * I] + h1[2 * I + 1]; }
                 }
             }
-            uint8_t* rp = p.ws_rec + (size_t)rec * kRecBytes;
             if (h8 == 0) {
                 float t0 = 0.f, t1 = 0.f;
 #pragma unroll
                 for (int q = 0; q < 8; ++q) { t0 += h0[q]; t1 += h1[q]; }
-                *reinterpret_cast<float2*>(rp + kRecEg + c0 * 4) = make_float2(__expf(t0), __expf(t1));
+                *reinterpret_cast<float2*>(sm + O_SEG + c0 * 4) = make_float2(__expf(t0), __expf(t1));
             }
             const float qscale = p.scale;
             const uint32_t bo = blk * 16384u, yb = blk * kYBlock;
-            float a0 = am0, a1 = am1, ac0 = acm0, ac1 = acm1, eh0 = 0.f, eh1 = 0.f;
-            uint32_t kh0[4], kh1[4];
+            // Forward over the group: the running products a (exact gates, from the
+            // chunk start) and ac (floored gates, from the block start).  The second
+            // half of a block starts from the first half's product.
+            {
+                float a0 = __expf(pre0 + (hf ? hA.x : 0.f)), a1 = __expf(pre1 + (hf ? hA.y : 0.f));
+                float ac0 = hf ? __expf(fA.x) : 1.f, ac1 = hf ? __expf(fA.y) : 1.f;
+                uint32_t kw[8], qw[8], vw[8];
+                const uint8_t* in = sm + (8 * h8) * 256 + c0 * 2;
 #pragma unroll
-            for (int l = 0; l < 8; ++l) {
-                const int i = 8 * h8 + l;
-                const bool valid = i < len;
-                a0 *= p0[l]; a1 *= p1[l];
-                ac0 *= fmaxf(p0[l], kPFloor); ac1 *= fmaxf(p1[l], kPFloor);
-                float2 kk = ld_bf16x2(sm + O_IK + i * 256 + c0 * 2);
-                float2 qq = ld_bf16x2(sm + O_IQ + i * 256 + c0 * 2);
-                float2 vv = ld_bf16x2(sm + O_IV + i * 256 + c0 * 2);
-                if (!valid) { kk = make_float2(0.f, 0.f); qq = kk; vv = kk; }
-                qq.x *= qscale; qq.y *= qscale;
-                // R = [K ac ; Q ac]
-                st_u32(sm + O_R + bo + sw128_off(i, cc), pack_bf16x2(kk.x * ac0, kk.y * ac1));
-                st_u32(sm + O_R + bo + sw128_off(64 + i, cc), pack_bf16x2(qq.x * ac0, qq.y * ac1));
-                // Yd (diagonal blocks): K / ac = K zc / ac_block
-                const float kz0 = kk.x * z0[l], kz1 = kk.y * z1[l];
-                st_u32(sm + O_Y + yb + sw128_off(96 + i, cc),
-                       pack_bf16x2(kk.x * zc0[l] * zci0, kk.y * zc1[l] * zci1));
-                // Yoff: column block G seen from each later row block I
+                for (int l = 0; l < 8; ++l) {
+                    kw[l] = *reinterpret_cast<const uint32_t*>(in + O_IK + l * 256);
+                    qw[l] = *reinterpret_cast<const uint32_t*>(in + O_IQ + l * 256);
+                    vw[l] = *reinterpret_cast<const uint32_t*>(in + O_IV + l * 256);
+                }
 #pragma unroll
-                for (int I = 1; I < 4; ++I)
-                    if (I > G)
-                        st_u32(sm + O_Y + yb + sw128_off(yoff_row(I, G, 8 * hf + l), cc),
-                               pack_bf16x2(kz0 * zD0[I], kz1 * zD1[I]));
-                // Q e^Gam for Q', [K e^Gam | V] (MN-major: token row i, channels contiguous)
-                const float ea0 = a0 * Bg0, ea1 = a1 * Bg1;
-                st_u32(sm + O_QT + i * kQtPitch + c0 * 2, pack_bf16x2(qq.x * ea0, qq.y * ea1));
-                st_u32(sm + O_KV + mn_sw128_off(i, c0, kKvSbo), pack_bf16x2(kk.x * ea0, kk.y * ea1));
-                st_u32(sm + O_KV + mn_sw128_off(i, 128 + c0, kKvSbo), pack_bf16x2(vv.x, vv.y));
-                // Kt = (K e^{gam - Gam})^T, packed by token pairs
-                const float hh0 = kz0 * zE0, hh1 = kz1 * zE1;
-                if ((l & 1) == 0) {
-                    eh0 = hh0; eh1 = hh1;
-                } else {
-                    kh0[l >> 1] = pack_bf16x2(eh0, hh0);
-                    kh1[l >> 1] = pack_bf16x2(eh1, hh1);
+                for (int l = 0; l < 8; ++l) {
+                    const int i = 8 * h8 + l;
+                    a0 *= p0[l]; a1 *= p1[l];
+                    ac0 *= fmaxf(p0[l], kPFloor); ac1 *= fmaxf(p1[l], kPFloor);
+                    const float2 kk = bf16x2_to_float2(kw[l]);
+                    float2 qq = bf16x2_to_float2(qw[l]);
+                    qq.x *= qscale; qq.y *= qscale;
+                    // R = [K ac ; Q ac]
+                    st_u32(sm + O_R + bo + sw128_off(i, cc), pack_bf16x2(kk.x * ac0, kk.y * ac1));
+                    st_u32(sm + O_R + bo + sw128_off(64 + i, cc), pack_bf16x2(qq.x * ac0, qq.y * ac1));
+                    // Q e^Gam for Q', [K e^Gam | V] (MN-major: token row i, channels contiguous)
+                    st_u32(sm + O_QT + i * kQtPitch + c0 * 2, pack_bf16x2(qq.x * a0, qq.y * a1));
+                    st_u32(sm + O_KV + mn_sw128_off(i, c0, kKvSbo), pack_bf16x2(kk.x * a0, kk.y * a1));
+                    st_u32(sm + O_KV + mn_sw128_off(i, 128 + c0, kKvSbo), vw[l]);
                 }
             }
-            // Kt image rows c0, c0 + 1: tokens 8 h8 .. 8 h8 + 7 are 16-byte chunk h8
-            uint8_t* kt = rp + kRecKt;
-            *reinterpret_cast<uint4*>(kt + sw128_off(c0, 8 * h8)) = make_uint4(kh0[0], kh0[1], kh0[2], kh0[3]);
-            *reinterpret_cast<uint4*>(kt + sw128_off(c0 + 1, 8 * h8)) = make_uint4(kh1[0], kh1[1], kh1[2], kh1[3]);
+            // Backward over the group: the suffix products z (exact gates, to the block
+            // end) and zc (floored gates); the first half of a block continues through
+            // the second half.
+            {
+                float z0 = hf ? 1.f : __expf(hB.x), z1 = hf ? 1.f : __expf(hB.y);
+                // zc / (floored-gate block product) = 1 / ac: <= e^86.4
+                float zc0 = __expf((hf ? 0.f : fB.x) - (fA.x + fB.x));
+                float zc1 = __expf((hf ? 0.f : fB.y) - (fA.y + fB.y));
+                const float E0 = __expf(post0), E1 = __expf(post1);  // block end -> chunk end
+                float eh0 = 0.f, eh1 = 0.f;
+                uint32_t kh0[4], kh1[4], kw[8];
+#pragma unroll
+                for (int l = 0; l < 8; ++l)
+                    kw[l] = *reinterpret_cast<const uint32_t*>(sm + O_IK + (8 * h8 + l) * 256 + c0 * 2);
+#pragma unroll
+                for (int l = 7; l >= 0; --l) {
+                    const int i = 8 * h8 + l;
+                    const float2 kk = bf16x2_to_float2(kw[l]);
+                    // Yd (diagonal blocks): K / ac
+                    st_u32(sm + O_Y + yb + sw128_off(96 + i, cc), pack_bf16x2(kk.x * zc0, kk.y * zc1));
+                    // Yoff: column block G seen from each later row block I
+                    const float kz0 = kk.x * z0, kz1 = kk.y * z1;
+#pragma unroll
+                    for (int I = 1; I < 4; ++I)
+                        if (I > G)
+                            st_u32(sm + O_Y + yb + sw128_off(yoff_row(I, G, 8 * hf + l), cc),
+                                   pack_bf16x2(kz0 * Dm0[I], kz1 * Dm1[I]));
+                    // Kt = (K e^{gam - Gam})^T, packed by token pairs
+                    const float hh0 = kz0 * E0, hh1 = kz1 * E1;
+                    if (l & 1) {
+                        eh0 = hh0; eh1 = hh1;
+                    } else {
+                        kh0[l >> 1] = pack_bf16x2(hh0, eh0);
+                        kh1[l >> 1] = pack_bf16x2(hh1, eh1);
+                    }
+                    z0 *= p0[l]; z1 *= p1[l];
+                    zc0 *= fmaxf(p0[l], kPFloor); zc1 *= fmaxf(p1[l], kPFloor);
+                }
+                // Kt image rows c0, c0 + 1: tokens 8 h8 .. 8 h8 + 7 are 16-byte chunk h8
+                uint8_t* kt = sm + O_SKT;
+                *reinterpret_cast<uint4*>(kt + sw128_off(c0, 8 * h8)) = make_uint4(kh0[0], kh0[1], kh0[2], kh0[3]);
+                *reinterpret_cast<uint4*>(kt + sw128_off(c0 + 1, 8 * h8)) = make_uint4(kh1[0], kh1[1], kh1[2], kh1[3]);
+            }
         }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        // The input tiles are consumed: fetch the next record's while this one
-        // goes through the tensor cores and the solve.
-        if (tid == 0 && cn.len > 0) {
-            load_inputs(sm, maps, cn, rec_next % p.H, &bar_in);
-        }
-        if (cn.len > 0) bcur = load_beta(cn, rec_next % p.H);
-        if (cn.len > 0) pend_parity = (int)((it + 1) & 1);
-
-        // ---- MMA A: D = R [Yoff ; Yd]^T, N = 160 (off-diagonal and diagonal blocks)
         if (tid == 0) {
+            // ---- MMA A: D = R [Yoff ; Yd]^T, N = 160 (off-diagonal and diagonal blocks)
             umma_tile(tb + TM_A, smem_u32(sm + O_R), 16384, smem_u32(sm + O_Y), kYBlock, 128,
                       idesc_bf16_f32(128, 160), false);
             umma_commit(&bar_mma[0]);
+            // The Kt and e^gam images leave by bulk copy.
+            uint8_t* rp = p.ws_rec + (size_t)rec * kRecBytes;
+            bulk_store(rp + kRecKt, sm + O_SKT, 16384);
+            bulk_store(rp + kRecEg, sm + O_SEG, 512);
+            bulk_commit();
         }
-        ok = __syncthreads_and(mbar_wait(&bar_mma[0], it & 1, nullptr));
+        if (cn.len > 0) bcur = load_beta(cn, rec_next % p.H);
+        ok = __syncthreads_and(tid == 0 ? mbar_wait(&bar_mma[0], it & 1, nullptr) : true);
         tc_fence_after();
         if (!ok) break;
+        // Once the Kt image has been read out of the consumed gate tile, the input
+        // tiles are free: the next record's load while this one goes through the
+        // solve and the other two products.
+        if (tid == 0 && cn.len > 0) {
+            bulk_wait_read();
+            load_inputs(sm, maps, cn, rec_next % p.H, &bar_in);
+        }
+        if (cn.len > 0) pend_parity = (int)((it + 1) & 1);
 
         float* sA = reinterpret_cast<float*>(sm + O_A);
         float* sT = reinterpret_cast<float*>(sm + O_T);
@@ -484,7 +517,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                       idesc_bf16_f32(128, 64), false);
             umma_commit(&bar_mma[1]);
         }
-        ok = __syncthreads_and(mbar_wait(&bar_mma[1], it & 1, nullptr));
+        ok = __syncthreads_and(tid == 0 ? mbar_wait(&bar_mma[1], it & 1, nullptr) : true);
         tc_fence_after();
         if (!ok) break;
         if (qd < 2) {
@@ -512,7 +545,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                           idesc_bf16_f32_bmn(128, 256), k > 0 ? 1u : 0u);
             umma_commit(&bar_mma[2]);
         }
-        ok = __syncthreads_and(mbar_wait(&bar_mma[2], it & 1, nullptr));
+        ok = __syncthreads_and(tid == 0 ? mbar_wait(&bar_mma[2], it & 1, nullptr) : true);
         tc_fence_after();
         if (!ok) break;
         {
