@@ -58,7 +58,7 @@ constexpr uint32_t O_KV = 155648;     // B operand [K e^Gam | V], MN-major: 8 to
 constexpr uint32_t kKvSbo = 4096;     // byte distance between 8-token groups of the KV operand
 constexpr uint32_t O_QT = 188416;     // bf16 [64][136] Q e^Gam (row pitch 272 B)
 constexpr uint32_t kQtPitch = 272;
-constexpr uint32_t O_TOT = 205824;    // fp32 [2][8][128] gate sums (exact, floored) of 8-token groups
+constexpr uint32_t O_TOT = 205824;    // fp32 [2][8][128] decay products (exact, floored) of 8-token groups
 constexpr uint32_t O_BETA = 214016;   // fp32 [64] beta
 constexpr uint32_t kPrepSmem = 214272 + 1024;
 // Scratch of the solve and MMA B / C, over R and Y once MMA A has completed.
@@ -229,20 +229,22 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             __syncthreads();
         }
 
-        // ---- E1: p = exp(g) and the 8-token group's gate sums, exact and floored.
+        // ---- E1: p = exp(g) and the 8-token group's decay products, exact and
+        // with the floored gate.  Every decay factor below is a product of these,
+        // so the gate phase takes one exponential per element and no more.
         float p0[8], p1[8];
         {
-            float d0 = 0.f, d1 = 0.f, e0 = 0.f, e1 = 0.f;
+            float e0 = 1.f, e1 = 1.f, f0 = 1.f, f1 = 1.f;
 #pragma unroll
             for (int l = 0; l < 8; ++l) {
                 const float2 gv = *reinterpret_cast<const float2*>(sm + O_IG + (8 * h8 + l) * 512 + c0 * 4);
-                d0 += gv.x; d1 += gv.y;
-                e0 += fmaxf(gv.x, kGateFloor); e1 += fmaxf(gv.y, kGateFloor);
                 p0[l] = __expf(gv.x); p1[l] = __expf(gv.y);
+                e0 *= p0[l]; e1 *= p1[l];
+                f0 *= fmaxf(p0[l], kPFloor); f1 *= fmaxf(p1[l], kPFloor);
             }
             float* tot = reinterpret_cast<float*>(sm + O_TOT);
-            *reinterpret_cast<float2*>(tot + h8 * 128 + c0) = make_float2(d0, d1);
-            *reinterpret_cast<float2*>(tot + 1024 + h8 * 128 + c0) = make_float2(e0, e1);
+            *reinterpret_cast<float2*>(tot + h8 * 128 + c0) = make_float2(e0, e1);
+            *reinterpret_cast<float2*>(tot + 1024 + h8 * 128 + c0) = make_float2(f0, f1);
         }
         if (tid == 0) bulk_wait_read();  // the previous record's images have left the staging area
         __syncthreads();
@@ -250,46 +252,42 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         // ---- E2: the MMA operands and the records that need no MMA.
         {
             const float* tot = reinterpret_cast<const float*>(sm + O_TOT);
-            float h0[8], h1[8];  // exact gate sums of the eight 8-token groups
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float2 t = *reinterpret_cast<const float2*>(tot + q * 128 + c0);
-                h0[q] = t.x; h1[q] = t.y;
-            }
-            // exact (hA, hB) and floored (fA, fB) sums of block G's two halves
-            const float2 hA = *reinterpret_cast<const float2*>(tot + (2 * G) * 128 + c0);
-            const float2 hB = *reinterpret_cast<const float2*>(tot + (2 * G + 1) * 128 + c0);
-            const float2 fA = *reinterpret_cast<const float2*>(tot + 1024 + (2 * G) * 128 + c0);
-            const float2 fB = *reinterpret_cast<const float2*>(tot + 1024 + (2 * G + 1) * 128 + c0);
-            float pre0 = 0.f, pre1 = 0.f, post0 = 0.f, post1 = 0.f;
+            float b0[4], b1[4];  // exact decay of each 16-token block
 #pragma unroll
             for (int J = 0; J < 4; ++J) {
-                if (J < G) { pre0 += h0[2 * J] + h0[2 * J + 1]; pre1 += h1[2 * J] + h1[2 * J + 1]; }
-                if (J > G) { post0 += h0[2 * J] + h0[2 * J + 1]; post1 += h1[2 * J] + h1[2 * J + 1]; }
+                const float2 u = *reinterpret_cast<const float2*>(tot + (2 * J) * 128 + c0);
+                const float2 w = *reinterpret_cast<const float2*>(tot + (2 * J + 1) * 128 + c0);
+                b0[J] = u.x * w.x; b1[J] = u.y * w.y;
             }
-            float Dm0[4], Dm1[4];  // decay over the blocks strictly between G and I
+            // exact (eA, eB) and floored (fA, fB) decay of block G's two halves
+            const float2 eA = *reinterpret_cast<const float2*>(tot + (2 * G) * 128 + c0);
+            const float2 eB = *reinterpret_cast<const float2*>(tot + (2 * G + 1) * 128 + c0);
+            const float2 fA = *reinterpret_cast<const float2*>(tot + 1024 + (2 * G) * 128 + c0);
+            const float2 fB = *reinterpret_cast<const float2*>(tot + 1024 + (2 * G + 1) * 128 + c0);
+            // Bg: chunk start -> block start; E: block end -> chunk end;
+            // Dm[I]: the blocks strictly between G and I
+            float Bg0 = 1.f, Bg1 = 1.f, E0 = 1.f, E1 = 1.f, Dm0[4], Dm1[4];
             {
-                float s0 = 0.f, s1 = 0.f;
+                float d0 = 1.f, d1 = 1.f;
 #pragma unroll
-                for (int I = 0; I < 4; ++I) {
-                    Dm0[I] = __expf(s0); Dm1[I] = __expf(s1);
-                    if (I > G) { s0 += h0[2 * I] + h0[2 * I + 1]; s1 += h1[2 * I] + h1[2 * I + 1]; }
+                for (int J = 0; J < 4; ++J) {
+                    if (J < G) { Bg0 *= b0[J]; Bg1 *= b1[J]; }
+                    if (J > G) { E0 *= b0[J]; E1 *= b1[J]; }
+                    Dm0[J] = d0; Dm1[J] = d1;
+                    if (J > G) { d0 *= b0[J]; d1 *= b1[J]; }
                 }
             }
-            if (h8 == 0) {
-                float t0 = 0.f, t1 = 0.f;
-#pragma unroll
-                for (int q = 0; q < 8; ++q) { t0 += h0[q]; t1 += h1[q]; }
-                *reinterpret_cast<float2*>(sm + O_SEG + c0 * 4) = make_float2(__expf(t0), __expf(t1));
-            }
+            if (h8 == 0)
+                *reinterpret_cast<float2*>(sm + O_SEG + c0 * 4) =
+                    make_float2(b0[0] * b0[1] * b0[2] * b0[3], b1[0] * b1[1] * b1[2] * b1[3]);
             const float qscale = p.scale;
             const uint32_t bo = blk * 16384u, yb = blk * kYBlock;
             // Forward over the group: the running products a (exact gates, from the
             // chunk start) and ac (floored gates, from the block start).  The second
             // half of a block starts from the first half's product.
             {
-                float a0 = __expf(pre0 + (hf ? hA.x : 0.f)), a1 = __expf(pre1 + (hf ? hA.y : 0.f));
-                float ac0 = hf ? __expf(fA.x) : 1.f, ac1 = hf ? __expf(fA.y) : 1.f;
+                float a0 = hf ? Bg0 * eA.x : Bg0, a1 = hf ? Bg1 * eA.y : Bg1;
+                float ac0 = hf ? fA.x : 1.f, ac1 = hf ? fA.y : 1.f;
                 uint32_t kw[8], qw[8], vw[8];
                 const uint8_t* in = sm + (8 * h8) * 256 + c0 * 2;
 #pragma unroll
@@ -319,11 +317,10 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             // end) and zc (floored gates); the first half of a block continues through
             // the second half.
             {
-                float z0 = hf ? 1.f : __expf(hB.x), z1 = hf ? 1.f : __expf(hB.y);
-                // zc / (floored-gate block product) = 1 / ac: <= e^86.4
-                float zc0 = __expf((hf ? 0.f : fB.x) - (fA.x + fB.x));
-                float zc1 = __expf((hf ? 0.f : fB.y) - (fA.y + fB.y));
-                const float E0 = __expf(post0), E1 = __expf(post1);  // block end -> chunk end
+                float z0 = hf ? 1.f : eB.x, z1 = hf ? 1.f : eB.y;
+                // zc / (floored-gate block product) = 1 / ac: at most e^86.4, since
+                // each floored factor is at least e^-5.4
+                float zc0 = __frcp_rn(hf ? fA.x * fB.x : fA.x), zc1 = __frcp_rn(hf ? fA.y * fB.y : fA.y);
                 float eh0 = 0.f, eh1 = 0.f;
                 uint32_t kh0[4], kh1[4], kw[8];
 #pragma unroll

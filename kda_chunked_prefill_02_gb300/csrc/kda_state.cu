@@ -23,7 +23,8 @@
 // barrier before TMEM is freed (the dealloc ordering of the TensorRT-LLM
 // MQA-logits page).  All mbarrier waits are bounded; a wait that runs out sets
 // KDA_ERR_TIMEOUT, and every epilogue warp still reaches the named barriers of
-// that chunk before all of them stop together.
+// that chunk; the chunk barrier's OR-reduction of the abort flag makes all of
+// them stop at the same chunk.
 #include "kda_internal.h"
 #include "sm103.cuh"
 
@@ -39,6 +40,7 @@ constexpr uint32_t ST_EG = 57344;      // e^gam [128] fp32
 constexpr uint32_t kStage = 58368;
 constexpr uint32_t kStageTx = 32768 + 16384 + kSlabImg * 2 + 512;
 constexpr int kStages = 3;
+constexpr int kPrefetchAhead = 6;      // chunks between an L2 prefetch and its record's bulk copy
 // B operands of P1 and P2, MN-major with the 128-byte swizzle: one 128-byte
 // row per K index (key for S, token for V_new) holding the slab's 32 columns,
 // 8-row groups 1024 B apart, so each thread stores its own row.
@@ -58,7 +60,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-    __shared__ uint64_t full[kStages], empty[kStages], p1_done, p2_done;
+    __shared__ uint64_t full[kStages], empty[kStages], p1_done, p2_done, bar_fin;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
 
@@ -83,7 +85,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 2);
         }
-        mbar_init(&p1_done, 1); mbar_init(&p2_done, 1);
+        mbar_init(&p1_done, 1); mbar_init(&p2_done, 1); mbar_init(&bar_fin, 1);
         abort_flag = 0;
         fence_mbar_init();
     }
@@ -116,6 +118,11 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
                 bulk_load(sb + ST_OL, rp + kRecOl + slab * kSlabImg, kSlabImg, &full[st]);
                 bulk_load(sb + ST_EG, rp + kRecEg, 512, &full[st]);
                 issued = c + 1;
+                // Records further ahead are pulled into L2 so that their bulk copies,
+                // issued once a stage frees up, do not wait on HBM.
+                if (c + kPrefetchAhead < count)
+                    bulk_prefetch_l2(p.ws_rec + (size_t)((first + c + kPrefetchAhead) * p.H + h) * kRecBytes,
+                                     kRecBytes);
             }
             // Never leave the CTA with copies in flight: wait (bounded) for the
             // last stages issued.  In a normal run these phases completed long ago.
@@ -158,7 +165,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
             tc_fence_before();
         };
         write_state_image();
-        named_bar_sync(kBarChunk, 128);
+        named_bar_or(kBarChunk, 128, false);
 
         for (int c = 0; c < count; ++c) {
             const int st = c % kStages;
@@ -177,6 +184,15 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
                               bd + k * ((2 * kRowGroup) >> 4), id, k > 0 ? 1u : 0u);
                 umma_commit(&p1_done);
             }
+            // This thread's U (W rows) or O_loc (Q' rows) slab row, read while P1 runs.
+            uint4 slab_row[4];
+            {
+                const uint8_t* src = sb + (qd < 2 ? ST_U : ST_OL);
+                const int r = qd < 2 ? row : row - 64;
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch)
+                    slab_row[ch] = *reinterpret_cast<const uint4*>(src + slab_chunk_off(r, ch));
+            }
             ok = ok && warp_wait(&p1_done, c & 1, abort);
             tc_fence_after();
             float d[kSlab];
@@ -190,7 +206,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
                     float vn[kSlab];
 #pragma unroll
                     for (int ch = 0; ch < 4; ++ch) {
-                        const uint4 u = *reinterpret_cast<const uint4*>(sb + ST_U + slab_chunk_off(row, ch));
+                        const uint4 u = slab_row[ch];
                         const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
                         for (int x = 0; x < 4; ++x) {
@@ -223,7 +239,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
                     uint32_t o[kSlab / 2];
 #pragma unroll
                     for (int ch = 0; ch < 4; ++ch) {
-                        const uint4 ol = *reinterpret_cast<const uint4*>(sb + ST_OL + slab_chunk_off(i, ch));
+                        const uint4 ol = slab_row[ch];
                         const uint32_t ow[4] = {ol.x, ol.y, ol.z, ol.w};
 #pragma unroll
                         for (int x = 0; x < 4; ++x) {
@@ -251,9 +267,15 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
             } else {
                 fail();
             }
-            named_bar_sync(kBarChunk, 128);
-            if (*abort) break;
+            // Every epilogue thread takes the same decision: the fetcher warp may set
+            // the abort flag at any time, so it is reduced over the barrier.
+            if (named_bar_or(kBarChunk, 128, *abort != 0)) break;
             if (issuer) mbar_arrive(&empty[st]);
+        }
+        if (issuer && count > 0) {
+            // every product issued has completed before TMEM is released
+            umma_commit(&bar_fin);
+            mbar_wait(&bar_fin, 0, nullptr);
         }
         if (!*abort && p.hT) {
             float4* dst = reinterpret_cast<float4*>(p.hT + st_off);

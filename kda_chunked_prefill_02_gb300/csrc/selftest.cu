@@ -205,7 +205,153 @@ __global__ void __launch_bounds__(128)
     if (warp == 0) tmem_dealloc(tmem_base, 32);
 }
 
+// D = A B^T with A (128 x 128) held in TMEM (written by the threads with
+// tcgen05.st, row m in lane m) and B (N x 128) K-major SW128 in shared memory.
+__global__ void __launch_bounds__(128)
+    umma_tmem_a_selftest_kernel(const __nv_bfloat16* __restrict__ A, const __nv_bfloat16* __restrict__ B,
+                                float* __restrict__ D, int N, int* status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sB = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+    __shared__ uint64_t bar_mma;
+    __shared__ uint32_t tmem_base;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    constexpr uint32_t kACol = 256;  // A occupies columns 256..319, D columns 0..N-1
+    if (tid == 0) {
+        mbar_init(&bar_mma, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_base, 512);
+        tmem_relinquish();
+    }
+    for (int i = tid; i < N * 128; i += 128) {
+        const int r = i >> 7, c = i & 127;
+        *reinterpret_cast<__nv_bfloat16*>(sB + (c >> 6) * (N * 128) + sw128_off(r, c & 63)) = B[i];
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = tmem_base;
+    {
+        const int row = warp * 32 + lane;
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(A + row * 128);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t w[16];
+#pragma unroll
+            for (int x = 0; x < 16; ++x) w[x] = src[16 * j + x];
+            tmem_st16(tmem_addr(tb, warp * 32, kACol + 16 * j), w);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {
+        const uint64_t bd = sdesc_kmajor_sw128(smem_u32(sB));
+        const uint32_t id = idesc_bf16_f32(128, N);
+        for (uint32_t k = 0; k < 8; ++k)
+            umma_bf16_ta(tb, tb + kACol + 8 * k, bd + (k >> 2) * ((uint32_t)(N * 128) >> 4) + (k & 3) * 2, id,
+                         k > 0 ? 1u : 0u);
+        umma_commit(&bar_mma);
+    }
+    const bool ok = mbar_wait(&bar_mma, 0, nullptr);
+    if (!ok) atomicExch(status, 4);
+    tc_fence_after();
+    if (ok) {
+        for (int c0 = 0; c0 < N; c0 += 16) {
+            float v[16];
+            tmem_ld16(tmem_addr(tb, warp * 32, c0), v);
+            const int row = warp * 32 + lane;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) D[row * N + c0 + i] = v[i];
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tb, 512);
+}
+
+// Throughput of back-to-back MMAs of one shape (operands are zeros: only the
+// time matters).  mode: 0 A smem / B MN-major SW128 N=32; 1 A TMEM / B MN-major
+// SW128 N=32; 2 A smem / B MN-major SW128 N=128 with 64-column atoms 16 KB
+// apart; 3 A smem / B MN-major SW64 N=32; 4 A smem / B K-major N=256;
+// 5 A smem / B K-major N=32; 6 A smem / B MN-major SW128 N=64; 7 as 5 with D
+// alternating between two TMEM tiles; 8 as 5 with M = 64; 9 as 5 with N = 16.
+__global__ void __launch_bounds__(128)
+    mma_rate_kernel(int mode, int reps, long long* cycles, int* status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+    __shared__ uint64_t bar;
+    __shared__ uint32_t tmem_base;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    for (int i = tid; i < 49152 / 16; i += 128) reinterpret_cast<uint4*>(sm)[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = tmem_base;
+    if (tid == 0) {
+        const uint32_t a = smem_u32(sm), bsm = smem_u32(sm + 16384);
+        const uint64_t ad = sdesc_kmajor_sw128(a);
+        uint64_t bd;
+        uint32_t id;
+        switch (mode) {
+            case 0: case 1: bd = sdesc_mnmajor_sw128(bsm, 1024u, 1024u); id = idesc_bf16_f32_bmn(128, 32); break;
+            case 2: bd = sdesc_mnmajor_sw128(bsm, 16384u, 1024u); id = idesc_bf16_f32_bmn(128, 128); break;
+            case 3: bd = sdesc_mnmajor_sw64(bsm, 512u, 512u); id = idesc_bf16_f32_bmn(128, 32); break;
+            case 4: bd = sdesc_kmajor_sw128(bsm); id = idesc_bf16_f32(128, 256); break;
+            case 5: bd = sdesc_kmajor_sw128(bsm); id = idesc_bf16_f32(128, 32); break;
+            case 6: bd = sdesc_mnmajor_sw128(bsm, 1024u, 2048u); id = idesc_bf16_f32_bmn(128, 64); break;
+            case 8: bd = sdesc_kmajor_sw128(bsm); id = idesc_bf16_f32(64, 32); break;
+            case 9: bd = sdesc_kmajor_sw128(bsm); id = idesc_bf16_f32(128, 16); break;
+            default: bd = sdesc_kmajor_sw128(bsm); id = idesc_bf16_f32(128, 32); break;
+        }
+        tc_fence_after();
+        const long long t0 = clock64();
+        for (int r = 0; r < reps; ++r) {
+            if (mode == 1) umma_bf16_ta(tb, tb + 256, bd, id, r > 0 ? 1u : 0u);
+            else if (mode == 7) umma_bf16(tb + 64 * (r & 1), ad, bd, id, r > 1 ? 1u : 0u);
+            else umma_bf16(tb, ad, bd, id, r > 0 ? 1u : 0u);
+        }
+        const long long t1 = clock64();
+        umma_commit(&bar);
+        const bool ok = mbar_wait(&bar, 0, nullptr);
+        const long long t2 = clock64();
+        if (!ok) atomicExch(status, 4);
+        cycles[0] = t1 - t0;  // issue
+        cycles[1] = t2 - t0;  // issue + completion
+    } else if (warp == 0) {
+        // nothing: warp 0's other lanes wait at the barrier
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tb, 512);
+}
+
 }  // namespace
+
+extern "C" int kda_selftest_umma_tmem_a(const void* A, const void* B, float* D, int N, int* status,
+                                        void* stream) {
+    if (N < 16 || N > 256 || (N % 16) != 0) return 1;
+    const size_t smem = 1024 + 2 * (size_t)N * 128;
+    if (cudaFuncSetAttribute(umma_tmem_a_selftest_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+        return 3;
+    umma_tmem_a_selftest_kernel<<<1, 128, smem, (cudaStream_t)stream>>>(
+        (const __nv_bfloat16*)A, (const __nv_bfloat16*)B, D, N, status);
+    return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
 
 extern "C" int kda_selftest_umma_mn64(const void* A, const void* B, float* D, int* status,
                                       void* stream) {
@@ -250,5 +396,15 @@ extern "C" int kda_selftest_umma(const void* A, const void* B, float* D, int N, 
         return 3;
     umma_selftest_kernel<<<1, 128, smem, (cudaStream_t)stream>>>(
         (const __nv_bfloat16*)A, (const __nv_bfloat16*)B, D, N, use_tma, ma, mb, status);
+    return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
+
+extern "C" int kda_selftest_mma_rate(int mode, int reps, long long* cycles, int* status, void* stream) {
+    if (mode < 0 || mode > 9 || reps < 1 || reps > 4096) return 1;
+    const size_t smem = 1024 + 49152;
+    if (cudaFuncSetAttribute(mma_rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+        return 3;
+    mma_rate_kernel<<<1, 128, smem, (cudaStream_t)stream>>>(mode, reps, cycles, status);
     return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }

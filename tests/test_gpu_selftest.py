@@ -72,3 +72,38 @@ def test_umma_tile_b_mn_major_sw64(selftest):
     torch.cuda.synchronize()
     assert status.item() == 0
     torch.testing.assert_close(D, A.float() @ B.float().T, atol=2e-3, rtol=1e-4)
+
+
+@pytest.mark.parametrize("N", [32, 128])
+def test_umma_tile_a_from_tmem(selftest, N):
+    """A operand (128 x 128 bf16) read by the MMA from TMEM, packed two bf16 per
+    32-bit column (row m in lane m), B K-major SW128 in shared memory."""
+    f = selftest.kda_selftest_umma_tmem_a
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] + [ctypes.c_void_p] * 2
+    g = torch.Generator(device="cpu").manual_seed(300 + N)
+    A = torch.randn(128, 128, generator=g).to(torch.bfloat16).cuda()
+    B = torch.randn(N, 128, generator=g).to(torch.bfloat16).cuda()
+    D = torch.full((128, N), float("nan"), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert f(A.data_ptr(), B.data_ptr(), D.data_ptr(), N, status.data_ptr(),
+             torch.cuda.current_stream().cuda_stream) == 0
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    torch.testing.assert_close(D, A.float() @ B.float().T, atol=2e-3, rtol=1e-4)
+
+
+def test_mma_rate_probe_runs(selftest):
+    """The MMA throughput probe (back-to-back tcgen05.mma of one shape, timed
+    with clock64 on the issuing thread) completes and reports a positive time."""
+    f = selftest.kda_selftest_mma_rate
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    cyc = torch.zeros(2, dtype=torch.int64, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for mode in (0, 4):
+        assert f(mode, 8, cyc.data_ptr(), status.data_ptr(), torch.cuda.current_stream().cuda_stream) == 0
+        torch.cuda.synchronize()
+        assert status.item() == 0
+        issue, total = cyc.tolist()
+        assert 0 < issue <= total
