@@ -316,7 +316,7 @@ def run_e2e(r, args, ws):
 def cpu_baseline(inp, target_s=15.0):
     """The oracle, as it stands, on a bounded prefix sample of the workload."""
     tok, sec, used = cpu_oracle_sample(inp, 256)
-    m = int(256 * max(1.0, min(64.0, target_s / max(sec, 1e-3))))
+    m = int(256 * max(1.0, min(1024.0, target_s / max(sec, 1e-3))))
     m = min(m, max(inp.lengths))
     tok, sec, used = cpu_oracle_sample(inp, m)
     return {"value": tok / sec, "unit": "tokens/s", "cores": used, "kind": "oracle",
@@ -371,9 +371,9 @@ def main_reference(args):
     if rank != 0:
         return
     inp = workload(args.config)
-    sample = 256
+    sample = 2048  # tokens of every sequence per step: about 0.15 s of oracle work on 16 cores
     for _ in range(args.warmup):
-        cpu_oracle_sample(inp, 16)
+        cpu_oracle_sample(inp, 64)
     times, tok, used = [], 0, 1
     for _ in range(args.steps):
         tok, sec, used = cpu_oracle_sample(inp, sample)
