@@ -9,7 +9,9 @@
 // the drafts sequentially on CUDA cores with the state column of each thread
 // in registers, which also yields the per-draft outputs directly.
 //
-// Layout: one CTA per (head, request), 256 threads; lanes 2m and 2m+1 of a warp
+// Layout: one CTA per (head, request), 256 threads; the drafts' q, k, e^g, v
+// and beta are staged in shared memory in the same pass as the state load;
+// lanes 2m and 2m+1 of a warp
 // own value column j = 16*warp + m, split over key rows [0,64) and [64,128), so
 // the reductions over key channels (S^T k, S^T q) are 64 in-thread FMAs plus one
 // lane-pair shuffle, and every pool row is read and written in 64-byte runs.
@@ -19,16 +21,20 @@ namespace kda {
 namespace {
 
 constexpr int kRows = kHeadDim / 2;
+constexpr int kMaxDrafts = 16;
 
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 2)
     verify_kernel(const VerifyParams p) {
     const int h = blockIdx.x, r = blockIdx.y, tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int j = 16 * warp + (lane >> 1), half = lane & 1, r0 = half * kRows;
-    __shared__ __align__(16) float s_k[kHeadDim];
-    __shared__ __align__(16) float s_q[kHeadDim];
-    __shared__ __align__(16) float s_e[kHeadDim];
-    __shared__ float s_beta;
+    // Every draft's inputs, loaded once together with the state so that the
+    // request pays one memory latency, not one per draft.
+    __shared__ __align__(16) float s_k[kMaxDrafts][kHeadDim];
+    __shared__ __align__(16) float s_q[kMaxDrafts][kHeadDim];
+    __shared__ __align__(16) float s_e[kMaxDrafts][kHeadDim];
+    __shared__ __align__(16) float s_v[kMaxDrafts][kHeadDim];
+    __shared__ float s_beta[kMaxDrafts];
 
     const int slot = p.slot ? p.slot[r] : r;
     const int acc = p.accepted[r];
@@ -40,29 +46,26 @@ __global__ void __launch_bounds__(256)
     float S[kRows];
 #pragma unroll
     for (int c = 0; c < kRows; ++c) S[c] = st[(r0 + c) * kHeadDim + j];
+    for (int e = tid; e < p.D * kHeadDim; e += blockDim.x) {
+        const int t = e >> 7, i = e & (kHeadDim - 1);
+        s_q[t][i] = __bfloat162float(p.q[r * p.qs[0] + t * p.qs[1] + h * p.qs[2] + i]) * p.scale;
+        s_k[t][i] = __bfloat162float(p.k[r * p.ks[0] + t * p.ks[1] + h * p.ks[2] + i]);
+        s_e[t][i] = __expf(p.g[r * p.gs[0] + t * p.gs[1] + h * p.gs[2] + i]);
+        s_v[t][i] = __bfloat162float(p.v[r * p.vs[0] + t * p.vs[1] + h * p.vs[2] + i]);
+    }
+    if (tid < p.D) {
+        const float bb = p.beta[r * p.bs[0] + tid * p.bs[1] + h * p.bs[2]];
+        s_beta[tid] = p.beta_is_logit ? 1.0f / (1.0f + __expf(-bb)) : bb;
+    }
+    __syncthreads();
 
     for (int t = 0; t < p.D; ++t) {
-        __syncthreads();  // the previous token's readers of s_k / s_q / s_e are done
-        if (tid < kHeadDim) {
-            const int64_t qo = r * p.qs[0] + t * p.qs[1] + h * p.qs[2];
-            const int64_t ko = r * p.ks[0] + t * p.ks[1] + h * p.ks[2];
-            const int64_t go = r * p.gs[0] + t * p.gs[1] + h * p.gs[2];
-            s_q[tid] = __bfloat162float(p.q[qo + tid]) * p.scale;
-            s_k[tid] = __bfloat162float(p.k[ko + tid]);
-            s_e[tid] = __expf(p.g[go + tid]);
-        }
-        if (tid == 0) {
-            const float b = p.beta[r * p.bs[0] + t * p.bs[1] + h * p.bs[2]];
-            s_beta = p.beta_is_logit ? 1.0f / (1.0f + __expf(-b)) : b;
-        }
-        const float vj = __bfloat162float(p.v[r * p.vs[0] + t * p.vs[1] + h * p.vs[2] + j]);
-        __syncthreads();
         // decay, then u = v - S^T k (four partial sums, then the lane pair)
         float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
         for (int c = 0; c < kRows; c += 4) {
-            const float4 e = *reinterpret_cast<const float4*>(&s_e[r0 + c]);
-            const float4 kk = *reinterpret_cast<const float4*>(&s_k[r0 + c]);
+            const float4 e = *reinterpret_cast<const float4*>(&s_e[t][r0 + c]);
+            const float4 kk = *reinterpret_cast<const float4*>(&s_k[t][r0 + c]);
             S[c] *= e.x; S[c + 1] *= e.y; S[c + 2] *= e.z; S[c + 3] *= e.w;
             a0 = fmaf(S[c], kk.x, a0);
             a1 = fmaf(S[c + 1], kk.y, a1);
@@ -71,12 +74,12 @@ __global__ void __launch_bounds__(256)
         }
         float sk = (a0 + a1) + (a2 + a3);
         sk += __shfl_xor_sync(0xffffffffu, sk, 1);
-        const float bu = s_beta * (vj - sk);
+        const float bu = s_beta[t] * (s_v[t][j] - sk);
         float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
 #pragma unroll
         for (int c = 0; c < kRows; c += 4) {
-            const float4 kk = *reinterpret_cast<const float4*>(&s_k[r0 + c]);
-            const float4 qq = *reinterpret_cast<const float4*>(&s_q[r0 + c]);
+            const float4 kk = *reinterpret_cast<const float4*>(&s_k[t][r0 + c]);
+            const float4 qq = *reinterpret_cast<const float4*>(&s_q[t][r0 + c]);
             S[c] = fmaf(kk.x, bu, S[c]);
             S[c + 1] = fmaf(kk.y, bu, S[c + 1]);
             S[c + 2] = fmaf(kk.z, bu, S[c + 2]);
