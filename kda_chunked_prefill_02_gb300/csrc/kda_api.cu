@@ -199,6 +199,8 @@ kda_status kda_verify(const kda_verify_args* a, void* stream) {
     for (int t = 0; t < 6; ++t)
         for (int i = 0; i < 3; ++i)
             if (ss[t][i] < 0) return KDA_ERR_UNSUPPORTED;
+    // The state is read and written in 16-byte vectors.
+    if (reinterpret_cast<uintptr_t>(a->state_pool) & 15) return KDA_ERR_UNSUPPORTED;
     VerifyParams p;
     memset(&p, 0, sizeof(p));
     p.q = static_cast<const __nv_bfloat16*>(a->q);

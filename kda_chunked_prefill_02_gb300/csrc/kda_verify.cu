@@ -9,30 +9,33 @@
 // the drafts sequentially on CUDA cores with the state column of each thread
 // in registers, which also yields the per-draft outputs directly.
 //
-// Layout: one CTA per (head, request), 256 threads; the drafts' q, k, e^g, v
-// and beta are staged in shared memory in the same pass as the state load;
-// lanes 2m and 2m+1 of a warp
-// own value column j = 16*warp + m, split over key rows [0,64) and [64,128), so
-// the reductions over key channels (S^T k, S^T q) are 64 in-thread FMAs plus one
-// lane-pair shuffle, and every pool row is read and written in 64-byte runs.
+// Layout: one CTA per (head, request), 256 threads.  Every draft's q, k, e^g,
+// v and beta are staged in shared memory in the same pass as the state load.
+// Thread (row group rg = lane & 7, column group cg = 4*warp + lane / 8) owns the
+// 16 x 4 block of the state at key rows 16*rg.., value columns 4*cg..: each
+// staged key-channel value it reads from shared memory serves four columns,
+// and the reductions over key channels (S^T k, S^T q) are 16 in-thread FMAs per
+// column plus three shuffle levels over the row groups of the warp.  The
+// staged rows are padded by 16 bytes every 16 floats, so the eight row groups
+// of a warp read eight different bank quads.
 #include "kda_internal.h"
 
 namespace kda {
 namespace {
 
-constexpr int kRows = kHeadDim / 2;
 constexpr int kMaxDrafts = 16;
+constexpr int kPadRow = kHeadDim + kHeadDim / 4;   // 160 floats: 16 B of padding per 16 floats
+__device__ __forceinline__ int padded(int i) { return i + (i >> 4) * 4; }
 
 __global__ void __launch_bounds__(256, 2)
     verify_kernel(const VerifyParams p) {
     const int h = blockIdx.x, r = blockIdx.y, tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int j = 16 * warp + (lane >> 1), half = lane & 1, r0 = half * kRows;
-    // Every draft's inputs, loaded once together with the state so that the
-    // request pays one memory latency, not one per draft.
-    __shared__ __align__(16) float s_k[kMaxDrafts][kHeadDim];
-    __shared__ __align__(16) float s_q[kMaxDrafts][kHeadDim];
-    __shared__ __align__(16) float s_e[kMaxDrafts][kHeadDim];
+    const int rg = lane & 7, cg = 4 * warp + (lane >> 3);
+    const int row0 = 16 * rg, col0 = 4 * cg;
+    __shared__ __align__(16) float s_e[kMaxDrafts][kPadRow];
+    __shared__ __align__(16) float s_k[kMaxDrafts][kPadRow];
+    __shared__ __align__(16) float s_q[kMaxDrafts][kPadRow];
     __shared__ __align__(16) float s_v[kMaxDrafts][kHeadDim];
     __shared__ float s_beta[kMaxDrafts];
 
@@ -43,14 +46,17 @@ __global__ void __launch_bounds__(256, 2)
         return;
     }
     float* st = p.pool + ((int64_t)slot * p.H + h) * (kHeadDim * kHeadDim);
-    float S[kRows];
+    float S[16][4];
 #pragma unroll
-    for (int c = 0; c < kRows; ++c) S[c] = st[(r0 + c) * kHeadDim + j];
+    for (int i = 0; i < 16; ++i) {
+        const float4 x = *reinterpret_cast<const float4*>(st + (row0 + i) * kHeadDim + col0);
+        S[i][0] = x.x; S[i][1] = x.y; S[i][2] = x.z; S[i][3] = x.w;
+    }
     for (int e = tid; e < p.D * kHeadDim; e += blockDim.x) {
-        const int t = e >> 7, i = e & (kHeadDim - 1);
-        s_q[t][i] = __bfloat162float(p.q[r * p.qs[0] + t * p.qs[1] + h * p.qs[2] + i]) * p.scale;
-        s_k[t][i] = __bfloat162float(p.k[r * p.ks[0] + t * p.ks[1] + h * p.ks[2] + i]);
-        s_e[t][i] = __expf(p.g[r * p.gs[0] + t * p.gs[1] + h * p.gs[2] + i]);
+        const int t = e >> 7, i = e & (kHeadDim - 1), pi = padded(i);
+        s_q[t][pi] = __bfloat162float(p.q[r * p.qs[0] + t * p.qs[1] + h * p.qs[2] + i]) * p.scale;
+        s_k[t][pi] = __bfloat162float(p.k[r * p.ks[0] + t * p.ks[1] + h * p.ks[2] + i]);
+        s_e[t][pi] = __expf(p.g[r * p.gs[0] + t * p.gs[1] + h * p.gs[2] + i]);
         s_v[t][i] = __bfloat162float(p.v[r * p.vs[0] + t * p.vs[1] + h * p.vs[2] + i]);
     }
     if (tid < p.D) {
@@ -59,42 +65,62 @@ __global__ void __launch_bounds__(256, 2)
     }
     __syncthreads();
 
+    const int prow = padded(row0);  // the 16 rows of a group are contiguous after padding
     for (int t = 0; t < p.D; ++t) {
-        // decay, then u = v - S^T k (four partial sums, then the lane pair)
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        float kk[16], x[16];
 #pragma unroll
-        for (int c = 0; c < kRows; c += 4) {
-            const float4 e = *reinterpret_cast<const float4*>(&s_e[t][r0 + c]);
-            const float4 kk = *reinterpret_cast<const float4*>(&s_k[t][r0 + c]);
-            S[c] *= e.x; S[c + 1] *= e.y; S[c + 2] *= e.z; S[c + 3] *= e.w;
-            a0 = fmaf(S[c], kk.x, a0);
-            a1 = fmaf(S[c + 1], kk.y, a1);
-            a2 = fmaf(S[c + 2], kk.z, a2);
-            a3 = fmaf(S[c + 3], kk.w, a3);
+        for (int i = 0; i < 16; i += 4) {
+            const float4 e4 = *reinterpret_cast<const float4*>(&s_e[t][prow + i]);
+            const float4 k4 = *reinterpret_cast<const float4*>(&s_k[t][prow + i]);
+            x[i] = e4.x; x[i + 1] = e4.y; x[i + 2] = e4.z; x[i + 3] = e4.w;
+            kk[i] = k4.x; kk[i + 1] = k4.y; kk[i + 2] = k4.z; kk[i + 3] = k4.w;
         }
-        float sk = (a0 + a1) + (a2 + a3);
-        sk += __shfl_xor_sync(0xffffffffu, sk, 1);
-        const float bu = s_beta[t] * (s_v[t][j] - sk);
-        float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+        // decay, then u = v - S^T k
+        float sk[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < kRows; c += 4) {
-            const float4 kk = *reinterpret_cast<const float4*>(&s_k[t][r0 + c]);
-            const float4 qq = *reinterpret_cast<const float4*>(&s_q[t][r0 + c]);
-            S[c] = fmaf(kk.x, bu, S[c]);
-            S[c + 1] = fmaf(kk.y, bu, S[c + 1]);
-            S[c + 2] = fmaf(kk.z, bu, S[c + 2]);
-            S[c + 3] = fmaf(kk.w, bu, S[c + 3]);
-            o0 = fmaf(S[c], qq.x, o0);
-            o1 = fmaf(S[c + 1], qq.y, o1);
-            o2 = fmaf(S[c + 2], qq.z, o2);
-            o3 = fmaf(S[c + 3], qq.w, o3);
+        for (int i = 0; i < 16; ++i)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                S[i][c] *= x[i];
+                sk[c] = fmaf(S[i][c], kk[i], sk[c]);
+            }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            sk[c] += __shfl_xor_sync(0xffffffffu, sk[c], 1);
+            sk[c] += __shfl_xor_sync(0xffffffffu, sk[c], 2);
+            sk[c] += __shfl_xor_sync(0xffffffffu, sk[c], 4);
         }
-        float o = (o0 + o1) + (o2 + o3);
-        o += __shfl_xor_sync(0xffffffffu, o, 1);
-        if (half == 0) p.out[r * p.os[0] + t * p.os[1] + h * p.os[2] + j] = __float2bfloat16_rn(o);
+        const float4 v4 = *reinterpret_cast<const float4*>(&s_v[t][col0]);
+        const float bt = s_beta[t];
+        const float u[4] = {bt * (v4.x - sk[0]), bt * (v4.y - sk[1]), bt * (v4.z - sk[2]), bt * (v4.w - sk[3])};
+#pragma unroll
+        for (int i = 0; i < 16; i += 4) {
+            const float4 q4 = *reinterpret_cast<const float4*>(&s_q[t][prow + i]);
+            x[i] = q4.x; x[i + 1] = q4.y; x[i + 2] = q4.z; x[i + 3] = q4.w;
+        }
+        float o[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                S[i][c] = fmaf(kk[i], u[c], S[i][c]);
+                o[c] = fmaf(S[i][c], x[i], o[c]);
+            }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            o[c] += __shfl_xor_sync(0xffffffffu, o[c], 1);
+            o[c] += __shfl_xor_sync(0xffffffffu, o[c], 2);
+            o[c] += __shfl_xor_sync(0xffffffffu, o[c], 4);
+        }
+        if (rg < 4) {
+            const float oc = rg == 0 ? o[0] : rg == 1 ? o[1] : rg == 2 ? o[2] : o[3];
+            p.out[r * p.os[0] + t * p.os[1] + h * p.os[2] + col0 + rg] = __float2bfloat16_rn(oc);
+        }
         if (t + 1 == acc) {
 #pragma unroll
-            for (int c = 0; c < kRows; ++c) st[(r0 + c) * kHeadDim + j] = S[c];
+            for (int i = 0; i < 16; ++i)
+                *reinterpret_cast<float4*>(st + (row0 + i) * kHeadDim + col0) =
+                    make_float4(S[i][0], S[i][1], S[i][2], S[i][3]);
         }
     }
 }

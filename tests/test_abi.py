@@ -104,3 +104,19 @@ def test_verify_validation(K):
 def test_status_strings(K):
     for s in range(5):
         assert K.status_string(s).startswith("KDA_")
+
+
+def test_verify_refuses_misaligned_state_pool(K):
+    """The verify kernel moves the state in 16-byte vectors: a pool pointer that
+    is not 16-byte aligned is refused on the host, before any CUDA call."""
+    lib = K.lib()
+    a = K.VerifyArgs()
+    fake = ctypes.c_void_p(1 << 20)
+    a.q = a.k = a.v = a.g = a.beta = a.out = a.accepted = fake
+    a.state_pool = ctypes.c_void_p((1 << 20) + 4)
+    for f in ("q_stride", "k_stride", "v_stride", "g_stride", "out_stride"):
+        setattr(a, f, K._i64x3(4 * 2 * 128, 2 * 128, 128))
+    a.beta_stride = K._i64x3(8, 2, 1)
+    a.head_dim_k = a.head_dim_v = 128
+    a.num_requests, a.num_drafts, a.num_heads, a.pool_size = 2, 4, 2, 2
+    assert lib.kda_verify(ctypes.byref(a), None) == K.KDA_ERR_UNSUPPORTED
