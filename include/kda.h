@@ -252,6 +252,43 @@ kda_status kda_verify(const kda_verify_args* args, void* stream);
 #define KDA_NOALLOC_MAX_WORKSPACE_BYTES ((size_t)32 << 20)
 kda_status kda_prefill_noalloc(const kda_prefill_args* args, void* stream);
 
+/*
+ * kda_prefill for inputs and outputs that live in host memory.  (The pages have
+ * no counterpart; this is a runtime entry of this library for callers that keep
+ * their tensors on the host.)
+ *
+ * args: as for kda_prefill, except that q, k, v, g, beta, out, initial_state and
+ * final_state point to PAGE-LOCKED HOST memory (cudaHostAlloc or
+ * cudaHostRegister) in the contiguous layouts (padded: q/k/v/g/out
+ * [B, T, H, 128], beta [B, T, H]; varlen: [T_total, H, 128] and [T_total, H]),
+ * cu_seqlens (varlen) is a HOST int32 array [N + 1], and the stride, workspace
+ * and workspace_bytes fields are ignored.
+ * staging: caller-owned device memory, 256-byte aligned, at least
+ * kda_prefill_host_staging_size(args) bytes; piece_tokens: tokens per piece, a
+ * multiple of 64, or 0 for the library's choice (about an eighth of the input,
+ * at least 1024).
+ *
+ * The work is cut into pieces (padded: a range of chunk-aligned tokens of every
+ * sequence, with each chain's state carried from piece to piece on the device,
+ * so the result is bitwise that of one kda_prefill call; varlen: runs of whole
+ * sequences).  Piece p + 1 is copied in while piece p runs and each piece's
+ * output is copied out while later pieces run, on two copy streams the call
+ * creates and releases, ordered after the work already on `stream`; when
+ * `stream` reaches the point after this call, every output is in host memory.
+ * The host buffers and the staging memory must stay valid until then.  Errors:
+ * KDA_ERR_INVALID_ARG for missing pointers, unusable shapes or cu_seqlens, or a
+ * small / misaligned staging area (nothing is launched); otherwise the statuses
+ * of kda_prefill.
+ */
+typedef struct kda_prefill_host_args {
+    kda_prefill_args args;
+    void* staging;
+    size_t staging_bytes;
+    int64_t piece_tokens;
+} kda_prefill_host_args;
+size_t kda_prefill_host_staging_size(const kda_prefill_host_args* args);
+kda_status kda_prefill_host(const kda_prefill_host_args* args, void* stream);
+
 /* Static string naming a status code. */
 const char* kda_status_string(kda_status status);
 

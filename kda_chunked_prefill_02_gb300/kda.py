@@ -36,6 +36,11 @@ class PrefillArgs(ctypes.Structure):
                 ("device_status", _p)]
 
 
+class PrefillHostArgs(ctypes.Structure):
+    _fields_ = [("args", PrefillArgs), ("staging", _p), ("staging_bytes", ctypes.c_size_t),
+                ("piece_tokens", _i64)]
+
+
 class VerifyArgs(ctypes.Structure):
     _fields_ = [("q", _p), ("k", _p), ("v", _p), ("g", _p), ("beta", _p), ("out", _p),
                 ("q_stride", _i64x3), ("k_stride", _i64x3), ("v_stride", _i64x3),
@@ -73,6 +78,10 @@ def lib():
             f = getattr(L, name)
             f.restype = ctypes.c_int
             f.argtypes = [ctypes.POINTER(PrefillArgs), _p]
+        L.kda_prefill_host_staging_size.restype = ctypes.c_size_t
+        L.kda_prefill_host_staging_size.argtypes = [ctypes.POINTER(PrefillHostArgs)]
+        L.kda_prefill_host.restype = ctypes.c_int
+        L.kda_prefill_host.argtypes = [ctypes.POINTER(PrefillHostArgs), _p]
         L.kda_verify.restype = ctypes.c_int
         L.kda_verify.argtypes = [ctypes.POINTER(VerifyArgs), _p]
         L.kda_status_string.restype = ctypes.c_char_p
@@ -291,4 +300,68 @@ def kda_prefill_noalloc(q, k, v, g, beta, *, initial_state=None, cu_seqlens=None
     a = _prefill_args(q, k, v, g, beta, initial_state, cu_seqlens, out, final_state,
                       beta_is_logit, scale, None, device_status, chunk)
     _check(f(ctypes.byref(a), _stream_handle(stream)))
+    return out, final_state
+
+
+def _host_args(q, k, v, g, beta, initial_state, cu_seqlens, out, final_state, beta_is_logit,
+               scale, chunk, staging, piece_tokens, check=True):
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16),
+                        ("v", v, torch.bfloat16), ("g", g, torch.float32),
+                        ("beta", beta, torch.float32), ("out", out, torch.bfloat16),
+                        ("initial_state", initial_state, torch.float32),
+                        ("final_state", final_state, torch.float32)):
+        if t is None or not check:
+            continue
+        if t.device.type != "cpu" or not t.is_pinned() or t.dtype != dt or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous page-locked host tensor of %s" % (name, dt))
+    if cu_seqlens is not None and (cu_seqlens.device.type != "cpu" or cu_seqlens.dtype != torch.int32
+                                   or not cu_seqlens.is_contiguous()):
+        raise ValueError("cu_seqlens must be a contiguous host int32 tensor here")
+    a = PrefillArgs()
+    a.q, a.k, a.v, a.g, a.beta, a.out = (_ptr(t) for t in (q, k, v, g, beta, out))
+    a.initial_state = _ptr(initial_state)
+    a.final_state = _ptr(final_state)
+    a.cu_seqlens = _ptr(cu_seqlens)
+    if cu_seqlens is not None:
+        a.batch, a.seqlen, a.num_seqs, a.num_heads = 1, q.shape[0], cu_seqlens.shape[0] - 1, q.shape[1]
+    else:
+        a.batch, a.seqlen, a.num_seqs, a.num_heads = q.shape[0], q.shape[1], q.shape[0], q.shape[2]
+    a.head_dim_k, a.head_dim_v = q.shape[-1], v.shape[-1]
+    a.chunk = int(chunk)
+    a.beta_is_logit = 1 if beta_is_logit else 0
+    a.scale = float(scale)
+    h = PrefillHostArgs()
+    h.args = a
+    h.staging = _ptr(staging)
+    h.staging_bytes = 0 if staging is None else staging.numel() * staging.element_size()
+    h.piece_tokens = int(piece_tokens)
+    return h
+
+
+def host_staging_size(q, v, *, cu_seqlens=None, piece_tokens=0):
+    """Bytes of device staging kda_prefill_host needs (q, v: host tensors)."""
+    h = _host_args(q, q, v, None, None, None, cu_seqlens, None, None, True, 1.0, CHUNK, None,
+                   piece_tokens, check=False)
+    return int(lib().kda_prefill_host_staging_size(ctypes.byref(h)))
+
+
+def kda_prefill_host(q, k, v, g, beta, *, initial_state=None, cu_seqlens=None, chunk=CHUNK,
+                     beta_is_logit=True, scale=1.0, out=None, final_state=None,
+                     output_final_state=True, staging=None, piece_tokens=0, stream=None):
+    """KDA prefill with every tensor in page-locked host memory (cu_seqlens a host
+    int32 tensor), through the C ABI's kda_prefill_host: the copies in and out
+    overlap the kernels piece by piece.  Asynchronous on `stream`; returns the
+    host (out, final_state), complete once the stream reaches this point."""
+    N = (cu_seqlens.shape[0] - 1) if cu_seqlens is not None else q.shape[0]
+    H = q.shape[-2]
+    if out is None:
+        out = torch.empty(v.shape, dtype=torch.bfloat16, pin_memory=True)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H, q.shape[-1], v.shape[-1]), dtype=torch.float32, pin_memory=True)
+    if staging is None:
+        nbytes = host_staging_size(q, v, cu_seqlens=cu_seqlens, piece_tokens=piece_tokens)
+        staging = torch.empty(max(nbytes, 1), dtype=torch.uint8, device="cuda")
+    h = _host_args(q, k, v, g, beta, initial_state, cu_seqlens, out, final_state, beta_is_logit,
+                   scale, chunk, staging, piece_tokens)
+    _check(lib().kda_prefill_host(ctypes.byref(h), _stream_handle(stream)))
     return out, final_state
