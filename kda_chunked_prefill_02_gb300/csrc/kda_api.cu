@@ -199,8 +199,19 @@ kda_status kda_verify(const kda_verify_args* a, void* stream) {
     for (int t = 0; t < 6; ++t)
         for (int i = 0; i < 3; ++i)
             if (ss[t][i] < 0) return KDA_ERR_UNSUPPORTED;
-    // The state is read and written in 16-byte vectors.
-    if (reinterpret_cast<uintptr_t>(a->state_pool) & 15) return KDA_ERR_UNSUPPORTED;
+    // Draft rows and state blocks are moved in 16-byte pieces: every q, k, v, g row
+    // and the pool must start on a 16-byte boundary.
+    auto aligned16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; };
+    if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->g) ||
+        !aligned16(a->state_pool))
+        return KDA_ERR_UNSUPPORTED;
+    for (int i = 0; i < 3; ++i)
+        if (a->q_stride[i] % 8 || a->k_stride[i] % 8 || a->v_stride[i] % 8 || a->g_stride[i] % 4)
+            return KDA_ERR_UNSUPPORTED;
+    int dev = 0, num_sms = 1;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return KDA_ERR_CUDA;
     VerifyParams p;
     memset(&p, 0, sizeof(p));
     p.q = static_cast<const __nv_bfloat16*>(a->q);
@@ -223,7 +234,7 @@ kda_status kda_verify(const kda_verify_args* a, void* stream) {
     p.P = (int)a->pool_size;
     p.beta_is_logit = a->beta_is_logit ? 1 : 0;
     p.scale = a->scale;
-    return launch_verify(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KDA_OK
+    return launch_verify(p, num_sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KDA_OK
                                                                                : KDA_ERR_CUDA;
 }
 

@@ -116,6 +116,6 @@ struct VerifyParams {
     float scale;
 };
 
-cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s);
+cudaError_t launch_verify(const VerifyParams& p, int num_sms, cudaStream_t s);
 
 }  // namespace kda

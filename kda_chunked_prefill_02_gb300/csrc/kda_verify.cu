@@ -5,132 +5,239 @@
 // tcgen05 KDA MTP verify kernel and its replay-only commit on the TensorRT-LLM
 // page "Kimi K3 work for Rubin (SM107)", Description).  With at most 16 drafts
 // the work per (request, head) is ~4 x 16K FMAs against 128 KB of state
-// traffic, so the kernel is bound by HBM bandwidth on the state pool; it runs
-// the drafts sequentially on CUDA cores with the state column of each thread
-// in registers, which also yields the per-draft outputs directly.
+// traffic, so the kernel is bound by HBM bandwidth on the state pool.
 //
-// Layout: one CTA per (head, request), 256 threads.  Every draft's q, k, e^g,
-// v and beta are staged in shared memory in the same pass as the state load.
-// Thread (row group rg = lane & 7, column group cg = 4*warp + lane / 8) owns the
-// 16 x 4 block of the state at key rows 16*rg.., value columns 4*cg..: each
-// staged key-channel value it reads from shared memory serves four columns,
-// and the reductions over key channels (S^T k, S^T q) are 16 in-thread FMAs per
-// column plus three shuffle levels over the row groups of the warp.  The
-// staged rows are padded by 16 bytes every 16 floats, so the eight row groups
-// of a warp read eight different bank quads.
+// Organisation: persistent CTAs (two per SM when the drafts fit) stream
+// (request, head) items.  As soon as an item's state sits in registers, the
+// next item's 64 KB state block and draft rows are requested with cp.async, so
+// every item's loads overlap the previous item's compute; the updated state
+// goes from registers straight to the pool.  Thread (row group rg = lane & 7,
+// column group cg = 4*warp + lane / 8) owns the 16 x 4 block of the state at
+// key rows 16*rg.., value columns 4*cg..: each staged key-channel value serves
+// four columns, and the reductions over key channels (S^T k, S^T q) are 16
+// in-thread FMAs per column plus three shuffle levels over the row groups of
+// the warp.  Shared-memory layouts keep every access conflict-free: the
+// state's 16-byte chunks are XOR-swizzled by row group, and the staged q, k
+// and e^g rows carry 16 bytes of padding per row group.
 #include "kda_internal.h"
 
 namespace kda {
 namespace {
 
 constexpr int kMaxDrafts = 16;
-constexpr int kPadRow = kHeadDim + kHeadDim / 4;   // 160 floats: 16 B of padding per 16 floats
-__device__ __forceinline__ int padded(int i) { return i + (i >> 4) * 4; }
+constexpr int kVerifyThreads = 256;
+constexpr uint32_t kStateBytes = kHeadDim * kHeadDim * 4;   // 64 KB
+// Staged draft row t (bytes): q bf16 and k bf16 rows of 128 with 16 B of
+// padding after each 32 B (row group), v bf16 unpadded, e^g fp32 with 16 B
+// after each 64 B.
+constexpr uint32_t kQRow = 384, kVRow = 256, kERow = 640;
+constexpr uint32_t TO_Q = 0, TO_K = kQRow, TO_V = 2 * kQRow, TO_E = 2 * kQRow + kVRow;
+constexpr uint32_t kTokBytes = 2 * kQRow + kVRow + kERow;    // 1664
 
-__global__ void __launch_bounds__(256, 2)
-    verify_kernel(const VerifyParams p) {
-    const int h = blockIdx.x, r = blockIdx.y, tid = threadIdx.x;
-    const int warp = tid >> 5, lane = tid & 31;
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+// Byte offset of the 16-byte chunk holding columns 4c..4c+3 of state row r.
+__device__ __forceinline__ uint32_t state_chunk(int r, int c) {
+    return (uint32_t)r * 512u + ((uint32_t)(c ^ ((r >> 4) & 7)) << 4);
+}
+__device__ __forceinline__ float2 bf16x2f(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+struct Item {
+    int r, h, slot, acc;
+    bool valid;
+};
+
+__global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyParams p) {
+    extern __shared__ __align__(16) uint8_t smv[];
+    __shared__ float s_beta[kMaxDrafts];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int rg = lane & 7, cg = 4 * warp + (lane >> 3);
     const int row0 = 16 * rg, col0 = 4 * cg;
-    __shared__ __align__(16) float s_e[kMaxDrafts][kPadRow];
-    __shared__ __align__(16) float s_k[kMaxDrafts][kPadRow];
-    __shared__ __align__(16) float s_q[kMaxDrafts][kPadRow];
-    __shared__ __align__(16) float s_v[kMaxDrafts][kHeadDim];
-    __shared__ float s_beta[kMaxDrafts];
+    const int nitems = p.R * p.H, D = p.D;
+    if ((int)blockIdx.x >= nitems) return;
+    uint8_t* sst = smv;
+    auto tokb = [&](int b) { return smv + kStateBytes + b * D * kTokBytes; };  // draft buffers 0, 1
 
-    const int slot = p.slot ? p.slot[r] : r;
-    const int acc = p.accepted[r];
-    if (slot < 0 || slot >= p.P || acc < 0 || acc > p.D) {
-        if (tid == 0 && p.status) atomicExch(p.status, 1);
-        return;
-    }
-    float* st = p.pool + ((int64_t)slot * p.H + h) * (kHeadDim * kHeadDim);
-    float S[16][4];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const float4 x = *reinterpret_cast<const float4*>(st + (row0 + i) * kHeadDim + col0);
-        S[i][0] = x.x; S[i][1] = x.y; S[i][2] = x.z; S[i][3] = x.w;
-    }
-    for (int e = tid; e < p.D * kHeadDim; e += blockDim.x) {
-        const int t = e >> 7, i = e & (kHeadDim - 1), pi = padded(i);
-        s_q[t][pi] = __bfloat162float(p.q[r * p.qs[0] + t * p.qs[1] + h * p.qs[2] + i]) * p.scale;
-        s_k[t][pi] = __bfloat162float(p.k[r * p.ks[0] + t * p.ks[1] + h * p.ks[2] + i]);
-        s_e[t][pi] = __expf(p.g[r * p.gs[0] + t * p.gs[1] + h * p.gs[2] + i]);
-        s_v[t][i] = __bfloat162float(p.v[r * p.vs[0] + t * p.vs[1] + h * p.vs[2] + i]);
-    }
-    if (tid < p.D) {
-        const float bb = p.beta[r * p.bs[0] + tid * p.bs[1] + h * p.bs[2]];
-        s_beta[tid] = p.beta_is_logit ? 1.0f / (1.0f + __expf(-bb)) : bb;
-    }
-    __syncthreads();
+    auto item_of = [&](int it) -> Item {
+        Item x;
+        x.r = it / p.H;
+        x.h = it - x.r * p.H;
+        x.slot = p.slot ? p.slot[x.r] : x.r;
+        x.acc = p.accepted[x.r];
+        x.valid = x.slot >= 0 && x.slot < p.P && x.acc >= 0 && x.acc <= D;
+        return x;
+    };
+    auto state_of = [&](const Item& x) -> float* {
+        return p.pool + ((int64_t)x.slot * p.H + x.h) * (kHeadDim * kHeadDim);
+    };
+    auto load_beta = [&](const Item& x) -> float {
+        return (tid < D && x.valid) ? p.beta[x.r * p.bs[0] + tid * p.bs[1] + x.h * p.bs[2]] : 0.f;
+    };
+    // Item x's state block into sst and its draft rows into tb (cp.async, one group).
+    auto prefetch = [&](const Item& x, uint8_t* tb) {
+        if (x.valid) {
+            const float* st = state_of(x);
+            for (int e = tid; e < kHeadDim * 32; e += kVerifyThreads) {
+                const int r = e >> 5, c = e & 31;
+                cp_async16(sst + state_chunk(r, c), st + r * kHeadDim + 4 * c);
+            }
+            for (int e = tid; e < D * 80; e += kVerifyThreads) {
+                const int t = e / 80, j = e - t * 80;
+                uint8_t* row = tb + t * kTokBytes;
+                if (j < 16) {
+                    cp_async16(row + TO_Q + j * 16 + (j >> 1) * 16, p.q + x.r * p.qs[0] + t * p.qs[1] + x.h * p.qs[2] + 8 * j);
+                } else if (j < 32) {
+                    const int jj = j - 16;
+                    cp_async16(row + TO_K + jj * 16 + (jj >> 1) * 16, p.k + x.r * p.ks[0] + t * p.ks[1] + x.h * p.ks[2] + 8 * jj);
+                } else if (j < 48) {
+                    const int jj = j - 32;
+                    cp_async16(row + TO_V + jj * 16, p.v + x.r * p.vs[0] + t * p.vs[1] + x.h * p.vs[2] + 8 * jj);
+                } else {
+                    const int jj = j - 48;
+                    cp_async16(row + TO_E + jj * 16 + (jj >> 2) * 16, p.g + x.r * p.gs[0] + t * p.gs[1] + x.h * p.gs[2] + 4 * jj);
+                }
+            }
+        }
+        cp_async_commit();
+    };
 
-    const int prow = padded(row0);  // the 16 rows of a group are contiguous after padding
-    for (int t = 0; t < p.D; ++t) {
-        float kk[16], x[16];
-#pragma unroll
-        for (int i = 0; i < 16; i += 4) {
-            const float4 e4 = *reinterpret_cast<const float4*>(&s_e[t][prow + i]);
-            const float4 k4 = *reinterpret_cast<const float4*>(&s_k[t][prow + i]);
-            x[i] = e4.x; x[i + 1] = e4.y; x[i + 2] = e4.z; x[i + 3] = e4.w;
-            kk[i] = k4.x; kk[i + 1] = k4.y; kk[i + 2] = k4.z; kk[i + 3] = k4.w;
-        }
-        // decay, then u = v - S^T k
-        float sk[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                S[i][c] *= x[i];
-                sk[c] = fmaf(S[i][c], kk[i], sk[c]);
+    int it = blockIdx.x;
+    Item cur = item_of(it);
+    float bcur = load_beta(cur);
+    prefetch(cur, tokb(0));
+    Item nxt = it + (int)gridDim.x < nitems ? item_of(it + gridDim.x) : Item{0, 0, 0, 0, false};
+    for (int k = 0;; ++k) {
+        cp_async_wait_all();
+        __syncthreads();  // this item's state and drafts have landed; the previous item is done
+        uint8_t* tb = tokb(k & 1);
+        float S[16][4];
+        if (cur.valid) {
+            for (int e = tid; e < D * kHeadDim; e += kVerifyThreads) {  // e^g in place
+                const int t = e >> 7, i = e & (kHeadDim - 1);
+                float* ge = reinterpret_cast<float*>(tb + t * kTokBytes + TO_E + i * 4 + (i >> 4) * 16);
+                *ge = __expf(*ge);
             }
+            if (tid < D) s_beta[tid] = p.beta_is_logit ? 1.0f / (1.0f + __expf(-bcur)) : bcur;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            sk[c] += __shfl_xor_sync(0xffffffffu, sk[c], 1);
-            sk[c] += __shfl_xor_sync(0xffffffffu, sk[c], 2);
-            sk[c] += __shfl_xor_sync(0xffffffffu, sk[c], 4);
-        }
-        const float4 v4 = *reinterpret_cast<const float4*>(&s_v[t][col0]);
-        const float bt = s_beta[t];
-        const float u[4] = {bt * (v4.x - sk[0]), bt * (v4.y - sk[1]), bt * (v4.z - sk[2]), bt * (v4.w - sk[3])};
-#pragma unroll
-        for (int i = 0; i < 16; i += 4) {
-            const float4 q4 = *reinterpret_cast<const float4*>(&s_q[t][prow + i]);
-            x[i] = q4.x; x[i + 1] = q4.y; x[i + 2] = q4.z; x[i + 3] = q4.w;
-        }
-        float o[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                S[i][c] = fmaf(kk[i], u[c], S[i][c]);
-                o[c] = fmaf(S[i][c], x[i], o[c]);
+            for (int i = 0; i < 16; ++i) {
+                const float4 x = *reinterpret_cast<const float4*>(sst + state_chunk(row0 + i, cg));
+                S[i][0] = x.x; S[i][1] = x.y; S[i][2] = x.z; S[i][3] = x.w;
             }
+        } else if (tid == 0 && p.status) {
+            atomicExch(p.status, 1);
+        }
+        __syncthreads();  // the state block is in registers: its buffer takes the next item
+        prefetch(nxt, tokb((k + 1) & 1));
+        const float bnext = load_beta(nxt);
+        const int nit = it + gridDim.x;
+        const Item after = nit + (int)gridDim.x < nitems ? item_of(nit + gridDim.x) : Item{0, 0, 0, 0, false};
+        if (cur.valid) {
+            float* st = state_of(cur);
+            for (int t = 0; t < D; ++t) {
+                const uint8_t* row = tb + t * kTokBytes;
+                float kk[16], x[16];
+                {
+                    const uint4 k0 = *reinterpret_cast<const uint4*>(row + TO_K + 48 * rg);
+                    const uint4 k1 = *reinterpret_cast<const uint4*>(row + TO_K + 48 * rg + 16);
+                    const uint32_t kw[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            o[c] += __shfl_xor_sync(0xffffffffu, o[c], 1);
-            o[c] += __shfl_xor_sync(0xffffffffu, o[c], 2);
-            o[c] += __shfl_xor_sync(0xffffffffu, o[c], 4);
-        }
-        if (rg < 4) {
-            const float oc = rg == 0 ? o[0] : rg == 1 ? o[1] : rg == 2 ? o[2] : o[3];
-            p.out[r * p.os[0] + t * p.os[1] + h * p.os[2] + col0 + rg] = __float2bfloat16_rn(oc);
-        }
-        if (t + 1 == acc) {
+                    for (int w = 0; w < 8; ++w) {
+                        const float2 f = bf16x2f(kw[w]);
+                        kk[2 * w] = f.x; kk[2 * w + 1] = f.y;
+                    }
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                *reinterpret_cast<float4*>(st + (row0 + i) * kHeadDim + col0) =
-                    make_float4(S[i][0], S[i][1], S[i][2], S[i][3]);
+                    for (int i = 0; i < 16; i += 4) {
+                        const float4 e4 = *reinterpret_cast<const float4*>(row + TO_E + 80 * rg + 4 * i);
+                        x[i] = e4.x; x[i + 1] = e4.y; x[i + 2] = e4.z; x[i + 3] = e4.w;
+                    }
+                }
+                // decay, then u = v - S^T k
+                float sk[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        S[i][c] *= x[i];
+                        sk[c] = fmaf(S[i][c], kk[i], sk[c]);
+                    }
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    sk[c] += __shfl_xor_sync(0xffffffffu, sk[c], 1);
+                    sk[c] += __shfl_xor_sync(0xffffffffu, sk[c], 2);
+                    sk[c] += __shfl_xor_sync(0xffffffffu, sk[c], 4);
+                }
+                const uint2 vw = *reinterpret_cast<const uint2*>(row + TO_V + 2 * col0);
+                const float2 v01 = bf16x2f(vw.x), v23 = bf16x2f(vw.y);
+                const float bt = s_beta[t];
+                const float u[4] = {bt * (v01.x - sk[0]), bt * (v01.y - sk[1]), bt * (v23.x - sk[2]),
+                                    bt * (v23.y - sk[3])};
+                {
+                    const uint4 q0 = *reinterpret_cast<const uint4*>(row + TO_Q + 48 * rg);
+                    const uint4 q1 = *reinterpret_cast<const uint4*>(row + TO_Q + 48 * rg + 16);
+                    const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+                    for (int w = 0; w < 8; ++w) {
+                        const float2 f = bf16x2f(qw[w]);
+                        x[2 * w] = f.x * p.scale; x[2 * w + 1] = f.y * p.scale;
+                    }
+                }
+                float o[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        S[i][c] = fmaf(kk[i], u[c], S[i][c]);
+                        o[c] = fmaf(S[i][c], x[i], o[c]);
+                    }
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    o[c] += __shfl_xor_sync(0xffffffffu, o[c], 1);
+                    o[c] += __shfl_xor_sync(0xffffffffu, o[c], 2);
+                    o[c] += __shfl_xor_sync(0xffffffffu, o[c], 4);
+                }
+                if (rg < 4) {
+                    const float oc = rg == 0 ? o[0] : rg == 1 ? o[1] : rg == 2 ? o[2] : o[3];
+                    p.out[cur.r * p.os[0] + t * p.os[1] + cur.h * p.os[2] + col0 + rg] = __float2bfloat16_rn(oc);
+                }
+                if (t + 1 == cur.acc) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        *reinterpret_cast<float4*>(st + (row0 + i) * kHeadDim + col0) =
+                            make_float4(S[i][0], S[i][1], S[i][2], S[i][3]);
+                }
+            }
         }
+        if (nit >= nitems) break;
+        it = nit;
+        cur = nxt;
+        bcur = bnext;
+        nxt = after;
     }
+    cp_async_wait_all();  // the last (empty or unused) prefetch group
 }
 
 }  // namespace
 
-cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s) {
+cudaError_t launch_verify(const VerifyParams& p, int num_sms, cudaStream_t s) {
     if (p.R == 0 || p.H == 0) return cudaSuccess;
-    dim3 grid(p.H, p.R);
-    verify_kernel<<<grid, 256, 0, s>>>(p);
+    const size_t smem = kStateBytes + 2 * (size_t)p.D * kTokBytes;
+    cudaError_t e = cudaFuncSetAttribute(verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, verify_kernel, kVerifyThreads, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    const long long items = (long long)p.R * p.H;
+    const long long cap = (long long)num_sms * per_sm;
+    verify_kernel<<<(unsigned)(items < cap ? items : cap), kVerifyThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -120,3 +120,28 @@ def test_verify_refuses_misaligned_state_pool(K):
     a.head_dim_k = a.head_dim_v = 128
     a.num_requests, a.num_drafts, a.num_heads, a.pool_size = 2, 4, 2, 2
     assert lib.kda_verify(ctypes.byref(a), None) == K.KDA_ERR_UNSUPPORTED
+
+
+def test_verify_refuses_rows_it_cannot_move_in_16_byte_pieces(K):
+    """Verify moves draft rows and state blocks in 16-byte pieces, so a
+    misaligned pointer or stride is refused on the host (no CUDA call)."""
+    lib = K.lib()
+
+    def args(**kw):
+        a = K.VerifyArgs()
+        fake = ctypes.c_void_p(1 << 20)
+        a.q = a.k = a.v = a.g = a.beta = a.out = a.state_pool = a.accepted = fake
+        for f in ("q_stride", "k_stride", "v_stride", "g_stride", "out_stride"):
+            setattr(a, f, K._i64x3(4 * 2 * 128, 2 * 128, 128))
+        a.beta_stride = K._i64x3(8, 2, 1)
+        a.head_dim_k = a.head_dim_v = 128
+        a.num_requests, a.num_drafts, a.num_heads, a.pool_size = 2, 4, 2, 2
+        for k_, v_ in kw.items():
+            setattr(a, k_, v_)
+        return a
+
+    run = lambda a: lib.kda_verify(ctypes.byref(a), None)
+    assert run(args(q=ctypes.c_void_p((1 << 20) + 2))) == K.KDA_ERR_UNSUPPORTED
+    assert run(args(g=ctypes.c_void_p((1 << 20) + 4))) == K.KDA_ERR_UNSUPPORTED
+    assert run(args(k_stride=K._i64x3(4 * 2 * 128, 2 * 128 + 4, 128))) == K.KDA_ERR_UNSUPPORTED
+    assert run(args(g_stride=K._i64x3(4 * 2 * 128, 2 * 128 + 2, 128))) == K.KDA_ERR_UNSUPPORTED
