@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define KDA_ABI_VERSION 1
+#define KDA_ABI_VERSION 2
 
 typedef enum {
     KDA_OK = 0,
@@ -179,9 +179,16 @@ typedef struct kda_workspace_layout {
 kda_status kda_prefill_workspace_layout(const kda_prefill_args* args,
                                         kda_workspace_layout* layout);
 
+/* State pool element types of kda_verify. */
+#define KDA_POOL_F32 0
+#define KDA_POOL_BF16 1
+
 /*
  * MTP verify: R requests, each with D <= 16 draft tokens, run against a fp32
- * state pool.  For request r and head h the state is read from
+ * or bf16 state pool (both are accepted, as on the TensorRT-LLM page "Kimi K3
+ * work for Rubin (SM107)", Description).  A bf16 pool is read widened to fp32,
+ * the drafts run in fp32, and the state written back is rounded to nearest
+ * even; it halves the pool traffic.  For request r and head h the state is read from
  * state_pool[slot[r], h] (slot == NULL: slot r), all D drafts go through the
  * recurrence in order and produce outputs, and the state after the first
  * accepted[r] drafts is written back to the same pool slot (accepted 0 leaves
@@ -193,6 +200,10 @@ kda_status kda_prefill_workspace_layout(const kda_prefill_args* args,
  *   slot, accepted: device int32 [R]; accepted[r] in 0..D, slot[r] in
  *   0..pool_size-1 (out-of-range entries are skipped and reported through
  *   device_status)
+ * replay_only = 1 is the commit of accepted drafts (the replay-only mode of
+ * the same page): for each request only its first accepted[r] drafts run, no
+ * output is written (out may be NULL) and the state after them is stored;
+ * accepted 0 leaves the state unchanged.
  * Draft rows and state blocks are moved in 16-byte pieces, so q, k, v, g and
  * state_pool must be 16-byte aligned, the q/k/v strides multiples of 8
  * elements and the g strides multiples of 4; otherwise KDA_ERR_UNSUPPORTED and
@@ -211,7 +222,7 @@ typedef struct kda_verify_args {
     int64_t g_stride[3];
     int64_t beta_stride[3];
     int64_t out_stride[3];
-    float* state_pool;
+    void* state_pool;           /* fp32 or bf16 (pool_dtype) [pool_size, H, 128, 128] */
     int64_t pool_size;
     const int32_t* slot;        /* device int32 [R] or NULL */
     const int32_t* accepted;    /* device int32 [R] */
@@ -223,6 +234,8 @@ typedef struct kda_verify_args {
     int32_t beta_is_logit;
     float scale;
     int32_t* device_status;     /* optional device int32 */
+    int32_t pool_dtype;         /* KDA_POOL_F32 or KDA_POOL_BF16 */
+    int32_t replay_only;        /* 1: commit mode, see above */
 } kda_verify_args;
 
 kda_status kda_verify(const kda_verify_args* args, void* stream);

@@ -189,9 +189,10 @@ kda_status kda_verify(const kda_verify_args* a, void* stream) {
         return KDA_ERR_INVALID_ARG;
     if (a->num_drafts > 16) return KDA_ERR_UNSUPPORTED;
     if (a->num_requests == 0) return KDA_OK;
-    if (!a->q || !a->k || !a->v || !a->g || !a->beta || !a->out || !a->state_pool || !a->accepted ||
-        a->pool_size < 1)
+    if (!a->q || !a->k || !a->v || !a->g || !a->beta || (!a->out && !a->replay_only) ||
+        !a->state_pool || !a->accepted || a->pool_size < 1)
         return KDA_ERR_INVALID_ARG;
+    if (a->pool_dtype != KDA_POOL_F32 && a->pool_dtype != KDA_POOL_BF16) return KDA_ERR_UNSUPPORTED;
     if (a->num_requests > 65535 || a->num_heads > 65535 || a->pool_size > (1 << 30))
         return KDA_ERR_UNSUPPORTED;
     const int64_t* ss[6] = {a->q_stride, a->k_stride, a->v_stride, a->g_stride, a->beta_stride,
@@ -234,6 +235,8 @@ kda_status kda_verify(const kda_verify_args* a, void* stream) {
     p.P = (int)a->pool_size;
     p.beta_is_logit = a->beta_is_logit ? 1 : 0;
     p.scale = a->scale;
+    p.pool_bf16 = a->pool_dtype == KDA_POOL_BF16 ? 1 : 0;
+    p.replay_only = a->replay_only ? 1 : 0;
     return launch_verify(p, num_sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KDA_OK
                                                                                : KDA_ERR_CUDA;
 }

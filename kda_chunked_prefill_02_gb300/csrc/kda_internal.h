@@ -107,13 +107,15 @@ struct VerifyParams {
     const float* beta;
     __nv_bfloat16* out;
     int64_t qs[3], ks[3], vs[3], gs[3], bs[3], os[3];
-    float* pool;
+    void* pool;              // fp32 or bf16 [P, H, 128, 128]
     const int32_t* slot;
     const int32_t* accepted;
     int32_t* status;         // may be null
     int R, D, H, P;
     int beta_is_logit;
     float scale;
+    int pool_bf16;           // 1: the pool holds bf16 states
+    int replay_only;         // 1: run the accepted drafts only, store the state, no outputs
 };
 
 cudaError_t launch_verify(const VerifyParams& p, int num_sms, cudaStream_t s);

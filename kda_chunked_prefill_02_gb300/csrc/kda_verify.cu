@@ -20,13 +20,14 @@
 // state's 16-byte chunks are XOR-swizzled by row group, and the staged q, k
 // and e^g rows carry 16 bytes of padding per row group.
 #include "kda_internal.h"
+#include "sm103.cuh"
 
 namespace kda {
 namespace {
 
 constexpr int kMaxDrafts = 16;
 constexpr int kVerifyThreads = 256;
-constexpr uint32_t kStateBytes = kHeadDim * kHeadDim * 4;   // 64 KB
+constexpr uint32_t kStateBytesMax = kHeadDim * kHeadDim * 4;   // 64 KB (fp32 pool; bf16: 32 KB)
 // Staged draft row t (bytes): q bf16 and k bf16 rows of 128 with 16 B of
 // padding after each 32 B (row group), v bf16 unpadded, e^g fp32 with 16 B
 // after each 64 B.
@@ -42,9 +43,11 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-// Byte offset of the 16-byte chunk holding columns 4c..4c+3 of state row r.
+// Byte offset of 16-byte chunk c of state row r in shared memory (fp32 rows:
+// 32 chunks of 4 values; bf16 rows: 16 chunks of 8), XOR-swizzled by the row group.
+template <bool kBf16>
 __device__ __forceinline__ uint32_t state_chunk(int r, int c) {
-    return (uint32_t)r * 512u + ((uint32_t)(c ^ ((r >> 4) & 7)) << 4);
+    return (uint32_t)r * (kBf16 ? 256u : 512u) + ((uint32_t)(c ^ ((r >> 4) & 7)) << 4);
 }
 __device__ __forceinline__ float2 bf16x2f(uint32_t w) {
     return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
@@ -55,7 +58,11 @@ struct Item {
     bool valid;
 };
 
+// kBf16: the pool holds bf16 states (read widened to fp32, written back rounded
+// to nearest even); otherwise fp32.
+template <bool kBf16>
 __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyParams p) {
+    constexpr uint32_t kStateBytes = kHeadDim * kHeadDim * (kBf16 ? 2 : 4);
     extern __shared__ __align__(16) uint8_t smv[];
     __shared__ float s_beta[kMaxDrafts];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -75,8 +82,8 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyP
         x.valid = x.slot >= 0 && x.slot < p.P && x.acc >= 0 && x.acc <= D;
         return x;
     };
-    auto state_of = [&](const Item& x) -> float* {
-        return p.pool + ((int64_t)x.slot * p.H + x.h) * (kHeadDim * kHeadDim);
+    auto state_of = [&](const Item& x) -> uint8_t* {
+        return static_cast<uint8_t*>(p.pool) + ((int64_t)x.slot * p.H + x.h) * (int64_t)kStateBytes;
     };
     auto load_beta = [&](const Item& x) -> float {
         return (tid < D && x.valid) ? p.beta[x.r * p.bs[0] + tid * p.bs[1] + x.h * p.bs[2]] : 0.f;
@@ -84,10 +91,11 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyP
     // Item x's state block into sst and its draft rows into tb (cp.async, one group).
     auto prefetch = [&](const Item& x, uint8_t* tb) {
         if (x.valid) {
-            const float* st = state_of(x);
-            for (int e = tid; e < kHeadDim * 32; e += kVerifyThreads) {
-                const int r = e >> 5, c = e & 31;
-                cp_async16(sst + state_chunk(r, c), st + r * kHeadDim + 4 * c);
+            const uint8_t* st = state_of(x);
+            constexpr int kChunksPerRow = kBf16 ? 16 : 32;
+            for (int e = tid; e < kHeadDim * kChunksPerRow; e += kVerifyThreads) {
+                const int r = e / kChunksPerRow, c = e % kChunksPerRow;
+                cp_async16(sst + state_chunk<kBf16>(r, c), st + (r * kChunksPerRow + c) * 16);
             }
             for (int e = tid; e < D * 80; e += kVerifyThreads) {
                 const int t = e / 80, j = e - t * 80;
@@ -128,8 +136,15 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyP
             if (tid < D) s_beta[tid] = p.beta_is_logit ? 1.0f / (1.0f + __expf(-bcur)) : bcur;
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                const float4 x = *reinterpret_cast<const float4*>(sst + state_chunk(row0 + i, cg));
-                S[i][0] = x.x; S[i][1] = x.y; S[i][2] = x.z; S[i][3] = x.w;
+                if (kBf16) {
+                    const uint2 w = *reinterpret_cast<const uint2*>(sst + state_chunk<true>(row0 + i, cg >> 1) +
+                                                                    (cg & 1) * 8);
+                    const float2 a = bf16x2f(w.x), b = bf16x2f(w.y);
+                    S[i][0] = a.x; S[i][1] = a.y; S[i][2] = b.x; S[i][3] = b.y;
+                } else {
+                    const float4 x = *reinterpret_cast<const float4*>(sst + state_chunk<false>(row0 + i, cg));
+                    S[i][0] = x.x; S[i][1] = x.y; S[i][2] = x.z; S[i][3] = x.w;
+                }
             }
         } else if (tid == 0 && p.status) {
             atomicExch(p.status, 1);
@@ -140,8 +155,10 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyP
         const int nit = it + gridDim.x;
         const Item after = nit + (int)gridDim.x < nitems ? item_of(nit + gridDim.x) : Item{0, 0, 0, 0, false};
         if (cur.valid) {
-            float* st = state_of(cur);
-            for (int t = 0; t < D; ++t) {
+            uint8_t* st = state_of(cur);
+            // replay-only: the chunk is the accepted drafts and only the state is stored
+            const int tend = p.replay_only ? cur.acc : D;
+            for (int t = 0; t < tend; ++t) {
                 const uint8_t* row = tb + t * kTokBytes;
                 float kk[16], x[16];
                 {
@@ -203,15 +220,20 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyP
                     o[c] += __shfl_xor_sync(0xffffffffu, o[c], 2);
                     o[c] += __shfl_xor_sync(0xffffffffu, o[c], 4);
                 }
-                if (rg < 4) {
+                if (rg < 4 && !p.replay_only) {
                     const float oc = rg == 0 ? o[0] : rg == 1 ? o[1] : rg == 2 ? o[2] : o[3];
                     p.out[cur.r * p.os[0] + t * p.os[1] + cur.h * p.os[2] + col0 + rg] = __float2bfloat16_rn(oc);
                 }
                 if (t + 1 == cur.acc) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        *reinterpret_cast<float4*>(st + (row0 + i) * kHeadDim + col0) =
-                            make_float4(S[i][0], S[i][1], S[i][2], S[i][3]);
+                    for (int i = 0; i < 16; ++i) {
+                        if (kBf16)
+                            *reinterpret_cast<uint2*>(st + ((row0 + i) * kHeadDim + col0) * 2) =
+                                make_uint2(pack_bf16x2(S[i][0], S[i][1]), pack_bf16x2(S[i][2], S[i][3]));
+                        else
+                            *reinterpret_cast<float4*>(st + ((row0 + i) * kHeadDim + col0) * 4) =
+                                make_float4(S[i][0], S[i][1], S[i][2], S[i][3]);
+                    }
                 }
             }
         }
@@ -224,21 +246,27 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyP
     cp_async_wait_all();  // the last (empty or unused) prefetch group
 }
 
-}  // namespace
-
-cudaError_t launch_verify(const VerifyParams& p, int num_sms, cudaStream_t s) {
-    if (p.R == 0 || p.H == 0) return cudaSuccess;
-    const size_t smem = kStateBytes + 2 * (size_t)p.D * kTokBytes;
-    cudaError_t e = cudaFuncSetAttribute(verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+template <bool kBf16>
+cudaError_t launch_verify_t(const VerifyParams& p, int num_sms, cudaStream_t s) {
+    const size_t smem = (size_t)kHeadDim * kHeadDim * (kBf16 ? 2 : 4) + 2 * (size_t)p.D * kTokBytes;
+    cudaError_t e = cudaFuncSetAttribute(verify_kernel<kBf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, verify_kernel, kVerifyThreads, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, verify_kernel<kBf16>, kVerifyThreads, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
     const long long items = (long long)p.R * p.H;
     const long long cap = (long long)num_sms * per_sm;
-    verify_kernel<<<(unsigned)(items < cap ? items : cap), kVerifyThreads, smem, s>>>(p);
+    verify_kernel<kBf16><<<(unsigned)(items < cap ? items : cap), kVerifyThreads, smem, s>>>(p);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_verify(const VerifyParams& p, int num_sms, cudaStream_t s) {
+    if (p.R == 0 || p.H == 0) return cudaSuccess;
+    return p.pool_bf16 ? launch_verify_t<true>(p, num_sms, s) : launch_verify_t<false>(p, num_sms, s);
 }
 
 }  // namespace kda

@@ -49,7 +49,11 @@ class VerifyArgs(ctypes.Structure):
                 ("num_requests", _i64), ("num_drafts", _i64), ("num_heads", _i64),
                 ("head_dim_k", _i64), ("head_dim_v", _i64),
                 ("beta_is_logit", ctypes.c_int32), ("scale", ctypes.c_float),
-                ("device_status", _p)]
+                ("device_status", _p), ("pool_dtype", ctypes.c_int32),
+                ("replay_only", ctypes.c_int32)]
+
+
+KDA_POOL_F32, KDA_POOL_BF16 = 0, 1
 
 
 class WorkspaceLayout(ctypes.Structure):
@@ -239,30 +243,37 @@ def kda_prefill(q, k, v, g, beta, *, initial_state=None, cu_seqlens=None, chunk=
 
 
 def kda_verify(q, k, v, g, beta, state_pool, accepted, *, slot=None, beta_is_logit=True,
-               scale=1.0, out=None, device_status=None, stream=None):
+               scale=1.0, out=None, device_status=None, stream=None, replay_only=False):
     """MTP verify through the C ABI; state_pool is updated in place.
 
-    q, k, g [R, D, H, 128]; v [R, D, H, 128]; beta [R, D, H]; state_pool fp32
-    [P, H, 128, 128]; accepted (and slot) int32 [R] on the device.  Returns out.
+    q, k, g [R, D, H, 128]; v [R, D, H, 128]; beta [R, D, H]; state_pool fp32 or
+    bf16 [P, H, 128, 128]; accepted (and slot) int32 [R] on the device.  Returns
+    out; with replay_only=True only the accepted drafts run, the states are
+    stored and nothing else is written (returns None).
     """
+    if state_pool is None or state_pool.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("state_pool must be a fp32 or bf16 CUDA tensor")
     for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16),
                         ("v", v, torch.bfloat16), ("g", g, torch.float32),
-                        ("beta", beta, torch.float32), ("state_pool", state_pool, torch.float32),
+                        ("beta", beta, torch.float32), ("state_pool", state_pool, state_pool.dtype),
                         ("accepted", accepted, torch.int32), ("slot", slot, torch.int32),
                         ("device_status", device_status, torch.int32)):
         _need_cuda(name, t, dt)
     if not state_pool.is_contiguous():
         raise ValueError("state_pool must be contiguous [P, H, 128, 128]")
-    if out is None:
+    if out is None and not replay_only:
         out = torch.empty(v.shape, dtype=torch.bfloat16, device=v.device)
-    _need_cuda("out", out, torch.bfloat16)
+    if out is not None:
+        _need_cuda("out", out, torch.bfloat16)
     a = VerifyArgs()
     a.q, a.k, a.v, a.g, a.beta, a.out = (_ptr(t) for t in (q, k, v, g, beta, out))
+    a.pool_dtype = KDA_POOL_BF16 if state_pool.dtype == torch.bfloat16 else KDA_POOL_F32
+    a.replay_only = 1 if replay_only else 0
     a.q_stride = _i64x3(*_strides3(q, False))
     a.k_stride = _i64x3(*_strides3(k, False))
     a.v_stride = _i64x3(*_strides3(v, False))
     a.g_stride = _i64x3(*_strides3(g, False))
-    a.out_stride = _i64x3(*_strides3(out, False))
+    a.out_stride = _i64x3(*_strides3(out if out is not None else v, False))
     a.beta_stride = _i64x3(*_strides3(beta, False, last_is_channel=False))
     a.state_pool = _ptr(state_pool)
     a.pool_size = state_pool.shape[0]

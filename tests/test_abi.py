@@ -33,7 +33,7 @@ def test_exports_every_declared_symbol(K):
             "kda_status_string"} <= names
     for n in sorted(names):
         assert hasattr(lib, n), n
-    assert lib.kda_abi_version() == 1
+    assert lib.kda_abi_version() == 2
 
 
 def _args(K, **kw):

@@ -73,3 +73,52 @@ def test_verify_full_config_sampled():
     out, pool = _run(vi)
     rows = np.random.default_rng(0).choice(vi.q.shape[0], 24, replace=False)
     _check(vi, out, pool, rows=sorted(rows.tolist()))
+
+
+def _bf16_case(seed, R=6, D=4, H=2, **kw):
+    vi = inputs.verify_inputs(seed, R=R, D=D, H=H, **kw)
+    vi.state_pool = vi.state_pool.to(torch.bfloat16).float()  # the pool's exact values
+    return vi
+
+
+def test_verify_bf16_pool():
+    """bf16 state pool: read widened exactly, drafts in fp32, state written back
+    rounded to nearest even.  Outputs against the oracle run from the same bf16
+    values; the stored state within a bf16 rounding of the oracle's."""
+    import kda_chunked_prefill_02_gb300 as K
+    vi = _bf16_case(31, permute_slots=True, pool_size=9)
+    d = vi.to("cuda")
+    pool = d.state_pool.to(torch.bfloat16)
+    out = K.kda_verify(d.q, d.k, d.v, d.g, d.beta, pool, d.accepted, slot=d.slot)
+    torch.cuda.synchronize()
+    rows = list(range(vi.q.shape[0]))
+    o_ref, st_ref = oracle.verify(vi.q, vi.k, vi.v, vi.g, vi.beta, vi.state_pool, vi.accepted,
+                                  slot=vi.slot)
+    assert np.abs(to_np(out) - o_ref).max() <= OUT_ATOL
+    st = to_np(pool[vi.slot.long().cuda()])
+    assert rel_fro(st, st_ref) <= 1e-2
+    # the written states are the bf16 rounding of a state within tolerance; untouched
+    # rows (accepted 0) keep their bits
+    for r in rows:
+        if vi.accepted[r] == 0:
+            assert torch.equal(pool[int(vi.slot[r])].cpu(), vi.state_pool[int(vi.slot[r])].to(torch.bfloat16))
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_verify_replay_only_commits_the_accepted_drafts(bf16):
+    """Replay-only: only the first accepted[r] drafts run, nothing but the state
+    is written (out is not touched), and the state equals the one a normal
+    verify stores."""
+    import kda_chunked_prefill_02_gb300 as K
+    vi = _bf16_case(41, R=7) if bf16 else inputs.verify_inputs(41, R=7, D=4, H=2)
+    vi.accepted[:3] = torch.tensor([0, 4, 2], dtype=torch.int32)
+    d = vi.to("cuda")
+    dt = torch.bfloat16 if bf16 else torch.float32
+    pool_a = d.state_pool.to(dt).clone()   # .to() returns the tensor itself when dt matches
+    pool_b = d.state_pool.to(dt).clone()
+    K.kda_verify(d.q, d.k, d.v, d.g, d.beta, pool_a, d.accepted)
+    assert K.kda_verify(d.q, d.k, d.v, d.g, d.beta, pool_b, d.accepted, replay_only=True) is None
+    torch.cuda.synchronize()
+    assert torch.equal(pool_a, pool_b)
+    _, st_ref = oracle.verify(vi.q, vi.k, vi.v, vi.g, vi.beta, vi.state_pool, vi.accepted)
+    assert rel_fro(to_np(pool_b[:vi.q.shape[0]]), st_ref) <= (1e-2 if bf16 else 1e-4)
