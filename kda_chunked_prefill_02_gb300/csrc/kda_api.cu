@@ -1,6 +1,7 @@
 // kda_api.cu -- the C ABI of include/kda.h: host-side argument checks, the
 // workspace plan, TMA descriptors and the kernel launches.  Nothing here
 // allocates or caches device memory.
+#include <stdlib.h>
 #include <string.h>
 
 #include "../../include/kda.h"
@@ -136,8 +137,8 @@ kda_status run_prefill(const kda_prefill_args* a, void* stream, int stages) {
     PrepMaps pmaps;
     memset(&pmaps, 0, sizeof(pmaps));
     int num_sms = 1;
-    if (prep) {
-        if (!make_prep_maps(a, &pmaps)) return KDA_ERR_UNSUPPORTED;
+    if (prep && !make_prep_maps(a, &pmaps)) return KDA_ERR_UNSUPPORTED;
+    {
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -150,7 +151,16 @@ kda_status run_prefill(const kda_prefill_args* a, void* stream, int stages) {
         if (launch_chunk_table(p, s) != cudaSuccess) return KDA_ERR_CUDA;
         if (launch_prep(p, pmaps, num_sms, s) != cudaSuccess) return KDA_ERR_CUDA;
     }
-    if (state_pass && launch_state(p, s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (state_pass) {
+        // One CTA per chain (all 128 value columns) when the 32-column slab CTAs
+        // would not fit in one wave; the two kernels compute the same chunk step.
+        // KDA_STATE_KERNEL=head|slab overrides the choice (tests, measurements).
+        const char* force = getenv("KDA_STATE_KERNEL");
+        const bool head = force && !strcmp(force, "head") ? true
+                          : force && !strcmp(force, "slab") ? false
+                          : (long long)p.N * p.H * (kHeadDim / kSlab) > num_sms;
+        if ((head ? launch_state_head(p, s) : launch_state(p, s)) != cudaSuccess) return KDA_ERR_CUDA;
+    }
     return KDA_OK;
 }
 

@@ -98,6 +98,7 @@ struct PrepMaps {
 cudaError_t launch_chunk_table(const PrefillParams& p, cudaStream_t s);
 cudaError_t launch_prep(const PrefillParams& p, const PrepMaps& maps, int num_sms, cudaStream_t s);
 cudaError_t launch_state(const PrefillParams& p, cudaStream_t s);
+cudaError_t launch_state_head(const PrefillParams& p, cudaStream_t s);
 
 struct VerifyParams {
     const __nv_bfloat16* q;

@@ -1,0 +1,293 @@
+// kda_state_head.cu -- the serial inter-chunk state pass (steps A6-A7) with one
+// CTA per whole chain (sequence n, head h): all 128 value columns of the state.
+//
+// A tcgen05.mma of M = 128 and K = 16 takes the same ~100 SM cycles for every
+// N <= 128 on this GPU (measured by the MMA throughput probe in the selftest
+// library), so one CTA that runs the chunk step at N = 128 costs about what a
+// 32-column slab CTA costs, and needs a quarter of the CTAs.  That matters when
+// there are more chains than SMs (the slab kernel then runs in several waves),
+// and it leaves SMs free for other work.  Per chunk, with the record the prep
+// kernel left (W, Q', Kt, U, O_loc, e^gam):
+//   P1 (tensor core)  D1 = [W ; Q'] S    M = 128 (64 W rows + 64 Q' rows), N = 128, K = 128
+//   epilogue          V_new = U - D1[0:64],  O = O_loc + D1[64:128] -> out (bf16)
+//   P2 (tensor core)  D2 = Kt V_new       M = 128 keys, N = 128, K = 64 tokens
+//   epilogue          S <- Diag(e^gam) S + D2   (fp32 in registers, bf16 image for P1)
+// Warp roles: all 16 warps are the epilogue, warp w owning TMEM lane quarter
+// w % 4 and the 32-column quarter w / 4, so a thread holds 32 fp32 state
+// values as in the slab kernel.  One thread of an output warp issues the MMAs
+// (an MMA issue holds its thread for tens of cycles, and the output rows are
+// off the serial chain) and the record copies: each record arrives by one 1-D
+// bulk copy into one of two stages, issued as soon as the chunk barrier has
+// shown the stage's previous chunk finished with it (P2 complete, every read
+// done), with an L2 prefetch further ahead.  Hand-offs are
+// mbarriers and named barriers; every mbarrier wait is bounded, and the chunk
+// barrier's OR-reduction of the abort flag makes all epilogue warps stop at the
+// same chunk.  Every MMA has completed, and every thread that read TMEM has
+// waited for its loads and crossed a tcgen05 fence plus a CTA barrier, before
+// TMEM is freed (the dealloc ordering of the TensorRT-LLM MQA-logits page).
+#include "kda_internal.h"
+#include "sm103.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int kHeadThreads = 16 * 32;
+constexpr uint32_t SH_A1 = 0;          // [W ; Q'] 2 x (128 rows x 128 B)
+constexpr uint32_t SH_KT = 32768;      // Kt 128 rows x 128 B
+constexpr uint32_t SH_U = 49152;       // U: 4 value slabs (64-byte swizzle), 16 KB
+constexpr uint32_t SH_OL = 65536;      // O_loc, same layout
+constexpr uint32_t SH_EG = 81920;      // e^gam [128] fp32
+constexpr uint32_t kHStageTx = kRecBytes;  // the whole record, one bulk copy
+constexpr uint32_t kHStage = 82944;     // kRecBytes rounded up to 1 KB (swizzle atoms)
+constexpr int kHStages = 2;
+constexpr int kHPrefetchAhead = 4;
+// B operands of P1 and P2, MN-major with the 128-byte swizzle: per K index
+// (key for S, token for V_new) two 64-column atoms 1024 B apart, 8-row groups
+// 2048 B apart.
+constexpr uint32_t kHSbo = 2048;
+constexpr uint32_t OH_S = kHStages * kHStage;       // S bf16: 128 key rows (32 KB)
+constexpr uint32_t OH_VN = OH_S + 32768;            // V_new bf16: 64 token rows (16 KB)
+constexpr uint32_t kHeadSmem = OH_VN + 16384 + 1024;
+constexpr uint32_t TMH_D1 = 0, TMH_D2 = 128, TMH_COLS = 256;
+constexpr uint32_t kBarHVn = 1, kBarHChunk = 2;     // named barriers (0 is __syncthreads)
+
+__device__ __forceinline__ bool warp_wait_h(uint64_t* bar, uint32_t parity, volatile int* abort) {
+    const bool ok = mbar_wait(bar, parity, abort);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Row `r`, columns 32*cq .. 32*cq + 31 of an MN-major image: four 16-byte chunks.
+__device__ __forceinline__ void store_quarter(uint8_t* base, int r, int cq, const float* x) {
+    uint8_t* rp = base + (r >> 3) * kHSbo + (cq >> 1) * 1024 + (r & 7) * 128;
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch) {
+        const int c = 4 * (cq & 1) + ch;
+        *reinterpret_cast<uint4*>(rp + ((c ^ (r & 7)) << 4)) =
+            make_uint4(pack_bf16x2(x[8 * ch], x[8 * ch + 1]), pack_bf16x2(x[8 * ch + 2], x[8 * ch + 3]),
+                       pack_bf16x2(x[8 * ch + 4], x[8 * ch + 5]), pack_bf16x2(x[8 * ch + 6], x[8 * ch + 7]));
+    }
+}
+
+__global__ void __launch_bounds__(kHeadThreads, 1) state_head_kernel(const PrefillParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+    __shared__ uint64_t full[kHStages], p1_done, p2_done, bar_fin;
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int abort_flag;
+
+    const int h = blockIdx.x, n = blockIdx.y;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    // Chain extent.
+    int first, count, seq_len, b, tbase;
+    if (p.cu == nullptr) {
+        const int cps = (p.T + kChunk - 1) / kChunk;
+        first = n * cps; count = cps; seq_len = p.T; b = n; tbase = 0;
+    } else {
+        first = p.chunk_off[n];
+        count = p.chunk_off[n + 1] - first;
+        seq_len = p.cu[n + 1] - p.cu[n];
+        b = 0; tbase = p.cu[n];
+        if (count < 0) count = 0;
+    }
+
+    if (tid == 0) {
+        for (int i = 0; i < kHStages; ++i) mbar_init(&full[i], 1);
+        mbar_init(&p1_done, 1); mbar_init(&p2_done, 1); mbar_init(&bar_fin, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_base_sh, TMH_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = tmem_base_sh;
+    volatile int* abort = &abort_flag;
+    auto fail = [&]() {
+        if (atomicExch(&abort_flag, 1) == 0) atomicExch(p.status, 4);
+    };
+    auto rec_ptr = [&](int c) -> const uint8_t* {
+        return p.ws_rec + (size_t)((first + c) * p.H + h) * kRecBytes;
+    };
+
+    {
+        // ---------------- lane quarter qd, column quarter cq, thread row = key / token
+        const int qd = warp & 3, cq = warp >> 2;
+        const int row = 32 * qd + lane;
+        const uint32_t lane_base = (uint32_t)(32 * qd) << 16;
+        const bool issuer = (warp == 2 && lane == 0);  // warp 2: an output warp
+        const uint32_t id = idesc_bf16_f32_bmn(128, 128);
+        const uint32_t sS_addr = smem_u32(sm + OH_S), sVn_addr = smem_u32(sm + OH_VN);
+        float S[kSlab];
+        const size_t st_off = (((size_t)n * p.H + h) * kHeadDim + row) * kHeadDim + kSlab * cq;
+        if (p.h0) {
+            const float4* src = reinterpret_cast<const float4*>(p.h0 + st_off);
+#pragma unroll
+            for (int x = 0; x < kSlab / 4; ++x) {
+                const float4 t = src[x];
+                S[4 * x] = t.x; S[4 * x + 1] = t.y; S[4 * x + 2] = t.z; S[4 * x + 3] = t.w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < kSlab; ++j) S[j] = 0.f;
+        }
+        // Records of chunks 0 and 1 into the two stages.
+        auto issue_load = [&](int c) {
+            const int st = c % kHStages;
+            mbar_arrive_expect_tx(&full[st], kHStageTx);
+            bulk_load(sm + st * kHStage, rec_ptr(c), kRecBytes, &full[st]);
+            if (c + kHPrefetchAhead < count) bulk_prefetch_l2(rec_ptr(c + kHPrefetchAhead), kRecBytes);
+        };
+        int issued = 0;  // records requested so far (issuer thread)
+        if (issuer)
+            for (; issued < kHStages && issued < count; ++issued) issue_load(issued);
+        store_quarter(sm + OH_S, row, cq, S);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        named_bar_or(kBarHChunk, 512, false);
+        int done = 0;    // chunks finished
+
+        for (int c = 0; c < count; ++c) {
+            const int st = c % kHStages;
+            const uint8_t* sb = sm + st * kHStage;
+            const uint32_t sb_addr = smem_u32(sb);
+            bool ok = warp_wait_h(&full[st], (c / kHStages) & 1, abort);
+            if (issuer && ok) {
+                tc_fence_after();
+                const uint64_t ad = sdesc_kmajor_sw128(sb_addr + SH_A1);
+                const uint64_t bd = sdesc_mnmajor_sw128(sS_addr, 1024u, kHSbo);
+#pragma unroll
+                for (uint32_t k = 0; k < 8; ++k)
+                    umma_bf16(tb + TMH_D1, ad + ((k >> 2) * (16384 >> 4) + (k & 3) * 2),
+                              bd + k * ((2 * kHSbo) >> 4), id, k > 0 ? 1u : 0u);
+                umma_commit(&p1_done);
+            }
+            __syncwarp();
+            // This thread's U (W rows) or O_loc (Q' rows) values, read while P1 runs.
+            uint4 sr[4];
+            {
+                const uint8_t* src = sb + (qd < 2 ? SH_U : SH_OL) + cq * kSlabImg;
+                const int r = qd < 2 ? row : row - 64;
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) sr[ch] = *reinterpret_cast<const uint4*>(src + slab_chunk_off(r, ch));
+            }
+            ok = ok && warp_wait_h(&p1_done, c & 1, abort);
+            tc_fence_after();
+            float d[kSlab];
+            if (ok) {
+                tmem_ld16(tb + lane_base + TMH_D1 + kSlab * cq, *reinterpret_cast<float(*)[16]>(&d[0]));
+                tmem_ld16(tb + lane_base + TMH_D1 + kSlab * cq + 16, *reinterpret_cast<float(*)[16]>(&d[16]));
+            }
+            if (qd < 2) {
+                // V_new = U - W S for token row `row`
+                if (ok) {
+                    float vn[kSlab];
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch) {
+                        const uint32_t uw[4] = {sr[ch].x, sr[ch].y, sr[ch].z, sr[ch].w};
+#pragma unroll
+                        for (int x = 0; x < 4; ++x) {
+                            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&uw[x]));
+                            vn[8 * ch + 2 * x] = f.x - d[8 * ch + 2 * x];
+                            vn[8 * ch + 2 * x + 1] = f.y - d[8 * ch + 2 * x + 1];
+                        }
+                    }
+                    store_quarter(sm + OH_VN, row, cq, vn);
+                    fence_proxy_async_smem();
+                }
+                tc_fence_before();
+                named_bar_sync(kBarHVn, 288);  // the eight V_new warps and the issuer's warp
+            } else {
+                if (warp == 2) {
+                    tc_fence_before();
+                    named_bar_sync(kBarHVn, 288);
+                    if (issuer && ok && !*abort) {
+                        tc_fence_after();
+                        const uint64_t kt = sdesc_kmajor_sw128(sb_addr + SH_KT);
+                        const uint64_t bv = sdesc_mnmajor_sw128(sVn_addr, 1024u, kHSbo);
+#pragma unroll
+                        for (uint32_t k = 0; k < 4; ++k)  // K = 64 tokens
+                            umma_bf16(tb + TMH_D2, kt + k * 2, bv + k * ((2 * kHSbo) >> 4), id, k > 0 ? 1u : 0u);
+                        umma_commit(&p2_done);
+                    }
+                    __syncwarp();
+                }
+                // O = O_loc + Q' S for token row `row - 64`
+                const int i = row - 64, t0 = 64 * c;
+                if (ok && t0 + i < seq_len) {
+                    uint32_t o[kSlab / 2];
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch) {
+                        const uint32_t ow[4] = {sr[ch].x, sr[ch].y, sr[ch].z, sr[ch].w};
+#pragma unroll
+                        for (int x = 0; x < 4; ++x) {
+                            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[x]));
+                            o[4 * ch + x] = pack_bf16x2(f.x + d[8 * ch + 2 * x], f.y + d[8 * ch + 2 * x + 1]);
+                        }
+                    }
+                    const int64_t t = (int64_t)tbase + t0 + i;
+                    uint4* dst = reinterpret_cast<uint4*>(p.out + b * p.os[0] + t * p.os[1] + h * p.os[2] + kSlab * cq);
+#pragma unroll
+                    for (int x = 0; x < kSlab / 8; ++x) dst[x] = make_uint4(o[4 * x], o[4 * x + 1], o[4 * x + 2], o[4 * x + 3]);
+                }
+                tc_fence_before();
+            }
+            ok = ok && warp_wait_h(&p2_done, c & 1, abort);
+            tc_fence_after();
+            if (ok) {
+                tmem_ld16(tb + lane_base + TMH_D2 + kSlab * cq, *reinterpret_cast<float(*)[16]>(&d[0]));
+                tmem_ld16(tb + lane_base + TMH_D2 + kSlab * cq + 16, *reinterpret_cast<float(*)[16]>(&d[16]));
+                const float eg = reinterpret_cast<const float*>(sb + SH_EG)[row];
+#pragma unroll
+                for (int j = 0; j < kSlab; ++j) S[j] = fmaf(eg, S[j], d[j]);
+                if (c + 1 < count) {
+                    store_quarter(sm + OH_S, row, cq, S);
+                    fence_proxy_async_smem();
+                }
+            } else {
+                fail();
+            }
+            tc_fence_before();
+            if (named_bar_or(kBarHChunk, 512, *abort != 0)) break;
+            done = c + 1;
+            // stage st is free: P2 of chunk c completed and every read of it is done
+            if (issuer && issued < count) issue_load(issued++);
+        }
+        if (issuer) {
+            // Never leave with a copy in flight (bounded; normally complete).
+            for (int c = done; c < issued; ++c) mbar_wait(&full[c % kHStages], (c / kHStages) & 1, nullptr);
+        }
+        if (issuer && count > 0) {
+            // every product issued has completed before TMEM is released
+            umma_commit(&bar_fin);
+            mbar_wait(&bar_fin, 0, nullptr);
+        }
+        if (!*abort && p.hT) {
+            float4* dst = reinterpret_cast<float4*>(p.hT + st_off);
+#pragma unroll
+            for (int x = 0; x < kSlab / 4; ++x)
+                dst[x] = make_float4(S[4 * x], S[4 * x + 1], S[4 * x + 2], S[4 * x + 3]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tb, TMH_COLS);
+}
+
+}  // namespace
+
+cudaError_t launch_state_head(const PrefillParams& p, cudaStream_t s) {
+    if (p.N == 0 || p.H == 0) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(state_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kHeadSmem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.H, p.N);
+    state_head_kernel<<<grid, kHeadThreads, kHeadSmem, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace kda
