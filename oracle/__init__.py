@@ -15,6 +15,8 @@ Contents
     (Kimi Delta Attention as named by the TensorRT-LLM "Kimi K3 KDA prefill"
     page, Description; fp64 oracle practice from the cuDNN-frontend sm90 KDA
     page, Conversation).
+  * ``norm.gated_rmsnorm``: the gated RMSNorm of the output (a reading of the
+    TensorRT-LLM "Kimi K3 work for Rubin (SM107)" page; formula in norm.py).
   * ``chunked``: an independent numpy fp64 restatement in chunked (WY / UT)
     form, used only to pin the sequential oracle by brute force on tiny inputs
     and to give reference values for per-chunk intermediates.

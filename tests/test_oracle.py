@@ -266,3 +266,41 @@ def test_verify_matches_prefill_prefixes(oracle):
         _, fa = oracle.prefill(q[r, :a], k[r, :a], v[r, :a], g[r, :a], b[r, :a],
                                cu_seqlens=[0, a], initial_state=pool[slot[r]][None])
         np.testing.assert_array_equal(st[r], fa[0])
+
+
+# ---- gated RMSNorm of the output (oracle/norm.py), pinned by closed forms
+
+
+def test_gated_rmsnorm_constant_row_closed_form():
+    """o = c (every channel): mean(o^2) = c^2, so y = c / sqrt(c^2 + eps) * w * sigmoid(g)."""
+    from oracle.norm import gated_rmsnorm
+    V = 128
+    c, eps = -3.0, 0.25
+    w = np.linspace(0.5, 2.0, V)
+    g = np.linspace(-4.0, 4.0, V)
+    y = gated_rmsnorm(np.full((2, V), c), np.tile(g, (2, 1)), w, eps)
+    expect = c / np.sqrt(c * c + eps) * w / (1.0 + np.exp(-g))
+    assert np.allclose(y, np.tile(expect, (2, 1)), rtol=0, atol=1e-15)
+
+
+def test_gated_rmsnorm_scale_invariance_and_gate_limits():
+    """With eps = 0: y(lambda o) = sign(lambda) y(o); a gate of +40 gives plain
+    RMSNorm times w (the rows then have mean square w^2 weighted), a gate of 0
+    halves it, and a one-hot row o = a e_j gives sqrt(V) sign(a) w_j at j."""
+    from oracle.norm import gated_rmsnorm
+    rng = np.random.default_rng(7)
+    V = 128
+    o = rng.standard_normal((3, V))
+    w = rng.uniform(0.5, 1.5, V)
+    g = rng.standard_normal((3, V))
+    y = gated_rmsnorm(o, g, w, 0.0)
+    assert np.allclose(gated_rmsnorm(7.5 * o, g, w, 0.0), y, rtol=1e-13, atol=1e-14)
+    assert np.allclose(gated_rmsnorm(-0.2 * o, g, w, 0.0), -y, rtol=1e-13, atol=1e-14)
+    plain = gated_rmsnorm(o, np.full_like(g, 40.0), np.ones(V), 0.0)
+    assert np.allclose(np.mean(plain * plain, axis=-1), 1.0, rtol=0, atol=1e-12)
+    half = gated_rmsnorm(o, np.zeros_like(g), np.ones(V), 0.0)
+    assert np.allclose(half, 0.5 * plain, rtol=0, atol=1e-15)
+    e = np.zeros(V)
+    e[5] = -2.0
+    y1 = gated_rmsnorm(e, np.full(V, 40.0), w, 0.0)
+    assert abs(y1[5] - (-np.sqrt(V) * w[5])) < 1e-12 and np.count_nonzero(y1) == 1
