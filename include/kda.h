@@ -115,6 +115,21 @@ typedef struct kda_prefill_args {
     void* workspace;
     size_t workspace_bytes;
     int32_t* device_status;     /* optional device int32 */
+    /* Gated RMSNorm fused into the output (out_gate == NULL: off).  A reading of
+     * the "gated RMSNorm in the epilogue (fuse_output_norm)" of the TensorRT-LLM
+     * page "Kimi K3 work for Rubin (SM107)" (Description), which names it
+     * without a formula: per (token, head), over the 128 value channels c,
+     *   out_c = o_c / sqrt(mean_c(o_c^2) + norm_eps) * norm_weight[c] * sigmoid(gate_c)
+     * with o the attention output in fp32 before rounding.  out_gate: bf16,
+     * element (b, t, h, c) at b*gate_stride[0] + t*gate_stride[1] +
+     * h*gate_stride[2] + c; norm_weight: fp32 [128].  Both or neither;
+     * 16-byte aligned rows (strides multiples of 8) and weight, else
+     * KDA_ERR_UNSUPPORTED.  With the norm on, the state pass always runs one CTA
+     * per chain (the norm needs whole output rows). */
+    const void* out_gate;
+    int64_t gate_stride[3];
+    const float* norm_weight;
+    float norm_eps;
 } kda_prefill_args;
 
 /*
@@ -278,7 +293,8 @@ kda_status kda_prefill_noalloc(const kda_prefill_args* args, void* stream);
  * cudaHostRegister) in the contiguous layouts (padded: q/k/v/g/out
  * [B, T, H, 128], beta [B, T, H]; varlen: [T_total, H, 128] and [T_total, H]),
  * cu_seqlens (varlen) is a HOST int32 array [N + 1], and the stride, workspace
- * and workspace_bytes fields are ignored.
+ * and workspace_bytes fields are ignored; the fused output norm is not
+ * available here (out_gate must be NULL, else KDA_ERR_UNSUPPORTED).
  * staging: caller-owned device memory, 256-byte aligned, at least
  * kda_prefill_host_staging_size(args) bytes; piece_tokens: tokens per piece, a
  * multiple of 64, or 0 for the library's choice (about an eighth of the input,

@@ -68,6 +68,11 @@ kda_status check_prefill(const kda_prefill_args* a) {
     if ((a->initial_state && !aligned16(a->initial_state)) ||
         (a->final_state && !aligned16(a->final_state)))
         return KDA_ERR_UNSUPPORTED;
+    // fused gated RMSNorm: both operands or neither
+    if ((a->out_gate != nullptr) != (a->norm_weight != nullptr)) return KDA_ERR_INVALID_ARG;
+    if (a->out_gate && (!aligned16(a->out_gate) || !aligned16(a->norm_weight) ||
+                        !strides_ok(a->gate_stride, 8) || !(a->norm_eps >= 0.f)))
+        return KDA_ERR_UNSUPPORTED;
     if (a->num_seqs > (1 << 30) || a->num_heads > 65535 || a->seqlen > (int64_t)1 << 31)
         return KDA_ERR_UNSUPPORTED;
     kda_workspace_layout L;
@@ -103,6 +108,10 @@ void fill_params(const kda_prefill_args* a, const kda_workspace_layout& L, Prefi
     p->beta_is_logit = a->beta_is_logit ? 1 : 0;
     p->scale = a->scale;
     p->ws_rec = ws + L.records;
+    p->gate = static_cast<const __nv_bfloat16*>(a->out_gate);
+    for (int i = 0; i < 3; ++i) p->gts[i] = a->gate_stride[i];
+    p->norm_w = a->norm_weight;
+    p->norm_eps = a->norm_eps;
 }
 
 // 4-D input tensor map [channel 128, head, token, batch] with one chunk of
@@ -156,7 +165,9 @@ kda_status run_prefill(const kda_prefill_args* a, void* stream, int stages) {
         // would not fit in one wave; the two kernels compute the same chunk step.
         // KDA_STATE_KERNEL=head|slab overrides the choice (tests, measurements).
         const char* force = getenv("KDA_STATE_KERNEL");
-        const bool head = force && !strcmp(force, "head") ? true
+        // The fused output norm needs whole rows: one CTA per chain.
+        const bool head = p.gate ? true
+                          : force && !strcmp(force, "head") ? true
                           : force && !strcmp(force, "slab") ? false
                           : (long long)p.N * p.H * (kHeadDim / kSlab) > num_sms;
         if ((head ? launch_state_head(p, s) : launch_state(p, s)) != cudaSuccess) return KDA_ERR_CUDA;

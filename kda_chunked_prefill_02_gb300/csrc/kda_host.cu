@@ -122,6 +122,7 @@ extern "C" kda_status kda_prefill_host(const kda_prefill_host_args* h, void* str
     if (!h) return KDA_ERR_INVALID_ARG;
     const kda_prefill_args& a = h->args;
     if (!a.q || !a.k || !a.v || !a.g || !a.beta || !a.out || !h->staging) return KDA_ERR_INVALID_ARG;
+    if (a.out_gate || a.norm_weight) return KDA_ERR_UNSUPPORTED;  // the gate is not staged here
     Plan pl;
     if (!make_plan(h, &pl)) return KDA_ERR_INVALID_ARG;
     if (h->staging_bytes < pl.total || (reinterpret_cast<uintptr_t>(h->staging) & 255))

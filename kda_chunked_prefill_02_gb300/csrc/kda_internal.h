@@ -51,6 +51,10 @@ struct PrefillParams {
     int beta_is_logit;
     float scale;
     uint8_t* ws_rec;         // kRecBytes per (chunk, head) record, record r = chunk * H + head
+    const __nv_bfloat16* gate;   // gated RMSNorm of the output: gate (nullptr = off)
+    int64_t gts[3];              // gate strides (batch, token, head)
+    const float* norm_w;         // [128]
+    float norm_eps;
 };
 
 // Chunk c (global index) -> sequence, token start and length.

@@ -49,7 +49,15 @@ constexpr uint32_t OH_S = kHStages * kHStage;       // S bf16: 128 key rows (32 
 constexpr uint32_t OH_VN = OH_S + 32768;            // V_new bf16: 64 token rows (16 KB)
 constexpr uint32_t kHeadSmem = OH_VN + 16384 + 1024;
 constexpr uint32_t TMH_D1 = 0, TMH_D2 = 128, TMH_COLS = 256;
-constexpr uint32_t kBarHVn = 1, kBarHChunk = 2;     // named barriers (0 is __syncthreads)
+constexpr uint32_t kBarHVn = 1, kBarHChunk = 2, kBarHNorm = 3;  // named barriers (0 is __syncthreads)
+
+// sigmoid(x) = 1/2 + tanh(x/2)/2, with the hardware tanh approximation
+// (relative error ~2^-11, below the bf16 rounding of the output).
+__device__ __forceinline__ float sigmoid_fast(float x) {
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * x));
+    return fmaf(0.5f, t, 0.5f);
+}
 
 __device__ __forceinline__ bool warp_wait_h(uint64_t* bar, uint32_t parity, volatile int* abort) {
     const bool ok = mbar_wait(bar, parity, abort);
@@ -75,6 +83,8 @@ __global__ void __launch_bounds__(kHeadThreads, 1) state_head_kernel(const Prefi
     __shared__ uint64_t full[kHStages], p1_done, p2_done, bar_fin;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
+    __shared__ float s_ss[4][64];      // fused norm: partial sums of squares per column quarter
+    __shared__ __align__(16) float s_w[kHeadDim];  // fused norm: weights
 
     const int h = blockIdx.x, n = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -98,6 +108,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1) state_head_kernel(const Prefi
         abort_flag = 0;
         fence_mbar_init();
     }
+    if (p.gate && tid < kHeadDim) s_w[tid] = p.norm_w[tid];
     if (warp == 0) {
         tmem_alloc(&tmem_base_sh, TMH_COLS);
         tmem_relinquish();
@@ -218,21 +229,57 @@ __global__ void __launch_bounds__(kHeadThreads, 1) state_head_kernel(const Prefi
                 }
                 // O = O_loc + Q' S for token row `row - 64`
                 const int i = row - 64, t0 = 64 * c;
-                if (ok && t0 + i < seq_len) {
-                    uint32_t o[kSlab / 2];
+                const bool valid_row = t0 + i < seq_len;
+                const int64_t t = (int64_t)tbase + t0 + i;
+                float o[kSlab];
 #pragma unroll
-                    for (int ch = 0; ch < 4; ++ch) {
-                        const uint32_t ow[4] = {sr[ch].x, sr[ch].y, sr[ch].z, sr[ch].w};
+                for (int ch = 0; ch < 4; ++ch) {
+                    const uint32_t ow[4] = {sr[ch].x, sr[ch].y, sr[ch].z, sr[ch].w};
 #pragma unroll
-                        for (int x = 0; x < 4; ++x) {
-                            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[x]));
-                            o[4 * ch + x] = pack_bf16x2(f.x + d[8 * ch + 2 * x], f.y + d[8 * ch + 2 * x + 1]);
+                    for (int x = 0; x < 4; ++x) {
+                        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[x]));
+                        o[8 * ch + 2 * x] = f.x + d[8 * ch + 2 * x];
+                        o[8 * ch + 2 * x + 1] = f.y + d[8 * ch + 2 * x + 1];
+                    }
+                }
+                if (p.gate) {
+                    // gated RMSNorm over the 128 channels of the row: the four column
+                    // quarters' sums of squares meet in shared memory
+                    uint4 gw[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
+                                   make_uint4(0, 0, 0, 0)};
+                    if (ok && valid_row) {
+                        const uint4* gsrc = reinterpret_cast<const uint4*>(p.gate + b * p.gts[0] + t * p.gts[1] +
+                                                                           h * p.gts[2] + kSlab * cq);
+#pragma unroll
+                        for (int x = 0; x < 4; ++x) gw[x] = gsrc[x];
+                    }
+                    float ss = 0.f;
+#pragma unroll
+                    for (int j = 0; j < kSlab; ++j) ss = fmaf(o[j], o[j], ss);
+                    s_ss[cq][i] = ss;
+                    named_bar_sync(kBarHNorm, 256);  // the eight output warps
+                    const float ms = (s_ss[0][i] + s_ss[1][i] + s_ss[2][i] + s_ss[3][i]) * (1.0f / kHeadDim);
+                    const float rn = rsqrtf(ms + p.norm_eps);
+                    const float4* wq = reinterpret_cast<const float4*>(s_w + kSlab * cq);
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) {
+                        const uint32_t gv[4] = {gw[x].x, gw[x].y, gw[x].z, gw[x].w};
+                        const float4 w0 = wq[2 * x], w1 = wq[2 * x + 1];
+                        const float ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gv[e]));
+                            o[8 * x + 2 * e] *= rn * ww[2 * e] * sigmoid_fast(gf.x);
+                            o[8 * x + 2 * e + 1] *= rn * ww[2 * e + 1] * sigmoid_fast(gf.y);
                         }
                     }
-                    const int64_t t = (int64_t)tbase + t0 + i;
+                }
+                if (ok && valid_row) {
                     uint4* dst = reinterpret_cast<uint4*>(p.out + b * p.os[0] + t * p.os[1] + h * p.os[2] + kSlab * cq);
 #pragma unroll
-                    for (int x = 0; x < kSlab / 8; ++x) dst[x] = make_uint4(o[4 * x], o[4 * x + 1], o[4 * x + 2], o[4 * x + 3]);
+                    for (int x = 0; x < kSlab / 8; ++x)
+                        dst[x] = make_uint4(pack_bf16x2(o[8 * x], o[8 * x + 1]), pack_bf16x2(o[8 * x + 2], o[8 * x + 3]),
+                                            pack_bf16x2(o[8 * x + 4], o[8 * x + 5]), pack_bf16x2(o[8 * x + 6], o[8 * x + 7]));
                 }
                 tc_fence_before();
             }

@@ -33,7 +33,8 @@ class PrefillArgs(ctypes.Structure):
                 ("chunk", ctypes.c_int32), ("beta_is_logit", ctypes.c_int32),
                 ("scale", ctypes.c_float),
                 ("workspace", _p), ("workspace_bytes", ctypes.c_size_t),
-                ("device_status", _p)]
+                ("device_status", _p), ("out_gate", _p), ("gate_stride", _i64x3),
+                ("norm_weight", _p), ("norm_eps", ctypes.c_float)]
 
 
 class PrefillHostArgs(ctypes.Structure):
@@ -141,7 +142,8 @@ def _strides3(t, varlen, last_is_channel=True):
 
 
 def _prefill_args(q, k, v, g, beta, initial_state, cu_seqlens, out, final_state, beta_is_logit,
-                  scale, workspace, device_status, chunk):
+                  scale, workspace, device_status, chunk, out_gate=None, norm_weight=None,
+                  norm_eps=1e-6):
     varlen = cu_seqlens is not None
     for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16),
                         ("v", v, torch.bfloat16), ("g", g, torch.float32),
@@ -178,6 +180,13 @@ def _prefill_args(q, k, v, g, beta, initial_state, cu_seqlens, out, final_state,
     a.workspace = _ptr(workspace)
     a.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     a.device_status = _ptr(device_status)
+    if out_gate is not None or norm_weight is not None:
+        _need_cuda("out_gate", out_gate, torch.bfloat16)
+        _need_cuda("norm_weight", norm_weight, torch.float32)
+        a.out_gate = _ptr(out_gate)
+        a.gate_stride = _i64x3(*_strides3(out_gate, varlen))
+        a.norm_weight = _ptr(norm_weight.contiguous())
+        a.norm_eps = float(norm_eps)
     return a
 
 
@@ -209,7 +218,7 @@ def workspace_layout(q, *, cu_seqlens=None):
 def kda_prefill(q, k, v, g, beta, *, initial_state=None, cu_seqlens=None, chunk=CHUNK,
                 beta_is_logit=True, scale=1.0, out=None, final_state=None,
                 output_final_state=True, workspace=None, device_status=None, stream=None,
-                prep_only=False, stage=None):
+                prep_only=False, stage=None, out_gate=None, norm_weight=None, norm_eps=1e-6):
     """KDA prefill through the C ABI.
 
     Padded: q, k, g [B, T, H, 128]; v [B, T, H, 128]; beta [B, T, H].
@@ -231,7 +240,8 @@ def kda_prefill(q, k, v, g, beta, *, initial_state=None, cu_seqlens=None, chunk=
         nbytes = workspace_size(q, v, cu_seqlens=cu_seqlens)
         workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
     a = _prefill_args(q, k, v, g, beta, initial_state, cu_seqlens, out, final_state,
-                      beta_is_logit, scale, workspace, device_status, chunk)
+                      beta_is_logit, scale, workspace, device_status, chunk, out_gate, norm_weight,
+                      norm_eps)
     fn = {None: lib().kda_prefill, "prep": lib().kda_prefill_prep,
           "state": lib().kda_prefill_state}[stage]
     if prep_only:
