@@ -162,14 +162,16 @@ kda_status run_prefill(const kda_prefill_args* a, void* stream, int stages) {
     }
     if (state_pass) {
         // One CTA per chain (all 128 value columns) when the 32-column slab CTAs
-        // would not fit in one wave; the two kernels compute the same chunk step.
-        // KDA_STATE_KERNEL=head|slab overrides the choice (tests, measurements).
+        // would need more than two waves of SMs: a whole-chain CTA takes about
+        // twice as long per chunk step (measured), so below that the slab kernel
+        // is as fast or faster.  The two kernels compute the same chunk step.
+        // KDA_STATE_KERNEL=head|slab overrides the choice (tests, measurements);
+        // the fused output norm needs whole rows and always takes the head kernel.
         const char* force = getenv("KDA_STATE_KERNEL");
-        // The fused output norm needs whole rows: one CTA per chain.
         const bool head = p.gate ? true
                           : force && !strcmp(force, "head") ? true
                           : force && !strcmp(force, "slab") ? false
-                          : (long long)p.N * p.H * (kHeadDim / kSlab) > num_sms;
+                          : (long long)p.N * p.H * (kHeadDim / kSlab) > 2LL * num_sms;
         if ((head ? launch_state_head(p, s) : launch_state(p, s)) != cudaSuccess) return KDA_ERR_CUDA;
     }
     return KDA_OK;
