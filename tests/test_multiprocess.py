@@ -1,0 +1,62 @@
+"""Multi-process (world size 2) checks of the bench's host-side rank logic on
+CPU with the gloo backend: every (sequence, head) chain is independent, so N
+GPUs run N replicas with no data-path collective; the only collectives are the
+timing barrier and the max over ranks of the elapsed time.  The reference arm
+under torchrun must print one line, from rank 0, with every rank exiting 0."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), WORLD_SIZE="2",
+                      RANK=str(rank), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+    import torch.distributed as dist
+    r, ws, _ = bench.dist_init(2)
+    bench.barrier(ws)
+    m = bench.max_over_ranks(10.0 + r, ws)
+    q.put((r, ws, m, dist.get_backend()))
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_agree_on_the_max_time():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(2))
+    assert [g[0] for g in got] == [0, 1]
+    assert all(g[1] == 2 and g[2] == 11.0 and g[3] == "gloo" for g in got)
+
+
+def test_reference_arm_under_torchrun_prints_once_from_rank_zero():
+    port = _free_port()
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+           "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "0", "--config", "tiny"]
+    r = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    rec = json.loads(lines[0])
+    assert rec["impl"] == "reference" and rec["n_gpus"] == 2 and rec["value"] > 0
