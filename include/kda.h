@@ -297,8 +297,8 @@ kda_status kda_prefill_noalloc(const kda_prefill_args* args, void* stream);
  * available here (out_gate must be NULL, else KDA_ERR_UNSUPPORTED).
  * staging: caller-owned device memory, 256-byte aligned, at least
  * kda_prefill_host_staging_size(args) bytes; piece_tokens: tokens per piece, a
- * multiple of 64, or 0 for the library's choice (about an eighth of the input,
- * at least 1024).
+ * multiple of 64, or 0 for the library's choice (about a thirty-second of the
+ * input, at least 2048 tokens).
  *
  * The work is cut into pieces (padded: a range of chunk-aligned tokens of every
  * sequence, with each chain's state carried from piece to piece on the device,

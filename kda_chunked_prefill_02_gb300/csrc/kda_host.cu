@@ -54,7 +54,7 @@ bool make_plan(const kda_prefill_host_args* h, Plan* pl) {
     if (!pl->varlen) {
         if (a.batch < 1 || a.seqlen < 0 || a.num_seqs != a.batch) return false;
         pl->B = a.batch; pl->T = a.seqlen; pl->N = a.batch;
-        int64_t P = h->piece_tokens ? h->piece_tokens : up64(std::max<int64_t>((pl->T + 7) / 8, 1024));
+        int64_t P = h->piece_tokens ? h->piece_tokens : up64(std::max<int64_t>((pl->T + 31) / 32, 2048));
         P = std::min(P, std::max<int64_t>(up64(pl->T), kChunk));
         if (pl->T == 0) pl->pieces.push_back({0, 0, 0, 0});
         for (int64_t t0 = 0; t0 < pl->T; t0 += P) pl->pieces.push_back({t0, std::min(P, pl->T - t0), 0, 0});
@@ -67,7 +67,7 @@ bool make_plan(const kda_prefill_host_args* h, Plan* pl) {
         if (cu[0] != 0 || cu[pl->N] != pl->T) return false;
         for (int64_t n = 0; n < pl->N; ++n)
             if (cu[n + 1] < cu[n]) return false;
-        const int64_t P = h->piece_tokens ? h->piece_tokens : up64(std::max<int64_t>((pl->T + 7) / 8, 1024));
+        const int64_t P = h->piece_tokens ? h->piece_tokens : up64(std::max<int64_t>((pl->T + 31) / 32, 2048));
         int64_t n0 = 0;
         while (n0 < pl->N) {
             int64_t n1 = n0 + 1;
