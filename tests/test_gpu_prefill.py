@@ -212,3 +212,33 @@ def test_split_stages_equal_one_call():
                       cu_seqlens=d.cu_seqlens, workspace=ws, stage="state")
     torch.cuda.synchronize()
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_padded_zero_length_keeps_the_state():
+    """B sequences of T = 0 tokens: no chunk at all, the final state is the
+    initial one bit for bit (both state kernels)."""
+    import os
+    import kda_chunked_prefill_02_gb300 as K
+    inp = inputs.prefill_inputs(701, B=2, T=64, H=3)
+    d = inp.to("cuda")
+    q, k, v, g, b = (t[:, :0].contiguous() for t in (d.q, d.k, d.v, d.g, d.beta))
+    for kern in ("slab", "head"):
+        os.environ["KDA_STATE_KERNEL"] = kern
+        try:
+            out, fin = K.kda_prefill(q, k, v, g, b, initial_state=d.initial_state)
+            torch.cuda.synchronize()
+        finally:
+            del os.environ["KDA_STATE_KERNEL"]
+        assert out.numel() == 0
+        assert torch.equal(fin, d.initial_state)
+
+
+def test_many_heads_sampled():
+    """H = 300 heads (grids and record indexing far past the workloads' 32),
+    ragged T; oracle on a few heads."""
+    inp = inputs.prefill_inputs(702, B=1, T=150, H=300)
+    out, fin = gpu_prefill(inp)
+    heads = [0, 1, 137, 299]
+    sub = head_subset(inp, heads)
+    ro, rf = oracle_prefill(sub)
+    assert_parity(out[:, :, heads], fin[:, heads], ro, rf, "H=300")
