@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyP
         const Item after = nit + (int)gridDim.x < nitems ? item_of(nit + gridDim.x) : Item{0, 0, 0, 0, false};
         if (cur.valid) {
             uint8_t* st = state_of(cur);
-            // replay-only: the chunk is the accepted drafts and only the state is stored
+            // replay-only: run just the accepted drafts; write no output, keep the state
             const int tend = p.replay_only ? cur.acc : D;
             for (int t = 0; t < tend; ++t) {
                 const uint8_t* row = tb + t * kTokBytes;
