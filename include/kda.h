@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define KDA_ABI_VERSION 2
+#define KDA_ABI_VERSION 3
 
 typedef enum {
     KDA_OK = 0,
@@ -149,9 +149,30 @@ size_t kda_prefill_workspace_size(const kda_prefill_args* args);
  *      attention folded into Q' = Q e^Gam - Aqk W and O_loc = Aqk U;
  *   A6-A7 the serial inter-chunk state pass on tcgen05 tensor cores, per
  *      (sequence, head, value slab), with the output epilogue.
+ * Padded calls with few, long chains are run in token segments: the state
+ * pass of segment s (on a second stream, joined back into `stream` before
+ * the call's work ends) overlaps the prep of segment s+1, the state of every
+ * chain passing between segments in fp32 through the workspace's
+ * state_carry region, so the results are those of one state pass over the
+ * whole sequence.  KDA_SEGMENT_CHUNKS=n in the environment forces segments of
+ * n chunks (0: never segment).
  * Returns KDA_OK once the kernels are enqueued.
  */
 kda_status kda_prefill(const kda_prefill_args* args, void* stream);
+
+/*
+ * The schedule kda_prefill would run for these arguments on a GPU with
+ * num_sms SMs (host only: no device call; reads the same environment
+ * overrides as kda_prefill).  segmented: 1 if the tokens are cut into
+ * segments of segment_chunks chunks, the state pass of one beside the prep
+ * of the next, prep on prep_ctas CTAs; whole_chain: 1 if the state pass runs
+ * one CTA per chain (all 128 value columns), 0 for four 32-column slab CTAs
+ * per chain.  KDA_ERR_INVALID_ARG for NULL pointers or num_sms < 1.
+ */
+typedef struct kda_schedule {
+    int32_t segmented, whole_chain, segment_chunks, prep_ctas;
+} kda_schedule;
+kda_status kda_prefill_schedule(const kda_prefill_args* args, int num_sms, kda_schedule* schedule);
 
 /*
  * Runs only steps A1-A5 of kda_prefill and leaves the per-chunk operands in
@@ -186,10 +207,14 @@ kda_status kda_prefill_state(const kda_prefill_args* args, void* stream);
  *   [65536, 81920)    O_loc = Aqk U bf16, same layout
  *   [81920, 82432)    exp(gam) fp32 [128], gam = chunk total of g
  * Rows past a tail chunk's length are zero.  chunk_offset: int32 [N+1].
+ * A segmented kda_prefill (see there) keeps the records of each token segment
+ * together: segment s's records follow those of segments 0..s-1, numbered
+ * as above within the segment.
  */
 typedef struct kda_workspace_layout {
     size_t records, record_bytes, chunk_offset, status, total;
     int64_t max_chunks;         /* records per head */
+    size_t state_carry;         /* padded calls: fp32 [B, H, 128, 128] */
 } kda_workspace_layout;
 kda_status kda_prefill_workspace_layout(const kda_prefill_args* args,
                                         kda_workspace_layout* layout);

@@ -32,6 +32,12 @@ bool layout_of(const kda_prefill_args* a, kda_workspace_layout* L) {
     L->records = o; o = align_up(o + nrec * kRecBytes);
     L->chunk_offset = o; o = align_up(o + sizeof(int32_t) * (size_t)(a->num_seqs + 1));
     L->status = o; o = align_up(o + sizeof(int32_t));
+    // padded calls: the state of every chain between two segments of the
+    // segmented schedule (run_prefill)
+    const size_t carry = a->cu_seqlens == nullptr
+                             ? (size_t)a->batch * (size_t)a->num_heads * kHeadDim * kHeadDim * sizeof(float)
+                             : 0;
+    L->state_carry = o; o = align_up(o + carry);
     L->total = o;
     return true;
 }
@@ -135,6 +141,136 @@ bool make_prep_maps(const kda_prefill_args* a, PrepMaps* m) {
            make_input_map(&m->g, a->g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a->g_stride, H, T, B);
 }
 
+// Which state kernel a sequential call runs: one CTA per chain (all 128 value
+// columns) when the 32-column slab CTAs would need more than two waves of SMs
+// (a whole-chain CTA takes about twice as long per chunk step, measured), so
+// below that the slab kernel is as fast or faster.  The two kernels compute the
+// same chunk step.  KDA_STATE_KERNEL=head|slab overrides the choice (tests,
+// measurements); the fused output norm needs whole rows and always takes the
+// whole-chain kernel.
+bool whole_chain_kernel(const PrefillParams& p, int num_sms) {
+    const char* force = getenv("KDA_STATE_KERNEL");
+    if (p.gate) return true;
+    if (force && !strcmp(force, "head")) return true;
+    if (force && !strcmp(force, "slab")) return false;
+    return (long long)p.N * p.H * (kHeadDim / kSlab) > 2LL * num_sms;
+}
+
+// Segmented schedule of a padded call.  The state pass is one latency-bound
+// chain per (sequence, head), prep is throughput-bound over all SMs, and the
+// two kernels cannot share an SM (each needs most of its shared memory).  With
+// few chains the state pass leaves most SMs idle for its whole length, so the
+// tokens are cut into segments: prep of segment s+1 runs on the SMs the state
+// pass of segment s leaves free.  The choice compares the estimated time of
+// both schedules from per-unit costs measured on GB300 (SM clock 2070 MHz):
+// one (chunk, head) record takes a prep CTA 8.7 us; a chunk step takes 1.14 us
+// in the slab kernel (four CTAs per chain) and 2.14 us in the whole-chain
+// kernel; each extra pair of launches costs about 5 us.
+struct Segments {
+    bool on = false;
+    bool head = false;       // whole-chain state kernel (else slab)
+    int chunks = 0;          // chunks of every sequence per segment
+    int prep_ctas = 0;       // prep grid while a state pass runs beside it
+};
+
+Segments plan_segments(const PrefillParams& p, int num_sms) {
+    constexpr double kRecUs = 8.7, kSlabStepUs = 1.14, kHeadStepUs = 2.14, kLaunchUs = 5.0;
+    Segments sg;
+    if (p.cu != nullptr || p.T <= 0 || p.N <= 0 || num_sms < 4) return sg;
+    const char* env = getenv("KDA_SEGMENT_CHUNKS");
+    const long long forced = env ? atoll(env) : -1;
+    if (forced == 0) return sg;
+    const long long chains = (long long)p.N * p.H, cps = (p.T + kChunk - 1) / kChunk;
+    const char* force = getenv("KDA_STATE_KERNEL");
+    const bool allow_slab = !p.gate && !(force && !strcmp(force, "head"));
+    const bool allow_head = p.gate || !(force && !strcmp(force, "slab"));
+    auto waves = [](long long n, long long m) { return (double)((n + m - 1) / m); };
+    // sequential: prep on every SM, then the state pass
+    double best = waves(cps * chains, num_sms) * kRecUs +
+                  (whole_chain_kernel(p, num_sms) ? waves(chains, num_sms) * cps * kHeadStepUs
+                                                  : waves(4 * chains, num_sms) * cps * kSlabStepUs);
+    if (forced > 0) best = 1e300;
+    for (int head = 0; head < 2; ++head) {
+        if (head ? !allow_head : !allow_slab) continue;
+        if (forced > 0 && (bool)head != whole_chain_kernel(p, num_sms)) continue;
+        const long long state_ctas = head ? chains : 4 * chains;
+        long long ctas = num_sms - state_ctas;
+        if (ctas < num_sms / 4) {
+            if (forced <= 0) continue;  // prep would be starved of SMs
+            ctas = num_sms / 4;
+        }
+        // about 16 prep rounds per segment: short enough that filling and
+        // draining the pipeline is cheap, long enough to amortise the launches
+        const long long seg = forced > 0 ? forced : (16 * ctas / chains > 4 ? 16 * ctas / chains : 4);
+        const long long nseg = (cps + seg - 1) / seg;
+        if (nseg > 65536) continue;
+        const double a = waves(seg * chains, ctas) * kRecUs;
+        const double b = (double)seg * (head ? kHeadStepUs : kSlabStepUs) * waves(state_ctas, num_sms);
+        const double t = a + b + (double)(nseg - 1) * (a > b ? a : b) + (double)nseg * kLaunchUs;
+        if (t < 0.92 * best) {
+            best = t;
+            sg.on = true;
+            sg.head = head != 0;
+            sg.chunks = (int)seg;
+            sg.prep_ctas = (int)ctas;
+        }
+    }
+    return sg;
+}
+
+// Runs a planned segmented call: prep of every segment on `s`, the state pass of
+// every segment on a second stream, each after its segment's prep and after the
+// previous segment's state pass; `s` waits for the last state pass.
+kda_status run_segments(const kda_prefill_args* a, const PrefillParams& p, const Segments& sg,
+                        const kda_workspace_layout& L, cudaStream_t s) {
+    cudaStream_t ss = nullptr;
+    cudaEvent_t ev_prep = nullptr, ev_done = nullptr;
+    auto ck = [](cudaError_t e) { return e == cudaSuccess; };
+    bool ok = ck(cudaStreamCreateWithFlags(&ss, cudaStreamNonBlocking)) &&
+              ck(cudaEventCreateWithFlags(&ev_prep, cudaEventDisableTiming)) &&
+              ck(cudaEventCreateWithFlags(&ev_done, cudaEventDisableTiming));
+    // the side stream starts after the work already queued on `s`
+    ok = ok && ck(cudaEventRecord(ev_prep, s)) && ck(cudaStreamWaitEvent(ss, ev_prep, 0));
+    float* carry = reinterpret_cast<float*>(static_cast<uint8_t*>(a->workspace) + L.state_carry);
+    const int64_t seg_tokens = (int64_t)sg.chunks * kChunk;
+    size_t rec_base = 0;
+    for (int64_t t0 = 0; ok && t0 < p.T; t0 += seg_tokens) {
+        const int ts = (int)(p.T - t0 < seg_tokens ? p.T - t0 : seg_tokens);
+        const bool first = t0 == 0, last = t0 + ts >= p.T;
+        PrefillParams q = p;
+        q.q = p.q + t0 * p.qs[1];
+        q.k = p.k + t0 * p.ks[1];
+        q.v = p.v + t0 * p.vs[1];
+        q.g = p.g + t0 * p.gs[1];
+        q.beta = p.beta + t0 * p.bs[1];
+        q.out = p.out + t0 * p.os[1];
+        if (p.gate) q.gate = p.gate + t0 * p.gts[1];
+        q.T = ts;
+        q.max_chunks = p.B * ((ts + kChunk - 1) / kChunk);
+        q.ws_rec = p.ws_rec + rec_base * kRecBytes;
+        rec_base += (size_t)q.max_chunks * p.H;
+        q.h0 = first ? p.h0 : carry;
+        q.hT = last ? p.hT : carry;   // each chain's state is read before it is rewritten
+        PrepMaps maps;
+        kda_prefill_args sa = *a;
+        sa.q = q.q; sa.k = q.k; sa.v = q.v; sa.g = q.g;
+        sa.seqlen = ts;
+        if (!make_prep_maps(&sa, &maps)) return KDA_ERR_UNSUPPORTED;
+        ok = launch_prep(q, maps, sg.prep_ctas, s) == cudaSuccess &&
+             ck(cudaEventRecord(ev_prep, s)) && ck(cudaStreamWaitEvent(ss, ev_prep, 0)) &&
+             (sg.head ? launch_state_head(q, ss) : launch_state(q, ss)) == cudaSuccess;
+    }
+    if (ss && ev_done) {
+        // join even after a failure, so that nothing queued later on `s`
+        // overtakes a state pass already enqueued
+        if (ck(cudaEventRecord(ev_done, ss))) ck(cudaStreamWaitEvent(s, ev_done, 0));
+    }
+    if (ev_prep) cudaEventDestroy(ev_prep);
+    if (ev_done) cudaEventDestroy(ev_done);
+    if (ss) cudaStreamDestroy(ss);   // released once its work completes
+    return ok ? KDA_OK : KDA_ERR_CUDA;
+}
+
 kda_status run_prefill(const kda_prefill_args* a, void* stream, int stages) {
     const bool state_pass = (stages & 2) != 0, prep = (stages & 1) != 0;
     kda_status st = check_prefill(a);
@@ -143,10 +279,7 @@ kda_status run_prefill(const kda_prefill_args* a, void* stream, int stages) {
     layout_of(a, &L);
     PrefillParams p;
     fill_params(a, L, &p);
-    PrepMaps pmaps;
-    memset(&pmaps, 0, sizeof(pmaps));
     int num_sms = 1;
-    if (prep && !make_prep_maps(a, &pmaps)) return KDA_ERR_UNSUPPORTED;
     {
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -154,24 +287,21 @@ kda_status run_prefill(const kda_prefill_args* a, void* stream, int stages) {
             return KDA_ERR_CUDA;
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (prep && !a->device_status && cudaMemsetAsync(p.status, 0, sizeof(int32_t), s) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    if (prep && state_pass) {
+        const Segments sg = plan_segments(p, num_sms);
+        if (sg.on) return run_segments(a, p, sg, L, s);
+    }
     if (prep) {
-        if (!a->device_status && cudaMemsetAsync(p.status, 0, sizeof(int32_t), s) != cudaSuccess)
-            return KDA_ERR_CUDA;
+        PrepMaps pmaps;
+        memset(&pmaps, 0, sizeof(pmaps));
+        if (!make_prep_maps(a, &pmaps)) return KDA_ERR_UNSUPPORTED;
         if (launch_chunk_table(p, s) != cudaSuccess) return KDA_ERR_CUDA;
         if (launch_prep(p, pmaps, num_sms, s) != cudaSuccess) return KDA_ERR_CUDA;
     }
     if (state_pass) {
-        // One CTA per chain (all 128 value columns) when the 32-column slab CTAs
-        // would need more than two waves of SMs: a whole-chain CTA takes about
-        // twice as long per chunk step (measured), so below that the slab kernel
-        // is as fast or faster.  The two kernels compute the same chunk step.
-        // KDA_STATE_KERNEL=head|slab overrides the choice (tests, measurements);
-        // the fused output norm needs whole rows and always takes the head kernel.
-        const char* force = getenv("KDA_STATE_KERNEL");
-        const bool head = p.gate ? true
-                          : force && !strcmp(force, "head") ? true
-                          : force && !strcmp(force, "slab") ? false
-                          : (long long)p.N * p.H * (kHeadDim / kSlab) > 2LL * num_sms;
+        const bool head = whole_chain_kernel(p, num_sms);
         if ((head ? launch_state_head(p, s) : launch_state(p, s)) != cudaSuccess) return KDA_ERR_CUDA;
     }
     return KDA_OK;
@@ -195,6 +325,24 @@ kda_status kda_prefill_workspace_layout(const kda_prefill_args* args, kda_worksp
 
 kda_status kda_prefill(const kda_prefill_args* args, void* stream) {
     return run_prefill(args, stream, 3);
+}
+
+kda_status kda_prefill_schedule(const kda_prefill_args* args, int num_sms, kda_schedule* out) {
+    if (!args || !out || num_sms < 1) return KDA_ERR_INVALID_ARG;
+    PrefillParams p;
+    memset(&p, 0, sizeof(p));
+    p.cu = args->cu_seqlens;
+    p.T = (int)args->seqlen;
+    p.N = (int)args->num_seqs;
+    p.H = (int)args->num_heads;
+    p.B = (int)args->batch;
+    p.gate = static_cast<const __nv_bfloat16*>(args->out_gate);
+    const Segments sg = plan_segments(p, num_sms);
+    out->segmented = sg.on ? 1 : 0;
+    out->whole_chain = sg.on ? (sg.head ? 1 : 0) : (whole_chain_kernel(p, num_sms) ? 1 : 0);
+    out->segment_chunks = sg.on ? sg.chunks : 0;
+    out->prep_ctas = sg.on ? sg.prep_ctas : num_sms;
+    return KDA_OK;
 }
 
 kda_status kda_prefill_prep(const kda_prefill_args* args, void* stream) {

@@ -60,7 +60,13 @@ KDA_POOL_F32, KDA_POOL_BF16 = 0, 1
 class WorkspaceLayout(ctypes.Structure):
     _fields_ = [("records", ctypes.c_size_t), ("record_bytes", ctypes.c_size_t),
                 ("chunk_offset", ctypes.c_size_t), ("status", ctypes.c_size_t),
-                ("total", ctypes.c_size_t), ("max_chunks", _i64)]
+                ("total", ctypes.c_size_t), ("max_chunks", _i64),
+                ("state_carry", ctypes.c_size_t)]
+
+
+class Schedule(ctypes.Structure):
+    _fields_ = [("segmented", ctypes.c_int32), ("whole_chain", ctypes.c_int32),
+                ("segment_chunks", ctypes.c_int32), ("prep_ctas", ctypes.c_int32)]
 
 
 _lib = None
@@ -79,6 +85,9 @@ def lib():
         L.kda_prefill_workspace_layout.restype = ctypes.c_int
         L.kda_prefill_workspace_layout.argtypes = [ctypes.POINTER(PrefillArgs),
                                                    ctypes.POINTER(WorkspaceLayout)]
+        L.kda_prefill_schedule.restype = ctypes.c_int
+        L.kda_prefill_schedule.argtypes = [ctypes.POINTER(PrefillArgs), ctypes.c_int,
+                                           ctypes.POINTER(Schedule)]
         for name in ("kda_prefill", "kda_prefill_prep", "kda_prefill_state"):
             f = getattr(L, name)
             f.restype = ctypes.c_int
@@ -213,6 +222,27 @@ def workspace_layout(q, *, cu_seqlens=None):
     L = WorkspaceLayout()
     _check(lib().kda_prefill_workspace_layout(ctypes.byref(a), ctypes.byref(L)))
     return L
+
+
+def prefill_schedule(q, *, cu_seqlens=None, norm=False, num_sms=None):
+    """The schedule kda_prefill runs for q's shape (kda_prefill_schedule):
+    dict(segmented, whole_chain, segment_chunks, prep_ctas).  Host only; q may
+    live anywhere (only its shape is read).  num_sms defaults to the current
+    CUDA device's SM count."""
+    a = PrefillArgs()
+    if cu_seqlens is not None:
+        a.batch, a.seqlen, a.num_seqs, a.num_heads = 1, q.shape[0], cu_seqlens.shape[0] - 1, q.shape[1]
+        a.cu_seqlens = ctypes.c_void_p(1)
+    else:
+        a.batch, a.seqlen, a.num_seqs, a.num_heads = q.shape[0], q.shape[1], q.shape[0], q.shape[2]
+    if norm:
+        a.out_gate = ctypes.c_void_p(1)
+    if num_sms is None:
+        num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    sch = Schedule()
+    _check(lib().kda_prefill_schedule(ctypes.byref(a), int(num_sms), ctypes.byref(sch)))
+    return dict(segmented=bool(sch.segmented), whole_chain=bool(sch.whole_chain),
+                segment_chunks=sch.segment_chunks, prep_ctas=sch.prep_ctas)
 
 
 def kda_prefill(q, k, v, g, beta, *, initial_state=None, cu_seqlens=None, chunk=CHUNK,

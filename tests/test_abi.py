@@ -33,7 +33,7 @@ def test_exports_every_declared_symbol(K):
             "kda_status_string"} <= names
     for n in sorted(names):
         assert hasattr(lib, n), n
-    assert lib.kda_abi_version() == 2
+    assert lib.kda_abi_version() == 3
 
 
 def _args(K, **kw):
@@ -80,8 +80,10 @@ def test_workspace_plan(K):
     assert lib.kda_prefill_workspace_layout(ctypes.byref(a), ctypes.byref(L)) == 0
     assert L.max_chunks == 4                        # padded: ceil(256 / 64)
     assert L.total == lib.kda_prefill_workspace_size(ctypes.byref(a))
-    offs = [L.records, L.chunk_offset, L.status]
+    offs = [L.records, L.chunk_offset, L.status, L.state_carry]
     assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
+    # padded: one fp32 128 x 128 state per chain (batch 1 x 2 heads) carried between segments
+    assert L.total == L.state_carry + 2 * 128 * 128 * 4
     assert L.record_bytes == 82432 and L.chunk_offset >= L.records + 8 * L.record_bytes
     # varlen upper bound on chunks: floor(T / 64) + N
     a2 = _args(K, cu_seqlens=ctypes.c_void_p(1 << 12), num_seqs=3, seqlen=130)
@@ -145,3 +147,43 @@ def test_verify_refuses_rows_it_cannot_move_in_16_byte_pieces(K):
     assert run(args(g=ctypes.c_void_p((1 << 20) + 4))) == K.KDA_ERR_UNSUPPORTED
     assert run(args(k_stride=K._i64x3(4 * 2 * 128, 2 * 128 + 4, 128))) == K.KDA_ERR_UNSUPPORTED
     assert run(args(g_stride=K._i64x3(4 * 2 * 128, 2 * 128 + 2, 128))) == K.KDA_ERR_UNSUPPORTED
+
+
+def _sched(K, num_sms=152, **kw):
+    a = _args(K, **kw)
+    s = K.Schedule()
+    assert K.lib().kda_prefill_schedule(ctypes.byref(a), num_sms, ctypes.byref(s)) == 0
+    return (s.segmented, s.whole_chain, s.segment_chunks, s.prep_ctas)
+
+
+def test_prefill_schedule(K, monkeypatch):
+    """Host-side schedule choice (no GPU call): segments only for few long
+    padded chains, with the state kernel that leaves prep the most SMs."""
+    monkeypatch.delenv("KDA_SEGMENT_CHUNKS", raising=False)
+    monkeypatch.delenv("KDA_STATE_KERNEL", raising=False)
+    # 32 chains of 2048 chunks: whole-chain state CTAs on 32 SMs, prep on 120,
+    # 16 prep rounds (60 chunks x 32 heads / 120 CTAs) per segment
+    assert _sched(K, batch=1, num_seqs=1, seqlen=131072, num_heads=32) == (1, 1, 60, 120)
+    # 8 chains: slab state CTAs (4 per chain) on 32 SMs, prep on 120
+    assert _sched(K, batch=1, num_seqs=1, seqlen=131072, num_heads=8) == (1, 0, 240, 120)
+    # short sequences, many chains, varlen: one pass, as before
+    assert _sched(K, batch=1, num_seqs=1, seqlen=256, num_heads=2) == (0, 0, 0, 152)
+    assert _sched(K, batch=4, num_seqs=4, seqlen=4096, num_heads=16) == (0, 0, 0, 152)
+    assert _sched(K, cu_seqlens=ctypes.c_void_p(1 << 12), num_seqs=8, seqlen=32768,
+                  num_heads=32) == (0, 1, 0, 152)
+    # two chains: the slab pass (2048 steps) dominates and prep is short, so
+    # moving prep beside it gains little
+    assert _sched(K, batch=1, num_seqs=1, seqlen=131072, num_heads=2)[0] == 0
+    # the fused norm needs whole rows: whole-chain kernel in either schedule
+    assert _sched(K, batch=1, num_seqs=1, seqlen=131072, num_heads=32,
+                  out_gate=ctypes.c_void_p(1))[1] == 1
+    # overrides
+    monkeypatch.setenv("KDA_SEGMENT_CHUNKS", "0")
+    assert _sched(K, batch=1, num_seqs=1, seqlen=131072, num_heads=32)[0] == 0
+    monkeypatch.setenv("KDA_SEGMENT_CHUNKS", "3")
+    assert _sched(K, batch=1, num_seqs=1, seqlen=256, num_heads=2) == (1, 0, 3, 144)
+    monkeypatch.setenv("KDA_STATE_KERNEL", "head")
+    assert _sched(K, batch=1, num_seqs=1, seqlen=256, num_heads=2) == (1, 1, 3, 150)
+    a = _args(K)
+    assert K.lib().kda_prefill_schedule(ctypes.byref(a), 0, ctypes.byref(K.Schedule())) == \
+        K.KDA_ERR_INVALID_ARG

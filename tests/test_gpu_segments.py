@@ -1,0 +1,144 @@
+"""GPU parity of the segmented schedule of padded calls: the tokens are cut into
+segments, the state pass of one segment runs on a second stream beside the
+prep of the next, and every chain's state passes between segments in fp32
+through the workspace.  Forced with KDA_SEGMENT_CHUNKS on small shapes: bit
+for bit equal to the one-pass call with the same state kernel (the chunk steps
+are the same, the state crosses a segment boundary exactly), and within the
+tolerances of the fp64 oracle.  The long workload at full size takes this
+schedule by default (test_gpu_prefill.test_full_size_configs)."""
+import os
+
+import pytest
+import torch
+
+from kda_chunked_prefill_02_gb300 import inputs
+from kda_test_util import assert_parity, oracle_prefill, rel_fro, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+class _env:
+    def __init__(self, **kv):
+        self.kv = kv
+
+    def __enter__(self):
+        self.old = {k: os.environ.get(k) for k in self.kv}
+        for k, v in self.kv.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = str(v)
+
+    def __exit__(self, *exc):
+        for k, v in self.old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+
+
+def _run(d, **kw):
+    import kda_chunked_prefill_02_gb300 as K
+    out, fin = K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, initial_state=d.initial_state, **kw)
+    torch.cuda.synchronize()
+    return out.cpu(), fin.cpu()
+
+
+@pytest.mark.parametrize("kernel", ["slab", "head"])
+@pytest.mark.parametrize("case,seg", [(dict(B=1, T=64 * 9 + 5, H=2), 2),
+                                      (dict(B=2, T=64 * 5, H=3, init_std=None), 1),
+                                      (dict(B=3, T=64 * 4 + 63, H=1), 3),
+                                      (dict(B=1, T=200, H=2), 100)])
+def test_segments_equal_one_pass(kernel, case, seg):
+    import kda_chunked_prefill_02_gb300 as K
+    inp = inputs.prefill_inputs(800 + seg + case["T"], **case)
+    d = inp.to("cuda")
+    with _env(KDA_STATE_KERNEL=kernel, KDA_SEGMENT_CHUNKS=seg):
+        sch = K.prefill_schedule(d.q)
+        assert sch["segmented"] and sch["segment_chunks"] == seg
+        assert sch["whole_chain"] == (kernel == "head")
+        out_s, fin_s = _run(d)
+    with _env(KDA_STATE_KERNEL=kernel, KDA_SEGMENT_CHUNKS=0):
+        assert not K.prefill_schedule(d.q)["segmented"]
+        out_1, fin_1 = _run(d)
+    assert torch.equal(out_s, out_1) and torch.equal(fin_s, fin_1)
+    ro, rf = oracle_prefill(inp)
+    assert_parity(out_s, fin_s, ro, rf, "segmented, %s kernel" % kernel)
+
+
+def test_segments_in_place_state():
+    """initial_state and final_state the same buffer: the first segment reads
+    it, only the last one writes it."""
+    import kda_chunked_prefill_02_gb300 as K
+    inp = inputs.prefill_inputs(851, B=2, T=64 * 6 + 10, H=2)
+    d = inp.to("cuda")
+    ro, rf = oracle_prefill(inp)
+    st = d.initial_state.clone()
+    with _env(KDA_SEGMENT_CHUNKS=2, KDA_STATE_KERNEL=None):
+        out, fin = K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, initial_state=st, final_state=st)
+        torch.cuda.synchronize()
+    assert fin.data_ptr() == st.data_ptr()
+    assert_parity(out, st, ro, rf, "segmented, in-place state")
+
+
+def test_segments_with_fused_norm():
+    """The fused gated RMSNorm in the segmented schedule (whole-chain kernel):
+    the gate pointer moves with the segment."""
+    import kda_chunked_prefill_02_gb300 as K
+    from oracle.norm import gated_rmsnorm
+    inp = inputs.prefill_inputs(852, B=2, T=64 * 5 + 7, H=2)
+    gen = torch.Generator().manual_seed(853)
+    gate = (torch.randn(inp.v.shape, generator=gen) * 2).to(torch.bfloat16)
+    w = (torch.rand(128, generator=gen) + 0.5).float()
+    d = inp.to("cuda")
+    kw = dict(out_gate=gate.cuda(), norm_weight=w.cuda(), norm_eps=1e-6)
+    with _env(KDA_SEGMENT_CHUNKS=2, KDA_STATE_KERNEL=None):
+        assert K.prefill_schedule(d.q, norm=True)["whole_chain"]
+        out_s, fin_s = _run(d, **kw)
+    with _env(KDA_SEGMENT_CHUNKS=0, KDA_STATE_KERNEL=None):
+        out_1, fin_1 = _run(d, **kw)
+    assert torch.equal(out_s, out_1) and torch.equal(fin_s, fin_1)
+    ro, rf = oracle_prefill(inp)
+    ref = gated_rmsnorm(ro, gate.float().numpy(), w.numpy(), 1e-6)
+    assert rel_fro(to_np(out_s), ref) <= 2e-2
+    assert rel_fro(to_np(fin_s), rf) <= 1e-2
+
+
+def test_segments_strided_views():
+    """Strided (non-contiguous) inputs: each segment's base pointers advance by
+    its first token times the token stride."""
+    import kda_chunked_prefill_02_gb300 as K
+    inp = inputs.prefill_inputs(854, B=2, T=64 * 4 + 1, H=2)
+    d = inp.to("cuda")
+    # views into a wider buffer: heads interleaved with a dummy head
+    def widen(t):
+        shape = list(t.shape)
+        shape[2] = 3
+        w = torch.zeros(shape, dtype=t.dtype, device=t.device)
+        w[:, :, 0:3:2] = t
+        return w[:, :, 0:3:2]
+    q, k, v, g = (widen(t) for t in (d.q, d.k, d.v, d.g))
+    b = torch.zeros(d.beta.shape[0], d.beta.shape[1], 3, device="cuda")
+    b[:, :, 0:3:2] = d.beta
+    beta = b[:, :, 0:3:2]
+    assert not q.is_contiguous()
+    with _env(KDA_SEGMENT_CHUNKS=1, KDA_STATE_KERNEL=None):
+        out_s, fin_s = K.kda_prefill(q, k, v, g, beta, initial_state=d.initial_state)
+        torch.cuda.synchronize()
+    with _env(KDA_SEGMENT_CHUNKS=0, KDA_STATE_KERNEL=None):
+        out_1, fin_1 = K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, initial_state=d.initial_state)
+        torch.cuda.synchronize()
+    assert torch.equal(out_s, out_1) and torch.equal(fin_s, fin_1)
+
+
+def test_default_schedule_of_the_long_workload():
+    """On a 152-SM GB300 the long workload (B 1, T 131072, H 32) takes the
+    segmented schedule with the whole-chain state kernel on 32 SMs; the
+    full-size parity test then runs it."""
+    import kda_chunked_prefill_02_gb300 as K
+    q = torch.empty(1, 131072, 32, 128, dtype=torch.bfloat16, device="meta")
+    with _env(KDA_SEGMENT_CHUNKS=None, KDA_STATE_KERNEL=None):
+        sch = K.prefill_schedule(q)
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("schedule constants are for 152 SMs")
+    assert sch == dict(segmented=True, whole_chain=True, segment_chunks=60, prep_ctas=120)
