@@ -262,7 +262,18 @@ def run_ours(args, rank, ws, local):
     tensor_frac = flops / (ms / 1e3) / 1e12 / tf_burst
     path_bytes = bytes_prep + bytes_state
     traffic = captured_traffic(dom, th)
+    sched = K.prefill_schedule(d.q, cu_seqlens=d.cu_seqlens)
+    if sched["segmented"]:
+        chunks = -(-inp.lengths[0] // 64)            # padded: every sequence has T tokens
+        nseg = -(-chunks // sched["segment_chunks"])
+        launches = 2 * nseg
+        sched["segments"] = nseg
+    else:
+        launches = 2 + (1 if inp.cu_seqlens is not None else 0)
+    sched["state_kernel"] = "whole-chain" if sched.pop("whole_chain") else "slab"
+    sched["kernels_per_call"] = launches
     return dict(traffic=traffic, ms=ms, value=value, clk=clk, ms_prep=ms_prep, ms_state=ms_state, dom=dom,
+                sched=sched,
                 achieved=achieved, hbm=hbm, peak_src=peak_src, tensor_frac=tensor_frac,
                 tf_burst=tf_burst, path_gbs=path_bytes / (ms / 1e3) / 1e9, inp=inp, d=d,
                 out=out, fin=fin, wsb=wsb, stream=stream, flops=flops, dbytes=dbytes)
@@ -354,10 +365,12 @@ def main():
                          "traffic": r["traffic"], "peak_source": r["peak_src"],
                          "algorithmic_bytes": r["dbytes"],
                          "traffic_note": "ncu DRAM bytes of the capture in profiles/, scaled by token-heads"},
-            "kernels_ms": {"prep": r["ms_prep"], "state": r["ms_state"]},
+            "kernels_ms": {"prep": r["ms_prep"], "state": r["ms_state"],
+                           "note": "each stage alone, one pass over all tokens (prep on every SM, then the state pass)"},
             "path_gbs": r["path_gbs"],
             "e2e": e2e, "cpu_baseline": cpu,
-            "gpu_launches": 2 * args.steps + (args.steps if inp.cu_seqlens is not None else 0),
+            "gpu_launches": r["sched"]["kernels_per_call"] * args.steps,
+            "schedule": r["sched"],
             "clocks": r["clk"],
         }
         print(json.dumps(line), flush=True)

@@ -161,11 +161,12 @@ bool whole_chain_kernel(const PrefillParams& p, int num_sms) {
 // two kernels cannot share an SM (each needs most of its shared memory).  With
 // few chains the state pass leaves most SMs idle for its whole length, so the
 // tokens are cut into segments: prep of segment s+1 runs on the SMs the state
-// pass of segment s leaves free.  The choice compares the estimated time of
-// both schedules from per-unit costs measured on GB300 (SM clock 2070 MHz):
-// one (chunk, head) record takes a prep CTA 8.7 us; a chunk step takes 1.14 us
-// in the slab kernel (four CTAs per chain) and 2.14 us in the whole-chain
-// kernel; each extra pair of launches costs about 5 us.
+// pass of segment s leaves free.  The choice simulates both streams from
+// per-unit costs measured on GB300 (SM clock 2070 MHz, long workload): one
+// (chunk, head) record takes a prep CTA 8.7 us, 5 % more beside a state pass; a
+// chunk step takes 1.14 us in the slab kernel (four CTAs per chain) and 2.14 us
+// in the whole-chain kernel, about 12 % more beside prep; every segment adds
+// about 14 us to each stream (launch, start-up, the slowest CTA's tail).
 struct Segments {
     bool on = false;
     bool head = false;       // whole-chain state kernel (else slab)
@@ -173,8 +174,23 @@ struct Segments {
     int prep_ctas = 0;       // prep grid while a state pass runs beside it
 };
 
+constexpr double kRecUs = 8.7, kSlabStepUs = 1.14, kHeadStepUs = 2.14;
+constexpr double kPrepBeside = 1.05, kStateBeside = 1.12, kSegmentUs = 14.0;
+
+// Estimated time of the segmented schedule: prep of segment i ends at P_i =
+// P_{i-1} + a_i; its state pass starts when both P_i and the previous state pass
+// are done.
+double segmented_us(long long cps, long long chains, long long seg, long long ctas, double step) {
+    double P = 0.0, S = 0.0;
+    for (long long t0 = 0; t0 < cps; t0 += seg) {
+        const long long c = cps - t0 < seg ? cps - t0 : seg;
+        P += (double)((c * chains + ctas - 1) / ctas) * kRecUs * kPrepBeside + kSegmentUs;
+        S = (P > S ? P : S) + (double)c * step * kStateBeside + kSegmentUs;
+    }
+    return S;
+}
+
 Segments plan_segments(const PrefillParams& p, int num_sms) {
-    constexpr double kRecUs = 8.7, kSlabStepUs = 1.14, kHeadStepUs = 2.14, kLaunchUs = 5.0;
     Segments sg;
     if (p.cu != nullptr || p.T <= 0 || p.N <= 0 || num_sms < 4) return sg;
     const char* env = getenv("KDA_SEGMENT_CHUNKS");
@@ -189,6 +205,7 @@ Segments plan_segments(const PrefillParams& p, int num_sms) {
     double best = waves(cps * chains, num_sms) * kRecUs +
                   (whole_chain_kernel(p, num_sms) ? waves(chains, num_sms) * cps * kHeadStepUs
                                                   : waves(4 * chains, num_sms) * cps * kSlabStepUs);
+    best *= 0.95;   // segment only for a clear gain
     if (forced > 0) best = 1e300;
     for (int head = 0; head < 2; ++head) {
         if (head ? !allow_head : !allow_slab) continue;
@@ -199,20 +216,27 @@ Segments plan_segments(const PrefillParams& p, int num_sms) {
             if (forced <= 0) continue;  // prep would be starved of SMs
             ctas = num_sms / 4;
         }
-        // about 16 prep rounds per segment: short enough that filling and
-        // draining the pipeline is cheap, long enough to amortise the launches
-        const long long seg = forced > 0 ? forced : (16 * ctas / chains > 4 ? 16 * ctas / chains : 4);
-        const long long nseg = (cps + seg - 1) / seg;
-        if (nseg > 65536) continue;
-        const double a = waves(seg * chains, ctas) * kRecUs;
-        const double b = (double)seg * (head ? kHeadStepUs : kSlabStepUs) * waves(state_ctas, num_sms);
-        const double t = a + b + (double)(nseg - 1) * (a > b ? a : b) + (double)nseg * kLaunchUs;
-        if (t < 0.92 * best) {
-            best = t;
+        const char* pc_env = getenv("KDA_SEGMENT_PREP_CTAS");   // measurements
+        if (forced > 0 && pc_env && atoi(pc_env) > 0) ctas = atoi(pc_env) < num_sms ? atoi(pc_env) : num_sms;
+        const double step = head ? kHeadStepUs : kSlabStepUs;
+        if (forced > 0) {
             sg.on = true;
             sg.head = head != 0;
-            sg.chunks = (int)seg;
+            sg.chunks = (int)(forced < cps ? forced : cps);
             sg.prep_ctas = (int)ctas;
+            break;
+        }
+        // segment lengths of 8, 16, ... chunks (at most 512 candidates)
+        const long long stride = 8 * ((cps / 8 + 511) / 512 > 1 ? (cps / 8 + 511) / 512 : 1);
+        for (long long seg = stride; seg < cps; seg += stride) {
+            const double t = segmented_us(cps, chains, seg, ctas, step);
+            if (t < best) {
+                best = t;
+                sg.on = true;
+                sg.head = head != 0;
+                sg.chunks = (int)seg;
+                sg.prep_ctas = (int)ctas;
+            }
         }
     }
     return sg;
@@ -233,6 +257,8 @@ kda_status run_segments(const kda_prefill_args* a, const PrefillParams& p, const
     ok = ok && ck(cudaEventRecord(ev_prep, s)) && ck(cudaStreamWaitEvent(ss, ev_prep, 0));
     float* carry = reinterpret_cast<float*>(static_cast<uint8_t*>(a->workspace) + L.state_carry);
     const int64_t seg_tokens = (int64_t)sg.chunks * kChunk;
+    const char* pdl_env = getenv("KDA_SEGMENT_PDL");
+    const bool pdl = !(pdl_env && !strcmp(pdl_env, "0"));
     size_t rec_base = 0;
     for (int64_t t0 = 0; ok && t0 < p.T; t0 += seg_tokens) {
         const int ts = (int)(p.T - t0 < seg_tokens ? p.T - t0 : seg_tokens);
@@ -256,7 +282,7 @@ kda_status run_segments(const kda_prefill_args* a, const PrefillParams& p, const
         sa.q = q.q; sa.k = q.k; sa.v = q.v; sa.g = q.g;
         sa.seqlen = ts;
         if (!make_prep_maps(&sa, &maps)) return KDA_ERR_UNSUPPORTED;
-        ok = launch_prep(q, maps, sg.prep_ctas, s) == cudaSuccess &&
+        ok = launch_prep(q, maps, sg.prep_ctas, s, !first && pdl) == cudaSuccess &&
              ck(cudaEventRecord(ev_prep, s)) && ck(cudaStreamWaitEvent(ss, ev_prep, 0)) &&
              (sg.head ? launch_state_head(q, ss) : launch_state(q, ss)) == cudaSuccess;
     }

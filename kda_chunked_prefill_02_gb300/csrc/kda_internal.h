@@ -100,7 +100,10 @@ struct PrepMaps {
 };
 
 cudaError_t launch_chunk_table(const PrefillParams& p, cudaStream_t s);
-cudaError_t launch_prep(const PrefillParams& p, const PrepMaps& maps, int num_sms, cudaStream_t s);
+// overlap_previous: launched programmatically after another prep grid in the
+// same stream (the two may overlap; they must touch disjoint records).
+cudaError_t launch_prep(const PrefillParams& p, const PrepMaps& maps, int num_sms, cudaStream_t s,
+                        bool overlap_previous = false);
 cudaError_t launch_state(const PrefillParams& p, cudaStream_t s);
 cudaError_t launch_state_head(const PrefillParams& p, cudaStream_t s);
 

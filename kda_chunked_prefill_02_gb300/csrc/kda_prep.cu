@@ -33,6 +33,8 @@
 // records.  The q, k, v and g tiles of a record arrive by TMA; the next
 // record's tiles are requested as soon as the current record's gate phase has
 // consumed its inputs, so the loads overlap the tensor-core and solve phases.
+#include <string.h>
+
 #include "kda_internal.h"
 #include "sm103.cuh"
 
@@ -207,6 +209,9 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         const int len = ci.len;
         const int rec_next = rec + gridDim.x;
         const ChunkInfo cn = rec_next < nrec ? chunk_info(p, rec_next / p.H) : ChunkInfo{0, 0, 0, 0, 0};
+        // This CTA's last record: a grid launched programmatically after this one
+        // may start once every CTA has reached this point.
+        if (rec_next >= nrec) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         // One thread waits on each mbarrier; the others wait at the CTA barrier.
         ok = __syncthreads_and(tid == 0 ? mbar_wait(&bar_in, it & 1, nullptr) : true);
         if (!ok) break;
@@ -668,15 +673,33 @@ cudaError_t launch_chunk_table(const PrefillParams& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_prep(const PrefillParams& p, const PrepMaps& maps, int num_sms, cudaStream_t s) {
+cudaError_t launch_prep(const PrefillParams& p, const PrepMaps& maps, int num_sms, cudaStream_t s,
+                        bool overlap_previous) {
     const long long recs = (long long)p.max_chunks * p.H;
     if (recs == 0) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kPrepSmem);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)(recs < num_sms ? recs : num_sms);
-    prep_kernel<<<grid, kPrepThreads, kPrepSmem, s>>>(p, maps);
-    return cudaGetLastError();
+    if (!overlap_previous) {
+        prep_kernel<<<grid, kPrepThreads, kPrepSmem, s>>>(p, maps);
+        return cudaGetLastError();
+    }
+    // Programmatic launch: this grid's CTAs may start while the previous prep
+    // grid in the stream finishes its last records (it reads nothing that grid
+    // writes), so that its tail and this grid's start-up overlap.
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kPrepThreads);
+    cfg.dynamicSmemBytes = kPrepSmem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prep_kernel, p, maps);
 }
 
 }  // namespace kda

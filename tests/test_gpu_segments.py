@@ -38,8 +38,12 @@ class _env:
 
 
 def _run(d, **kw):
+    """One call on a workspace filled with 0xff bytes (NaN as fp32 / bf16), so
+    that a record or carried state read before it is written shows."""
     import kda_chunked_prefill_02_gb300 as K
-    out, fin = K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, initial_state=d.initial_state, **kw)
+    ws = torch.full((K.workspace_size(d.q, d.v),), 0xFF, dtype=torch.uint8, device="cuda")
+    out, fin = K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, initial_state=d.initial_state,
+                             workspace=ws, **kw)
     torch.cuda.synchronize()
     return out.cpu(), fin.cpu()
 
@@ -141,4 +145,16 @@ def test_default_schedule_of_the_long_workload():
         sch = K.prefill_schedule(q)
     if torch.cuda.get_device_properties(0).multi_processor_count != 152:
         pytest.skip("schedule constants are for 152 SMs")
-    assert sch == dict(segmented=True, whole_chain=True, segment_chunks=60, prep_ctas=120)
+    assert sch == dict(segmented=True, whole_chain=True, segment_chunks=120, prep_ctas=120)
+
+
+def test_segments_without_programmatic_launch():
+    """KDA_SEGMENT_PDL=0: the prep grids of consecutive segments run strictly
+    one after the other; same bits as with the programmatic launch."""
+    inp = inputs.prefill_inputs(855, B=1, T=64 * 11 + 3, H=3)
+    d = inp.to("cuda")
+    with _env(KDA_SEGMENT_CHUNKS=2, KDA_STATE_KERNEL=None, KDA_SEGMENT_PDL=None):
+        a = _run(d)
+    with _env(KDA_SEGMENT_CHUNKS=2, KDA_STATE_KERNEL=None, KDA_SEGMENT_PDL=0):
+        b = _run(d)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
