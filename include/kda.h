@@ -154,9 +154,20 @@ size_t kda_prefill_workspace_size(const kda_prefill_args* args);
  * the call's work ends) overlaps the prep of segment s+1, the state of every
  * chain passing between segments in fp32 through the workspace's
  * state_carry region, so the results are those of one state pass over the
- * whole sequence.  KDA_SEGMENT_CHUNKS=n in the environment forces segments of
- * n chunks (0: never segment).
+ * whole sequence.
  * Returns KDA_OK once the kernels are enqueued.
+ *
+ * Environment overrides, read on every call (tests and measurements; results
+ * are the same within the stated tolerances whatever they select):
+ *   KDA_STATE_KERNEL=slab|head   state kernel (the fused norm always takes head)
+ *   KDA_SEGMENT_CHUNKS=n         segments of n chunks (0: never segment)
+ *   KDA_SEGMENT_PREP_CTAS=n      prep grid of a forced segmented call
+ *   KDA_SEGMENT_PDL=0            no programmatic launch between prep grids
+ *   KDA_STALL_INJECT=seed        kernels with the stall hook: a quarter of the
+ *                                warps at each injection site spin for a
+ *                                pseudo-random 0..4095 cycles; every result
+ *                                must be bit-identical to the run without it
+ *                                (also read by kda_verify)
  */
 kda_status kda_prefill(const kda_prefill_args* args, void* stream);
 

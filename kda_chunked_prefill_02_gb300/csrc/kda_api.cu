@@ -88,6 +88,13 @@ kda_status check_prefill(const kda_prefill_args* a) {
     return KDA_OK;
 }
 
+// KDA_STALL_INJECT=<seed>: the kernels' stall_point hook (timing perturbation
+// for ordering tests; results must not change).  Unset or 0: off.
+uint32_t stall_seed_from_env() {
+    const char* e = getenv("KDA_STALL_INJECT");
+    return e ? (uint32_t)strtoul(e, nullptr, 10) : 0u;
+}
+
 void fill_params(const kda_prefill_args* a, const kda_workspace_layout& L, PrefillParams* p) {
     memset(p, 0, sizeof(*p));
     uint8_t* ws = static_cast<uint8_t*>(a->workspace);
@@ -118,6 +125,7 @@ void fill_params(const kda_prefill_args* a, const kda_workspace_layout& L, Prefi
     for (int i = 0; i < 3; ++i) p->gts[i] = a->gate_stride[i];
     p->norm_w = a->norm_weight;
     p->norm_eps = a->norm_eps;
+    p->stall_seed = stall_seed_from_env();
 }
 
 // 4-D input tensor map [channel 128, head, token, batch] with one chunk of
@@ -434,6 +442,7 @@ kda_status kda_verify(const kda_verify_args* a, void* stream) {
     p.scale = a->scale;
     p.pool_bf16 = a->pool_dtype == KDA_POOL_BF16 ? 1 : 0;
     p.replay_only = a->replay_only ? 1 : 0;
+    p.stall_seed = stall_seed_from_env();
     return launch_verify(p, num_sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KDA_OK
                                                                                : KDA_ERR_CUDA;
 }

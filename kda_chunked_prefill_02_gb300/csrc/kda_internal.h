@@ -55,6 +55,7 @@ struct PrefillParams {
     int64_t gts[3];              // gate strides (batch, token, head)
     const float* norm_w;         // [128]
     float norm_eps;
+    uint32_t stall_seed;         // test hook: timing perturbation (stall_point), 0 = off
 };
 
 // Chunk c (global index) -> sequence, token start and length.
@@ -124,6 +125,7 @@ struct VerifyParams {
     float scale;
     int pool_bf16;           // 1: the pool holds bf16 states
     int replay_only;         // 1: run the accepted drafts only, store the state, no outputs
+    uint32_t stall_seed;     // test hook: timing perturbation (stall_point), 0 = off
 };
 
 cudaError_t launch_verify(const VerifyParams& p, int num_sms, cudaStream_t s);

@@ -156,6 +156,7 @@ __device__ __forceinline__ void load_inputs(uint8_t* sm, const PrepMaps& m, cons
     tma_load_4d(sm + O_IG, &m.g, 0, h, ci.t0, ci.b, bar);
 }
 
+template <bool kStall>
 __global__ void __launch_bounds__(kPrepThreads, 1)
     prep_kernel(const PrefillParams p, const __grid_constant__ PrepMaps maps) {
     extern __shared__ uint8_t smem_raw[];
@@ -212,6 +213,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         // This CTA's last record: a grid launched programmatically after this one
         // may start once every CTA has reached this point.
         if (rec_next >= nrec) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        stall_point<kStall>(p.stall_seed, 1, it);
         // One thread waits on each mbarrier; the others wait at the CTA barrier.
         ok = __syncthreads_and(tid == 0 ? mbar_wait(&bar_in, it & 1, nullptr) : true);
         if (!ok) break;
@@ -251,6 +253,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             *reinterpret_cast<float2*>(tot + h8 * 128 + c0) = make_float2(e0, e1);
             *reinterpret_cast<float2*>(tot + 1024 + h8 * 128 + c0) = make_float2(f0, f1);
         }
+        stall_point<kStall>(p.stall_seed, 2, it);
         if (tid == 0) bulk_wait_read();  // the previous record's images have left the staging area
         __syncthreads();
 
@@ -318,6 +321,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                     st_u32(sm + O_KV + mn_sw128_off(i, 128 + c0, kKvSbo), vw[l]);
                 }
             }
+            stall_point<kStall>(p.stall_seed, 3, it);
             // Backward over the group: the suffix products z (exact gates, to the block
             // end) and zc (floored gates); the first half of a block continues through
             // the second half.
@@ -361,6 +365,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                 *reinterpret_cast<uint4*>(kt + sw128_off(c0 + 1, 8 * h8)) = make_uint4(kh1[0], kh1[1], kh1[2], kh1[3]);
             }
         }
+        stall_point<kStall>(p.stall_seed, 4, it);
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -389,6 +394,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         }
         if (cn.len > 0) pend_parity = (int)((it + 1) & 1);
 
+        stall_point<kStall>(p.stall_seed, 5, it);
         float* sA = reinterpret_cast<float*>(sm + O_A);
         float* sT = reinterpret_cast<float*>(sm + O_T);
         float* sX = reinterpret_cast<float*>(sm + O_X);
@@ -428,6 +434,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                 *reinterpret_cast<uint4*>(sm + O_AQK + sw128_off(i, 16 * J + 8)) = make_uint4(w[4], w[5], w[6], w[7]);
             }
         }
+        stall_point<kStall>(p.stall_seed, 6, it);
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -476,6 +483,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                     make_uint4(0u, 0u, 0u, 0u);
             }
         }
+        stall_point<kStall>(p.stall_seed, 7, it);
         __syncthreads();
         // Off-diagonal blocks with warp-level tf32 tensor-core products (fp32
         // accumulation; T' is rounded to bf16 for MMA C anyway).
@@ -488,6 +496,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             float d[4];
             warp_mma_16x8(sA + (pb + 16) * kPA + pb, kPA, sT + pb * kPA + pb + c0, kPA, ct, 2, d, lane);
             store_tile_tf32(x, kPX, d, lane);
+            stall_point<kStall>(p.stall_seed, 8, it);
             __syncwarp();
             warp_mma_16x8(sT + (pb + 16) * kPA + pb + 16, kPA, x, kPX, 0, 2, d, lane);
             d[0] = -d[0]; d[1] = -d[1]; d[2] = -d[2]; d[3] = -d[3];
@@ -504,12 +513,14 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             float d[4];
             warp_mma_16x8(sA + (32 + 16 * rt) * kPA, kPA, sT + c0, kPA, ct, 4, d, lane);
             store_tile_tf32(sX + 16 * rt * kPX + c0, kPX, d, lane);
+            stall_point<kStall>(p.stall_seed, 9, it);
             named_bar_sync(1, 256);
             warp_mma_16x8(sT + (32 + 16 * rt) * kPA + 32, kPA, sX + c0, kPX, 0, 2 * (rt + 1), d, lane);
             const int r0 = 32 + 16 * rt + g4;
             store_tprime_pair(sm, r0, c0 + 2 * t4, -d[0], -d[1], sBeta);
             store_tprime_pair(sm, r0 + 8, c0 + 2 * t4, -d[2], -d[3], sBeta);
         }
+        stall_point<kStall>(p.stall_seed, 10, it);
         fence_proxy_async_smem();
         __syncthreads();
         // ---- MMA B: D_b = Aqk T'  -> rows 64..127 of the TT operand
@@ -522,6 +533,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         ok = __syncthreads_and(tid == 0 ? mbar_wait(&bar_mma[1], it & 1, nullptr) : true);
         tc_fence_after();
         if (!ok) break;
+        stall_point<kStall>(p.stall_seed, 11, it);
         if (qd < 2) {
             const int i = 32 * qd + lane;
             {
@@ -550,6 +562,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         ok = __syncthreads_and(tid == 0 ? mbar_wait(&bar_mma[2], it & 1, nullptr) : true);
         tc_fence_after();
         if (!ok) break;
+        stall_point<kStall>(p.stall_seed, 12, it);
         {
             // ---- Epilogue C: [W ; Q'] rows (Q' = Q e^Gam - Aqk W) from the first 128
             // columns and U / O_loc from the last 128, written as the record's
@@ -589,6 +602,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                 }
             }
         }
+        stall_point<kStall>(p.stall_seed, 13, it);
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -677,12 +691,14 @@ cudaError_t launch_prep(const PrefillParams& p, const PrepMaps& maps, int num_sm
                         bool overlap_previous) {
     const long long recs = (long long)p.max_chunks * p.H;
     if (recs == 0) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    // the instantiation with the stall hook runs only when a test asks for it
+    auto kern = p.stall_seed ? prep_kernel<true> : prep_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kPrepSmem);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)(recs < num_sms ? recs : num_sms);
     if (!overlap_previous) {
-        prep_kernel<<<grid, kPrepThreads, kPrepSmem, s>>>(p, maps);
+        kern<<<grid, kPrepThreads, kPrepSmem, s>>>(p, maps);
         return cudaGetLastError();
     }
     // Programmatic launch: this grid's CTAs may start while the previous prep
@@ -699,7 +715,7 @@ cudaError_t launch_prep(const PrefillParams& p, const PrepMaps& maps, int num_sm
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prep_kernel, p, maps);
+    return cudaLaunchKernelEx(&cfg, kern, p, maps);
 }
 
 }  // namespace kda

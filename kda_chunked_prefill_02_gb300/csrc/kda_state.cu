@@ -56,6 +56,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     return __all_sync(0xffffffffu, ok);
 }
 
+template <bool kStall>
 __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -109,6 +110,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
             for (int c = 0; c < count; ++c) {
                 const int st = c % kStages;
                 if (c >= kStages && !mbar_wait(&empty[st], ((c / kStages) - 1) & 1, abort)) { fail(); break; }
+                stall_point<kStall>(p.stall_seed, 1, c);
                 uint8_t* sb = sm + st * kStage;
                 const uint8_t* rp = p.ws_rec + (size_t)((first + c) * p.H + h) * kRecBytes;
                 mbar_arrive_expect_tx(&full[st], kStageTx);
@@ -172,6 +174,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
             const uint8_t* sb = sm + st * kStage;
             const uint32_t sb_addr = smem_u32(sb);
             bool ok = warp_wait(&full[st], (c / kStages) & 1, abort);
+            stall_point<kStall>(p.stall_seed, 2, c);
             if (issuer && ok) {
                 tc_fence_after();
                 // K = 128 keys: A K-major, B (S) MN-major; descriptors built once,
@@ -215,6 +218,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
                             vn[8 * ch + 2 * x + 1] = f.y - d[8 * ch + 2 * x + 1];
                         }
                     }
+                    stall_point<kStall>(p.stall_seed, 3, c);
                     store_row(sm + O_VN, row, vn);
                     fence_proxy_async_smem();
                 }
@@ -235,6 +239,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
                 // O = O_loc + Q' S for token row `row - 64`
                 const int i = row - 64;
                 const int t0 = 64 * c;
+                stall_point<kStall>(p.stall_seed, 4, c);
                 if (t0 + i < seq_len) {
                     uint32_t o[kSlab / 2];
 #pragma unroll
@@ -263,6 +268,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
                 const float eg = reinterpret_cast<const float*>(sb + ST_EG)[row];
 #pragma unroll
                 for (int j = 0; j < kSlab; ++j) S[j] = fmaf(eg, S[j], d[j]);
+                stall_point<kStall>(p.stall_seed, 5, c);
                 write_state_image();
             } else {
                 fail();
@@ -293,11 +299,12 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
 
 cudaError_t launch_state(const PrefillParams& p, cudaStream_t s) {
     if (p.N == 0 || p.H == 0) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto kern = p.stall_seed ? state_kernel<true> : state_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kStateSmem);
     if (e != cudaSuccess) return e;
     dim3 grid(kHeadDim / kSlab, p.H, p.N);
-    state_kernel<<<grid, kStateThreads, kStateSmem, s>>>(p);
+    kern<<<grid, kStateThreads, kStateSmem, s>>>(p);
     return cudaGetLastError();
 }
 

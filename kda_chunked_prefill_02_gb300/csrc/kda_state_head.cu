@@ -76,6 +76,7 @@ __device__ __forceinline__ void store_quarter(uint8_t* base, int r, int cq, cons
     }
 }
 
+template <bool kStall>
 __global__ void __launch_bounds__(kHeadThreads, 1) state_head_kernel(const PrefillParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -167,6 +168,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1) state_head_kernel(const Prefi
             const uint8_t* sb = sm + st * kHStage;
             const uint32_t sb_addr = smem_u32(sb);
             bool ok = warp_wait_h(&full[st], (c / kHStages) & 1, abort);
+            stall_point<kStall>(p.stall_seed, 1, c);
             if (issuer && ok) {
                 tc_fence_after();
                 const uint64_t ad = sdesc_kmajor_sw128(sb_addr + SH_A1);
@@ -207,6 +209,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1) state_head_kernel(const Prefi
                             vn[8 * ch + 2 * x + 1] = f.y - d[8 * ch + 2 * x + 1];
                         }
                     }
+                    stall_point<kStall>(p.stall_seed, 2, c);
                     store_quarter(sm + OH_VN, row, cq, vn);
                     fence_proxy_async_smem();
                 }
@@ -274,6 +277,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1) state_head_kernel(const Prefi
                         }
                     }
                 }
+                stall_point<kStall>(p.stall_seed, 3, c);
                 if (ok && valid_row) {
                     uint4* dst = reinterpret_cast<uint4*>(p.out + b * p.os[0] + t * p.os[1] + h * p.os[2] + kSlab * cq);
 #pragma unroll
@@ -291,6 +295,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1) state_head_kernel(const Prefi
                 const float eg = reinterpret_cast<const float*>(sb + SH_EG)[row];
 #pragma unroll
                 for (int j = 0; j < kSlab; ++j) S[j] = fmaf(eg, S[j], d[j]);
+                stall_point<kStall>(p.stall_seed, 4, c);
                 if (c + 1 < count) {
                     store_quarter(sm + OH_S, row, cq, S);
                     fence_proxy_async_smem();
@@ -302,6 +307,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1) state_head_kernel(const Prefi
             if (named_bar_or(kBarHChunk, 512, *abort != 0)) break;
             done = c + 1;
             // stage st is free: P2 of chunk c completed and every read of it is done
+            stall_point<kStall>(p.stall_seed, 5, c);
             if (issuer && issued < count) issue_load(issued++);
         }
         if (issuer) {
@@ -329,11 +335,12 @@ __global__ void __launch_bounds__(kHeadThreads, 1) state_head_kernel(const Prefi
 
 cudaError_t launch_state_head(const PrefillParams& p, cudaStream_t s) {
     if (p.N == 0 || p.H == 0) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(state_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto kern = p.stall_seed ? state_head_kernel<true> : state_head_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kHeadSmem);
     if (e != cudaSuccess) return e;
     dim3 grid(p.H, p.N);
-    state_head_kernel<<<grid, kHeadThreads, kHeadSmem, s>>>(p);
+    kern<<<grid, kHeadThreads, kHeadSmem, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -60,7 +60,7 @@ struct Item {
 
 // kBf16: the pool holds bf16 states (read widened to fp32, written back rounded
 // to nearest even); otherwise fp32.
-template <bool kBf16>
+template <bool kBf16, bool kStall>
 __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyParams p) {
     constexpr uint32_t kStateBytes = kHeadDim * kHeadDim * (kBf16 ? 2 : 4);
     extern __shared__ __align__(16) uint8_t smv[];
@@ -123,6 +123,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyP
     prefetch(cur, tokb(0));
     Item nxt = it + (int)gridDim.x < nitems ? item_of(it + gridDim.x) : Item{0, 0, 0, 0, false};
     for (int k = 0;; ++k) {
+        stall_point<kStall>(p.stall_seed, 1, k);
         cp_async_wait_all();
         __syncthreads();  // this item's state and drafts have landed; the previous item is done
         uint8_t* tb = tokb(k & 1);
@@ -149,7 +150,9 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyP
         } else if (tid == 0 && p.status) {
             atomicExch(p.status, 1);
         }
+        stall_point<kStall>(p.stall_seed, 2, k);
         __syncthreads();  // the state block is in registers: its buffer takes the next item
+        stall_point<kStall>(p.stall_seed, 3, k);
         prefetch(nxt, tokb((k + 1) & 1));
         const float bnext = load_beta(nxt);
         const int nit = it + gridDim.x;
@@ -225,6 +228,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyP
                     p.out[cur.r * p.os[0] + t * p.os[1] + cur.h * p.os[2] + col0 + rg] = __float2bfloat16_rn(oc);
                 }
                 if (t + 1 == cur.acc) {
+                    stall_point<kStall>(p.stall_seed, 4, k);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         if (kBf16)
@@ -246,19 +250,19 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyP
     cp_async_wait_all();  // the last (empty or unused) prefetch group
 }
 
-template <bool kBf16>
+template <bool kBf16, bool kStall>
 cudaError_t launch_verify_t(const VerifyParams& p, int num_sms, cudaStream_t s) {
     const size_t smem = (size_t)kHeadDim * kHeadDim * (kBf16 ? 2 : 4) + 2 * (size_t)p.D * kTokBytes;
-    cudaError_t e = cudaFuncSetAttribute(verify_kernel<kBf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(verify_kernel<kBf16, kStall>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, verify_kernel<kBf16>, kVerifyThreads, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, verify_kernel<kBf16, kStall>, kVerifyThreads, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
     const long long items = (long long)p.R * p.H;
     const long long cap = (long long)num_sms * per_sm;
-    verify_kernel<kBf16><<<(unsigned)(items < cap ? items : cap), kVerifyThreads, smem, s>>>(p);
+    verify_kernel<kBf16, kStall><<<(unsigned)(items < cap ? items : cap), kVerifyThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
 
@@ -266,7 +270,10 @@ cudaError_t launch_verify_t(const VerifyParams& p, int num_sms, cudaStream_t s) 
 
 cudaError_t launch_verify(const VerifyParams& p, int num_sms, cudaStream_t s) {
     if (p.R == 0 || p.H == 0) return cudaSuccess;
-    return p.pool_bf16 ? launch_verify_t<true>(p, num_sms, s) : launch_verify_t<false>(p, num_sms, s);
+    // the instantiations with the stall hook run only when a test asks for them
+    if (p.stall_seed)
+        return p.pool_bf16 ? launch_verify_t<true, true>(p, num_sms, s) : launch_verify_t<false, true>(p, num_sms, s);
+    return p.pool_bf16 ? launch_verify_t<true, false>(p, num_sms, s) : launch_verify_t<false, false>(p, num_sms, s);
 }
 
 }  // namespace kda

@@ -331,4 +331,30 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Timing perturbation for tests of the pipelines' ordering.  With seed != 0 a
+// quarter of the warps that reach injection site `site` in iteration `iter`
+// spin for a pseudo-random 0..4095 SM cycles (a hash of seed, block, warp, site
+// and iteration, the same for every lane) before going on.  Only the timing
+// changes, so every result must stay bit-identical; a missing barrier or a
+// hand-off read too early shows as a difference.  The wait is bounded by its
+// cycle count.
+// kOn selects the kernel instantiation: production launches take kOn = false,
+// where the hook compiles to nothing.
+template <bool kOn>
+__device__ __forceinline__ void stall_point(uint32_t seed, uint32_t site, uint32_t iter) {
+    if constexpr (kOn) {
+        if (seed == 0u) return;
+        uint32_t x = seed * 0x9E3779B1u;
+        x ^= (blockIdx.x + 0x632BE5ABu * blockIdx.y + 0x85157AF5u * blockIdx.z) * 0x85EBCA77u;
+        x ^= ((threadIdx.x >> 5) + 64u * site) * 0xC2B2AE3Du;
+        x ^= iter * 0x27D4EB2Fu;
+        x ^= x >> 15; x *= 0x2C1B3C6Du; x ^= x >> 12; x *= 0x297A2D39u; x ^= x >> 15;
+        if ((x & 3u) != 0u) return;
+        const long long n = (long long)((x >> 2) & 4095u);
+        const long long t0 = clock64();
+        while (clock64() - t0 < n) {
+        }
+    }
+}
+
 }  // namespace kda
