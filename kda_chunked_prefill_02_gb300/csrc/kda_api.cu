@@ -188,11 +188,14 @@ constexpr double kPrepBeside = 1.05, kStateBeside = 1.12, kSegmentUs = 14.0;
 // Estimated time of the segmented schedule: prep of segment i ends at P_i =
 // P_{i-1} + a_i; its state pass starts when both P_i and the previous state pass
 // are done.
-double segmented_us(long long cps, long long chains, long long seg, long long ctas, double step) {
+// The first segment's prep has every SM to itself.
+double segmented_us(long long cps, long long chains, long long seg, long long ctas, double step,
+                    int num_sms) {
     double P = 0.0, S = 0.0;
     for (long long t0 = 0; t0 < cps; t0 += seg) {
         const long long c = cps - t0 < seg ? cps - t0 : seg;
-        P += (double)((c * chains + ctas - 1) / ctas) * kRecUs * kPrepBeside + kSegmentUs;
+        const long long grid = t0 == 0 ? num_sms : ctas;
+        P += (double)((c * chains + grid - 1) / grid) * kRecUs * (t0 == 0 ? 1.0 : kPrepBeside) + kSegmentUs;
         S = (P > S ? P : S) + (double)c * step * kStateBeside + kSegmentUs;
     }
     return S;
@@ -237,7 +240,7 @@ Segments plan_segments(const PrefillParams& p, int num_sms) {
         // segment lengths of 8, 16, ... chunks (at most 512 candidates)
         const long long stride = 8 * ((cps / 8 + 511) / 512 > 1 ? (cps / 8 + 511) / 512 : 1);
         for (long long seg = stride; seg < cps; seg += stride) {
-            const double t = segmented_us(cps, chains, seg, ctas, step);
+            const double t = segmented_us(cps, chains, seg, ctas, step, num_sms);
             if (t < best) {
                 best = t;
                 sg.on = true;
@@ -254,7 +257,7 @@ Segments plan_segments(const PrefillParams& p, int num_sms) {
 // every segment on a second stream, each after its segment's prep and after the
 // previous segment's state pass; `s` waits for the last state pass.
 kda_status run_segments(const kda_prefill_args* a, const PrefillParams& p, const Segments& sg,
-                        const kda_workspace_layout& L, cudaStream_t s) {
+                        const kda_workspace_layout& L, int num_sms, cudaStream_t s) {
     cudaStream_t ss = nullptr;
     cudaEvent_t ev_prep = nullptr, ev_done = nullptr;
     auto ck = [](cudaError_t e) { return e == cudaSuccess; };
@@ -290,7 +293,8 @@ kda_status run_segments(const kda_prefill_args* a, const PrefillParams& p, const
         sa.q = q.q; sa.k = q.k; sa.v = q.v; sa.g = q.g;
         sa.seqlen = ts;
         if (!make_prep_maps(&sa, &maps)) return KDA_ERR_UNSUPPORTED;
-        ok = launch_prep(q, maps, sg.prep_ctas, s, !first && pdl) == cudaSuccess &&
+        // no state pass runs yet while the first segment is prepared: every SM
+        ok = launch_prep(q, maps, first ? num_sms : sg.prep_ctas, s, !first && pdl) == cudaSuccess &&
              ck(cudaEventRecord(ev_prep, s)) && ck(cudaStreamWaitEvent(ss, ev_prep, 0)) &&
              (sg.head ? launch_state_head(q, ss) : launch_state(q, ss)) == cudaSuccess;
     }
@@ -325,7 +329,7 @@ kda_status run_prefill(const kda_prefill_args* a, void* stream, int stages) {
         return KDA_ERR_CUDA;
     if (prep && state_pass) {
         const Segments sg = plan_segments(p, num_sms);
-        if (sg.on) return run_segments(a, p, sg, L, s);
+        if (sg.on) return run_segments(a, p, sg, L, num_sms, s);
     }
     if (prep) {
         PrepMaps pmaps;

@@ -206,7 +206,6 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     bool ok = true;
     int pend_parity = ci.len > 0 ? 0 : -1;  // parity of an input load still in flight
     for (uint32_t it = 0; ci.len > 0; ++it) {
-        const int chunk = rec / p.H, h = rec - chunk * p.H;
         const int len = ci.len;
         const int rec_next = rec + gridDim.x;
         const ChunkInfo cn = rec_next < nrec ? chunk_info(p, rec_next / p.H) : ChunkInfo{0, 0, 0, 0, 0};

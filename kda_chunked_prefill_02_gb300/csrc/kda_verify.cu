@@ -27,7 +27,6 @@ namespace {
 
 constexpr int kMaxDrafts = 16;
 constexpr int kVerifyThreads = 256;
-constexpr uint32_t kStateBytesMax = kHeadDim * kHeadDim * 4;   // 64 KB (fp32 pool; bf16: 32 KB)
 // Staged draft row t (bytes): q bf16 and k bf16 rows of 128 with 16 B of
 // padding after each 32 B (row group), v bf16 unpadded, e^g fp32 with 16 B
 // after each 64 B.
