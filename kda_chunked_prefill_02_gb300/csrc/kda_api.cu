@@ -140,6 +140,33 @@ bool make_input_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, ui
     return make_tensor_map(m, dt, 4, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
+// Tensor map of out for the whole-chain state kernel's tensor stores: [channel
+// 128, head, token, batch] with the caller's strides, box [32, 1, 64, 1] and the
+// 64-byte swizzle (the layout of the records' value slabs).  base and T are
+// those of the launch (a segment's own).  False if the driver refuses the
+// layout; the kernel then stores rows one by one.
+bool make_out_map(CUtensorMap* m, const kda_prefill_args* a, const void* base, int64_t T) {
+    const int64_t B = a->cu_seqlens ? 1 : a->batch, H = a->num_heads;
+    if (T <= 0 || B <= 0 || !base) return false;
+    const int64_t* st = a->out_stride;
+    const uint64_t tstride = (uint64_t)st[1] * 2;
+    const uint64_t bstride = st[0] != 0 ? (uint64_t)st[0] * 2 : tstride * (uint64_t)T;
+    const uint64_t dims[4] = {128, (uint64_t)H, (uint64_t)T, (uint64_t)B};
+    const uint64_t strides[3] = {(uint64_t)st[2] * 2, tstride, bstride};
+    const uint32_t box[4] = {32, 1, (uint32_t)kChunk, 1};
+    return make_tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
+// Launches the state pass of `p` with the chosen kernel.
+cudaError_t launch_state_pass(const kda_prefill_args* a, PrefillParams p, bool head, cudaStream_t s) {
+    if (!head) return launch_state(p, s);
+    CUtensorMap om;
+    memset(&om, 0, sizeof(om));
+    p.out_tma = make_out_map(&om, a, p.out, p.T) ? 1 : 0;
+    return launch_state_head(p, om, s);
+}
+
 bool make_prep_maps(const kda_prefill_args* a, PrepMaps* m) {
     const int64_t T = a->seqlen, B = a->cu_seqlens ? 1 : a->batch, H = a->num_heads;
     if (T == 0 || B == 0) return true;
@@ -296,7 +323,7 @@ kda_status run_segments(const kda_prefill_args* a, const PrefillParams& p, const
         // no state pass runs yet while the first segment is prepared: every SM
         ok = launch_prep(q, maps, first ? num_sms : sg.prep_ctas, s, !first && pdl) == cudaSuccess &&
              ck(cudaEventRecord(ev_prep, s)) && ck(cudaStreamWaitEvent(ss, ev_prep, 0)) &&
-             (sg.head ? launch_state_head(q, ss) : launch_state(q, ss)) == cudaSuccess;
+             launch_state_pass(a, q, sg.head, ss) == cudaSuccess;
     }
     if (ss && ev_done) {
         // join even after a failure, so that nothing queued later on `s`
@@ -339,8 +366,7 @@ kda_status run_prefill(const kda_prefill_args* a, void* stream, int stages) {
         if (launch_prep(p, pmaps, num_sms, s) != cudaSuccess) return KDA_ERR_CUDA;
     }
     if (state_pass) {
-        const bool head = whole_chain_kernel(p, num_sms);
-        if ((head ? launch_state_head(p, s) : launch_state(p, s)) != cudaSuccess) return KDA_ERR_CUDA;
+        if (launch_state_pass(a, p, whole_chain_kernel(p, num_sms), s) != cudaSuccess) return KDA_ERR_CUDA;
     }
     return KDA_OK;
 }

@@ -49,7 +49,7 @@ constexpr uint32_t OH_S = kHStages * kHStage;       // S bf16: 128 key rows (32 
 constexpr uint32_t OH_VN = OH_S + 32768;            // V_new bf16: 64 token rows (16 KB)
 constexpr uint32_t kHeadSmem = OH_VN + 16384 + 1024;
 constexpr uint32_t TMH_D1 = 0, TMH_D2 = 128, TMH_COLS = 256;
-constexpr uint32_t kBarHVn = 1, kBarHChunk = 2, kBarHNorm = 3;  // named barriers (0 is __syncthreads)
+constexpr uint32_t kBarHVn = 1, kBarHChunk = 2, kBarHNorm = 3, kBarHOut = 4;  // named barriers (0 is __syncthreads)
 
 // sigmoid(x) = 1/2 + tanh(x/2)/2, with the hardware tanh approximation
 // (relative error ~2^-11, below the bf16 rounding of the output).
@@ -77,7 +77,8 @@ __device__ __forceinline__ void store_quarter(uint8_t* base, int r, int cq, cons
 }
 
 template <bool kStall>
-__global__ void __launch_bounds__(kHeadThreads, 1) state_head_kernel(const PrefillParams p) {
+__global__ void __launch_bounds__(kHeadThreads, 1)
+    state_head_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap out_map) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -278,7 +279,30 @@ __global__ void __launch_bounds__(kHeadThreads, 1) state_head_kernel(const Prefi
                     }
                 }
                 stall_point<kStall>(p.stall_seed, 3, c);
-                if (ok && valid_row) {
+                // Rows of a chunk that lies inside its sequence (padded calls: every
+                // chunk, the tensor store clips the rows past T) leave by tensor store:
+                // each thread writes its bf16 row piece over the O_loc bytes it read
+                // (the same 64-byte-swizzled slab layout as the store box), and one
+                // thread stores the four slabs.  Rows of a varlen tail chunk, which
+                // the next sequence's rows follow, are stored one by one.
+                const bool by_tma = p.out_tma && (p.cu == nullptr || t0 + kChunk <= seq_len);
+                if (by_tma) {
+                    uint8_t* img = sm + st * kHStage + SH_OL + cq * kSlabImg;
+#pragma unroll
+                    for (int x = 0; x < kSlab / 8; ++x)
+                        *reinterpret_cast<uint4*>(img + slab_chunk_off(i, x)) =
+                            make_uint4(pack_bf16x2(o[8 * x], o[8 * x + 1]), pack_bf16x2(o[8 * x + 2], o[8 * x + 3]),
+                                       pack_bf16x2(o[8 * x + 4], o[8 * x + 5]), pack_bf16x2(o[8 * x + 6], o[8 * x + 7]));
+                    fence_proxy_async_smem();
+                    named_bar_sync(kBarHOut, 256);  // the eight output warps
+                    if (issuer && ok && !*abort) {
+                        const int tok = (int)(p.cu == nullptr ? t0 : (int64_t)tbase + t0);
+#pragma unroll
+                        for (int sl = 0; sl < kHeadDim / kSlab; ++sl)
+                            tma_store_4d(&out_map, kSlab * sl, h, tok, b, sb + SH_OL + sl * kSlabImg);
+                        bulk_commit();
+                    }
+                } else if (ok && valid_row) {
                     uint4* dst = reinterpret_cast<uint4*>(p.out + b * p.os[0] + t * p.os[1] + h * p.os[2] + kSlab * cq);
 #pragma unroll
                     for (int x = 0; x < kSlab / 8; ++x)
@@ -306,11 +330,16 @@ __global__ void __launch_bounds__(kHeadThreads, 1) state_head_kernel(const Prefi
             tc_fence_before();
             if (named_bar_or(kBarHChunk, 512, *abort != 0)) break;
             done = c + 1;
-            // stage st is free: P2 of chunk c completed and every read of it is done
+            // stage st is free: P2 of chunk c completed, every read of it is done
+            // and (issuer) the output tensor stores have read their slabs
             stall_point<kStall>(p.stall_seed, 5, c);
-            if (issuer && issued < count) issue_load(issued++);
+            if (issuer && issued < count) {
+                bulk_wait_read();
+                issue_load(issued++);
+            }
         }
         if (issuer) {
+            bulk_wait_all();  // the output tensor stores are complete
             // Never leave with a copy in flight (bounded; normally complete).
             for (int c = done; c < issued; ++c) mbar_wait(&full[c % kHStages], (c / kHStages) & 1, nullptr);
         }
@@ -333,14 +362,14 @@ __global__ void __launch_bounds__(kHeadThreads, 1) state_head_kernel(const Prefi
 
 }  // namespace
 
-cudaError_t launch_state_head(const PrefillParams& p, cudaStream_t s) {
+cudaError_t launch_state_head(const PrefillParams& p, const CUtensorMap& out_map, cudaStream_t s) {
     if (p.N == 0 || p.H == 0) return cudaSuccess;
     auto kern = p.stall_seed ? state_head_kernel<true> : state_head_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kHeadSmem);
     if (e != cudaSuccess) return e;
     dim3 grid(p.H, p.N);
-    kern<<<grid, kHeadThreads, kHeadSmem, s>>>(p);
+    kern<<<grid, kHeadThreads, kHeadSmem, s>>>(p, out_map);
     return cudaGetLastError();
 }
 

@@ -124,13 +124,23 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
-// 1-D bulk copy global -> shared, completing on an mbarrier (16-byte aligned
-// addresses, size a multiple of 16).
+// Tiled tensor store shared -> global (4-D box at coordinates c0..c3), in the
+// issuing thread's bulk group; elements outside the tensor are not written.
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                             const void* src) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(map),
+        "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(src))
+        : "memory");
+}
+
 // Asks for a global range (16-byte aligned, size a multiple of 16) to be brought
 // into L2 ahead of a later bulk copy.
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
+// 1-D bulk copy global -> shared, completing on an mbarrier (16-byte aligned
+// addresses, size a multiple of 16).
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
