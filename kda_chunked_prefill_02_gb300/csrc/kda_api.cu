@@ -198,10 +198,11 @@ bool whole_chain_kernel(const PrefillParams& p, int num_sms) {
 // tokens are cut into segments: prep of segment s+1 runs on the SMs the state
 // pass of segment s leaves free.  The choice simulates both streams from
 // per-unit costs measured on GB300 (SM clock 2070 MHz, long workload): one
-// (chunk, head) record takes a prep CTA 8.7 us, 5 % more beside a state pass; a
-// chunk step takes 1.14 us in the slab kernel (four CTAs per chain) and 2.14 us
-// in the whole-chain kernel, about 12 % more beside prep; every segment adds
-// about 14 us to each stream (launch, start-up, the slowest CTA's tail).
+// (chunk, head) record takes a prep CTA 8.7 us on a full GPU and 8.25 us on the
+// SMs beside a state pass; a chunk step takes 1.13 us in the slab kernel (four
+// CTAs per chain) and 2.15 us in the whole-chain kernel, 2 % more beside prep;
+// every segment adds about 12 us to each stream (launch, start-up, the slowest
+// CTA's tail).  Fitted to a sweep of segment lengths 30..160 within 2 %.
 struct Segments {
     bool on = false;
     bool head = false;       // whole-chain state kernel (else slab)
@@ -209,8 +210,8 @@ struct Segments {
     int prep_ctas = 0;       // prep grid while a state pass runs beside it
 };
 
-constexpr double kRecUs = 8.7, kSlabStepUs = 1.14, kHeadStepUs = 2.14;
-constexpr double kPrepBeside = 1.05, kStateBeside = 1.12, kSegmentUs = 14.0;
+constexpr double kRecUs = 8.7, kSlabStepUs = 1.13, kHeadStepUs = 2.15;
+constexpr double kPrepBeside = 0.95, kStateBeside = 1.02, kSegmentUs = 12.0;
 
 // Estimated time of the segmented schedule: prep of segment i ends at P_i =
 // P_{i-1} + a_i; its state pass starts when both P_i and the previous state pass
