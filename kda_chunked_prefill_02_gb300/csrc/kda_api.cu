@@ -140,7 +140,7 @@ bool make_input_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, ui
     return make_tensor_map(m, dt, 4, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-// Tensor map of out for the whole-chain state kernel's tensor stores: [channel
+// Tensor map of out for the state kernels' tensor stores: [channel
 // 128, head, token, batch] with the caller's strides, box [32, 1, 64, 1] and the
 // 64-byte swizzle (the layout of the records' value slabs).  base and T are
 // those of the launch (a segment's own).  False if the driver refuses the
@@ -160,11 +160,10 @@ bool make_out_map(CUtensorMap* m, const kda_prefill_args* a, const void* base, i
 
 // Launches the state pass of `p` with the chosen kernel.
 cudaError_t launch_state_pass(const kda_prefill_args* a, PrefillParams p, bool head, cudaStream_t s) {
-    if (!head) return launch_state(p, s);
     CUtensorMap om;
     memset(&om, 0, sizeof(om));
     p.out_tma = make_out_map(&om, a, p.out, p.T) ? 1 : 0;
-    return launch_state_head(p, om, s);
+    return head ? launch_state_head(p, om, s) : launch_state(p, om, s);
 }
 
 bool make_prep_maps(const kda_prefill_args* a, PrepMaps* m) {

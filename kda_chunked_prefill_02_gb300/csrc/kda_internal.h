@@ -56,7 +56,7 @@ struct PrefillParams {
     const float* norm_w;         // [128]
     float norm_eps;
     uint32_t stall_seed;         // test hook: timing perturbation (stall_point), 0 = off
-    int out_tma;                 // 1: the whole-chain state kernel got a tensor map of out
+    int out_tma;                 // 1: the state kernel got a tensor map of out
 };
 
 // Chunk c (global index) -> sequence, token start and length.
@@ -106,9 +106,9 @@ cudaError_t launch_chunk_table(const PrefillParams& p, cudaStream_t s);
 // same stream (the two may overlap; they must touch disjoint records).
 cudaError_t launch_prep(const PrefillParams& p, const PrepMaps& maps, int num_sms, cudaStream_t s,
                         bool overlap_previous = false);
-cudaError_t launch_state(const PrefillParams& p, cudaStream_t s);
 // out_map: tensor map of out, [channel 128, head, token, batch] with a box of
 // [32, 1, 64, 1] and the 64-byte swizzle (used when p.out_tma is set).
+cudaError_t launch_state(const PrefillParams& p, const CUtensorMap& out_map, cudaStream_t s);
 cudaError_t launch_state_head(const PrefillParams& p, const CUtensorMap& out_map, cudaStream_t s);
 
 struct VerifyParams {

@@ -49,7 +49,7 @@ constexpr uint32_t O_VN = O_S + 16384;         // V_new bf16: 64 token rows (8 K
 constexpr uint32_t kStateSmem = O_VN + 8192 + 1024;
 constexpr uint32_t kRowGroup = 1024;
 constexpr uint32_t TM_D1 = 0, TM_D2 = 32, TM_COLS = 64;
-constexpr uint32_t kBarVn = 1, kBarChunk = 2;  // named barriers (0 is __syncthreads)
+constexpr uint32_t kBarVn = 1, kBarChunk = 2, kBarOut = 3;  // named barriers (0 is __syncthreads)
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
     const bool ok = mbar_wait(bar, parity, abort);
@@ -57,7 +57,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 template <bool kStall>
-__global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillParams p) {
+__global__ void __launch_bounds__(kStateThreads, 1)
+    state_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap out_map) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -235,23 +236,42 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
                     umma_commit(&p2_done);
                     umma_commit(&empty[st]);
                 }
-            } else if (ok) {
+            } else {
                 // O = O_loc + Q' S for token row `row - 64`
                 const int i = row - 64;
                 const int t0 = 64 * c;
                 stall_point<kStall>(p.stall_seed, 4, c);
-                if (t0 + i < seq_len) {
-                    uint32_t o[kSlab / 2];
+                uint32_t o[kSlab / 2];
 #pragma unroll
-                    for (int ch = 0; ch < 4; ++ch) {
-                        const uint4 ol = slab_row[ch];
-                        const uint32_t ow[4] = {ol.x, ol.y, ol.z, ol.w};
+                for (int ch = 0; ch < 4; ++ch) {
+                    const uint4 ol = slab_row[ch];
+                    const uint32_t ow[4] = {ol.x, ol.y, ol.z, ol.w};
 #pragma unroll
-                        for (int x = 0; x < 4; ++x) {
-                            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[x]));
-                            o[4 * ch + x] = pack_bf16x2(f.x + d[8 * ch + 2 * x], f.y + d[8 * ch + 2 * x + 1]);
-                        }
+                    for (int x = 0; x < 4; ++x) {
+                        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[x]));
+                        o[4 * ch + x] = pack_bf16x2(f.x + d[8 * ch + 2 * x], f.y + d[8 * ch + 2 * x + 1]);
                     }
+                }
+                // Rows of a chunk inside its sequence (padded: every chunk, the tensor
+                // store clips rows past T) leave by one tensor store of the slab: each
+                // thread writes its row over the O_loc bytes it read (the box's
+                // 64-byte-swizzled layout).  Rows of a varlen tail chunk, which the
+                // next sequence's rows follow, are stored one by one.
+                const bool by_tma = p.out_tma && (p.cu == nullptr || t0 + kChunk <= seq_len);
+                if (by_tma) {
+                    uint8_t* img = sm + st * kStage + ST_OL;
+#pragma unroll
+                    for (int x = 0; x < kSlab / 8; ++x)
+                        *reinterpret_cast<uint4*>(img + slab_chunk_off(i, x)) =
+                            make_uint4(o[4 * x], o[4 * x + 1], o[4 * x + 2], o[4 * x + 3]);
+                    fence_proxy_async_smem();
+                    named_bar_sync(kBarOut, 64);  // the two output warps
+                    if (qd == 2 && lane == 0 && ok && !*abort) {
+                        const int tok = (int)(p.cu == nullptr ? t0 : (int64_t)tbase + t0);
+                        tma_store_4d(&out_map, kSlab * slab, h, tok, b, img);
+                        bulk_commit();
+                    }
+                } else if (ok && t0 + i < seq_len) {
                     const int64_t t = (int64_t)tbase + t0 + i;
                     uint4* dst = reinterpret_cast<uint4*>(p.out + b * p.os[0] + t * p.os[1] + h * p.os[2] + slab * kSlab);
 #pragma unroll
@@ -273,11 +293,15 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
             } else {
                 fail();
             }
+            // The output slab's tensor store has read the stage before the stage is
+            // released (the issuer's arrive below follows the barrier).
+            if (qd == 2 && lane == 0) bulk_wait_read();
             // Every epilogue thread takes the same decision: the fetcher warp may set
             // the abort flag at any time, so it is reduced over the barrier.
             if (named_bar_or(kBarChunk, 128, *abort != 0)) break;
             if (issuer) mbar_arrive(&empty[st]);
         }
+        if (qd == 2 && lane == 0) bulk_wait_all();  // the output tensor stores are complete
         if (issuer && count > 0) {
             // every product issued has completed before TMEM is released
             umma_commit(&bar_fin);
@@ -297,14 +321,14 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const PrefillPa
 
 }  // namespace
 
-cudaError_t launch_state(const PrefillParams& p, cudaStream_t s) {
+cudaError_t launch_state(const PrefillParams& p, const CUtensorMap& out_map, cudaStream_t s) {
     if (p.N == 0 || p.H == 0) return cudaSuccess;
     auto kern = p.stall_seed ? state_kernel<true> : state_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kStateSmem);
     if (e != cudaSuccess) return e;
     dim3 grid(kHeadDim / kSlab, p.H, p.N);
-    kern<<<grid, kStateThreads, kStateSmem, s>>>(p);
+    kern<<<grid, kStateThreads, kStateSmem, s>>>(p, out_map);
     return cudaGetLastError();
 }
 
