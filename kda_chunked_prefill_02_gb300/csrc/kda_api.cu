@@ -198,7 +198,7 @@ bool whole_chain_kernel(const PrefillParams& p, int num_sms) {
 // pass of segment s leaves free.  The choice simulates both streams from
 // per-unit costs measured on GB300 (SM clock 2070 MHz, long workload): one
 // (chunk, head) record takes a prep CTA 8.7 us on a full GPU and 8.25 us on the
-// SMs beside a state pass; a chunk step takes 1.13 us in the slab kernel (four
+// SMs beside a state pass; a chunk step takes 1.05 us in the slab kernel (four
 // CTAs per chain) and 2.15 us in the whole-chain kernel, 2 % more beside prep;
 // every segment adds about 12 us to each stream (launch, start-up, the slowest
 // CTA's tail).  Fitted to a sweep of segment lengths 30..160 within 2 %.
@@ -209,7 +209,7 @@ struct Segments {
     int prep_ctas = 0;       // prep grid while a state pass runs beside it
 };
 
-constexpr double kRecUs = 8.7, kSlabStepUs = 1.13, kHeadStepUs = 2.15;
+constexpr double kRecUs = 8.7, kSlabStepUs = 1.05, kHeadStepUs = 2.15;
 constexpr double kPrepBeside = 0.95, kStateBeside = 1.02, kSegmentUs = 12.0;
 
 // Estimated time of the segmented schedule: prep of segment i ends at P_i =
@@ -239,8 +239,9 @@ Segments plan_segments(const PrefillParams& p, int num_sms) {
     const bool allow_slab = !p.gate && !(force && !strcmp(force, "head"));
     const bool allow_head = p.gate || !(force && !strcmp(force, "slab"));
     auto waves = [](long long n, long long m) { return (double)((n + m - 1) / m); };
-    // sequential: prep on every SM, then the state pass
-    double best = waves(cps * chains, num_sms) * kRecUs +
+    // sequential: prep on every SM, then the state pass (each with its start-up
+    // and tail, as a segment's)
+    double best = waves(cps * chains, num_sms) * kRecUs + 2.0 * kSegmentUs +
                   (whole_chain_kernel(p, num_sms) ? waves(chains, num_sms) * cps * kHeadStepUs
                                                   : waves(4 * chains, num_sms) * cps * kSlabStepUs);
     best *= 0.95;   // segment only for a clear gain
