@@ -49,7 +49,7 @@ constexpr uint32_t OH_S = kHStages * kHStage;       // S bf16: 128 key rows (32 
 constexpr uint32_t OH_VN = OH_S + 32768;            // V_new bf16: 64 token rows (16 KB)
 constexpr uint32_t kHeadSmem = OH_VN + 16384 + 1024;
 constexpr uint32_t TMH_D1 = 0, TMH_D2 = 128, TMH_COLS = 256;
-constexpr uint32_t kBarHVn = 1, kBarHChunk = 2, kBarHNorm = 3;  // named barriers (0 is __syncthreads)
+constexpr uint32_t kBarHVn = 1, kBarHChunk = 2, kBarHNorm = 3, kBarHOut = 4;  // named barriers (0 is __syncthreads)
 
 // sigmoid(x) = 1/2 + tanh(x/2)/2, with the hardware tanh approximation
 // (relative error ~2^-11, below the bf16 rounding of the output).
@@ -163,15 +163,11 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
         tc_fence_before();
         named_bar_or(kBarHChunk, 512, false);
         int done = 0;    // chunks finished
-        bool reload = false;  // issuer: the previous chunk's stage awaits its next record
 
         for (int c = 0; c < count; ++c) {
             const int st = c % kHStages;
             const uint8_t* sb = sm + st * kHStage;
             const uint32_t sb_addr = smem_u32(sb);
-            // the chunk lies inside its sequence (padded: always; the tensor map
-            // clips rows past T): its output rows leave by tensor store
-            const bool by_tma = p.out_tma && (p.cu == nullptr || 64 * c + kChunk <= seq_len);
             bool ok = warp_wait_h(&full[st], (c / kHStages) & 1, abort);
             stall_point<kStall>(p.stall_seed, 1, c);
             if (issuer && ok) {
@@ -183,12 +179,6 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
                     umma_bf16(tb + TMH_D1, ad + ((k >> 2) * (16384 >> 4) + (k & 3) * 2),
                               bd + k * ((2 * kHSbo) >> 4), id, k > 0 ? 1u : 0u);
                 umma_commit(&p1_done);
-            }
-            if (issuer && reload) {
-                // the previous chunk's output tensor stores have read its stage
-                bulk_wait_read();
-                if (issued < count) issue_load(issued++);
-                reload = false;
             }
             __syncwarp();
             // This thread's U (W rows) or O_loc (Q' rows) values, read while P1 runs.
@@ -292,10 +282,10 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
                 // Rows of a chunk that lies inside its sequence (padded calls: every
                 // chunk, the tensor store clips the rows past T) leave by tensor store:
                 // each thread writes its bf16 row piece over the O_loc bytes it read
-                // (the same 64-byte-swizzled slab layout as the store box), and once
-                // the chunk barrier has gathered every row one thread stores the four
-                // slabs.  Rows of a varlen tail chunk, which the next sequence's rows
-                // follow, are stored one by one.
+                // (the same 64-byte-swizzled slab layout as the store box), and one
+                // thread stores the four slabs.  Rows of a varlen tail chunk, which
+                // the next sequence's rows follow, are stored one by one.
+                const bool by_tma = p.out_tma && (p.cu == nullptr || t0 + kChunk <= seq_len);
                 if (by_tma) {
                     uint8_t* img = sm + st * kHStage + SH_OL + cq * kSlabImg;
 #pragma unroll
@@ -304,6 +294,14 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
                             make_uint4(pack_bf16x2(o[8 * x], o[8 * x + 1]), pack_bf16x2(o[8 * x + 2], o[8 * x + 3]),
                                        pack_bf16x2(o[8 * x + 4], o[8 * x + 5]), pack_bf16x2(o[8 * x + 6], o[8 * x + 7]));
                     fence_proxy_async_smem();
+                    named_bar_sync(kBarHOut, 256);  // the eight output warps
+                    if (issuer && ok && !*abort) {
+                        const int tok = (int)(p.cu == nullptr ? t0 : (int64_t)tbase + t0);
+#pragma unroll
+                        for (int sl = 0; sl < kHeadDim / kSlab; ++sl)
+                            tma_store_4d(&out_map, kSlab * sl, h, tok, b, sb + SH_OL + sl * kSlabImg);
+                        bulk_commit();
+                    }
                 } else if (ok && valid_row) {
                     uint4* dst = reinterpret_cast<uint4*>(p.out + b * p.os[0] + t * p.os[1] + h * p.os[2] + kSlab * cq);
 #pragma unroll
@@ -332,22 +330,12 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
             tc_fence_before();
             if (named_bar_or(kBarHChunk, 512, *abort != 0)) break;
             done = c + 1;
-            // stage st is free but for the output rows staged in it: P2 of chunk c
-            // completed and every other read of it is done.  The issuer stores the
-            // rows now and loads the stage's next record after the next chunk's P1
-            // issue, once the stores have read it.
+            // stage st is free: P2 of chunk c completed, every read of it is done
+            // and (issuer) the output tensor stores have read their slabs
             stall_point<kStall>(p.stall_seed, 5, c);
-            if (issuer) {
-                if (by_tma) {
-                    const int tok = (int)(p.cu == nullptr ? 64 * c : (int64_t)tbase + 64 * c);
-#pragma unroll
-                    for (int sl = 0; sl < kHeadDim / kSlab; ++sl)
-                        tma_store_4d(&out_map, kSlab * sl, h, tok, b, sb + SH_OL + sl * kSlabImg);
-                    bulk_commit();
-                    reload = true;
-                } else if (issued < count) {
-                    issue_load(issued++);
-                }
+            if (issuer && issued < count) {
+                bulk_wait_read();
+                issue_load(issued++);
             }
         }
         if (issuer) {
