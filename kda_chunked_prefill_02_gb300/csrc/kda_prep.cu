@@ -406,12 +406,20 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             const bool lo = lane < 16;
             const float bi = sBeta[i];
             const int J = cq;
+            // The three tiles this warp may need, with one wait (a tile the warp's
+            // rows do not use is read and ignored; every address lies inside
+            // the allocation).
             float t0[16], t1[16], tm[16];
-#pragma unroll
-            for (int x = 0; x < 16; ++x) { t0[x] = 0.f; t1[x] = 0.f; tm[x] = 0.f; }
-            if (J < I0) tmem_ld16(tmem_addr(tb, 32 * qd, TM_A + yoff_row(I0, J, 0)), t0);
-            if (J < I1) tmem_ld16(tmem_addr(tb, 32 * qd, TM_A + yoff_row(I1, J, 0)), t1);
-            if (J <= I1) tmem_ld16(tmem_addr(tb, 32 * qd, TM_DIAG + 16 * J), tm);
+            {
+                uint32_t r0[16], r1[16], rm[16];
+                tmem_ld16_issue(tmem_addr(tb, 32 * qd, TM_A + yoff_row(I0, J, 0)), r0);
+                tmem_ld16_issue(tmem_addr(tb, 32 * qd, TM_A + yoff_row(I1, J, 0)), r1);
+                tmem_ld16_issue(tmem_addr(tb, 32 * qd, TM_DIAG + 16 * J), rm);
+                tmem_wait_ld();
+                tmem_take16(r0, t0);
+                tmem_take16(r1, t1);
+                tmem_take16(rm, tm);
+            }
             float v[16];
 #pragma unroll
             for (int x = 0; x < 16; ++x) {
@@ -570,10 +578,14 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             const bool top = qd < 2;
             const int half = cq >> 1;
 #pragma unroll 1
-            for (int cg = 0; cg < 4; ++cg) {
-                const int col = 64 * (cq & 1) + 16 * cg;
-                float v[16];
-                tmem_ld16(tmem_addr(tb, 32 * qd, TM_C + 128 * half + col), v);
+            for (int cg2 = 0; cg2 < 2; ++cg2) {
+              // two 16-column groups per load wait
+              float vv[32];
+              tmem_ld32(tmem_addr(tb, 32 * qd, TM_C + 128 * half + 64 * (cq & 1) + 32 * cg2), vv);
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                const int col = 64 * (cq & 1) + 32 * cg2 + 16 * hh;
+                const float* v = vv + 16 * hh;
                 if (half == 0) {
                     uint32_t w[8];
                     if (top) {
@@ -599,6 +611,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                     *reinterpret_cast<uint4*>(img + slab_chunk_off(i, c8)) = make_uint4(w[0], w[1], w[2], w[3]);
                     *reinterpret_cast<uint4*>(img + slab_chunk_off(i, c8 + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
                 }
+              }
             }
         }
         stall_point<kStall>(p.stall_seed, 13, it);

@@ -201,8 +201,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
             tc_fence_after();
             float d[kSlab];
             if (ok) {
-                tmem_ld16(tb + lane_base + TM_D1, *reinterpret_cast<float(*)[16]>(&d[0]));
-                tmem_ld16(tb + lane_base + TM_D1 + 16, *reinterpret_cast<float(*)[16]>(&d[16]));
+                tmem_ld32(tb + lane_base + TM_D1, d);
             }
             if (qd < 2) {
                 // V_new = U - W S for token row `row`; stored transposed (K-major over tokens)
@@ -283,8 +282,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
             ok = ok && warp_wait(&p2_done, c & 1, abort);
             tc_fence_after();
             if (ok) {
-                tmem_ld16(tb + lane_base + TM_D2, *reinterpret_cast<float(*)[16]>(&d[0]));
-                tmem_ld16(tb + lane_base + TM_D2 + 16, *reinterpret_cast<float(*)[16]>(&d[16]));
+                tmem_ld32(tb + lane_base + TM_D2, d);
                 const float eg = reinterpret_cast<const float*>(sb + ST_EG)[row];
 #pragma unroll
                 for (int j = 0; j < kSlab; ++j) S[j] = fmaf(eg, S[j], d[j]);

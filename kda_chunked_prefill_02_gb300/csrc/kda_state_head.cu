@@ -193,8 +193,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
             tc_fence_after();
             float d[kSlab];
             if (ok) {
-                tmem_ld16(tb + lane_base + TMH_D1 + kSlab * cq, *reinterpret_cast<float(*)[16]>(&d[0]));
-                tmem_ld16(tb + lane_base + TMH_D1 + kSlab * cq + 16, *reinterpret_cast<float(*)[16]>(&d[16]));
+                tmem_ld32(tb + lane_base + TMH_D1 + kSlab * cq, d);
             }
             if (qd < 2) {
                 // V_new = U - W S for token row `row`
@@ -314,8 +313,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
             ok = ok && warp_wait_h(&p2_done, c & 1, abort);
             tc_fence_after();
             if (ok) {
-                tmem_ld16(tb + lane_base + TMH_D2 + kSlab * cq, *reinterpret_cast<float(*)[16]>(&d[0]));
-                tmem_ld16(tb + lane_base + TMH_D2 + kSlab * cq + 16, *reinterpret_cast<float(*)[16]>(&d[16]));
+                tmem_ld32(tb + lane_base + TMH_D2 + kSlab * cq, d);
                 const float eg = reinterpret_cast<const float*>(sb + SH_EG)[row];
 #pragma unroll
                 for (int j = 0; j < kSlab; ++j) S[j] = fmaf(eg, S[j], d[j]);
