@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define KDA_ABI_VERSION 3
+#define KDA_ABI_VERSION 4
 
 typedef enum {
     KDA_OK = 0,
@@ -218,6 +218,9 @@ kda_status kda_prefill_state(const kda_prefill_args* args, void* stream);
  *   [65536, 81920)    O_loc = Aqk U bf16, same layout
  *   [81920, 82432)    exp(gam) fp32 [128], gam = chunk total of g
  * Rows past a tail chunk's length are zero.  chunk_offset: int32 [N+1].
+ * seq_order (varlen): the sequences by descending chunk count (ties by index;
+ * index order beyond 1024 sequences), the order in which the state pass's
+ * CTAs take them.
  * A segmented kda_prefill (see there) keeps the records of each token segment
  * together: segment s's records follow those of segments 0..s-1, numbered
  * as above within the segment.
@@ -226,6 +229,7 @@ typedef struct kda_workspace_layout {
     size_t records, record_bytes, chunk_offset, status, total;
     int64_t max_chunks;         /* records per head */
     size_t state_carry;         /* padded calls: fp32 [B, H, 128, 128] */
+    size_t seq_order;           /* varlen calls: int32 [N], sequences longest first */
 } kda_workspace_layout;
 kda_status kda_prefill_workspace_layout(const kda_prefill_args* args,
                                         kda_workspace_layout* layout);

@@ -31,6 +31,7 @@ bool layout_of(const kda_prefill_args* a, kda_workspace_layout* L) {
     L->record_bytes = kRecBytes;
     L->records = o; o = align_up(o + nrec * kRecBytes);
     L->chunk_offset = o; o = align_up(o + sizeof(int32_t) * (size_t)(a->num_seqs + 1));
+    L->seq_order = o; o = align_up(o + (a->cu_seqlens ? sizeof(int32_t) * (size_t)a->num_seqs : 0));
     L->status = o; o = align_up(o + sizeof(int32_t));
     // padded calls: the state of every chain between two segments of the
     // segmented schedule (run_prefill)
@@ -112,6 +113,7 @@ void fill_params(const kda_prefill_args* a, const kda_workspace_layout& L, Prefi
     p->hT = a->final_state;
     p->cu = a->cu_seqlens;
     p->chunk_off = reinterpret_cast<int32_t*>(ws + L.chunk_offset);
+    p->seq_order = a->cu_seqlens ? reinterpret_cast<int32_t*>(ws + L.seq_order) : nullptr;
     p->status = a->device_status ? a->device_status : reinterpret_cast<int32_t*>(ws + L.status);
     p->B = (int)a->batch;
     p->T = (int)a->seqlen;

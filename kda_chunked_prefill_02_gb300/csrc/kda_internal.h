@@ -45,6 +45,7 @@ struct PrefillParams {
     float* hT;
     const int32_t* cu;       // device cu_seqlens (varlen) or nullptr (padded)
     int32_t* chunk_off;      // [N+1] in the workspace (varlen)
+    int32_t* seq_order;      // [N] in the workspace (varlen): sequences, longest first
     int32_t* status;         // device status word (never null)
     int B, T, N, H;          // T: per-sequence length (padded) or total tokens (varlen)
     int max_chunks;          // chunk records per head (upper bound)

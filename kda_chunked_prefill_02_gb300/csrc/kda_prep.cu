@@ -658,6 +658,8 @@ __global__ void __launch_bounds__(1024) chunk_table_kernel(const PrefillParams p
     __syncthreads();
     if (bad) {
         for (int n = tid; n <= p.N; n += blockDim.x) p.chunk_off[n] = 0;
+        if (p.seq_order)
+            for (int n = tid; n < p.N; n += blockDim.x) p.seq_order[n] = n;
         if (tid == 0) atomicExch(p.status, 1);
         return;
     }
@@ -689,6 +691,30 @@ __global__ void __launch_bounds__(1024) chunk_table_kernel(const PrefillParams p
         __syncthreads();
     }
     if (tid == 0) p.chunk_off[p.N] = carry;
+    // The order in which the state pass takes the sequences (its CTAs are
+    // launched sequence by sequence): longest chain first, so that the chains
+    // that set the pass's length start in the first wave of CTAs and the short
+    // ones fill in behind them.  Up to 1024 sequences are ranked (ties by
+    // index); beyond that the order is the index order.
+    if (p.seq_order) {
+        __shared__ int cnts[1024];
+        if (p.N <= (int)blockDim.x) {
+            const int n = tid;
+            const int mine = n < p.N ? (p.cu[n + 1] - p.cu[n] + kChunk - 1) / kChunk : 0;
+            if (n < p.N) cnts[n] = mine;
+            __syncthreads();
+            if (n < p.N) {
+                int rank = 0;
+                for (int m = 0; m < p.N; ++m) {
+                    const int cm = cnts[m];
+                    rank += (cm > mine || (cm == mine && m < n)) ? 1 : 0;
+                }
+                p.seq_order[rank] = n;
+            }
+        } else {
+            for (int n = tid; n < p.N; n += blockDim.x) p.seq_order[n] = n;
+        }
+    }
 }
 
 }  // namespace

@@ -66,7 +66,9 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
 
-    const int slab = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
+    const int slab = blockIdx.x, h = blockIdx.y;
+    // varlen: the sequences in the order of the chunk table (longest first)
+    const int n = p.seq_order ? p.seq_order[blockIdx.z] : (int)blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     // Chain extent.

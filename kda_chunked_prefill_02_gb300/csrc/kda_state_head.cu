@@ -88,7 +88,9 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
     __shared__ float s_ss[4][64];      // fused norm: partial sums of squares per column quarter
     __shared__ __align__(16) float s_w[kHeadDim];  // fused norm: weights
 
-    const int h = blockIdx.x, n = blockIdx.y;
+    const int h = blockIdx.x;
+    // varlen: the sequences in the order of the chunk table (longest first)
+    const int n = p.seq_order ? p.seq_order[blockIdx.y] : (int)blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     // Chain extent.

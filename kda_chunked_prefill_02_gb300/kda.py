@@ -61,7 +61,7 @@ class WorkspaceLayout(ctypes.Structure):
     _fields_ = [("records", ctypes.c_size_t), ("record_bytes", ctypes.c_size_t),
                 ("chunk_offset", ctypes.c_size_t), ("status", ctypes.c_size_t),
                 ("total", ctypes.c_size_t), ("max_chunks", _i64),
-                ("state_carry", ctypes.c_size_t)]
+                ("state_carry", ctypes.c_size_t), ("seq_order", ctypes.c_size_t)]
 
 
 class Schedule(ctypes.Structure):

@@ -33,7 +33,7 @@ def test_exports_every_declared_symbol(K):
             "kda_status_string"} <= names
     for n in sorted(names):
         assert hasattr(lib, n), n
-    assert lib.kda_abi_version() == 3
+    assert lib.kda_abi_version() == 4
 
 
 def _args(K, **kw):
@@ -89,6 +89,9 @@ def test_workspace_plan(K):
     a2 = _args(K, cu_seqlens=ctypes.c_void_p(1 << 12), num_seqs=3, seqlen=130)
     assert lib.kda_prefill_workspace_layout(ctypes.byref(a2), ctypes.byref(L)) == 0
     assert L.max_chunks == 130 // 64 + 3
+    # varlen: the state-pass order of the sequences, int32 [N], after the chunk table
+    assert L.seq_order >= L.chunk_offset + 4 * 4 and L.seq_order % 256 == 0
+    assert L.status >= L.seq_order + 3 * 4
 
 
 def test_verify_validation(K):

@@ -242,3 +242,23 @@ def test_many_heads_sampled():
     sub = head_subset(inp, heads)
     ro, rf = oracle_prefill(sub)
     assert_parity(out[:, :, heads], fin[:, heads], ro, rf, "H=300")
+
+
+def test_state_pass_takes_longest_sequences_first():
+    """The chunk table ranks varlen sequences by chunk count, longest first
+    (ties by index), for the order of the state pass's CTAs; results do not
+    depend on it."""
+    import kda_chunked_prefill_02_gb300 as K
+    lengths = [17, 0, 300, 64, 65, 1]            # chunks 1, 0, 5, 1, 2, 1
+    inp = inputs.prefill_inputs(95, lengths=lengths, H=2)
+    d = inp.to("cuda")
+    ws = torch.full((K.workspace_size(d.q, d.v, cu_seqlens=d.cu_seqlens),), 0xFF, dtype=torch.uint8,
+                    device="cuda")
+    out, fin = K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, initial_state=d.initial_state,
+                             cu_seqlens=d.cu_seqlens, workspace=ws)
+    torch.cuda.synchronize()
+    L = K.workspace_layout(d.q, cu_seqlens=d.cu_seqlens)
+    order = ws[L.seq_order:L.seq_order + 4 * len(lengths)].cpu().view(torch.int32).tolist()
+    assert order == [2, 4, 0, 3, 5, 1]
+    ro, rf = oracle_prefill(inp)
+    assert_parity(out, fin, ro, rf, "longest-first order")
