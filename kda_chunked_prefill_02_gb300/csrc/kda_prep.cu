@@ -205,43 +205,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     float bcur = load_beta(ci, rec % p.H);
     bool ok = true;
     int pend_parity = ci.len > 0 ? 0 : -1;  // parity of an input load still in flight
-
-    // Gate phase of a record whose input tiles were requested with the given
-    // mbarrier parity: wait for them, zero the rows past the chunk length (k =
-    // q = v = 0 and g = 0, no decay), then E1: p = exp(g) and each 8-token
-    // group's decay products, exact and with the floored gate, into the TOT
-    // table.  Every decay factor of the operand build is a product of these.
-    // Runs for the first record before the loop and for each next record
-    // while the current record's last tensor-core product runs.
-    auto gate_phase = [&](const ChunkInfo& c, uint32_t parity) -> bool {
-        // One thread waits on each mbarrier; the others wait at the CTA barrier.
-        if (!__syncthreads_and(tid == 0 ? mbar_wait(&bar_in, parity, nullptr) : true)) return false;
-        pend_parity = -1;
-        if (c.len < kChunk) {
-            for (int e = tid; e < (kChunk - c.len) * 80; e += kPrepThreads) {
-                const int row = c.len + e / 80, u = e % 80;
-                uint8_t* dst = u < 48 ? sm + (u >> 4) * 16384 + row * 256 + (u & 15) * 16
-                                      : sm + O_IG + row * 512 + (u - 48) * 16;
-                *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
-            }
-            __syncthreads();
-        }
-        float e0 = 1.f, e1 = 1.f, f0 = 1.f, f1 = 1.f;
-#pragma unroll
-        for (int l = 0; l < 8; ++l) {
-            const float2 gv = *reinterpret_cast<const float2*>(sm + O_IG + (8 * h8 + l) * 512 + c0 * 4);
-            const float q0 = __expf(gv.x), q1 = __expf(gv.y);
-            e0 *= q0; e1 *= q1;
-            f0 *= fmaxf(q0, kPFloor); f1 *= fmaxf(q1, kPFloor);
-        }
-        float* tot = reinterpret_cast<float*>(sm + O_TOT);
-        *reinterpret_cast<float2*>(tot + h8 * 128 + c0) = make_float2(e0, e1);
-        *reinterpret_cast<float2*>(tot + 1024 + h8 * 128 + c0) = make_float2(f0, f1);
-        return true;
-    };
-    if (ci.len > 0) ok = gate_phase(ci, 0);
-
-    for (uint32_t it = 0; ok && ci.len > 0; ++it) {
+    for (uint32_t it = 0; ci.len > 0; ++it) {
         const int len = ci.len;
         const int rec_next = rec + gridDim.x;
         const ChunkInfo cn = rec_next < nrec ? chunk_info(p, rec_next / p.H) : ChunkInfo{0, 0, 0, 0, 0};
@@ -249,19 +213,44 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         // may start once every CTA has reached this point.
         if (rec_next >= nrec) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         stall_point<kStall>(p.stall_seed, 1, it);
+        // One thread waits on each mbarrier; the others wait at the CTA barrier.
+        ok = __syncthreads_and(tid == 0 ? mbar_wait(&bar_in, it & 1, nullptr) : true);
+        if (!ok) break;
+        pend_parity = -1;
         if (tid < 64) {
             float bval = bcur;
             if (tid < len && p.beta_is_logit) bval = 1.0f / (1.0f + __expf(-bval));
             reinterpret_cast<float*>(sm + O_BETA)[tid] = tid < len ? bval : 0.f;
         }
-        // p = exp(g) again for this thread's elements (the gate phase kept only
-        // the group products; the same instruction on the same input gives the
-        // same bits).
+
+        // Tokens past the chunk length (the tail of a sequence) read as zeros:
+        // k = q = v = 0 and g = 0 (no decay).
+        if (len < kChunk) {
+            for (int e = tid; e < (kChunk - len) * 80; e += kPrepThreads) {
+                const int row = len + e / 80, u = e % 80;
+                uint8_t* dst = u < 48 ? sm + (u >> 4) * 16384 + row * 256 + (u & 15) * 16
+                                      : sm + O_IG + row * 512 + (u - 48) * 16;
+                *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            __syncthreads();
+        }
+
+        // ---- E1: p = exp(g) and the 8-token group's decay products, exact and
+        // with the floored gate.  Every decay factor below is a product of these,
+        // so the gate phase takes one exponential per element and no more.
         float p0[8], p1[8];
+        {
+            float e0 = 1.f, e1 = 1.f, f0 = 1.f, f1 = 1.f;
 #pragma unroll
-        for (int l = 0; l < 8; ++l) {
-            const float2 gv = *reinterpret_cast<const float2*>(sm + O_IG + (8 * h8 + l) * 512 + c0 * 4);
-            p0[l] = __expf(gv.x); p1[l] = __expf(gv.y);
+            for (int l = 0; l < 8; ++l) {
+                const float2 gv = *reinterpret_cast<const float2*>(sm + O_IG + (8 * h8 + l) * 512 + c0 * 4);
+                p0[l] = __expf(gv.x); p1[l] = __expf(gv.y);
+                e0 *= p0[l]; e1 *= p1[l];
+                f0 *= fmaxf(p0[l], kPFloor); f1 *= fmaxf(p1[l], kPFloor);
+            }
+            float* tot = reinterpret_cast<float*>(sm + O_TOT);
+            *reinterpret_cast<float2*>(tot + h8 * 128 + c0) = make_float2(e0, e1);
+            *reinterpret_cast<float2*>(tot + 1024 + h8 * 128 + c0) = make_float2(f0, f1);
         }
         stall_point<kStall>(p.stall_seed, 2, it);
         if (tid == 0) bulk_wait_read();  // the previous record's images have left the staging area
@@ -577,14 +566,9 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                           idesc_bf16_f32_bmn(128, 256), k > 0 ? 1u : 0u);
             umma_commit(&bar_mma[2]);
         }
-        // While MMA C runs, the next record's gate phase (its inputs were requested
-        // once MMA A completed; it writes only the input tiles' tails and the TOT
-        // table, which neither MMA C nor epilogue C reads).
-        const bool next_ok = cn.len > 0 ? gate_phase(cn, (it + 1) & 1) : true;
         ok = __syncthreads_and(tid == 0 ? mbar_wait(&bar_mma[2], it & 1, nullptr) : true);
         tc_fence_after();
         if (!ok) break;
-        ok = next_ok;   // on a failed input wait this record still completes
         stall_point<kStall>(p.stall_seed, 12, it);
         {
             // ---- Epilogue C: [W ; Q'] rows (Q' = Q e^Gam - Aqk W) from the first 128
