@@ -158,3 +158,22 @@ def test_segments_without_programmatic_launch():
     with _env(KDA_SEGMENT_CHUNKS=2, KDA_STATE_KERNEL=None, KDA_SEGMENT_PDL=0):
         b = _run(d)
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("kernel,seg", [("head", 0), ("slab", 0), ("head", 2), ("slab", 2)])
+def test_output_tensor_store_into_strided_out(kernel, seg):
+    """The state kernels store the output rows by tensor store through a map of
+    `out` with the caller's strides: a row-padded out view (token and head
+    strides not dense) gets the same bits as a dense one, and the padding
+    between rows stays untouched."""
+    import kda_chunked_prefill_02_gb300 as K
+    inp = inputs.prefill_inputs(856, B=2, T=64 * 4 + 9, H=3)
+    d = inp.to("cuda")
+    with _env(KDA_STATE_KERNEL=kernel, KDA_SEGMENT_CHUNKS=seg):
+        ref, _ = K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, initial_state=d.initial_state)
+        big = torch.full(d.v.shape[:-1] + (128 + 24,), 7.0, dtype=torch.bfloat16, device="cuda")
+        out = big[..., :128]
+        K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, initial_state=d.initial_state, out=out)
+        torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    assert bool((big[..., 128:] == 7.0).all())
