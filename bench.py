@@ -306,7 +306,7 @@ def run_e2e(r, args, ws):
         K.kda_prefill_host(host.q, host.k, host.v, host.g, host.beta, initial_state=host.initial_state,
                            cu_seqlens=cu, out=out_h, final_state=fin_h, staging=staging, stream=stream)
 
-    for _ in range(2):
+    for _ in range(max(3, args.warmup)):
         step()
     k = max(3, args.steps // 4)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
