@@ -177,15 +177,6 @@ bool make_prep_maps(const kda_prefill_args* a, PrepMaps* m) {
            make_input_map(&m->g, a->g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a->g_stride, H, T, B);
 }
 
-// Which prep kernel a one-pass call runs: the one-CTA-per-SM kernel, or with
-// KDA_PREP_KERNEL=2 the two-CTAs-per-SM kernel (same records, bit for bit).
-// The segmented schedule keeps the one-CTA kernel, whose SMs the state
-// kernel's CTAs can take.
-bool prep_two_per_sm() {
-    const char* e = getenv("KDA_PREP_KERNEL");
-    return e && !strcmp(e, "2");
-}
-
 // Which state kernel a sequential call runs: one CTA per chain (all 128 value
 // columns) when the 32-column slab CTAs would need more than two waves of SMs
 // (a whole-chain CTA takes about twice as long per chunk step, measured), so
@@ -371,15 +362,11 @@ kda_status run_prefill(const kda_prefill_args* a, void* stream, int stages) {
         if (sg.on) return run_segments(a, p, sg, L, num_sms, s);
     }
     if (prep) {
+        PrepMaps pmaps;
+        memset(&pmaps, 0, sizeof(pmaps));
+        if (!make_prep_maps(a, &pmaps)) return KDA_ERR_UNSUPPORTED;
         if (launch_chunk_table(p, s) != cudaSuccess) return KDA_ERR_CUDA;
-        if (prep_two_per_sm()) {
-            if (launch_prep2(p, num_sms, s) != cudaSuccess) return KDA_ERR_CUDA;
-        } else {
-            PrepMaps pmaps;
-            memset(&pmaps, 0, sizeof(pmaps));
-            if (!make_prep_maps(a, &pmaps)) return KDA_ERR_UNSUPPORTED;
-            if (launch_prep(p, pmaps, num_sms, s) != cudaSuccess) return KDA_ERR_CUDA;
-        }
+        if (launch_prep(p, pmaps, num_sms, s) != cudaSuccess) return KDA_ERR_CUDA;
     }
     if (state_pass) {
         if (launch_state_pass(a, p, whole_chain_kernel(p, num_sms), s) != cudaSuccess) return KDA_ERR_CUDA;

@@ -107,9 +107,6 @@ cudaError_t launch_chunk_table(const PrefillParams& p, cudaStream_t s);
 // same stream (the two may overlap; they must touch disjoint records).
 cudaError_t launch_prep(const PrefillParams& p, const PrepMaps& maps, int num_sms, cudaStream_t s,
                         bool overlap_previous = false);
-// The same preparation with two records in flight per SM (two 8-warp CTAs),
-// writing the same records bit for bit; inputs are read from global memory.
-cudaError_t launch_prep2(const PrefillParams& p, int num_sms, cudaStream_t s, bool overlap_previous = false);
 // out_map: tensor map of out, [channel 128, head, token, batch] with a box of
 // [32, 1, 64, 1] and the 64-byte swizzle (used when p.out_tma is set).
 cudaError_t launch_state(const PrefillParams& p, const CUtensorMap& out_map, cudaStream_t s);
