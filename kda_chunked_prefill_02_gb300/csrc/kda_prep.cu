@@ -625,8 +625,9 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             bulk_store(rp + kRecOl, sm + O_SOL, 4 * kSlabImg);
             bulk_commit();
         }
+        // Epilogue C's TMEM reads are ordered before the next record's MMA A by
+        // this fence and the CTA barrier of the next input wait (the loop's top).
         tc_fence_before();
-        __syncthreads();
         rec = rec_next;
         ci = cn;
     }
