@@ -154,7 +154,8 @@ size_t kda_prefill_workspace_size(const kda_prefill_args* args);
  * the call's work ends) overlaps the prep of segment s+1, the state of every
  * chain passing between segments in fp32 through the workspace's
  * state_carry region, so the results are those of one state pass over the
- * whole sequence.
+ * whole sequence.  A call made while `stream` is being captured into a CUDA
+ * graph always takes the one-pass schedule (same results).
  * Returns KDA_OK once the kernels are enqueued.
  *
  * Environment overrides, read on every call (tests and measurements; results

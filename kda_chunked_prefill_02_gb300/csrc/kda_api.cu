@@ -358,8 +358,13 @@ kda_status run_prefill(const kda_prefill_args* a, void* stream, int stages) {
     if (prep && !a->device_status && cudaMemsetAsync(p.status, 0, sizeof(int32_t), s) != cudaSuccess)
         return KDA_ERR_CUDA;
     if (prep && state_pass) {
+        // The segmented schedule creates and releases a stream per call, which
+        // a stream capture (CUDA graph) cannot record: a capturing caller gets
+        // the one-pass schedule.
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) return KDA_ERR_CUDA;
         const Segments sg = plan_segments(p, num_sms);
-        if (sg.on) return run_segments(a, p, sg, L, num_sms, s);
+        if (sg.on && cap == cudaStreamCaptureStatusNone) return run_segments(a, p, sg, L, num_sms, s);
     }
     if (prep) {
         PrepMaps pmaps;
