@@ -236,6 +236,14 @@ def run_ours(args, rank, ws, local):
     clk = clocks.stop()
     ms = max_over_ranks(ms, ws)
 
+    # per call with a synchronize around each (median of 7), besides the
+    # back-to-back timing above
+    singles = []
+    for _ in range(7):
+        torch.cuda.synchronize()
+        singles.append(timed(step, 1))
+    ms_single = max_over_ranks(sorted(singles)[len(singles) // 2], ws)
+
     # per-kernel durations (each stage alone, same stream, same workspace)
     for _ in range(2):
         step("prep")
@@ -247,6 +255,7 @@ def run_ours(args, rank, ws, local):
         ms_prep -= ms_flush
         ms_state -= ms_flush
         ms -= ms_flush
+        ms_single -= ms_flush
 
     tokens_step = T * ws
     value = tokens_step / (ms / 1e3)
@@ -273,7 +282,7 @@ def run_ours(args, rank, ws, local):
     sched["state_kernel"] = "whole-chain" if sched.pop("whole_chain") else "slab"
     sched["kernels_per_call"] = launches
     return dict(traffic=traffic, ms=ms, value=value, clk=clk, ms_prep=ms_prep, ms_state=ms_state, dom=dom,
-                sched=sched,
+                sched=sched, ms_single=ms_single,
                 achieved=achieved, hbm=hbm, peak_src=peak_src, tensor_frac=tensor_frac,
                 tf_burst=tf_burst, path_gbs=path_bytes / (ms / 1e3) / 1e9, inp=inp, d=d,
                 out=out, fin=fin, wsb=wsb, stream=stream, flops=flops, dbytes=dbytes)
@@ -365,6 +374,8 @@ def main():
                          "traffic": r["traffic"], "peak_source": r["peak_src"],
                          "algorithmic_bytes": r["dbytes"],
                          "traffic_note": "ncu DRAM bytes of the capture in profiles/, scaled by token-heads"},
+            "per_call": {"ms": r["ms_single"], "tokens_per_s": inp.total_tokens * ws / (r["ms_single"] / 1e3),
+                         "note": "each call alone, synchronised before and after, median of 7"},
             "kernels_ms": {"prep": r["ms_prep"], "state": r["ms_state"],
                            "note": "each stage alone, one pass over all tokens (prep on every SM, then the state pass)"},
             "path_gbs": r["path_gbs"],
