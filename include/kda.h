@@ -154,8 +154,10 @@ size_t kda_prefill_workspace_size(const kda_prefill_args* args);
  * the call's work ends) overlaps the prep of segment s+1, the state of every
  * chain passing between segments in fp32 through the workspace's
  * state_carry region, so the results are those of one state pass over the
- * whole sequence.  A call made while `stream` is being captured into a CUDA
- * graph always takes the one-pass schedule (same results).
+ * whole sequence.  The second stream and two events are created on a host
+ * thread's first segmented call on a device and kept for the thread's life
+ * (calls of one thread share them), so segmented calls can be captured into a
+ * CUDA graph once one has run outside the capture.
  * Returns KDA_OK once the kernels are enqueued.
  *
  * Environment overrides, read on every call (tests and measurements; results

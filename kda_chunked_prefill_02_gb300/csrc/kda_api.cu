@@ -286,16 +286,43 @@ Segments plan_segments(const PrefillParams& p, int num_sms) {
 // Runs a planned segmented call: prep of every segment on `s`, the state pass of
 // every segment on a second stream, each after its segment's prep and after the
 // previous segment's state pass; `s` waits for the last state pass.
+// The second stream and the two events of segmented calls: one set per host
+// thread and device, created on the first segmented call and kept for the
+// thread's life, so that calls recorded into a CUDA graph create nothing.
+// Calls of one thread share the set (their state passes queue one after the
+// other on it; every dependency goes through the events).
+struct SideSet {
+    cudaStream_t ss;
+    cudaEvent_t ev_prep, ev_done;
+};
+bool side_set(SideSet* out) {
+    constexpr int kMaxDevices = 64;
+    thread_local SideSet sets[kMaxDevices] = {};
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    SideSet& st = sets[dev];
+    if (!st.ss) {
+        SideSet n{nullptr, nullptr, nullptr};
+        if (cudaStreamCreateWithFlags(&n.ss, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&n.ev_prep, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&n.ev_done, cudaEventDisableTiming) != cudaSuccess) {
+            if (n.ev_prep) cudaEventDestroy(n.ev_prep);
+            if (n.ss) cudaStreamDestroy(n.ss);
+            return false;
+        }
+        st = n;
+    }
+    *out = st;
+    return true;
+}
+
 kda_status run_segments(const kda_prefill_args* a, const PrefillParams& p, const Segments& sg,
-                        const kda_workspace_layout& L, int num_sms, cudaStream_t s) {
-    cudaStream_t ss = nullptr;
-    cudaEvent_t ev_prep = nullptr, ev_done = nullptr;
+                        const kda_workspace_layout& L, int num_sms, const SideSet& side, cudaStream_t s) {
+    cudaStream_t ss = side.ss;
+    cudaEvent_t ev_prep = side.ev_prep, ev_done = side.ev_done;
     auto ck = [](cudaError_t e) { return e == cudaSuccess; };
-    bool ok = ck(cudaStreamCreateWithFlags(&ss, cudaStreamNonBlocking)) &&
-              ck(cudaEventCreateWithFlags(&ev_prep, cudaEventDisableTiming)) &&
-              ck(cudaEventCreateWithFlags(&ev_done, cudaEventDisableTiming));
     // the side stream starts after the work already queued on `s`
-    ok = ok && ck(cudaEventRecord(ev_prep, s)) && ck(cudaStreamWaitEvent(ss, ev_prep, 0));
+    bool ok = ck(cudaEventRecord(ev_prep, s)) && ck(cudaStreamWaitEvent(ss, ev_prep, 0));
     float* carry = reinterpret_cast<float*>(static_cast<uint8_t*>(a->workspace) + L.state_carry);
     const int64_t seg_tokens = (int64_t)sg.chunks * kChunk;
     const char* pdl_env = getenv("KDA_SEGMENT_PDL");
@@ -328,14 +355,9 @@ kda_status run_segments(const kda_prefill_args* a, const PrefillParams& p, const
              ck(cudaEventRecord(ev_prep, s)) && ck(cudaStreamWaitEvent(ss, ev_prep, 0)) &&
              launch_state_pass(a, q, sg.head, ss) == cudaSuccess;
     }
-    if (ss && ev_done) {
-        // join even after a failure, so that nothing queued later on `s`
-        // overtakes a state pass already enqueued
-        if (ck(cudaEventRecord(ev_done, ss))) ck(cudaStreamWaitEvent(s, ev_done, 0));
-    }
-    if (ev_prep) cudaEventDestroy(ev_prep);
-    if (ev_done) cudaEventDestroy(ev_done);
-    if (ss) cudaStreamDestroy(ss);   // released once its work completes
+    // join even after a failure, so that nothing queued later on `s` overtakes
+    // a state pass already enqueued
+    if (ck(cudaEventRecord(ev_done, ss))) ck(cudaStreamWaitEvent(s, ev_done, 0));
     return ok ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -358,13 +380,10 @@ kda_status run_prefill(const kda_prefill_args* a, void* stream, int stages) {
     if (prep && !a->device_status && cudaMemsetAsync(p.status, 0, sizeof(int32_t), s) != cudaSuccess)
         return KDA_ERR_CUDA;
     if (prep && state_pass) {
-        // The segmented schedule creates and releases a stream per call, which
-        // a stream capture (CUDA graph) cannot record: a capturing caller gets
-        // the one-pass schedule.
-        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-        if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) return KDA_ERR_CUDA;
         const Segments sg = plan_segments(p, num_sms);
-        if (sg.on && cap == cudaStreamCaptureStatusNone) return run_segments(a, p, sg, L, num_sms, s);
+        SideSet side;
+        // without a second stream (none could be created) the call runs in one pass
+        if (sg.on && side_set(&side)) return run_segments(a, p, sg, L, num_sms, side, s);
     }
     if (prep) {
         PrepMaps pmaps;

@@ -179,31 +179,32 @@ def test_output_tensor_store_into_strided_out(kernel, seg):
     assert bool((big[..., 128:] == 7.0).all())
 
 
-def test_graph_capture_takes_one_pass():
-    """A call captured into a CUDA graph (where the segmented schedule's own
-    stream cannot be recorded) runs the one-pass schedule; replaying the graph
-    gives the bits of the uncaptured call with the same state kernel."""
+def test_segmented_call_in_a_cuda_graph():
+    """A segmented call captured into a CUDA graph (after one call outside the
+    capture created the second stream and its events) replays to the bits of
+    the uncaptured segmented call; replaying twice gives the same bits."""
     import kda_chunked_prefill_02_gb300 as K
-    inp = inputs.prefill_inputs(857, B=1, T=64 * 6, H=2)
+    inp = inputs.prefill_inputs(857, B=1, T=64 * 6 + 5, H=2)
     d = inp.to("cuda")
     ws = torch.empty(K.workspace_size(d.q, d.v), dtype=torch.uint8, device="cuda")
     out = torch.empty_like(d.v)
     fin = torch.empty_like(d.initial_state)
-    with _env(KDA_SEGMENT_CHUNKS=2, KDA_STATE_KERNEL="slab"):
+    with _env(KDA_SEGMENT_CHUNKS=2, KDA_STATE_KERNEL=None):
         s = torch.cuda.Stream()
         with torch.cuda.stream(s):
-            # warm-up outside the capture (loads the library, sets kernel attributes)
             K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, initial_state=d.initial_state, out=out,
                           final_state=fin, workspace=ws, stream=s)
         torch.cuda.synchronize()
+        ref_out, ref_fin = out.clone(), fin.clone()
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=s):
             K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, initial_state=d.initial_state, out=out,
                           final_state=fin, workspace=ws, stream=s)
-        out.zero_()
-        graph.replay()
-        torch.cuda.synchronize()
-    with _env(KDA_SEGMENT_CHUNKS=0, KDA_STATE_KERNEL="slab"):
-        ref_out, ref_fin = K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, initial_state=d.initial_state)
-        torch.cuda.synchronize()
-    assert torch.equal(out, ref_out) and torch.equal(fin, ref_fin)
+        for _ in range(2):
+            out.zero_()
+            fin.zero_()
+            graph.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(out, ref_out) and torch.equal(fin, ref_fin)
+    ro, rf = oracle_prefill(inp)
+    assert_parity(out, fin, ro, rf, "segmented call replayed from a CUDA graph")
