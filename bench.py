@@ -208,12 +208,12 @@ def run_ours(args, rank, ws, local):
     if T * H * BYTES_PREP < 256e6:
         flush = torch.empty(int(256e6) // 4, dtype=torch.float32, device=dev)
 
-    def step(stage=None):
+    def step(stage=None, on=None):
         if flush is not None:
             flush.zero_()
         K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, initial_state=d.initial_state,
                       cu_seqlens=d.cu_seqlens, out=out, final_state=fin, workspace=wsb,
-                      stream=stream, stage=stage)
+                      stream=stream if on is None else on, stage=stage)
 
     def timed(fn, k):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -244,6 +244,23 @@ def run_ours(args, rank, ws, local):
         singles.append(timed(step, 1))
     ms_single = max_over_ranks(sorted(singles)[len(singles) // 2], ws)
 
+    # the same calls replayed from a CUDA graph of 8 (as a serving loop would)
+    ms_graph = None
+    try:
+        gs = torch.cuda.Stream()
+        gs.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=gs):
+            for _ in range(8):
+                step(on=gs)
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        ms_graph = max_over_ranks(timed(graph.replay, max(2, args.steps // 8)) / 8, ws)
+        del graph
+    except RuntimeError as e:  # capture refused: report no graph number
+        print("graph capture failed: %s" % e, file=sys.stderr)
+
     # per-kernel durations (each stage alone, same stream, same workspace)
     for _ in range(2):
         step("prep")
@@ -256,6 +273,8 @@ def run_ours(args, rank, ws, local):
         ms_state -= ms_flush
         ms -= ms_flush
         ms_single -= ms_flush
+        if ms_graph is not None:
+            ms_graph -= ms_flush
 
     tokens_step = T * ws
     value = tokens_step / (ms / 1e3)
@@ -282,7 +301,7 @@ def run_ours(args, rank, ws, local):
     sched["state_kernel"] = "whole-chain" if sched.pop("whole_chain") else "slab"
     sched["kernels_per_call"] = launches
     return dict(traffic=traffic, ms=ms, value=value, clk=clk, ms_prep=ms_prep, ms_state=ms_state, dom=dom,
-                sched=sched, ms_single=ms_single,
+                sched=sched, ms_single=ms_single, ms_graph=ms_graph,
                 achieved=achieved, hbm=hbm, peak_src=peak_src, tensor_frac=tensor_frac,
                 tf_burst=tf_burst, path_gbs=path_bytes / (ms / 1e3) / 1e9, inp=inp, d=d,
                 out=out, fin=fin, wsb=wsb, stream=stream, flops=flops, dbytes=dbytes)
@@ -376,6 +395,9 @@ def main():
                          "traffic_note": "ncu DRAM bytes of the capture in profiles/, scaled by token-heads"},
             "per_call": {"ms": r["ms_single"], "tokens_per_s": inp.total_tokens * ws / (r["ms_single"] / 1e3),
                          "note": "each call alone, synchronised before and after, median of 7"},
+            "graph": None if r["ms_graph"] is None else {
+                "ms_per_call": r["ms_graph"], "tokens_per_s": inp.total_tokens * ws / (r["ms_graph"] / 1e3),
+                "note": "CUDA graph of 8 calls replayed back to back"},
             "kernels_ms": {"prep": r["ms_prep"], "state": r["ms_state"],
                            "note": "each stage alone, one pass over all tokens (prep on every SM, then the state pass)"},
             "path_gbs": r["path_gbs"],
