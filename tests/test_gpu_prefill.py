@@ -262,3 +262,31 @@ def test_state_pass_takes_longest_sequences_first():
     assert order == [2, 4, 0, 3, 5, 1]
     ro, rf = oracle_prefill(inp)
     assert_parity(out, fin, ro, rf, "longest-first order")
+
+
+@pytest.mark.parametrize("nseq", [1000, 1100])
+def test_many_sequences_order_paths(nseq):
+    """Up to 1024 sequences the chunk table ranks them longest first; beyond,
+    the state pass takes them in index order.  Both give the oracle's result."""
+    import numpy as np
+    import kda_chunked_prefill_02_gb300 as K
+    rng = np.random.default_rng(nseq)
+    lengths = [int(x) for x in rng.integers(0, 5, nseq)]
+    lengths[7] = 130                                   # one sequence of three chunks
+    inp = inputs.prefill_inputs(97, lengths=lengths, H=1)
+    d = inp.to("cuda")
+    ws = torch.full((K.workspace_size(d.q, d.v, cu_seqlens=d.cu_seqlens),), 0xFF, dtype=torch.uint8,
+                    device="cuda")
+    out, fin = K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, initial_state=d.initial_state,
+                             cu_seqlens=d.cu_seqlens, workspace=ws)
+    torch.cuda.synchronize()
+    L = K.workspace_layout(d.q, cu_seqlens=d.cu_seqlens)
+    order = ws[L.seq_order:L.seq_order + 4 * nseq].cpu().view(torch.int32).tolist()
+    if nseq <= 1024:
+        assert order[0] == 7 and sorted(order) == list(range(nseq))
+        counts = [-(-n // 64) for n in lengths]
+        assert all(counts[order[i]] >= counts[order[i + 1]] for i in range(nseq - 1))
+    else:
+        assert order == list(range(nseq))
+    ro, rf = oracle_prefill(inp)
+    assert_parity(out, fin, ro, rf, "%d sequences" % nseq)

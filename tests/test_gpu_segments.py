@@ -208,3 +208,20 @@ def test_segmented_call_in_a_cuda_graph():
             assert torch.equal(out, ref_out) and torch.equal(fin, ref_fin)
     ro, rf = oracle_prefill(inp)
     assert_parity(out, fin, ro, rf, "segmented call replayed from a CUDA graph")
+
+
+def test_segments_without_final_state():
+    """output_final_state=False: the segments still carry the state between
+    them through the workspace; the outputs are those of one pass."""
+    import kda_chunked_prefill_02_gb300 as K
+    inp = inputs.prefill_inputs(858, B=2, T=64 * 5 + 3, H=2)
+    d = inp.to("cuda")
+    with _env(KDA_SEGMENT_CHUNKS=2, KDA_STATE_KERNEL=None):
+        out_s, fin_s = K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, initial_state=d.initial_state,
+                                     output_final_state=False)
+        torch.cuda.synchronize()
+    with _env(KDA_SEGMENT_CHUNKS=0, KDA_STATE_KERNEL=None):
+        out_1, _ = K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, initial_state=d.initial_state)
+        torch.cuda.synchronize()
+    assert fin_s is None
+    assert torch.equal(out_s, out_1)
