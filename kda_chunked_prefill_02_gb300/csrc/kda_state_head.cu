@@ -14,12 +14,14 @@
 //   epilogue          S <- Diag(e^gam) S + D2   (fp32 in registers, bf16 image for P1)
 // Warp roles: all 16 warps are the epilogue, warp w owning TMEM lane quarter
 // w % 4 and the 32-column quarter w / 4, so a thread holds 32 fp32 state
-// values as in the slab kernel.  One thread of an output warp issues the MMAs
-// (an MMA issue holds its thread for tens of cycles, and the output rows are
-// off the serial chain) and the record copies: each record arrives by one 1-D
-// bulk copy into one of two stages, issued as soon as the chunk barrier has
-// shown the stage's previous chunk finished with it (P2 complete, every read
-// done), with an L2 prefetch further ahead.  Hand-offs are
+// values as in the slab kernel.  An MMA issue holds its thread for about the
+// product's duration, so P1 is issued by a thread of an output warp (every warp
+// waits for P1) and P2 by a thread of a V_new warp (those wait for P2, while
+// the output warps compute and store the output rows).  The P1 thread also
+// issues the record copies: each record arrives by one 1-D bulk copy into one
+// of two stages, issued as soon as the chunk barrier has shown the stage's
+// previous chunk finished with it (P2 complete, every read done), with an L2
+// prefetch further ahead.  Hand-offs are
 // mbarriers and named barriers; every mbarrier wait is bounded, and the chunk
 // barrier's OR-reduction of the abort flag makes all epilogue warps stop at the
 // same chunk.  Every MMA has completed, and every thread that read TMEM has
@@ -82,7 +84,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-    __shared__ uint64_t full[kHStages], p1_done, p2_done, bar_fin;
+    __shared__ uint64_t full[kHStages], p1_done, p2_done, bar_fin, bar_fin2;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
     __shared__ float s_ss[4][64];      // fused norm: partial sums of squares per column quarter
@@ -108,7 +110,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
 
     if (tid == 0) {
         for (int i = 0; i < kHStages; ++i) mbar_init(&full[i], 1);
-        mbar_init(&p1_done, 1); mbar_init(&p2_done, 1); mbar_init(&bar_fin, 1);
+        mbar_init(&p1_done, 1); mbar_init(&p2_done, 1); mbar_init(&bar_fin, 1); mbar_init(&bar_fin2, 1);
         abort_flag = 0;
         fence_mbar_init();
     }
@@ -134,7 +136,11 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
         const int qd = warp & 3, cq = warp >> 2;
         const int row = 32 * qd + lane;
         const uint32_t lane_base = (uint32_t)(32 * qd) << 16;
-        const bool issuer = (warp == 2 && lane == 0);  // warp 2: an output warp
+        // P1 and the copies: a thread of an output warp; P2: a thread of a V_new
+        // warp, which waits for P2 anyway, so that the output warps' work is not
+        // held up behind the P2 issue.
+        const bool issuer = (warp == 2 && lane == 0);
+        const bool issuer2 = (warp == 0 && lane == 0);
         const uint32_t id = idesc_bf16_f32_bmn(128, 128);
         const uint32_t sS_addr = smem_u32(sm + OH_S), sVn_addr = smem_u32(sm + OH_VN);
         float S[kSlab];
@@ -216,22 +222,18 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
                     fence_proxy_async_smem();
                 }
                 tc_fence_before();
-                named_bar_sync(kBarHVn, 288);  // the eight V_new warps and the issuer's warp
-            } else {
-                if (warp == 2) {
-                    tc_fence_before();
-                    named_bar_sync(kBarHVn, 288);
-                    if (issuer && ok && !*abort) {
-                        tc_fence_after();
-                        const uint64_t kt = sdesc_kmajor_sw128(sb_addr + SH_KT);
-                        const uint64_t bv = sdesc_mnmajor_sw128(sVn_addr, 1024u, kHSbo);
+                named_bar_sync(kBarHVn, 256);  // the eight V_new warps
+                if (issuer2 && ok && !*abort) {
+                    tc_fence_after();
+                    const uint64_t kt = sdesc_kmajor_sw128(sb_addr + SH_KT);
+                    const uint64_t bv = sdesc_mnmajor_sw128(sVn_addr, 1024u, kHSbo);
 #pragma unroll
-                        for (uint32_t k = 0; k < 4; ++k)  // K = 64 tokens
-                            umma_bf16(tb + TMH_D2, kt + k * 2, bv + k * ((2 * kHSbo) >> 4), id, k > 0 ? 1u : 0u);
-                        umma_commit(&p2_done);
-                    }
-                    __syncwarp();
+                    for (uint32_t k = 0; k < 4; ++k)  // K = 64 tokens
+                        umma_bf16(tb + TMH_D2, kt + k * 2, bv + k * ((2 * kHSbo) >> 4), id, k > 0 ? 1u : 0u);
+                    umma_commit(&p2_done);
                 }
+                __syncwarp();
+            } else {
                 // O = O_loc + Q' S for token row `row - 64`
                 const int i = row - 64, t0 = 64 * c;
                 const bool valid_row = t0 + i < seq_len;
@@ -347,6 +349,10 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
             // every product issued has completed before TMEM is released
             umma_commit(&bar_fin);
             mbar_wait(&bar_fin, 0, nullptr);
+        }
+        if (issuer2 && count > 0) {
+            umma_commit(&bar_fin2);
+            mbar_wait(&bar_fin2, 0, nullptr);
         }
         if (!*abort && p.hT) {
             float4* dst = reinterpret_cast<float4*>(p.hT + st_off);
