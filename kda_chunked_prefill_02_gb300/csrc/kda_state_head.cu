@@ -17,11 +17,12 @@
 // values as in the slab kernel.  An MMA issue holds its thread for about the
 // product's duration, so P1 is issued by a thread of an output warp (every warp
 // waits for P1) and P2 by a thread of a V_new warp (those wait for P2, while
-// the output warps compute and store the output rows).  The P1 thread also
-// issues the record copies: each record arrives by one 1-D bulk copy into one
-// of two stages, issued as soon as the chunk barrier has shown the stage's
-// previous chunk finished with it (P2 complete, every read done), with an L2
-// prefetch further ahead.  Hand-offs are
+// the output warps compute and store the output rows).  A thread of another
+// output warp issues the output tensor stores and the record copies: each
+// record arrives by one 1-D bulk copy into one of two stages, issued as soon as
+// the chunk barrier has shown the stage's previous chunk finished with it (P2
+// complete, every read done, the stores' reads of the staged rows done), with
+// an L2 prefetch further ahead.  Hand-offs are
 // mbarriers and named barriers; every mbarrier wait is bounded, and the chunk
 // barrier's OR-reduction of the abort flag makes all epilogue warps stop at the
 // same chunk.  Every MMA has completed, and every thread that read TMEM has
@@ -141,6 +142,10 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
         // held up behind the P2 issue.
         const bool issuer = (warp == 2 && lane == 0);
         const bool issuer2 = (warp == 0 && lane == 0);
+        // The output tensor stores and the record copies: a thread of another
+        // output warp, so that the P1 thread goes from the chunk barrier straight
+        // to the next P1.
+        const bool storer = (warp == 3 && lane == 0);
         const uint32_t id = idesc_bf16_f32_bmn(128, 128);
         const uint32_t sS_addr = smem_u32(sm + OH_S), sVn_addr = smem_u32(sm + OH_VN);
         float S[kSlab];
@@ -163,8 +168,8 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
             bulk_load(sm + st * kHStage, rec_ptr(c), kRecBytes, &full[st]);
             if (c + kHPrefetchAhead < count) bulk_prefetch_l2(rec_ptr(c + kHPrefetchAhead), kRecBytes);
         };
-        int issued = 0;  // records requested so far (issuer thread)
-        if (issuer)
+        int issued = 0;  // records requested so far (storer thread)
+        if (storer)
             for (; issued < kHStages && issued < count; ++issued) issue_load(issued);
         store_quarter(sm + OH_S, row, cq, S);
         fence_proxy_async_smem();
@@ -298,7 +303,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
                                        pack_bf16x2(o[8 * x + 4], o[8 * x + 5]), pack_bf16x2(o[8 * x + 6], o[8 * x + 7]));
                     fence_proxy_async_smem();
                     named_bar_sync(kBarHOut, 256);  // the eight output warps
-                    if (issuer && ok && !*abort) {
+                    if (storer && ok && !*abort) {
                         const int tok = (int)(p.cu == nullptr ? t0 : (int64_t)tbase + t0);
 #pragma unroll
                         for (int sl = 0; sl < kHeadDim / kSlab; ++sl)
@@ -333,14 +338,14 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
             if (named_bar_or(kBarHChunk, 512, *abort != 0)) break;
             done = c + 1;
             // stage st is free: P2 of chunk c completed, every read of it is done
-            // and (issuer) the output tensor stores have read their slabs
+            // and (storer) the output tensor stores have read their slabs
             stall_point<kStall>(p.stall_seed, 5, c);
-            if (issuer && issued < count) {
+            if (storer && issued < count) {
                 bulk_wait_read();
                 issue_load(issued++);
             }
         }
-        if (issuer) {
+        if (storer) {
             bulk_wait_all();  // the output tensor stores are complete
             // Never leave with a copy in flight (bounded; normally complete).
             for (int c = done; c < issued; ++c) mbar_wait(&full[c % kHStages], (c / kHStages) & 1, nullptr);
