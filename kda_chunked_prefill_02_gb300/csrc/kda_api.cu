@@ -201,9 +201,9 @@ bool whole_chain_kernel(const PrefillParams& p, int num_sms) {
 // per-unit costs measured on GB300 (SM clock 2070 MHz, long workload): one
 // (chunk, head) record takes a prep CTA 8.7 us on a full GPU and 8.25 us on the
 // SMs beside a state pass; a chunk step takes 1.05 us in the slab kernel (four
-// CTAs per chain) and 2.15 us in the whole-chain kernel, 2 % more beside prep;
-// every segment adds about 12 us to each stream (launch, start-up, the slowest
-// CTA's tail).  Fitted to a sweep of segment lengths 30..160 within 2 %.
+// CTAs per chain) and 1.90 us in the whole-chain kernel, 12 % more beside prep;
+// every segment adds about 5 us to each stream (launch, start-up, the slowest
+// CTA's tail).  Fitted to a sweep of segment lengths 60..240 within 1 %.
 struct Segments {
     bool on = false;
     bool head = false;       // whole-chain state kernel (else slab)
@@ -211,8 +211,8 @@ struct Segments {
     int prep_ctas = 0;       // prep grid while a state pass runs beside it
 };
 
-constexpr double kRecUs = 8.7, kSlabStepUs = 1.05, kHeadStepUs = 2.15;
-constexpr double kPrepBeside = 0.95, kStateBeside = 1.02, kSegmentUs = 12.0;
+constexpr double kRecUs = 8.7, kSlabStepUs = 1.05, kHeadStepUs = 1.90;
+constexpr double kPrepBeside = 0.95, kStateBeside = 1.12, kSegmentUs = 5.0;
 
 // Estimated time of the segmented schedule: prep of segment i ends at P_i =
 // P_{i-1} + a_i; its state pass starts when both P_i and the previous state pass

@@ -165,8 +165,8 @@ def test_prefill_schedule(K, monkeypatch):
     monkeypatch.delenv("KDA_SEGMENT_CHUNKS", raising=False)
     monkeypatch.delenv("KDA_STATE_KERNEL", raising=False)
     # 32 chains of 2048 chunks: whole-chain state CTAs on 32 SMs, prep on 120,
-    # 120-chunk segments (32 prep rounds of 120 CTAs)
-    assert _sched(K, batch=1, num_seqs=1, seqlen=131072, num_heads=32) == (1, 1, 120, 120)
+    # 56-chunk segments
+    assert _sched(K, batch=1, num_seqs=1, seqlen=131072, num_heads=32) == (1, 1, 56, 120)
     # 8 chains: slab state CTAs (4 per chain) on 32 SMs, prep on 120
     s8 = _sched(K, batch=1, num_seqs=1, seqlen=131072, num_heads=8)
     assert s8[:2] == (1, 0) and s8[3] == 120 and s8[2] % 8 == 0
