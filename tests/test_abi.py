@@ -175,7 +175,9 @@ def test_prefill_schedule(K, monkeypatch):
     assert _sched(K, batch=4, num_seqs=4, seqlen=4096, num_heads=16) == (1, 1, 48, 88)
     # short sequences and varlen: one pass
     assert _sched(K, batch=1, num_seqs=1, seqlen=256, num_heads=2) == (0, 0, 0, 152)
-    assert _sched(K, batch=1, num_seqs=1, seqlen=16384, num_heads=32)[0] == 0
+    assert _sched(K, batch=1, num_seqs=1, seqlen=4096, num_heads=32)[0] == 0
+    # 16384 tokens of 32 heads: segmented (measured 0.69 ms against 0.75 one pass)
+    assert _sched(K, batch=1, num_seqs=1, seqlen=16384, num_heads=32)[:2] == (1, 1)
     assert _sched(K, cu_seqlens=ctypes.c_void_p(1 << 12), num_seqs=8, seqlen=32768,
                   num_heads=32) == (0, 1, 0, 152)
     # two chains: the slab pass (2048 steps) dominates and prep is short, so
