@@ -384,14 +384,11 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         ok = __syncthreads_and(tid == 0 ? mbar_wait(&bar_mma[0], it & 1, nullptr) : true);
         tc_fence_after();
         if (!ok) break;
-        // Once the Kt image has been read out of the consumed gate tile, the input
-        // tiles are free: the next record's load while this one goes through the
-        // solve and the other two products.
-        if (tid == 0 && cn.len > 0) {
-            bulk_wait_read();
-            load_inputs(sm, maps, cn, rec_next % p.H, &bar_in);
-        }
-        if (cn.len > 0) pend_parity = (int)((it + 1) & 1);
+        // Once the Kt image has been read out of the consumed gate tile (this
+        // thread's bulk store), the input tiles are free: the next record's load
+        // is issued by an idle warp during the 16 -> 32 products and lands while
+        // this record goes through the solve and the other two products.
+        if (tid == 0 && cn.len > 0) bulk_wait_read();
 
         stall_point<kStall>(p.stall_seed, 5, it);
         float* sA = reinterpret_cast<float*>(sm + O_A);
@@ -510,8 +507,11 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             store_tile_tf32(sT + (pb + 16) * kPA + pb + c0, kPA, d, lane);
             store_tprime_pair(sm, pb + 16 + g4, pb + c0 + 2 * t4, d[0], d[1], sBeta);
             store_tprime_pair(sm, pb + 24 + g4, pb + c0 + 2 * t4, d[2], d[3], sBeta);
+        } else if (warp == 4 && lane == 0 && cn.len > 0) {
+            load_inputs(sm, maps, cn, rec_next % p.H, &bar_in);
         }
         __syncthreads();
+        if (cn.len > 0) pend_parity = (int)((it + 1) & 1);
         if (warp < 8) {
             // 32 -> 64, row tile rt (16 rows), columns c0..c0+7:
             // X = A[32:, :32] T[:32, :32] (k >= c0), then T[32:, :32] = -T[32:, 32:] X
