@@ -63,3 +63,30 @@ def test_host_call_refuses_small_staging():
     with pytest.raises(K.KdaError) as e:
         K.kda_prefill_host(hq, hk, hv, hg, hb, staging=small)
     assert e.value.status == 1
+
+
+@pytest.mark.parametrize("piece", [16384, 8192])
+def test_host_pieces_take_the_segmented_schedule(piece):
+    """Pieces long enough for the segmented schedule (32 chains): the device
+    call and the host-buffer call run the whole-chain state kernel, the state
+    passing between segments and between pieces exactly, so both give the same
+    bits; two heads are checked against the oracle."""
+    import os
+    from kda_test_util import head_subset
+    import kda_chunked_prefill_02_gb300 as K
+    inp = inputs.prefill_inputs(403, B=1, T=16384, H=32)
+    old = os.environ.get("KDA_STATE_KERNEL")
+    os.environ["KDA_STATE_KERNEL"] = "head"
+    try:
+        assert K.prefill_schedule(inp.q[:, :piece], num_sms=152)["segmented"]
+        ref_out, ref_fin, out, fin = _both(inp, piece)
+    finally:
+        if old is None:
+            del os.environ["KDA_STATE_KERNEL"]
+        else:
+            os.environ["KDA_STATE_KERNEL"] = old
+    assert torch.equal(out, ref_out)
+    assert torch.equal(fin, ref_fin)
+    sub = head_subset(inp, [0, 31])
+    ro, rf = oracle_prefill(sub)
+    assert_parity(out[:, :, [0, 31]], fin[:, [0, 31]], ro, rf, "segmented host pieces")
