@@ -67,10 +67,11 @@ def test_host_call_refuses_small_staging():
 
 @pytest.mark.parametrize("piece", [16384, 8192])
 def test_host_pieces_take_the_segmented_schedule(piece):
-    """Pieces long enough for the segmented schedule (32 chains): the device
-    call and the host-buffer call run the whole-chain state kernel, the state
-    passing between segments and between pieces exactly, so both give the same
-    bits; two heads are checked against the oracle."""
+    """Long pieces of 32 chains: the device call takes the segmented schedule,
+    the host-buffer call's pieces the segmented (16384 tokens) or the one-pass
+    (8192) schedule, all with the whole-chain state kernel, the state passing
+    between segments and between pieces exactly, so both give the same bits;
+    two heads are checked against the oracle."""
     import os
     from kda_test_util import head_subset
     import kda_chunked_prefill_02_gb300 as K
@@ -78,7 +79,7 @@ def test_host_pieces_take_the_segmented_schedule(piece):
     old = os.environ.get("KDA_STATE_KERNEL")
     os.environ["KDA_STATE_KERNEL"] = "head"
     try:
-        assert K.prefill_schedule(inp.q[:, :piece], num_sms=152)["segmented"]
+        assert K.prefill_schedule(inp.q, num_sms=152)["segmented"]
         ref_out, ref_fin, out, fin = _both(inp, piece)
     finally:
         if old is None:
