@@ -19,7 +19,8 @@
  * Conventions shared by every call.
  *  - All tensor pointers are DEVICE pointers owned by the caller.  The library
  *    allocates no device or pinned memory and caches none; scratch memory is
- *    the caller's `workspace`.
+ *    the caller's `workspace`.  (It keeps one CUDA stream and two events per
+ *    host thread and device for segmented prefill calls, see kda_prefill.)
  *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL
  *    = the legacy default stream).  Argument errors found on the host come
  *    back synchronously and launch nothing.
@@ -148,7 +149,8 @@ size_t kda_prefill_workspace_size(const kda_prefill_args* args);
  *      (I + Diag(beta) tril(K K^T . decay))^{-1}, W, U and the intra-chunk
  *      attention folded into Q' = Q e^Gam - Aqk W and O_loc = Aqk U;
  *   A6-A7 the serial inter-chunk state pass on tcgen05 tensor cores, per
- *      (sequence, head, value slab), with the output epilogue.
+ *      (sequence, head) chain in four 32-column slab CTAs or one whole-chain
+ *      CTA, with the output epilogue (rows stored by TMA tensor stores).
  * Padded calls with few, long chains are run in token segments: the state
  * pass of segment s (on a second stream, joined back into `stream` before
  * the call's work ends) overlaps the prep of segment s+1, the state of every
