@@ -290,3 +290,19 @@ def test_many_sequences_order_paths(nseq):
         assert order == list(range(nseq))
     ro, rf = oracle_prefill(inp)
     assert_parity(out, fin, ro, rf, "%d sequences" % nseq)
+
+
+def test_empty_batch_launches_nothing():
+    """B = 0 sequences: nothing to compute, the call succeeds with empty outputs
+    (no grid of zero CTAs is launched); the same through the split stages."""
+    import kda_chunked_prefill_02_gb300 as K
+    inp = inputs.prefill_inputs(703, B=1, T=100, H=2)
+    d = inp.to("cuda")
+    q, k, v, g, b = (t[:0] for t in (d.q, d.k, d.v, d.g, d.beta))
+    out, fin = K.kda_prefill(q, k, v, g, b)
+    torch.cuda.synchronize()
+    assert out.shape == (0, 100, 2, 128) and fin.shape == (0, 2, 128, 128)
+    ws = torch.empty(K.workspace_size(q, v), dtype=torch.uint8, device="cuda")
+    for stage in ("prep", "state"):
+        K.kda_prefill(q, k, v, g, b, workspace=ws, stage=stage)
+    torch.cuda.synchronize()

@@ -122,3 +122,15 @@ def test_verify_replay_only_commits_the_accepted_drafts(bf16):
     assert torch.equal(pool_a, pool_b)
     _, st_ref = oracle.verify(vi.q, vi.k, vi.v, vi.g, vi.beta, vi.state_pool, vi.accepted)
     assert rel_fro(to_np(pool_b[:vi.q.shape[0]]), st_ref) <= (1e-2 if bf16 else 1e-4)
+
+
+def test_verify_no_requests():
+    """R = 0 requests: the call succeeds, writes nothing and leaves the pool."""
+    import kda_chunked_prefill_02_gb300 as K
+    vi = inputs.verify_inputs(41, R=3, D=4, H=2)
+    d = vi.to("cuda")
+    pool = d.state_pool.clone()
+    out = K.kda_verify(d.q[:0], d.k[:0], d.v[:0], d.g[:0], d.beta[:0], pool, d.accepted[:0])
+    torch.cuda.synchronize()
+    assert out.shape == (0, 4, 2, 128)
+    assert torch.equal(pool.cpu(), vi.state_pool)
