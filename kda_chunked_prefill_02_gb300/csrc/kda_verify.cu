@@ -15,8 +15,9 @@
 // column group cg = 4*warp + lane / 8) owns the 16 x 4 block of the state at
 // key rows 16*rg.., value columns 4*cg..: each staged key-channel value serves
 // four columns, and the reductions over key channels (S^T k, S^T q) are 16
-// in-thread FMAs per column plus three shuffle levels over the row groups of
-// the warp.  Shared-memory layouts keep every access conflict-free: the
+// in-thread FMAs per column plus a shuffle reduce-scatter over the row groups
+// of the warp (each lane ends with one column's sum; u goes back to all four
+// by a gather).  Shared-memory layouts keep every access conflict-free: the
 // state's 16-byte chunks are XOR-swizzled by row group, and the staged q, k
 // and e^g rows carry 16 bytes of padding per row group.
 #include "kda_internal.h"
@@ -52,6 +53,37 @@ __device__ __forceinline__ float2 bf16x2f(uint32_t w) {
     return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
+// Column sums over the eight row groups of a warp (lanes rg = 0..7 of one
+// column group): a[c] holds this lane's partial sum for column c of its four.
+// Reduce-scatter in three shuffle levels (4, 2, 1): the lanes keep half of the
+// columns at each level, so lane rg ends with the full sum of column
+// ccol(rg) = 2*bit2 + bit1 (4 shuffles instead of the 12 of an all-reduce).  The
+// two lanes of a pair (rg, rg^1) add the same two terms, so they hold equal sums.
+__device__ __forceinline__ int ccol(int rg) { return (rg >> 1) & 3; }
+__device__ __forceinline__ float sum_scatter(const float a[4], int rg) {
+    const bool h2 = (rg & 4) != 0, h1 = (rg & 2) != 0;
+    const float s0 = __shfl_xor_sync(0xffffffffu, h2 ? a[0] : a[2], 4);
+    const float s1 = __shfl_xor_sync(0xffffffffu, h2 ? a[1] : a[3], 4);
+    const float c0 = (h2 ? a[2] : a[0]) + s0;  // column 2*h2
+    const float c1 = (h2 ? a[3] : a[1]) + s1;  // column 2*h2 + 1
+    const float s = __shfl_xor_sync(0xffffffffu, h1 ? c0 : c1, 2);
+    float d = (h1 ? c1 : c0) + s;              // column 2*h2 + h1
+    d += __shfl_xor_sync(0xffffffffu, d, 1);
+    return d;
+}
+// Inverse of the scatter: lane rg holds x for column ccol(rg); every lane of the
+// row-group octet gets all four columns (3 shuffles).
+__device__ __forceinline__ void gather4(float x, int rg, float u[4]) {
+    const bool h2 = (rg & 4) != 0, h1 = (rg & 2) != 0;
+    const float y = __shfl_xor_sync(0xffffffffu, x, 2);
+    const float lo = h1 ? y : x, hi = h1 ? x : y;  // columns 2*h2, 2*h2 + 1
+    const float lo2 = __shfl_xor_sync(0xffffffffu, lo, 4), hi2 = __shfl_xor_sync(0xffffffffu, hi, 4);
+    u[0] = h2 ? lo2 : lo;
+    u[1] = h2 ? hi2 : hi;
+    u[2] = h2 ? lo : lo2;
+    u[3] = h2 ? hi : hi2;
+}
+
 struct Item {
     int r, h, slot, acc;
     bool valid;
@@ -66,7 +98,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyP
     __shared__ float s_beta[kMaxDrafts];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int rg = lane & 7, cg = 4 * warp + (lane >> 3);
-    const int row0 = 16 * rg, col0 = 4 * cg;
+    const int row0 = 16 * rg, col0 = 4 * cg, cc = ccol(rg);
     const int nitems = p.R * p.H, D = p.D;
     if ((int)blockIdx.x >= nitems) return;
     uint8_t* sst = smv;
@@ -187,17 +219,12 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyP
                         S[i][c] *= x[i];
                         sk[c] = fmaf(S[i][c], kk[i], sk[c]);
                     }
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    sk[c] += __shfl_xor_sync(0xffffffffu, sk[c], 1);
-                    sk[c] += __shfl_xor_sync(0xffffffffu, sk[c], 2);
-                    sk[c] += __shfl_xor_sync(0xffffffffu, sk[c], 4);
-                }
-                const uint2 vw = *reinterpret_cast<const uint2*>(row + TO_V + 2 * col0);
-                const float2 v01 = bf16x2f(vw.x), v23 = bf16x2f(vw.y);
-                const float bt = s_beta[t];
-                const float u[4] = {bt * (v01.x - sk[0]), bt * (v01.y - sk[1]), bt * (v23.x - sk[2]),
-                                    bt * (v23.y - sk[3])};
+                // u for this lane's column of the four, then all four to every lane
+                const float skc = sum_scatter(sk, rg);
+                const float vc = __uint_as_float(
+                    (uint32_t)*reinterpret_cast<const uint16_t*>(row + TO_V + 2 * (col0 + cc)) << 16);
+                float u[4];
+                gather4(s_beta[t] * (vc - skc), rg, u);
                 {
                     const uint4 q0 = *reinterpret_cast<const uint4*>(row + TO_Q + 48 * rg);
                     const uint4 q1 = *reinterpret_cast<const uint4*>(row + TO_Q + 48 * rg + 16);
@@ -205,7 +232,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyP
 #pragma unroll
                     for (int w = 0; w < 8; ++w) {
                         const float2 f = bf16x2f(qw[w]);
-                        x[2 * w] = f.x * p.scale; x[2 * w + 1] = f.y * p.scale;
+                        x[2 * w] = f.x; x[2 * w + 1] = f.y;
                     }
                 }
                 float o[4] = {0.f, 0.f, 0.f, 0.f};
@@ -216,16 +243,10 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyP
                         S[i][c] = fmaf(kk[i], u[c], S[i][c]);
                         o[c] = fmaf(S[i][c], x[i], o[c]);
                     }
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    o[c] += __shfl_xor_sync(0xffffffffu, o[c], 1);
-                    o[c] += __shfl_xor_sync(0xffffffffu, o[c], 2);
-                    o[c] += __shfl_xor_sync(0xffffffffu, o[c], 4);
-                }
-                if (rg < 4 && !p.replay_only) {
-                    const float oc = rg == 0 ? o[0] : rg == 1 ? o[1] : rg == 2 ? o[2] : o[3];
-                    p.out[cur.r * p.os[0] + t * p.os[1] + cur.h * p.os[2] + col0 + rg] = __float2bfloat16_rn(oc);
-                }
+                const float oc = sum_scatter(o, rg);
+                if (!(rg & 1) && !p.replay_only)
+                    p.out[cur.r * p.os[0] + t * p.os[1] + cur.h * p.os[2] + col0 + cc] =
+                        __float2bfloat16_rn(oc * p.scale);
                 if (t + 1 == cur.acc) {
                     stall_point<kStall>(p.stall_seed, 4, k);
 #pragma unroll
