@@ -122,11 +122,18 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyP
     // Item x's state block into sst and its draft rows into tb (cp.async, one group).
     auto prefetch = [&](const Item& x, uint8_t* tb) {
         if (x.valid) {
-            const uint8_t* st = state_of(x);
-            constexpr int kChunksPerRow = kBf16 ? 16 : 32;
-            for (int e = tid; e < kHeadDim * kChunksPerRow; e += kVerifyThreads) {
-                const int r = e / kChunksPerRow, c = e % kChunksPerRow;
-                cp_async16(sst + state_chunk<kBf16>(r, c), st + (r * kChunksPerRow + c) * 16);
+            // Thread tid copies the block's 16-byte chunks tid + 256 j: row r0 + kRows j,
+            // chunk c of the row.  r0 < kRows, so the row group (r >> 4) of pass j is
+            // j >> 1 (fp32 rows: 8 rows a pass) or j (bf16: 16 rows a pass), a
+            // constant of the unrolled pass.
+            constexpr int kChunksPerRow = kBf16 ? 16 : 32, kRows = kVerifyThreads / kChunksPerRow;
+            const uint8_t* st = state_of(x) + tid * 16;
+            const int r0 = tid / kChunksPerRow, c = tid % kChunksPerRow;
+            uint8_t* dst = sst + state_chunk<kBf16>(r0, 0);
+#pragma unroll
+            for (int j = 0; j < kHeadDim / kRows; ++j) {
+                const int rgrp = (kBf16 ? j : j >> 1) & 7;
+                cp_async16(dst + j * kRows * kChunksPerRow * 16 + ((c ^ rgrp) << 4), st + j * 4096);
             }
             for (int e = tid; e < D * 80; e += kVerifyThreads) {
                 const int t = e / 80, j = e - t * 80;
