@@ -34,21 +34,24 @@ from . import build as _build
 _lib = None
 
 
+def _bind(lib):
+    """Declare the C entry points' signatures on a loaded oracle library."""
+    d = ctypes.POINTER(ctypes.c_double)
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    i64 = ctypes.c_int64
+    lib.kda_oracle_prefill.restype = ctypes.c_int
+    lib.kda_oracle_prefill.argtypes = [i64, i64p, i64, i64, i64, d, d, d, d, d,
+                                       ctypes.c_int, ctypes.c_double, d, d, d]
+    lib.kda_oracle_verify.restype = ctypes.c_int
+    lib.kda_oracle_verify.argtypes = [i64, i64, i64, i64, i64, d, d, d, d, d,
+                                      ctypes.c_int, ctypes.c_double, d, i64p, i64p, d, d]
+    return lib
+
+
 def _load():
     global _lib
     if _lib is None:
-        path = _build.build()
-        lib = ctypes.CDLL(path)
-        d = ctypes.POINTER(ctypes.c_double)
-        i64p = ctypes.POINTER(ctypes.c_int64)
-        i64 = ctypes.c_int64
-        lib.kda_oracle_prefill.restype = ctypes.c_int
-        lib.kda_oracle_prefill.argtypes = [i64, i64p, i64, i64, i64, d, d, d, d, d,
-                                           ctypes.c_int, ctypes.c_double, d, d, d]
-        lib.kda_oracle_verify.restype = ctypes.c_int
-        lib.kda_oracle_verify.argtypes = [i64, i64, i64, i64, i64, d, d, d, d, d,
-                                          ctypes.c_int, ctypes.c_double, d, i64p, i64p, d, d]
-        _lib = lib
+        _lib = _bind(ctypes.CDLL(_build.build()))
     return _lib
 
 
