@@ -2,7 +2,7 @@
 """KDA prefill throughput on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--config long|varlen|padded|tiny]
+                    [--config long|varlen|padded|tiny|verify] [--pool fp32|bf16]
 
 One step = one kda_prefill call (chunk prep + serial state pass, the whole hot
 path) over the workload, inputs resident in HBM.  The default workload is the
@@ -15,6 +15,11 @@ scaling is weak and value = tokens processed by all ranks / max-over-ranks time.
 --impl reference times the fp64 CPU oracle (sequential recurrence, OpenMP over
 chains) on the host cores, on a bounded sample of the same workload per step;
 it is a deliberately slow reference, not a target.
+
+--config verify times MTP verify instead: one step = one kda_verify call over
+256 requests x 4 draft tokens x 32 heads against a device-resident state pool
+(fp32, or bf16 with --pool bf16; 537 / 268 MB, larger than L2), the accepted
+prefix's state written back in place.  Its line reports draft tokens/s.
 """
 import argparse
 import hashlib
@@ -45,7 +50,9 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", choices=["long", "varlen", "padded", "tiny"], default="long")
+    ap.add_argument("--config", choices=["long", "varlen", "padded", "tiny", "verify"], default="long")
+    ap.add_argument("--pool", choices=["fp32", "bf16"], default="fp32",
+                    help="state pool element type of --config verify")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -373,6 +380,8 @@ def cpu_baseline(inp, target_s=15.0):
 
 def main():
     args = parse()
+    if args.config == "verify":
+        return main_verify(args)
     if args.impl == "reference":
         return main_reference(args)
     import torch
@@ -443,6 +452,185 @@ def main_reference(args):
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+# ---- MTP verify (--config verify)
+
+VERIFY_METRIC = "KDA MTP verify draft tokens/s (R=256 requests x D=4 drafts, H=32, dk=dv=128), 1×GB300"
+
+
+def _timed(fn, k, stream, ws):
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(k):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    return e0.elapsed_time(e1) / k
+
+
+def verify_workload(pool):
+    import torch
+    vi = workload("verify")
+    if pool == "bf16":
+        vi.state_pool = vi.state_pool.to(torch.bfloat16)
+    return vi
+
+
+def verify_bytes(vi):
+    """Algorithmic bytes of one verify call: every request's state block read,
+    the blocks of requests with accepted > 0 written back, the draft rows (q, k,
+    v bf16, g fp32, beta) read and the bf16 outputs written."""
+    R, D, H = vi.q.shape[:3]
+    blk = 128 * 128 * vi.state_pool.element_size()
+    written = int((vi.accepted > 0).sum())
+    return R * H * blk + written * H * blk + R * D * H * (3 * 256 + 512 + 4 + 256)
+
+
+def verify_config(vi, pool):
+    from kda_chunked_prefill_02_gb300 import inputs
+    R, D, H = vi.q.shape[:3]
+    return {"workload": "verify", "description": inputs.CONFIG_DESCRIPTIONS["verify"],
+            "requests": R, "drafts": D, "heads": H, "head_dim": 128, "pool": pool,
+            "pool_bytes": vi.state_pool.numel() * vi.state_pool.element_size(),
+            "l2": "state pool larger than L2 (no flush)"}
+
+
+def oracle_verify_sample(vi, m):
+    """The fp64 oracle's verify on the first m requests (all drafts and heads).
+    Returns (draft tokens, seconds, threads)."""
+    import oracle
+    if vi.slot is None:
+        pool, slot = vi.state_pool[:m], None
+    else:
+        pool, slot = vi.state_pool, vi.slot[:m]
+    t0 = time.perf_counter()
+    _, _, used = oracle.verify(vi.q[:m], vi.k[:m], vi.v[:m], vi.g[:m], vi.beta[:m], pool,
+                               vi.accepted[:m], slot=slot, return_threads=True)
+    return m * vi.q.shape[1], time.perf_counter() - t0, used
+
+
+def verify_sample_size(vi, target_s):
+    """Requests per oracle run so that one run takes about target_s seconds
+    (at least 16, at most the whole workload)."""
+    R = vi.q.shape[0]
+    _, sec, _ = oracle_verify_sample(vi, 16)
+    return int(max(16, min(R, 16 * target_s / max(sec, 1e-3))))
+
+
+def main_verify(args):
+    rank = int(os.environ.get("RANK", "0"))
+    vi = verify_workload(args.pool)
+    R, D, H = vi.q.shape[:3]
+    if args.impl == "reference":
+        ws = int(os.environ.get("WORLD_SIZE", "1"))
+        if rank != 0:
+            return
+        for _ in range(args.warmup):
+            oracle_verify_sample(vi, 8)
+        m = verify_sample_size(vi, 1.0)
+        times, tok, used = [], 0, 1
+        for _ in range(args.steps):
+            tok, sec, used = oracle_verify_sample(vi, m)
+            times.append(sec)
+        sec = statistics.median(times)
+        value = tok / sec
+        line = {"impl": "reference", "metric": VERIFY_METRIC, "value": value, "unit": "draft tokens/s",
+                "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic, seeded", "config": verify_config(vi, args.pool),
+                "cpu_baseline": {"value": value, "unit": "draft tokens/s", "cores": used, "kind": "oracle",
+                                 "sample": "the first %d of %d requests (all drafts and heads) per step"
+                                           % (m, R)},
+                "e2e": {"value": value, "unit": "draft tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    import torch
+
+    import kda_chunked_prefill_02_gb300 as K
+    rank, ws, local = dist_init(args.gpus)
+    hbm, _, _, peak_src = peaks()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    d = vi.to(dev)
+    out = torch.empty(d.v.shape, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        K.kda_verify(d.q, d.k, d.v, d.g, d.beta, d.state_pool, d.accepted, slot=d.slot, out=out,
+                     stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    ms = max_over_ranks(_timed(step, args.steps, stream, ws), ws)
+    clk = clocks.stop()
+
+    # end to end: each step copies its draft rows and accepted counts in from
+    # page-locked host memory and the outputs back; the pool stays on the device
+    ins_h = [t.pin_memory() for t in (vi.q, vi.k, vi.v, vi.g, vi.beta, vi.accepted)]
+    ins_d = [d.q, d.k, d.v, d.g, d.beta, d.accepted]
+    out_h = torch.empty(tuple(out.shape), dtype=torch.bfloat16, pin_memory=True)
+
+    def e2e_step():
+        for src, dst in zip(ins_h, ins_d):
+            dst.copy_(src, non_blocking=True)
+        step()
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    ms_e2e = max_over_ranks(_timed(e2e_step, args.steps, stream, ws), ws)
+    e2e = {"value": R * D * ws / (ms_e2e / 1e3), "unit": "draft tokens/s", "ms_per_step": ms_e2e,
+           "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in ins_h),
+           "d2h_bytes_per_step": out_h.numel() * out_h.element_size(),
+           "api": "kda_verify (C ABI) with the step's inputs copied from page-locked host memory "
+                  "and the outputs copied back; the state pool stays on the device"}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        m = verify_sample_size(vi, 2.0)
+        tok, sec, used = oracle_verify_sample(vi, m)
+        reps = int(max(1, min(20, 10.0 / max(sec, 1e-3))))
+        for _ in range(reps - 1):
+            t_, s_, used = oracle_verify_sample(vi, m)
+            tok, sec = tok + t_, sec + s_
+        cpu = {"value": tok / sec, "unit": "draft tokens/s", "cores": used, "kind": "oracle",
+               "sample": "the first %d of %d requests (x %d drafts x %d heads), %d runs, fp64, %.1f s"
+                         % (m, R, D, H, reps, sec),
+               "host_cores_available": len(os.sched_getaffinity(0))}
+    if rank == 0:
+        nbytes = verify_bytes(vi)
+        achieved = nbytes / (ms / 1e3) / 1e9
+        line = {
+            "metric": VERIFY_METRIC, "value": R * D * ws / (ms / 1e3), "unit": "draft tokens/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16 q/k/v/out, fp32 gate/beta, %s state pool, fp32 arithmetic" % args.pool,
+            "data": "synthetic, seeded (q,k L2-normalised, g=-5*sigmoid(N(0,1)), beta logits N(0,1), "
+                    "accepted U{0..4})",
+            "config": dict(verify_config(vi, args.pool),
+                           parallelism="replica per GPU" if ws > 1 else "1 GPU"),
+            "requests_per_s": R * ws / (ms / 1e3),
+            "roofline": {"bound": "hbm", "kernel": "verify", "achieved": achieved, "peak": hbm,
+                         "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                         "peak_source": peak_src, "algorithmic_bytes": nbytes,
+                         "traffic_note": "no DRAM capture of the current verify kernel"},
+            "e2e": e2e, "cpu_baseline": cpu,
+            "gpu_launches": args.steps,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
 
 
 if __name__ == "__main__":

@@ -60,3 +60,19 @@ def test_reference_arm_under_torchrun_prints_once_from_rank_zero():
     assert len(lines) == 1
     rec = json.loads(lines[0])
     assert rec["impl"] == "reference" and rec["n_gpus"] == 2 and rec["value"] > 0
+
+
+def test_verify_reference_arm_prints_one_line():
+    """bench.py --config verify --impl reference: the oracle's verify on a
+    bounded sample of the verify workload, one JSON line in draft tokens/s."""
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--config", "verify",
+           "--pool", "bf16", "--steps", "1", "--warmup", "0"]
+    r = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    rec = json.loads(lines[0])
+    assert rec["impl"] == "reference" and rec["unit"] == "draft tokens/s" and rec["value"] > 0
+    assert rec["config"]["workload"] == "verify" and rec["config"]["pool"] == "bf16"
+    assert rec["cpu_baseline"]["kind"] == "oracle" and rec["e2e"]["h2d_bytes_per_step"] == 0
