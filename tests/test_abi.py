@@ -196,3 +196,31 @@ def test_prefill_schedule(K, monkeypatch):
     a = _args(K)
     assert K.lib().kda_prefill_schedule(ctypes.byref(a), 0, ctypes.byref(K.Schedule())) == \
         K.KDA_ERR_INVALID_ARG
+
+
+def test_host_call_staging_plan(K):
+    """kda_prefill_host's staging size (host only): the default piece, growth
+    with the piece length, the clamp to the input, a lower bound of two piece
+    buffers + the chain states + one piece's workspace, and refusals of bad
+    piece lengths and bad host cu_seqlens."""
+    import torch
+    B, T, H = 2, 10000, 4
+    q = torch.empty(B, T, H, 128, dtype=torch.bfloat16)
+    assert K.host_staging_size(q, q) == K.host_staging_size(q, q, piece_tokens=2048) > 0
+    sizes = [K.host_staging_size(q, q, piece_tokens=p) for p in (64, 512, 4096, 10048, 20480)]
+    assert sizes[0] < sizes[1] < sizes[2] < sizes[3] == sizes[4]
+    per_tok = 3 * 256 + 512 + 4 + 256          # q, k, v, g, beta in; out back
+    P = 512
+    ws = K.workspace_size(torch.empty(B, P, H, 128, dtype=torch.bfloat16), q)
+    assert sizes[1] >= 2 * B * P * H * per_tok + B * H * 128 * 128 * 4 + ws
+    for bad in (100, -64):
+        assert K.host_staging_size(q, q, piece_tokens=bad) == 0
+
+    cu = torch.tensor([0, 3000, 3001, 3001, 8001, 8065], dtype=torch.int32)
+    qv = torch.empty(8065, H, 128, dtype=torch.bfloat16)
+    good = K.host_staging_size(qv, qv, cu_seqlens=cu, piece_tokens=64)
+    assert good >= 2 * 5000 * H * per_tok      # whole sequences: the longest one fits a buffer
+    for i, val in ((0, 1), (2, 2000), (5, 8000)):   # cu[0] != 0, decreasing, end != T
+        bad = cu.clone()
+        bad[i] = val
+        assert K.host_staging_size(qv, qv, cu_seqlens=bad) == 0
