@@ -7,7 +7,7 @@
 // the work per (request, head) is ~4 x 16K FMAs against 128 KB of state
 // traffic, so the kernel is bound by HBM bandwidth on the state pool.
 //
-// Organisation: persistent CTAs (two per SM when the drafts fit) stream
+// Organisation: persistent CTAs (two per SM) stream
 // (request, head) items.  As soon as an item's state sits in registers, the
 // next item's 64 KB state block and draft rows are requested with cp.async, so
 // every item's loads overlap the previous item's compute; the updated state
@@ -19,7 +19,7 @@
 // of the warp (each lane ends with one column's sum; u goes back to all four
 // by a gather).  Shared-memory layouts keep every access conflict-free: the
 // state's 16-byte chunks are XOR-swizzled by row group, and the staged q, k
-// and e^g rows carry 16 bytes of padding per row group.
+// and e^g rows carry 16 bytes of padding after every 128 bytes.
 #include "kda_internal.h"
 #include "sm103.cuh"
 
@@ -28,12 +28,17 @@ namespace {
 
 constexpr int kMaxDrafts = 16;
 constexpr int kVerifyThreads = 256;
-// Staged draft row t (bytes): q bf16 and k bf16 rows of 128 with 16 B of
-// padding after each 32 B (row group), v bf16 unpadded, e^g fp32 with 16 B
-// after each 64 B.
-constexpr uint32_t kQRow = 384, kVRow = 256, kERow = 640;
+// Staged draft row t (bytes): q bf16 and k bf16 rows of 128, v bf16, e^g fp32,
+// the q, k and e^g rows with 16 B of padding after every 128 B (four row groups
+// of q / k, two of e^g): row group rg's 16-byte pieces then fall on eight
+// distinct bank groups for rg = 0..7.  1360 B per draft keeps two CTAs per SM
+// up to 16 drafts with a fp32 pool.
+constexpr uint32_t kQRow = 272, kVRow = 256, kERow = 560;
 constexpr uint32_t TO_Q = 0, TO_K = kQRow, TO_V = 2 * kQRow, TO_E = 2 * kQRow + kVRow;
-constexpr uint32_t kTokBytes = 2 * kQRow + kVRow + kERow;    // 1664
+constexpr uint32_t kTokBytes = 2 * kQRow + kVRow + kERow;    // 1360
+// byte offsets of row group rg in a staged q / k row and in an e^g row
+__device__ __forceinline__ uint32_t qk_group(int rg) { return 32u * rg + 16u * (rg >> 2); }
+__device__ __forceinline__ uint32_t e_group(int rg) { return 64u * rg + 16u * (rg >> 1); }
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -139,16 +144,16 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyP
                 const int t = e / 80, j = e - t * 80;
                 uint8_t* row = tb + t * kTokBytes;
                 if (j < 16) {
-                    cp_async16(row + TO_Q + j * 16 + (j >> 1) * 16, p.q + x.r * p.qs[0] + t * p.qs[1] + x.h * p.qs[2] + 8 * j);
+                    cp_async16(row + TO_Q + j * 16 + (j >> 3) * 16, p.q + x.r * p.qs[0] + t * p.qs[1] + x.h * p.qs[2] + 8 * j);
                 } else if (j < 32) {
                     const int jj = j - 16;
-                    cp_async16(row + TO_K + jj * 16 + (jj >> 1) * 16, p.k + x.r * p.ks[0] + t * p.ks[1] + x.h * p.ks[2] + 8 * jj);
+                    cp_async16(row + TO_K + jj * 16 + (jj >> 3) * 16, p.k + x.r * p.ks[0] + t * p.ks[1] + x.h * p.ks[2] + 8 * jj);
                 } else if (j < 48) {
                     const int jj = j - 32;
                     cp_async16(row + TO_V + jj * 16, p.v + x.r * p.vs[0] + t * p.vs[1] + x.h * p.vs[2] + 8 * jj);
                 } else {
                     const int jj = j - 48;
-                    cp_async16(row + TO_E + jj * 16 + (jj >> 2) * 16, p.g + x.r * p.gs[0] + t * p.gs[1] + x.h * p.gs[2] + 4 * jj);
+                    cp_async16(row + TO_E + jj * 16 + (jj >> 3) * 16, p.g + x.r * p.gs[0] + t * p.gs[1] + x.h * p.gs[2] + 4 * jj);
                 }
             }
         }
@@ -169,7 +174,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyP
         if (cur.valid) {
             for (int e = tid; e < D * kHeadDim; e += kVerifyThreads) {  // e^g in place
                 const int t = e >> 7, i = e & (kHeadDim - 1);
-                float* ge = reinterpret_cast<float*>(tb + t * kTokBytes + TO_E + i * 4 + (i >> 4) * 16);
+                float* ge = reinterpret_cast<float*>(tb + t * kTokBytes + TO_E + i * 4 + (i >> 5) * 16);
                 *ge = __expf(*ge);
             }
             if (tid < D) s_beta[tid] = p.beta_is_logit ? 1.0f / (1.0f + __expf(-bcur)) : bcur;
@@ -203,8 +208,8 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyP
                 const uint8_t* row = tb + t * kTokBytes;
                 float kk[16], x[16];
                 {
-                    const uint4 k0 = *reinterpret_cast<const uint4*>(row + TO_K + 48 * rg);
-                    const uint4 k1 = *reinterpret_cast<const uint4*>(row + TO_K + 48 * rg + 16);
+                    const uint4 k0 = *reinterpret_cast<const uint4*>(row + TO_K + qk_group(rg));
+                    const uint4 k1 = *reinterpret_cast<const uint4*>(row + TO_K + qk_group(rg) + 16);
                     const uint32_t kw[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
 #pragma unroll
                     for (int w = 0; w < 8; ++w) {
@@ -213,7 +218,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyP
                     }
 #pragma unroll
                     for (int i = 0; i < 16; i += 4) {
-                        const float4 e4 = *reinterpret_cast<const float4*>(row + TO_E + 80 * rg + 4 * i);
+                        const float4 e4 = *reinterpret_cast<const float4*>(row + TO_E + e_group(rg) + 4 * i);
                         x[i] = e4.x; x[i + 1] = e4.y; x[i + 2] = e4.z; x[i + 3] = e4.w;
                     }
                 }
@@ -233,8 +238,8 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyP
                 float u[4];
                 gather4(s_beta[t] * (vc - skc), rg, u);
                 {
-                    const uint4 q0 = *reinterpret_cast<const uint4*>(row + TO_Q + 48 * rg);
-                    const uint4 q1 = *reinterpret_cast<const uint4*>(row + TO_Q + 48 * rg + 16);
+                    const uint4 q0 = *reinterpret_cast<const uint4*>(row + TO_Q + qk_group(rg));
+                    const uint4 q1 = *reinterpret_cast<const uint4*>(row + TO_Q + qk_group(rg) + 16);
                     const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
                     for (int w = 0; w < 8; ++w) {
