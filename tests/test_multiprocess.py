@@ -76,3 +76,31 @@ def test_verify_reference_arm_prints_one_line():
     assert rec["impl"] == "reference" and rec["unit"] == "draft tokens/s" and rec["value"] > 0
     assert rec["config"]["workload"] == "verify" and rec["config"]["pool"] == "bf16"
     assert rec["cpu_baseline"]["kind"] == "oracle" and rec["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_clock_sampler_reads_median_clock_and_throttle_reasons(tmp_path):
+    """The bench's nvidia-smi sampler: median SM clock under load, the maximum
+    clock, and every throttle reason seen Active in any sample (fed a recorded
+    CSV instead of a live nvidia-smi)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    csv = tmp_path / "clocks.csv"
+    csv.write_text(
+        "0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active\n"
+        "0, 1980, 2070, 1390.5, 0x4, Not Active, Not Active, Not Active, Active\n"
+        "0, 2070, 2070, 1100.0, 0x0, Not Active, Not Active, Not Active, Not Active\n"
+        "garbled line\n")
+
+    class _Done:
+        def terminate(self):
+            pass
+
+        def wait(self, timeout=None):
+            return 0
+
+    s = bench.ClockSampler(0)
+    s.proc, s.path = _Done(), str(csv)
+    clk = s.stop()
+    assert clk["sm_mhz"] == 2070.0 and clk["sm_max_mhz"] == 2070.0 and clk["samples"] == 3
+    assert clk["reasons"] == ["sw_power_cap"]
+    assert not csv.exists()
