@@ -104,3 +104,25 @@ def test_clock_sampler_reads_median_clock_and_throttle_reasons(tmp_path):
     assert clk["sm_mhz"] == 2070.0 and clk["sm_max_mhz"] == 2070.0 and clk["samples"] == 3
     assert clk["reasons"] == ["sw_power_cap"]
     assert not csv.exists()
+
+
+def test_captured_traffic_only_for_the_profiled_kernel_source(tmp_path, monkeypatch):
+    """The bench's roofline `traffic` comes from a committed ncu record only
+    while the kernel source still has the hash the record names; scaled by
+    token-heads."""
+    import hashlib
+    sys.path.insert(0, ROOT)
+    import bench
+    (tmp_path / "profiles").mkdir()
+    src_dir = tmp_path / "kda_chunked_prefill_02_gb300" / "csrc"
+    src_dir.mkdir(parents=True)
+    src = src_dir / "kda_prep.cu"
+    src.write_bytes(b"// kernel v1\n")
+    sha = hashlib.sha256(b"// kernel v1\n").hexdigest()[:16]
+    (tmp_path / "profiles" / "prep_kernel_traffic.txt").write_text(
+        "kernel: prep_kernel\nsource_sha256_prefix: %s\ndram_bytes_per_token_head: 2500.0\n" % sha)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.captured_traffic("prep", 1000) == 2500.0 * 1000
+    assert bench.captured_traffic("state", 1000) is None      # no record
+    src.write_bytes(b"// kernel v2\n")
+    assert bench.captured_traffic("prep", 1000) is None       # source changed since the capture
