@@ -2,7 +2,9 @@
 CPU with the gloo backend: every (sequence, head) chain is independent, so N
 GPUs run N replicas with no data-path collective; the only collectives are the
 timing barrier and the max over ranks of the elapsed time.  The reference arm
-under torchrun must print one line, from rank 0, with every rank exiting 0."""
+under torchrun must print one line, from rank 0, with every rank exiting 0.
+Also the bench's other host logic: the verify reference arm, the clock
+sampler's parsing and the traffic record lookup."""
 import json
 import os
 import socket
