@@ -256,7 +256,7 @@ kda_status kda_prefill_workspace_layout(const kda_prefill_args* args,
  * distinct across requests.
  *   q, k: bf16, g: fp32, element (r, t, h, c) at r*s[0] + t*s[1] + h*s[2] + c
  *   v, out: bf16 likewise; beta: fp32 (r, t, h)
- *   state_pool: fp32 [pool_size, H, 128, 128] contiguous
+ *   state_pool: fp32 or bf16 (pool_dtype) [pool_size, H, 128, 128] contiguous
  *   slot, accepted: device int32 [R]; accepted[r] in 0..D, slot[r] in
  *   0..pool_size-1 (out-of-range entries are skipped and reported through
  *   device_status)
