@@ -87,6 +87,10 @@ typedef enum {
  * workspace: device scratch of at least kda_prefill_workspace_size(args) bytes,
  *   256-byte aligned, owned by the caller, used only during the call's kernels
  *   (so it may be reused by the next call on the same stream).
+ * Size limits: num_seqs <= 65535 and num_heads <= 65535 per call (the state
+ *   pass gives every (sequence, head) chain its own CTA and indexes sequences
+ *   and heads by grid dimensions), seqlen <= 2^31; larger calls return
+ *   KDA_ERR_UNSUPPORTED and launch nothing (split the batch).
  */
 typedef struct kda_prefill_args {
     const void* q;              /* bf16 */
@@ -267,7 +271,8 @@ kda_status kda_prefill_workspace_layout(const kda_prefill_args* args,
  * Draft rows and state blocks are moved in 16-byte pieces, so q, k, v, g and
  * state_pool must be 16-byte aligned, the q/k/v strides multiples of 8
  * elements and the g strides multiples of 4; otherwise KDA_ERR_UNSUPPORTED and
- * nothing is launched.
+ * nothing is launched.  Size limits: R <= 65535, H <= 65535, R * H < 2^31 and
+ * pool_size <= 2^30 (else KDA_ERR_UNSUPPORTED).
  */
 typedef struct kda_verify_args {
     const void* q;

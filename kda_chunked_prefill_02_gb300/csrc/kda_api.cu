@@ -80,7 +80,8 @@ kda_status check_prefill(const kda_prefill_args* a) {
     if (a->out_gate && (!aligned16(a->out_gate) || !aligned16(a->norm_weight) ||
                         !strides_ok(a->gate_stride, 8) || !(a->norm_eps >= 0.f)))
         return KDA_ERR_UNSUPPORTED;
-    if (a->num_seqs > (1 << 30) || a->num_heads > 65535 || a->seqlen > (int64_t)1 << 31)
+    // the state kernels index sequences and heads by grid dimensions (at most 65535)
+    if (a->num_seqs > 65535 || a->num_heads > 65535 || a->seqlen > (int64_t)1 << 31)
         return KDA_ERR_UNSUPPORTED;
     kda_workspace_layout L;
     if (!layout_of(a, &L)) return KDA_ERR_INVALID_ARG;
@@ -455,7 +456,9 @@ kda_status kda_verify(const kda_verify_args* a, void* stream) {
         !a->state_pool || !a->accepted || a->pool_size < 1)
         return KDA_ERR_INVALID_ARG;
     if (a->pool_dtype != KDA_POOL_F32 && a->pool_dtype != KDA_POOL_BF16) return KDA_ERR_UNSUPPORTED;
-    if (a->num_requests > 65535 || a->num_heads > 65535 || a->pool_size > (1 << 30))
+    // the kernel numbers the (request, head) items with 32-bit ints
+    if (a->num_requests > 65535 || a->num_heads > 65535 || a->pool_size > (1 << 30) ||
+        a->num_requests * a->num_heads > INT32_MAX)
         return KDA_ERR_UNSUPPORTED;
     const int64_t* ss[6] = {a->q_stride, a->k_stride, a->v_stride, a->g_stride, a->beta_stride,
                             a->out_stride};

@@ -224,3 +224,22 @@ def test_host_call_staging_plan(K):
         bad = cu.clone()
         bad[i] = val
         assert K.host_staging_size(qv, qv, cu_seqlens=bad) == 0
+
+
+def test_size_limits_refused_on_host(K):
+    """Calls past the kernels' index ranges are refused before any CUDA call:
+    more than 65535 sequences or heads in a prefill (grid dimensions), and
+    verify with R * H at or beyond 2^31 items."""
+    lib = K.lib()
+    run = lambda a: lib.kda_prefill(ctypes.byref(a), None)
+    assert run(_args(K, batch=65536, num_seqs=65536)) == K.KDA_ERR_UNSUPPORTED
+    assert run(_args(K, num_heads=65536)) == K.KDA_ERR_UNSUPPORTED
+    a = K.VerifyArgs()
+    fake = ctypes.c_void_p(1 << 20)
+    a.q = a.k = a.v = a.g = a.beta = a.out = a.state_pool = a.accepted = fake
+    for f in ("q_stride", "k_stride", "v_stride", "g_stride", "out_stride"):
+        setattr(a, f, K._i64x3(4 * 2 * 128, 2 * 128, 128))
+    a.beta_stride = K._i64x3(8, 2, 1)
+    a.head_dim_k = a.head_dim_v = 128
+    a.num_requests, a.num_drafts, a.num_heads, a.pool_size = 65535, 4, 65535, 65535
+    assert lib.kda_verify(ctypes.byref(a), None) == K.KDA_ERR_UNSUPPORTED
