@@ -89,7 +89,7 @@ typedef enum {
  *   (so it may be reused by the next call on the same stream).
  * Size limits: num_seqs <= 65535 and num_heads <= 65535 per call (the state
  *   pass gives every (sequence, head) chain its own CTA and indexes sequences
- *   and heads by grid dimensions), seqlen <= 2^31; larger calls return
+ *   and heads by grid dimensions), seqlen < 2^31; larger calls return
  *   KDA_ERR_UNSUPPORTED and launch nothing (split the batch).
  */
 typedef struct kda_prefill_args {

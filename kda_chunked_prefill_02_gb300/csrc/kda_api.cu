@@ -81,7 +81,7 @@ kda_status check_prefill(const kda_prefill_args* a) {
                         !strides_ok(a->gate_stride, 8) || !(a->norm_eps >= 0.f)))
         return KDA_ERR_UNSUPPORTED;
     // the state kernels index sequences and heads by grid dimensions (at most 65535)
-    if (a->num_seqs > 65535 || a->num_heads > 65535 || a->seqlen > (int64_t)1 << 31)
+    if (a->num_seqs > 65535 || a->num_heads > 65535 || a->seqlen > INT32_MAX)
         return KDA_ERR_UNSUPPORTED;
     kda_workspace_layout L;
     if (!layout_of(a, &L)) return KDA_ERR_INVALID_ARG;

@@ -234,6 +234,7 @@ def test_size_limits_refused_on_host(K):
     run = lambda a: lib.kda_prefill(ctypes.byref(a), None)
     assert run(_args(K, batch=65536, num_seqs=65536)) == K.KDA_ERR_UNSUPPORTED
     assert run(_args(K, num_heads=65536)) == K.KDA_ERR_UNSUPPORTED
+    assert run(_args(K, seqlen=1 << 31)) == K.KDA_ERR_UNSUPPORTED
     a = K.VerifyArgs()
     fake = ctypes.c_void_p(1 << 20)
     a.q = a.k = a.v = a.g = a.beta = a.out = a.state_pool = a.accepted = fake
