@@ -17,9 +17,10 @@ chains) on the host cores, on a bounded sample of the same workload per step;
 it is a deliberately slow reference, not a target.
 
 --config verify times MTP verify instead: one step = one kda_verify call over
-256 requests x 4 draft tokens x 32 heads against a device-resident state pool
-(fp32, or bf16 with --pool bf16; 537 / 268 MB, larger than L2), the accepted
-prefix's state written back in place.  Its line reports draft tokens/s.
+256 requests x 4 draft tokens (--drafts D: 1..16) x 32 heads against a
+device-resident state pool (fp32, or bf16 with --pool bf16; 537 / 268 MB,
+larger than L2), the accepted prefix's state written back in place.  Its line
+reports draft tokens/s.
 """
 import argparse
 import hashlib
@@ -53,6 +54,8 @@ def parse():
     ap.add_argument("--config", choices=["long", "varlen", "padded", "tiny", "verify"], default="long")
     ap.add_argument("--pool", choices=["fp32", "bf16"], default="fp32",
                     help="state pool element type of --config verify")
+    ap.add_argument("--drafts", type=int, default=4, choices=range(1, 17), metavar="1..16",
+                    help="draft tokens per request of --config verify")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -456,7 +459,8 @@ def main_reference(args):
 
 # ---- MTP verify (--config verify)
 
-VERIFY_METRIC = "KDA MTP verify draft tokens/s (R=256 requests x D=4 drafts, H=32, dk=dv=128), 1×GB300"
+def verify_metric(drafts):
+    return "KDA MTP verify draft tokens/s (R=256 requests x D=%d drafts, H=32, dk=dv=128), 1×GB300" % drafts
 
 
 def _timed(fn, k, stream, ws):
@@ -473,9 +477,11 @@ def _timed(fn, k, stream, ws):
     return e0.elapsed_time(e1) / k
 
 
-def verify_workload(pool):
+def verify_workload(pool, drafts=4):
     import torch
-    vi = workload("verify")
+    from kda_chunked_prefill_02_gb300 import inputs
+    # the verify workload (seed 4); other draft counts draw the same way
+    vi = workload("verify") if drafts == 4 else inputs.verify_inputs(4, R=256, D=drafts, H=32)
     if pool == "bf16":
         vi.state_pool = vi.state_pool.to(torch.bfloat16)
     return vi
@@ -494,7 +500,10 @@ def verify_bytes(vi):
 def verify_config(vi, pool):
     from kda_chunked_prefill_02_gb300 import inputs
     R, D, H = vi.q.shape[:3]
-    return {"workload": "verify", "description": inputs.CONFIG_DESCRIPTIONS["verify"],
+    desc = inputs.CONFIG_DESCRIPTIONS["verify"]
+    if D != 4:
+        desc = desc.replace("x 4 drafts", "x %d drafts" % D).replace("U{0..4}", "U{0..%d}" % D)
+    return {"workload": "verify", "description": desc,
             "requests": R, "drafts": D, "heads": H, "head_dim": 128, "pool": pool,
             "pool_bytes": vi.state_pool.numel() * vi.state_pool.element_size(),
             "l2": "state pool larger than L2 (no flush)"}
@@ -524,7 +533,7 @@ def verify_sample_size(vi, target_s):
 
 def main_verify(args):
     rank = int(os.environ.get("RANK", "0"))
-    vi = verify_workload(args.pool)
+    vi = verify_workload(args.pool, args.drafts)
     R, D, H = vi.q.shape[:3]
     if args.impl == "reference":
         ws = int(os.environ.get("WORLD_SIZE", "1"))
@@ -539,7 +548,7 @@ def main_verify(args):
             times.append(sec)
         sec = statistics.median(times)
         value = tok / sec
-        line = {"impl": "reference", "metric": VERIFY_METRIC, "value": value, "unit": "draft tokens/s",
+        line = {"impl": "reference", "metric": verify_metric(D), "value": value, "unit": "draft tokens/s",
                 "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic, seeded", "config": verify_config(vi, args.pool),
@@ -610,12 +619,12 @@ def main_verify(args):
         nbytes = verify_bytes(vi)
         achieved = nbytes / (ms / 1e3) / 1e9
         line = {
-            "metric": VERIFY_METRIC, "value": R * D * ws / (ms / 1e3), "unit": "draft tokens/s",
+            "metric": verify_metric(D), "value": R * D * ws / (ms / 1e3), "unit": "draft tokens/s",
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16 q/k/v/out, fp32 gate/beta, %s state pool, fp32 arithmetic" % args.pool,
             "data": "synthetic, seeded (q,k L2-normalised, g=-5*sigmoid(N(0,1)), beta logits N(0,1), "
-                    "accepted U{0..4})",
+                    "accepted U{0..%d})" % D,
             "config": dict(verify_config(vi, args.pool),
                            parallelism="replica per GPU" if ws > 1 else "1 GPU"),
             "requests_per_s": R * ws / (ms / 1e3),
