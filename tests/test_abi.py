@@ -244,3 +244,21 @@ def test_size_limits_refused_on_host(K):
     a.head_dim_k = a.head_dim_v = 128
     a.num_requests, a.num_drafts, a.num_heads, a.pool_size = 65535, 4, 65535, 65535
     assert lib.kda_verify(ctypes.byref(a), None) == K.KDA_ERR_UNSUPPORTED
+
+
+def test_no_fallback_without_the_library_or_a_gpu(K, monkeypatch, tmp_path):
+    """The product path never computes on the CPU: CPU tensors are refused, and
+    a missing libkda.so is an error, not a detour."""
+    import torch
+    from kda_chunked_prefill_02_gb300 import inputs
+    inp = inputs.prefill_inputs(3, B=1, T=70, H=2)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        K.kda_prefill(inp.q, inp.k, inp.v, inp.g, inp.beta, out=torch.empty_like(inp.v),
+                      final_state=torch.empty(1, 2, 128, 128), workspace=torch.empty(1, dtype=torch.uint8))
+    vi = inputs.verify_inputs(3, R=2, D=2, H=1)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        K.kda_verify(vi.q, vi.k, vi.v, vi.g, vi.beta, vi.state_pool, vi.accepted)
+    monkeypatch.setattr(K, "_lib", None)
+    monkeypatch.setattr(K, "LIB_PATH", str(tmp_path / "libkda.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        K.workspace_size(inp.q, inp.v)
