@@ -321,7 +321,8 @@ kda_status kda_verify(const kda_verify_args* args, void* stream);
  * Limits and behaviour:
  *  - Returns KDA_ERR_UNSUPPORTED, launching nothing, when
  *    kda_prefill_workspace_size(args) exceeds KDA_NOALLOC_MAX_WORKSPACE_BYTES
- *    (about 290 chunk-head records: e.g. 2048 tokens x 8 heads).
+ *    (about 400 chunk-head records of 82,432 bytes, less 64 KB of state per
+ *    padded chain: e.g. 2048 tokens x 12 heads, or 8192 tokens x 3 heads).
  *  - The first call on each device looks up the array's device address for
  *    that device (with the device current); make that first call before any
  *    stream capture.  It allocates nothing, here or later.

@@ -262,3 +262,14 @@ def test_no_fallback_without_the_library_or_a_gpu(K, monkeypatch, tmp_path):
     monkeypatch.setattr(K, "LIB_PATH", str(tmp_path / "libkda.so"))
     with pytest.raises(RuntimeError, match="not built"):
         K.workspace_size(inp.q, inp.v)
+
+
+def test_noalloc_capacity_as_documented(K):
+    """kda_prefill_noalloc's scratch holds the workspace of 2048 tokens x 12
+    heads (and 8192 x 3), but not 2048 x 13 (host-side sizes only)."""
+    import torch
+    lim = K.NOALLOC_MAX_WORKSPACE_BYTES
+    size = lambda T, H: K.workspace_size(torch.empty(1, T, H, 128, dtype=torch.bfloat16),
+                                         torch.empty(1, T, H, 128, dtype=torch.bfloat16))
+    assert size(2048, 12) <= lim < size(2048, 13)
+    assert size(8192, 3) <= lim < size(8192, 4)
