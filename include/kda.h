@@ -37,6 +37,10 @@
  *    that ran out) are written as a kda_status value to *device_status when it
  *    is non-NULL (a caller-owned device int32 that the caller zeroes); the
  *    kernels then skip the offending work instead of faulting.
+ *  - Per-device set-up (the kernels' shared-memory limits, the no-alloc
+ *    scratch address) is done on a device's first call and remembered for the
+ *    process; after cudaDeviceReset the library must not be called again in
+ *    that process.
  */
 #ifndef KDA_H
 #define KDA_H
@@ -48,7 +52,41 @@
 extern "C" {
 #endif
 
-#define KDA_ABI_VERSION 4
+#define KDA_ABI_VERSION 5
+
+/*
+ * Test and measurement overrides of the library's own choices, passed per call
+ * through kda_prefill_args.overrides / kda_verify_args.overrides (NULL = none).
+ * Results stay within the stated tolerances whatever is selected (the
+ * schedule choices give bitwise-equal results for a given state kernel).
+ * Nothing is read from the process environment: a call's kernels and schedule
+ * depend only on its arguments.
+ *   state_kernel    0: library's choice, 1: 32-column slab CTAs, 2: one
+ *                   whole-chain CTA per (sequence, head) (the fused norm
+ *                   always takes 2)
+ *   segment_chunks  -1: library's choice, 0: never segment, n > 0: segments of
+ *                   n chunks (padded calls)
+ *   prep_ctas       > 0: prep grid of a forced segmented call (0: choice)
+ *   no_pdl          1: no programmatic launch between consecutive prep grids
+ *   stall_seed      != 0: the kernel instantiations with the stall hook, in
+ *                   which a quarter of the warps at each injection site spin
+ *                   for a pseudo-random 0..4095 cycles; every result must be
+ *                   bit-identical to the run without it
+ *   reserved0       must be 0
+ *   wait_limit_ns   > 0: bound of the kernels' working mbarrier waits instead
+ *                   of 200 ms (a wait that runs out writes KDA_ERR_TIMEOUT to
+ *                   the status word and the CTA winds down; the wind-down's own
+ *                   waits for copies and products in flight keep 200 ms)
+ */
+typedef struct kda_overrides {
+    int32_t state_kernel;
+    int32_t segment_chunks;
+    int32_t prep_ctas;
+    int32_t no_pdl;
+    uint32_t stall_seed;
+    int32_t reserved0;
+    int64_t wait_limit_ns;
+} kda_overrides;
 
 typedef enum {
     KDA_OK = 0,
@@ -135,6 +173,7 @@ typedef struct kda_prefill_args {
     int64_t gate_stride[3];
     const float* norm_weight;
     float norm_eps;
+    const kda_overrides* overrides;   /* NULL: the library's choices (see kda_overrides) */
 } kda_prefill_args;
 
 /*
@@ -166,24 +205,20 @@ size_t kda_prefill_workspace_size(const kda_prefill_args* args);
  * CUDA graph once one has run outside the capture.
  * Returns KDA_OK once the kernels are enqueued.
  *
- * Environment overrides, read on every call (tests and measurements; results
- * are the same within the stated tolerances whatever they select):
- *   KDA_STATE_KERNEL=slab|head   state kernel (the fused norm always takes head)
- *   KDA_SEGMENT_CHUNKS=n         segments of n chunks (0: never segment)
- *   KDA_SEGMENT_PREP_CTAS=n      prep grid of a forced segmented call
- *   KDA_SEGMENT_PDL=0            no programmatic launch between prep grids
- *   KDA_STALL_INJECT=seed        kernels with the stall hook: a quarter of the
- *                                warps at each injection site spin for a
- *                                pseudo-random 0..4095 cycles; every result
- *                                must be bit-identical to the run without it
- *                                (also read by kda_verify)
+ * Segmented calls of one host thread share its second stream, so the state
+ * passes of two such calls made from one thread on different caller streams
+ * run one after the other (results are unaffected; give each concurrent
+ * caller stream its own host thread to overlap them).
+ *
+ * Tests and measurements can override the kernel and schedule choices per
+ * call through args->overrides (see kda_overrides).
  */
 kda_status kda_prefill(const kda_prefill_args* args, void* stream);
 
 /*
  * The schedule kda_prefill would run for these arguments on a GPU with
- * num_sms SMs (host only: no device call; reads the same environment
- * overrides as kda_prefill).  segmented: 1 if the tokens are cut into
+ * num_sms SMs (host only: no device call; honours args->overrides as
+ * kda_prefill does).  segmented: 1 if the tokens are cut into
  * segments of segment_chunks chunks, the state pass of one beside the prep
  * of the next, prep on prep_ctas CTAs; whole_chain: 1 if the state pass runs
  * one CTA per chain (all 128 value columns), 0 for four 32-column slab CTAs
@@ -301,6 +336,7 @@ typedef struct kda_verify_args {
     int32_t* device_status;     /* optional device int32 */
     int32_t pool_dtype;         /* KDA_POOL_F32 or KDA_POOL_BF16 */
     int32_t replay_only;        /* 1: commit mode, see above */
+    const kda_overrides* overrides;   /* NULL: none; only stall_seed applies here */
 } kda_verify_args;
 
 kda_status kda_verify(const kda_verify_args* args, void* stream);
@@ -355,8 +391,10 @@ kda_status kda_prefill_noalloc(const kda_prefill_args* args, void* stream);
  * sequence, with each chain's state carried from piece to piece on the device,
  * so the result is bitwise that of one kda_prefill call; varlen: runs of whole
  * sequences).  Piece p + 1 is copied in while piece p runs and each piece's
- * output is copied out while later pieces run, on two copy streams the call
- * creates and releases, ordered after the work already on `stream`; when
+ * output is copied out while later pieces run, on two copy streams (created
+ * on a host thread's first call on a device and kept for the thread's life,
+ * like kda_prefill's second stream), ordered after the work already on
+ * `stream`; when
  * `stream` reaches the point after this call, every output is in host memory.
  * The host buffers and the staging memory must stay valid until then.  Errors:
  * KDA_ERR_INVALID_ARG for missing pointers, unusable shapes or cu_seqlens, or a

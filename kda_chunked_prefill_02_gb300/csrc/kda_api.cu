@@ -6,6 +6,7 @@
 
 #include "../../include/kda.h"
 #include "kda_internal.h"
+#include "sm103.cuh"
 #include "tmap.h"
 
 using namespace kda;
@@ -23,9 +24,20 @@ int64_t max_chunks_of(const kda_prefill_args* a) {
 }
 
 bool layout_of(const kda_prefill_args* a, kda_workspace_layout* L) {
+    if (a->num_heads < 1 || a->seqlen < 0 || a->num_seqs < 0 || a->batch < 0) return false;
+    // Sizes that cannot be described in size_t (with room for the alignment of
+    // every region) are refused rather than wrapped.
+    constexpr int64_t kMaxDim = (int64_t)1 << 40;
+    if (a->seqlen > kMaxDim || a->num_seqs > kMaxDim || a->batch > kMaxDim || a->num_heads > kMaxDim)
+        return false;
     const int64_t mc = max_chunks_of(a);
-    if (mc < 0 || a->num_heads < 1) return false;
+    if (mc < 0) return false;
+    const size_t limit = SIZE_MAX / 4;
+    if ((size_t)mc > limit / (size_t)a->num_heads) return false;
     const size_t nrec = (size_t)mc * (size_t)a->num_heads;
+    if (nrec > limit / kRecBytes) return false;
+    const size_t chains = (size_t)(a->cu_seqlens ? a->num_seqs : a->batch);
+    if (chains > limit / ((size_t)a->num_heads * kHeadDim * kHeadDim * sizeof(float))) return false;
     size_t o = 0;
     L->max_chunks = mc;
     L->record_bytes = kRecBytes;
@@ -49,7 +61,8 @@ bool strides_ok(const int64_t* s, int64_t mult) {
     return true;
 }
 
-kda_status check_prefill(const kda_prefill_args* a) {
+// Every argument check of a prefill call except the workspace.
+kda_status check_args(const kda_prefill_args* a) {
     if (!a) return KDA_ERR_INVALID_ARG;
     if (a->head_dim_k != kHeadDim || a->head_dim_v != kHeadDim || a->chunk != kChunk)
         return KDA_ERR_UNSUPPORTED;
@@ -85,16 +98,31 @@ kda_status check_prefill(const kda_prefill_args* a) {
         return KDA_ERR_UNSUPPORTED;
     kda_workspace_layout L;
     if (!layout_of(a, &L)) return KDA_ERR_INVALID_ARG;
+    if (a->overrides && a->overrides->reserved0 != 0) return KDA_ERR_INVALID_ARG;
+    return KDA_OK;
+}
+
+// The checks of check_args plus the caller's workspace.
+kda_status check_prefill(const kda_prefill_args* a) {
+    const kda_status st = check_args(a);
+    if (st != KDA_OK) return st;
+    kda_workspace_layout L;
+    layout_of(a, &L);
     if (!a->workspace || a->workspace_bytes < L.total) return KDA_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(a->workspace) & (kAlign - 1)) != 0) return KDA_ERR_UNSUPPORTED;
     return KDA_OK;
 }
 
-// KDA_STALL_INJECT=<seed>: the kernels' stall_point hook (timing perturbation
-// for ordering tests; results must not change).  Unset or 0: off.
-uint32_t stall_seed_from_env() {
-    const char* e = getenv("KDA_STALL_INJECT");
-    return e ? (uint32_t)strtoul(e, nullptr, 10) : 0u;
+// The call's overrides (tests and measurements), or the library's defaults.
+kda_overrides overrides_of(const kda_overrides* o) {
+    kda_overrides r;
+    memset(&r, 0, sizeof(r));
+    r.segment_chunks = -1;
+    if (o) r = *o;
+    return r;
+}
+uint64_t wait_limit_of(const kda_overrides& o) {
+    return o.wait_limit_ns > 0 ? (uint64_t)o.wait_limit_ns : kWaitLimitNs;
 }
 
 void fill_params(const kda_prefill_args* a, const kda_workspace_layout& L, PrefillParams* p) {
@@ -128,7 +156,9 @@ void fill_params(const kda_prefill_args* a, const kda_workspace_layout& L, Prefi
     for (int i = 0; i < 3; ++i) p->gts[i] = a->gate_stride[i];
     p->norm_w = a->norm_weight;
     p->norm_eps = a->norm_eps;
-    p->stall_seed = stall_seed_from_env();
+    const kda_overrides o = overrides_of(a->overrides);
+    p->stall_seed = o.stall_seed;
+    p->wait_ns = wait_limit_of(o);
 }
 
 // 4-D input tensor map [channel 128, head, token, batch] with one chunk of
@@ -182,14 +212,13 @@ bool make_prep_maps(const kda_prefill_args* a, PrepMaps* m) {
 // columns) when the 32-column slab CTAs would need more than two waves of SMs
 // (a whole-chain CTA takes about twice as long per chunk step, measured), so
 // below that the slab kernel is as fast or faster.  The two kernels compute the
-// same chunk step.  KDA_STATE_KERNEL=head|slab overrides the choice (tests,
-// measurements); the fused output norm needs whole rows and always takes the
+// same chunk step.  The overrides' state_kernel (tests, measurements) replaces
+// the choice; the fused output norm needs whole rows and always takes the
 // whole-chain kernel.
-bool whole_chain_kernel(const PrefillParams& p, int num_sms) {
-    const char* force = getenv("KDA_STATE_KERNEL");
+bool whole_chain_kernel(const PrefillParams& p, const kda_overrides& o, int num_sms) {
     if (p.gate) return true;
-    if (force && !strcmp(force, "head")) return true;
-    if (force && !strcmp(force, "slab")) return false;
+    if (o.state_kernel == 2) return true;
+    if (o.state_kernel == 1) return false;
     return (long long)p.N * p.H * (kHeadDim / kSlab) > 2LL * num_sms;
 }
 
@@ -231,35 +260,32 @@ double segmented_us(long long cps, long long chains, long long seg, long long ct
     return S;
 }
 
-Segments plan_segments(const PrefillParams& p, int num_sms) {
+Segments plan_segments(const PrefillParams& p, const kda_overrides& o, int num_sms) {
     Segments sg;
     if (p.cu != nullptr || p.T <= 0 || p.N <= 0 || num_sms < 4) return sg;
-    const char* env = getenv("KDA_SEGMENT_CHUNKS");
-    const long long forced = env ? atoll(env) : -1;
+    const long long forced = o.segment_chunks < 0 ? -1 : o.segment_chunks;
     if (forced == 0) return sg;
     const long long chains = (long long)p.N * p.H, cps = (p.T + kChunk - 1) / kChunk;
-    const char* force = getenv("KDA_STATE_KERNEL");
-    const bool allow_slab = !p.gate && !(force && !strcmp(force, "head"));
-    const bool allow_head = p.gate || !(force && !strcmp(force, "slab"));
+    const bool allow_slab = !p.gate && o.state_kernel != 2;
+    const bool allow_head = p.gate || o.state_kernel != 1;
     auto waves = [](long long n, long long m) { return (double)((n + m - 1) / m); };
     // sequential: prep on every SM, then the state pass (each with its start-up
     // and tail, as a segment's)
     double best = waves(cps * chains, num_sms) * kRecUs + 2.0 * kSegmentUs +
-                  (whole_chain_kernel(p, num_sms) ? waves(chains, num_sms) * cps * kHeadStepUs
+                  (whole_chain_kernel(p, o, num_sms) ? waves(chains, num_sms) * cps * kHeadStepUs
                                                   : waves(4 * chains, num_sms) * cps * kSlabStepUs);
     best *= 0.95;   // segment only for a clear gain
     if (forced > 0) best = 1e300;
     for (int head = 0; head < 2; ++head) {
         if (head ? !allow_head : !allow_slab) continue;
-        if (forced > 0 && (bool)head != whole_chain_kernel(p, num_sms)) continue;
+        if (forced > 0 && (bool)head != whole_chain_kernel(p, o, num_sms)) continue;
         const long long state_ctas = head ? chains : 4 * chains;
         long long ctas = num_sms - state_ctas;
         if (ctas < num_sms / 4) {
             if (forced <= 0) continue;  // prep would be starved of SMs
             ctas = num_sms / 4;
         }
-        const char* pc_env = getenv("KDA_SEGMENT_PREP_CTAS");   // measurements
-        if (forced > 0 && pc_env && atoi(pc_env) > 0) ctas = atoi(pc_env) < num_sms ? atoi(pc_env) : num_sms;
+        if (forced > 0 && o.prep_ctas > 0) ctas = o.prep_ctas < num_sms ? o.prep_ctas : num_sms;
         const double step = head ? kHeadStepUs : kSlabStepUs;
         if (forced > 0) {
             sg.on = true;
@@ -317,8 +343,9 @@ bool side_set(SideSet* out) {
     return true;
 }
 
-kda_status run_segments(const kda_prefill_args* a, const PrefillParams& p, const Segments& sg,
-                        const kda_workspace_layout& L, int num_sms, const SideSet& side, cudaStream_t s) {
+kda_status run_segments(const kda_prefill_args* a, const PrefillParams& p, const kda_overrides& o,
+                        const Segments& sg, const kda_workspace_layout& L, int num_sms,
+                        const SideSet& side, cudaStream_t s) {
     cudaStream_t ss = side.ss;
     cudaEvent_t ev_prep = side.ev_prep, ev_done = side.ev_done;
     auto ck = [](cudaError_t e) { return e == cudaSuccess; };
@@ -326,8 +353,7 @@ kda_status run_segments(const kda_prefill_args* a, const PrefillParams& p, const
     bool ok = ck(cudaEventRecord(ev_prep, s)) && ck(cudaStreamWaitEvent(ss, ev_prep, 0));
     float* carry = reinterpret_cast<float*>(static_cast<uint8_t*>(a->workspace) + L.state_carry);
     const int64_t seg_tokens = (int64_t)sg.chunks * kChunk;
-    const char* pdl_env = getenv("KDA_SEGMENT_PDL");
-    const bool pdl = !(pdl_env && !strcmp(pdl_env, "0"));
+    const bool pdl = o.no_pdl == 0;
     size_t rec_base = 0;
     for (int64_t t0 = 0; ok && t0 < p.T; t0 += seg_tokens) {
         const int ts = (int)(p.T - t0 < seg_tokens ? p.T - t0 : seg_tokens);
@@ -378,13 +404,14 @@ kda_status run_prefill(const kda_prefill_args* a, void* stream, int stages) {
             return KDA_ERR_CUDA;
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const kda_overrides o = overrides_of(a->overrides);
     if (prep && !a->device_status && cudaMemsetAsync(p.status, 0, sizeof(int32_t), s) != cudaSuccess)
         return KDA_ERR_CUDA;
     if (prep && state_pass) {
-        const Segments sg = plan_segments(p, num_sms);
+        const Segments sg = plan_segments(p, o, num_sms);
         SideSet side;
         // without a second stream (none could be created) the call runs in one pass
-        if (sg.on && side_set(&side)) return run_segments(a, p, sg, L, num_sms, side, s);
+        if (sg.on && side_set(&side)) return run_segments(a, p, o, sg, L, num_sms, side, s);
     }
     if (prep) {
         PrepMaps pmaps;
@@ -394,12 +421,14 @@ kda_status run_prefill(const kda_prefill_args* a, void* stream, int stages) {
         if (launch_prep(p, pmaps, num_sms, s) != cudaSuccess) return KDA_ERR_CUDA;
     }
     if (state_pass) {
-        if (launch_state_pass(a, p, whole_chain_kernel(p, num_sms), s) != cudaSuccess) return KDA_ERR_CUDA;
+        if (launch_state_pass(a, p, whole_chain_kernel(p, o, num_sms), s) != cudaSuccess) return KDA_ERR_CUDA;
     }
     return KDA_OK;
 }
 
 }  // namespace
+
+int kda::prefill_check_args(const kda_prefill_args* a) { return (int)check_args(a); }
 
 extern "C" {
 
@@ -429,9 +458,10 @@ kda_status kda_prefill_schedule(const kda_prefill_args* args, int num_sms, kda_s
     p.H = (int)args->num_heads;
     p.B = (int)args->batch;
     p.gate = static_cast<const __nv_bfloat16*>(args->out_gate);
-    const Segments sg = plan_segments(p, num_sms);
+    const kda_overrides o = overrides_of(args->overrides);
+    const Segments sg = plan_segments(p, o, num_sms);
     out->segmented = sg.on ? 1 : 0;
-    out->whole_chain = sg.on ? (sg.head ? 1 : 0) : (whole_chain_kernel(p, num_sms) ? 1 : 0);
+    out->whole_chain = sg.on ? (sg.head ? 1 : 0) : (whole_chain_kernel(p, o, num_sms) ? 1 : 0);
     out->segment_chunks = sg.on ? sg.chunks : 0;
     out->prep_ctas = sg.on ? sg.prep_ctas : num_sms;
     return KDA_OK;
@@ -502,7 +532,7 @@ kda_status kda_verify(const kda_verify_args* a, void* stream) {
     p.scale = a->scale;
     p.pool_bf16 = a->pool_dtype == KDA_POOL_BF16 ? 1 : 0;
     p.replay_only = a->replay_only ? 1 : 0;
-    p.stall_seed = stall_seed_from_env();
+    p.stall_seed = overrides_of(a->overrides).stall_seed;
     return launch_verify(p, num_sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KDA_OK
                                                                                : KDA_ERR_CUDA;
 }

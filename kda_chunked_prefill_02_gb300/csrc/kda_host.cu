@@ -110,6 +110,44 @@ bool make_plan(const kda_prefill_host_args* h, Plan* pl) {
     return true;
 }
 
+// The copy streams and events of host-buffer calls: one set per host thread
+// and device, created on the thread's first call on that device and kept for
+// the thread's life (calls of one thread share them; every dependency between
+// calls goes through the caller's stream).
+struct CopySet {
+    cudaStream_t hs = nullptr, ds = nullptr;      // copies in, copies out
+    cudaEvent_t ev_start = nullptr, ev_end = nullptr, ev_in_done = nullptr;
+    cudaEvent_t ev_in[2] = {}, ev_comp[2] = {}, ev_out[2] = {};
+};
+
+bool copy_set(CopySet* out) {
+    constexpr int kMaxDevices = 64;
+    thread_local CopySet sets[kMaxDevices];
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    CopySet& cs = sets[dev];
+    if (!cs.hs) {
+        CopySet n;
+        auto ev = [](cudaEvent_t* e) { return cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess; };
+        bool ok = cudaStreamCreateWithFlags(&n.hs, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaStreamCreateWithFlags(&n.ds, cudaStreamNonBlocking) == cudaSuccess &&
+                  ev(&n.ev_start) && ev(&n.ev_end) && ev(&n.ev_in_done);
+        for (int b = 0; b < 2 && ok; ++b) ok = ev(&n.ev_in[b]) && ev(&n.ev_comp[b]) && ev(&n.ev_out[b]);
+        if (!ok) {
+            cudaEvent_t all[] = {n.ev_start, n.ev_end, n.ev_in_done, n.ev_in[0], n.ev_in[1], n.ev_comp[0],
+                                 n.ev_comp[1], n.ev_out[0], n.ev_out[1]};
+            for (cudaEvent_t e : all)
+                if (e) cudaEventDestroy(e);
+            if (n.hs) cudaStreamDestroy(n.hs);
+            if (n.ds) cudaStreamDestroy(n.ds);
+            return false;
+        }
+        cs = n;
+    }
+    *out = cs;
+    return true;
+}
+
 }  // namespace
 
 extern "C" size_t kda_prefill_host_staging_size(const kda_prefill_host_args* h) {
@@ -131,21 +169,19 @@ extern "C" kda_status kda_prefill_host(const kda_prefill_host_args* h, void* str
     const int64_t H = pl.H, T = pl.T, B = pl.B;
     const size_t sblock = (size_t)H * kD * kD * 4;  // one sequence's states
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    cudaStream_t hs = nullptr, ds = nullptr;
-    cudaEvent_t ev_start = nullptr, ev_end = nullptr, ev_in[2] = {}, ev_comp[2] = {}, ev_out[2] = {};
+    CopySet set;
+    if (!copy_set(&set)) return KDA_ERR_CUDA;
+    cudaStream_t hs = set.hs, ds = set.ds;
+    cudaEvent_t ev_start = set.ev_start, ev_end = set.ev_end;
+    cudaEvent_t* ev_in = set.ev_in;
+    cudaEvent_t* ev_comp = set.ev_comp;
+    cudaEvent_t* ev_out = set.ev_out;
     kda_status ret = KDA_OK;
     auto ck = [&](cudaError_t e) {
         if (e != cudaSuccess && ret == KDA_OK) ret = KDA_ERR_CUDA;
         return e == cudaSuccess;
     };
-    bool ok = ck(cudaStreamCreateWithFlags(&hs, cudaStreamNonBlocking)) &&
-              ck(cudaStreamCreateWithFlags(&ds, cudaStreamNonBlocking)) &&
-              ck(cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming)) &&
-              ck(cudaEventCreateWithFlags(&ev_end, cudaEventDisableTiming));
-    for (int b = 0; b < 2 && ok; ++b)
-        ok = ck(cudaEventCreateWithFlags(&ev_in[b], cudaEventDisableTiming)) &&
-             ck(cudaEventCreateWithFlags(&ev_comp[b], cudaEventDisableTiming)) &&
-             ck(cudaEventCreateWithFlags(&ev_out[b], cudaEventDisableTiming));
+    bool ok = true;
     // Work already queued on the caller's stream (an earlier use of the staging
     // memory) comes first.
     ok = ok && ck(cudaEventRecord(ev_start, cs)) && ck(cudaStreamWaitEvent(hs, ev_start, 0)) &&
@@ -236,23 +272,9 @@ extern "C" kda_status kda_prefill_host(const kda_prefill_host_args* h, void* str
         ok = ck(cudaStreamWaitEvent(ds, ev_comp[(pl.pieces.size() - 1) & 1], 0)) &&
              ck(cudaMemcpyAsync(a.final_state, dstate0, (size_t)B * sblock, cudaMemcpyDeviceToHost, ds));
     }
-    // The caller's stream completes only after every copy has landed.
-    if (ds && ev_end && ck(cudaEventRecord(ev_end, ds))) ck(cudaStreamWaitEvent(cs, ev_end, 0));
-    if (hs && ev_start) {
-        cudaEvent_t e2 = nullptr;
-        if (ck(cudaEventCreateWithFlags(&e2, cudaEventDisableTiming)) && ck(cudaEventRecord(e2, hs)))
-            ck(cudaStreamWaitEvent(cs, e2, 0));
-        if (e2) cudaEventDestroy(e2);
-    }
-    // Streams and events are released once their work completes.
-    for (int b = 0; b < 2; ++b) {
-        if (ev_in[b]) cudaEventDestroy(ev_in[b]);
-        if (ev_comp[b]) cudaEventDestroy(ev_comp[b]);
-        if (ev_out[b]) cudaEventDestroy(ev_out[b]);
-    }
-    if (ev_start) cudaEventDestroy(ev_start);
-    if (ev_end) cudaEventDestroy(ev_end);
-    if (hs) cudaStreamDestroy(hs);
-    if (ds) cudaStreamDestroy(ds);
+    // The caller's stream completes only after every copy has landed (also
+    // after a failure, so that nothing queued later on it overtakes a copy).
+    if (ck(cudaEventRecord(ev_end, ds))) ck(cudaStreamWaitEvent(cs, ev_end, 0));
+    if (ck(cudaEventRecord(set.ev_in_done, hs))) ck(cudaStreamWaitEvent(cs, set.ev_in_done, 0));
     return ret;
 }

@@ -7,7 +7,28 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
+struct kda_prefill_args;
+
 namespace kda {
+
+// Every argument check of kda_prefill except the workspace (a kda_status value).
+int prefill_check_args(const kda_prefill_args* a);
+
+// Raises a kernel's dynamic shared-memory limit once per device (the attribute
+// stays set for the device's context), so that launches after the first skip
+// the driver call.  `done` holds one bit per device.
+inline cudaError_t set_smem_limit_once(const void* kern, int bytes, std::atomic<uint64_t>& done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
 
 constexpr int kHeadDim = 128;   // K = V = 128
 constexpr int kChunk = 64;      // tokens per chunk
@@ -58,6 +79,8 @@ struct PrefillParams {
     float norm_eps;
     uint32_t stall_seed;         // test hook: timing perturbation (stall_point), 0 = off
     int out_tma;                 // 1: the state kernel got a tensor map of out
+    uint64_t wait_ns;            // bound of the kernels' working mbarrier waits (kWaitLimitNs
+                                 // unless a test lowers it; wind-down waits keep kWaitLimitNs)
 };
 
 // Chunk c (global index) -> sequence, token start and length.

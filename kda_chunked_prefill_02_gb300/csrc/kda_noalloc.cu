@@ -18,6 +18,7 @@
 #include <mutex>
 
 #include "../../include/kda.h"
+#include "kda_internal.h"
 
 namespace {
 
@@ -50,6 +51,11 @@ kda_status scratch_on_current_device(void** out) {
 
 extern "C" kda_status kda_prefill_noalloc(const kda_prefill_args* args, void* stream) {
     if (!args) return KDA_ERR_INVALID_ARG;
+    // The arguments are checked as kda_prefill checks them (all but the
+    // workspace) before the size test, so that bad arguments come back as
+    // KDA_ERR_INVALID_ARG and not as an oversize problem.
+    const kda_status checked = static_cast<kda_status>(kda::prefill_check_args(args));
+    if (checked != KDA_OK) return checked;
     const size_t need = kda_prefill_workspace_size(args);
     if (need > kNoAllocScratchBytes) return KDA_ERR_UNSUPPORTED;
     void* scratch = nullptr;

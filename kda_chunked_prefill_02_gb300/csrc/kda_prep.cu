@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-    __shared__ uint64_t bar_in, bar_mma[3];
+    __shared__ uint64_t bar_in, bar_mma[3], bar_fin;
     __shared__ uint32_t tmem_base_sh;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -171,6 +171,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     if (tid == 0) {
         mbar_init(&bar_in, 1);
         for (int i = 0; i < 3; ++i) mbar_init(&bar_mma[i], 1);
+        mbar_init(&bar_fin, 1);
         fence_mbar_init();
         tma_prefetch_desc(&maps.q); tma_prefetch_desc(&maps.k);
         tma_prefetch_desc(&maps.v); tma_prefetch_desc(&maps.g);
@@ -214,7 +215,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         if (rec_next >= nrec) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         stall_point<kStall>(p.stall_seed, 1, it);
         // One thread waits on each mbarrier; the others wait at the CTA barrier.
-        ok = __syncthreads_and(tid == 0 ? mbar_wait(&bar_in, it & 1, nullptr) : true);
+        ok = __syncthreads_and(tid == 0 ? mbar_wait(&bar_in, it & 1, nullptr, p.wait_ns) : true);
         if (!ok) break;
         pend_parity = -1;
         if (tid < 64) {
@@ -381,7 +382,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             bulk_commit();
         }
         if (cn.len > 0) bcur = load_beta(cn, rec_next % p.H);
-        ok = __syncthreads_and(tid == 0 ? mbar_wait(&bar_mma[0], it & 1, nullptr) : true);
+        ok = __syncthreads_and(tid == 0 ? mbar_wait(&bar_mma[0], it & 1, nullptr, p.wait_ns) : true);
         tc_fence_after();
         if (!ok) break;
         // Once the Kt image has been read out of the consumed gate tile (this
@@ -537,7 +538,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                       idesc_bf16_f32(128, 64), false);
             umma_commit(&bar_mma[1]);
         }
-        ok = __syncthreads_and(tid == 0 ? mbar_wait(&bar_mma[1], it & 1, nullptr) : true);
+        ok = __syncthreads_and(tid == 0 ? mbar_wait(&bar_mma[1], it & 1, nullptr, p.wait_ns) : true);
         tc_fence_after();
         if (!ok) break;
         stall_point<kStall>(p.stall_seed, 11, it);
@@ -566,7 +567,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                           idesc_bf16_f32_bmn(128, 256), k > 0 ? 1u : 0u);
             umma_commit(&bar_mma[2]);
         }
-        ok = __syncthreads_and(tid == 0 ? mbar_wait(&bar_mma[2], it & 1, nullptr) : true);
+        ok = __syncthreads_and(tid == 0 ? mbar_wait(&bar_mma[2], it & 1, nullptr, p.wait_ns) : true);
         tc_fence_after();
         if (!ok) break;
         stall_point<kStall>(p.stall_seed, 12, it);
@@ -631,7 +632,13 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         rec = rec_next;
         ci = cn;
     }
-    if (!ok && tid == 0) atomicExch(p.status, 4);
+    if (!ok && tid == 0) {
+        atomicExch(p.status, 4);
+        // A working wait ran out: every product issued so far completes before
+        // the CTA lets go of TMEM and shared memory (bounded).
+        umma_commit(&bar_fin);
+        mbar_wait(&bar_fin, 0, nullptr);
+    }
     if (tid == 0) bulk_wait_all();  // no bulk store may outlive the CTA's shared memory
     // Never leave with a copy in flight (only possible after a failed wait).
     if (pend_parity >= 0 && tid == 0) mbar_wait(&bar_in, (uint32_t)pend_parity, nullptr);
@@ -731,9 +738,9 @@ cudaError_t launch_prep(const PrefillParams& p, const PrepMaps& maps, int num_sm
     const long long recs = (long long)p.max_chunks * p.H;
     if (recs == 0) return cudaSuccess;
     // the instantiation with the stall hook runs only when a test asks for it
+    static std::atomic<uint64_t> smem_set[2];
     auto kern = p.stall_seed ? prep_kernel<true> : prep_kernel<false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kPrepSmem);
+    cudaError_t e = set_smem_limit_once((const void*)kern, (int)kPrepSmem, smem_set[p.stall_seed ? 1 : 0]);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)(recs < num_sms ? recs : num_sms);
     if (!overlap_previous) {

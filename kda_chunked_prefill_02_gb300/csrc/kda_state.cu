@@ -51,8 +51,9 @@ constexpr uint32_t kRowGroup = 1024;
 constexpr uint32_t TM_D1 = 0, TM_D2 = 32, TM_COLS = 64;
 constexpr uint32_t kBarVn = 1, kBarChunk = 2, kBarOut = 3;  // named barriers (0 is __syncthreads)
 
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
-    const bool ok = mbar_wait(bar, parity, abort);
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns) {
+    const bool ok = mbar_wait(bar, parity, abort, limit_ns);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -112,7 +113,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
             int issued = 0;
             for (int c = 0; c < count; ++c) {
                 const int st = c % kStages;
-                if (c >= kStages && !mbar_wait(&empty[st], ((c / kStages) - 1) & 1, abort)) { fail(); break; }
+                if (c >= kStages && !mbar_wait(&empty[st], ((c / kStages) - 1) & 1, abort, p.wait_ns)) { fail(); break; }
                 stall_point<kStall>(p.stall_seed, 1, c);
                 uint8_t* sb = sm + st * kStage;
                 const uint8_t* rp = p.ws_rec + (size_t)((first + c) * p.H + h) * kRecBytes;
@@ -176,7 +177,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
             const int st = c % kStages;
             const uint8_t* sb = sm + st * kStage;
             const uint32_t sb_addr = smem_u32(sb);
-            bool ok = warp_wait(&full[st], (c / kStages) & 1, abort);
+            bool ok = warp_wait(&full[st], (c / kStages) & 1, abort, p.wait_ns);
             stall_point<kStall>(p.stall_seed, 2, c);
             if (issuer && ok) {
                 tc_fence_after();
@@ -199,7 +200,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
                 for (int ch = 0; ch < 4; ++ch)
                     slab_row[ch] = *reinterpret_cast<const uint4*>(src + slab_chunk_off(r, ch));
             }
-            ok = ok && warp_wait(&p1_done, c & 1, abort);
+            ok = ok && warp_wait(&p1_done, c & 1, abort, p.wait_ns);
             tc_fence_after();
             float d[kSlab];
             if (ok) {
@@ -281,7 +282,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
                 }
                 tc_fence_before();
             }
-            ok = ok && warp_wait(&p2_done, c & 1, abort);
+            ok = ok && warp_wait(&p2_done, c & 1, abort, p.wait_ns);
             tc_fence_after();
             if (ok) {
                 tmem_ld32(tb + lane_base + TM_D2, d);
@@ -323,9 +324,9 @@ __global__ void __launch_bounds__(kStateThreads, 1)
 
 cudaError_t launch_state(const PrefillParams& p, const CUtensorMap& out_map, cudaStream_t s) {
     if (p.N == 0 || p.H == 0) return cudaSuccess;
+    static std::atomic<uint64_t> smem_set[2];
     auto kern = p.stall_seed ? state_kernel<true> : state_kernel<false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kStateSmem);
+    cudaError_t e = set_smem_limit_once((const void*)kern, (int)kStateSmem, smem_set[p.stall_seed ? 1 : 0]);
     if (e != cudaSuccess) return e;
     dim3 grid(kHeadDim / kSlab, p.H, p.N);
     kern<<<grid, kStateThreads, kStateSmem, s>>>(p, out_map);

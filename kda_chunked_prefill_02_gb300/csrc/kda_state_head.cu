@@ -62,8 +62,9 @@ __device__ __forceinline__ float sigmoid_fast(float x) {
     return fmaf(0.5f, t, 0.5f);
 }
 
-__device__ __forceinline__ bool warp_wait_h(uint64_t* bar, uint32_t parity, volatile int* abort) {
-    const bool ok = mbar_wait(bar, parity, abort);
+__device__ __forceinline__ bool warp_wait_h(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                            uint64_t limit_ns) {
+    const bool ok = mbar_wait(bar, parity, abort, limit_ns);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -181,7 +182,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
             const int st = c % kHStages;
             const uint8_t* sb = sm + st * kHStage;
             const uint32_t sb_addr = smem_u32(sb);
-            bool ok = warp_wait_h(&full[st], (c / kHStages) & 1, abort);
+            bool ok = warp_wait_h(&full[st], (c / kHStages) & 1, abort, p.wait_ns);
             stall_point<kStall>(p.stall_seed, 1, c);
             if (issuer && ok) {
                 tc_fence_after();
@@ -202,7 +203,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch) sr[ch] = *reinterpret_cast<const uint4*>(src + slab_chunk_off(r, ch));
             }
-            ok = ok && warp_wait_h(&p1_done, c & 1, abort);
+            ok = ok && warp_wait_h(&p1_done, c & 1, abort, p.wait_ns);
             tc_fence_after();
             float d[kSlab];
             if (ok) {
@@ -319,7 +320,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
                 }
                 tc_fence_before();
             }
-            ok = ok && warp_wait_h(&p2_done, c & 1, abort);
+            ok = ok && warp_wait_h(&p2_done, c & 1, abort, p.wait_ns);
             tc_fence_after();
             if (ok) {
                 tmem_ld32(tb + lane_base + TMH_D2 + kSlab * cq, d);
@@ -375,9 +376,9 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
 
 cudaError_t launch_state_head(const PrefillParams& p, const CUtensorMap& out_map, cudaStream_t s) {
     if (p.N == 0 || p.H == 0) return cudaSuccess;
+    static std::atomic<uint64_t> smem_set[2];
     auto kern = p.stall_seed ? state_head_kernel<true> : state_head_kernel<false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kHeadSmem);
+    cudaError_t e = set_smem_limit_once((const void*)kern, (int)kHeadSmem, smem_set[p.stall_seed ? 1 : 0]);
     if (e != cudaSuccess) return e;
     dim3 grid(p.H, p.N);
     kern<<<grid, kHeadThreads, kHeadSmem, s>>>(p, out_map);

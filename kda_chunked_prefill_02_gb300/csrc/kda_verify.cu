@@ -284,9 +284,11 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyP
 
 template <bool kBf16, bool kStall>
 cudaError_t launch_verify_t(const VerifyParams& p, int num_sms, cudaStream_t s) {
+    // the limit is set once per device for the largest draft count
+    constexpr size_t kSmemMax = (size_t)kHeadDim * kHeadDim * (kBf16 ? 2 : 4) + 2 * (size_t)kMaxDrafts * kTokBytes;
+    static std::atomic<uint64_t> smem_set;
     const size_t smem = (size_t)kHeadDim * kHeadDim * (kBf16 ? 2 : 4) + 2 * (size_t)p.D * kTokBytes;
-    cudaError_t e = cudaFuncSetAttribute(verify_kernel<kBf16, kStall>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    cudaError_t e = set_smem_limit_once((const void*)verify_kernel<kBf16, kStall>, (int)kSmemMax, smem_set);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, verify_kernel<kBf16, kStall>, kVerifyThreads, smem);

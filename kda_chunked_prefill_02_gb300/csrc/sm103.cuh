@@ -60,15 +60,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Returns false if the
-// wait ran past kWaitLimitNs or if *abort (shared flag) became non-zero.
+// wait ran past limit_ns or if *abort (shared flag) became non-zero.  The
+// kernels' working waits take the call's limit (kWaitLimitNs unless a test
+// lowers it); the waits of a wind-down, for copies and products still in
+// flight, always take kWaitLimitNs.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          const volatile int* abort) {
+                                          const volatile int* abort,
+                                          uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (abort && *abort) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
 

@@ -6,6 +6,8 @@ and the workspace through torch (the library itself allocates nothing), and
 raises on any status other than KDA_OK.  There is no fallback: if the library
 is missing or a tensor is not on a CUDA device, the call fails.
 """
+import contextlib
+import contextvars
 import ctypes
 import os
 
@@ -23,6 +25,48 @@ _i64 = ctypes.c_int64
 _i64x3 = ctypes.c_int64 * 3
 
 
+class Overrides(ctypes.Structure):
+    """kda_overrides: test and measurement overrides of the library's choices."""
+    _fields_ = [("state_kernel", ctypes.c_int32), ("segment_chunks", ctypes.c_int32),
+                ("prep_ctas", ctypes.c_int32), ("no_pdl", ctypes.c_int32),
+                ("stall_seed", ctypes.c_uint32), ("reserved0", ctypes.c_int32),
+                ("wait_limit_ns", ctypes.c_int64)]
+
+
+_STATE_KERNELS = {None: 0, "slab": 1, "head": 2}
+_overrides_var = contextvars.ContextVar("kda_overrides", default=None)
+
+
+def _make_overrides(state_kernel=None, segment_chunks=None, prep_ctas=None, no_pdl=False,
+                    stall_seed=0, wait_limit_ns=0):
+    o = Overrides()
+    o.state_kernel = _STATE_KERNELS[state_kernel]
+    o.segment_chunks = -1 if segment_chunks is None else int(segment_chunks)
+    o.prep_ctas = int(prep_ctas or 0)
+    o.no_pdl = 1 if no_pdl else 0
+    o.stall_seed = int(stall_seed or 0)
+    o.wait_limit_ns = int(wait_limit_ns or 0)
+    return o
+
+
+@contextlib.contextmanager
+def overrides(**kw):
+    """Within the block, calls of this module pass these kda_overrides to the
+    library (tests and measurements): state_kernel ("slab" | "head"),
+    segment_chunks (0: never segment, n: segments of n chunks), prep_ctas,
+    no_pdl, stall_seed, wait_limit_ns.  Nothing is taken from the environment."""
+    tok = _overrides_var.set(_make_overrides(**kw))
+    try:
+        yield
+    finally:
+        _overrides_var.reset(tok)
+
+
+def _current_overrides():
+    o = _overrides_var.get()
+    return None if o is None else ctypes.pointer(o)
+
+
 class PrefillArgs(ctypes.Structure):
     _fields_ = [("q", _p), ("k", _p), ("v", _p), ("g", _p), ("beta", _p), ("out", _p),
                 ("q_stride", _i64x3), ("k_stride", _i64x3), ("v_stride", _i64x3),
@@ -34,7 +78,8 @@ class PrefillArgs(ctypes.Structure):
                 ("scale", ctypes.c_float),
                 ("workspace", _p), ("workspace_bytes", ctypes.c_size_t),
                 ("device_status", _p), ("out_gate", _p), ("gate_stride", _i64x3),
-                ("norm_weight", _p), ("norm_eps", ctypes.c_float)]
+                ("norm_weight", _p), ("norm_eps", ctypes.c_float),
+                ("overrides", ctypes.POINTER(Overrides))]
 
 
 class PrefillHostArgs(ctypes.Structure):
@@ -51,7 +96,7 @@ class VerifyArgs(ctypes.Structure):
                 ("head_dim_k", _i64), ("head_dim_v", _i64),
                 ("beta_is_logit", ctypes.c_int32), ("scale", ctypes.c_float),
                 ("device_status", _p), ("pool_dtype", ctypes.c_int32),
-                ("replay_only", ctypes.c_int32)]
+                ("replay_only", ctypes.c_int32), ("overrides", ctypes.POINTER(Overrides))]
 
 
 KDA_POOL_F32, KDA_POOL_BF16 = 0, 1
@@ -125,6 +170,14 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+def _on_stream(stream, like):
+    """Context in which torch allocations belong to `stream` (None or a CPU
+    tensor: the current stream)."""
+    if stream is None or not getattr(like, "is_cuda", False):
+        return contextlib.nullcontext()
+    return torch.cuda.stream(stream)
+
+
 def _stream_handle(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -192,10 +245,13 @@ def _prefill_args(q, k, v, g, beta, initial_state, cu_seqlens, out, final_state,
     if out_gate is not None or norm_weight is not None:
         _need_cuda("out_gate", out_gate, torch.bfloat16)
         _need_cuda("norm_weight", norm_weight, torch.float32)
+        if norm_weight is None or not norm_weight.is_contiguous():
+            raise ValueError("norm_weight must be a contiguous fp32 [128] CUDA tensor")
         a.out_gate = _ptr(out_gate)
         a.gate_stride = _i64x3(*_strides3(out_gate, varlen))
-        a.norm_weight = _ptr(norm_weight.contiguous())
+        a.norm_weight = _ptr(norm_weight)
         a.norm_eps = float(norm_eps)
+    a.overrides = _current_overrides()
     return a
 
 
@@ -239,6 +295,7 @@ def prefill_schedule(q, *, cu_seqlens=None, norm=False, num_sms=None):
         a.out_gate = ctypes.c_void_p(1)
     if num_sms is None:
         num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    a.overrides = _current_overrides()
     sch = Schedule()
     _check(lib().kda_prefill_schedule(ctypes.byref(a), int(num_sms), ctypes.byref(sch)))
     return dict(segmented=bool(sch.segmented), whole_chain=bool(sch.whole_chain),
@@ -261,14 +318,18 @@ def kda_prefill(q, k, v, g, beta, *, initial_state=None, cu_seqlens=None, chunk=
     """
     N = (cu_seqlens.shape[0] - 1) if cu_seqlens is not None else q.shape[0]
     H = q.shape[-2]
-    if out is None:
-        out = torch.empty(v.shape, dtype=torch.bfloat16, device=v.device)
-    if final_state is None and output_final_state and not prep_only:
-        final_state = torch.empty((N, H, q.shape[-1], v.shape[-1]), dtype=torch.float32,
-                                  device=q.device)
-    if workspace is None:
-        nbytes = workspace_size(q, v, cu_seqlens=cu_seqlens)
-        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    # Tensors made here belong to the stream the kernels run on, so that the
+    # caching allocator cannot hand their memory to other work while the
+    # call's kernels still use it.
+    with _on_stream(stream, q):
+        if out is None:
+            out = torch.empty(v.shape, dtype=torch.bfloat16, device=v.device)
+        if final_state is None and output_final_state and not prep_only:
+            final_state = torch.empty((N, H, q.shape[-1], v.shape[-1]), dtype=torch.float32,
+                                      device=q.device)
+        if workspace is None:
+            nbytes = workspace_size(q, v, cu_seqlens=cu_seqlens)
+            workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
     a = _prefill_args(q, k, v, g, beta, initial_state, cu_seqlens, out, final_state,
                       beta_is_logit, scale, workspace, device_status, chunk, out_gate, norm_weight,
                       norm_eps)
@@ -302,7 +363,8 @@ def kda_verify(q, k, v, g, beta, state_pool, accepted, *, slot=None, beta_is_log
     if not state_pool.is_contiguous():
         raise ValueError("state_pool must be contiguous [P, H, 128, 128]")
     if out is None and not replay_only:
-        out = torch.empty(v.shape, dtype=torch.bfloat16, device=v.device)
+        with _on_stream(stream, v):
+            out = torch.empty(v.shape, dtype=torch.bfloat16, device=v.device)
     if out is not None:
         _need_cuda("out", out, torch.bfloat16)
     a = VerifyArgs()
@@ -324,6 +386,7 @@ def kda_verify(q, k, v, g, beta, state_pool, accepted, *, slot=None, beta_is_log
     a.beta_is_logit = 1 if beta_is_logit else 0
     a.scale = float(scale)
     a.device_status = _ptr(device_status)
+    a.overrides = _current_overrides()
     _check(lib().kda_verify(ctypes.byref(a), _stream_handle(stream)))
     return out
 
@@ -343,11 +406,12 @@ def kda_prefill_noalloc(q, k, v, g, beta, *, initial_state=None, cu_seqlens=None
     f.restype = ctypes.c_int
     f.argtypes = [ctypes.POINTER(PrefillArgs), _p]
     N = (cu_seqlens.shape[0] - 1) if cu_seqlens is not None else q.shape[0]
-    if out is None:
-        out = torch.empty(v.shape, dtype=torch.bfloat16, device=v.device)
-    if final_state is None:
-        final_state = torch.empty((N, q.shape[-2], q.shape[-1], v.shape[-1]),
-                                  dtype=torch.float32, device=q.device)
+    with _on_stream(stream, q):
+        if out is None:
+            out = torch.empty(v.shape, dtype=torch.bfloat16, device=v.device)
+        if final_state is None:
+            final_state = torch.empty((N, q.shape[-2], q.shape[-1], v.shape[-1]),
+                                      dtype=torch.float32, device=q.device)
     a = _prefill_args(q, k, v, g, beta, initial_state, cu_seqlens, out, final_state,
                       beta_is_logit, scale, None, device_status, chunk)
     _check(f(ctypes.byref(a), _stream_handle(stream)))
@@ -411,7 +475,8 @@ def kda_prefill_host(q, k, v, g, beta, *, initial_state=None, cu_seqlens=None, c
         final_state = torch.empty((N, H, q.shape[-1], v.shape[-1]), dtype=torch.float32, pin_memory=True)
     if staging is None:
         nbytes = host_staging_size(q, v, cu_seqlens=cu_seqlens, piece_tokens=piece_tokens)
-        staging = torch.empty(max(nbytes, 1), dtype=torch.uint8, device="cuda")
+        with (torch.cuda.stream(stream) if stream is not None else contextlib.nullcontext()):
+            staging = torch.empty(max(nbytes, 1), dtype=torch.uint8, device="cuda")
     h = _host_args(q, k, v, g, beta, initial_state, cu_seqlens, out, final_state, beta_is_logit,
                    scale, chunk, staging, piece_tokens)
     _check(lib().kda_prefill_host(ctypes.byref(h), _stream_handle(stream)))

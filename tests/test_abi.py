@@ -33,7 +33,7 @@ def test_exports_every_declared_symbol(K):
             "kda_status_string"} <= names
     for n in sorted(names):
         assert hasattr(lib, n), n
-    assert lib.kda_abi_version() == 4
+    assert lib.kda_abi_version() == 5
 
 
 def _args(K, **kw):
@@ -154,6 +154,7 @@ def test_verify_refuses_rows_it_cannot_move_in_16_byte_pieces(K):
 
 def _sched(K, num_sms=152, **kw):
     a = _args(K, **kw)
+    a.overrides = K._current_overrides()
     s = K.Schedule()
     assert K.lib().kda_prefill_schedule(ctypes.byref(a), num_sms, ctypes.byref(s)) == 0
     return (s.segmented, s.whole_chain, s.segment_chunks, s.prep_ctas)
@@ -161,9 +162,13 @@ def _sched(K, num_sms=152, **kw):
 
 def test_prefill_schedule(K, monkeypatch):
     """Host-side schedule choice (no GPU call): segments only for few long
-    padded chains, with the state kernel that leaves prep the most SMs."""
-    monkeypatch.delenv("KDA_SEGMENT_CHUNKS", raising=False)
-    monkeypatch.delenv("KDA_STATE_KERNEL", raising=False)
+    padded chains, with the state kernel that leaves prep the most SMs.  The
+    process environment plays no part (the names earlier builds read are set
+    here to values that would change the schedule); only the call's overrides
+    do."""
+    monkeypatch.setenv("KDA_SEGMENT_CHUNKS", "3")
+    monkeypatch.setenv("KDA_STATE_KERNEL", "slab")
+    monkeypatch.setenv("KDA_STALL_INJECT", "7")
     # 32 chains of 2048 chunks: whole-chain state CTAs on 32 SMs, prep on 120,
     # 56-chunk segments
     assert _sched(K, batch=1, num_seqs=1, seqlen=131072, num_heads=32) == (1, 1, 56, 120)
@@ -187,12 +192,22 @@ def test_prefill_schedule(K, monkeypatch):
     assert _sched(K, batch=1, num_seqs=1, seqlen=131072, num_heads=32,
                   out_gate=ctypes.c_void_p(1))[1] == 1
     # overrides
-    monkeypatch.setenv("KDA_SEGMENT_CHUNKS", "0")
-    assert _sched(K, batch=1, num_seqs=1, seqlen=131072, num_heads=32)[0] == 0
-    monkeypatch.setenv("KDA_SEGMENT_CHUNKS", "3")
-    assert _sched(K, batch=1, num_seqs=1, seqlen=256, num_heads=2) == (1, 0, 3, 144)
-    monkeypatch.setenv("KDA_STATE_KERNEL", "head")
-    assert _sched(K, batch=1, num_seqs=1, seqlen=256, num_heads=2) == (1, 1, 3, 150)
+    with K.overrides(segment_chunks=0):
+        assert _sched(K, batch=1, num_seqs=1, seqlen=131072, num_heads=32)[0] == 0
+    with K.overrides(segment_chunks=3):
+        assert _sched(K, batch=1, num_seqs=1, seqlen=256, num_heads=2) == (1, 0, 3, 144)
+    with K.overrides(segment_chunks=3, state_kernel="head"):
+        assert _sched(K, batch=1, num_seqs=1, seqlen=256, num_heads=2) == (1, 1, 3, 150)
+    with K.overrides(segment_chunks=3, prep_ctas=40):
+        assert _sched(K, batch=1, num_seqs=1, seqlen=256, num_heads=2) == (1, 0, 3, 40)
+    with K.overrides(state_kernel="head"):
+        assert _sched(K, batch=1, num_seqs=1, seqlen=4096, num_heads=2) == (0, 1, 0, 152)
+    # overrides with the reserved field set are refused
+    a = _args(K, batch=1, num_seqs=1, seqlen=256, num_heads=2)
+    o = K._make_overrides()
+    o.reserved0 = 1
+    a.overrides = ctypes.pointer(o)
+    assert K.lib().kda_prefill(ctypes.byref(a), None) == K.KDA_ERR_INVALID_ARG
     a = _args(K)
     assert K.lib().kda_prefill_schedule(ctypes.byref(a), 0, ctypes.byref(K.Schedule())) == \
         K.KDA_ERR_INVALID_ARG
@@ -273,3 +288,33 @@ def test_noalloc_capacity_as_documented(K):
                                          torch.empty(1, T, H, 128, dtype=torch.bfloat16))
     assert size(2048, 12) <= lim < size(2048, 13)
     assert size(8192, 3) <= lim < size(8192, 4)
+
+
+def test_noalloc_checks_arguments_before_the_size(K):
+    """kda_prefill_noalloc runs kda_prefill's argument checks first: a bad
+    argument comes back as KDA_ERR_INVALID_ARG / KDA_ERR_UNSUPPORTED exactly as
+    from kda_prefill (never as an oversize problem), dimensions whose sizes
+    would wrap size_t are refused, and a well-formed problem past the scratch
+    is KDA_ERR_UNSUPPORTED.  All before any CUDA call."""
+    lib = K.lib()
+    f = lib.kda_prefill_noalloc
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.POINTER(K.PrefillArgs), ctypes.c_void_p]
+    run = lambda a: f(ctypes.byref(a), None)
+    assert run(_args(K, num_seqs=-1)) == K.KDA_ERR_INVALID_ARG
+    assert run(_args(K, batch=-3, num_seqs=-3)) == K.KDA_ERR_INVALID_ARG
+    assert run(_args(K, num_heads=0)) == K.KDA_ERR_INVALID_ARG
+    assert run(_args(K, chunk=32)) == K.KDA_ERR_UNSUPPORTED
+    assert run(_args(K, q=None)) == K.KDA_ERR_INVALID_ARG
+    assert f(None, None) == K.KDA_ERR_INVALID_ARG
+    # well formed but larger than the scratch (2048 tokens x 13 heads)
+    assert run(_args(K, seqlen=2048, num_heads=13)) == K.KDA_ERR_UNSUPPORTED
+    # sizes that would overflow the workspace plan are refused, not wrapped
+    huge = _args(K, cu_seqlens=ctypes.c_void_p(1 << 12), batch=1, num_seqs=60000,
+                 seqlen=(1 << 31) - 1, num_heads=60000)
+    assert run(huge) != K.KDA_OK
+    assert lib.kda_prefill_workspace_size(ctypes.byref(huge)) > 0   # representable here
+    L = K.WorkspaceLayout()
+    big = _args(K, batch=1 << 41, num_seqs=1 << 41, seqlen=1 << 30, num_heads=1 << 20)
+    assert lib.kda_prefill_workspace_size(ctypes.byref(big)) == 0
+    assert lib.kda_prefill_workspace_layout(ctypes.byref(big), ctypes.byref(L)) == K.KDA_ERR_INVALID_ARG

@@ -72,20 +72,12 @@ def test_host_pieces_take_the_segmented_schedule(piece):
     (8192) schedule, all with the whole-chain state kernel, the state passing
     between segments and between pieces exactly, so both give the same bits;
     two heads are checked against the oracle."""
-    import os
     from kda_test_util import head_subset
     import kda_chunked_prefill_02_gb300 as K
     inp = inputs.prefill_inputs(403, B=1, T=16384, H=32)
-    old = os.environ.get("KDA_STATE_KERNEL")
-    os.environ["KDA_STATE_KERNEL"] = "head"
-    try:
+    with K.overrides(state_kernel="head"):
         assert K.prefill_schedule(inp.q, num_sms=152)["segmented"]
         ref_out, ref_fin, out, fin = _both(inp, piece)
-    finally:
-        if old is None:
-            del os.environ["KDA_STATE_KERNEL"]
-        else:
-            os.environ["KDA_STATE_KERNEL"] = old
     assert torch.equal(out, ref_out)
     assert torch.equal(fin, ref_fin)
     sub = head_subset(inp, [0, 31])

@@ -1,13 +1,11 @@
 """GPU parity of the segmented schedule of padded calls: the tokens are cut into
 segments, the state pass of one segment runs on a second stream beside the
 prep of the next, and every chain's state passes between segments in fp32
-through the workspace.  Forced with KDA_SEGMENT_CHUNKS on small shapes: bit
+through the workspace.  Forced through the call's overrides on small shapes: bit
 for bit equal to the one-pass call with the same state kernel (the chunk steps
 are the same, the state crosses a segment boundary exactly), and within the
 tolerances of the fp64 oracle.  The long workload at full size takes this
 schedule by default (test_gpu_prefill.test_full_size_configs)."""
-import os
-
 import pytest
 import torch
 
@@ -15,26 +13,6 @@ from kda_chunked_prefill_02_gb300 import inputs
 from kda_test_util import assert_parity, oracle_prefill, rel_fro, to_np
 
 pytestmark = pytest.mark.gpu
-
-
-class _env:
-    def __init__(self, **kv):
-        self.kv = kv
-
-    def __enter__(self):
-        self.old = {k: os.environ.get(k) for k in self.kv}
-        for k, v in self.kv.items():
-            if v is None:
-                os.environ.pop(k, None)
-            else:
-                os.environ[k] = str(v)
-
-    def __exit__(self, *exc):
-        for k, v in self.old.items():
-            if v is None:
-                os.environ.pop(k, None)
-            else:
-                os.environ[k] = v
 
 
 def _run(d, **kw):
@@ -57,12 +35,12 @@ def test_segments_equal_one_pass(kernel, case, seg):
     import kda_chunked_prefill_02_gb300 as K
     inp = inputs.prefill_inputs(800 + seg + case["T"], **case)
     d = inp.to("cuda")
-    with _env(KDA_STATE_KERNEL=kernel, KDA_SEGMENT_CHUNKS=seg):
+    with K.overrides(state_kernel=kernel, segment_chunks=seg):
         sch = K.prefill_schedule(d.q)
         assert sch["segmented"] and sch["segment_chunks"] == min(seg, -(-case["T"] // 64))
         assert sch["whole_chain"] == (kernel == "head")
         out_s, fin_s = _run(d)
-    with _env(KDA_STATE_KERNEL=kernel, KDA_SEGMENT_CHUNKS=0):
+    with K.overrides(state_kernel=kernel, segment_chunks=0):
         assert not K.prefill_schedule(d.q)["segmented"]
         out_1, fin_1 = _run(d)
     assert torch.equal(out_s, out_1) and torch.equal(fin_s, fin_1)
@@ -78,7 +56,7 @@ def test_segments_in_place_state():
     d = inp.to("cuda")
     ro, rf = oracle_prefill(inp)
     st = d.initial_state.clone()
-    with _env(KDA_SEGMENT_CHUNKS=2, KDA_STATE_KERNEL=None):
+    with K.overrides(segment_chunks=2):
         out, fin = K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, initial_state=st, final_state=st)
         torch.cuda.synchronize()
     assert fin.data_ptr() == st.data_ptr()
@@ -96,10 +74,10 @@ def test_segments_with_fused_norm():
     w = (torch.rand(128, generator=gen) + 0.5).float()
     d = inp.to("cuda")
     kw = dict(out_gate=gate.cuda(), norm_weight=w.cuda(), norm_eps=1e-6)
-    with _env(KDA_SEGMENT_CHUNKS=2, KDA_STATE_KERNEL=None):
+    with K.overrides(segment_chunks=2):
         assert K.prefill_schedule(d.q, norm=True)["whole_chain"]
         out_s, fin_s = _run(d, **kw)
-    with _env(KDA_SEGMENT_CHUNKS=0, KDA_STATE_KERNEL=None):
+    with K.overrides(segment_chunks=0):
         out_1, fin_1 = _run(d, **kw)
     assert torch.equal(out_s, out_1) and torch.equal(fin_s, fin_1)
     ro, rf = oracle_prefill(inp)
@@ -126,10 +104,10 @@ def test_segments_strided_views():
     b[:, :, 0:3:2] = d.beta
     beta = b[:, :, 0:3:2]
     assert not q.is_contiguous()
-    with _env(KDA_SEGMENT_CHUNKS=1, KDA_STATE_KERNEL=None):
+    with K.overrides(segment_chunks=1):
         out_s, fin_s = K.kda_prefill(q, k, v, g, beta, initial_state=d.initial_state)
         torch.cuda.synchronize()
-    with _env(KDA_SEGMENT_CHUNKS=0, KDA_STATE_KERNEL=None):
+    with K.overrides(segment_chunks=0):
         out_1, fin_1 = K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, initial_state=d.initial_state)
         torch.cuda.synchronize()
     assert torch.equal(out_s, out_1) and torch.equal(fin_s, fin_1)
@@ -141,7 +119,7 @@ def test_default_schedule_of_the_long_workload():
     full-size parity test then runs it."""
     import kda_chunked_prefill_02_gb300 as K
     q = torch.empty(1, 131072, 32, 128, dtype=torch.bfloat16, device="meta")
-    with _env(KDA_SEGMENT_CHUNKS=None, KDA_STATE_KERNEL=None):
+    with K.overrides():
         sch = K.prefill_schedule(q)
     if torch.cuda.get_device_properties(0).multi_processor_count != 152:
         pytest.skip("schedule constants are for 152 SMs")
@@ -153,9 +131,9 @@ def test_segments_without_programmatic_launch():
     one after the other; same bits as with the programmatic launch."""
     inp = inputs.prefill_inputs(855, B=1, T=64 * 11 + 3, H=3)
     d = inp.to("cuda")
-    with _env(KDA_SEGMENT_CHUNKS=2, KDA_STATE_KERNEL=None, KDA_SEGMENT_PDL=None):
+    with K.overrides(segment_chunks=2):
         a = _run(d)
-    with _env(KDA_SEGMENT_CHUNKS=2, KDA_STATE_KERNEL=None, KDA_SEGMENT_PDL=0):
+    with K.overrides(segment_chunks=2, no_pdl=True):
         b = _run(d)
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
@@ -169,7 +147,7 @@ def test_output_tensor_store_into_strided_out(kernel, seg):
     import kda_chunked_prefill_02_gb300 as K
     inp = inputs.prefill_inputs(856, B=2, T=64 * 4 + 9, H=3)
     d = inp.to("cuda")
-    with _env(KDA_STATE_KERNEL=kernel, KDA_SEGMENT_CHUNKS=seg):
+    with K.overrides(state_kernel=kernel, segment_chunks=seg):
         ref, _ = K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, initial_state=d.initial_state)
         big = torch.full(d.v.shape[:-1] + (128 + 24,), 7.0, dtype=torch.bfloat16, device="cuda")
         out = big[..., :128]
@@ -189,7 +167,7 @@ def test_segmented_call_in_a_cuda_graph():
     ws = torch.empty(K.workspace_size(d.q, d.v), dtype=torch.uint8, device="cuda")
     out = torch.empty_like(d.v)
     fin = torch.empty_like(d.initial_state)
-    with _env(KDA_SEGMENT_CHUNKS=2, KDA_STATE_KERNEL=None):
+    with K.overrides(segment_chunks=2):
         s = torch.cuda.Stream()
         with torch.cuda.stream(s):
             K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, initial_state=d.initial_state, out=out,
@@ -216,11 +194,11 @@ def test_segments_without_final_state():
     import kda_chunked_prefill_02_gb300 as K
     inp = inputs.prefill_inputs(858, B=2, T=64 * 5 + 3, H=2)
     d = inp.to("cuda")
-    with _env(KDA_SEGMENT_CHUNKS=2, KDA_STATE_KERNEL=None):
+    with K.overrides(segment_chunks=2):
         out_s, fin_s = K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, initial_state=d.initial_state,
                                      output_final_state=False)
         torch.cuda.synchronize()
-    with _env(KDA_SEGMENT_CHUNKS=0, KDA_STATE_KERNEL=None):
+    with K.overrides(segment_chunks=0):
         out_1, _ = K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, initial_state=d.initial_state)
         torch.cuda.synchronize()
     assert fin_s is None

@@ -1,6 +1,6 @@
 """Bit-identical results under injected warp stalls.
 
-KDA_STALL_INJECT=<seed> launches the kernel instantiations with the stall hook:
+An overrides stall_seed launches the kernel instantiations with the stall hook:
 at every injection site (before and after each barrier, mbarrier wait,
 tensor-core issue, copy issue and hand-off of the prep, state and verify
 kernels) a quarter of the warps, chosen by a hash of the seed, block, warp, site
@@ -9,8 +9,6 @@ output, final state, workspace record and verify pool must equal the
 unperturbed run's bit for bit; a missing barrier or a buffer reused too early
 would show as a difference.  Each case also runs twice without stalls (the
 plain run is deterministic)."""
-import os
-
 import pytest
 import torch
 
@@ -21,31 +19,11 @@ pytestmark = pytest.mark.gpu
 SEEDS = (1, 2, 3)
 
 
-class _env:
-    def __init__(self, **kv):
-        self.kv = kv
-
-    def __enter__(self):
-        self.old = {k: os.environ.get(k) for k in self.kv}
-        for k, v in self.kv.items():
-            if v is None:
-                os.environ.pop(k, None)
-            else:
-                os.environ[k] = str(v)
-
-    def __exit__(self, *exc):
-        for k, v in self.old.items():
-            if v is None:
-                os.environ.pop(k, None)
-            else:
-                os.environ[k] = v
-
-
-def _prefill(d, seed, **env):
+def _prefill(d, seed, **over):
     import kda_chunked_prefill_02_gb300 as K
     ws = torch.full((K.workspace_size(d.q, d.v, cu_seqlens=d.cu_seqlens),), 0xFF, dtype=torch.uint8,
                     device="cuda")
-    with _env(KDA_STALL_INJECT=seed or None, **env):
+    with K.overrides(stall_seed=seed or 0, **over):
         out, fin = K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, initial_state=d.initial_state,
                                  cu_seqlens=d.cu_seqlens, workspace=ws)
         torch.cuda.synchronize()
@@ -62,10 +40,10 @@ def _same(a, b):
 def test_prefill_bit_identical_under_stalls(kernel, case):
     inp = inputs.prefill_inputs(900 + len(case), **case)
     d = inp.to("cuda")
-    ref = _prefill(d, 0, KDA_STATE_KERNEL=kernel, KDA_SEGMENT_CHUNKS=0)
-    assert _same(ref, _prefill(d, 0, KDA_STATE_KERNEL=kernel, KDA_SEGMENT_CHUNKS=0))
+    ref = _prefill(d, 0, state_kernel=kernel, segment_chunks=0)
+    assert _same(ref, _prefill(d, 0, state_kernel=kernel, segment_chunks=0))
     for seed in SEEDS:
-        got = _prefill(d, seed, KDA_STATE_KERNEL=kernel, KDA_SEGMENT_CHUNKS=0)
+        got = _prefill(d, seed, state_kernel=kernel, segment_chunks=0)
         assert _same(ref, got), "seed %d changed the result" % seed
 
 
@@ -74,9 +52,9 @@ def test_segmented_bit_identical_under_stalls():
     segments, with stalls in both kernels."""
     inp = inputs.prefill_inputs(910, B=1, T=64 * 9 + 3, H=4)
     d = inp.to("cuda")
-    ref = _prefill(d, 0, KDA_STATE_KERNEL=None, KDA_SEGMENT_CHUNKS=2)
+    ref = _prefill(d, 0, segment_chunks=2)
     for seed in SEEDS:
-        assert _same(ref, _prefill(d, seed, KDA_STATE_KERNEL=None, KDA_SEGMENT_CHUNKS=2)), seed
+        assert _same(ref, _prefill(d, seed, segment_chunks=2)), seed
 
 
 def test_prep_records_bit_identical_under_stalls():
@@ -88,7 +66,7 @@ def test_prep_records_bit_identical_under_stalls():
     def records(seed):
         ws = torch.full((K.workspace_size(d.q, d.v, cu_seqlens=d.cu_seqlens),), 0xFF,
                         dtype=torch.uint8, device="cuda")
-        with _env(KDA_STALL_INJECT=seed or None):
+        with K.overrides(stall_seed=seed or 0):
             K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, initial_state=d.initial_state,
                           cu_seqlens=d.cu_seqlens, workspace=ws, stage="prep")
             torch.cuda.synchronize()
@@ -110,7 +88,7 @@ def test_norm_bit_identical_under_stalls():
     w = (torch.rand(128, generator=gen) + 0.5).float().cuda()
 
     def run(seed):
-        with _env(KDA_STALL_INJECT=seed or None):
+        with K.overrides(stall_seed=seed or 0):
             out, fin = K.kda_prefill(d.q, d.k, d.v, d.g, d.beta, initial_state=d.initial_state,
                                      out_gate=gate, norm_weight=w)
             torch.cuda.synchronize()
@@ -131,7 +109,7 @@ def test_verify_bit_identical_under_stalls(pool_dtype, replay):
 
     def run(seed):
         pool = pool0.clone()
-        with _env(KDA_STALL_INJECT=seed or None):
+        with K.overrides(stall_seed=seed or 0):
             out = K.kda_verify(d.q, d.k, d.v, d.g, d.beta, pool, d.accepted, slot=d.slot,
                                replay_only=replay)
             torch.cuda.synchronize()

@@ -1,9 +1,7 @@
 """GPU parity of the one-CTA-per-chain state kernel (all 128 value columns per
-CTA), forced with KDA_STATE_KERNEL=head on shapes where the default would pick
+CTA), forced through the call's overrides on shapes where the default would pick
 the 32-column slab kernel: against the fp64 oracle, and against the slab
 kernel on the same inputs (same chunk step, same MMA K order)."""
-import os
-
 import pytest
 import torch
 
@@ -14,17 +12,11 @@ pytestmark = pytest.mark.gpu
 
 
 def _with_kernel(name, inp):
-    old = os.environ.get("KDA_STATE_KERNEL")
-    os.environ["KDA_STATE_KERNEL"] = name
-    try:
+    import kda_chunked_prefill_02_gb300 as K
+    with K.overrides(state_kernel=name):
         out, fin = gpu_prefill(inp)
         torch.cuda.synchronize()
-        return out.cpu(), fin.cpu()
-    finally:
-        if old is None:
-            del os.environ["KDA_STATE_KERNEL"]
-        else:
-            os.environ["KDA_STATE_KERNEL"] = old
+    return out.cpu(), fin.cpu()
 
 
 @pytest.mark.parametrize("case", [dict(B=1, T=256, H=2), dict(B=2, T=1000, H=3),
