@@ -51,7 +51,14 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", choices=["long", "varlen", "padded", "tiny", "verify"], default="long")
+    ap.add_argument("--config", choices=["long", "varlen", "padded", "tiny", "verify", "long_h8"],
+                    default="long")
+    ap.add_argument("--state-kernel", choices=["auto", "slab", "head"], default="auto",
+                    help="measurements: force the state kernel (kda_overrides.state_kernel)")
+    ap.add_argument("--segments", type=int, default=None,
+                    help="measurements: force segments of N chunks (0: one pass)")
+    ap.add_argument("--scan", type=int, default=0,
+                    help="measurements: 1 rules the segment-parallel scan out, N >= 2 forces N segments")
     ap.add_argument("--pool", choices=["fp32", "bf16"], default="fp32",
                     help="state pool element type of --config verify")
     ap.add_argument("--drafts", type=int, default=4, choices=range(1, 17), metavar="1..16",
@@ -199,6 +206,19 @@ def cpu_oracle_sample(inp, max_tokens):
     return sub.total_tokens, time.perf_counter() - t0, used
 
 
+def schedule_overrides(args):
+    """kda_overrides of the measurement flags (None: the library's choices)."""
+    import kda_chunked_prefill_02_gb300 as K
+    kw = {}
+    if args.state_kernel != "auto":
+        kw["state_kernel"] = args.state_kernel
+    if args.segments is not None:
+        kw["segment_chunks"] = args.segments
+    if args.scan:
+        kw["scan_segments"] = args.scan
+    return K.overrides(**kw) if kw else None
+
+
 def run_ours(args, rank, ws, local):
     import torch
 
@@ -301,7 +321,9 @@ def run_ours(args, rank, ws, local):
     path_bytes = bytes_prep + bytes_state
     traffic = captured_traffic(dom, th)
     sched = K.prefill_schedule(d.q, cu_seqlens=d.cu_seqlens)
-    if sched["segmented"]:
+    if sched["scan_segments"]:
+        launches = 4     # prep, the segments' operators, the combine, the outputs
+    elif sched["segmented"]:
         chunks = -(-inp.lengths[0] // 64)            # padded: every sequence has T tokens
         nseg = -(-chunks // sched["segment_chunks"])
         launches = 2 * nseg
@@ -388,9 +410,11 @@ def main():
     if args.impl == "reference":
         return main_reference(args)
     import torch
+    import contextlib
     rank, ws, local = dist_init(args.gpus)
-    r = run_ours(args, rank, ws, local)
-    e2e = run_e2e(r, args, ws)
+    with schedule_overrides(args) or contextlib.nullcontext():
+        r = run_ours(args, rank, ws, local)
+        e2e = run_e2e(r, args, ws)
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(r["inp"])

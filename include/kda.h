@@ -72,11 +72,19 @@ extern "C" {
  *                   which a quarter of the warps at each injection site spin
  *                   for a pseudo-random 0..4095 cycles; every result must be
  *                   bit-identical to the run without it
- *   reserved0       must be 0
+ *   scan_segments   0: library's choice, 1: never run the segment-parallel
+ *                   scan, n >= 2: run it with n segments per chain (padded
+ *                   calls; clamped to the scan_max_segments of the workspace
+ *                   layout, and not run when that is below 2)
  *   wait_limit_ns   > 0: bound of the kernels' working mbarrier waits instead
  *                   of 200 ms (a wait that runs out writes KDA_ERR_TIMEOUT to
  *                   the status word and the CTA winds down; the wind-down's own
  *                   waits for copies and products in flight keep 200 ms)
+ *   timeout_probe   1: in every prep and state-pass CTA, the first wait for a
+ *                   tensor-core product waits instead on an mbarrier that
+ *                   nothing arrives on, so that it runs out (after
+ *                   wait_limit_ns) with the product and tile copies still in
+ *                   flight: the wind-down path, exercised without a fault
  */
 typedef struct kda_overrides {
     int32_t state_kernel;
@@ -84,8 +92,10 @@ typedef struct kda_overrides {
     int32_t prep_ctas;
     int32_t no_pdl;
     uint32_t stall_seed;
-    int32_t reserved0;
+    int32_t scan_segments;
     int64_t wait_limit_ns;
+    int32_t timeout_probe;
+    int32_t reserved;           /* must be 0 */
 } kda_overrides;
 
 typedef enum {
@@ -199,7 +209,18 @@ size_t kda_prefill_workspace_size(const kda_prefill_args* args);
  * the call's work ends) overlaps the prep of segment s+1, the state of every
  * chain passing between segments in fp32 through the workspace's
  * state_carry region, so the results are those of one state pass over the
- * whole sequence.  The second stream and two events are created on a host
+ * whole sequence.
+ * Padded calls with very few chains may instead run the segment-parallel
+ * inter-chunk scan (the seg / comb kernels of the cuDNN-frontend sm90 KDA
+ * page, Conversation): each chain's chunks are cut into n segments; for every
+ * segment but the last, the transition M (the state map of the segment's
+ * chunks, taken from the identity with U read as zero) and the offset C (the
+ * state the segment leaves from a zero entry) are computed in parallel; a
+ * combine kernel then forms the entry states E_{s+1} = M_s E_s + C_s in fp32
+ * in a fixed order (E_0 = initial_state), and the outputs of all segments are
+ * computed in parallel from their entry states.  The result is deterministic
+ * and within the stated tolerances, but not bitwise that of the one-pass
+ * state recurrence (the state's rounding path differs).  The second stream and two events are created on a host
  * thread's first segmented call on a device and kept for the thread's life
  * (calls of one thread share them), so segmented calls can be captured into a
  * CUDA graph once one has run outside the capture.
@@ -222,10 +243,13 @@ kda_status kda_prefill(const kda_prefill_args* args, void* stream);
  * segments of segment_chunks chunks, the state pass of one beside the prep
  * of the next, prep on prep_ctas CTAs; whole_chain: 1 if the state pass runs
  * one CTA per chain (all 128 value columns), 0 for four 32-column slab CTAs
- * per chain.  KDA_ERR_INVALID_ARG for NULL pointers or num_sms < 1.
+ * per chain; scan_segments: n >= 2 if the call runs the segment-parallel scan
+ * with n segments of scan_chunks chunks (whole-chain CTAs; then segmented is
+ * 0), else 0.  KDA_ERR_INVALID_ARG for NULL pointers or num_sms < 1.
  */
 typedef struct kda_schedule {
     int32_t segmented, whole_chain, segment_chunks, prep_ctas;
+    int32_t scan_segments, scan_chunks;
 } kda_schedule;
 kda_status kda_prefill_schedule(const kda_prefill_args* args, int num_sms, kda_schedule* schedule);
 
@@ -268,12 +292,20 @@ kda_status kda_prefill_state(const kda_prefill_args* args, void* stream);
  * A segmented kda_prefill (see there) keeps the records of each token segment
  * together: segment s's records follow those of segments 0..s-1, numbered
  * as above within the segment.
+ * scan (padded calls with at most 64 chains and at least 128 chunks per
+ * sequence): room for the segment-parallel scan with up to scan_max_segments
+ * = min(32, chunks per sequence / 64) segments: the segments' transitions and
+ * offsets, fp32 [(scan_max_segments - 1) * 2, B * H, 128, 128] (block
+ * (2 s + w) * B * H + chain, w = 0 transition, 1 offset), then the entry
+ * states fp32 [scan_max_segments, B * H, 128, 128].
  */
 typedef struct kda_workspace_layout {
     size_t records, record_bytes, chunk_offset, status, total;
     int64_t max_chunks;         /* records per head */
     size_t state_carry;         /* padded calls: fp32 [B, H, 128, 128] */
     size_t seq_order;           /* varlen calls: int32 [N], sequences longest first */
+    size_t scan;                /* padded calls: segment-parallel scan buffers (see above) */
+    int64_t scan_max_segments;  /* 0 when the layout has no scan room */
 } kda_workspace_layout;
 kda_status kda_prefill_workspace_layout(const kda_prefill_args* args,
                                         kda_workspace_layout* layout);

@@ -23,6 +23,19 @@ int64_t max_chunks_of(const kda_prefill_args* a) {
     return a->seqlen / kChunk + a->num_seqs;
 }
 
+// Segments the workspace has room for in the segment-parallel scan: padded
+// calls with at most 64 chains and at least 128 chunks per sequence, one
+// segment per 64 chunks up to 32 (0: no scan room).
+constexpr int64_t kScanMaxChains = 64, kScanChunksPerSegment = 64;
+int64_t scan_max_segments(const kda_prefill_args* a) {
+    if (a->cu_seqlens != nullptr || a->batch < 1 || a->num_heads < 1) return 0;
+    if (a->batch * a->num_heads > kScanMaxChains) return 0;
+    const int64_t cps = (a->seqlen + kChunk - 1) / kChunk;
+    const int64_t n = cps / kScanChunksPerSegment;
+    if (n < 2) return 0;
+    return n < kScanMaxSegments ? n : kScanMaxSegments;
+}
+
 bool layout_of(const kda_prefill_args* a, kda_workspace_layout* L) {
     if (a->num_heads < 1 || a->seqlen < 0 || a->num_seqs < 0 || a->batch < 0) return false;
     // Sizes that cannot be described in size_t (with room for the alignment of
@@ -51,6 +64,13 @@ bool layout_of(const kda_prefill_args* a, kda_workspace_layout* L) {
                              ? (size_t)a->batch * (size_t)a->num_heads * kHeadDim * kHeadDim * sizeof(float)
                              : 0;
     L->state_carry = o; o = align_up(o + carry);
+    // padded calls with few, long chains: the segment-parallel scan's operators
+    // and entry states
+    const int64_t smax = scan_max_segments(a);
+    L->scan_max_segments = smax;
+    const size_t blk = (size_t)kHeadDim * kHeadDim * sizeof(float);
+    const size_t scan = smax >= 2 ? (size_t)(3 * smax - 2) * chains * (size_t)a->num_heads * blk : 0;
+    L->scan = o; o = align_up(o + scan);
     L->total = o;
     return true;
 }
@@ -98,7 +118,8 @@ kda_status check_args(const kda_prefill_args* a) {
         return KDA_ERR_UNSUPPORTED;
     kda_workspace_layout L;
     if (!layout_of(a, &L)) return KDA_ERR_INVALID_ARG;
-    if (a->overrides && a->overrides->reserved0 != 0) return KDA_ERR_INVALID_ARG;
+    if (a->overrides && (a->overrides->scan_segments < 0 || a->overrides->reserved != 0))
+        return KDA_ERR_INVALID_ARG;
     return KDA_OK;
 }
 
@@ -159,6 +180,7 @@ void fill_params(const kda_prefill_args* a, const kda_workspace_layout& L, Prefi
     const kda_overrides o = overrides_of(a->overrides);
     p->stall_seed = o.stall_seed;
     p->wait_ns = wait_limit_of(o);
+    p->timeout_probe = o.timeout_probe ? 1 : 0;
 }
 
 // 4-D input tensor map [channel 128, head, token, batch] with one chunk of
@@ -234,15 +256,52 @@ bool whole_chain_kernel(const PrefillParams& p, const kda_overrides& o, int num_
 // CTAs per chain) and 1.90 us in the whole-chain kernel, 12 % more beside prep;
 // every segment adds about 5 us to each stream (launch, start-up, the slowest
 // CTA's tail).  Fitted to a sweep of segment lengths 60..240 within 1 %.
+//
+// The segment-parallel scan (chosen when its estimate wins by 5 %): prep on
+// every SM, then the operator pass (2 (n - 1) whole-chain CTAs per chain), the
+// combine (one fp32 128 x 128 x 128 product per segment and chain, 6.6 us
+// each) and the output pass (n CTAs per chain), each launch adding
+// kSegmentUs.  A pass step takes the whole-chain step (1.90 us) unless the
+// resident CTAs' record reads (82.4 KB per step each; the transition and
+// offset CTAs of a segment read the same records, so half as many distinct
+// ones) need longer at the 4.2 TB/s these reads reach.  Fitted to B 1,
+// T 131072, H 1..16 and T 32768, H 8 within 3 % (launch-list durations and
+// event-timed calls).
 struct Segments {
     bool on = false;
     bool head = false;       // whole-chain state kernel (else slab)
     int chunks = 0;          // chunks of every sequence per segment
     int prep_ctas = 0;       // prep grid while a state pass runs beside it
+    int scan_nseg = 0;       // >= 2: segment-parallel scan with this many segments
+    int scan_chunks = 0;     //        of this many chunks
 };
 
 constexpr double kRecUs = 8.7, kSlabStepUs = 1.05, kHeadStepUs = 1.90;
 constexpr double kPrepBeside = 0.95, kStateBeside = 1.12, kSegmentUs = 5.0;
+constexpr double kScanCombUs = 6.6, kScanRecordGBs = 4200.0;
+
+// Estimated time of the segment-parallel scan with nseg segments.
+double scan_us(long long cps, long long chains, long long nseg, int num_sms) {
+    auto waves = [](long long n, long long m) { return (double)((n + m - 1) / m); };
+    // step time of a pass whose resident CTAs read `distinct` records per step
+    auto step = [&](long long ctas, double share) {
+        const double resident = (double)(ctas < num_sms ? ctas : num_sms) * share;
+        const double bw_us = resident * (double)kRecBytes / (kScanRecordGBs * 1e3);
+        return bw_us > kHeadStepUs ? bw_us : kHeadStepUs;
+    };
+    const long long L = (cps + nseg - 1) / nseg;
+    const long long ops = 2 * (nseg - 1) * chains, outs = nseg * chains;
+    return waves(cps * chains, num_sms) * kRecUs + waves(ops, num_sms) * L * step(ops, 0.5) +
+           (double)(nseg - 1) * kScanCombUs + waves(outs, num_sms) * L * step(outs, 1.0) + 4.0 * kSegmentUs;
+}
+
+// Segment length and count of a scan with (at most) nseg segments: every
+// segment but the last has L chunks, the last at least one.
+void scan_shape(long long cps, long long nseg, int* out_nseg, int* out_chunks) {
+    const long long L = (cps + nseg - 1) / nseg;
+    *out_chunks = (int)L;
+    *out_nseg = (int)((cps + L - 1) / L);
+}
 
 // Estimated time of the segmented schedule: prep of segment i ends at P_i =
 // P_{i-1} + a_i; its state pass starts when both P_i and the previous state pass
@@ -260,21 +319,29 @@ double segmented_us(long long cps, long long chains, long long seg, long long ct
     return S;
 }
 
-Segments plan_segments(const PrefillParams& p, const kda_overrides& o, int num_sms) {
+Segments plan_segments(const PrefillParams& p, const kda_overrides& o, int num_sms, int64_t scan_max) {
     Segments sg;
     if (p.cu != nullptr || p.T <= 0 || p.N <= 0 || num_sms < 4) return sg;
+    const long long chains = (long long)p.N * p.H, cps = (p.T + kChunk - 1) / kChunk;
+    // the scan, when forced (and the workspace has room for it)
+    if (o.scan_segments >= 2 && scan_max >= 2) {
+        sg.scan_nseg = 1;
+        scan_shape(cps, o.scan_segments < scan_max ? o.scan_segments : scan_max, &sg.scan_nseg, &sg.scan_chunks);
+        if (sg.scan_nseg < 2) sg.scan_nseg = sg.scan_chunks = 0;
+        sg.head = true;
+        return sg;
+    }
     const long long forced = o.segment_chunks < 0 ? -1 : o.segment_chunks;
     if (forced == 0) return sg;
-    const long long chains = (long long)p.N * p.H, cps = (p.T + kChunk - 1) / kChunk;
     const bool allow_slab = !p.gate && o.state_kernel != 2;
     const bool allow_head = p.gate || o.state_kernel != 1;
     auto waves = [](long long n, long long m) { return (double)((n + m - 1) / m); };
     // sequential: prep on every SM, then the state pass (each with its start-up
     // and tail, as a segment's)
-    double best = waves(cps * chains, num_sms) * kRecUs + 2.0 * kSegmentUs +
-                  (whole_chain_kernel(p, o, num_sms) ? waves(chains, num_sms) * cps * kHeadStepUs
-                                                  : waves(4 * chains, num_sms) * cps * kSlabStepUs);
-    best *= 0.95;   // segment only for a clear gain
+    const double one_pass = waves(cps * chains, num_sms) * kRecUs + 2.0 * kSegmentUs +
+                            (whole_chain_kernel(p, o, num_sms) ? waves(chains, num_sms) * cps * kHeadStepUs
+                                                            : waves(4 * chains, num_sms) * cps * kSlabStepUs);
+    double best = one_pass * 0.95;   // segment only for a clear gain
     if (forced > 0) best = 1e300;
     for (int head = 0; head < 2; ++head) {
         if (head ? !allow_head : !allow_slab) continue;
@@ -306,6 +373,21 @@ Segments plan_segments(const PrefillParams& p, const kda_overrides& o, int num_s
                 sg.prep_ctas = (int)ctas;
             }
         }
+    }
+    // the scan, unless a segment length is forced or the scan is ruled out
+    if (forced < 0 && o.scan_segments != 1 && scan_max >= 2 && allow_head) {
+        const double cur = sg.on ? best : one_pass;
+        double best_scan = cur * 0.95;
+        for (long long n = 2; n <= scan_max; ++n) {
+            const double t = scan_us(cps, chains, n, num_sms);
+            if (t < best_scan) {
+                best_scan = t;
+                sg = Segments();
+                sg.head = true;
+                scan_shape(cps, n, &sg.scan_nseg, &sg.scan_chunks);
+            }
+        }
+        if (sg.scan_nseg == 1) sg = Segments();
     }
     return sg;
 }
@@ -388,6 +470,33 @@ kda_status run_segments(const kda_prefill_args* a, const PrefillParams& p, const
     return ok ? KDA_OK : KDA_ERR_CUDA;
 }
 
+// Runs a planned segment-parallel scan on `s`: prep of every record on every
+// SM, the segments' operators, the combine into entry states, and the outputs
+// of every segment from its entry state.
+kda_status run_scan(const kda_prefill_args* a, const PrefillParams& p, const Segments& sg,
+                    const kda_workspace_layout& L, int num_sms, cudaStream_t s) {
+    PrepMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    if (!make_prep_maps(a, &maps)) return KDA_ERR_UNSUPPORTED;
+    if (launch_prep(p, maps, num_sms, s) != cudaSuccess) return KDA_ERR_CUDA;
+    uint8_t* ws = static_cast<uint8_t*>(a->workspace);
+    const size_t blk = (size_t)kHeadDim * kHeadDim;
+    PrefillParams q = p;
+    q.scan_nseg = sg.scan_nseg;
+    q.scan_chunks = sg.scan_chunks;
+    q.scan_ops = reinterpret_cast<float*>(ws + L.scan);
+    q.scan_entry = q.scan_ops + (size_t)(2 * (L.scan_max_segments - 1)) * p.N * p.H * blk;
+    PrefillParams ops = q;
+    ops.scan_mode = kScanOps;
+    ops.gate = nullptr;   // no outputs in the operator pass
+    PrefillParams outp = q;
+    outp.scan_mode = kScanOut;
+    if (launch_state_pass(a, ops, true, s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (launch_scan_combine(q, s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (launch_state_pass(a, outp, true, s) != cudaSuccess) return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
 kda_status run_prefill(const kda_prefill_args* a, void* stream, int stages) {
     const bool state_pass = (stages & 2) != 0, prep = (stages & 1) != 0;
     kda_status st = check_prefill(a);
@@ -408,7 +517,8 @@ kda_status run_prefill(const kda_prefill_args* a, void* stream, int stages) {
     if (prep && !a->device_status && cudaMemsetAsync(p.status, 0, sizeof(int32_t), s) != cudaSuccess)
         return KDA_ERR_CUDA;
     if (prep && state_pass) {
-        const Segments sg = plan_segments(p, o, num_sms);
+        const Segments sg = plan_segments(p, o, num_sms, L.scan_max_segments);
+        if (sg.scan_nseg >= 2) return run_scan(a, p, sg, L, num_sms, s);
         SideSet side;
         // without a second stream (none could be created) the call runs in one pass
         if (sg.on && side_set(&side)) return run_segments(a, p, o, sg, L, num_sms, side, s);
@@ -459,11 +569,14 @@ kda_status kda_prefill_schedule(const kda_prefill_args* args, int num_sms, kda_s
     p.B = (int)args->batch;
     p.gate = static_cast<const __nv_bfloat16*>(args->out_gate);
     const kda_overrides o = overrides_of(args->overrides);
-    const Segments sg = plan_segments(p, o, num_sms);
+    const Segments sg = plan_segments(p, o, num_sms, scan_max_segments(args));
+    const bool scan = sg.scan_nseg >= 2;
     out->segmented = sg.on ? 1 : 0;
-    out->whole_chain = sg.on ? (sg.head ? 1 : 0) : (whole_chain_kernel(p, o, num_sms) ? 1 : 0);
+    out->whole_chain = (sg.on || scan) ? (sg.head ? 1 : 0) : (whole_chain_kernel(p, o, num_sms) ? 1 : 0);
     out->segment_chunks = sg.on ? sg.chunks : 0;
     out->prep_ctas = sg.on ? sg.prep_ctas : num_sms;
+    out->scan_segments = scan ? sg.scan_nseg : 0;
+    out->scan_chunks = scan ? sg.scan_chunks : 0;
     return KDA_OK;
 }
 

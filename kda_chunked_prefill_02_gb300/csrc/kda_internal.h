@@ -81,7 +81,27 @@ struct PrefillParams {
     int out_tma;                 // 1: the state kernel got a tensor map of out
     uint64_t wait_ns;            // bound of the kernels' working mbarrier waits (kWaitLimitNs
                                  // unless a test lowers it; wind-down waits keep kWaitLimitNs)
+    int timeout_probe;           // test: the first product wait of a CTA waits on an
+                                 // mbarrier that nothing arrives on (runs out)
+    // Segment-parallel scan of padded calls (whole-chain state kernel only):
+    int scan_mode;               // kScanOff, kScanOps or kScanOut
+    int scan_chunks;             // chunks per segment
+    int scan_nseg;               // segments per chain
+    float* scan_ops;             // [(nseg - 1) * 2][B * H] fp32 128 x 128 blocks: M_s, C_s
+    float* scan_entry;           // [nseg][B * H] fp32 128 x 128 blocks: E_s (s >= 1 used)
 };
+
+// Modes of the whole-chain state kernel.
+//  kScanOff: one pass over each chain (blockIdx.y = sequence).
+//  kScanOps: blockIdx.y = (2 s + w) N + n, segment s < nseg - 1: w = 0 its
+//            transition M_s (entry = identity, U read as zero), w = 1 its
+//            offset C_s (entry = zero); no outputs; the state after the
+//            segment goes to scan_ops.
+//  kScanOut: blockIdx.y = s N + n: segment s from its entry state (the initial
+//            state for s = 0, else scan_entry) with outputs; the last segment
+//            stores the final state.
+constexpr int kScanOff = 0, kScanOps = 1, kScanOut = 2;
+constexpr int kScanMaxSegments = 32;
 
 // Chunk c (global index) -> sequence, token start and length.
 struct ChunkInfo {
@@ -134,6 +154,9 @@ cudaError_t launch_prep(const PrefillParams& p, const PrepMaps& maps, int num_sm
 // [32, 1, 64, 1] and the 64-byte swizzle (used when p.out_tma is set).
 cudaError_t launch_state(const PrefillParams& p, const CUtensorMap& out_map, cudaStream_t s);
 cudaError_t launch_state_head(const PrefillParams& p, const CUtensorMap& out_map, cudaStream_t s);
+// Entry states of the scan: E_{s+1} = M_s E_s + C_s (E_0 = p.h0 or zero) for
+// every chain, in fp32 with a fixed summation order.
+cudaError_t launch_scan_combine(const PrefillParams& p, cudaStream_t s);
 
 struct VerifyParams {
     const __nv_bfloat16* q;

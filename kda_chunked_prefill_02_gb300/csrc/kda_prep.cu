@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-    __shared__ uint64_t bar_in, bar_mma[3], bar_fin;
+    __shared__ uint64_t bar_in, bar_mma[3], bar_fin, bar_never;
     __shared__ uint32_t tmem_base_sh;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -172,6 +172,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         mbar_init(&bar_in, 1);
         for (int i = 0; i < 3; ++i) mbar_init(&bar_mma[i], 1);
         mbar_init(&bar_fin, 1);
+        mbar_init(&bar_never, 1);   // nothing arrives on it (the timeout probe's wait)
         fence_mbar_init();
         tma_prefetch_desc(&maps.q); tma_prefetch_desc(&maps.k);
         tma_prefetch_desc(&maps.v); tma_prefetch_desc(&maps.g);
@@ -382,7 +383,9 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             bulk_commit();
         }
         if (cn.len > 0) bcur = load_beta(cn, rec_next % p.H);
-        ok = __syncthreads_and(tid == 0 ? mbar_wait(&bar_mma[0], it & 1, nullptr, p.wait_ns) : true);
+        ok = __syncthreads_and(
+            tid == 0 ? mbar_wait((p.timeout_probe && it == 0) ? &bar_never : &bar_mma[0], it & 1, nullptr, p.wait_ns)
+                     : true);
         tc_fence_after();
         if (!ok) break;
         // Once the Kt image has been read out of the consumed gate tile (this

@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-    __shared__ uint64_t full[kStages], empty[kStages], p1_done, p2_done, bar_fin;
+    __shared__ uint64_t full[kStages], empty[kStages], p1_done, p2_done, bar_fin, bar_never;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
 
@@ -91,6 +91,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
             mbar_init(&empty[i], 2);
         }
         mbar_init(&p1_done, 1); mbar_init(&p2_done, 1); mbar_init(&bar_fin, 1);
+        mbar_init(&bar_never, 1);   // nothing arrives on it (the timeout probe's wait)
         abort_flag = 0;
         fence_mbar_init();
     }
@@ -200,7 +201,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
                 for (int ch = 0; ch < 4; ++ch)
                     slab_row[ch] = *reinterpret_cast<const uint4*>(src + slab_chunk_off(r, ch));
             }
-            ok = ok && warp_wait(&p1_done, c & 1, abort, p.wait_ns);
+            ok = ok && warp_wait((p.timeout_probe && c == 0) ? &bar_never : &p1_done, c & 1, abort, p.wait_ns);
             tc_fence_after();
             float d[kSlab];
             if (ok) {

@@ -86,22 +86,44 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-    __shared__ uint64_t full[kHStages], p1_done, p2_done, bar_fin, bar_fin2;
+    __shared__ uint64_t full[kHStages], p1_done, p2_done, bar_fin, bar_fin2, bar_never;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
     __shared__ float s_ss[4][64];      // fused norm: partial sums of squares per column quarter
     __shared__ __align__(16) float s_w[kHeadDim];  // fused norm: weights
 
     const int h = blockIdx.x;
-    // varlen: the sequences in the order of the chunk table (longest first)
-    const int n = p.seq_order ? p.seq_order[blockIdx.y] : (int)blockIdx.y;
+    // Which chain (and, in the scan modes, which segment and operator) this CTA
+    // runs; varlen: the sequences in the order of the chunk table (longest first).
+    int n, seg = 0, which = 0;
+    if (p.scan_mode == kScanOps) {
+        n = (int)blockIdx.y % p.N;
+        seg = ((int)blockIdx.y / p.N) >> 1;
+        which = ((int)blockIdx.y / p.N) & 1;
+    } else if (p.scan_mode == kScanOut) {
+        n = (int)blockIdx.y % p.N;
+        seg = (int)blockIdx.y / p.N;
+    } else {
+        n = p.seq_order ? p.seq_order[blockIdx.y] : (int)blockIdx.y;
+    }
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // Scan operator passes: the transition reads U as zero and starts from the
+    // identity; neither writes outputs.
+    const bool no_out = p.scan_mode == kScanOps;
+    const bool zero_u = no_out && which == 0;
+    const size_t chain = (size_t)n * p.H + h;
 
-    // Chain extent.
-    int first, count, seq_len, b, tbase;
+    // Chain extent (cbase: the chain's chunk index of this CTA's first chunk).
+    int first, count, seq_len, b, tbase, cbase = 0;
     if (p.cu == nullptr) {
         const int cps = (p.T + kChunk - 1) / kChunk;
         first = n * cps; count = cps; seq_len = p.T; b = n; tbase = 0;
+        if (p.scan_mode != kScanOff) {
+            cbase = seg * p.scan_chunks;
+            first += cbase;
+            count = min(p.scan_chunks, cps - cbase);
+            if (count < 0) count = 0;
+        }
     } else {
         first = p.chunk_off[n];
         count = p.chunk_off[n + 1] - first;
@@ -113,6 +135,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
     if (tid == 0) {
         for (int i = 0; i < kHStages; ++i) mbar_init(&full[i], 1);
         mbar_init(&p1_done, 1); mbar_init(&p2_done, 1); mbar_init(&bar_fin, 1); mbar_init(&bar_fin2, 1);
+        mbar_init(&bar_never, 1);   // nothing arrives on it (the timeout probe's wait)
         abort_flag = 0;
         fence_mbar_init();
     }
@@ -150,9 +173,19 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
         const uint32_t id = idesc_bf16_f32_bmn(128, 128);
         const uint32_t sS_addr = smem_u32(sm + OH_S), sVn_addr = smem_u32(sm + OH_VN);
         float S[kSlab];
-        const size_t st_off = (((size_t)n * p.H + h) * kHeadDim + row) * kHeadDim + kSlab * cq;
-        if (p.h0) {
-            const float4* src = reinterpret_cast<const float4*>(p.h0 + st_off);
+        const size_t blk_off = (size_t)row * kHeadDim + kSlab * cq;   // inside a 128 x 128 block
+        const size_t st_off = chain * kHeadDim * kHeadDim + blk_off;
+        // Entry state: the call's initial state, or in the scan the identity
+        // (transition), zero (offset) or the combine's entry state E_seg.
+        const float* h0 = p.h0 ? p.h0 + st_off : nullptr;
+        if (p.scan_mode == kScanOps) h0 = nullptr;
+        if (p.scan_mode == kScanOut && seg > 0)
+            h0 = p.scan_entry + ((size_t)seg * p.N * p.H + chain) * kHeadDim * kHeadDim + blk_off;
+        if (zero_u) {
+#pragma unroll
+            for (int j = 0; j < kSlab; ++j) S[j] = (row == kSlab * cq + j) ? 1.f : 0.f;
+        } else if (h0) {
+            const float4* src = reinterpret_cast<const float4*>(h0);
 #pragma unroll
             for (int x = 0; x < kSlab / 4; ++x) {
                 const float4 t = src[x];
@@ -203,7 +236,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch) sr[ch] = *reinterpret_cast<const uint4*>(src + slab_chunk_off(r, ch));
             }
-            ok = ok && warp_wait_h(&p1_done, c & 1, abort, p.wait_ns);
+            ok = ok && warp_wait_h((p.timeout_probe && c == 0) ? &bar_never : &p1_done, c & 1, abort, p.wait_ns);
             tc_fence_after();
             float d[kSlab];
             if (ok) {
@@ -218,7 +251,8 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
                         const uint32_t uw[4] = {sr[ch].x, sr[ch].y, sr[ch].z, sr[ch].w};
 #pragma unroll
                         for (int x = 0; x < 4; ++x) {
-                            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&uw[x]));
+                            float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&uw[x]));
+                            if (zero_u) f = make_float2(0.f, 0.f);
                             vn[8 * ch + 2 * x] = f.x - d[8 * ch + 2 * x];
                             vn[8 * ch + 2 * x + 1] = f.y - d[8 * ch + 2 * x + 1];
                         }
@@ -239,9 +273,9 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
                     umma_commit(&p2_done);
                 }
                 __syncwarp();
-            } else {
+            } else if (!no_out) {
                 // O = O_loc + Q' S for token row `row - 64`
-                const int i = row - 64, t0 = 64 * c;
+                const int i = row - 64, t0 = 64 * (cbase + c);
                 const bool valid_row = t0 + i < seq_len;
                 const int64_t t = (int64_t)tbase + t0 + i;
                 float o[kSlab];
@@ -360,8 +394,14 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
             umma_commit(&bar_fin2);
             mbar_wait(&bar_fin2, 0, nullptr);
         }
-        if (!*abort && p.hT) {
-            float4* dst = reinterpret_cast<float4*>(p.hT + st_off);
+        // The state after the chain (or the segment): the final state, a scan
+        // operator, or nothing (scan segments before the last).
+        float* fin = p.hT ? p.hT + st_off : nullptr;
+        if (p.scan_mode == kScanOps)
+            fin = p.scan_ops + (((size_t)(2 * seg + which)) * p.N * p.H + chain) * kHeadDim * kHeadDim + blk_off;
+        if (p.scan_mode == kScanOut && seg != p.scan_nseg - 1) fin = nullptr;
+        if (!*abort && fin) {
+            float4* dst = reinterpret_cast<float4*>(fin);
 #pragma unroll
             for (int x = 0; x < kSlab / 4; ++x)
                 dst[x] = make_float4(S[4 * x], S[4 * x + 1], S[4 * x + 2], S[4 * x + 3]);
@@ -380,8 +420,106 @@ cudaError_t launch_state_head(const PrefillParams& p, const CUtensorMap& out_map
     auto kern = p.stall_seed ? state_head_kernel<true> : state_head_kernel<false>;
     cudaError_t e = set_smem_limit_once((const void*)kern, (int)kHeadSmem, smem_set[p.stall_seed ? 1 : 0]);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.H, p.N);
+    const int ys = p.scan_mode == kScanOps ? 2 * (p.scan_nseg - 1) : (p.scan_mode == kScanOut ? p.scan_nseg : 1);
+    if (ys <= 0) return cudaSuccess;
+    dim3 grid(p.H, p.N * ys);
     kern<<<grid, kHeadThreads, kHeadSmem, s>>>(p, out_map);
+    return cudaGetLastError();
+}
+
+namespace {
+
+// ---------------------------------------------------------------- scan combine
+// E_{s+1} = M_s E_s + C_s, s = 0 .. nseg - 2, for one chain and a 16-column
+// slab of the state (value columns never mix, so the eight slabs of a chain
+// run in separate CTAs).  fp32 FMAs in a fixed order (C first, then the key
+// index k ascending), so the entry states are bitwise reproducible.
+// M_{s+1} and the slab of C_{s+1} are copied into shared memory (cp.async; M
+// with a row pitch of 132 floats) while the product of segment s runs; E_s
+// stays in shared memory from one segment to the next.  Thread = 4 rows
+// (r0 + 32 m, m = 0..3) x 4 columns: per key index one broadcast M value per
+// row (the eight rows a warp reads fall on distinct banks) and one float4 of E.
+constexpr int kCombThreads = 128;
+constexpr int kCombCols = 16;
+constexpr int kMPitch = kHeadDim + 4;
+constexpr uint32_t kCombSmem =
+    (2 * kHeadDim * kMPitch + 2 * kHeadDim * kCombCols + kHeadDim * kCombCols) * sizeof(float);
+
+__device__ __forceinline__ void cp_async16_comb(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+__global__ void __launch_bounds__(kCombThreads) scan_combine_kernel(const PrefillParams p) {
+    extern __shared__ __align__(16) float smc[];
+    float* Ms[2] = {smc, smc + kHeadDim * kMPitch};           // M[i][k] at i * 132 + k
+    float* Cs[2] = {smc + 2 * kHeadDim * kMPitch, smc + 2 * kHeadDim * kMPitch + kHeadDim * kCombCols};
+    float* Es = smc + 2 * kHeadDim * kMPitch + 2 * kHeadDim * kCombCols;   // E[k][16 columns]
+    const int slab = blockIdx.x, col0 = kCombCols * slab;
+    const size_t chain = blockIdx.y, chains = (size_t)p.N * p.H;
+    constexpr size_t kBlk = (size_t)kHeadDim * kHeadDim;
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+    const int cg = lane & 3, r0 = (lane >> 2) + 8 * w;        // rows r0 + 32 m, columns 4 cg ..
+    // M_s and the slab of C_s into shared memory (one cp.async group)
+    auto stage = [&](int s, int buf) {
+        const float* M = p.scan_ops + ((size_t)(2 * s) * chains + chain) * kBlk;
+        const float* C = p.scan_ops + ((size_t)(2 * s + 1) * chains + chain) * kBlk;
+        for (int e = tid; e < kHeadDim * kHeadDim / 4; e += kCombThreads)
+            cp_async16_comb(Ms[buf] + (e >> 5) * kMPitch + 4 * (e & 31), M + 4 * (size_t)e);
+        for (int e = tid; e < kHeadDim * kCombCols / 4; e += kCombThreads)
+            cp_async16_comb(Cs[buf] + 4 * e, C + (size_t)(e >> 2) * kHeadDim + col0 + 4 * (e & 3));
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    if (p.scan_nseg >= 2) stage(0, 0);
+    for (int e = tid; e < kHeadDim * kCombCols; e += kCombThreads) {
+        const int k = e / kCombCols, j = e % kCombCols;
+        Es[e] = p.h0 ? p.h0[chain * kBlk + (size_t)k * kHeadDim + col0 + j] : 0.f;
+    }
+    for (int s = 0; s + 1 < p.scan_nseg; ++s) {
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncthreads();   // M_s and C_s have landed; E_s is complete; the other buffers are free
+        if (s + 2 < p.scan_nseg) stage(s + 1, (s + 1) & 1);
+        const float* M = Ms[s & 1];
+        const float* C = Cs[s & 1];
+        float acc[4][4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const float4 c4 = *reinterpret_cast<const float4*>(C + (r0 + 32 * m) * kCombCols + 4 * cg);
+            acc[m][0] = c4.x; acc[m][1] = c4.y; acc[m][2] = c4.z; acc[m][3] = c4.w;
+        }
+#pragma unroll 4
+        for (int k = 0; k < kHeadDim; ++k) {
+            const float4 e4 = *reinterpret_cast<const float4*>(Es + k * kCombCols + 4 * cg);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const float mv = M[(r0 + 32 * m) * kMPitch + k];
+                acc[m][0] = fmaf(mv, e4.x, acc[m][0]);
+                acc[m][1] = fmaf(mv, e4.y, acc[m][1]);
+                acc[m][2] = fmaf(mv, e4.z, acc[m][2]);
+                acc[m][3] = fmaf(mv, e4.w, acc[m][3]);
+            }
+        }
+        __syncthreads();   // every read of E_s is done
+        float* out = p.scan_entry + ((size_t)(s + 1) * chains + chain) * kBlk + col0 + 4 * cg;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int r = r0 + 32 * m;
+            const float4 v = make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
+            *reinterpret_cast<float4*>(Es + r * kCombCols + 4 * cg) = v;
+            *reinterpret_cast<float4*>(out + (size_t)r * kHeadDim) = v;
+        }
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
+}  // namespace
+
+cudaError_t launch_scan_combine(const PrefillParams& p, cudaStream_t s) {
+    if (p.N == 0 || p.H == 0 || p.scan_nseg < 2) return cudaSuccess;
+    static std::atomic<uint64_t> smem_set;
+    cudaError_t e = set_smem_limit_once((const void*)scan_combine_kernel, (int)kCombSmem, smem_set);
+    if (e != cudaSuccess) return e;
+    dim3 grid(kHeadDim / kCombCols, p.N * p.H);
+    scan_combine_kernel<<<grid, kCombThreads, kCombSmem, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -204,11 +204,13 @@ CONFIG_DESCRIPTIONS = {
     "varlen": "8 packed sequences (one of length 1) summing to 32768 tokens, H=32 (seed 2)",
     "long": "B=1 T=131072 H=32 K=V=128 chunk=64, initial state N(0,0.02^2) (seed 3)",
     "verify": "256 requests x 4 drafts, H=32, fp32 state pool N(0,0.02^2), accepted U{0..4} (seed 4)",
+    "long_h8": "B=1 T=131072 H=8 K=V=128 chunk=64, initial state N(0,0.02^2) (seed 5): the long "
+               "workload with few chains",
 }
 
 
 def config_inputs(name: str):
-    """The five workloads, seeds 0..4."""
+    """The five workloads, seeds 0..4, and the few-chain long workload (seed 5)."""
     if name == "tiny":
         return prefill_inputs(0, B=1, T=256, H=2, init_std=None)
     if name == "padded":
@@ -219,6 +221,8 @@ def config_inputs(name: str):
         return prefill_inputs(3, B=1, T=131072, H=32)
     if name == "verify":
         return verify_inputs(4, R=256, D=4, H=32)
+    if name == "long_h8":
+        return prefill_inputs(5, B=1, T=131072, H=8)
     raise KeyError(name)
 
 

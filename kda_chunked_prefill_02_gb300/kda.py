@@ -29,8 +29,9 @@ class Overrides(ctypes.Structure):
     """kda_overrides: test and measurement overrides of the library's choices."""
     _fields_ = [("state_kernel", ctypes.c_int32), ("segment_chunks", ctypes.c_int32),
                 ("prep_ctas", ctypes.c_int32), ("no_pdl", ctypes.c_int32),
-                ("stall_seed", ctypes.c_uint32), ("reserved0", ctypes.c_int32),
-                ("wait_limit_ns", ctypes.c_int64)]
+                ("stall_seed", ctypes.c_uint32), ("scan_segments", ctypes.c_int32),
+                ("wait_limit_ns", ctypes.c_int64), ("timeout_probe", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 _STATE_KERNELS = {None: 0, "slab": 1, "head": 2}
@@ -38,7 +39,7 @@ _overrides_var = contextvars.ContextVar("kda_overrides", default=None)
 
 
 def _make_overrides(state_kernel=None, segment_chunks=None, prep_ctas=None, no_pdl=False,
-                    stall_seed=0, wait_limit_ns=0):
+                    stall_seed=0, wait_limit_ns=0, scan_segments=0, timeout_probe=False):
     o = Overrides()
     o.state_kernel = _STATE_KERNELS[state_kernel]
     o.segment_chunks = -1 if segment_chunks is None else int(segment_chunks)
@@ -46,6 +47,8 @@ def _make_overrides(state_kernel=None, segment_chunks=None, prep_ctas=None, no_p
     o.no_pdl = 1 if no_pdl else 0
     o.stall_seed = int(stall_seed or 0)
     o.wait_limit_ns = int(wait_limit_ns or 0)
+    o.scan_segments = int(scan_segments or 0)
+    o.timeout_probe = 1 if timeout_probe else 0
     return o
 
 
@@ -54,7 +57,9 @@ def overrides(**kw):
     """Within the block, calls of this module pass these kda_overrides to the
     library (tests and measurements): state_kernel ("slab" | "head"),
     segment_chunks (0: never segment, n: segments of n chunks), prep_ctas,
-    no_pdl, stall_seed, wait_limit_ns.  Nothing is taken from the environment."""
+    no_pdl, stall_seed, wait_limit_ns, scan_segments (1: never run the
+    segment-parallel scan, n >= 2: run it with n segments), timeout_probe.
+    Nothing is taken from the environment."""
     tok = _overrides_var.set(_make_overrides(**kw))
     try:
         yield
@@ -106,12 +111,14 @@ class WorkspaceLayout(ctypes.Structure):
     _fields_ = [("records", ctypes.c_size_t), ("record_bytes", ctypes.c_size_t),
                 ("chunk_offset", ctypes.c_size_t), ("status", ctypes.c_size_t),
                 ("total", ctypes.c_size_t), ("max_chunks", _i64),
-                ("state_carry", ctypes.c_size_t), ("seq_order", ctypes.c_size_t)]
+                ("state_carry", ctypes.c_size_t), ("seq_order", ctypes.c_size_t),
+                ("scan", ctypes.c_size_t), ("scan_max_segments", _i64)]
 
 
 class Schedule(ctypes.Structure):
     _fields_ = [("segmented", ctypes.c_int32), ("whole_chain", ctypes.c_int32),
-                ("segment_chunks", ctypes.c_int32), ("prep_ctas", ctypes.c_int32)]
+                ("segment_chunks", ctypes.c_int32), ("prep_ctas", ctypes.c_int32),
+                ("scan_segments", ctypes.c_int32), ("scan_chunks", ctypes.c_int32)]
 
 
 _lib = None
@@ -282,7 +289,8 @@ def workspace_layout(q, *, cu_seqlens=None):
 
 def prefill_schedule(q, *, cu_seqlens=None, norm=False, num_sms=None):
     """The schedule kda_prefill runs for q's shape (kda_prefill_schedule):
-    dict(segmented, whole_chain, segment_chunks, prep_ctas).  Host only; q may
+    dict(segmented, whole_chain, segment_chunks, prep_ctas, scan_segments,
+    scan_chunks).  Host only; q may
     live anywhere (only its shape is read).  num_sms defaults to the current
     CUDA device's SM count."""
     a = PrefillArgs()
@@ -299,7 +307,8 @@ def prefill_schedule(q, *, cu_seqlens=None, norm=False, num_sms=None):
     sch = Schedule()
     _check(lib().kda_prefill_schedule(ctypes.byref(a), int(num_sms), ctypes.byref(sch)))
     return dict(segmented=bool(sch.segmented), whole_chain=bool(sch.whole_chain),
-                segment_chunks=sch.segment_chunks, prep_ctas=sch.prep_ctas)
+                segment_chunks=sch.segment_chunks, prep_ctas=sch.prep_ctas,
+                scan_segments=sch.scan_segments, scan_chunks=sch.scan_chunks)
 
 
 def kda_prefill(q, k, v, g, beta, *, initial_state=None, cu_seqlens=None, chunk=CHUNK,

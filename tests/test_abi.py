@@ -172,8 +172,11 @@ def test_prefill_schedule(K, monkeypatch):
     # 32 chains of 2048 chunks: whole-chain state CTAs on 32 SMs, prep on 120,
     # 56-chunk segments
     assert _sched(K, batch=1, num_seqs=1, seqlen=131072, num_heads=32) == (1, 1, 56, 120)
-    # 8 chains: slab state CTAs (4 per chain) on 32 SMs, prep on 120
-    s8 = _sched(K, batch=1, num_seqs=1, seqlen=131072, num_heads=8)
+    # 8 chains: the segment-parallel scan (test_scan_schedule_and_workspace);
+    # with the scan ruled out, slab state CTAs (4 per chain) on 32 SMs beside
+    # prep on 120
+    with K.overrides(scan_segments=1):
+        s8 = _sched(K, batch=1, num_seqs=1, seqlen=131072, num_heads=8)
     assert s8[:2] == (1, 0) and s8[3] == 120 and s8[2] % 8 == 0
     # the padded workload (64 chains of 64 chunks): two segments, whole-chain
     # state CTAs on 64 SMs, prep on 88 (measured 0.360 ms against 0.399 one pass)
@@ -202,12 +205,54 @@ def test_prefill_schedule(K, monkeypatch):
         assert _sched(K, batch=1, num_seqs=1, seqlen=256, num_heads=2) == (1, 0, 3, 40)
     with K.overrides(state_kernel="head"):
         assert _sched(K, batch=1, num_seqs=1, seqlen=4096, num_heads=2) == (0, 1, 0, 152)
-    # overrides with the reserved field set are refused
+    # negative scan segment counts are refused
     a = _args(K, batch=1, num_seqs=1, seqlen=256, num_heads=2)
     o = K._make_overrides()
-    o.reserved0 = 1
+    o.scan_segments = -2
     a.overrides = ctypes.pointer(o)
     assert K.lib().kda_prefill(ctypes.byref(a), None) == K.KDA_ERR_INVALID_ARG
+
+
+def _sched_full(K, num_sms=152, **kw):
+    a = _args(K, **kw)
+    a.overrides = K._current_overrides()
+    s = K.Schedule()
+    assert K.lib().kda_prefill_schedule(ctypes.byref(a), num_sms, ctypes.byref(s)) == 0
+    return s
+
+
+def test_scan_schedule_and_workspace(K):
+    """The segment-parallel scan: chosen for few long padded chains (a quarter
+    of the long workload's heads or fewer), never for the long workload itself
+    or varlen calls; forced and ruled out by the overrides; its workspace room
+    as include/kda.h states (host only)."""
+    long = dict(batch=1, num_seqs=1, seqlen=131072)
+    for H in (1, 2, 4, 8):
+        s = _sched_full(K, num_heads=H, **long)
+        assert s.scan_segments >= 2 and s.segmented == 0 and s.whole_chain == 1, H
+        assert (s.scan_segments - 1) * s.scan_chunks < 2048 <= s.scan_segments * s.scan_chunks
+    assert _sched_full(K, num_heads=32, **long).scan_segments == 0
+    assert _sched_full(K, cu_seqlens=ctypes.c_void_p(1 << 12), num_seqs=8, seqlen=32768,
+                       num_heads=2).scan_segments == 0
+    with K.overrides(scan_segments=1):       # never: the two-stream schedule instead
+        s = _sched_full(K, num_heads=8, **long)
+        assert s.scan_segments == 0 and s.segmented == 1
+    with K.overrides(scan_segments=3):       # 12300 tokens: 193 chunks, room for 3
+        s = _sched_full(K, batch=1, num_seqs=1, seqlen=12300, num_heads=2)
+        assert (s.scan_segments, s.scan_chunks) == (3, 65)
+    with K.overrides(scan_segments=9):       # clamped to the room
+        assert _sched_full(K, batch=1, num_seqs=1, seqlen=12300, num_heads=2).scan_segments == 3
+    with K.overrides(scan_segments=2):       # no room below 128 chunks: not run
+        assert _sched_full(K, batch=1, num_seqs=1, seqlen=8000, num_heads=2).scan_segments == 0
+    lib = K.lib()
+    L = K.WorkspaceLayout()
+    a = _args(K, num_heads=8, **long)
+    assert lib.kda_prefill_workspace_layout(ctypes.byref(a), ctypes.byref(L)) == 0
+    assert L.scan_max_segments == 32 and L.scan >= L.state_carry + 8 * 65536
+    assert L.total - L.scan >= (3 * 32 - 2) * 8 * 65536
+    a = _args(K, batch=1, num_seqs=1, seqlen=131072, num_heads=65)   # too many chains
+    assert lib.kda_prefill_workspace_layout(ctypes.byref(a), ctypes.byref(L)) == 0
+    assert L.scan_max_segments == 0
     a = _args(K)
     assert K.lib().kda_prefill_schedule(ctypes.byref(a), 0, ctypes.byref(K.Schedule())) == \
         K.KDA_ERR_INVALID_ARG

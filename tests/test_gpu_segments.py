@@ -123,12 +123,14 @@ def test_default_schedule_of_the_long_workload():
         sch = K.prefill_schedule(q)
     if torch.cuda.get_device_properties(0).multi_processor_count != 152:
         pytest.skip("schedule constants are for 152 SMs")
-    assert sch == dict(segmented=True, whole_chain=True, segment_chunks=56, prep_ctas=120)
+    assert sch == dict(segmented=True, whole_chain=True, segment_chunks=56, prep_ctas=120,
+                       scan_segments=0, scan_chunks=0)
 
 
 def test_segments_without_programmatic_launch():
-    """KDA_SEGMENT_PDL=0: the prep grids of consecutive segments run strictly
-    one after the other; same bits as with the programmatic launch."""
+    """no_pdl: the prep grids of consecutive segments run strictly one after the
+    other; same bits as with the programmatic launch."""
+    import kda_chunked_prefill_02_gb300 as K
     inp = inputs.prefill_inputs(855, B=1, T=64 * 11 + 3, H=3)
     d = inp.to("cuda")
     with K.overrides(segment_chunks=2):

@@ -5,10 +5,12 @@ out writes KDA_ERR_TIMEOUT to the status word, and the CTA winds down: the
 epilogue warps agree on stopping through the OR-reduction of the chunk
 barrier, and before TMEM and shared memory are released every copy still in
 flight and every product already issued is waited for (with the full 200 ms
-bound).  A call's overrides can lower the bound of the working waits to 1 ns,
-far below the time a tile copy or a tensor-core product takes, so that those
-waits run out.  The call must still return, the device must stay usable, and
-the next normal call on the same stream must give the oracle's result (the
+bound).  A call's overrides can lower the bound of the working waits and turn
+on a probe: the first wait of every CTA for a tensor-core product then waits
+on an mbarrier that nothing arrives on, so it runs out while that product and
+the tile copies are still in flight.  The call must still return, the device
+must stay usable, and the next normal call on the same stream must give the
+oracle's result (the
 failure detection plan of the build: device-side timeouts reported through a
 status word, the context kept alive; the TMEM-dealloc ordering of the
 TensorRT-LLM MQA-logits page)."""
@@ -42,7 +44,7 @@ def test_wait_that_runs_out_is_reported_and_the_context_survives(stage, kernel):
             _call(d, status, workspace=ws, stage="prep")
             torch.cuda.synchronize()
             assert status.item() == 0
-        with K.overrides(state_kernel=kernel, segment_chunks=0, wait_limit_ns=1):
+        with K.overrides(state_kernel=kernel, segment_chunks=0, wait_limit_ns=2000, timeout_probe=True):
             _call(d, status, workspace=ws, stage=stage)
         torch.cuda.synchronize()            # returns: no hang, no fault
         assert status.item() == KDA_ERR_TIMEOUT
@@ -56,15 +58,16 @@ def test_wait_that_runs_out_is_reported_and_the_context_survives(stage, kernel):
 
 
 def test_timeout_in_the_segmented_schedule_and_under_stalls():
-    """Both streams of the segmented schedule wind down; with the stall hook on
-    as well, so that the waits run out at many different points."""
+    """Both streams of the segmented schedule wind down; also with the stall
+    hook on, so that the probe's wait runs out at many different points of
+    the other warps' work."""
     import kda_chunked_prefill_02_gb300 as K
     inp = inputs.prefill_inputs(1202, B=1, T=64 * 9 + 3, H=4)
     d = inp.to("cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     for seed in (0, 5):
         status.zero_()
-        with K.overrides(segment_chunks=2, wait_limit_ns=1, stall_seed=seed):
+        with K.overrides(segment_chunks=2, wait_limit_ns=2000, timeout_probe=True, stall_seed=seed):
             _call(d, status)
         torch.cuda.synchronize()
         assert status.item() == KDA_ERR_TIMEOUT, seed
@@ -91,3 +94,23 @@ def test_production_calls_ignore_the_environment(monkeypatch):
     got = _call(d, status)
     torch.cuda.synchronize()
     assert torch.equal(ref[0], got[0]) and torch.equal(ref[1], got[1])
+
+
+def test_timeout_in_the_scan():
+    """The operator, combine-fed and output passes of the segment-parallel scan
+    wind down like the other passes."""
+    import kda_chunked_prefill_02_gb300 as K
+    inp = inputs.prefill_inputs(1204, B=1, T=8192 + 64, H=2)
+    d = inp.to("cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    with K.overrides(scan_segments=2, wait_limit_ns=2000, timeout_probe=True):
+        _call(d, status)
+    torch.cuda.synchronize()
+    assert status.item() == KDA_ERR_TIMEOUT
+    status.zero_()
+    with K.overrides(scan_segments=2):
+        out, fin = _call(d, status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    ro, rf = oracle_prefill(inp)
+    assert_parity(out, fin, ro, rf, "scan after a timed-out scan")
