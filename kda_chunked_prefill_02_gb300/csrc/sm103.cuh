@@ -316,6 +316,61 @@ __host__ __device__ __forceinline__ uint32_t mn_sw128_off(uint32_t k, uint32_t n
            (((((n & 63u) >> 3) ^ (k & 7u)) << 4) | ((n & 7u) << 1));
 }
 
+// Instruction descriptor for tcgen05.mma kind::tf32: tf32 A and B (fp32 bit
+// patterns of which the tensor core uses the top 19 bits), fp32 accumulator;
+// a_mn / b_mn: the operand is MN-major (M or N contiguous) instead of K-major.
+__host__ __device__ constexpr uint32_t idesc_tf32_f32(uint32_t M, uint32_t N, bool a_mn, bool b_mn) {
+    return (1u << 4)                 // D format: f32
+           | (2u << 7)               // A format: tf32
+           | (2u << 10)              // B format: tf32
+           | (a_mn ? (1u << 15) : 0u) | (b_mn ? (1u << 16) : 0u)
+           | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// D[tmem] (+)= A * B^T for one K step of 8 tf32 elements (32 bytes of a
+// 128-byte swizzled row), issued by a single thread.
+__device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// The same with the A operand (M x 8 tf32, row m in lane m, one element per
+// 32-bit column) read from TMEM at a_tmem.
+__device__ __forceinline__ void umma_tf32_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Byte offsets of fp32 element (r, k) in the 128-byte-swizzled operand layouts
+// (32 fp32 per 128-byte row, 8-row atoms of 1024 B):
+//  K-major: k contiguous; 32-wide K blocks of (rows x 128 B), block_bytes apart.
+__host__ __device__ __forceinline__ uint32_t f32_kmajor_off(uint32_t r, uint32_t k, uint32_t block_bytes) {
+    return (k >> 5) * block_bytes + r * 128u + (((((k & 31u) >> 2) ^ (r & 7u))) << 4) + (k & 3u) * 4u;
+}
+//  MN-major: r (the M or N index) contiguous; per K index a 128-byte row of 32
+//  consecutive r; 8-row K groups sbo apart, 32-wide r blocks lbo apart.
+__host__ __device__ __forceinline__ uint32_t f32_mnmajor_off(uint32_t r, uint32_t k, uint32_t lbo, uint32_t sbo) {
+    return (r >> 5) * lbo + (k >> 3) * sbo + (k & 7u) * 128u + (((((r & 31u) >> 2) ^ (k & 7u))) << 4) +
+           (r & 3u) * 4u;
+}
+
+// fp32 -> tf32 with round-to-nearest (ties away from zero), as an fp32 pattern.
+__device__ __forceinline__ float to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+
 // D[tmem] (+)= A * B^T, issued by a single thread.  A is M x 16 (K-major),
 // B is N x 16 (K-major), one K step of 16 bf16 elements.
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,

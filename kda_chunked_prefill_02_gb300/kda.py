@@ -31,7 +31,7 @@ class Overrides(ctypes.Structure):
                 ("prep_ctas", ctypes.c_int32), ("no_pdl", ctypes.c_int32),
                 ("stall_seed", ctypes.c_uint32), ("scan_segments", ctypes.c_int32),
                 ("wait_limit_ns", ctypes.c_int64), ("timeout_probe", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("verify_kernel", ctypes.c_int32)]
 
 
 _STATE_KERNELS = {None: 0, "slab": 1, "head": 2}
@@ -39,7 +39,8 @@ _overrides_var = contextvars.ContextVar("kda_overrides", default=None)
 
 
 def _make_overrides(state_kernel=None, segment_chunks=None, prep_ctas=None, no_pdl=False,
-                    stall_seed=0, wait_limit_ns=0, scan_segments=0, timeout_probe=False):
+                    stall_seed=0, wait_limit_ns=0, scan_segments=0, timeout_probe=False,
+                    verify_kernel=None):
     o = Overrides()
     o.state_kernel = _STATE_KERNELS[state_kernel]
     o.segment_chunks = -1 if segment_chunks is None else int(segment_chunks)
@@ -49,6 +50,7 @@ def _make_overrides(state_kernel=None, segment_chunks=None, prep_ctas=None, no_p
     o.wait_limit_ns = int(wait_limit_ns or 0)
     o.scan_segments = int(scan_segments or 0)
     o.timeout_probe = 1 if timeout_probe else 0
+    o.verify_kernel = {None: 0, "sequential": 1, "tensor": 2}[verify_kernel]
     return o
 
 
@@ -58,8 +60,9 @@ def overrides(**kw):
     library (tests and measurements): state_kernel ("slab" | "head"),
     segment_chunks (0: never segment, n: segments of n chunks), prep_ctas,
     no_pdl, stall_seed, wait_limit_ns, scan_segments (1: never run the
-    segment-parallel scan, n >= 2: run it with n segments), timeout_probe.
-    Nothing is taken from the environment."""
+    segment-parallel scan, n >= 2: run it with n segments), timeout_probe,
+    verify_kernel ("sequential" | "tensor").  Nothing is taken from the
+    environment."""
     tok = _overrides_var.set(_make_overrides(**kw))
     try:
         yield

@@ -107,3 +107,37 @@ def test_mma_rate_probe_runs(selftest):
         assert status.item() == 0
         issue, total = cyc.tolist()
         assert 0 < issue <= total
+
+
+def _tf32(x):
+    """fp32 -> the tf32 value the tensor core uses (the low 13 mantissa bits
+    dropped)."""
+    b = x.contiguous().view(torch.int32) & ~0x1FFF
+    return b.view(torch.float32)
+
+
+@pytest.mark.parametrize("a_mn,b_mn,N,K", [(0, 0, 32, 128), (0, 0, 16, 128), (0, 0, 128, 16),
+                                           (0, 0, 128, 8), (0, 0, 64, 64), (2, 0, 32, 128),
+                                           (2, 0, 128, 128)])
+def test_umma_tf32_operand_forms(selftest, a_mn, b_mn, N, K):
+    """tcgen05 kind::tf32 with K-major operands (128-byte swizzle, fp32
+    elements) in shared memory, or A (a_mn = 2) in TMEM, one element per
+    column, row m in lane m: the forms of the tensor-core verify kernel's two
+    products (S^T [W; Q']^T with S^T in TMEM: N = 32, K = 128; V_new^T Kt_a^T:
+    N = 128, K = 8 or 16), against a matmul of the tf32-rounded operands.
+    (tf32 operands in shared memory must be K-major: an MN-major tf32 operand
+    gave zeros on GB300.)"""
+    f = selftest.kda_selftest_umma_tf32
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 4 + [ctypes.c_void_p] * 2
+    g = torch.Generator(device="cpu").manual_seed(900 + N + K + 2 * a_mn + b_mn)
+    A = torch.randn(128, K, generator=g).cuda()
+    B = torch.randn(N, K, generator=g).cuda()
+    D = torch.full((128, N), float("nan"), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert f(A.data_ptr(), B.data_ptr(), D.data_ptr(), N, K, a_mn, b_mn, status.data_ptr(),
+             torch.cuda.current_stream().cuda_stream) == 0
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    ref = (_tf32(A).double() @ _tf32(B).double().T).float()
+    torch.testing.assert_close(D, ref, atol=1e-4, rtol=1e-5)

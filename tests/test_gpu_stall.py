@@ -99,17 +99,18 @@ def test_norm_bit_identical_under_stalls():
         assert _same(ref, run(seed)), seed
 
 
+@pytest.mark.parametrize("kernel,D", [("sequential", 4), ("tensor", 4), ("tensor", 11)])
 @pytest.mark.parametrize("pool_dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("replay", [False, True])
-def test_verify_bit_identical_under_stalls(pool_dtype, replay):
+def test_verify_bit_identical_under_stalls(pool_dtype, replay, kernel, D):
     import kda_chunked_prefill_02_gb300 as K
-    vi = inputs.verify_inputs(914, R=40, D=4, H=3)
+    vi = inputs.verify_inputs(914, R=40, D=D, H=3)
     d = vi.to("cuda")
     pool0 = d.state_pool.to(pool_dtype)
 
     def run(seed):
         pool = pool0.clone()
-        with K.overrides(stall_seed=seed or 0):
+        with K.overrides(stall_seed=seed or 0, verify_kernel=kernel):
             out = K.kda_verify(d.q, d.k, d.v, d.g, d.beta, pool, d.accepted, slot=d.slot,
                                replay_only=replay)
             torch.cuda.synchronize()

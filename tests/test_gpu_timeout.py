@@ -114,3 +114,28 @@ def test_timeout_in_the_scan():
     assert status.item() == 0
     ro, rf = oracle_prefill(inp)
     assert_parity(out, fin, ro, rf, "scan after a timed-out scan")
+
+
+def test_timeout_in_the_tensor_core_verify():
+    """The tensor-core verify kernel's first product wait runs out under the
+    probe: the call returns, the status says so, and a normal call on the same
+    stream then matches the oracle."""
+    import numpy as np
+    import kda_chunked_prefill_02_gb300 as K
+    import oracle
+    vi = inputs.verify_inputs(1205, R=20, D=6, H=2)
+    d = vi.to("cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pool = d.state_pool.clone()
+    with K.overrides(verify_kernel="tensor", wait_limit_ns=2000, timeout_probe=True):
+        K.kda_verify(d.q, d.k, d.v, d.g, d.beta, pool, d.accepted, device_status=status)
+    torch.cuda.synchronize()
+    assert status.item() == KDA_ERR_TIMEOUT
+    status.zero_()
+    pool = d.state_pool.clone()
+    with K.overrides(verify_kernel="tensor"):
+        out = K.kda_verify(d.q, d.k, d.v, d.g, d.beta, pool, d.accepted, device_status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    o_ref, _ = oracle.verify(vi.q, vi.k, vi.v, vi.g, vi.beta, vi.state_pool, vi.accepted)
+    assert np.abs(out.float().cpu().numpy() - o_ref).max() <= 2e-2
