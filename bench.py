@@ -62,6 +62,9 @@ def parse():
                     help="measurements: 1 rules the segment-parallel scan out, N >= 2 forces N segments")
     ap.add_argument("--verify-kernel", choices=["auto", "sequential", "tensor"], default="auto",
                     help="--config verify: force the sequential or the tensor-core kernel")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="measurements and profiling captures: the first N tokens of every sequence of "
+                         "the workload (a shorter workload of the same shape)")
     ap.add_argument("--pool", choices=["fp32", "bf16"], default="fp32",
                     help="state pool element type of --config verify")
     ap.add_argument("--drafts", type=int, default=4, choices=range(1, 17), metavar="1..16",
@@ -183,14 +186,19 @@ def captured_traffic(kernel, token_heads):
     return float(rec["dram_bytes_per_token_head"]) * token_heads
 
 
-def workload(name):
+def workload(name, tokens=None):
     from kda_chunked_prefill_02_gb300 import inputs
-    return inputs.config_inputs(name)
+    inp = inputs.config_inputs(name)
+    return inp if tokens is None else inputs.prefix_sample(inp, tokens)
 
 
-def config_dict(name, inp):
+def config_dict(name, inp, tokens=None):
     from kda_chunked_prefill_02_gb300 import inputs
-    return {"workload": name, "description": inputs.CONFIG_DESCRIPTIONS[name],
+    desc = inputs.CONFIG_DESCRIPTIONS[name]
+    if tokens is not None:
+        name = "%s_first%d" % (name, tokens)
+        desc += "; first %d tokens of every sequence" % tokens
+    return {"workload": name, "description": desc,
             "num_seqs": inp.num_seqs, "total_tokens": inp.total_tokens,
             "heads": inp.num_heads, "head_dim": 128, "chunk": 64,
             "l2": "inputs larger than L2 (no flush)" if inp.total_tokens * inp.num_heads * 1284 > 129e6
@@ -230,7 +238,7 @@ def run_ours(args, rank, ws, local):
     import kda_chunked_prefill_02_gb300 as K
 
     hbm, tf_burst, tf_sust, peak_src = peaks()
-    inp = workload(args.config)
+    inp = workload(args.config, args.tokens)
     dev = torch.device("cuda", torch.cuda.current_device())
     d = inp.to(dev)
     N, H, T = inp.num_seqs, inp.num_heads, inp.total_tokens
@@ -431,7 +439,8 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16 q/k/v/out, fp32 gate/beta/state, bf16 tcgen05 MMA with fp32 accumulation",
             "data": "synthetic, seeded (q,k L2-normalised, g=-5*sigmoid(N(0,1)), beta=sigmoid(N(0,1)))",
-            "config": dict(config_dict(args.config, inp), parallelism="replica per GPU" if ws > 1 else "1 GPU"),
+            "config": dict(config_dict(args.config, inp, args.tokens),
+                           parallelism="replica per GPU" if ws > 1 else "1 GPU"),
             "tensor_pipe": {"algorithmic_tflops": r["flops"] / (r["ms"] / 1e3) / 1e12,
                             "peak": r["tf_burst"], "frac": r["tensor_frac"],
                             "note": "whole-call algorithmic tensor FLOP (180,224 per token-head) / call time, of measured peak"},
@@ -464,7 +473,7 @@ def main_reference(args):
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     if rank != 0:
         return
-    inp = workload(args.config)
+    inp = workload(args.config, args.tokens)
     sample = 2048  # tokens of every sequence per step: about 0.15 s of oracle work on 16 cores
     for _ in range(args.warmup):
         cpu_oracle_sample(inp, 64)
@@ -478,7 +487,7 @@ def main_reference(args):
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic, seeded",
-            "config": config_dict(args.config, inp),
+            "config": config_dict(args.config, inp, args.tokens),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": used, "kind": "oracle",
                              "sample": "first %d tokens of every sequence, all heads, per step" % sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
