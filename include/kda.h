@@ -204,7 +204,7 @@ size_t kda_prefill_workspace_size(const kda_prefill_args* args);
  *   A2-A5 per-chunk prep: in-chunk gate cumsum and chunk total, beta sigmoid,
  *      tail masking, gate-scaled operands, the UT transform
  *      (I + Diag(beta) tril(K K^T . decay))^{-1}, W, U and the intra-chunk
- *      attention folded into Q' = Q e^Gam - Aqk W and O_loc = Aqk U;
+ *      attention matrix Aqk;
  *   A6-A7 the serial inter-chunk state pass on tcgen05 tensor cores, per
  *      (sequence, head) chain in four 32-column slab CTAs or one whole-chain
  *      CTA, with the output epilogue (rows stored by TMA tensor stores).
@@ -280,15 +280,16 @@ kda_status kda_prefill_state(const kda_prefill_args* args, void* stream);
  * holds shared-memory images of the state pass's operands.  bf16 images use
  * the 128-byte swizzle (16-byte chunk c of 128-byte row x stored at
  * x*128 + ((c ^ (x mod 8)) * 16)):
- *   [0, 32768)        [W ; Q'] bf16: key channels 0-63 then 64-127, each
- *                     128 rows x 128 B; rows 0-63 W = T Diag(beta)(K e^Gam),
- *                     rows 64-127 Q' = scale*Q e^Gam - Aqk W
- *   [32768, 49152)    Kt bf16: 128 key rows x 64 tokens, (K e^{gam - Gam})^T
- *   [49152, 65536)    U = T Diag(beta) V bf16: value slabs 0-3 (32 columns
+ *   [0, 32768)        [Q e^Gam ; W] bf16: key channels 0-63 then 64-127,
+ *                     each 128 rows x 128 B; rows 0-63 scale*Q e^Gam, rows
+ *                     64-127 W = T Diag(beta)(K e^Gam)
+ *   [32768, 49152)    Kt fp16: 128 key rows x 64 tokens, (K e^{gam - Gam})^T
+ *   [49152, 57344)    Aqk fp16: 64 token rows x 64 tokens, the masked
+ *                     (j <= i) gate-decayed scale*Q K^T of the chunk
+ *   [57344, 73728)    U = T Diag(beta) V bf16: value slabs 0-3 (32 columns
  *                     each, 4 KB), 64-byte rows, 16-byte chunk c of row x at
  *                     x*64 + ((c ^ ((x / 2) mod 4)) * 16)
- *   [65536, 81920)    O_loc = Aqk U bf16, same layout
- *   [81920, 82432)    exp(gam) fp32 [128], gam = chunk total of g
+ *   [73728, 74240)    exp(gam) fp32 [128], gam = chunk total of g
  * Rows past a tail chunk's length are zero.  chunk_offset: int32 [N+1].
  * seq_order (varlen): the sequences by descending chunk count (ties by index;
  * index order beyond 1024 sequences), the order in which the state pass's
@@ -394,8 +395,8 @@ kda_status kda_verify(const kda_verify_args* args, void* stream);
  * Limits and behaviour:
  *  - Returns KDA_ERR_UNSUPPORTED, launching nothing, when
  *    kda_prefill_workspace_size(args) exceeds KDA_NOALLOC_MAX_WORKSPACE_BYTES
- *    (about 400 chunk-head records of 82,432 bytes, less 64 KB of state per
- *    padded chain: e.g. 2048 tokens x 12 heads, or 8192 tokens x 3 heads).
+ *    (about 450 chunk-head records of 74,240 bytes, less 64 KB of state per
+ *    padded chain: e.g. 2048 tokens x 13 heads, or 8192 tokens x 3 heads).
  *  - The first call on each device looks up the array's device address for
  *    that device (with the device current); make that first call before any
  *    stream capture.  It allocates nothing, here or later.

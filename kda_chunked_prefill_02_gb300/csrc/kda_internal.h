@@ -37,19 +37,23 @@ constexpr float kGateFloor = -5.4f;   // per-token gate floor inside 16-token bl
 
 // Workspace record per (chunk, head): shared-memory images, written by the prep
 // kernel with bulk copies and read back by the state pass with bulk copies.
-// [W ; Q'] and Kt use the 128-byte swizzle of K-major tcgen05 operands (16-byte
-// chunk c of 128-byte row r at r*128 + ((c ^ (r & 7)) << 4)).  U and O_loc are
-// bf16 value slabs of 32 columns, 64-byte rows, chunk c of row r at
-// r*64 + ((c ^ ((r >> 1) & 3)) << 4) (conflict-free row reads).
-constexpr uint32_t kRecA1 = 0;          // [W ; Q'] bf16: 2 column blocks x 128 rows x 128 B
-constexpr uint32_t kRecKt = 32768;      // Kt bf16: 128 key rows x 64 tokens
-constexpr uint32_t kRecU = 49152;       // U bf16: 4 value slabs x 64 rows x 32
-constexpr uint32_t kRecOl = 65536;      // O_loc bf16: 4 value slabs x 64 rows x 32
-constexpr uint32_t kRecEg = 81920;      // e^gam fp32 [128]
-constexpr uint32_t kRecBytes = 82432;
-constexpr uint32_t kSlabImg = 4096;     // bytes of one U / O_loc slab image
+// [Q e^Gam ; W], Kt and Aqk use the 128-byte swizzle of K-major tcgen05
+// operands (16-byte chunk c of 128-byte row r at r*128 + ((c ^ (r & 7)) << 4));
+// Aqk follows Kt, so that [Kt ; Aqk] is one 192-row operand.  Kt and Aqk are
+// fp16 (the operands of the products with V_new, which the state pass forms
+// in fp16: 3 more mantissa bits than bf16 where the rounding of V_new reaches
+// the output through 64-term sums).  U is bf16 value slabs of 32 columns,
+// 64-byte rows, chunk c of row r at r*64 + ((c ^ ((r >> 1) & 3)) << 4)
+// (conflict-free row reads).
+constexpr uint32_t kRecA1 = 0;          // [Q e^Gam ; W] bf16: 2 column blocks x 128 rows x 128 B
+constexpr uint32_t kRecKt = 32768;      // Kt fp16: 128 key rows x 64 tokens
+constexpr uint32_t kRecAqk = 49152;     // Aqk fp16: 64 token rows x 64 tokens
+constexpr uint32_t kRecU = 57344;       // U bf16: 4 value slabs x 64 rows x 32
+constexpr uint32_t kRecEg = 73728;      // e^gam fp32 [128]
+constexpr uint32_t kRecBytes = 74240;
+constexpr uint32_t kSlabImg = 4096;     // bytes of one U slab image
 
-// Byte offset of 16-byte chunk c of row r in a U / O_loc slab image.
+// Byte offset of 16-byte chunk c of row r in a U (or output) slab image.
 __host__ __device__ __forceinline__ uint32_t slab_chunk_off(uint32_t r, uint32_t c) {
     return r * 64u + ((c ^ ((r >> 1) & 3u)) << 4);
 }

@@ -9,10 +9,9 @@
 //   A[i,j]   = beta_i sum_c k_i k_j exp(Gam_i - Gam_j)     j <  i
 //   Aqk[i,j] =        sum_c q_i k_j exp(Gam_i - Gam_j)     j <= i
 //   T = (I + A)^-1,  T' = T Diag(beta)
-//   W  = T' (K e^Gam),  U = T' V,  Q' = Q e^Gam - Aqk W,  O_loc = Aqk U
-//   Kt = (K e^{gam - Gam})^T,  eg = e^gam
+//   W  = T' (K e^Gam),  U = T' V,  Kt = (K e^{gam - Gam})^T,  eg = e^gam
 // so that, for the chunk's entry state S, the serial pass only needs
-//   V_new = U - W S,  O = Q' S + O_loc,  S <- Diag(eg) S + Kt V_new.
+//   V_new = U - W S,  O = (Q e^Gam) S + Aqk V_new,  S <- Diag(eg) S + Kt V_new.
 //
 // Overflow guard (the "100% NaN at gate -5" hazard on the cuDNN-frontend sm90
 // KDA page, Conversation): exp(Gam_i - Gam_j) is never formed as
@@ -50,7 +49,7 @@ constexpr uint32_t O_IV = 32768;      // bf16 [64][128] v tile
 constexpr uint32_t O_IG = 49152;      // fp32 [64][128] g tile
 constexpr uint32_t kInBytes = 81920;
 // Once the gate phase has read the g tile, its space stages the record's Kt
-// image (16 KB, same bytes as in the record) and e^gam (512 B).
+// image (16 KB fp16, same bytes as in the record) and e^gam (512 B).
 constexpr uint32_t O_SKT = O_IG;
 constexpr uint32_t O_SEG = O_IG + 16384;
 constexpr uint32_t O_R = 81920;       // A operand R = [K ac ; Q ac]: 2 x (128 rows x 128 B)
@@ -58,12 +57,11 @@ constexpr uint32_t O_Y = 114688;      // B operand [Yoff (96 rows) ; Yd (64 rows
 constexpr uint32_t kYBlock = 160 * 128;
 constexpr uint32_t O_KV = 155648;     // B operand [K e^Gam | V], MN-major: 8 token groups x 4 KB
 constexpr uint32_t kKvSbo = 4096;     // byte distance between 8-token groups of the KV operand
-constexpr uint32_t O_QT = 188416;     // bf16 [64][136] Q e^Gam (row pitch 272 B)
-constexpr uint32_t kQtPitch = 272;
+constexpr uint32_t O_QT = 188416;     // Q e^Gam image: 2 column blocks x 64 rows x 128 B (the record's rows 0-63)
 constexpr uint32_t O_TOT = 205824;    // fp32 [2][8][128] decay products (exact, floored) of 8-token groups
 constexpr uint32_t O_BETA = 214016;   // fp32 [64] beta
 constexpr uint32_t kPrepSmem = 214272 + 1024;
-// Scratch of the solve and MMA B / C, over R and Y once MMA A has completed.
+// Scratch of the solve and MMA C, over R and Y once MMA A has completed.
 // The fp32 matrices hold tf32-rounded values (operands of the warp MMAs); the
 // row pitch 68 (4 mod 32) makes the MMA row-fragment loads and the epilogue's
 // float4 row stores conflict-free.
@@ -72,37 +70,30 @@ constexpr int kPX = 40;               // fp32 row pitch of the products X (8 mod
 constexpr uint32_t O_A = 81920;       // fp32 [64][68] beta-scaled A
 constexpr uint32_t O_T = 99328;       // fp32 [64][68] T
 constexpr uint32_t O_X = 116736;      // fp32 [32][40] products
-constexpr uint32_t O_AQK = 122880;    // A operand Aqk: 64 rows x 128 B (rows 64..127 are don't-care)
-constexpr uint32_t O_TT = 131072;     // A operand [T' ; Aqk T']: 128 rows x 128 B
-constexpr uint32_t O_TTR = 147456;    // B operand T'^T: 64 rows x 128 B
-// Staging of the record images written by the last epilogue (over R, Y, KV).
-constexpr uint32_t O_SA1 = 81920;     // [W ; Q'] image, 32 KB
-constexpr uint32_t O_SU = 114688;     // U image, 16 KB
-constexpr uint32_t O_SOL = 131072;    // O_loc image, 16 KB
+constexpr uint32_t O_AQK = 122880;    // Aqk image, fp16: 64 rows x 128 B (the record's, K-major over tokens)
+constexpr uint32_t O_TT = 131072;     // A operand [T' ; T']: 128 rows x 128 B
+// Staging of the record images written by the last epilogue (over the solve's
+// scratch, which MMA C no longer needs).
+constexpr uint32_t O_SW = 81920;      // W image: 2 column blocks x 64 rows x 128 B (the record's rows 64-127)
+constexpr uint32_t O_SU = 98304;      // U image, 16 KB
 
 // TMEM columns.
-constexpr uint32_t TM_A = 0, TM_DIAG = 96, TM_B = 192, TM_C = 0, TM_COLS = 256;
+constexpr uint32_t TM_A = 0, TM_DIAG = 96, TM_C = 0, TM_COLS = 256;
 
-__device__ __forceinline__ float2 ld_bf16x2(const uint8_t* p) {
-    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
-}
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
     return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 __device__ __forceinline__ void st_u32(uint8_t* p, uint32_t v) {
     *reinterpret_cast<uint32_t*>(p) = v;
 }
-__device__ __forceinline__ void st_bf16(uint8_t* p, float v) {
-    *reinterpret_cast<__nv_bfloat16*>(p) = __float2bfloat16_rn(v);
-}
 // Stores T' = T Diag(beta) entries (i, j) and (i, j + 1) of a computed T block
-// into the TT operand (row i, K index j) and the T'^T operand (row j, K index i).
+// into the TT operand, rows i and 64 + i (MMA C then writes W and U to both
+// halves of TMEM's lanes, so that every epilogue warp has work).
 __device__ __forceinline__ void store_tprime_pair(uint8_t* sm, int i, int j, float t0, float t1,
                                                   const float* sBeta) {
-    const float a = t0 * sBeta[j], b = t1 * sBeta[j + 1];
-    st_u32(sm + O_TT + sw128_off(i, j), pack_bf16x2(a, b));
-    st_bf16(sm + O_TTR + sw128_off(j, i), a);
-    st_bf16(sm + O_TTR + sw128_off(j + 1, i), b);
+    const uint32_t ab = pack_bf16x2(t0 * sBeta[j], t1 * sBeta[j + 1]);
+    st_u32(sm + O_TT + sw128_off(i, j), ab);
+    st_u32(sm + O_TT + sw128_off(64 + i, j), ab);
 }
 // Row of the Yoff operand holding column block J as seen from row block I > J:
 // block I's group holds its 16*I earlier columns.
@@ -162,7 +153,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-    __shared__ uint64_t bar_in, bar_mma[3], bar_fin, bar_never;
+    __shared__ uint64_t bar_in, bar_mma[2], bar_fin, bar_never;
     __shared__ uint32_t tmem_base_sh;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -170,7 +161,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     if (blockIdx.x >= nrec) return;
     if (tid == 0) {
         mbar_init(&bar_in, 1);
-        for (int i = 0; i < 3; ++i) mbar_init(&bar_mma[i], 1);
+        for (int i = 0; i < 2; ++i) mbar_init(&bar_mma[i], 1);
         mbar_init(&bar_fin, 1);
         mbar_init(&bar_never, 1);   // nothing arrives on it (the timeout probe's wait)
         fence_mbar_init();
@@ -316,8 +307,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                     // R = [K ac ; Q ac]
                     st_u32(sm + O_R + bo + sw128_off(i, cc), pack_bf16x2(kk.x * ac0, kk.y * ac1));
                     st_u32(sm + O_R + bo + sw128_off(64 + i, cc), pack_bf16x2(qq.x * ac0, qq.y * ac1));
-                    // Q e^Gam for Q', [K e^Gam | V] (MN-major: token row i, channels contiguous)
-                    st_u32(sm + O_QT + i * kQtPitch + c0 * 2, pack_bf16x2(qq.x * a0, qq.y * a1));
+                    // the record's Q e^Gam rows; [K e^Gam | V] (MN-major: token row i, channels contiguous)
+                    st_u32(sm + O_QT + blk * 8192u + sw128_off(i, cc), pack_bf16x2(qq.x * a0, qq.y * a1));
                     st_u32(sm + O_KV + mn_sw128_off(i, c0, kKvSbo), pack_bf16x2(kk.x * a0, kk.y * a1));
                     st_u32(sm + O_KV + mn_sw128_off(i, 128 + c0, kKvSbo), vw[l]);
                 }
@@ -349,13 +340,13 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                         if (I > G)
                             st_u32(sm + O_Y + yb + sw128_off(yoff_row(I, G, 8 * hf + l), cc),
                                    pack_bf16x2(kz0 * Dm0[I], kz1 * Dm1[I]));
-                    // Kt = (K e^{gam - Gam})^T, packed by token pairs
+                    // Kt = (K e^{gam - Gam})^T in fp16, packed by token pairs
                     const float hh0 = kz0 * E0, hh1 = kz1 * E1;
                     if (l & 1) {
                         eh0 = hh0; eh1 = hh1;
                     } else {
-                        kh0[l >> 1] = pack_bf16x2(hh0, eh0);
-                        kh1[l >> 1] = pack_bf16x2(hh1, eh1);
+                        kh0[l >> 1] = pack_f16x2(hh0, eh0);
+                        kh1[l >> 1] = pack_f16x2(hh1, eh1);
                     }
                     z0 *= p0[l]; z1 *= p1[l];
                     zc0 *= fmaxf(p0[l], kPFloor); zc1 *= fmaxf(p1[l], kPFloor);
@@ -376,10 +367,12 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             umma_tile(tb + TM_A, smem_u32(sm + O_R), 16384, smem_u32(sm + O_Y), kYBlock, 128,
                       idesc_bf16_f32(128, 160), false);
             umma_commit(&bar_mma[0]);
-            // The Kt and e^gam images leave by bulk copy.
+            // The Kt, e^gam and Q e^Gam images leave by bulk copy.
             uint8_t* rp = p.ws_rec + (size_t)rec * kRecBytes;
             bulk_store(rp + kRecKt, sm + O_SKT, 16384);
             bulk_store(rp + kRecEg, sm + O_SEG, 512);
+            bulk_store(rp + kRecA1, sm + O_QT, 8192);
+            bulk_store(rp + kRecA1 + 16384, sm + O_QT + 8192, 8192);
             bulk_commit();
         }
         if (cn.len > 0) bcur = load_beta(cn, rec_next % p.H);
@@ -401,7 +394,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         const float* sBeta = reinterpret_cast<const float*>(sm + O_BETA);
         {
             // ---- Epilogue A: TMEM rows 0..63 are k rows (-> A, beta-scaled, j < i),
-            // rows 64..127 are q rows (-> Aqk, j <= i, bf16 operand of MMA B).
+            // rows 64..127 are q rows (-> Aqk, j <= i, the record's fp16 image).
             const bool isq = qd >= 2;
             const int i = 32 * (qd & 1) + lane, I = i >> 4, I0 = 2 * (qd & 1), I1 = I0 + 1;
             const bool lo = lane < 16;
@@ -437,7 +430,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             } else {
                 uint32_t w[8];
 #pragma unroll
-                for (int x = 0; x < 8; ++x) w[x] = pack_bf16x2(v[2 * x], v[2 * x + 1]);
+                for (int x = 0; x < 8; ++x) w[x] = pack_f16x2(v[2 * x], v[2 * x + 1]);
                 *reinterpret_cast<uint4*>(sm + O_AQK + sw128_off(i, 16 * J)) = make_uint4(w[0], w[1], w[2], w[3]);
                 *reinterpret_cast<uint4*>(sm + O_AQK + sw128_off(i, 16 * J + 8)) = make_uint4(w[4], w[5], w[6], w[7]);
             }
@@ -446,6 +439,10 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
+        if (tid == 0) {
+            bulk_store(p.ws_rec + (size_t)rec * kRecBytes + kRecAqk, sm + O_AQK, 8192);
+            bulk_commit();
+        }
 
         // ---- UT transform: T = (I + A)^-1 for the unit lower-triangular 64 x 64
         // system, blocked: four 16 x 16 diagonal inverses by forward substitution,
@@ -478,17 +475,15 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             const int i = s0 + m, j = s0 + l;
             *reinterpret_cast<float2*>(sT + i * kPA + j) = make_float2(tf32_round(xa), tf32_round(xb));
             store_tprime_pair(sm, i, j, xa, xb, sBeta);
-            // Zero the 16 x 16 blocks of T' above the diagonal (TT: column block
-            // J > row block I) and below it in T'^T: 12 blocks x 16 rows x 2 chunks.
-            if (tid < 12 * 32) {
-                const int blkid = tid >> 5, rr = (tid >> 1) & 15, hc = tid & 1;
-                const int bi = blkid % 6;
+            // Zero the 16 x 16 blocks of T' above the diagonal (column block J >
+            // row block I), in both row halves of TT: 6 blocks x 16 rows x 2 chunks.
+            if (tid < 6 * 32) {
+                const int bi = tid >> 5, rr = (tid >> 1) & 15, hc = tid & 1;
                 const int Ib = bi < 3 ? 0 : (bi < 5 ? 1 : 2);
                 const int Jb = bi < 3 ? bi + 1 : (bi < 5 ? bi - 1 : 3);
-                const int row = blkid < 6 ? 16 * Ib + rr : 16 * Jb + rr;
-                const int col = blkid < 6 ? 16 * Jb + 8 * hc : 16 * Ib + 8 * hc;
-                *reinterpret_cast<uint4*>(sm + (blkid < 6 ? O_TT : O_TTR) + sw128_off(row, col)) =
-                    make_uint4(0u, 0u, 0u, 0u);
+                const int row = 16 * Ib + rr, col = 16 * Jb + 8 * hc;
+                *reinterpret_cast<uint4*>(sm + O_TT + sw128_off(row, col)) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(sm + O_TT + sw128_off(64 + row, col)) = make_uint4(0u, 0u, 0u, 0u);
             }
         }
         stall_point<kStall>(p.stall_seed, 7, it);
@@ -533,34 +528,10 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         }
         stall_point<kStall>(p.stall_seed, 10, it);
         fence_proxy_async_smem();
-        __syncthreads();
-        // ---- MMA B: D_b = Aqk T'  -> rows 64..127 of the TT operand
-        if (tid == 0) {
-            tc_fence_after();
-            umma_tile(tb + TM_B, smem_u32(sm + O_AQK), 0, smem_u32(sm + O_TTR), 0, 64,
-                      idesc_bf16_f32(128, 64), false);
-            umma_commit(&bar_mma[1]);
-        }
-        ok = __syncthreads_and(tid == 0 ? mbar_wait(&bar_mma[1], it & 1, nullptr, p.wait_ns) : true);
-        tc_fence_after();
-        if (!ok) break;
-        stall_point<kStall>(p.stall_seed, 11, it);
-        if (qd < 2) {
-            const int i = 32 * qd + lane;
-            {
-                const int col = 16 * cq;
-                float v[16];
-                tmem_ld16(tmem_addr(tb, 32 * qd, TM_B + col), v);
-#pragma unroll
-                for (int x = 0; x < 16; x += 2)
-                    st_u32(sm + O_TT + sw128_off(64 + i, col + x), pack_bf16x2(v[x], v[x + 1]));
-            }
-        }
-        fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
 
-        // ---- MMA C: [T' ; Aqk T'] [K e^Gam | V] = [W | U ; Aqk W | Aqk U]  (N = 256)
+        // ---- MMA C: [T' ; T'] [K e^Gam | V] = [W | U ; W | U]  (N = 256)
         if (tid == 0) {
             tc_fence_after();
             const uint32_t tt = smem_u32(sm + O_TT), kv = smem_u32(sm + O_KV);
@@ -568,54 +539,37 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                 umma_bf16(tb + TM_C, sdesc_kmajor_sw128(tt + k * 32u),
                           sdesc_mnmajor_sw128(kv + k * 2u * kKvSbo, 1024u, kKvSbo),
                           idesc_bf16_f32_bmn(128, 256), k > 0 ? 1u : 0u);
-            umma_commit(&bar_mma[2]);
+            umma_commit(&bar_mma[1]);
         }
-        ok = __syncthreads_and(tid == 0 ? mbar_wait(&bar_mma[2], it & 1, nullptr, p.wait_ns) : true);
+        ok = __syncthreads_and(tid == 0 ? mbar_wait(&bar_mma[1], it & 1, nullptr, p.wait_ns) : true);
         tc_fence_after();
         if (!ok) break;
         stall_point<kStall>(p.stall_seed, 12, it);
         {
-            // ---- Epilogue C: [W ; Q'] rows (Q' = Q e^Gam - Aqk W) from the first 128
-            // columns and U / O_loc from the last 128, written as the record's
-            // shared-memory images and stored with bulk copies.
-            const int r = 32 * qd + lane, i = r & 63;
-            const bool top = qd < 2;
-            const int half = cq >> 1;
-#pragma unroll 1
-            for (int cg2 = 0; cg2 < 2; ++cg2) {
-              // two 16-column groups per load wait
-              float vv[32];
-              tmem_ld32(tmem_addr(tb, 32 * qd, TM_C + 128 * half + 64 * (cq & 1) + 32 * cg2), vv);
+            // ---- Epilogue C: W from the upper lanes' first 128 columns, U from the
+            // lower lanes' last 128 (the same rows twice), 32 columns per warp,
+            // written as the record's shared-memory images and stored with bulk
+            // copies.
+            const bool wpart = qd < 2;
+            const int i = 32 * (qd & 1) + lane;
+            float v[32];
+            tmem_ld32(tmem_addr(tb, 32 * qd, TM_C + (wpart ? 0 : 128) + 32 * cq), v);
+            uint32_t w[16];
 #pragma unroll
-              for (int hh = 0; hh < 2; ++hh) {
-                const int col = 64 * (cq & 1) + 32 * cg2 + 16 * hh;
-                const float* v = vv + 16 * hh;
-                if (half == 0) {
-                    uint32_t w[8];
-                    if (top) {
+            for (int x = 0; x < 16; ++x) w[x] = pack_bf16x2(v[2 * x], v[2 * x + 1]);
+            if (wpart) {
+                uint8_t* img = sm + O_SW + (cq >> 1) * 8192;
+                const int c0w = 32 * (cq & 1);
 #pragma unroll
-                        for (int x = 0; x < 8; ++x) w[x] = pack_bf16x2(v[2 * x], v[2 * x + 1]);
-                    } else {
-                        const uint8_t* qt = sm + O_QT + i * kQtPitch + col * 2;
+                for (int x = 0; x < 4; ++x)
+                    *reinterpret_cast<uint4*>(img + sw128_off(i, c0w + 8 * x)) =
+                        make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+            } else {
+                uint8_t* img = sm + O_SU + cq * kSlabImg;
 #pragma unroll
-                        for (int x = 0; x < 8; ++x) {
-                            const float2 q2 = ld_bf16x2(qt + 4 * x);
-                            w[x] = pack_bf16x2(q2.x - v[2 * x], q2.y - v[2 * x + 1]);
-                        }
-                    }
-                    uint8_t* img = sm + O_SA1 + (col >> 6) * 16384;
-                    *reinterpret_cast<uint4*>(img + sw128_off(r, col & 63)) = make_uint4(w[0], w[1], w[2], w[3]);
-                    *reinterpret_cast<uint4*>(img + sw128_off(r, (col & 63) + 8)) = make_uint4(w[4], w[5], w[6], w[7]);
-                } else {
-                    uint8_t* img = sm + (top ? O_SU : O_SOL) + (col >> 5) * kSlabImg;
-                    const int c8 = (col & 31) >> 3;
-                    uint32_t w[8];
-#pragma unroll
-                    for (int x = 0; x < 8; ++x) w[x] = pack_bf16x2(v[2 * x], v[2 * x + 1]);
-                    *reinterpret_cast<uint4*>(img + slab_chunk_off(i, c8)) = make_uint4(w[0], w[1], w[2], w[3]);
-                    *reinterpret_cast<uint4*>(img + slab_chunk_off(i, c8 + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
-                }
-              }
+                for (int x = 0; x < 4; ++x)
+                    *reinterpret_cast<uint4*>(img + slab_chunk_off(i, x)) =
+                        make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
             }
         }
         stall_point<kStall>(p.stall_seed, 13, it);
@@ -624,9 +578,9 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         __syncthreads();
         if (tid == 0) {
             uint8_t* rp = p.ws_rec + (size_t)rec * kRecBytes;
-            bulk_store(rp + kRecA1, sm + O_SA1, 32768);
+            bulk_store(rp + kRecA1 + 8192, sm + O_SW, 8192);
+            bulk_store(rp + kRecA1 + 16384 + 8192, sm + O_SW + 8192, 8192);
             bulk_store(rp + kRecU, sm + O_SU, 4 * kSlabImg);
-            bulk_store(rp + kRecOl, sm + O_SOL, 4 * kSlabImg);
             bulk_commit();
         }
         // Epilogue C's TMEM reads are ordered before the next record's MMA A by

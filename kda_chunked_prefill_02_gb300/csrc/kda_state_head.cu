@@ -1,33 +1,43 @@
 // kda_state_head.cu -- the serial inter-chunk state pass (steps A6-A7) with one
 // CTA per whole chain (sequence n, head h): all 128 value columns of the state.
 //
-// A tcgen05.mma of M = 128 and K = 16 takes the same ~100 SM cycles for every
-// N <= 128 on this GPU (measured by the MMA throughput probe in the selftest
-// library), so one CTA that runs the chunk step at N = 128 costs about what a
-// 32-column slab CTA costs, and needs a quarter of the CTAs.  That matters when
-// there are more chains than SMs (the slab kernel then runs in several waves),
-// and it leaves SMs free for other work.  Per chunk, with the record the prep
-// kernel left (W, Q', Kt, U, O_loc, e^gam):
-//   P1 (tensor core)  D1 = [W ; Q'] S    M = 128 (64 W rows + 64 Q' rows), N = 128, K = 128
-//   epilogue          V_new = U - D1[0:64],  O = O_loc + D1[64:128] -> out (bf16)
-//   P2 (tensor core)  D2 = Kt V_new       M = 128 keys, N = 128, K = 64 tokens
-//   epilogue          S <- Diag(e^gam) S + D2   (fp32 in registers, bf16 image for P1)
-// Warp roles: all 16 warps are the epilogue, warp w owning TMEM lane quarter
-// w % 4 and the 32-column quarter w / 4, so a thread holds 32 fp32 state
-// values as in the slab kernel.  An MMA issue holds its thread for about the
-// product's duration, so P1 is issued by a thread of an output warp (every warp
-// waits for P1) and P2 by a thread of a V_new warp (those wait for P2, while
-// the output warps compute and store the output rows).  A thread of another
-// output warp issues the output tensor stores and the record copies: each
-// record arrives by one 1-D bulk copy into one of two stages, issued as soon as
-// the chunk barrier has shown the stage's previous chunk finished with it (P2
-// complete, every read done, the stores' reads of the staged rows done), with
-// an L2 prefetch further ahead.  Hand-offs are
-// mbarriers and named barriers; every mbarrier wait is bounded, and the chunk
-// barrier's OR-reduction of the abort flag makes all epilogue warps stop at the
-// same chunk.  Every MMA has completed, and every thread that read TMEM has
-// waited for its loads and crossed a tcgen05 fence plus a CTA barrier, before
-// TMEM is freed (the dealloc ordering of the TensorRT-LLM MQA-logits page).
+// The chunk step runs in the transposed orientation: the TMEM lanes are the
+// 128 value columns of the state, so that both tensor-core products take their
+// A operand from TMEM and every operand the threads produce goes to TMEM
+// (tcgen05.st) rather than to a shared-memory image behind a proxy fence.  The
+// fp32 state itself lives in TMEM as the accumulator of the second product.
+// Per chunk, with the record the prep kernel left (Q e^Gam, W, Kt, Aqk, U,
+// e^gam):
+//   decay             S^T <- S^T Diag(e^gam)                 (threads, in TMEM)
+//   P1 (tensor core)  D1^T = S_in^T [Q e^Gam ; W]^T          M = 128 values, N = 128, K = 128 keys
+//   epilogue          V_new^T = U^T - D1^T[W part]           (fp16, to TMEM: P23's A operand)
+//   P23 (tensor core) [S^T | D1^T[Q part]] += V_new^T [Kt ; Aqk]^T   N = 192 (128 keys + 64 tokens), K = 64
+//   epilogue          S^T (the next entry state) -> bf16 to TMEM (P1's A operand);
+//                     O^T = D1^T[Q part] = (Q e^Gam) S_in + Aqk V_new -> out (bf16)
+// S_in is the chunk's entry state; the decay with the chunk's e^gam is applied
+// to the TMEM copy before P23 accumulates Kt V_new onto it.  One instruction
+// of M = 128, K = 16 takes about the same time for any N up to 128 on this GPU
+// and not much more at N = 192, so the output product rides along with the
+// state update.
+//
+// Warp roles: warp w owns TMEM lane quarter qd = w % 4 (value columns 32 qd ..
+// 32 qd + 31, thread = one value column v) and column quarter cq = w / 4: in
+// D1 32 tokens of the Q part (cq 0, 1: the output warps) or of the W part
+// (cq 2, 3: the V_new warps, two on every SM sub-partition), in the state 32
+// keys.  An MMA issue holds its thread for about the product's duration, so P1
+// is issued by a thread of an output warp as soon as the chunk barrier has
+// published the state operand, and P23 by a thread of a V_new warp (those wait
+// for P23 anyway).  The output warps take the output of chunk c while P1 of
+// chunk c + 1 runs.  A thread of another output warp issues the output tensor
+// stores and the record copies: each record arrives by one 1-D bulk copy into
+// one of two stages, issued as soon as the chunk barrier has shown the stage's
+// previous chunk finished with it, with an L2 prefetch further ahead.
+// Hand-offs are mbarriers and named barriers; every mbarrier wait is bounded,
+// and the chunk barrier's OR-reduction of the abort flag makes all warps stop
+// at the same chunk.  Every MMA has completed, and every thread that read TMEM
+// has waited for its loads and crossed a tcgen05 fence plus a CTA barrier,
+// before TMEM is freed (the dealloc ordering of the TensorRT-LLM MQA-logits
+// page).
 #include "kda_internal.h"
 #include "sm103.cuh"
 
@@ -35,24 +45,26 @@ namespace kda {
 namespace {
 
 constexpr int kHeadThreads = 16 * 32;
-constexpr uint32_t SH_A1 = 0;          // [W ; Q'] 2 x (128 rows x 128 B)
-constexpr uint32_t SH_KT = 32768;      // Kt 128 rows x 128 B
-constexpr uint32_t SH_U = 49152;       // U: 4 value slabs (64-byte swizzle), 16 KB
-constexpr uint32_t SH_OL = 65536;      // O_loc, same layout
-constexpr uint32_t SH_EG = 81920;      // e^gam [128] fp32
+// A stage holds one record as the prep kernel wrote it (one bulk copy).
+constexpr uint32_t SH_A1 = kRecA1;     // [Q e^Gam ; W] 2 x (128 rows x 128 B), K-major: P1's B operand
+constexpr uint32_t SH_KT = kRecKt;     // [Kt ; Aqk] 192 rows x 128 B, K-major: P23's B operand
+constexpr uint32_t SH_U = kRecU;       // U: 4 value slabs (64-byte swizzle), 16 KB
+constexpr uint32_t SH_EG = kRecEg;     // e^gam [128] fp32
 constexpr uint32_t kHStageTx = kRecBytes;  // the whole record, one bulk copy
-constexpr uint32_t kHStage = 82944;     // kRecBytes rounded up to 1 KB (swizzle atoms)
+constexpr uint32_t kHStage = 74752;     // kRecBytes rounded up to 1 KB (swizzle atoms)
 constexpr int kHStages = 2;
 constexpr int kHPrefetchAhead = 4;
-// B operands of P1 and P2, MN-major with the 128-byte swizzle: per K index
-// (key for S, token for V_new) two 64-column atoms 1024 B apart, 8-row groups
-// 2048 B apart.
-constexpr uint32_t kHSbo = 2048;
-constexpr uint32_t OH_S = kHStages * kHStage;       // S bf16: 128 key rows (32 KB)
-constexpr uint32_t OH_VN = OH_S + 32768;            // V_new bf16: 64 token rows (16 KB)
-constexpr uint32_t kHeadSmem = OH_VN + 16384 + 1024;
-constexpr uint32_t TMH_D1 = 0, TMH_D2 = 128, TMH_COLS = 256;
+constexpr uint32_t OH_OUT = kHStages * kHStage;   // output rows: 4 slabs [64 tokens x 32 values] bf16
+constexpr uint32_t kHeadSmem = OH_OUT + 4 * kSlabImg + 1024;
+// TMEM columns (lane = value column v).
+constexpr uint32_t TMH_S = 0;      // S^T fp32: keys 0..127 (P23 accumulates onto it)
+constexpr uint32_t TMH_D1 = 128;   // D1^T fp32: Q part (tokens 0..63, P23 adds Aqk V_new), then W part
+constexpr uint32_t TMH_AS = 256;   // S^T bf16 pairs: keys 0..127 in 64 columns (P1's A operand)
+constexpr uint32_t TMH_AV = 320;   // V_new^T fp16 pairs: tokens 0..63 in 32 columns (P23's A operand)
+constexpr uint32_t TMH_COLS = 512;
 constexpr uint32_t kBarHVn = 1, kBarHChunk = 2, kBarHNorm = 3, kBarHOut = 4;  // named barriers (0 is __syncthreads)
+static_assert(kRecAqk == kRecKt + 16384, "P23's B operand is Kt followed by Aqk");
+static_assert(kRecBytes <= kHStage, "a record fits a stage");
 
 // sigmoid(x) = 1/2 + tanh(x/2)/2, with the hardware tanh approximation
 // (relative error ~2^-11, below the bf16 rounding of the output).
@@ -68,16 +80,32 @@ __device__ __forceinline__ bool warp_wait_h(uint64_t* bar, uint32_t parity, vola
     return __all_sync(0xffffffffu, ok);
 }
 
-// Row `r`, columns 32*cq .. 32*cq + 31 of an MN-major image: four 16-byte chunks.
-__device__ __forceinline__ void store_quarter(uint8_t* base, int r, int cq, const float* x) {
-    uint8_t* rp = base + (r >> 3) * kHSbo + (cq >> 1) * 1024 + (r & 7) * 128;
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t b) {
+    return __uint_as_float(b << 16);
+}
+
+// Byte offset of element (token t, value column v) in a 4-slab U / output image
+// (slab v / 32, 64-byte rows of 32 values, 16-byte chunks swizzled).
+__device__ __forceinline__ uint32_t slab_elem_off(int t, int v) {
+    return (uint32_t)(v >> 5) * kSlabImg + slab_chunk_off((uint32_t)t, (uint32_t)((v & 31) >> 3)) +
+           (uint32_t)(v & 7) * 2u;
+}
+
+// The 32 values x[0..31] of each lane summed over the warp's 32 lanes: after the
+// call lane l holds the sum of index l (31 shuffles; each round halves the
+// indices a lane keeps).
+__device__ __forceinline__ float warp_transpose_sum(float (&x)[32], int lane) {
 #pragma unroll
-    for (int ch = 0; ch < 4; ++ch) {
-        const int c = 4 * (cq & 1) + ch;
-        *reinterpret_cast<uint4*>(rp + ((c ^ (r & 7)) << 4)) =
-            make_uint4(pack_bf16x2(x[8 * ch], x[8 * ch + 1]), pack_bf16x2(x[8 * ch + 2], x[8 * ch + 3]),
-                       pack_bf16x2(x[8 * ch + 4], x[8 * ch + 5]), pack_bf16x2(x[8 * ch + 6], x[8 * ch + 7]));
+    for (int s = 16; s >= 1; s >>= 1) {
+        const bool upper = (lane & s) != 0;
+#pragma unroll
+        for (int j = 0; j < s; ++j) {
+            const float send = upper ? x[j] : x[j + s];
+            const float keep = upper ? x[j + s] : x[j];
+            x[j] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+        }
     }
+    return x[0];
 }
 
 template <bool kStall>
@@ -89,7 +117,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
     __shared__ uint64_t full[kHStages], p1_done, p2_done, bar_fin, bar_fin2, bar_never;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
-    __shared__ float s_ss[4][64];      // fused norm: partial sums of squares per column quarter
+    __shared__ float s_ss[4][64];      // fused norm: partial sums of squares per lane quarter
     __shared__ __align__(16) float s_w[kHeadDim];  // fused norm: weights
 
     const int h = blockIdx.x;
@@ -157,23 +185,23 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
     };
 
     {
-        // ---------------- lane quarter qd, column quarter cq, thread row = key / token
+        // ---------------- lane quarter qd (value column v), column quarter cq
         const int qd = warp & 3, cq = warp >> 2;
-        const int row = 32 * qd + lane;
+        const int v = 32 * qd + lane;
+        const bool vwarp = cq >= 2;         // V_new warp (W part) or output warp (Q part)
+        const int tq = 32 * (cq & 1);       // this warp's first token within its part
+        const int k0 = 32 * cq;             // this thread's first key in the state
         const uint32_t lane_base = (uint32_t)(32 * qd) << 16;
-        // P1 and the copies: a thread of an output warp; P2: a thread of a V_new
-        // warp, which waits for P2 anyway, so that the output warps' work is not
-        // held up behind the P2 issue.
-        const bool issuer = (warp == 2 && lane == 0);
-        const bool issuer2 = (warp == 0 && lane == 0);
-        // The output tensor stores and the record copies: a thread of another
-        // output warp, so that the P1 thread goes from the chunk barrier straight
-        // to the next P1.
-        const bool storer = (warp == 3 && lane == 0);
-        const uint32_t id = idesc_bf16_f32_bmn(128, 128);
-        const uint32_t sS_addr = smem_u32(sm + OH_S), sVn_addr = smem_u32(sm + OH_VN);
-        float S[kSlab];
-        const size_t blk_off = (size_t)row * kHeadDim + kSlab * cq;   // inside a 128 x 128 block
+        const uint32_t d1_col = TMH_D1 + 32 * cq;   // Q part (cq 0, 1) or W part (cq 2, 3)
+        // P1: a thread of an output warp; P23: a thread of a V_new warp; the output
+        // tensor stores and the record copies: a thread of another output warp.
+        const bool issuer = (warp == 0 && lane == 0);
+        const bool issuer2 = (warp == 8 && lane == 0);
+        const bool storer = (warp == 1 && lane == 0);
+        // P1 in bf16 (S and the record's rows), P23 in fp16 (V_new, Kt and Aqk)
+        const uint32_t id1 = idesc_bf16_f32(128, 128), id2 = idesc_f16_f32(128, 192);
+        float S[kSlab];                     // S[k0 + j][v]
+        const size_t blk_off = (size_t)k0 * kHeadDim + v;   // element (k0, v) of a 128 x 128 block
         const size_t st_off = chain * kHeadDim * kHeadDim + blk_off;
         // Entry state: the call's initial state, or in the scan the identity
         // (transition), zero (offset) or the combine's entry state E_seg.
@@ -183,203 +211,199 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
             h0 = p.scan_entry + ((size_t)seg * p.N * p.H + chain) * kHeadDim * kHeadDim + blk_off;
         if (zero_u) {
 #pragma unroll
-            for (int j = 0; j < kSlab; ++j) S[j] = (row == kSlab * cq + j) ? 1.f : 0.f;
+            for (int j = 0; j < kSlab; ++j) S[j] = (k0 + j == v) ? 1.f : 0.f;
         } else if (h0) {
-            const float4* src = reinterpret_cast<const float4*>(h0);
 #pragma unroll
-            for (int x = 0; x < kSlab / 4; ++x) {
-                const float4 t = src[x];
-                S[4 * x] = t.x; S[4 * x + 1] = t.y; S[4 * x + 2] = t.z; S[4 * x + 3] = t.w;
-            }
+            for (int j = 0; j < kSlab; ++j) S[j] = h0[(size_t)j * kHeadDim];
         } else {
 #pragma unroll
             for (int j = 0; j < kSlab; ++j) S[j] = 0.f;
         }
-        // Records of chunks 0 and 1 into the two stages.
+        // S^T in bf16 into P1's A operand: keys k0 .. k0 + 31 of lane v.
+        auto store_state_operand = [&]() {
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(S[2 * i], S[2 * i + 1]);
+            tmem_st16(tmem_addr(tb, 32 * qd, TMH_AS + 16 * cq), w);
+        };
         auto issue_load = [&](int c) {
             const int st = c % kHStages;
             mbar_arrive_expect_tx(&full[st], kHStageTx);
             bulk_load(sm + st * kHStage, rec_ptr(c), kRecBytes, &full[st]);
             if (c + kHPrefetchAhead < count) bulk_prefetch_l2(rec_ptr(c + kHPrefetchAhead), kRecBytes);
         };
+        // P1 of chunk c: D1^T = S^T [Q e^Gam ; W]^T (B: 128 token rows, K-major in
+        // two 64-key column blocks; A: S^T from TMEM, 8 columns per 16 keys).
+        auto issue_p1 = [&](int c) {
+            const uint8_t* sb = sm + (c % kHStages) * kHStage;
+            tc_fence_after();
+            const uint64_t bd = sdesc_kmajor_sw128(smem_u32(sb + SH_A1));
+#pragma unroll
+            for (uint32_t k = 0; k < 8; ++k)
+                umma_bf16_ta(tb + TMH_D1, tb + TMH_AS + 8 * k, bd + ((k >> 2) * (16384 >> 4) + (k & 3) * 2),
+                             id1, k > 0 ? 1u : 0u);
+            umma_commit(&p1_done);
+        };
+        // x: the output warps' O^T values (tokens tq .. tq + 31 of value column v),
+        // kept from the end of a chunk to the next one; the V_new warps' U values.
+        float x[kSlab];
+        // The output of chunk co (O^T in x): the optional gated RMSNorm, then the
+        // rows leave by tensor store (chunks inside their sequence; padded calls:
+        // every chunk, the tensor map clips the rows past T) or one by one (a
+        // varlen tail chunk, which the next sequence's rows follow).
+        auto output = [&](int co, bool ok) {
+            const int t0 = 64 * (cbase + co);
+            if (p.gate) {
+                // gated RMSNorm over the 128 channels of each token row: the
+                // lanes' squares meet by a transposing warp sum, the four lane
+                // quarters' partial sums in shared memory
+                float sq[kSlab];
+#pragma unroll
+                for (int j = 0; j < kSlab; ++j) sq[j] = x[j] * x[j];
+                s_ss[qd][tq + lane] = warp_transpose_sum(sq, lane);
+                named_bar_sync(kBarHNorm, 256);  // the eight output warps
+                const float ms = (s_ss[0][tq + lane] + s_ss[1][tq + lane] + s_ss[2][tq + lane] +
+                                  s_ss[3][tq + lane]) * (1.0f / kHeadDim);
+                const float rn_l = rsqrtf(ms + p.norm_eps);   // token tq + lane
+                const float wv = s_w[v];
+                const __nv_bfloat16* gp = p.gate + b * p.gts[0] + h * p.gts[2] + v;
+                const int64_t tg0 = (int64_t)tbase + t0 + tq;
+#pragma unroll
+                for (int j = 0; j < kSlab; ++j) {
+                    const float rn = __shfl_sync(0xffffffffu, rn_l, j);
+                    float gv = 0.f;
+                    if (ok && t0 + tq + j < seq_len) gv = __bfloat162float(gp[(tg0 + j) * p.gts[1]]);
+                    x[j] *= rn * wv * sigmoid_fast(gv);
+                }
+            }
+            stall_point<kStall>(p.stall_seed, 3, co);
+            const bool by_tma = p.out_tma && (p.cu == nullptr || t0 + kChunk <= seq_len);
+            if (by_tma) {
+                uint8_t* img = sm + OH_OUT;
+#pragma unroll
+                for (int j = 0; j < kSlab; ++j)
+                    *reinterpret_cast<__nv_bfloat16*>(img + slab_elem_off(tq + j, v)) = __float2bfloat16_rn(x[j]);
+                fence_proxy_async_smem();
+                named_bar_sync(kBarHOut, 256);  // the eight output warps
+                if (storer && ok && !*abort) {
+                    const int tok = (int)(p.cu == nullptr ? t0 : (int64_t)tbase + t0);
+#pragma unroll
+                    for (int sl = 0; sl < kHeadDim / kSlab; ++sl)
+                        tma_store_4d(&out_map, kSlab * sl, h, tok, b, img + sl * kSlabImg);
+                    bulk_commit();
+                }
+            } else if (ok) {
+                __nv_bfloat16* dst = p.out + b * p.os[0] + h * p.os[2] + v;
+#pragma unroll
+                for (int j = 0; j < kSlab; ++j)
+                    if (t0 + tq + j < seq_len) dst[((int64_t)tbase + t0 + tq + j) * p.os[1]] = __float2bfloat16_rn(x[j]);
+            }
+        };
+
         int issued = 0;  // records requested so far (storer thread)
         if (storer)
             for (; issued < kHStages && issued < count; ++issued) issue_load(issued);
-        store_quarter(sm + OH_S, row, cq, S);
-        fence_proxy_async_smem();
+        if (count > 0) store_state_operand();
         tc_fence_before();
         named_bar_or(kBarHChunk, 512, false);
+        if (issuer && count > 0) {
+            if (mbar_wait(&full[0], 0, abort, p.wait_ns)) issue_p1(0);
+            else fail();
+        }
         int done = 0;    // chunks finished
+        bool out_pending = false;
 
         for (int c = 0; c < count; ++c) {
             const int st = c % kHStages;
-            const uint8_t* sb = sm + st * kHStage;
+            uint8_t* sb = sm + st * kHStage;
             const uint32_t sb_addr = smem_u32(sb);
             bool ok = warp_wait_h(&full[st], (c / kHStages) & 1, abort, p.wait_ns);
             stall_point<kStall>(p.stall_seed, 1, c);
-            if (issuer && ok) {
-                tc_fence_after();
-                const uint64_t ad = sdesc_kmajor_sw128(sb_addr + SH_A1);
-                const uint64_t bd = sdesc_mnmajor_sw128(sS_addr, 1024u, kHSbo);
-#pragma unroll
-                for (uint32_t k = 0; k < 8; ++k)
-                    umma_bf16(tb + TMH_D1, ad + ((k >> 2) * (16384 >> 4) + (k & 3) * 2),
-                              bd + k * ((2 * kHSbo) >> 4), id, k > 0 ? 1u : 0u);
-                umma_commit(&p1_done);
-            }
-            __syncwarp();
-            // This thread's U (W rows) or O_loc (Q' rows) values, read while P1 runs.
-            uint4 sr[4];
-            {
-                const uint8_t* src = sb + (qd < 2 ? SH_U : SH_OL) + cq * kSlabImg;
-                const int r = qd < 2 ? row : row - 64;
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch) sr[ch] = *reinterpret_cast<const uint4*>(src + slab_chunk_off(r, ch));
-            }
-            ok = ok && warp_wait_h((p.timeout_probe && c == 0) ? &bar_never : &p1_done, c & 1, abort, p.wait_ns);
-            tc_fence_after();
-            float d[kSlab];
+            // The decay of the entry state by this chunk's e^gam, in TMEM, before
+            // P23 adds Kt V_new to it.
             if (ok) {
-                tmem_ld32(tb + lane_base + TMH_D1 + kSlab * cq, d);
+                const float4* egp = reinterpret_cast<const float4*>(sb + SH_EG) + k0 / 4;
+                uint32_t w[kSlab];
+#pragma unroll
+                for (int i = 0; i < kSlab / 4; ++i) {
+                    const float4 e = egp[i];
+                    w[4 * i] = __float_as_uint(e.x * S[4 * i]);
+                    w[4 * i + 1] = __float_as_uint(e.y * S[4 * i + 1]);
+                    w[4 * i + 2] = __float_as_uint(e.z * S[4 * i + 2]);
+                    w[4 * i + 3] = __float_as_uint(e.w * S[4 * i + 3]);
+                }
+                tmem_st32(tmem_addr(tb, 32 * qd, TMH_S + k0), w);
             }
-            if (qd < 2) {
-                // V_new = U - W S for token row `row`
+            tc_fence_before();
+            if (vwarp) {
+                // U of tokens tq .. tq + 31 of value column v, read while P1 runs
+#pragma unroll
+                for (int j = 0; j < kSlab; ++j)
+                    x[j] = zero_u ? 0.f
+                                  : bf16_bits_to_float(*reinterpret_cast<const uint16_t*>(sb + SH_U + slab_elem_off(tq + j, v)));
+                ok = ok && warp_wait_h((p.timeout_probe && c == 0) ? &bar_never : &p1_done, c & 1, abort, p.wait_ns);
+                tc_fence_after();
                 if (ok) {
-                    float vn[kSlab];
+                    // V_new = U - W S_in
+                    float d[kSlab];
+                    tmem_ld32(tb + lane_base + d1_col, d);
+                    uint32_t w[16];
 #pragma unroll
-                    for (int ch = 0; ch < 4; ++ch) {
-                        const uint32_t uw[4] = {sr[ch].x, sr[ch].y, sr[ch].z, sr[ch].w};
-#pragma unroll
-                        for (int x = 0; x < 4; ++x) {
-                            float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&uw[x]));
-                            if (zero_u) f = make_float2(0.f, 0.f);
-                            vn[8 * ch + 2 * x] = f.x - d[8 * ch + 2 * x];
-                            vn[8 * ch + 2 * x + 1] = f.y - d[8 * ch + 2 * x + 1];
-                        }
-                    }
+                    for (int i = 0; i < 16; ++i) w[i] = pack_f16x2(x[2 * i] - d[2 * i], x[2 * i + 1] - d[2 * i + 1]);
                     stall_point<kStall>(p.stall_seed, 2, c);
-                    store_quarter(sm + OH_VN, row, cq, vn);
-                    fence_proxy_async_smem();
+                    tmem_st16(tmem_addr(tb, 32 * qd, TMH_AV + 16 * (cq & 1)), w);
                 }
                 tc_fence_before();
-                named_bar_sync(kBarHVn, 256);  // the eight V_new warps
+                named_bar_sync(kBarHVn, 512);  // V_new and every thread's decayed state are in TMEM
                 if (issuer2 && ok && !*abort) {
                     tc_fence_after();
+                    // B = [Kt ; Aqk] (N = 192 rows, K = 64 tokens, K-major); A = V_new^T (all fp16)
                     const uint64_t kt = sdesc_kmajor_sw128(sb_addr + SH_KT);
-                    const uint64_t bv = sdesc_mnmajor_sw128(sVn_addr, 1024u, kHSbo);
 #pragma unroll
-                    for (uint32_t k = 0; k < 4; ++k)  // K = 64 tokens
-                        umma_bf16(tb + TMH_D2, kt + k * 2, bv + k * ((2 * kHSbo) >> 4), id, k > 0 ? 1u : 0u);
+                    for (uint32_t k = 0; k < 4; ++k)
+                        umma_bf16_ta(tb + TMH_S, tb + TMH_AV + 8 * k, kt + k * 2, id2, 1u);
                     umma_commit(&p2_done);
                 }
                 __syncwarp();
-            } else if (!no_out) {
-                // O = O_loc + Q' S for token row `row - 64`
-                const int i = row - 64, t0 = 64 * (cbase + c);
-                const bool valid_row = t0 + i < seq_len;
-                const int64_t t = (int64_t)tbase + t0 + i;
-                float o[kSlab];
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    const uint32_t ow[4] = {sr[ch].x, sr[ch].y, sr[ch].z, sr[ch].w};
-#pragma unroll
-                    for (int x = 0; x < 4; ++x) {
-                        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[x]));
-                        o[8 * ch + 2 * x] = f.x + d[8 * ch + 2 * x];
-                        o[8 * ch + 2 * x + 1] = f.y + d[8 * ch + 2 * x + 1];
-                    }
-                }
-                if (p.gate) {
-                    // gated RMSNorm over the 128 channels of the row: the four column
-                    // quarters' sums of squares meet in shared memory
-                    uint4 gw[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
-                                   make_uint4(0, 0, 0, 0)};
-                    if (ok && valid_row) {
-                        const uint4* gsrc = reinterpret_cast<const uint4*>(p.gate + b * p.gts[0] + t * p.gts[1] +
-                                                                           h * p.gts[2] + kSlab * cq);
-#pragma unroll
-                        for (int x = 0; x < 4; ++x) gw[x] = gsrc[x];
-                    }
-                    float ss = 0.f;
-#pragma unroll
-                    for (int j = 0; j < kSlab; ++j) ss = fmaf(o[j], o[j], ss);
-                    s_ss[cq][i] = ss;
-                    named_bar_sync(kBarHNorm, 256);  // the eight output warps
-                    const float ms = (s_ss[0][i] + s_ss[1][i] + s_ss[2][i] + s_ss[3][i]) * (1.0f / kHeadDim);
-                    const float rn = rsqrtf(ms + p.norm_eps);
-                    const float4* wq = reinterpret_cast<const float4*>(s_w + kSlab * cq);
-#pragma unroll
-                    for (int x = 0; x < 4; ++x) {
-                        const uint32_t gv[4] = {gw[x].x, gw[x].y, gw[x].z, gw[x].w};
-                        const float4 w0 = wq[2 * x], w1 = wq[2 * x + 1];
-                        const float ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gv[e]));
-                            o[8 * x + 2 * e] *= rn * ww[2 * e] * sigmoid_fast(gf.x);
-                            o[8 * x + 2 * e + 1] *= rn * ww[2 * e + 1] * sigmoid_fast(gf.y);
-                        }
-                    }
-                }
-                stall_point<kStall>(p.stall_seed, 3, c);
-                // Rows of a chunk that lies inside its sequence (padded calls: every
-                // chunk, the tensor store clips the rows past T) leave by tensor store:
-                // each thread writes its bf16 row piece over the O_loc bytes it read
-                // (the same 64-byte-swizzled slab layout as the store box), and one
-                // thread stores the four slabs.  Rows of a varlen tail chunk, which
-                // the next sequence's rows follow, are stored one by one.
-                const bool by_tma = p.out_tma && (p.cu == nullptr || t0 + kChunk <= seq_len);
-                if (by_tma) {
-                    uint8_t* img = sm + st * kHStage + SH_OL + cq * kSlabImg;
-#pragma unroll
-                    for (int x = 0; x < kSlab / 8; ++x)
-                        *reinterpret_cast<uint4*>(img + slab_chunk_off(i, x)) =
-                            make_uint4(pack_bf16x2(o[8 * x], o[8 * x + 1]), pack_bf16x2(o[8 * x + 2], o[8 * x + 3]),
-                                       pack_bf16x2(o[8 * x + 4], o[8 * x + 5]), pack_bf16x2(o[8 * x + 6], o[8 * x + 7]));
-                    fence_proxy_async_smem();
-                    named_bar_sync(kBarHOut, 256);  // the eight output warps
-                    if (storer && ok && !*abort) {
-                        const int tok = (int)(p.cu == nullptr ? t0 : (int64_t)tbase + t0);
-#pragma unroll
-                        for (int sl = 0; sl < kHeadDim / kSlab; ++sl)
-                            tma_store_4d(&out_map, kSlab * sl, h, tok, b, sb + SH_OL + sl * kSlabImg);
-                        bulk_commit();
-                    }
-                } else if (ok && valid_row) {
-                    uint4* dst = reinterpret_cast<uint4*>(p.out + b * p.os[0] + t * p.os[1] + h * p.os[2] + kSlab * cq);
-#pragma unroll
-                    for (int x = 0; x < kSlab / 8; ++x)
-                        dst[x] = make_uint4(pack_bf16x2(o[8 * x], o[8 * x + 1]), pack_bf16x2(o[8 * x + 2], o[8 * x + 3]),
-                                            pack_bf16x2(o[8 * x + 4], o[8 * x + 5]), pack_bf16x2(o[8 * x + 6], o[8 * x + 7]));
-                }
-                tc_fence_before();
+            } else {
+                named_bar_arrive(kBarHVn, 512);
+                // the previous chunk's output, while P1 of this one runs
+                if (out_pending) output(c - 1, ok);
+                out_pending = false;
             }
             ok = ok && warp_wait_h(&p2_done, c & 1, abort, p.wait_ns);
             tc_fence_after();
             if (ok) {
-                tmem_ld32(tb + lane_base + TMH_D2 + kSlab * cq, d);
-                const float eg = reinterpret_cast<const float*>(sb + SH_EG)[row];
+                // the next entry state, and (output warps) this chunk's output rows
+                float d[kSlab];
+                tmem_ld32(tb + lane_base + TMH_S + k0, d);
 #pragma unroll
-                for (int j = 0; j < kSlab; ++j) S[j] = fmaf(eg, S[j], d[j]);
-                stall_point<kStall>(p.stall_seed, 4, c);
-                if (c + 1 < count) {
-                    store_quarter(sm + OH_S, row, cq, S);
-                    fence_proxy_async_smem();
+                for (int j = 0; j < kSlab; ++j) S[j] = d[j];
+                if (!vwarp && !no_out) {
+                    tmem_ld32(tb + lane_base + d1_col, x);
+                    out_pending = true;
                 }
+                stall_point<kStall>(p.stall_seed, 4, c);
+                if (c + 1 < count) store_state_operand();
             } else {
                 fail();
             }
             tc_fence_before();
+            // (storer) the previous output's tensor stores have read the output rows
+            if (storer) bulk_wait_read();
             if (named_bar_or(kBarHChunk, 512, *abort != 0)) break;
             done = c + 1;
-            // stage st is free: P2 of chunk c completed, every read of it is done
-            // and (storer) the output tensor stores have read their slabs
-            stall_point<kStall>(p.stall_seed, 5, c);
-            if (storer && issued < count) {
-                bulk_wait_read();
-                issue_load(issued++);
+            if (issuer && c + 1 < count) {
+                const int sn = (c + 1) % kHStages;
+                if (mbar_wait(&full[sn], ((c + 1) / kHStages) & 1, abort, p.wait_ns)) issue_p1(c + 1);
+                else fail();
             }
+            // stage st is free: P1 and P23 of chunk c completed and every read of it is done
+            stall_point<kStall>(p.stall_seed, 5, c);
+            if (storer && issued < count) issue_load(issued++);
         }
+        // the last chunk's output
+        if (!vwarp && out_pending && done == count && !*abort) output(count - 1, true);
         if (storer) {
             bulk_wait_all();  // the output tensor stores are complete
             // Never leave with a copy in flight (bounded; normally complete).
@@ -401,10 +425,8 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
             fin = p.scan_ops + (((size_t)(2 * seg + which)) * p.N * p.H + chain) * kHeadDim * kHeadDim + blk_off;
         if (p.scan_mode == kScanOut && seg != p.scan_nseg - 1) fin = nullptr;
         if (!*abort && fin) {
-            float4* dst = reinterpret_cast<float4*>(fin);
 #pragma unroll
-            for (int x = 0; x < kSlab / 4; ++x)
-                dst[x] = make_float4(S[4 * x], S[4 * x + 1], S[4 * x + 2], S[4 * x + 3]);
+            for (int j = 0; j < kSlab; ++j) fin[(size_t)j * kHeadDim] = S[j];
         }
     }
     tc_fence_before();

@@ -83,8 +83,9 @@ __global__ void __launch_bounds__(128)
     if (warp == 0) tmem_dealloc(tmem_base, 256);
 }
 
-// D = A B^T with B stored MN-major (B^T as [K rows][N contiguous]); mode 0 uses
-// lbo = 1024 (atoms along N adjacent) and sbo = N/64 * 1024, mode 1 swaps them.
+// D = A B^T with B stored MN-major (B^T as [K rows][N contiguous]); mode bit 0
+// clear uses lbo = 1024 (atoms along N adjacent) and sbo = N/64 * 1024, set
+// swaps them; mode bit 1 takes A and B as fp16 (copied as 16-bit patterns).
 __global__ void __launch_bounds__(128)
     umma_mn_selftest_kernel(const __nv_bfloat16* __restrict__ A, const __nv_bfloat16* __restrict__ B,
                             float* __restrict__ D, int N, int mode, int* status) {
@@ -118,12 +119,14 @@ __global__ void __launch_bounds__(128)
     __syncthreads();
     tc_fence_after();
     if (tid == 0) {
-        const uint32_t lbo = mode == 0 ? 1024u : sbo, sb = mode == 0 ? sbo : 1024u;
+        // mode bit 0: atoms and 8-row groups swapped; bit 1: fp16 operands
+        const uint32_t lbo = (mode & 1) == 0 ? 1024u : sbo, sb = (mode & 1) == 0 ? sbo : 1024u;
+        const uint32_t id = (mode & 2) ? idesc_f16_f32_bmn(128, N) : idesc_bf16_f32_bmn(128, N);
         for (int k = 0; k < 8; ++k) {
             const uint32_t kb = k >> 2, kin = (k & 3u) * 32u;
             umma_bf16(tmem_base, sdesc_kmajor_sw128(smem_u32(sA) + kb * 16384 + kin),
-                      sdesc_mnmajor_sw128(smem_u32(sB) + (uint32_t)k * 2u * sbo, lbo, sb),
-                      idesc_bf16_f32_bmn(128, N), k > 0 ? 1u : 0u);
+                      sdesc_mnmajor_sw128(smem_u32(sB) + (uint32_t)k * 2u * sbo, lbo, sb), id,
+                      k > 0 ? 1u : 0u);
         }
         umma_commit(&bar_mma);
     }
@@ -206,10 +209,11 @@ __global__ void __launch_bounds__(128)
 }
 
 // D = A B^T with A (128 x 128) held in TMEM (written by the threads with
-// tcgen05.st, row m in lane m) and B (N x 128) K-major SW128 in shared memory.
+// tcgen05.st, row m in lane m) and B (N x 128) K-major SW128 in shared memory;
+// bf16 or (f16 != 0) fp16 operands, copied as 16-bit patterns.
 __global__ void __launch_bounds__(128)
     umma_tmem_a_selftest_kernel(const __nv_bfloat16* __restrict__ A, const __nv_bfloat16* __restrict__ B,
-                                float* __restrict__ D, int N, int* status) {
+                                float* __restrict__ D, int N, int f16, int* status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sB = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -250,7 +254,7 @@ __global__ void __launch_bounds__(128)
     tc_fence_after();
     if (tid == 0) {
         const uint64_t bd = sdesc_kmajor_sw128(smem_u32(sB));
-        const uint32_t id = idesc_bf16_f32(128, N);
+        const uint32_t id = f16 ? idesc_f16_f32(128, N) : idesc_bf16_f32(128, N);
         for (uint32_t k = 0; k < 8; ++k)
             umma_bf16_ta(tb, tb + kACol + 8 * k, bd + (k >> 2) * ((uint32_t)(N * 128) >> 4) + (k & 3) * 2, id,
                          k > 0 ? 1u : 0u);
@@ -437,16 +441,21 @@ extern "C" int kda_selftest_umma_tf32(const float* A, const float* B, float* D, 
     return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 
-extern "C" int kda_selftest_umma_tmem_a(const void* A, const void* B, float* D, int N, int* status,
-                                        void* stream) {
+extern "C" int kda_selftest_umma_tmem_a_typed(const void* A, const void* B, float* D, int N, int f16,
+                                              int* status, void* stream) {
     if (N < 16 || N > 256 || (N % 16) != 0) return 1;
     const size_t smem = 1024 + 2 * (size_t)N * 128;
     if (cudaFuncSetAttribute(umma_tmem_a_selftest_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
         return 3;
     umma_tmem_a_selftest_kernel<<<1, 128, smem, (cudaStream_t)stream>>>(
-        (const __nv_bfloat16*)A, (const __nv_bfloat16*)B, D, N, status);
+        (const __nv_bfloat16*)A, (const __nv_bfloat16*)B, D, N, f16 ? 1 : 0, status);
     return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
+
+extern "C" int kda_selftest_umma_tmem_a(const void* A, const void* B, float* D, int N, int* status,
+                                        void* stream) {
+    return kda_selftest_umma_tmem_a_typed(A, B, D, N, 0, status, stream);
 }
 
 extern "C" int kda_selftest_umma_mn64(const void* A, const void* B, float* D, int* status,

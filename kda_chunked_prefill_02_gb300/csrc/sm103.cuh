@@ -9,6 +9,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace kda {
@@ -79,6 +80,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
 // ---------------------------------------------------------------- barriers / fences
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// Arrives at a named barrier without waiting for it (the waiting threads use
+// named_bar_sync with the same count).
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // Named barrier over `nthreads` threads that also returns the OR of `pred`
@@ -251,8 +257,8 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     tmem_take16(b, &v[16]);
 }
 
-// Warp-collective store of 16 consecutive 32-bit columns, then the wait.
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+// Warp-collective store of 16 consecutive 32-bit columns (no wait).
+__device__ __forceinline__ void tmem_st16_issue(uint32_t taddr, const uint32_t* r) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
         "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
@@ -260,7 +266,20 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
         "r"(r[15])
         : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+// Store of 16 consecutive 32-bit columns, then the wait.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    tmem_st16_issue(taddr, r);
+    tmem_wait_st();
+}
+// 32 consecutive columns with one wait.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    tmem_st16_issue(taddr, r);
+    tmem_st16_issue(taddr + 16, r + 16);
+    tmem_wait_st();
 }
 
 // ---------------------------------------------------------------- UMMA
@@ -307,6 +326,17 @@ __device__ __forceinline__ uint64_t sdesc_mnmajor_sw64(uint32_t saddr, uint32_t 
 // Instruction descriptor as idesc_bf16_f32 but with B MN-major.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32_bmn(uint32_t M, uint32_t N) {
     return idesc_bf16_f32(M, N) | (1u << 16);
+}
+
+// Instruction descriptor for tcgen05.mma kind::f16 with fp16 A and B (format
+// 0; both operands of a product always share one type), fp32 accumulator,
+// both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N) {
+    return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+// The same with B MN-major.
+__host__ __device__ constexpr uint32_t idesc_f16_f32_bmn(uint32_t M, uint32_t N) {
+    return idesc_f16_f32(M, N) | (1u << 16);
 }
 
 // Byte offset of bf16 element (k, n) of an MN-major SW128 operand laid out as
@@ -430,6 +460,10 @@ __host__ __device__ __forceinline__ uint32_t sw128_off(uint32_t r, uint32_t c) {
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
 }
 

@@ -84,7 +84,7 @@ def test_workspace_plan(K):
     assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
     # padded: one fp32 128 x 128 state per chain (batch 1 x 2 heads) carried between segments
     assert L.total == L.state_carry + 2 * 128 * 128 * 4
-    assert L.record_bytes == 82432 and L.chunk_offset >= L.records + 8 * L.record_bytes
+    assert L.record_bytes == 74240 and L.chunk_offset >= L.records + 8 * L.record_bytes
     # varlen upper bound on chunks: floor(T / 64) + N
     a2 = _args(K, cu_seqlens=ctypes.c_void_p(1 << 12), num_seqs=3, seqlen=130)
     assert lib.kda_prefill_workspace_layout(ctypes.byref(a2), ctypes.byref(L)) == 0
@@ -325,13 +325,13 @@ def test_no_fallback_without_the_library_or_a_gpu(K, monkeypatch, tmp_path):
 
 
 def test_noalloc_capacity_as_documented(K):
-    """kda_prefill_noalloc's scratch holds the workspace of 2048 tokens x 12
-    heads (and 8192 x 3), but not 2048 x 13 (host-side sizes only)."""
+    """kda_prefill_noalloc's scratch holds the workspace of 2048 tokens x 13
+    heads (and 8192 x 3), but not 2048 x 14 (host-side sizes only)."""
     import torch
     lim = K.NOALLOC_MAX_WORKSPACE_BYTES
     size = lambda T, H: K.workspace_size(torch.empty(1, T, H, 128, dtype=torch.bfloat16),
                                          torch.empty(1, T, H, 128, dtype=torch.bfloat16))
-    assert size(2048, 12) <= lim < size(2048, 13)
+    assert size(2048, 13) <= lim < size(2048, 14)
     assert size(8192, 3) <= lim < size(8192, 4)
 
 
@@ -352,8 +352,8 @@ def test_noalloc_checks_arguments_before_the_size(K):
     assert run(_args(K, chunk=32)) == K.KDA_ERR_UNSUPPORTED
     assert run(_args(K, q=None)) == K.KDA_ERR_INVALID_ARG
     assert f(None, None) == K.KDA_ERR_INVALID_ARG
-    # well formed but larger than the scratch (2048 tokens x 13 heads)
-    assert run(_args(K, seqlen=2048, num_heads=13)) == K.KDA_ERR_UNSUPPORTED
+    # well formed but larger than the scratch (2048 tokens x 14 heads)
+    assert run(_args(K, seqlen=2048, num_heads=14)) == K.KDA_ERR_UNSUPPORTED
     # sizes that would overflow the workspace plan are refused, not wrapped
     huge = _args(K, cu_seqlens=ctypes.c_void_p(1 << 12), batch=1, num_seqs=60000,
                  seqlen=(1 << 31) - 1, num_heads=60000)

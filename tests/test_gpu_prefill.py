@@ -21,12 +21,14 @@ def _bf16(x):
     return torch.from_numpy(np.ascontiguousarray(x)).view(torch.bfloat16).float().numpy()
 
 
-def _unswizzle_bf16(img, rows):
-    """[rows x 64] bf16 block stored with the 128-byte swizzle -> float array."""
+def _unswizzle_bf16(img, rows, f16=False):
+    """[rows x 64] bf16 (or fp16) block stored with the 128-byte swizzle -> float array."""
     r = np.arange(rows)[:, None]
     c = np.arange(64)[None, :]
     off = r * 128 + (((c // 8) ^ (r % 8)) * 16) + (c % 8) * 2
     u16 = np.frombuffer(img.tobytes(), dtype=np.uint16)
+    if f16:
+        return u16[off // 2].view(np.float16).astype(np.float64)
     return _bf16(u16[off // 2])
 
 
@@ -41,13 +43,14 @@ def _unswizzle_slab(img):
 
 
 def decode_record(raw):
-    """Workspace record (include/kda.h layout) -> dict of W, Qp, Kt, U, Ol, eg."""
+    """Workspace record (include/kda.h layout) -> dict of Qt (scale Q e^Gam), W,
+    Kt (fp16), Aqk (fp16), U, eg."""
     a1 = np.concatenate([_unswizzle_bf16(raw[0:16384], 128), _unswizzle_bf16(raw[16384:32768], 128)], 1)
-    kt = _unswizzle_bf16(raw[32768:49152], 128)
-    u = np.concatenate([_unswizzle_slab(raw[49152 + 4096 * s:49152 + 4096 * (s + 1)]) for s in range(4)], 1)
-    ol = np.concatenate([_unswizzle_slab(raw[65536 + 4096 * s:65536 + 4096 * (s + 1)]) for s in range(4)], 1)
-    eg = np.frombuffer(raw[81920:82432].tobytes(), dtype=np.float32)
-    return dict(W=a1[:64], Qp=a1[64:], Kt=kt, U=u, Ol=ol, eg=eg)
+    kt = _unswizzle_bf16(raw[32768:49152], 128, f16=True)
+    aqk = _unswizzle_bf16(raw[49152:57344], 64, f16=True)
+    u = np.concatenate([_unswizzle_slab(raw[57344 + 4096 * s:57344 + 4096 * (s + 1)]) for s in range(4)], 1)
+    eg = np.frombuffer(raw[73728:74240].tobytes(), dtype=np.float32)
+    return dict(Qt=a1[:64], W=a1[64:], Kt=kt, Aqk=aqk, U=u, eg=eg)
 
 
 def test_prep_stage_intermediates():
@@ -71,12 +74,15 @@ def test_prep_stage_intermediates():
                 ref = chunked.chunk_step(np.zeros((128, 128)), 0.8 * q[bb, t0:t1, h], k[bb, t0:t1, h],
                                          v[bb, t0:t1, h], g[bb, t0:t1, h], beta[bb, t0:t1, h])
                 for name, got, want in (("W", rec["W"][:n], ref["W"]), ("U", rec["U"][:n], ref["U"]),
-                                        ("Qp", rec["Qp"][:n], ref["Qp"]), ("Ol", rec["Ol"][:n], ref["Oloc"]),
+                                        ("Qt", rec["Qt"][:n], ref["Qt"]), ("Aqk", rec["Aqk"][:n, :n], ref["Aqk"]),
                                         ("Kt", rec["Kt"][:, :n], ref["Kh"].T)):
                     assert rel_fro(got, want) < 1e-2, (name, bb, c, h, rel_fro(got, want))
                 np.testing.assert_allclose(rec["eg"], np.exp(ref["gam"]), rtol=1e-5, atol=1e-30)
-                for name, tail in (("W", rec["W"][n:]), ("U", rec["U"][n:]), ("Qp", rec["Qp"][n:]),
-                                   ("Ol", rec["Ol"][n:]), ("Kt", rec["Kt"][:, n:])):
+                # Aqk is masked to j <= i
+                assert not np.any(np.triu(rec["Aqk"], 1)), "Aqk above the diagonal"
+                for name, tail in (("W", rec["W"][n:]), ("U", rec["U"][n:]), ("Qt", rec["Qt"][n:]),
+                                   ("Aqk", rec["Aqk"][n:]), ("Aqk cols", rec["Aqk"][:, n:]),
+                                   ("Kt", rec["Kt"][:, n:])):
                     assert not np.any(tail), name
 
 

@@ -11,7 +11,7 @@ import pytest
 import torch
 
 from kda_chunked_prefill_02_gb300 import inputs
-from kda_test_util import assert_parity, gpu_prefill, oracle_prefill, rel_fro, to_np
+from kda_test_util import assert_norm_close, assert_parity, gpu_prefill, oracle_prefill, rel_fro, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -77,7 +77,7 @@ def test_scan_with_fused_norm():
                                  out_gate=gate.cuda(), norm_weight=w.cuda(), norm_eps=1e-6)
     torch.cuda.synchronize()
     same = gated_rmsnorm(to_np(plain_out), gate.float().numpy(), w.numpy(), 1e-6)
-    assert np.abs(to_np(out) - same).max() <= 2e-2
+    assert_norm_close(to_np(out), same)
     assert torch.equal(fin, plain_fin)
 
 

@@ -93,6 +93,43 @@ def test_umma_tile_a_from_tmem(selftest, N):
     torch.testing.assert_close(D, A.float() @ B.float().T, atol=2e-3, rtol=1e-4)
 
 
+@pytest.mark.parametrize("N", [128, 192])
+def test_umma_tile_a_from_tmem_fp16(selftest, N):
+    """The same with fp16 A and B (both operands of one product share the type):
+    the whole-chain state kernel's V_new^T [Kt ; Aqk]^T (N = 192)."""
+    f = selftest.kda_selftest_umma_tmem_a_typed
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 2 + [ctypes.c_void_p] * 2
+    g = torch.Generator(device="cpu").manual_seed(310 + N)
+    A = torch.randn(128, 128, generator=g).to(torch.float16).cuda()
+    B = torch.randn(N, 128, generator=g).to(torch.float16).cuda()
+    D = torch.full((128, N), float("nan"), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert f(A.data_ptr(), B.data_ptr(), D.data_ptr(), N, 1, status.data_ptr(),
+             torch.cuda.current_stream().cuda_stream) == 0
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    torch.testing.assert_close(D, A.float() @ B.float().T, atol=2e-3, rtol=1e-4)
+
+
+def test_umma_tile_b_mn_major_fp16(selftest):
+    """fp16 A (K-major) and B (MN-major, N = 32): the slab state kernel's
+    Kt V_new and Aqk V_new."""
+    f = selftest.kda_selftest_umma_mn
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 2 + [ctypes.c_void_p] * 2
+    g = torch.Generator(device="cpu").manual_seed(150)
+    A = torch.randn(128, 128, generator=g).to(torch.float16).cuda()
+    B = torch.randn(32, 128, generator=g).to(torch.float16).cuda()
+    D = torch.full((128, 32), float("nan"), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert f(A.data_ptr(), B.data_ptr(), D.data_ptr(), 32, 2, status.data_ptr(),
+             torch.cuda.current_stream().cuda_stream) == 0
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    torch.testing.assert_close(D, A.float() @ B.float().T, atol=2e-3, rtol=1e-4)
+
+
 def test_mma_rate_probe_runs(selftest):
     """The MMA throughput probe (back-to-back tcgen05.mma of one shape, timed
     with clock64 on the issuing thread) completes and reports a positive time."""
