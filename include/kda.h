@@ -286,9 +286,8 @@ kda_status kda_prefill_state(const kda_prefill_args* args, void* stream);
  *   [32768, 49152)    Kt fp16: 128 key rows x 64 tokens, (K e^{gam - Gam})^T
  *   [49152, 57344)    Aqk fp16: 64 token rows x 64 tokens, the masked
  *                     (j <= i) gate-decayed scale*Q K^T of the chunk
- *   [57344, 73728)    U = T Diag(beta) V bf16: value slabs 0-3 (32 columns
- *                     each, 4 KB), 64-byte rows, 16-byte chunk c of row x at
- *                     x*64 + ((c ^ ((x / 2) mod 4)) * 16)
+ *   [57344, 73728)    U^T bf16, U = T Diag(beta) V: 128 value rows x 64
+ *                     tokens (128 B, the swizzle above)
  *   [73728, 74240)    exp(gam) fp32 [128], gam = chunk total of g
  * Rows past a tail chunk's length are zero.  chunk_offset: int32 [N+1].
  * seq_order (varlen): the sequences by descending chunk count (ties by index;

@@ -42,16 +42,16 @@ constexpr float kGateFloor = -5.4f;   // per-token gate floor inside 16-token bl
 // Aqk follows Kt, so that [Kt ; Aqk] is one 192-row operand.  Kt and Aqk are
 // fp16 (the operands of the products with V_new, which the state pass forms
 // in fp16: 3 more mantissa bits than bf16 where the rounding of V_new reaches
-// the output through 64-term sums).  U is bf16 value slabs of 32 columns,
-// 64-byte rows, chunk c of row r at r*64 + ((c ^ ((r >> 1) & 3)) << 4)
-// (conflict-free row reads).
+// the output through 64-term sums).  U is stored transposed, U^T: 128 value
+// rows of 64 tokens (128 B, the same swizzle), so that a value column's tokens
+// are one row (and a 32-column slab's rows are 4 KB of the record).
 constexpr uint32_t kRecA1 = 0;          // [Q e^Gam ; W] bf16: 2 column blocks x 128 rows x 128 B
 constexpr uint32_t kRecKt = 32768;      // Kt fp16: 128 key rows x 64 tokens
 constexpr uint32_t kRecAqk = 49152;     // Aqk fp16: 64 token rows x 64 tokens
-constexpr uint32_t kRecU = 57344;       // U bf16: 4 value slabs x 64 rows x 32
+constexpr uint32_t kRecU = 57344;       // U^T bf16: 128 value rows x 64 tokens
 constexpr uint32_t kRecEg = 73728;      // e^gam fp32 [128]
 constexpr uint32_t kRecBytes = 74240;
-constexpr uint32_t kSlabImg = 4096;     // bytes of one U slab image
+constexpr uint32_t kSlabImg = 4096;     // bytes of one 32-column slab (U^T rows, or an output image)
 
 // Byte offset of 16-byte chunk c of row r in a U (or output) slab image.
 __host__ __device__ __forceinline__ uint32_t slab_chunk_off(uint32_t r, uint32_t c) {

@@ -9,7 +9,8 @@
 //   A[i,j]   = beta_i sum_c k_i k_j exp(Gam_i - Gam_j)     j <  i
 //   Aqk[i,j] =        sum_c q_i k_j exp(Gam_i - Gam_j)     j <= i
 //   T = (I + A)^-1,  T' = T Diag(beta)
-//   W  = T' (K e^Gam),  U = T' V,  Kt = (K e^{gam - Gam})^T,  eg = e^gam
+//   W  = T' (K e^Gam),  U = T' V (stored transposed),  Kt = (K e^{gam - Gam})^T,
+//   eg = e^gam
 // so that, for the chunk's entry state S, the serial pass only needs
 //   V_new = U - W S,  O = (Q e^Gam) S + Aqk V_new,  S <- Diag(eg) S + Kt V_new.
 //
@@ -75,7 +76,7 @@ constexpr uint32_t O_TT = 131072;     // A operand [T' ; T']: 128 rows x 128 B
 // Staging of the record images written by the last epilogue (over the solve's
 // scratch, which MMA C no longer needs).
 constexpr uint32_t O_SW = 81920;      // W image: 2 column blocks x 64 rows x 128 B (the record's rows 64-127)
-constexpr uint32_t O_SU = 98304;      // U image, 16 KB
+constexpr uint32_t O_SU = 98304;      // U^T image: 128 value rows x 128 B (64 tokens), 16 KB
 
 // TMEM columns.
 constexpr uint32_t TM_A = 0, TM_DIAG = 96, TM_C = 0, TM_COLS = 256;
@@ -531,14 +532,20 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         tc_fence_before();
         __syncthreads();
 
-        // ---- MMA C: [T' ; T'] [K e^Gam | V] = [W | U ; W | U]  (N = 256)
+        // ---- MMA C: W = [T' ; T'] (K e^Gam) (N = 128: W in both halves of the
+        // lanes) and U^T = V^T T'^T (M = 128 value columns, N = 64 tokens; A is
+        // the V half of the [K e^Gam | V] operand, read MN-major).
         if (tid == 0) {
             tc_fence_after();
             const uint32_t tt = smem_u32(sm + O_TT), kv = smem_u32(sm + O_KV);
             for (uint32_t k = 0; k < 4; ++k)
                 umma_bf16(tb + TM_C, sdesc_kmajor_sw128(tt + k * 32u),
                           sdesc_mnmajor_sw128(kv + k * 2u * kKvSbo, 1024u, kKvSbo),
-                          idesc_bf16_f32_bmn(128, 256), k > 0 ? 1u : 0u);
+                          idesc_bf16_f32_bmn(128, 128), k > 0 ? 1u : 0u);
+            for (uint32_t k = 0; k < 4; ++k)
+                umma_bf16(tb + TM_C + 128, sdesc_mnmajor_sw128(kv + 2048u + k * 2u * kKvSbo, 1024u, kKvSbo),
+                          sdesc_kmajor_sw128(tt + k * 32u), idesc_bf16_f32(128, 64) | (1u << 15),
+                          k > 0 ? 1u : 0u);
             umma_commit(&bar_mma[1]);
         }
         ok = __syncthreads_and(tid == 0 ? mbar_wait(&bar_mma[1], it & 1, nullptr, p.wait_ns) : true);
@@ -546,29 +553,28 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         if (!ok) break;
         stall_point<kStall>(p.stall_seed, 12, it);
         {
-            // ---- Epilogue C: W from the upper lanes' first 128 columns, U from the
-            // lower lanes' last 128 (the same rows twice), 32 columns per warp,
-            // written as the record's shared-memory images and stored with bulk
-            // copies.
-            const bool wpart = qd < 2;
-            const int i = 32 * (qd & 1) + lane;
+            // ---- Epilogue C, 32 columns per warp, written as the record's
+            // shared-memory images and stored with bulk copies: W (cq 0, 1) from
+            // the first 128 columns, keys 64 (qd / 2) + 32 cq .. of token row
+            // 32 (qd % 2) + lane; U^T (cq 2, 3) from the next 64, tokens
+            // 32 (cq - 2) .. of value row 32 qd + lane.
             float v[32];
-            tmem_ld32(tmem_addr(tb, 32 * qd, TM_C + (wpart ? 0 : 128) + 32 * cq), v);
+            tmem_ld32(tmem_addr(tb, 32 * qd, TM_C + (cq < 2 ? 64 * (qd >> 1) + 32 * cq : 128 + 32 * (cq - 2))), v);
             uint32_t w[16];
 #pragma unroll
             for (int x = 0; x < 16; ++x) w[x] = pack_bf16x2(v[2 * x], v[2 * x + 1]);
-            if (wpart) {
-                uint8_t* img = sm + O_SW + (cq >> 1) * 8192;
-                const int c0w = 32 * (cq & 1);
+            if (cq < 2) {
+                const int i = 32 * (qd & 1) + lane;
+                uint8_t* img = sm + O_SW + (qd >> 1) * 8192;
 #pragma unroll
                 for (int x = 0; x < 4; ++x)
-                    *reinterpret_cast<uint4*>(img + sw128_off(i, c0w + 8 * x)) =
+                    *reinterpret_cast<uint4*>(img + sw128_off(i, 32 * cq + 8 * x)) =
                         make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
             } else {
-                uint8_t* img = sm + O_SU + cq * kSlabImg;
+                const int vr = 32 * qd + lane;
 #pragma unroll
                 for (int x = 0; x < 4; ++x)
-                    *reinterpret_cast<uint4*>(img + slab_chunk_off(i, x)) =
+                    *reinterpret_cast<uint4*>(sm + O_SU + sw128_off(vr, 32 * (cq - 2) + 8 * x)) =
                         make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
             }
         }
@@ -580,7 +586,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             uint8_t* rp = p.ws_rec + (size_t)rec * kRecBytes;
             bulk_store(rp + kRecA1 + 8192, sm + O_SW, 8192);
             bulk_store(rp + kRecA1 + 16384 + 8192, sm + O_SW + 8192, 8192);
-            bulk_store(rp + kRecU, sm + O_SU, 4 * kSlabImg);
+            bulk_store(rp + kRecU, sm + O_SU, 16384);
             bulk_commit();
         }
         // Epilogue C's TMEM reads are ordered before the next record's MMA A by

@@ -43,7 +43,7 @@ constexpr int kStateThreads = 160;
 constexpr uint32_t ST_A1 = 0;          // [Q e^Gam ; W] 2 x (128 rows x 128 B)
 constexpr uint32_t ST_KT = 32768;      // [Kt ; Aqk] 192 rows x 128 B
 constexpr uint32_t ST_AQK = ST_KT + (kRecAqk - kRecKt);
-constexpr uint32_t ST_U = 57344;       // U slab: 64 rows x 32 bf16
+constexpr uint32_t ST_U = 57344;       // the slab's 32 rows of U^T (128 B: 64 tokens each)
 constexpr uint32_t ST_EG = 61440;      // e^gam [128] fp32
 constexpr uint32_t kStage = 62464;     // the record's parts, rounded up to 1 KB
 constexpr uint32_t kStageTx = 32768 + 24576 + kSlabImg + 512;
@@ -293,11 +293,15 @@ __global__ void __launch_bounds__(kStateThreads, 1)
             }
             __syncwarp();
             if (vwarp) {
-                // This thread's U row (token row - 64), read while P1 runs.
-                uint4 urow[4];
+                // U of this thread's token (row - 64) in the slab's 32 value
+                // columns: column row - 64 of the slab's U^T rows, read while P1 runs.
+                uint32_t uw[kSlab / 2];
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch)
-                    urow[ch] = *reinterpret_cast<const uint4*>(sb + ST_U + slab_chunk_off(row - 64, ch));
+                for (int x = 0; x < kSlab / 2; ++x) {
+                    const uint32_t lo = *reinterpret_cast<const uint16_t*>(sb + ST_U + sw128_off(2 * x, row - 64));
+                    const uint32_t hi = *reinterpret_cast<const uint16_t*>(sb + ST_U + sw128_off(2 * x + 1, row - 64));
+                    uw[x] = lo | (hi << 16);
+                }
                 ok = ok && warp_wait((p.timeout_probe && c == 0) ? &bar_never : &p1_done, c & 1, abort, p.wait_ns);
                 tc_fence_after();
                 // V_new = U - W S for token row `row - 64`; stored transposed (K-major over tokens)
@@ -306,15 +310,10 @@ __global__ void __launch_bounds__(kStateThreads, 1)
                     tmem_ld32(tb + lane_base + d1, d);
                     float vn[kSlab];
 #pragma unroll
-                    for (int ch = 0; ch < 4; ++ch) {
-                        const uint4 u = urow[ch];
-                        const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                        for (int x = 0; x < 4; ++x) {
-                            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&uw[x]));
-                            vn[8 * ch + 2 * x] = f.x - d[8 * ch + 2 * x];
-                            vn[8 * ch + 2 * x + 1] = f.y - d[8 * ch + 2 * x + 1];
-                        }
+                    for (int x = 0; x < kSlab / 2; ++x) {
+                        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&uw[x]));
+                        vn[2 * x] = f.x - d[2 * x];
+                        vn[2 * x + 1] = f.y - d[2 * x + 1];
                     }
                     stall_point<kStall>(p.stall_seed, 3, c);
                     store_row(sm + O_VN + 8192 * (c & 1), row - 64, vn, true);

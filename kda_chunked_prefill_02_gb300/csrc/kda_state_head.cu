@@ -48,14 +48,14 @@ constexpr int kHeadThreads = 16 * 32;
 // A stage holds one record as the prep kernel wrote it (one bulk copy).
 constexpr uint32_t SH_A1 = kRecA1;     // [Q e^Gam ; W] 2 x (128 rows x 128 B), K-major: P1's B operand
 constexpr uint32_t SH_KT = kRecKt;     // [Kt ; Aqk] 192 rows x 128 B, K-major: P23's B operand
-constexpr uint32_t SH_U = kRecU;       // U: 4 value slabs (64-byte swizzle), 16 KB
+constexpr uint32_t SH_U = kRecU;       // U^T: 128 value rows x 64 tokens (128-byte swizzle), 16 KB
 constexpr uint32_t SH_EG = kRecEg;     // e^gam [128] fp32
 constexpr uint32_t kHStageTx = kRecBytes;  // the whole record, one bulk copy
 constexpr uint32_t kHStage = 74752;     // kRecBytes rounded up to 1 KB (swizzle atoms)
 constexpr int kHStages = 2;
 constexpr int kHPrefetchAhead = 4;
-constexpr uint32_t OH_OUT = kHStages * kHStage;   // output rows: 4 slabs [64 tokens x 32 values] bf16
-constexpr uint32_t kHeadSmem = OH_OUT + 4 * kSlabImg + 1024;
+constexpr uint32_t OH_OUT = kHStages * kHStage;   // output rows: 2 images of 4 slabs [64 tokens x 32 values] bf16
+constexpr uint32_t kHeadSmem = OH_OUT + 2 * 4 * kSlabImg + 1024;
 // TMEM columns (lane = value column v).
 constexpr uint32_t TMH_S = 0;      // S^T fp32: keys 0..127 (P23 accumulates onto it)
 constexpr uint32_t TMH_D1 = 128;   // D1^T fp32: Q part (tokens 0..63, P23 adds Aqk V_new), then W part
@@ -84,7 +84,7 @@ __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) {
     return __uint_as_float(b << 16);
 }
 
-// Byte offset of element (token t, value column v) in a 4-slab U / output image
+// Byte offset of element (token t, value column v) in a 4-slab output image
 // (slab v / 32, 64-byte rows of 32 values, 16-byte chunks swizzled).
 __device__ __forceinline__ uint32_t slab_elem_off(int t, int v) {
     return (uint32_t)(v >> 5) * kSlabImg + slab_chunk_off((uint32_t)t, (uint32_t)((v & 31) >> 3)) +
@@ -279,24 +279,34 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
             stall_point<kStall>(p.stall_seed, 3, co);
             const bool by_tma = p.out_tma && (p.cu == nullptr || t0 + kChunk <= seq_len);
             if (by_tma) {
-                uint8_t* img = sm + OH_OUT;
+                // one of two images: the stores that read it two outputs ago are
+                // done reading (each output commits one bulk group)
+                uint8_t* img = sm + OH_OUT + (co & 1) * (4 * kSlabImg);
+                if (storer) bulk_wait_read_but_last();
+                named_bar_sync(kBarHOut, 256);  // the eight output warps: the image is free
 #pragma unroll
                 for (int j = 0; j < kSlab; ++j)
                     *reinterpret_cast<__nv_bfloat16*>(img + slab_elem_off(tq + j, v)) = __float2bfloat16_rn(x[j]);
                 fence_proxy_async_smem();
-                named_bar_sync(kBarHOut, 256);  // the eight output warps
-                if (storer && ok && !*abort) {
-                    const int tok = (int)(p.cu == nullptr ? t0 : (int64_t)tbase + t0);
+                named_bar_sync(kBarHOut, 256);  // the image is written
+                if (storer) {
+                    if (ok && !*abort) {
+                        const int tok = (int)(p.cu == nullptr ? t0 : (int64_t)tbase + t0);
 #pragma unroll
-                    for (int sl = 0; sl < kHeadDim / kSlab; ++sl)
-                        tma_store_4d(&out_map, kSlab * sl, h, tok, b, img + sl * kSlabImg);
+                        for (int sl = 0; sl < kHeadDim / kSlab; ++sl)
+                            tma_store_4d(&out_map, kSlab * sl, h, tok, b, img + sl * kSlabImg);
+                    }
                     bulk_commit();
                 }
-            } else if (ok) {
-                __nv_bfloat16* dst = p.out + b * p.os[0] + h * p.os[2] + v;
+            } else {
+                if (ok) {
+                    __nv_bfloat16* dst = p.out + b * p.os[0] + h * p.os[2] + v;
 #pragma unroll
-                for (int j = 0; j < kSlab; ++j)
-                    if (t0 + tq + j < seq_len) dst[((int64_t)tbase + t0 + tq + j) * p.os[1]] = __float2bfloat16_rn(x[j]);
+                    for (int j = 0; j < kSlab; ++j)
+                        if (t0 + tq + j < seq_len)
+                            dst[((int64_t)tbase + t0 + tq + j) * p.os[1]] = __float2bfloat16_rn(x[j]);
+                }
+                if (storer) bulk_commit();   // an empty group: one group per output
             }
         };
 
@@ -305,11 +315,9 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
             for (; issued < kHStages && issued < count; ++issued) issue_load(issued);
         if (count > 0) store_state_operand();
         tc_fence_before();
-        named_bar_or(kBarHChunk, 512, false);
-        if (issuer && count > 0) {
-            if (mbar_wait(&full[0], 0, abort, p.wait_ns)) issue_p1(0);
-            else fail();
-        }
+        if (issuer && count > 0 && !mbar_wait(&full[0], 0, abort, p.wait_ns)) fail();
+        if (named_bar_or(kBarHChunk, 512, *abort != 0)) count = 0;
+        if (issuer && count > 0) issue_p1(0);
         int done = 0;    // chunks finished
         bool out_pending = false;
 
@@ -317,11 +325,14 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
             const int st = c % kHStages;
             uint8_t* sb = sm + st * kHStage;
             const uint32_t sb_addr = smem_u32(sb);
-            bool ok = warp_wait_h(&full[st], (c / kHStages) & 1, abort, p.wait_ns);
+            // The record has arrived: the P1 thread waited for it before the chunk
+            // barrier that ended the previous chunk (or the one before the loop).
+            bool ok = true;
             stall_point<kStall>(p.stall_seed, 1, c);
             // The decay of the entry state by this chunk's e^gam, in TMEM, before
-            // P23 adds Kt V_new to it.
-            if (ok) {
+            // P23 adds Kt V_new to it (the stores complete before the V_new
+            // barrier: each warp waits for its TMEM stores before it).
+            {
                 const float4* egp = reinterpret_cast<const float4*>(sb + SH_EG) + k0 / 4;
                 uint32_t w[kSlab];
 #pragma unroll
@@ -332,15 +343,22 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
                     w[4 * i + 2] = __float_as_uint(e.z * S[4 * i + 2]);
                     w[4 * i + 3] = __float_as_uint(e.w * S[4 * i + 3]);
                 }
-                tmem_st32(tmem_addr(tb, 32 * qd, TMH_S + k0), w);
+                tmem_st16_issue(tmem_addr(tb, 32 * qd, TMH_S + k0), w);
+                tmem_st16_issue(tmem_addr(tb, 32 * qd, TMH_S + k0 + 16), w + 16);
             }
-            tc_fence_before();
             if (vwarp) {
-                // U of tokens tq .. tq + 31 of value column v, read while P1 runs
+                // U^T row v, tokens tq .. tq + 31 (four 16-byte chunks), read while
+                // P1 runs
 #pragma unroll
-                for (int j = 0; j < kSlab; ++j)
-                    x[j] = zero_u ? 0.f
-                                  : bf16_bits_to_float(*reinterpret_cast<const uint16_t*>(sb + SH_U + slab_elem_off(tq + j, v)));
+                for (int ch = 0; ch < 4; ++ch) {
+                    const uint4 u = *reinterpret_cast<const uint4*>(sb + SH_U + sw128_off(v, tq + 8 * ch));
+                    const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        x[8 * ch + 2 * e] = zero_u ? 0.f : bf16_bits_to_float(uw[e] & 0xffffu);
+                        x[8 * ch + 2 * e + 1] = zero_u ? 0.f : bf16_bits_to_float(uw[e] >> 16);
+                    }
+                }
                 ok = ok && warp_wait_h((p.timeout_probe && c == 0) ? &bar_never : &p1_done, c & 1, abort, p.wait_ns);
                 tc_fence_after();
                 if (ok) {
@@ -351,8 +369,9 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 16; ++i) w[i] = pack_f16x2(x[2 * i] - d[2 * i], x[2 * i + 1] - d[2 * i + 1]);
                     stall_point<kStall>(p.stall_seed, 2, c);
-                    tmem_st16(tmem_addr(tb, 32 * qd, TMH_AV + 16 * (cq & 1)), w);
+                    tmem_st16_issue(tmem_addr(tb, 32 * qd, TMH_AV + 16 * (cq & 1)), w);
                 }
+                tmem_wait_st();   // V_new and this thread's decayed state
                 tc_fence_before();
                 named_bar_sync(kBarHVn, 512);  // V_new and every thread's decayed state are in TMEM
                 if (issuer2 && ok && !*abort) {
@@ -366,6 +385,8 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
                 }
                 __syncwarp();
             } else {
+                tmem_wait_st();   // this thread's decayed state
+                tc_fence_before();
                 named_bar_arrive(kBarHVn, 512);
                 // the previous chunk's output, while P1 of this one runs
                 if (out_pending) output(c - 1, ok);
@@ -389,15 +410,14 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
                 fail();
             }
             tc_fence_before();
-            // (storer) the previous output's tensor stores have read the output rows
-            if (storer) bulk_wait_read();
+            // (P1 thread) the next record has arrived before the barrier, so that
+            // every thread may read its stage after it
+            if (issuer && c + 1 < count &&
+                !mbar_wait(&full[(c + 1) % kHStages], ((c + 1) / kHStages) & 1, abort, p.wait_ns))
+                fail();
             if (named_bar_or(kBarHChunk, 512, *abort != 0)) break;
             done = c + 1;
-            if (issuer && c + 1 < count) {
-                const int sn = (c + 1) % kHStages;
-                if (mbar_wait(&full[sn], ((c + 1) / kHStages) & 1, abort, p.wait_ns)) issue_p1(c + 1);
-                else fail();
-            }
+            if (issuer && c + 1 < count) issue_p1(c + 1);
             // stage st is free: P1 and P23 of chunk c completed and every read of it is done
             stall_point<kStall>(p.stall_seed, 5, c);
             if (storer && issued < count) issue_load(issued++);

@@ -85,7 +85,9 @@ __global__ void __launch_bounds__(128)
 
 // D = A B^T with B stored MN-major (B^T as [K rows][N contiguous]); mode bit 0
 // clear uses lbo = 1024 (atoms along N adjacent) and sbo = N/64 * 1024, set
-// swaps them; mode bit 1 takes A and B as fp16 (copied as 16-bit patterns).
+// swaps them; mode bit 1 takes A and B as fp16 (copied as 16-bit patterns);
+// mode bit 2 stores A MN-major as well (A^T as [K rows][M contiguous]: two
+// 64-row atoms 1024 B apart, 8-row K groups 2048 B apart).
 __global__ void __launch_bounds__(128)
     umma_mn_selftest_kernel(const __nv_bfloat16* __restrict__ A, const __nv_bfloat16* __restrict__ B,
                             float* __restrict__ D, int N, int mode, int* status) {
@@ -106,9 +108,13 @@ __global__ void __launch_bounds__(128)
         tmem_alloc(&tmem_base, 256);
         tmem_relinquish();
     }
+    const bool a_mn = (mode & 4) != 0;
     for (int i = tid; i < 128 * 128; i += 128) {
         const int r = i >> 7, c = i & 127;
-        *reinterpret_cast<__nv_bfloat16*>(sA + (c >> 6) * 16384 + sw128_off(r, c & 63)) = A[i];
+        if (a_mn)
+            *reinterpret_cast<__nv_bfloat16*>(sA + mn_sw128_off(c, r, 2048u)) = A[i];
+        else
+            *reinterpret_cast<__nv_bfloat16*>(sA + (c >> 6) * 16384 + sw128_off(r, c & 63)) = A[i];
     }
     for (int i = tid; i < N * 128; i += 128) {  // B[n][k] -> MN-major (k, n)
         const int n = i >> 7, k = i & 127;
@@ -121,11 +127,13 @@ __global__ void __launch_bounds__(128)
     if (tid == 0) {
         // mode bit 0: atoms and 8-row groups swapped; bit 1: fp16 operands
         const uint32_t lbo = (mode & 1) == 0 ? 1024u : sbo, sb = (mode & 1) == 0 ? sbo : 1024u;
-        const uint32_t id = (mode & 2) ? idesc_f16_f32_bmn(128, N) : idesc_bf16_f32_bmn(128, N);
+        const uint32_t id = ((mode & 2) ? idesc_f16_f32_bmn(128, N) : idesc_bf16_f32_bmn(128, N)) |
+                            (a_mn ? (1u << 15) : 0u);
         for (int k = 0; k < 8; ++k) {
             const uint32_t kb = k >> 2, kin = (k & 3u) * 32u;
-            umma_bf16(tmem_base, sdesc_kmajor_sw128(smem_u32(sA) + kb * 16384 + kin),
-                      sdesc_mnmajor_sw128(smem_u32(sB) + (uint32_t)k * 2u * sbo, lbo, sb), id,
+            const uint64_t ad = a_mn ? sdesc_mnmajor_sw128(smem_u32(sA) + (uint32_t)k * 2u * 2048u, 1024u, 2048u)
+                                     : sdesc_kmajor_sw128(smem_u32(sA) + kb * 16384 + kin);
+            umma_bf16(tmem_base, ad, sdesc_mnmajor_sw128(smem_u32(sB) + (uint32_t)k * 2u * sbo, lbo, sb), id,
                       k > 0 ? 1u : 0u);
         }
         umma_commit(&bar_mma);

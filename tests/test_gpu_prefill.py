@@ -32,23 +32,13 @@ def _unswizzle_bf16(img, rows, f16=False):
     return _bf16(u16[off // 2])
 
 
-def _unswizzle_slab(img):
-    """bf16 value slab: 64 rows x 32, 64-byte rows, chunk c of row r at
-    r*64 + ((c ^ ((r // 2) % 4)) * 16)."""
-    r = np.arange(64)[:, None]
-    c = np.arange(32)[None, :]
-    off = r * 64 + (((c // 8) ^ ((r // 2) % 4)) * 16) + (c % 8) * 2
-    u16 = np.frombuffer(img.tobytes(), dtype=np.uint16)
-    return _bf16(u16[off // 2])
-
-
 def decode_record(raw):
     """Workspace record (include/kda.h layout) -> dict of Qt (scale Q e^Gam), W,
     Kt (fp16), Aqk (fp16), U, eg."""
     a1 = np.concatenate([_unswizzle_bf16(raw[0:16384], 128), _unswizzle_bf16(raw[16384:32768], 128)], 1)
     kt = _unswizzle_bf16(raw[32768:49152], 128, f16=True)
     aqk = _unswizzle_bf16(raw[49152:57344], 64, f16=True)
-    u = np.concatenate([_unswizzle_slab(raw[57344 + 4096 * s:57344 + 4096 * (s + 1)]) for s in range(4)], 1)
+    u = _unswizzle_bf16(raw[57344:73728], 128).T     # stored as U^T: 128 value rows x 64 tokens
     eg = np.frombuffer(raw[73728:74240].tobytes(), dtype=np.float32)
     return dict(Qt=a1[:64], W=a1[64:], Kt=kt, Aqk=aqk, U=u, eg=eg)
 

@@ -130,6 +130,26 @@ def test_umma_tile_b_mn_major_fp16(selftest):
     torch.testing.assert_close(D, A.float() @ B.float().T, atol=2e-3, rtol=1e-4)
 
 
+@pytest.mark.parametrize("N", [32, 64])
+def test_umma_tile_a_and_b_mn_major(selftest, N):
+    """A stored MN-major too (A^T as [K rows][M contiguous], two 64-row atoms
+    1 KB apart): the form of prep's U^T = V^T T'^T, whose A operand is the V
+    half of the [K e^Gam | V] operand."""
+    f = selftest.kda_selftest_umma_mn
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 2 + [ctypes.c_void_p] * 2
+    g = torch.Generator(device="cpu").manual_seed(170 + N)
+    A = torch.randn(128, 128, generator=g).to(torch.bfloat16).cuda()
+    B = torch.randn(N, 128, generator=g).to(torch.bfloat16).cuda()
+    D = torch.full((128, N), float("nan"), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert f(A.data_ptr(), B.data_ptr(), D.data_ptr(), N, 4, status.data_ptr(),
+             torch.cuda.current_stream().cuda_stream) == 0
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    torch.testing.assert_close(D, A.float() @ B.float().T, atol=2e-3, rtol=1e-4)
+
+
 def test_mma_rate_probe_runs(selftest):
     """The MMA throughput probe (back-to-back tcgen05.mma of one shape, timed
     with clock64 on the issuing thread) completes and reports a positive time."""
