@@ -62,7 +62,8 @@ constexpr uint32_t TMH_D1 = 128;   // D1^T fp32: Q part (tokens 0..63, P23 adds 
 constexpr uint32_t TMH_AS = 256;   // S^T bf16 pairs: keys 0..127 in 64 columns (P1's A operand)
 constexpr uint32_t TMH_AV = 320;   // V_new^T fp16 pairs: tokens 0..63 in 32 columns (P23's A operand)
 constexpr uint32_t TMH_COLS = 512;
-constexpr uint32_t kBarHVn = 1, kBarHChunk = 2, kBarHNorm = 3, kBarHOut = 4;  // named barriers (0 is __syncthreads)
+// named barriers (0 is __syncthreads); kBarHOut + q for the output warps of lane quarter q
+constexpr uint32_t kBarHVn = 1, kBarHChunk = 2, kBarHNorm = 3, kBarHOut = 4;
 static_assert(kRecAqk == kRecKt + 16384, "P23's B operand is Kt followed by Aqk");
 static_assert(kRecBytes <= kHStage, "a record fits a stage");
 
@@ -82,13 +83,6 @@ __device__ __forceinline__ bool warp_wait_h(uint64_t* bar, uint32_t parity, vola
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) {
     return __uint_as_float(b << 16);
-}
-
-// Byte offset of element (token t, value column v) in a 4-slab output image
-// (slab v / 32, 64-byte rows of 32 values, 16-byte chunks swizzled).
-__device__ __forceinline__ uint32_t slab_elem_off(int t, int v) {
-    return (uint32_t)(v >> 5) * kSlabImg + slab_chunk_off((uint32_t)t, (uint32_t)((v & 31) >> 3)) +
-           (uint32_t)(v & 7) * 2u;
 }
 
 // The 32 values x[0..31] of each lane summed over the warp's 32 lanes: after the
@@ -193,39 +187,45 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
         const int k0 = 32 * cq;             // this thread's first key in the state
         const uint32_t lane_base = (uint32_t)(32 * qd) << 16;
         const uint32_t d1_col = TMH_D1 + 32 * cq;   // Q part (cq 0, 1) or W part (cq 2, 3)
-        // P1: a thread of an output warp; P23: a thread of a V_new warp; the output
-        // tensor stores and the record copies: a thread of another output warp.
+        // P1: a thread of an output warp; P23: a thread of a V_new warp (those wait
+        // for P23 anyway); the record copies: a thread of another V_new warp, once
+        // P23 has finished with the stage; the output tensor store of lane
+        // quarter qd's slab: a thread of the quarter's second output warp.
         const bool issuer = (warp == 0 && lane == 0);
         const bool issuer2 = (warp == 8 && lane == 0);
-        const bool storer = (warp == 1 && lane == 0);
+        const bool loader = (warp == 9 && lane == 0);
+        const bool storer = (cq == 1 && lane == 0);
         // P1 in bf16 (S and the record's rows), P23 in fp16 (V_new, Kt and Aqk)
         const uint32_t id1 = idesc_bf16_f32(128, 128), id2 = idesc_f16_f32(128, 192);
-        float S[kSlab];                     // S[k0 + j][v]
         const size_t blk_off = (size_t)k0 * kHeadDim + v;   // element (k0, v) of a 128 x 128 block
         const size_t st_off = chain * kHeadDim * kHeadDim + blk_off;
-        // Entry state: the call's initial state, or in the scan the identity
-        // (transition), zero (offset) or the combine's entry state E_seg.
-        const float* h0 = p.h0 ? p.h0 + st_off : nullptr;
-        if (p.scan_mode == kScanOps) h0 = nullptr;
-        if (p.scan_mode == kScanOut && seg > 0)
-            h0 = p.scan_entry + ((size_t)seg * p.N * p.H + chain) * kHeadDim * kHeadDim + blk_off;
-        if (zero_u) {
-#pragma unroll
-            for (int j = 0; j < kSlab; ++j) S[j] = (k0 + j == v) ? 1.f : 0.f;
-        } else if (h0) {
-#pragma unroll
-            for (int j = 0; j < kSlab; ++j) S[j] = h0[(size_t)j * kHeadDim];
-        } else {
-#pragma unroll
-            for (int j = 0; j < kSlab; ++j) S[j] = 0.f;
-        }
         // S^T in bf16 into P1's A operand: keys k0 .. k0 + 31 of lane v.
-        auto store_state_operand = [&]() {
+        auto store_state_operand = [&](const float (&s32)[kSlab]) {
             uint32_t w[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(S[2 * i], S[2 * i + 1]);
+            for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(s32[2 * i], s32[2 * i + 1]);
             tmem_st16(tmem_addr(tb, 32 * qd, TMH_AS + 16 * cq), w);
         };
+        // Entry state: the call's initial state, or in the scan the identity
+        // (transition), zero (offset) or the combine's entry state E_seg, into
+        // TMEM (fp32, keys k0 .. k0 + 31 of lane v; the state lives there) and
+        // P1's A operand.
+        if (count > 0) {
+            const float* h0 = p.h0 ? p.h0 + st_off : nullptr;
+            if (p.scan_mode == kScanOps) h0 = nullptr;
+            if (p.scan_mode == kScanOut && seg > 0)
+                h0 = p.scan_entry + ((size_t)seg * p.N * p.H + chain) * kHeadDim * kHeadDim + blk_off;
+            float s0[kSlab];
+#pragma unroll
+            for (int j = 0; j < kSlab; ++j)
+                s0[j] = zero_u ? ((k0 + j == v) ? 1.f : 0.f) : (h0 ? h0[(size_t)j * kHeadDim] : 0.f);
+            uint32_t w[kSlab];
+#pragma unroll
+            for (int j = 0; j < kSlab; ++j) w[j] = __float_as_uint(s0[j]);
+            tmem_st16_issue(tmem_addr(tb, 32 * qd, TMH_S + k0), w);
+            tmem_st16_issue(tmem_addr(tb, 32 * qd, TMH_S + k0 + 16), w + 16);
+            store_state_operand(s0);
+        }
         auto issue_load = [&](int c) {
             const int st = c % kHStages;
             mbar_arrive_expect_tx(&full[st], kHStageTx);
@@ -279,22 +279,29 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
             stall_point<kStall>(p.stall_seed, 3, co);
             const bool by_tma = p.out_tma && (p.cu == nullptr || t0 + kChunk <= seq_len);
             if (by_tma) {
-                // one of two images: the stores that read it two outputs ago are
-                // done reading (each output commits one bulk group)
-                uint8_t* img = sm + OH_OUT + (co & 1) * (4 * kSlabImg);
-                if (storer) bulk_wait_read_but_last();
-                named_bar_sync(kBarHOut, 256);  // the eight output warps: the image is free
+                // One of two images; the stores that read it two outputs ago were
+                // done reading before the last chunk barrier (each output commits
+                // one bulk group).  An image is 4 slabs (value v / 32) of 64-byte
+                // token rows, 16-byte chunk c of row t at t*64 + ((c ^ ((t/2) & 3))
+                // << 4); for token tq + j the swizzle depends on (j / 2) % 4 only
+                // (tq is a multiple of 32), so four offsets serve all 32 rows.
+                uint8_t* const img0 = sm + OH_OUT + (co & 1) * (4 * kSlabImg);
+                uint8_t* img = img0 + (uint32_t)tq * 64u;
+                uint32_t off[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    off[k] = (uint32_t)(v >> 5) * kSlabImg + ((((uint32_t)(v & 31) >> 3) ^ (uint32_t)k) << 4) +
+                             (uint32_t)(v & 7) * 2u;
 #pragma unroll
                 for (int j = 0; j < kSlab; ++j)
-                    *reinterpret_cast<__nv_bfloat16*>(img + slab_elem_off(tq + j, v)) = __float2bfloat16_rn(x[j]);
+                    *reinterpret_cast<__nv_bfloat16*>(img + (uint32_t)j * 64u + off[(j >> 1) & 3]) =
+                        __float2bfloat16_rn(x[j]);
                 fence_proxy_async_smem();
-                named_bar_sync(kBarHOut, 256);  // the image is written
+                named_bar_sync(kBarHOut + qd, 64);  // the quarter's two output warps: its slab is written
                 if (storer) {
                     if (ok && !*abort) {
                         const int tok = (int)(p.cu == nullptr ? t0 : (int64_t)tbase + t0);
-#pragma unroll
-                        for (int sl = 0; sl < kHeadDim / kSlab; ++sl)
-                            tma_store_4d(&out_map, kSlab * sl, h, tok, b, img + sl * kSlabImg);
+                        tma_store_4d(&out_map, kSlab * qd, h, tok, b, img0 + qd * kSlabImg);
                     }
                     bulk_commit();
                 }
@@ -310,10 +317,9 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
             }
         };
 
-        int issued = 0;  // records requested so far (storer thread)
-        if (storer)
+        int issued = 0;  // records requested so far (loader thread)
+        if (loader)
             for (; issued < kHStages && issued < count; ++issued) issue_load(issued);
-        if (count > 0) store_state_operand();
         tc_fence_before();
         if (issuer && count > 0 && !mbar_wait(&full[0], 0, abort, p.wait_ns)) fail();
         if (named_bar_or(kBarHChunk, 512, *abort != 0)) count = 0;
@@ -330,21 +336,30 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
             bool ok = true;
             stall_point<kStall>(p.stall_seed, 1, c);
             // The decay of the entry state by this chunk's e^gam, in TMEM, before
-            // P23 adds Kt V_new to it (the stores complete before the V_new
-            // barrier: each warp waits for its TMEM stores before it).
-            {
-                const float4* egp = reinterpret_cast<const float4*>(sb + SH_EG) + k0 / 4;
-                uint32_t w[kSlab];
+            // P23 adds Kt V_new to it, by the output warps: their own 32 keys
+            // (from registers) and those of the V_new warp of the same lane
+            // quarter (from TMEM), so that the V_new warps go straight to V_new.
+            // The stores complete before the V_new barrier.
+            if (!vwarp) {
+                const float4* egp = reinterpret_cast<const float4*>(sb + SH_EG);
 #pragma unroll
-                for (int i = 0; i < kSlab / 4; ++i) {
-                    const float4 e = egp[i];
-                    w[4 * i] = __float_as_uint(e.x * S[4 * i]);
-                    w[4 * i + 1] = __float_as_uint(e.y * S[4 * i + 1]);
-                    w[4 * i + 2] = __float_as_uint(e.z * S[4 * i + 2]);
-                    w[4 * i + 3] = __float_as_uint(e.w * S[4 * i + 3]);
+                for (int q16 = 0; q16 < 4; ++q16) {
+                    // 16 keys at a time, scaled in place
+                    const int kb = k0 + 64 * (q16 >> 1) + 16 * (q16 & 1);
+                    uint32_t r[16];
+                    tmem_ld16_issue(tb + lane_base + TMH_S + kb, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float4 f = egp[kb / 4 + i];
+                        asm volatile("" : "+r"(r[4 * i]), "+r"(r[4 * i + 1]), "+r"(r[4 * i + 2]), "+r"(r[4 * i + 3]));
+                        r[4 * i] = __float_as_uint(f.x * __uint_as_float(r[4 * i]));
+                        r[4 * i + 1] = __float_as_uint(f.y * __uint_as_float(r[4 * i + 1]));
+                        r[4 * i + 2] = __float_as_uint(f.z * __uint_as_float(r[4 * i + 2]));
+                        r[4 * i + 3] = __float_as_uint(f.w * __uint_as_float(r[4 * i + 3]));
+                    }
+                    tmem_st16_issue(tmem_addr(tb, 32 * qd, TMH_S + kb), r);
                 }
-                tmem_st16_issue(tmem_addr(tb, 32 * qd, TMH_S + k0), w);
-                tmem_st16_issue(tmem_addr(tb, 32 * qd, TMH_S + k0 + 16), w + 16);
             }
             if (vwarp) {
                 // U^T row v, tokens tq .. tq + 31 (four 16-byte chunks), read while
@@ -371,7 +386,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
                     stall_point<kStall>(p.stall_seed, 2, c);
                     tmem_st16_issue(tmem_addr(tb, 32 * qd, TMH_AV + 16 * (cq & 1)), w);
                 }
-                tmem_wait_st();   // V_new and this thread's decayed state
+                tmem_wait_st();   // V_new
                 tc_fence_before();
                 named_bar_sync(kBarHVn, 512);  // V_new and every thread's decayed state are in TMEM
                 if (issuer2 && ok && !*abort) {
@@ -385,7 +400,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
                 }
                 __syncwarp();
             } else {
-                tmem_wait_st();   // this thread's decayed state
+                tmem_wait_st();   // the decayed state
                 tc_fence_before();
                 named_bar_arrive(kBarHVn, 512);
                 // the previous chunk's output, while P1 of this one runs
@@ -394,41 +409,43 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
             }
             ok = ok && warp_wait_h(&p2_done, c & 1, abort, p.wait_ns);
             tc_fence_after();
+            // (loader) stage st is free: P1 and P23 of chunk c are complete and every
+            // thread's reads of it came before the V_new barrier
+            if (loader && ok && issued < count) issue_load(issued++);
             if (ok) {
                 // the next entry state, and (output warps) this chunk's output rows
-                float d[kSlab];
-                tmem_ld32(tb + lane_base + TMH_S + k0, d);
-#pragma unroll
-                for (int j = 0; j < kSlab; ++j) S[j] = d[j];
                 if (!vwarp && !no_out) {
                     tmem_ld32(tb + lane_base + d1_col, x);
                     out_pending = true;
                 }
                 stall_point<kStall>(p.stall_seed, 4, c);
-                if (c + 1 < count) store_state_operand();
+                if (c + 1 < count) {
+                    float d[kSlab];
+                    tmem_ld32(tb + lane_base + TMH_S + k0, d);
+                    store_state_operand(d);
+                }
             } else {
                 fail();
             }
             tc_fence_before();
-            // (P1 thread) the next record has arrived before the barrier, so that
-            // every thread may read its stage after it
+            // (storer) the output image the next chunk writes has been read by its
+            // last tensor store; (P1 thread) the next record has arrived before the
+            // barrier, so that every thread may read its stage after it
+            if (storer) bulk_wait_read_but_last();
             if (issuer && c + 1 < count &&
                 !mbar_wait(&full[(c + 1) % kHStages], ((c + 1) / kHStages) & 1, abort, p.wait_ns))
                 fail();
             if (named_bar_or(kBarHChunk, 512, *abort != 0)) break;
             done = c + 1;
             if (issuer && c + 1 < count) issue_p1(c + 1);
-            // stage st is free: P1 and P23 of chunk c completed and every read of it is done
             stall_point<kStall>(p.stall_seed, 5, c);
-            if (storer && issued < count) issue_load(issued++);
         }
         // the last chunk's output
         if (!vwarp && out_pending && done == count && !*abort) output(count - 1, true);
-        if (storer) {
-            bulk_wait_all();  // the output tensor stores are complete
-            // Never leave with a copy in flight (bounded; normally complete).
+        if (storer) bulk_wait_all();  // the output tensor stores are complete
+        // Never leave with a copy in flight (bounded; normally complete).
+        if (loader)
             for (int c = done; c < issued; ++c) mbar_wait(&full[c % kHStages], (c / kHStages) & 1, nullptr);
-        }
         if (issuer && count > 0) {
             // every product issued has completed before TMEM is released
             umma_commit(&bar_fin);
@@ -445,8 +462,23 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
             fin = p.scan_ops + (((size_t)(2 * seg + which)) * p.N * p.H + chain) * kHeadDim * kHeadDim + blk_off;
         if (p.scan_mode == kScanOut && seg != p.scan_nseg - 1) fin = nullptr;
         if (!*abort && fin) {
+            // count == 0: the entry state was never stored to TMEM; it is the
+            // initial state (or zero / the identity) as read above
+            float d[kSlab];
+            if (count > 0) {
+                tc_fence_after();
+                tmem_ld32(tb + lane_base + TMH_S + k0, d);
+            } else {
+                const float* h0 = p.h0 ? p.h0 + st_off : nullptr;
+                if (p.scan_mode == kScanOps) h0 = nullptr;
+                if (p.scan_mode == kScanOut && seg > 0)
+                    h0 = p.scan_entry + ((size_t)seg * p.N * p.H + chain) * kHeadDim * kHeadDim + blk_off;
 #pragma unroll
-            for (int j = 0; j < kSlab; ++j) fin[(size_t)j * kHeadDim] = S[j];
+                for (int j = 0; j < kSlab; ++j)
+                    d[j] = zero_u ? ((k0 + j == v) ? 1.f : 0.f) : (h0 ? h0[(size_t)j * kHeadDim] : 0.f);
+            }
+#pragma unroll
+            for (int j = 0; j < kSlab; ++j) fin[(size_t)j * kHeadDim] = d[j];
         }
     }
     tc_fence_before();
