@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define KDA_ABI_VERSION 5
+#define KDA_ABI_VERSION 6
 
 /*
  * Test and measurement overrides of the library's own choices, passed per call
@@ -296,6 +296,9 @@ kda_status kda_prefill_state(const kda_prefill_args* args, void* stream);
  * A segmented kda_prefill (see there) keeps the records of each token segment
  * together: segment s's records follow those of segments 0..s-1, numbered
  * as above within the segment.
+ * prep_counters (padded calls): int32 [chunks per sequence + 1], one
+ * record counter per segment of a segmented call, from which the prep CTAs of
+ * that segment take their records (set to zero at the start of the call).
  * scan (padded calls with at most 64 chains and at least 128 chunks per
  * sequence): room for the segment-parallel scan with up to scan_max_segments
  * = min(32, chunks per sequence / 64) segments: the segments' transitions and
@@ -310,6 +313,7 @@ typedef struct kda_workspace_layout {
     size_t seq_order;           /* varlen calls: int32 [N], sequences longest first */
     size_t scan;                /* padded calls: segment-parallel scan buffers (see above) */
     int64_t scan_max_segments;  /* 0 when the layout has no scan room */
+    size_t prep_counters;       /* padded calls: int32 per segment (see above) */
 } kda_workspace_layout;
 kda_status kda_prefill_workspace_layout(const kda_prefill_args* args,
                                         kda_workspace_layout* layout);

@@ -58,6 +58,10 @@ bool layout_of(const kda_prefill_args* a, kda_workspace_layout* L) {
     L->chunk_offset = o; o = align_up(o + sizeof(int32_t) * (size_t)(a->num_seqs + 1));
     L->seq_order = o; o = align_up(o + (a->cu_seqlens ? sizeof(int32_t) * (size_t)a->num_seqs : 0));
     L->status = o; o = align_up(o + sizeof(int32_t));
+    // padded calls: one record counter per segment of the segmented schedule
+    const size_t counters =
+        a->cu_seqlens == nullptr ? sizeof(int32_t) * (size_t)((a->seqlen + kChunk - 1) / kChunk + 1) : 0;
+    L->prep_counters = o; o = align_up(o + counters);
     // padded calls: the state of every chain between two segments of the
     // segmented schedule (run_prefill)
     const size_t carry = a->cu_seqlens == nullptr
@@ -233,12 +237,11 @@ bool make_prep_maps(const kda_prefill_args* a, PrepMaps* m) {
 }
 
 // Which state kernel a sequential call runs: one CTA per chain (all 128 value
-// columns) when the 32-column slab CTAs would need more than two waves of SMs
-// (a whole-chain CTA takes about twice as long per chunk step, measured), so
-// below that the slab kernel is as fast or faster.  The two kernels compute the
-// same chunk step.  The overrides' state_kernel (tests, measurements) replaces
-// the choice; the fused output norm needs whole rows and always takes the
-// whole-chain kernel.
+// columns) when the 32-column slab CTAs would need more than two waves of SMs;
+// below that the slab kernel's shorter step (1.2 against 1.56 us, measured)
+// wins.  The two kernels compute the same chunk step.  The overrides'
+// state_kernel (tests, measurements) replaces the choice; the fused output norm
+// needs whole rows and always takes the whole-chain kernel.
 bool whole_chain_kernel(const PrefillParams& p, const kda_overrides& o, int num_sms) {
     if (p.gate) return true;
     if (o.state_kernel == 2) return true;
@@ -251,20 +254,22 @@ bool whole_chain_kernel(const PrefillParams& p, const kda_overrides& o, int num_
 // two kernels cannot share an SM (each needs most of its shared memory).  With
 // few chains the state pass leaves most SMs idle for its whole length, so the
 // tokens are cut into segments: prep of segment s+1 runs on the SMs the state
-// pass of segment s leaves free.  The choice simulates both streams from
-// per-unit costs measured on GB300 (SM clock 2070 MHz, long workload): one
-// (chunk, head) record takes a prep CTA 8.7 us on a full GPU and 8.25 us on the
-// SMs beside a state pass; a chunk step takes 1.05 us in the slab kernel (four
-// CTAs per chain) and 1.90 us in the whole-chain kernel, 12 % more beside prep;
+// pass of segment s leaves free, and once that state pass is done a second
+// prep grid on its SMs joins in (both take records from the segment's
+// counter).  The choice simulates both streams from per-unit costs measured on
+// GB300 (SM clock 2070 MHz, long workload): one (chunk, head) record takes a
+// prep CTA 8.3 us on a full GPU and 5 % less on the SMs beside a state pass; a
+// chunk step takes 1.2 us in the slab kernel (four CTAs per chain) and 1.56 us
+// in the whole-chain kernel, 12 % more beside prep;
 // every segment adds about 5 us to each stream (launch, start-up, the slowest
-// CTA's tail).  Fitted to a sweep of segment lengths 60..240 within 1 %.
+// CTA's tail).
 //
 // The segment-parallel scan (chosen when its estimate wins by 5 %): prep on
 // every SM, then the operator pass (2 (n - 1) whole-chain CTAs per chain), the
 // combine (one fp32 128 x 128 x 128 product per segment and chain, 6.6 us
 // each) and the output pass (n CTAs per chain), each launch adding
-// kSegmentUs.  A pass step takes the whole-chain step (1.90 us) unless the
-// resident CTAs' record reads (82.4 KB per step each; the transition and
+// kSegmentUs.  A pass step takes the whole-chain step (1.56 us) unless the
+// resident CTAs' record reads (74 KB per step each; the transition and
 // offset CTAs of a segment read the same records, so half as many distinct
 // ones) need longer at the 4.2 TB/s these reads reach.  Fitted to B 1,
 // T 131072, H 1..16 and T 32768, H 8 within 3 % (launch-list durations and
@@ -278,7 +283,7 @@ struct Segments {
     int scan_chunks = 0;     //        of this many chunks
 };
 
-constexpr double kRecUs = 8.7, kSlabStepUs = 1.05, kHeadStepUs = 1.90;
+constexpr double kRecUs = 8.3, kSlabStepUs = 1.2, kHeadStepUs = 1.56;
 constexpr double kPrepBeside = 0.95, kStateBeside = 1.12, kSegmentUs = 5.0;
 constexpr double kScanCombUs = 6.6, kScanRecordGBs = 4200.0;
 
@@ -305,17 +310,27 @@ void scan_shape(long long cps, long long nseg, int* out_nseg, int* out_chunks) {
     *out_nseg = (int)((cps + L - 1) / L);
 }
 
-// Estimated time of the segmented schedule: prep of segment i ends at P_i =
-// P_{i-1} + a_i; its state pass starts when both P_i and the previous state pass
-// are done.
-// The first segment's prep has every SM to itself.
+// Estimated time of the segmented schedule.  Prep of segment i (work W_i in
+// SM-microseconds) runs on `ctas` SMs from the end of segment i-1's prep,
+// P_{i-1}, and on the other num_sms - ctas SMs (the helper grid) from the end of
+// segment i-1's state pass, S_{i-1}; its records are shared out dynamically, so
+// it ends when the two have done W_i between them (plus half a record of tail).
+// The state pass of segment i starts when both P_i and S_{i-1} are reached.  The
+// first segment's prep has every SM to itself.
 double segmented_us(long long cps, long long chains, long long seg, long long ctas, double step,
                     int num_sms) {
     double P = 0.0, S = 0.0;
+    const double hs = (double)(num_sms - ctas);
     for (long long t0 = 0; t0 < cps; t0 += seg) {
         const long long c = cps - t0 < seg ? cps - t0 : seg;
-        const long long grid = t0 == 0 ? num_sms : ctas;
-        P += (double)((c * chains + grid - 1) / grid) * kRecUs * (t0 == 0 ? 1.0 : kPrepBeside) + kSegmentUs;
+        if (t0 == 0) {
+            P = (double)((c * chains + num_sms - 1) / num_sms) * kRecUs + kSegmentUs;
+        } else {
+            const double W = (double)(c * chains) * kRecUs * kPrepBeside;
+            const double alone = P + W / (double)ctas;
+            const double end = (hs <= 0.0 || S >= alone) ? alone : (W + (double)ctas * P + hs * S) / ((double)ctas + hs);
+            P = end + 0.5 * kRecUs + kSegmentUs;
+        }
         S = (P > S ? P : S) + (double)c * step * kStateBeside + kSegmentUs;
     }
     return S;
@@ -436,10 +451,17 @@ kda_status run_segments(const kda_prefill_args* a, const PrefillParams& p, const
     // the side stream starts after the work already queued on `s`
     bool ok = ck(cudaEventRecord(ev_prep, s)) && ck(cudaStreamWaitEvent(ss, ev_prep, 0));
     float* carry = reinterpret_cast<float*>(static_cast<uint8_t*>(a->workspace) + L.state_carry);
+    int32_t* counters = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(a->workspace) + L.prep_counters);
     const int64_t seg_tokens = (int64_t)sg.chunks * kChunk;
+    const int64_t nseg = (p.T + seg_tokens - 1) / seg_tokens;
+    ok = ok && ck(cudaMemsetAsync(counters, 0, sizeof(int32_t) * (size_t)nseg, s));
     const bool pdl = o.no_pdl == 0;
+    // SMs the state pass leaves idle once it is done: a second prep grid there
+    // takes records of the segment being prepared from the same counter
+    const int helper_ctas = num_sms - sg.prep_ctas;
     size_t rec_base = 0;
-    for (int64_t t0 = 0; ok && t0 < p.T; t0 += seg_tokens) {
+    int64_t si = 0;
+    for (int64_t t0 = 0; ok && t0 < p.T; t0 += seg_tokens, ++si) {
         const int ts = (int)(p.T - t0 < seg_tokens ? p.T - t0 : seg_tokens);
         const bool first = t0 == 0, last = t0 + ts >= p.T;
         PrefillParams q = p;
@@ -456,13 +478,17 @@ kda_status run_segments(const kda_prefill_args* a, const PrefillParams& p, const
         rec_base += (size_t)q.max_chunks * p.H;
         q.h0 = first ? p.h0 : carry;
         q.hT = last ? p.hT : carry;   // each chain's state is read before it is rewritten
+        q.rec_counter = counters + si;
         PrepMaps maps;
         kda_prefill_args sa = *a;
         sa.q = q.q; sa.k = q.k; sa.v = q.v; sa.g = q.g;
         sa.seqlen = ts;
         if (!make_prep_maps(&sa, &maps)) return KDA_ERR_UNSUPPORTED;
-        // no state pass runs yet while the first segment is prepared: every SM
+        // no state pass runs yet while the first segment is prepared: every SM;
+        // later segments: prep_ctas CTAs, joined by the helper grid after the
+        // previous segment's state pass (queued before it on the second stream)
         ok = launch_prep(q, maps, first ? num_sms : sg.prep_ctas, s, !first && pdl) == cudaSuccess &&
+             (first || helper_ctas < 1 || launch_prep(q, maps, helper_ctas, ss) == cudaSuccess) &&
              ck(cudaEventRecord(ev_prep, s)) && ck(cudaStreamWaitEvent(ss, ev_prep, 0)) &&
              launch_state_pass(a, q, sg.head, ss) == cudaSuccess;
     }

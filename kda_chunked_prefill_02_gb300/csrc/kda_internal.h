@@ -93,6 +93,8 @@ struct PrefillParams {
     int scan_nseg;               // segments per chain
     float* scan_ops;             // [(nseg - 1) * 2][B * H] fp32 128 x 128 blocks: M_s, C_s
     float* scan_entry;           // [nseg][B * H] fp32 128 x 128 blocks: E_s (s >= 1 used)
+    int32_t* rec_counter;        // prep: records are taken from this counter (starting at 0)
+                                 // by every grid given it; nullptr: CTA b takes b, b + grid, ...
 };
 
 // Modes of the whole-chain state kernel.
@@ -152,7 +154,8 @@ struct PrepMaps {
 cudaError_t launch_chunk_table(const PrefillParams& p, cudaStream_t s);
 // overlap_previous: launched programmatically after another prep grid in the
 // same stream (the two may overlap; they must touch disjoint records).
-cudaError_t launch_prep(const PrefillParams& p, const PrepMaps& maps, int num_sms, cudaStream_t s,
+// grid: CTAs (at most one per SM and per record).
+cudaError_t launch_prep(const PrefillParams& p, const PrepMaps& maps, int grid, cudaStream_t s,
                         bool overlap_previous = false);
 // out_map: tensor map of out, [channel 128, head, token, batch] with a box of
 // [32, 1, 64, 1] and the 64-byte swizzle (used when p.out_tma is set).

@@ -156,6 +156,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                                              ~uintptr_t(1023));
     __shared__ uint64_t bar_in, bar_mma[2], bar_fin, bar_never;
     __shared__ uint32_t tmem_base_sh;
+    __shared__ int s_rec[3];   // counter mode: first record, then the next record by parity
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nrec = p.max_chunks * p.H;
@@ -168,6 +169,12 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         fence_mbar_init();
         tma_prefetch_desc(&maps.q); tma_prefetch_desc(&maps.k);
         tma_prefetch_desc(&maps.v); tma_prefetch_desc(&maps.g);
+        if (p.rec_counter) {
+            // records are taken from the counter, the next one a record ahead so
+            // that its inputs can be requested early
+            s_rec[2] = atomicAdd(p.rec_counter, 1);
+            s_rec[0] = atomicAdd(p.rec_counter, 1);
+        }
     }
     if (warp == 0) {
         tmem_alloc(&tmem_base_sh, TM_COLS);
@@ -187,8 +194,9 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     const int qd = warp & 3, cq = warp >> 2;
     const float kPFloor = __expf(kGateFloor);
 
-    int rec = blockIdx.x;
-    ChunkInfo ci = chunk_info(p, rec / p.H);
+    const bool counted = p.rec_counter != nullptr;
+    int rec = counted ? s_rec[2] : (int)blockIdx.x;
+    ChunkInfo ci = rec < nrec ? chunk_info(p, rec / p.H) : ChunkInfo{0, 0, 0, 0, 0};
     if (tid == 0 && ci.len > 0) load_inputs(sm, maps, ci, rec % p.H, &bar_in);
     // beta of the current record, loaded one record ahead (raw value; the
     // sigmoid is applied when it is stored)
@@ -201,7 +209,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     int pend_parity = ci.len > 0 ? 0 : -1;  // parity of an input load still in flight
     for (uint32_t it = 0; ci.len > 0; ++it) {
         const int len = ci.len;
-        const int rec_next = rec + gridDim.x;
+        const int rec_next = counted ? s_rec[it & 1] : rec + (int)gridDim.x;
         const ChunkInfo cn = rec_next < nrec ? chunk_info(p, rec_next / p.H) : ChunkInfo{0, 0, 0, 0, 0};
         // This CTA's last record: a grid launched programmatically after this one
         // may start once every CTA has reached this point.
@@ -211,6 +219,9 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         ok = __syncthreads_and(tid == 0 ? mbar_wait(&bar_in, it & 1, nullptr, p.wait_ns) : true);
         if (!ok) break;
         pend_parity = -1;
+        // the record after the next (read two iterations on, past many barriers;
+        // the slot was last read at the top of the previous iteration)
+        if (counted && tid == 0 && rec_next < nrec) s_rec[(it + 1) & 1] = atomicAdd(p.rec_counter, 1);
         if (tid < 64) {
             float bval = bcur;
             if (tid < len && p.beta_is_logit) bval = 1.0f / (1.0f + __expf(-bval));
@@ -698,6 +709,7 @@ cudaError_t launch_chunk_table(const PrefillParams& p, cudaStream_t s) {
 
 cudaError_t launch_prep(const PrefillParams& p, const PrepMaps& maps, int num_sms, cudaStream_t s,
                         bool overlap_previous) {
+    if (num_sms < 1) return cudaSuccess;
     const long long recs = (long long)p.max_chunks * p.H;
     if (recs == 0) return cudaSuccess;
     // the instantiation with the stall hook runs only when a test asks for it

@@ -115,7 +115,8 @@ class WorkspaceLayout(ctypes.Structure):
                 ("chunk_offset", ctypes.c_size_t), ("status", ctypes.c_size_t),
                 ("total", ctypes.c_size_t), ("max_chunks", _i64),
                 ("state_carry", ctypes.c_size_t), ("seq_order", ctypes.c_size_t),
-                ("scan", ctypes.c_size_t), ("scan_max_segments", _i64)]
+                ("scan", ctypes.c_size_t), ("scan_max_segments", _i64),
+                ("prep_counters", ctypes.c_size_t)]
 
 
 class Schedule(ctypes.Structure):

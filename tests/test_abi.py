@@ -33,7 +33,7 @@ def test_exports_every_declared_symbol(K):
             "kda_status_string"} <= names
     for n in sorted(names):
         assert hasattr(lib, n), n
-    assert lib.kda_abi_version() == 5
+    assert lib.kda_abi_version() == 6
 
 
 def _args(K, **kw):
@@ -82,8 +82,10 @@ def test_workspace_plan(K):
     assert L.total == lib.kda_prefill_workspace_size(ctypes.byref(a))
     offs = [L.records, L.chunk_offset, L.status, L.state_carry]
     assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
-    # padded: one fp32 128 x 128 state per chain (batch 1 x 2 heads) carried between segments
+    # padded: one fp32 128 x 128 state per chain (batch 1 x 2 heads) carried between segments,
+    # after the per-segment record counters (one int32 per chunk of a sequence, + 1)
     assert L.total == L.state_carry + 2 * 128 * 128 * 4
+    assert L.status < L.prep_counters and L.prep_counters + 4 * 5 <= L.state_carry
     assert L.record_bytes == 74240 and L.chunk_offset >= L.records + 8 * L.record_bytes
     # varlen upper bound on chunks: floor(T / 64) + N
     a2 = _args(K, cu_seqlens=ctypes.c_void_p(1 << 12), num_seqs=3, seqlen=130)
@@ -169,9 +171,10 @@ def test_prefill_schedule(K, monkeypatch):
     monkeypatch.setenv("KDA_SEGMENT_CHUNKS", "3")
     monkeypatch.setenv("KDA_STATE_KERNEL", "slab")
     monkeypatch.setenv("KDA_STALL_INJECT", "7")
-    # 32 chains of 2048 chunks: whole-chain state CTAs on 32 SMs, prep on 120,
-    # 56-chunk segments
-    assert _sched(K, batch=1, num_seqs=1, seqlen=131072, num_heads=32) == (1, 1, 56, 120)
+    # 32 chains of 2048 chunks: whole-chain state CTAs on 32 SMs, prep on 120
+    # (joined by a second prep grid on the state SMs once each state pass ends)
+    s32 = _sched(K, batch=1, num_seqs=1, seqlen=131072, num_heads=32)
+    assert s32[:2] == (1, 1) and s32[3] == 120 and s32[2] % 8 == 0
     # 8 chains: the segment-parallel scan (test_scan_schedule_and_workspace);
     # with the scan ruled out, slab state CTAs (4 per chain) on 32 SMs beside
     # prep on 120
