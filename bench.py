@@ -165,6 +165,11 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+def num_sms_of(t):
+    import torch
+    return torch.cuda.get_device_properties(t.device).multi_processor_count
+
+
 def captured_traffic(kernel, token_heads):
     """DRAM bytes per launch of `kernel` from the committed ncu summary
     (profiles/<kernel>_kernel_traffic.txt), scaled to `token_heads`; None when
@@ -339,7 +344,9 @@ def run_ours(args, rank, ws, local):
     elif sched["segmented"]:
         chunks = -(-inp.lengths[0] // 64)            # padded: every sequence has T tokens
         nseg = -(-chunks // sched["segment_chunks"])
-        launches = 2 * nseg
+        # per segment prep and the state pass; from the second segment on, the
+        # second prep grid on the state SMs
+        launches = 2 * nseg + (nseg - 1 if sched["prep_ctas"] < num_sms_of(d.q) else 0)
         sched["segments"] = nseg
     else:
         launches = 2 + (1 if inp.cu_seqlens is not None else 0)
