@@ -210,10 +210,12 @@ size_t kda_prefill_workspace_size(const kda_prefill_args* args);
  *      CTA, with the output epilogue (rows stored by TMA tensor stores).
  * Padded calls with few, long chains are run in token segments: the state
  * pass of segment s (on a second stream, joined back into `stream` before
- * the call's work ends) overlaps the prep of segment s+1, the state of every
- * chain passing between segments in fp32 through the workspace's
- * state_carry region, so the results are those of one state pass over the
- * whole sequence.
+ * the call's work ends) overlaps the prep of segment s+1, which a second prep
+ * grid on that stream joins once the state pass ends (both take the
+ * segment's records from its counter in prep_counters); the state of every
+ * chain passes between segments in fp32 through the workspace's state_carry
+ * region, so the results are those of one state pass over the whole
+ * sequence.
  * Padded calls with very few chains may instead run the segment-parallel
  * inter-chunk scan (the seg / comb kernels of the cuDNN-frontend sm90 KDA
  * page, Conversation): each chain's chunks are cut into n segments; for every
