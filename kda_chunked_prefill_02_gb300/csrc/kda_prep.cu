@@ -261,7 +261,12 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         if (tid == 0) bulk_wait_read();  // the previous record's images have left the staging area
         __syncthreads();
 
-        // ---- E2: the MMA operands and the records that need no MMA.
+        // ---- E2: the MMA operands and the records that need no MMA.  R and Y (MMA
+        // A's operands) are written first; the Q e^Gam, [K e^Gam | V] and Kt
+        // images, which MMA A does not read, are kept in registers and written
+        // while MMA A runs (warp 0, whose lane 0 issues MMA A, writes its share
+        // before).
+        uint32_t qt_w[8], kv_w[8], v_w[8], kt_w0[4], kt_w1[4];
         {
             const float* tot = reinterpret_cast<const float*>(sm + O_TOT);
             float b0[4], b1[4];  // exact decay of each 16-token block
@@ -319,10 +324,10 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                     // R = [K ac ; Q ac]
                     st_u32(sm + O_R + bo + sw128_off(i, cc), pack_bf16x2(kk.x * ac0, kk.y * ac1));
                     st_u32(sm + O_R + bo + sw128_off(64 + i, cc), pack_bf16x2(qq.x * ac0, qq.y * ac1));
-                    // the record's Q e^Gam rows; [K e^Gam | V] (MN-major: token row i, channels contiguous)
-                    st_u32(sm + O_QT + blk * 8192u + sw128_off(i, cc), pack_bf16x2(qq.x * a0, qq.y * a1));
-                    st_u32(sm + O_KV + mn_sw128_off(i, c0, kKvSbo), pack_bf16x2(kk.x * a0, kk.y * a1));
-                    st_u32(sm + O_KV + mn_sw128_off(i, 128 + c0, kKvSbo), vw[l]);
+                    // the record's Q e^Gam rows and [K e^Gam | V], written later
+                    qt_w[l] = pack_bf16x2(qq.x * a0, qq.y * a1);
+                    kv_w[l] = pack_bf16x2(kk.x * a0, kk.y * a1);
+                    v_w[l] = vw[l];
                 }
             }
             stall_point<kStall>(p.stall_seed, 3, it);
@@ -363,12 +368,27 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                     z0 *= p0[l]; z1 *= p1[l];
                     zc0 *= fmaxf(p0[l], kPFloor); zc1 *= fmaxf(p1[l], kPFloor);
                 }
-                // Kt image rows c0, c0 + 1: tokens 8 h8 .. 8 h8 + 7 are 16-byte chunk h8
-                uint8_t* kt = sm + O_SKT;
-                *reinterpret_cast<uint4*>(kt + sw128_off(c0, 8 * h8)) = make_uint4(kh0[0], kh0[1], kh0[2], kh0[3]);
-                *reinterpret_cast<uint4*>(kt + sw128_off(c0 + 1, 8 * h8)) = make_uint4(kh1[0], kh1[1], kh1[2], kh1[3]);
+#pragma unroll
+                for (int x = 0; x < 4; ++x) { kt_w0[x] = kh0[x]; kt_w1[x] = kh1[x]; }
             }
         }
+        // The images MMA A does not read: Q e^Gam, [K e^Gam | V] (MN-major: token
+        // row i, channels contiguous) and the Kt rows c0, c0 + 1 (tokens 8 h8 ..
+        // 8 h8 + 7 are 16-byte chunk h8).
+        auto write_late_images = [&]() {
+            const int blk2 = c0 >> 6, cc2 = c0 & 63;
+#pragma unroll
+            for (int l = 0; l < 8; ++l) {
+                const int i = 8 * h8 + l;
+                st_u32(sm + O_QT + blk2 * 8192u + sw128_off(i, cc2), qt_w[l]);
+                st_u32(sm + O_KV + mn_sw128_off(i, c0, kKvSbo), kv_w[l]);
+                st_u32(sm + O_KV + mn_sw128_off(i, 128 + c0, kKvSbo), v_w[l]);
+            }
+            uint8_t* kt = sm + O_SKT;
+            *reinterpret_cast<uint4*>(kt + sw128_off(c0, 8 * h8)) = make_uint4(kt_w0[0], kt_w0[1], kt_w0[2], kt_w0[3]);
+            *reinterpret_cast<uint4*>(kt + sw128_off(c0 + 1, 8 * h8)) = make_uint4(kt_w1[0], kt_w1[1], kt_w1[2], kt_w1[3]);
+        };
+        if (warp == 0) write_late_images();
         stall_point<kStall>(p.stall_seed, 4, it);
         fence_proxy_async_smem();
         tc_fence_before();
@@ -379,6 +399,11 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             umma_tile(tb + TM_A, smem_u32(sm + O_R), 16384, smem_u32(sm + O_Y), kYBlock, 128,
                       idesc_bf16_f32(128, 160), false);
             umma_commit(&bar_mma[0]);
+        }
+        if (warp != 0) write_late_images();
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
             // The Kt, e^gam and Q e^Gam images leave by bulk copy.
             uint8_t* rp = p.ws_rec + (size_t)rec * kRecBytes;
             bulk_store(rp + kRecKt, sm + O_SKT, 16384);
