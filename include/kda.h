@@ -67,7 +67,8 @@ extern "C" {
  *   segment_chunks  -1: library's choice, 0: never segment, n > 0: segments of
  *                   n chunks (padded calls)
  *   prep_ctas       > 0: prep grid of a forced segmented call (0: choice)
- *   no_pdl          1: no programmatic launch between consecutive prep grids
+ *   no_pdl          1: no programmatic launch between consecutive prep grids,
+ *                   nor of the state pass after a one-pass call's prep
  *   stall_seed      != 0: the kernel instantiations with the stall hook, in
  *                   which a quarter of the warps at each injection site spin
  *                   for a pseudo-random 0..4095 cycles; every result must be

@@ -220,11 +220,12 @@ bool make_out_map(CUtensorMap* m, const kda_prefill_args* a, const void* base, i
 }
 
 // Launches the state pass of `p` with the chosen kernel.
-cudaError_t launch_state_pass(const kda_prefill_args* a, PrefillParams p, bool head, cudaStream_t s) {
+cudaError_t launch_state_pass(const kda_prefill_args* a, PrefillParams p, bool head, cudaStream_t s,
+                              bool after_prep = false) {
     CUtensorMap om;
     memset(&om, 0, sizeof(om));
     p.out_tma = make_out_map(&om, a, p.out, p.T) ? 1 : 0;
-    return head ? launch_state_head(p, om, s) : launch_state(p, om, s);
+    return head ? launch_state_head(p, om, s, after_prep) : launch_state(p, om, s, after_prep);
 }
 
 bool make_prep_maps(const kda_prefill_args* a, PrepMaps* m) {
@@ -559,7 +560,9 @@ kda_status run_prefill(const kda_prefill_args* a, void* stream, int stages) {
         if (launch_prep(p, pmaps, num_sms, s) != cudaSuccess) return KDA_ERR_CUDA;
     }
     if (state_pass) {
-        if (launch_state_pass(a, p, whole_chain_kernel(p, o, num_sms), s) != cudaSuccess) return KDA_ERR_CUDA;
+        // right after this call's prep: launched programmatically
+        if (launch_state_pass(a, p, whole_chain_kernel(p, o, num_sms), s, prep && o.no_pdl == 0) != cudaSuccess)
+            return KDA_ERR_CUDA;
     }
     return KDA_OK;
 }

@@ -159,8 +159,33 @@ cudaError_t launch_prep(const PrefillParams& p, const PrepMaps& maps, int grid, 
                         bool overlap_previous = false);
 // out_map: tensor map of out, [channel 128, head, token, batch] with a box of
 // [32, 1, 64, 1] and the 64-byte swizzle (used when p.out_tma is set).
-cudaError_t launch_state(const PrefillParams& p, const CUtensorMap& out_map, cudaStream_t s);
-cudaError_t launch_state_head(const PrefillParams& p, const CUtensorMap& out_map, cudaStream_t s);
+// after_prep: launched programmatically right after a prep grid in the same
+// stream (the state pass's set-up overlaps prep's tail; it waits for prep's
+// completion before it reads a record).
+cudaError_t launch_state(const PrefillParams& p, const CUtensorMap& out_map, cudaStream_t s,
+                         bool after_prep = false);
+cudaError_t launch_state_head(const PrefillParams& p, const CUtensorMap& out_map, cudaStream_t s,
+                              bool after_prep = false);
+// Launches `kern` with the programmatic-serialization attribute when `pdl`.
+template <typename... Args>
+cudaError_t launch_maybe_pdl(void (*kern)(Args...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             bool pdl, Args... args) {
+    if (!pdl) {
+        kern<<<grid, block, smem, s>>>(args...);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 // Entry states of the scan: E_{s+1} = M_s E_s + C_s (E_0 = p.h0 or zero) for
 // every chain, in fp32 with a fixed summation order.
 cudaError_t launch_scan_combine(const PrefillParams& p, cudaStream_t s);

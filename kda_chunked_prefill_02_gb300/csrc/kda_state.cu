@@ -123,6 +123,9 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // Launched programmatically after prep: prep's records are complete and
+    // visible from here on (a no-op otherwise).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint32_t tb = tmem_base_sh;
     volatile int* abort = &abort_flag;
     auto fail = [&]() {
@@ -381,15 +384,14 @@ __global__ void __launch_bounds__(kStateThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_state(const PrefillParams& p, const CUtensorMap& out_map, cudaStream_t s) {
+cudaError_t launch_state(const PrefillParams& p, const CUtensorMap& out_map, cudaStream_t s, bool after_prep) {
     if (p.N == 0 || p.H == 0) return cudaSuccess;
     static std::atomic<uint64_t> smem_set[2];
     auto kern = p.stall_seed ? state_kernel<true> : state_kernel<false>;
     cudaError_t e = set_smem_limit_once((const void*)kern, (int)kStateSmem, smem_set[p.stall_seed ? 1 : 0]);
     if (e != cudaSuccess) return e;
     dim3 grid(kHeadDim / kSlab, p.H, p.N);
-    kern<<<grid, kStateThreads, kStateSmem, s>>>(p, out_map);
-    return cudaGetLastError();
+    return launch_maybe_pdl(kern, grid, dim3(kStateThreads), kStateSmem, s, after_prep, p, out_map);
 }
 
 }  // namespace kda

@@ -169,6 +169,9 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // Launched programmatically after prep: prep's records are complete and
+    // visible from here on (a no-op otherwise).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint32_t tb = tmem_base_sh;
     volatile int* abort = &abort_flag;
     auto fail = [&]() {
@@ -488,7 +491,8 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_state_head(const PrefillParams& p, const CUtensorMap& out_map, cudaStream_t s) {
+cudaError_t launch_state_head(const PrefillParams& p, const CUtensorMap& out_map, cudaStream_t s,
+                              bool after_prep) {
     if (p.N == 0 || p.H == 0) return cudaSuccess;
     static std::atomic<uint64_t> smem_set[2];
     auto kern = p.stall_seed ? state_head_kernel<true> : state_head_kernel<false>;
@@ -497,8 +501,7 @@ cudaError_t launch_state_head(const PrefillParams& p, const CUtensorMap& out_map
     const int ys = p.scan_mode == kScanOps ? 2 * (p.scan_nseg - 1) : (p.scan_mode == kScanOut ? p.scan_nseg : 1);
     if (ys <= 0) return cudaSuccess;
     dim3 grid(p.H, p.N * ys);
-    kern<<<grid, kHeadThreads, kHeadSmem, s>>>(p, out_map);
-    return cudaGetLastError();
+    return launch_maybe_pdl(kern, grid, dim3(kHeadThreads), kHeadSmem, s, after_prep, p, out_map);
 }
 
 namespace {
