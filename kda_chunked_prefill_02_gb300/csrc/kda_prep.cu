@@ -31,8 +31,11 @@
 //
 // Organisation: a persistent CTA (16 warps) per SM loops over (chunk, head)
 // records.  The q, k, v and g tiles of a record arrive by TMA; the next
-// record's tiles are requested as soon as the current record's gate phase has
-// consumed its inputs, so the loads overlap the tensor-core and solve phases.
+// record's tiles are requested during the UT solve, so that they land during
+// the solve and MMA C.  The record's images leave by bulk copies issued by
+// warps that have nothing else to do at that point.  Copies in either
+// direction are kept away from the shared-memory-heavy phases (operand build,
+// epilogues), which they measurably slow down.
 #include <string.h>
 
 #include "kda_internal.h"
@@ -49,19 +52,21 @@ constexpr uint32_t O_IK = 16384;      // bf16 [64][128] k tile
 constexpr uint32_t O_IV = 32768;      // bf16 [64][128] v tile
 constexpr uint32_t O_IG = 49152;      // fp32 [64][128] g tile
 constexpr uint32_t kInBytes = 81920;
-// Once the gate phase has read the g tile, its space stages the record's Kt
-// image (16 KB fp16, same bytes as in the record) and e^gam (512 B).
-constexpr uint32_t O_SKT = O_IG;
-constexpr uint32_t O_SEG = O_IG + 16384;
 constexpr uint32_t O_R = 81920;       // A operand R = [K ac ; Q ac]: 2 x (128 rows x 128 B)
 constexpr uint32_t O_Y = 114688;      // B operand [Yoff (96 rows) ; Yd (64 rows)]: 2 x (160 x 128 B)
 constexpr uint32_t kYBlock = 160 * 128;
 constexpr uint32_t O_KV = 155648;     // B operand [K e^Gam | V], MN-major: 8 token groups x 4 KB
 constexpr uint32_t kKvSbo = 4096;     // byte distance between 8-token groups of the KV operand
 constexpr uint32_t O_QT = 188416;     // Q e^Gam image: 2 column blocks x 64 rows x 128 B (the record's rows 0-63)
-constexpr uint32_t O_TOT = 205824;    // fp32 [2][8][128] decay products (exact, floored) of 8-token groups
-constexpr uint32_t O_BETA = 214016;   // fp32 [64] beta
-constexpr uint32_t kPrepSmem = 214272 + 1024;
+// Staging of the record's Kt image (16 KB fp16, the record's bytes) and e^gam
+// (512 B), apart from the input tiles, so that the next record's tiles may be
+// requested while these images are still being copied out.
+constexpr uint32_t O_SKT = 204800;
+constexpr uint32_t O_TOT = 221184;    // fp32 [2][8][128] decay products (exact, floored) of 8-token groups
+constexpr uint32_t O_BETA = 229376;   // fp32 [64] beta
+constexpr uint32_t O_SEG = 229632;
+constexpr uint32_t kPrepSmem = 230144 + 1024;
+static_assert(kPrepSmem <= 232448, "prep shared memory above the per-block limit");
 // Scratch of the solve and MMA C, over R and Y once MMA A has completed.
 // The fp32 matrices hold tf32-rounded values (operands of the warp MMAs); the
 // row pitch 68 (4 mod 32) makes the MMA row-fragment loads and the epilogue's
@@ -258,7 +263,9 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             *reinterpret_cast<float2*>(tot + 1024 + h8 * 128 + c0) = make_float2(f0, f1);
         }
         stall_point<kStall>(p.stall_seed, 2, it);
-        if (tid == 0) bulk_wait_read();  // the previous record's images have left the staging area
+        // The previous record's images have left their staging areas (each bulk
+        // store is waited for by the lane that issued it).
+        if (lane == 0) bulk_wait_read();
         __syncthreads();
 
         // ---- E2: the MMA operands and the records that need no MMA.  R and Y (MMA
@@ -400,29 +407,15 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                       idesc_bf16_f32(128, 160), false);
             umma_commit(&bar_mma[0]);
         }
+        // (no CTA barrier here: nothing reads the late images before the barrier
+        // that ends epilogue A)
         if (warp != 0) write_late_images();
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (tid == 0) {
-            // The Kt, e^gam and Q e^Gam images leave by bulk copy.
-            uint8_t* rp = p.ws_rec + (size_t)rec * kRecBytes;
-            bulk_store(rp + kRecKt, sm + O_SKT, 16384);
-            bulk_store(rp + kRecEg, sm + O_SEG, 512);
-            bulk_store(rp + kRecA1, sm + O_QT, 8192);
-            bulk_store(rp + kRecA1 + 16384, sm + O_QT + 8192, 8192);
-            bulk_commit();
-        }
         if (cn.len > 0) bcur = load_beta(cn, rec_next % p.H);
         ok = __syncthreads_and(
             tid == 0 ? mbar_wait((p.timeout_probe && it == 0) ? &bar_never : &bar_mma[0], it & 1, nullptr, p.wait_ns)
                      : true);
         tc_fence_after();
         if (!ok) break;
-        // Once the Kt image has been read out of the consumed gate tile (this
-        // thread's bulk store), the input tiles are free: the next record's load
-        // is issued by an idle warp during the 16 -> 32 products and lands while
-        // this record goes through the solve and the other two products.
-        if (tid == 0 && cn.len > 0) bulk_wait_read();
 
         stall_point<kStall>(p.stall_seed, 5, it);
         float* sA = reinterpret_cast<float*>(sm + O_A);
@@ -476,10 +469,6 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
-        if (tid == 0) {
-            bulk_store(p.ws_rec + (size_t)rec * kRecBytes + kRecAqk, sm + O_AQK, 8192);
-            bulk_commit();
-        }
 
         // ---- UT transform: T = (I + A)^-1 for the unit lower-triangular 64 x 64
         // system, blocked: four 16 x 16 diagonal inverses by forward substitution,
@@ -543,10 +532,24 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             store_tile_tf32(sT + (pb + 16) * kPA + pb + c0, kPA, d, lane);
             store_tprime_pair(sm, pb + 16 + g4, pb + c0 + 2 * t4, d[0], d[1], sBeta);
             store_tprime_pair(sm, pb + 24 + g4, pb + c0 + 2 * t4, d[2], d[3], sBeta);
-        } else if (warp == 4 && lane == 0 && cn.len > 0) {
+        } else if (warp == 13 && lane == 0 && cn.len > 0) {
+            // The next record's tiles: E2 has read the current ones, and they land
+            // during the rest of the solve and MMA C rather than during the
+            // shared-memory-heavy epilogues.
             load_inputs(sm, maps, cn, rec_next % p.H, &bar_in);
+        } else if (lane == 0 && warp >= 8 && warp <= 12) {
+            // The Aqk, Kt, e^gam and Q e^Gam images leave by bulk copy, one per
+            // idle warp (these warps take no part in the 32 -> 64 products).
+            uint8_t* rp = p.ws_rec + (size_t)rec * kRecBytes;
+            if (warp == 8) bulk_store(rp + kRecAqk, sm + O_AQK, 8192);
+            else if (warp == 9) bulk_store(rp + kRecKt, sm + O_SKT, 16384);
+            else if (warp == 10) bulk_store(rp + kRecEg, sm + O_SEG, 512);
+            else if (warp == 11) bulk_store(rp + kRecA1, sm + O_QT, 8192);
+            else bulk_store(rp + kRecA1 + 16384, sm + O_QT + 8192, 8192);
+            bulk_commit();
         }
-        __syncthreads();
+        // The 32 -> 64 products (warps 0-7) read the 16 -> 32 results.
+        if (warp < 8) named_bar_sync(2, 256);
         if (cn.len > 0) pend_parity = (int)((it + 1) & 1);
         if (warp < 8) {
             // 32 -> 64, row tile rt (16 rows), columns c0..c0+7:
@@ -638,7 +641,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         umma_commit(&bar_fin);
         mbar_wait(&bar_fin, 0, nullptr);
     }
-    if (tid == 0) bulk_wait_all();  // no bulk store may outlive the CTA's shared memory
+    if (lane == 0) bulk_wait_all();  // no bulk store may outlive the CTA's shared memory
     // Never leave with a copy in flight (only possible after a failed wait).
     if (pend_parity >= 0 && tid == 0) mbar_wait(&bar_in, (uint32_t)pend_parity, nullptr);
     tc_fence_before();
