@@ -306,6 +306,12 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                     make_float2(b0[0] * b0[1] * b0[2] * b0[3], b1[0] * b1[1] * b1[2] * b1[3]);
             const float qscale = p.scale;
             const uint32_t bo = blk * 16384u, yb = blk * kYBlock;
+            // Byte offset of token row 8 h8 + l (channels cc, cc + 1) in a SW128
+            // K-major tile: the row's 16-byte chunk index is XORed with l.
+            const uint32_t trow0 = h8 * 1024u + (((uint32_t)cc >> 3) << 4 | ((uint32_t)cc & 7u) << 1);
+            auto trow = [&](int l) -> uint32_t { return trow0 ^ (uint32_t)(l * 144); };
+            uint8_t* const sR = sm + O_R + bo;
+            uint8_t* const sY = sm + O_Y + yb;
             // Forward over the group: the running products a (exact gates, from the
             // chunk start) and ac (floored gates, from the block start).  The second
             // half of a block starts from the first half's product.
@@ -329,8 +335,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                     float2 qq = bf16x2_to_float2(qw[l]);
                     qq.x *= qscale; qq.y *= qscale;
                     // R = [K ac ; Q ac]
-                    st_u32(sm + O_R + bo + sw128_off(i, cc), pack_bf16x2(kk.x * ac0, kk.y * ac1));
-                    st_u32(sm + O_R + bo + sw128_off(64 + i, cc), pack_bf16x2(qq.x * ac0, qq.y * ac1));
+                    st_u32(sR + trow(l), pack_bf16x2(kk.x * ac0, kk.y * ac1));
+                    st_u32(sR + 8192 + trow(l), pack_bf16x2(qq.x * ac0, qq.y * ac1));
                     // the record's Q e^Gam rows and [K e^Gam | V], written later
                     qt_w[l] = pack_bf16x2(qq.x * a0, qq.y * a1);
                     kv_w[l] = pack_bf16x2(kk.x * a0, kk.y * a1);
@@ -356,14 +362,14 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                     const int i = 8 * h8 + l;
                     const float2 kk = bf16x2_to_float2(kw[l]);
                     // Yd (diagonal blocks): K / ac
-                    st_u32(sm + O_Y + yb + sw128_off(96 + i, cc), pack_bf16x2(kk.x * zc0, kk.y * zc1));
-                    // Yoff: column block G seen from each later row block I
+                    st_u32(sY + 96 * 128 + trow(l), pack_bf16x2(kk.x * zc0, kk.y * zc1));
+                    // Yoff: column block G seen from each later row block I (Y row
+                    // yoff_row(I, G, 8 hf + l) = 8 I (I - 1) + 8 h8 + l)
                     const float kz0 = kk.x * z0, kz1 = kk.y * z1;
 #pragma unroll
                     for (int I = 1; I < 4; ++I)
                         if (I > G)
-                            st_u32(sm + O_Y + yb + sw128_off(yoff_row(I, G, 8 * hf + l), cc),
-                                   pack_bf16x2(kz0 * Dm0[I], kz1 * Dm1[I]));
+                            st_u32(sY + 8 * I * (I - 1) * 128 + trow(l), pack_bf16x2(kz0 * Dm0[I], kz1 * Dm1[I]));
                     // Kt = (K e^{gam - Gam})^T in fp16, packed by token pairs
                     const float hh0 = kz0 * E0, hh1 = kz1 * E1;
                     if (l & 1) {
@@ -383,13 +389,17 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         // row i, channels contiguous) and the Kt rows c0, c0 + 1 (tokens 8 h8 ..
         // 8 h8 + 7 are 16-byte chunk h8).
         auto write_late_images = [&]() {
-            const int blk2 = c0 >> 6, cc2 = c0 & 63;
+            // token row 8 h8 + l as in E2; the [K e^Gam | V] operand's 8-token
+            // groups are kKvSbo apart and its 64-channel atoms 1 KB apart
+            const uint32_t t0 = h8 * 1024u + (((uint32_t)cc >> 3) << 4 | ((uint32_t)cc & 7u) << 1);
+            uint8_t* const qtb = sm + O_QT + blk * 8192u;
+            uint8_t* const kvb = sm + O_KV + h8 * (kKvSbo - 1024u) + blk * 1024u;
 #pragma unroll
             for (int l = 0; l < 8; ++l) {
-                const int i = 8 * h8 + l;
-                st_u32(sm + O_QT + blk2 * 8192u + sw128_off(i, cc2), qt_w[l]);
-                st_u32(sm + O_KV + mn_sw128_off(i, c0, kKvSbo), kv_w[l]);
-                st_u32(sm + O_KV + mn_sw128_off(i, 128 + c0, kKvSbo), v_w[l]);
+                const uint32_t o = t0 ^ (uint32_t)(l * 144);
+                st_u32(qtb + o, qt_w[l]);
+                st_u32(kvb + o, kv_w[l]);
+                st_u32(kvb + 2048 + o, v_w[l]);
             }
             uint8_t* kt = sm + O_SKT;
             *reinterpret_cast<uint4*>(kt + sw128_off(c0, 8 * h8)) = make_uint4(kt_w0[0], kt_w0[1], kt_w0[2], kt_w0[3]);
