@@ -109,11 +109,7 @@ __device__ __forceinline__ uint32_t yoff_row(int I, int J, int l) {
 
 // Warp-level m16n8k8 tf32 MMA with fp32 accumulation (used for the small block
 // products of the UT solve; fragment layouts of the PTX m16n8k8 tf32 shape).
-__device__ __forceinline__ float tf32_round(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return __uint_as_float(r);
-}
+__device__ __forceinline__ float tf32_round(float x) { return to_tf32(x); }
 // d (16 x 8 tile) = P (16 x 8*ke, row pitch pp) * Q (8*ke x 8, row pitch pq) over
 // the k-steps kb .. ke-1 (8 each), fp32 matrices of tf32-rounded values in shared
 // memory.  Thread (g = lane/4, t = lane%4) gets d0 (g, 2t), d1 (g, 2t+1),
@@ -220,10 +216,11 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         // may start once every CTA has reached this point.
         if (rec_next >= nrec) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         stall_point<kStall>(p.stall_seed, 1, it);
-        // One thread waits on each mbarrier; the others wait at the CTA barrier.
-        ok = __syncthreads_and(tid == 0 ? mbar_wait(&bar_in, it & 1, nullptr, p.wait_ns) : true);
-        if (!ok) break;
-        pend_parity = -1;
+        // Every thread waits on the input mbarrier itself (no CTA barrier here);
+        // a wait that ran out is acted on, by all threads alike, at the CTA
+        // barrier that ends the gate phase.
+        ok = mbar_wait(&bar_in, it & 1, nullptr, p.wait_ns);
+        if (ok) pend_parity = -1;
         // the record after the next (read two iterations on, past many barriers;
         // the slot was last read at the top of the previous iteration)
         if (counted && tid == 0 && rec_next < nrec) s_rec[(it + 1) & 1] = atomicAdd(p.rec_counter, 1);
@@ -266,7 +263,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         // The previous record's images have left their staging areas (each bulk
         // store is waited for by the lane that issued it).
         if (lane == 0) bulk_wait_read();
-        __syncthreads();
+        ok = __syncthreads_and(ok);
+        if (!ok) break;
 
         // ---- E2: the MMA operands and the records that need no MMA.  R and Y (MMA
         // A's operands) are written first; the Q e^Gam, [K e^Gam | V] and Kt
@@ -328,7 +326,6 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                 }
 #pragma unroll
                 for (int l = 0; l < 8; ++l) {
-                    const int i = 8 * h8 + l;
                     a0 *= p0[l]; a1 *= p1[l];
                     ac0 *= fmaxf(p0[l], kPFloor); ac1 *= fmaxf(p1[l], kPFloor);
                     const float2 kk = bf16x2_to_float2(kw[l]);
@@ -359,7 +356,6 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                     kw[l] = *reinterpret_cast<const uint32_t*>(sm + O_IK + (8 * h8 + l) * 256 + c0 * 2);
 #pragma unroll
                 for (int l = 7; l >= 0; --l) {
-                    const int i = 8 * h8 + l;
                     const float2 kk = bf16x2_to_float2(kw[l]);
                     // Yd (diagonal blocks): K / ac
                     st_u32(sY + 96 * 128 + trow(l), pack_bf16x2(kk.x * zc0, kk.y * zc1));

@@ -398,11 +398,13 @@ __host__ __device__ __forceinline__ uint32_t f32_mnmajor_off(uint32_t r, uint32_
            (r & 3u) * 4u;
 }
 
-// fp32 -> tf32 with round-to-nearest (ties away from zero), as an fp32 pattern.
+// fp32 -> tf32 with round-to-nearest (ties away from zero), as an fp32 pattern
+// (finite inputs): half a unit of the 13 dropped mantissa bits is added to the
+// magnitude, a carry moving into the exponent, and the bits are dropped.  Two
+// integer operations, where the conversion instruction measured far slower in
+// the epilogues that round whole tiles.
 __device__ __forceinline__ float to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return __uint_as_float(r);
+    return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u);
 }
 
 // D[tmem] (+)= A * B^T, issued by a single thread.  A is M x 16 (K-major),
