@@ -259,7 +259,11 @@ bool whole_chain_kernel(const PrefillParams& p, const kda_overrides& o, int num_
 // prep grid on its SMs joins in (both take records from the segment's
 // counter).  The choice simulates both streams from per-unit costs measured on
 // GB300 (SM clock 2070 MHz, long workload): one (chunk, head) record takes a
-// prep CTA 8.3 us on a full GPU and 5 % less on the SMs beside a state pass; a
+// prep CTA 8.3 us on a full GPU and 5 % less on the SMs beside a state pass (a
+// fitted value: the prep kernel now measures 7.1 us a record alone, but with
+// 7.1 the model picks shorter segments that measure 0.6-1 % slower on the
+// long workload and its 16384-token cut, so the constant also carries the
+// state pass's slowdown beside the faster prep, which the model leaves out); a
 // chunk step takes 1.2 us in the slab kernel (four CTAs per chain) and 1.56 us
 // in the whole-chain kernel, 12 % more beside prep;
 // every segment adds about 5 us to each stream (launch, start-up, the slowest
