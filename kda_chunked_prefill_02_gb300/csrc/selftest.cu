@@ -434,6 +434,19 @@ __global__ void __launch_bounds__(128)
     if (warp == 0) tmem_dealloc(tb, 512);
 }
 
+// to_tf32 (integer round to nearest, ties away from zero) beside the
+// conversion instruction, element by element, as bit patterns.
+__global__ void tf32_round_selftest_kernel(const float* __restrict__ x, uint32_t* __restrict__ fast,
+                                           uint32_t* __restrict__ ref, int n) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const float v = x[i];
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
+    fast[i] = __float_as_uint(to_tf32(v));
+    ref[i] = r;
+}
+
 }  // namespace
 
 extern "C" int kda_selftest_umma_tf32(const float* A, const float* B, float* D, int N, int K, int a_mn,
@@ -509,6 +522,13 @@ extern "C" int kda_selftest_umma(const void* A, const void* B, float* D, int N, 
         return 3;
     umma_selftest_kernel<<<1, 128, smem, (cudaStream_t)stream>>>(
         (const __nv_bfloat16*)A, (const __nv_bfloat16*)B, D, N, use_tma, ma, mb, status);
+    return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
+
+extern "C" int kda_selftest_tf32_round(const float* x, uint32_t* fast, uint32_t* ref, int n,
+                                       void* stream) {
+    if (n < 1) return 1;
+    tf32_round_selftest_kernel<<<(n + 255) / 256, 256, 0, (cudaStream_t)stream>>>(x, fast, ref, n);
     return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 

@@ -166,6 +166,36 @@ def test_mma_rate_probe_runs(selftest):
         assert 0 < issue <= total
 
 
+def test_tf32_rounding_matches_the_conversion_instruction(selftest):
+    """to_tf32 (two integer operations: add half a unit of the 13 dropped
+    mantissa bits, then drop them) equals cvt.rna.tf32.f32 bit for bit on
+    finite values: random values over the whole exponent range, exact ties of
+    both signs, ties that carry into the exponent, subnormals and zeros."""
+    f = selftest.kda_selftest_tf32_round
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int, ctypes.c_void_p]
+    gen = torch.Generator().manual_seed(11)
+    bits = torch.randint(0, 2 ** 31, (1 << 20,), generator=gen, dtype=torch.int64)
+    bits = bits | (torch.randint(0, 2, bits.shape, generator=gen) << 31)
+    bits = bits[((bits >> 23) & 0xFF) != 0xFF]                      # finite only
+    mant = torch.randint(0, 1 << 10, (4096,), generator=gen, dtype=torch.int64)
+    expo = torch.randint(1, 254, (4096,), generator=gen, dtype=torch.int64)
+    ties = (expo << 23) | (mant << 13) | 0x1000                    # exactly half way
+    carry = (expo << 23) | (0x3FF << 13) | torch.randint(0x1000, 0x2000, (4096,), generator=gen)
+    special = torch.tensor([0, 1, 0x1000, 0x1FFF, 0x7FFFFF, 0x800000, 0x7F7FEFFF], dtype=torch.int64)
+    extra = torch.cat([ties, carry, special])
+    bits = torch.cat([bits, extra, extra | (1 << 31)])
+    # the 32-bit patterns as int32 (two's complement), viewed as fp32
+    x = (((bits & 0xFFFFFFFF) + (1 << 31)) % (1 << 32) - (1 << 31)).to(torch.int32).view(torch.float32).cuda()
+    n = x.numel()
+    fast = torch.empty(n, dtype=torch.int32, device="cuda")
+    ref = torch.empty(n, dtype=torch.int32, device="cuda")
+    assert f(x.data_ptr(), fast.data_ptr(), ref.data_ptr(), n, torch.cuda.current_stream().cuda_stream) == 0
+    torch.cuda.synchronize()
+    bad = (fast != ref).nonzero().flatten()
+    assert bad.numel() == 0, (x[bad[:8]].tolist(), fast[bad[:8]].tolist(), ref[bad[:8]].tolist())
+
+
 def _tf32(x):
     """fp32 -> the tf32 value the tensor core uses (the low 13 mantissa bits
     dropped)."""
