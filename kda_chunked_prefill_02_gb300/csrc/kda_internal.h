@@ -19,6 +19,21 @@ int prefill_check_args(const kda_prefill_args* a);
 // Raises a kernel's dynamic shared-memory limit once per device (the attribute
 // stays set for the device's context), so that launches after the first skip
 // the driver call.  `done` holds one bit per device.
+// The device's SM count, read once per device (0 if it cannot be read).
+inline int device_sm_count() {
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+    if (dev < 64) {
+        const int c = cached[dev].load(std::memory_order_acquire);
+        if (c > 0) return c;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev < 64) cached[dev].store(n, std::memory_order_release);
+    return n;
+}
+
 inline cudaError_t set_smem_limit_once(const void* kern, int bytes, std::atomic<uint64_t>& done) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -95,6 +110,8 @@ struct PrefillParams {
     float* scan_entry;           // [nseg][B * H] fp32 128 x 128 blocks: E_s (s >= 1 used)
     int32_t* rec_counter;        // prep: records are taken from this counter (starting at 0)
                                  // by every grid given it; nullptr: CTA b takes b, b + grid, ...
+    int rec_prefetch;            // whole-chain state kernel: chunks between a record's L2
+                                 // prefetch and its bulk copy (0: none); set by its launcher
 };
 
 // Modes of the whole-chain state kernel.

@@ -53,7 +53,13 @@ constexpr uint32_t SH_EG = kRecEg;     // e^gam [128] fp32
 constexpr uint32_t kHStageTx = kRecBytes;  // the whole record, one bulk copy
 constexpr uint32_t kHStage = 74752;     // kRecBytes rounded up to 1 KB (swizzle atoms)
 constexpr int kHStages = 2;
-constexpr int kHPrefetchAhead = 4;
+// L2 prefetch of a chain's later records, when the launch's CTAs fit on the GPU
+// at once (few chains: the prefetched lines are read before anything evicts
+// them); with more CTAs than SMs the prefetches of the resident CTAs evicted
+// one another's records before use and cost DRAM traffic (varlen workload,
+// 256 chains: 1.056 ms per call without them, 1.096 ms at 4 chunks ahead;
+// long workload, 32 chains: 3.973 ms at 2 chunks ahead, 3.991 without).
+constexpr int kHPrefetchAhead = 2;
 constexpr uint32_t OH_OUT = kHStages * kHStage;   // output rows: 2 images of 4 slabs [64 tokens x 32 values] bf16
 constexpr uint32_t kHeadSmem = OH_OUT + 2 * 4 * kSlabImg + 1024;
 // TMEM columns (lane = value column v).
@@ -233,7 +239,8 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
             const int st = c % kHStages;
             mbar_arrive_expect_tx(&full[st], kHStageTx);
             bulk_load(sm + st * kHStage, rec_ptr(c), kRecBytes, &full[st]);
-            if (c + kHPrefetchAhead < count) bulk_prefetch_l2(rec_ptr(c + kHPrefetchAhead), kRecBytes);
+            if (p.rec_prefetch > 0 && c + p.rec_prefetch < count)
+                bulk_prefetch_l2(rec_ptr(c + p.rec_prefetch), kRecBytes);
         };
         // P1 of chunk c: D1^T = S^T [Q e^Gam ; W]^T (B: 128 token rows, K-major in
         // two 64-key column blocks; A: S^T from TMEM, 8 columns per 16 keys).
@@ -501,7 +508,11 @@ cudaError_t launch_state_head(const PrefillParams& p, const CUtensorMap& out_map
     const int ys = p.scan_mode == kScanOps ? 2 * (p.scan_nseg - 1) : (p.scan_mode == kScanOut ? p.scan_nseg : 1);
     if (ys <= 0) return cudaSuccess;
     dim3 grid(p.H, p.N * ys);
-    return launch_maybe_pdl(kern, grid, dim3(kHeadThreads), kHeadSmem, s, after_prep, p, out_map);
+    PrefillParams q = p;
+    const long long ctas = (long long)p.H * p.N * ys;
+    const int sms = device_sm_count();
+    q.rec_prefetch = (sms > 0 && ctas <= sms) ? kHPrefetchAhead : 0;
+    return launch_maybe_pdl(kern, grid, dim3(kHeadThreads), kHeadSmem, s, after_prep, q, out_map);
 }
 
 namespace {
