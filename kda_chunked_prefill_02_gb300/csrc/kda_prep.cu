@@ -67,6 +67,14 @@ constexpr uint32_t O_BETA = 229376;   // fp32 [64] beta
 constexpr uint32_t O_SEG = 229632;
 constexpr uint32_t kPrepSmem = 230144 + 1024;
 static_assert(kPrepSmem <= 232448, "prep shared memory above the per-block limit");
+// The regions live at the same time do not overlap: the input tiles, the MMA A
+// operands, the [K e^Gam | V] operand, the Q e^Gam and Kt images, the decay
+// products, beta and e^gam.
+static_assert(O_IG + 32768 == kInBytes && kInBytes <= O_R, "input tiles");
+static_assert(O_R + 2 * 16384 <= O_Y && O_Y + 2 * kYBlock <= O_KV, "MMA A operands");
+static_assert(O_KV + 8 * kKvSbo <= O_QT && O_QT + 2 * 8192 <= O_SKT, "KV operand and Q e^Gam image");
+static_assert(O_SKT + 16384 <= O_TOT && O_TOT + 2 * 8 * 128 * 4 <= O_BETA, "Kt image and decay products");
+static_assert(O_BETA + 64 * 4 <= O_SEG && O_SEG + 128 * 4 + 1024 <= kPrepSmem, "beta and e^gam");
 // Scratch of the solve and MMA C, over R and Y once MMA A has completed.
 // The fp32 matrices hold tf32-rounded values (operands of the warp MMAs); the
 // row pitch 68 (4 mod 32) makes the MMA row-fragment loads and the epilogue's
@@ -82,6 +90,11 @@ constexpr uint32_t O_TT = 131072;     // A operand [T' ; T']: 128 rows x 128 B
 // scratch, which MMA C no longer needs).
 constexpr uint32_t O_SW = 81920;      // W image: 2 column blocks x 64 rows x 128 B (the record's rows 64-127)
 constexpr uint32_t O_SU = 98304;      // U^T image: 128 value rows x 128 B (64 tokens), 16 KB
+// The solve's scratch and the last epilogue's staging stay inside R and Y.
+static_assert(O_A + 64 * kPA * 4 <= O_T && O_T + 64 * kPA * 4 <= O_X && O_X + 32 * kPX * 4 <= O_AQK,
+              "solve scratch");
+static_assert(O_AQK + 8192 <= O_TT && O_TT + 16384 <= O_KV, "Aqk image and T' operand");
+static_assert(O_SU + 16384 <= O_AQK, "W / U^T staging");
 
 // TMEM columns.
 constexpr uint32_t TM_A = 0, TM_DIAG = 96, TM_C = 0, TM_COLS = 256;
